@@ -1,0 +1,168 @@
+"""fp64 CPU attention oracle -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline /
+reference arm may import this package.  The product library never does, and
+this package imports nothing from it: the two share no code.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, one materialised
+probability row per query); this module compiles it with gcc and marshals
+numpy arrays through ctypes.  Every function here follows the definition
+written at the top of ``attn_oracle.c``, which cites the pages it restates:
+
+* ferrotensor_backend engine/attention.rs -- AttentionOptions (causal offset,
+  window predicate), AttentionDims (head_dim, GQA divisibility, 1/sqrt(hd)).
+* brotensor ops/flash_attention.h -- key mask (> 0.5 keeps a key), softcap
+  position, GQA head map, decode row positions, overwrite semantics.
+* vision_rs flash_attn2.rs -- forward with saved log-sum-exp, dQ and dK/dV.
+* forge attention.metal -- unfused forward with materialised P, D = dO.O,
+  softcap derivative, GQA group sums in dK/dV.
+
+Pins: every function here is checked against closed forms, invariants, an
+independent torch fp64 route and finite differences in
+``tests/test_oracle_pins.py``.  One reading is a choice among conflicting
+pages rather than a fixed fact: the non-causal sliding window (ferrotensor's
+``|p - j| < window``); its implementation is pinned to that formula, the choice
+of formula is recorded as a reading.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into a shared library (gcc, OpenMP). Returns its path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c99", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        dp = ctypes.POINTER(ctypes.c_double)
+        common = [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                       ctypes.c_longlong, dp, ctypes.c_longlong]
+        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp] + common
+        lib.oracle_attn_fwd.restype = ctypes.c_int
+        lib.oracle_attn_probs.argtypes = [dp, dp, dp, dp, ctypes.c_int, ctypes.c_int] + common
+        lib.oracle_attn_probs.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = [dp] * 7 + common
+        lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _shapes(q, k, H, Hkv):
+    if q.ndim != 3 or k.ndim != 3:
+        raise ValueError("q must be [B,Tq,H*hd] and k/v [B,Tk,Hkv*hd]")
+    B, Tq, qc = q.shape
+    _, Tk, kc = k.shape
+    if qc % H or kc % Hkv or qc // H != kc // Hkv:
+        raise ValueError("inconsistent head sizes")
+    return B, Tq, Tk, qc // H
+
+
+def _mask(key_mask, B, Tk):
+    """Returns (array or None, batch stride). A 1-D mask is shared by every batch."""
+    if key_mask is None:
+        return None, 0
+    m = _f64(key_mask)
+    if m.ndim == 1:
+        if m.shape[0] != Tk:
+            raise ValueError("key mask must have Tk entries")
+        return m, 0
+    if m.shape != (B, Tk):
+        raise ValueError("key mask must be [Tk] or [B,Tk]")
+    return m, Tk
+
+
+def _common(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, m, ms):
+    return [B, Tq, Tk, H, Hkv, hd, float(scale), int(bool(causal)), int(window), float(softcap),
+            int(q_offset), _ptr(m), int(ms)]
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on."""
+    return int(_load().oracle_num_threads())
+
+
+def fwd(q, k, v, *, H, Hkv, scale, causal=False, window=0, softcap=0.0, q_offset=0,
+        key_mask=None):
+    """O [B,Tq,H*hd] and LSE [B,H,Tq] of the plain definition (fp64)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Tq, Tk, hd = _shapes(q, k, H, Hkv)
+    m, ms = _mask(key_mask, B, Tk)
+    o = np.zeros((B, Tq, H * hd), np.float64)
+    lse = np.zeros((B, H, Tq), np.float64)
+    rc = _load().oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                 *_common(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap,
+                                          q_offset, m, ms))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd rejected its arguments")
+    return o, lse
+
+
+def probs(q, k, v, b, h, *, H, Hkv, scale, causal=False, window=0, softcap=0.0, q_offset=0,
+          key_mask=None):
+    """The materialised probability matrix P [Tq,Tk] of batch b, head h."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Tq, Tk, hd = _shapes(q, k, H, Hkv)
+    m, ms = _mask(key_mask, B, Tk)
+    P = np.zeros((Tq, Tk), np.float64)
+    rc = _load().oracle_attn_probs(_ptr(q), _ptr(k), _ptr(v), _ptr(P), int(b), int(h),
+                                   *_common(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap,
+                                            q_offset, m, ms))
+    if rc != 0:
+        raise ValueError("oracle_attn_probs rejected its arguments")
+    return P
+
+
+def bwd(q, k, v, do, *, H, Hkv, scale, causal=False, window=0, softcap=0.0, q_offset=0,
+        key_mask=None):
+    """dQ, dK, dV of the plain definition, with P rebuilt from the inputs."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Tq, Tk, hd = _shapes(q, k, H, Hkv)
+    if do.shape != q.shape:
+        raise ValueError("dO must have q's shape")
+    m, ms = _mask(key_mask, B, Tk)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    rc = _load().oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                                 *_common(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap,
+                                          q_offset, m, ms))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return dq, dk, dv
