@@ -1,0 +1,244 @@
+"""GB300 fused attention: a thin ctypes binding over libattn_gb300.so.
+
+The functions here only marshal arguments: they check tensor shapes, let
+PyTorch allocate outputs and scratch, and call the C ABI of include/attn.h
+with raw device pointers and the current CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback, and a missing or unloadable library raises.
+
+    o, lse = attn_fwd(q, k, v, H=32, Hkv=8, causal=True)
+    dq, dk, dv = attn_bwd(q, k, v, o, do, lse, H=32, Hkv=8, causal=True)
+    o, lse = attn_decode(q, k_cache, v_cache, H=32, Hkv=8, causal=True, q_offset=Tk - Lq)
+
+Layouts: q/o/do/dq [B, Tq, H*hd]; k/v/dk/dv [B, Tk, Hkv*hd]; lse [B, H, Tq] fp32;
+key_mask fp32 [Tk] (shared) or [B, Tk].
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_bwd_workspace_size", "attn_decode_workspace_size",
+           "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_launch_count", "AttnError", "lib",
+           "library_path"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+_DT = {"float32": 0, "float16": 1, "bfloat16": 2}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, _status_string(status), status))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libattn_gb300.so")
+
+
+def lib():
+    """The loaded C library (built in-tree on first use if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import build as _build
+
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
+        tail = [i, i, i, i, i, i, f, i, i, f, i, vp, ll, vp]
+        L.attn_fwd.argtypes = [i, vp, vp, vp, vp, vp] + tail
+        L.attn_fwd.restype = i
+        L.attn_bwd_workspace_size.argtypes = [i, i, i]
+        L.attn_bwd_workspace_size.restype = sz
+        L.attn_bwd.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz] + tail
+        L.attn_bwd.restype = i
+        L.attn_bwd_phases.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz] + tail + [i]
+        L.attn_bwd_phases.restype = i
+        L.attn_launch_count.argtypes = []
+        L.attn_launch_count.restype = ctypes.c_ulonglong
+        L.attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.attn_decode_workspace_size.restype = sz
+        L.attn_decode.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + tail
+        L.attn_decode.restype = i
+        L.attn_status_string.argtypes = [i]
+        L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+        L.attn_get_device_status.restype = i
+        L.attn_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
+        L.attn_selftest_bounded_wait.restype = i
+        L.attn_kernel_family.argtypes = [i, i]
+        L.attn_kernel_family.restype = i
+        L.attn_abi_version.argtypes = []
+        L.attn_abi_version.restype = i
+        _lib = L
+        return L
+
+
+def _status_string(st: int) -> str:
+    try:
+        return lib().attn_status_string(int(st)).decode()
+    except Exception:  # the library itself failed to load
+        return "status %d" % st
+
+
+def _check(st: int, what: str):
+    if st != OK:
+        raise AttnError(st, what)
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dt(t) -> int:
+    name = str(t.dtype).replace("torch.", "")
+    if name not in _DT:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    return _DT[name]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dims(q, k, H, Hkv):
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q must be [B,Tq,H*hd] and k/v [B,Tk,Hkv*hd]")
+    B, Tq, qc = q.shape
+    Bk, Tk, kc = k.shape
+    if Bk != B or qc % H or kc % Hkv or qc // H != kc // Hkv:
+        raise ValueError("inconsistent shapes: q %s, k %s, H=%d, Hkv=%d" % (tuple(q.shape), tuple(k.shape), H, Hkv))
+    return B, Tq, Tk, qc // H
+
+
+def _mask(key_mask, B, Tk):
+    if key_mask is None:
+        return None, 0
+    if key_mask.dtype != _torch().float32 or not key_mask.is_contiguous():
+        raise ValueError("key_mask must be a contiguous fp32 tensor")
+    if key_mask.dim() == 1:
+        if key_mask.shape[0] != Tk:
+            raise ValueError("key_mask must have Tk entries")
+        return key_mask, 0
+    if tuple(key_mask.shape) != (B, Tk):
+        raise ValueError("key_mask must be [Tk] or [B,Tk]")
+    return key_mask, Tk
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def attn_fwd(q, k, v, *, H, Hkv, scale=None, causal=False, window=0, softcap=0.0, q_offset=0, key_mask=None,
+             o=None, lse=None, want_lse=True, stream=None):
+    """Forward attention; returns (o, lse).  lse is None when want_lse is False."""
+    torch = _torch()
+    _contig(q, k, v, o, lse)
+    B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    st = lib().attn_fwd(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Tq, Tk, H, Hkv, hd,
+                        float(scale), int(bool(causal)), int(window), float(softcap), int(q_offset), _ptr(m),
+                        int(ms), _stream(stream))
+    _check(st, "attn_fwd")
+    return o, lse
+
+
+def attn_bwd_workspace_size(B, Tq, H) -> int:
+    return int(lib().attn_bwd_workspace_size(B, Tq, H))
+
+
+def attn_bwd(q, k, v, o, do, lse, *, H, Hkv, scale=None, causal=False, window=0, softcap=0.0, q_offset=0,
+             key_mask=None, dq=None, dk=None, dv=None, workspace=None, stream=None, phases=7):
+    """Backward attention; returns (dq, dk, dv), overwritten.
+
+    phases selects passes (1 = D = rowsum(dO*O), 2 = dK/dV, 4 = dQ); passes 2 and 4
+    read the D that pass 1 left in `workspace`, so pass the same workspace."""
+    torch = _torch()
+    _contig(q, k, v, o, do, lse, dq, dk, dv)
+    B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = attn_bwd_workspace_size(B, Tq, H)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    st = lib().attn_bwd_phases(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                               _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               B, Tq, Tk, H, Hkv, hd, float(scale), int(bool(causal)), int(window), float(softcap),
+                               int(q_offset), _ptr(m), int(ms), _stream(stream), int(phases))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd) -> int:
+    return int(lib().attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd))
+
+
+def attn_decode(q, k, v, *, H, Hkv, scale=None, causal=True, window=0, softcap=0.0, q_offset=None, key_mask=None,
+                o=None, lse=None, want_lse=True, workspace=None, stream=None):
+    """Split-KV decode of an Lq-row block; q_offset defaults to Tk - Lq. Returns (o, lse)."""
+    torch = _torch()
+    _contig(q, k, v, o, lse)
+    B, Lq, Tk, hd = _dims(q, k, H, Hkv)
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    q_offset = Tk - Lq if q_offset is None else q_offset
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    nbytes = attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    st = lib().attn_decode(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), B, Lq, Tk, H, Hkv, hd, float(scale),
+                           int(bool(causal)), int(window), float(softcap), int(q_offset), _ptr(m), int(ms),
+                           _stream(stream))
+    _check(st, "attn_decode")
+    return o, lse
+
+
+def attn_get_device_status(stream=None):
+    """(status, detail word); reads and clears the device status word."""
+    w = ctypes.c_uint(0)
+    st = lib().attn_get_device_status(_stream(stream), ctypes.byref(w))
+    return int(st), int(w.value)
+
+
+def attn_selftest_bounded_wait(timeout_us: int, stream=None):
+    _check(lib().attn_selftest_bounded_wait(int(timeout_us), _stream(stream)), "attn_selftest_bounded_wait")
+
+
+def attn_launch_count() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().attn_launch_count())
+
+
+def attn_kernel_family(dtype: str, hd: int) -> int:
+    return int(lib().attn_kernel_family(_DT[dtype], int(hd)))

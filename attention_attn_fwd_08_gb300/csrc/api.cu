@@ -1,0 +1,333 @@
+// api.cu -- the C ABI declared in include/attn.h: host-side validation,
+// planning (tile and split counts), TMA descriptor encoding and dispatch.
+//
+// Argument rules follow ferrotensor engine/attention.rs, AttentionDims::new
+// (num_heads a multiple of num_kv_heads, bounded head_dim) and the brotensor
+// ops/flash_attention.h contracts (caller-owned buffers, overwrite semantics,
+// a length-Tk fp32 key mask).  Nothing here allocates, frees or synchronises
+// (except attn_get_device_status, which exists to read the status word).
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+using namespace attn;
+
+#ifndef ATTN_USE_TCGEN05
+#define ATTN_USE_TCGEN05 0
+#endif
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::atomic<unsigned long long> g_launches{0};
+
+attn_status counted(cudaError_t e, int kernels) {
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    g_launches.fetch_add((unsigned long long)kernels, std::memory_order_relaxed);
+    return ATTN_OK;
+}
+
+// Device status word: bounded waits that run out OR a bit in here.
+__device__ unsigned int g_status_word;
+
+unsigned int* status_ptr() {
+    static unsigned int* ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned int*>(p);
+    }
+    return ptrs[dev];
+}
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a [batches][rows][inner] 16-bit tensor, box {64, box_rows, 1},
+// 128-byte swizzle (inner box = 64 elements = 128 bytes).
+bool make_map(CUtensorMap* m, int dt, const void* base, long long inner, long long rows, long long batches,
+              int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const CUtensorMapDataType t = dt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)batches};
+    cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * rows * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, t, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status check_common(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal,
+                         int window, float softcap, int q_offset, const float* key_mask, long long mstride) {
+    if (dt != ATTN_F32 && dt != ATTN_F16 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || Tq < 0 || Tk < 0) return ATTN_ERR_INVALID_ARG;
+    if (B > 65535) return ATTN_ERR_INVALID_ARG;
+    if (H <= 0 || Hkv <= 0 || H % Hkv != 0 || H > 65535) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!(softcap >= 0.f) || !isfinite(softcap)) return ATTN_ERR_INVALID_ARG;
+    if (window < 0 || q_offset < 0) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (mstride < 0) return ATTN_ERR_INVALID_ARG;
+    if (key_mask && (reinterpret_cast<uintptr_t>(key_mask) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if ((long long)Tq + q_offset > INT32_MAX - 1) return ATTN_ERR_INVALID_ARG;
+    if (hd != 64 && hd != 128) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal, int window,
+                   float softcap, int q_offset, const float* key_mask, long long mstride) {
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.B = B; p.Tq = Tq; p.Tk = Tk; p.H = H; p.Hkv = Hkv; p.hd = hd; p.G = H / Hkv;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.causal = causal; p.window = window; p.softcap = softcap; p.q_offset = q_offset;
+    p.key_mask = key_mask; p.mask_bstride = mstride;
+    p.status = status_ptr();
+    return p;
+}
+
+bool use_tcgen05(attn_dtype dt, int hd) {
+    (void)hd;
+    return dt != ATTN_F32 && ATTN_USE_TCGEN05;
+}
+
+// Decode split plan: a deterministic function of the shape.  Aim for about
+// eight waves of two resident CTAs on each of GB300's 152 SMs.
+void decode_plan(int B, int Lq, int Tk, int H, int Hkv, int* splits, int* chunk) {
+    const int R = (H / Hkv) * Lq;
+    const long long units = (long long)B * Hkv * ((R + 15) / 16);
+    const long long target = 8LL * 2 * 152;
+    long long s = (target + units - 1) / units;
+    const long long max_s = Tk > 0 ? (Tk + 63) / 64 : 1;
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    long long c = Tk > 0 ? (Tk + s - 1) / s : 64;
+    c = ((c + 63) / 64) * 64;
+    *chunk = (int)c;
+    *splits = Tk > 0 ? (int)((Tk + c - 1) / c) : 1;
+}
+
+attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// O = 0, LSE = -inf for every row (Tk == 0: no key is visible).
+template <typename T>
+__global__ void fill_empty_kernel(T* o, long long n_o, float* lse, long long n_lse) {
+    const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (i < n_o) o[i] = T(0.f);
+    if (lse && i < n_lse) lse[i] = -INFINITY;
+}
+
+attn_status fill_empty(attn_dtype dt, void* o, long long n_o, float* lse, long long n_lse, cudaStream_t s) {
+    const long long n = n_o > n_lse ? n_o : n_lse;
+    if (n == 0) return ATTN_OK;
+    const unsigned blocks = (unsigned)((n + 255) / 256);
+    if (dt == ATTN_F32) fill_empty_kernel<float><<<blocks, 256, 0, s>>>((float*)o, n_o, lse, n_lse);
+    else if (dt == ATTN_F16) fill_empty_kernel<__half><<<blocks, 256, 0, s>>>((__half*)o, n_o, lse, n_lse);
+    else fill_empty_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>((__nv_bfloat16*)o, n_o, lse, n_lse);
+    return counted(cudaGetLastError(), 1);
+}
+
+size_t elem_size(attn_dtype dt) { return dt == ATTN_F32 ? 4 : 2; }
+
+}  // namespace
+
+// ================================================================ C ABI
+extern "C" {
+
+int attn_abi_version(void) { return 1; }
+
+const char* attn_status_string(attn_status s) {
+    switch (s) {
+        case ATTN_OK: return "ok";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case ATTN_ERR_CUDA: return "CUDA error";
+        case ATTN_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    }
+    return "unknown status";
+}
+
+int attn_kernel_family(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) ? 1 : 0; }
+
+attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal, int window, float softcap,
+                     int q_offset, const float* key_mask, long long key_mask_bstride, void* stream) {
+    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    if (B == 0 || Tq == 0) return ATTN_OK;
+    if (!q || !o || (Tk > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+        return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fill_empty(dt, o, (long long)B * Tq * H * hd, lse, lse ? (long long)B * H * Tq : 0, s);
+    Params p = base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                           key_mask_bstride);
+    if (!p.status) return ATTN_ERR_CUDA;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    if (!use_tcgen05(dt, hd)) return counted(launch_simt_fwd(p, (int)dt, s), 1);
+    FwdMaps maps;
+    if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
+        !make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 128) ||
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128))
+        return ATTN_ERR_CUDA;
+    return counted(launch_tc_fwd(p, (int)dt, maps, s), 1);
+}
+
+size_t attn_bwd_workspace_size(int B, int Tq, int H) {
+    if (B < 0 || Tq < 0 || H < 0) return 0;
+    return (size_t)B * Tq * H * sizeof(float);
+}
+
+attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
+                            int causal, int window, float softcap, int q_offset, const float* key_mask,
+                            long long key_mask_bstride, void* stream, int phases) {
+    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    if (phases <= 0 || phases > 7) return ATTN_ERR_INVALID_ARG;
+    if (B == 0) return ATTN_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t es = elem_size(dt);
+    if (Tq == 0 || Tk == 0) {
+        // no visible pair: every gradient is zero
+        if (Tk > 0 && (phases & 2)) {
+            if (!dk || !dv || !aligned16(dk) || !aligned16(dv)) return ATTN_ERR_INVALID_ARG;
+            const size_t n = (size_t)B * Tk * Hkv * hd * es;
+            if (cudaMemsetAsync(dk, 0, n, s) != cudaSuccess || cudaMemsetAsync(dv, 0, n, s) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+        }
+        if (Tq > 0 && (phases & 4)) {
+            if (!dq || !aligned16(dq)) return ATTN_ERR_INVALID_ARG;
+            if (cudaMemsetAsync(dq, 0, (size_t)B * Tq * H * hd * es, s) != cudaSuccess) return ATTN_ERR_CUDA;
+        }
+        return ATTN_OK;
+    }
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < attn_bwd_workspace_size(B, Tq, H)) return ATTN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return ATTN_ERR_INVALID_ARG;
+    Params p = base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                           key_mask_bstride);
+    if (!p.status) return ATTN_ERR_CUDA;
+    p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse_in = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.delta = static_cast<float*>(workspace);
+    const int nk = ((phases & 1) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
+    if (!use_tcgen05(dt, hd)) return counted(launch_simt_bwd(p, (int)dt, phases, s), nk);
+    BwdMaps maps;
+    if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
+        !make_map(&maps.dout, dt, dout, (long long)H * hd, Tq, B, 128) ||
+        !make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 128) ||
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128))
+        return ATTN_ERR_CUDA;
+    return counted(launch_tc_bwd(p, (int)dt, maps, phases, s), nk);
+}
+
+attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
+                     int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal, int window, float softcap,
+                     int q_offset, const float* key_mask, long long key_mask_bstride, void* stream) {
+    return attn_bwd_phases(dt, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, Tq, Tk, H, Hkv,
+                           hd, scale, causal, window, softcap, q_offset, key_mask, key_mask_bstride, stream, 7);
+}
+
+unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv, int hd) {
+    if (B <= 0 || Lq <= 0 || Tk < 0 || H <= 0 || Hkv <= 0 || H % Hkv || (hd != 64 && hd != 128)) return 0;
+    int splits, chunk;
+    decode_plan(B, Lq, Tk, H, Hkv, &splits, &chunk);
+    return (size_t)B * H * Lq * splits * (hd + 2) * sizeof(float);
+}
+
+attn_status attn_decode(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                        void* workspace, size_t workspace_bytes, int B, int Lq, int Tk, int H, int Hkv, int hd,
+                        float scale, int causal, int window, float softcap, int q_offset, const float* key_mask,
+                        long long key_mask_bstride, void* stream) {
+    attn_status st = check_common(dt, B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    if (Lq > 16 || (H / Hkv) * Lq > 64) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Lq == 0) return ATTN_OK;
+    if (dt == ATTN_F32)  // fp32 stays on the fp32 CUDA-core kernel
+        return attn_fwd(dt, q, k, v, o, lse, B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset,
+                        key_mask, key_mask_bstride, stream);
+    if (!q || !o || (Tk > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+        return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fill_empty(dt, o, (long long)B * Lq * H * hd, lse, lse ? (long long)B * H * Lq : 0, s);
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd))
+        return ATTN_ERR_INVALID_ARG;
+    Params p = base_params(B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                           key_mask_bstride);
+    if (!p.status) return ATTN_ERR_CUDA;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.ws = static_cast<float*>(workspace);
+    decode_plan(B, Lq, Tk, H, Hkv, &p.splits, &p.chunk);
+    DecMaps maps;
+    if (!make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 64) ||
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 64))
+        return ATTN_ERR_CUDA;
+    return counted(launch_decode(p, (int)dt, maps, s), 2);
+}
+
+attn_status attn_get_device_status(void* stream, unsigned int* detail) {
+    unsigned int* ptr = status_ptr();
+    if (!ptr) return ATTN_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemcpy(&word, ptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(ptr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (detail) *detail = word;
+    return word ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status attn_selftest_bounded_wait(unsigned int timeout_us, void* stream) {
+    if (timeout_us == 0 || timeout_us > 2000000u) return ATTN_ERR_INVALID_ARG;
+    unsigned int* ptr = status_ptr();
+    if (!ptr) return ATTN_ERR_CUDA;
+    return counted(launch_selftest_wait(ptr, timeout_us, static_cast<cudaStream_t>(stream)), 1);
+}
+
+}  // extern "C"

@@ -1,0 +1,35 @@
+// kernels.h -- launchers the C ABI layer (api.cu) dispatches to.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace attn {
+
+// dt: 0 = fp32, 1 = fp16, 2 = bf16 (the attn_dtype values).
+cudaError_t launch_simt_fwd(const Params& p, int dt, cudaStream_t s);
+// phases: bit 1 = D = rowsum(dO*O), bit 2 = dK/dV, bit 4 = dQ
+cudaError_t launch_simt_bwd(const Params& p, int dt, int phases, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(const Params& p, int dt, cudaStream_t s);
+
+// tcgen05 prefill forward / backward (fp16 / bf16, hd 64 or 128).  The tensor
+// maps are built by the caller.
+struct FwdMaps {
+    CUtensorMap q, k, v;
+};
+cudaError_t launch_tc_fwd(const Params& p, int dt, const FwdMaps& maps, cudaStream_t s);
+struct BwdMaps {
+    CUtensorMap q, k, v, dout;
+};
+cudaError_t launch_tc_bwd(const Params& p, int dt, const BwdMaps& maps, int phases, cudaStream_t s);
+
+// split-KV decode (fp16 / bf16, hd 64 or 128).
+struct DecMaps {
+    CUtensorMap k, v;
+};
+cudaError_t launch_decode(const Params& p, int dt, const DecMaps& maps, cudaStream_t s);
+
+cudaError_t launch_selftest_wait(unsigned int* status, unsigned int timeout_us, cudaStream_t s);
+
+}  // namespace attn

@@ -1,0 +1,416 @@
+// simt.cu -- CUDA-core attention kernels: the fp32 forward and backward.
+//
+// fp32 inputs must stay off the tensor cores to keep fp32 accuracy (no TF32,
+// no 16-bit P), so these kernels do the whole computation with fp32 FMAs and
+// the accurate expf / logf / tanhf.  The same templates also instantiate for
+// 16-bit inputs (converted to fp32 on load); the D = rowsum(dO*O) preprocess
+// is shared with the tensor-core backward.
+//
+// Work split (one warp per output row, 8 rows per CTA sharing staged tiles):
+//   forward, dQ : CTA = 8 query rows of one (b, h); K/V tiles of 64 keys are
+//                 staged in shared memory as fp32, each lane scores 2 keys,
+//                 then owns hd/32 output columns for the P.V (or dS.K) update.
+//   dK/dV       : CTA = 8 key rows of one (b, kv head); Q/dO tiles of 64 rows
+//                 of every query head in the group are staged, each lane
+//                 handles 2 query rows; no atomics (the GQA group sum stays in
+//                 registers).
+// Sources: vision_rs flash_attn2.rs, Forward / Backward - dQ / Backward - dK,dV
+// (online-softmax recurrence, p = exp(s - LSE), dS = p (dO.V - D)); forge
+// attention.metal, attention_bwd_d_f32 / attention_bwd_dq_f32 /
+// attention_bwd_dkv_f32 (D = dO.O, softcap derivative, group sums).
+#include <math.h>
+
+#include "kernels.h"
+
+namespace attn {
+namespace {
+
+constexpr int kRows = 8;   // warps (rows) per CTA
+constexpr int kTile = 64;  // keys (or queries) staged per tile
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// capped score in natural units
+__device__ __forceinline__ float capped(float s, float softcap) {
+    return softcap > 0.f ? softcap * tanhf(s / softcap) : s;
+}
+
+template <typename T>
+__device__ __forceinline__ const T* qrow(const Params& P, const void* base, int b, int i, int h) {
+    return reinterpret_cast<const T*>(base) + ((long long)b * P.Tq + i) * (long long)P.H * P.hd +
+           (long long)h * P.hd;
+}
+template <typename T>
+__device__ __forceinline__ const T* kvrow(const Params& P, const void* base, int b, int j, int kvh) {
+    return reinterpret_cast<const T*>(base) + ((long long)b * P.Tk + j) * (long long)P.Hkv * P.hd +
+           (long long)kvh * P.hd;
+}
+
+// ------------------------------------------------------------------ forward
+template <typename T, int HD>
+__global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
+    extern __shared__ float sm[];
+    float* Ks = sm;                          // [kTile][HD+1]
+    float* Vs = Ks + kTile * (HD + 1);       // [kTile][HD]
+    float* Qs = Vs + kTile * HD;             // [kRows][HD]
+    float* Ps = Qs + kRows * HD;             // [kRows][kTile]
+    const int b = blockIdx.z, h = blockIdx.y, kvh = h / P.G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = blockIdx.x * kRows;
+    const int i = i0 + warp;
+    const bool row_ok = i < P.Tq;
+    const int p = i + P.q_offset;
+    const int ilast = min(i0 + kRows, P.Tq) - 1;
+    int lo, hi;
+    key_range(P.causal, P.window, P.Tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+
+    for (int d = lane; d < HD; d += 32)
+        Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, b, i, h)[d]) : 0.f;
+
+    float m = -INFINITY, l = 0.f;
+    float acc[HD / 32];
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) acc[c] = 0.f;
+
+    for (int j0 = (lo / kTile) * kTile; j0 < hi; j0 += kTile) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kTile * HD; e += blockDim.x) {
+            const int jj = e / HD, d = e % HD, j = j0 + jj;
+            float kv = 0.f, vv = 0.f;
+            if (j < P.Tk) {
+                kv = Elem<T>::to_f(kvrow<T>(P, P.k, b, j, kvh)[d]);
+                vv = Elem<T>::to_f(kvrow<T>(P, P.v, b, j, kvh)[d]);
+            }
+            Ks[jj * (HD + 1) + d] = kv;
+            Vs[jj * HD + d] = vv;
+        }
+        __syncthreads();
+        float s[2];
+        bool vis[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int jj = lane + 32 * t, j = j0 + jj;
+            float dot = 0.f;
+#pragma unroll 8
+            for (int d = 0; d < HD; ++d) dot = fmaf(Qs[warp * HD + d], Ks[jj * (HD + 1) + d], dot);
+            vis[t] = row_ok && visible(P, b, p, j);
+            s[t] = vis[t] ? capped(dot * P.scale, P.softcap) : -INFINITY;
+        }
+        const float m_new = fmaxf(m, warp_max(fmaxf(s[0], s[1])));
+        if (m_new == -INFINITY) continue;  // nothing visible yet for this row (warp-uniform)
+        const float alpha = expf(m - m_new);  // 0 when m = -inf
+        float pr[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) pr[t] = vis[t] ? expf(s[t] - m_new) : 0.f;
+        l = l * alpha + warp_sum(pr[0] + pr[1]);
+        Ps[warp * kTile + lane] = pr[0];
+        Ps[warp * kTile + lane + 32] = pr[1];
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+            float a = acc[c] * alpha;
+            const int d = lane + 32 * c;
+#pragma unroll 8
+            for (int jj = 0; jj < kTile; ++jj) a = fmaf(Ps[warp * kTile + jj], Vs[jj * HD + d], a);
+            acc[c] = a;
+        }
+        __syncwarp();
+        m = m_new;
+    }
+    if (!row_ok) return;
+    T* orow = reinterpret_cast<T*>(P.o) + ((long long)b * P.Tq + i) * (long long)P.H * P.hd +
+              (long long)h * P.hd;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) orow[lane + 32 * c] = Elem<T>::from_f(acc[c] * inv);
+    if (P.lse && lane == 0)
+        P.lse[((long long)b * P.H + h) * P.Tq + i] = l > 0.f ? m + logf(l) : -INFINITY;
+}
+
+// ------------------------------------------------------- backward: D = dO.O
+template <typename T>
+__global__ void bwd_preprocess_kernel(Params P) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const long long rows = (long long)P.B * P.Tq * P.H;
+    if (warp >= rows) return;
+    // row order (b, i, h) so consecutive warps read consecutive memory
+    const int h = warp % P.H;
+    const long long bi = warp / P.H;
+    const int i = (int)(bi % P.Tq), b = (int)(bi / P.Tq);
+    const T* o = qrow<T>(P, P.o_in, b, i, h);
+    const T* g = qrow<T>(P, P.dout, b, i, h);
+    float acc = 0.f;
+    for (int d = lane; d < P.hd; d += 32) acc = fmaf(Elem<T>::to_f(o[d]), Elem<T>::to_f(g[d]), acc);
+    acc = warp_sum(acc);
+    if (lane == 0) P.delta[((long long)b * P.H + h) * P.Tq + i] = acc;
+}
+
+// -------------------------------------------------------------- backward: dQ
+template <typename T, int HD>
+__global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
+    extern __shared__ float sm[];
+    float* Ks = sm;                      // [kTile][HD+1]
+    float* Vs = Ks + kTile * (HD + 1);   // [kTile][HD+1]
+    float* Qs = Vs + kTile * (HD + 1);   // [kRows][HD]
+    float* Gs = Qs + kRows * HD;         // [kRows][HD]  dO
+    float* Ss = Gs + kRows * HD;         // [kRows][kTile] dS
+    const int b = blockIdx.z, h = blockIdx.y, kvh = h / P.G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = blockIdx.x * kRows;
+    const int i = i0 + warp;
+    const bool row_ok = i < P.Tq;
+    const int p = i + P.q_offset;
+    const int ilast = min(i0 + kRows, P.Tq) - 1;
+    int lo, hi;
+    key_range(P.causal, P.window, P.Tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+    for (int d = lane; d < HD; d += 32) {
+        Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, b, i, h)[d]) : 0.f;
+        Gs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.dout, b, i, h)[d]) : 0.f;
+    }
+    const long long srow = ((long long)b * P.H + h) * P.Tq + i;
+    const float lse = row_ok ? P.lse_in[srow] : -INFINITY;
+    const float Dd = row_ok ? P.delta[srow] : 0.f;
+    const bool live = row_ok && lse != -INFINITY;
+    float acc[HD / 32];
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) acc[c] = 0.f;
+
+    for (int j0 = (lo / kTile) * kTile; j0 < hi; j0 += kTile) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < kTile * HD; e += blockDim.x) {
+            const int jj = e / HD, d = e % HD, j = j0 + jj;
+            float kv = 0.f, vv = 0.f;
+            if (j < P.Tk) {
+                kv = Elem<T>::to_f(kvrow<T>(P, P.k, b, j, kvh)[d]);
+                vv = Elem<T>::to_f(kvrow<T>(P, P.v, b, j, kvh)[d]);
+            }
+            Ks[jj * (HD + 1) + d] = kv;
+            Vs[jj * (HD + 1) + d] = vv;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int jj = lane + 32 * t, j = j0 + jj;
+            float ds = 0.f;
+            if (live && visible(P, b, p, j)) {
+                float qk = 0.f, gv = 0.f;
+#pragma unroll 8
+                for (int d = 0; d < HD; ++d) {
+                    qk = fmaf(Qs[warp * HD + d], Ks[jj * (HD + 1) + d], qk);
+                    gv = fmaf(Gs[warp * HD + d], Vs[jj * (HD + 1) + d], gv);
+                }
+                const float s = qk * P.scale;
+                float st = s, dcap = 1.f;
+                if (P.softcap > 0.f) {
+                    const float th = tanhf(s / P.softcap);
+                    st = P.softcap * th;
+                    dcap = 1.f - th * th;
+                }
+                const float pr = expf(st - lse);
+                ds = pr * (gv - Dd) * dcap;
+            }
+            Ss[warp * kTile + jj] = ds;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+            float a = acc[c];
+            const int d = lane + 32 * c;
+#pragma unroll 8
+            for (int jj = 0; jj < kTile; ++jj) a = fmaf(Ss[warp * kTile + jj], Ks[jj * (HD + 1) + d], a);
+            acc[c] = a;
+        }
+        __syncwarp();
+    }
+    if (!row_ok) return;
+    T* out = reinterpret_cast<T*>(P.dq) + ((long long)b * P.Tq + i) * (long long)P.H * P.hd +
+             (long long)h * P.hd;
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) out[lane + 32 * c] = Elem<T>::from_f(acc[c] * P.scale);
+}
+
+// ----------------------------------------------------------- backward: dK/dV
+template <typename T, int HD>
+__global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
+    extern __shared__ float sm[];
+    float* Qs = sm;                      // [kTile][HD+1]
+    float* Gs = Qs + kTile * (HD + 1);   // [kTile][HD+1]  dO
+    float* Ks = Gs + kTile * (HD + 1);   // [kRows][HD]
+    float* Vs = Ks + kRows * HD;         // [kRows][HD]
+    float* Ls = Vs + kRows * HD;         // [kTile] LSE
+    float* Ds = Ls + kTile;              // [kTile] D
+    float* Pw = Ds + kTile;              // [kRows][kTile] P
+    float* Sw = Pw + kRows * kTile;      // [kRows][kTile] dS
+    const int b = blockIdx.z, kvh = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j0 = blockIdx.x * kRows;
+    const int j = j0 + warp;
+    const bool key_ok = j < P.Tk;
+    const int jlast = min(j0 + kRows, P.Tk);
+    int qlo, qhi;
+    query_range(P.causal, P.window, P.Tq, P.q_offset, j0, jlast, &qlo, &qhi);
+    for (int d = lane; d < HD; d += 32) {
+        Ks[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.k, b, j, kvh)[d]) : 0.f;
+        Vs[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.v, b, j, kvh)[d]) : 0.f;
+    }
+    float dk[HD / 32], dv[HD / 32];
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) dk[c] = dv[c] = 0.f;
+
+    for (int h = kvh * P.G; h < (kvh + 1) * P.G; ++h) {
+        for (int i0 = (qlo / kTile) * kTile; i0 < qhi; i0 += kTile) {
+            __syncthreads();
+            for (int e = threadIdx.x; e < kTile * HD; e += blockDim.x) {
+                const int ii = e / HD, d = e % HD, i = i0 + ii;
+                float qv = 0.f, gv = 0.f;
+                if (i < P.Tq) {
+                    qv = Elem<T>::to_f(qrow<T>(P, P.q, b, i, h)[d]);
+                    gv = Elem<T>::to_f(qrow<T>(P, P.dout, b, i, h)[d]);
+                }
+                Qs[ii * (HD + 1) + d] = qv;
+                Gs[ii * (HD + 1) + d] = gv;
+            }
+            for (int ii = threadIdx.x; ii < kTile; ii += blockDim.x) {
+                const int i = i0 + ii;
+                const long long srow = ((long long)b * P.H + h) * P.Tq + i;
+                Ls[ii] = i < P.Tq ? P.lse_in[srow] : -INFINITY;
+                Ds[ii] = i < P.Tq ? P.delta[srow] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int ii = lane + 32 * t, i = i0 + ii;
+                float pr = 0.f, ds = 0.f;
+                if (key_ok && i < P.Tq && Ls[ii] != -INFINITY && visible(P, b, i + P.q_offset, j)) {
+                    float qk = 0.f, gv = 0.f;
+#pragma unroll 8
+                    for (int d = 0; d < HD; ++d) {
+                        qk = fmaf(Qs[ii * (HD + 1) + d], Ks[warp * HD + d], qk);
+                        gv = fmaf(Gs[ii * (HD + 1) + d], Vs[warp * HD + d], gv);
+                    }
+                    const float s = qk * P.scale;
+                    float st = s, dcap = 1.f;
+                    if (P.softcap > 0.f) {
+                        const float th = tanhf(s / P.softcap);
+                        st = P.softcap * th;
+                        dcap = 1.f - th * th;
+                    }
+                    pr = expf(st - Ls[ii]);
+                    ds = pr * (gv - Ds[ii]) * dcap;
+                }
+                Pw[warp * kTile + ii] = pr;
+                Sw[warp * kTile + ii] = ds;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                const int d = lane + 32 * c;
+                float a = dv[c], g = dk[c];
+#pragma unroll 8
+                for (int ii = 0; ii < kTile; ++ii) {
+                    a = fmaf(Pw[warp * kTile + ii], Gs[ii * (HD + 1) + d], a);
+                    g = fmaf(Sw[warp * kTile + ii], Qs[ii * (HD + 1) + d], g);
+                }
+                dv[c] = a;
+                dk[c] = g;
+            }
+            __syncwarp();
+        }
+    }
+    if (!key_ok) return;
+    const long long off = ((long long)b * P.Tk + j) * (long long)P.Hkv * P.hd + (long long)kvh * P.hd;
+    T* dkp = reinterpret_cast<T*>(P.dk) + off;
+    T* dvp = reinterpret_cast<T*>(P.dv) + off;
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) {
+        dkp[lane + 32 * c] = Elem<T>::from_f(dk[c] * P.scale);
+        dvp[lane + 32 * c] = Elem<T>::from_f(dv[c]);
+    }
+}
+
+template <typename T, int HD>
+cudaError_t fwd_typed(const Params& p, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (kTile * (HD + 1) + kTile * HD + kRows * HD + kRows * kTile);
+    auto kern = simt_fwd_kernel<T, HD>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.Tq + kRows - 1) / kRows, p.H, p.B);
+    kern<<<grid, kRows * 32, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t preprocess_typed(const Params& p, cudaStream_t s) {
+    const long long rows = (long long)p.B * p.Tq * p.H;
+    const int threads = 256;
+    const long long blocks = (rows * 32 + threads - 1) / threads;
+    bwd_preprocess_kernel<T><<<(unsigned)blocks, threads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, int HD>
+cudaError_t bwd_typed(const Params& p, int phases, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    if (phases & 1) {
+        e = preprocess_typed<T>(p, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (phases & 2) {
+        const size_t smem_kv =
+            sizeof(float) * (2 * kTile * (HD + 1) + 2 * kRows * HD + 2 * kTile + 2 * kRows * kTile);
+        auto kkv = simt_dkdv_kernel<T, HD>;
+        e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_kv);
+        if (e != cudaSuccess) return e;
+        kkv<<<dim3((p.Tk + kRows - 1) / kRows, p.Hkv, p.B), kRows * 32, smem_kv, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (!(phases & 4)) return cudaSuccess;
+    const size_t smem_dq =
+        sizeof(float) * (2 * kTile * (HD + 1) + 2 * kRows * HD + kRows * kTile);
+    auto kdq = simt_dq_kernel<T, HD>;
+    e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dq);
+    if (e != cudaSuccess) return e;
+    kdq<<<dim3((p.Tq + kRows - 1) / kRows, p.H, p.B), kRows * 32, smem_dq, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_simt_fwd(const Params& p, int dt, cudaStream_t s) {
+    if (p.hd == 64) {
+        if (dt == 0) return fwd_typed<float, 64>(p, s);
+        if (dt == 1) return fwd_typed<__half, 64>(p, s);
+        return fwd_typed<__nv_bfloat16, 64>(p, s);
+    }
+    if (dt == 0) return fwd_typed<float, 128>(p, s);
+    if (dt == 1) return fwd_typed<__half, 128>(p, s);
+    return fwd_typed<__nv_bfloat16, 128>(p, s);
+}
+
+cudaError_t launch_bwd_preprocess(const Params& p, int dt, cudaStream_t s) {
+    if (dt == 0) return preprocess_typed<float>(p, s);
+    if (dt == 1) return preprocess_typed<__half>(p, s);
+    return preprocess_typed<__nv_bfloat16>(p, s);
+}
+
+cudaError_t launch_simt_bwd(const Params& p, int dt, int phases, cudaStream_t s) {
+    if (p.hd == 64) {
+        if (dt == 0) return bwd_typed<float, 64>(p, phases, s);
+        if (dt == 1) return bwd_typed<__half, 64>(p, phases, s);
+        return bwd_typed<__nv_bfloat16, 64>(p, phases, s);
+    }
+    if (dt == 0) return bwd_typed<float, 128>(p, phases, s);
+    if (dt == 1) return bwd_typed<__half, 128>(p, phases, s);
+    return bwd_typed<__nv_bfloat16, 128>(p, phases, s);
+}
+
+}  // namespace attn

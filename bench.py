@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Throughput of the fused-attention hot path on GB300.
+
+One step = one pass of the whole path over the GQA causal prefill workload
+(B=4, T=2048, H=32, Hkv=8, hd=128, bf16, LSE saved): attn_fwd, then the
+backward's three passes (D, dK/dV, dQ).  `value` is that step's algorithmic
+TFLOP/s (fwd 4*hd flops per visible (query,key) pair per head, fwd+bwd 3.5x
+that).  Decode (B=16, H=32, Hkv=8, hd=128, Lk=32768, Lq=1 and 4) is measured in
+the same run and reported in GB/s under "components".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same workload on its own GPU (replicas, no
+collective on the data path); rank 0 prints one JSON line.  --impl reference
+times the fp64 CPU oracle on bounded samples of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd & fwd+bwd TFLOP/s vs BF16 peak; decode HBM GB/s vs peak"
+FWD_FLOPS_PER_PAIR = lambda hd: 4 * hd
+KERNEL_FLOPS_PER_PAIR = {  # algorithmic GEMM flops per visible pair per head, by kernel
+    "fwd": lambda hd: 4 * hd,     # S = QK^T, O += PV
+    "dkdv": lambda hd: 8 * hd,    # S^T and dP^T recompute, dV += P^T dO, dK += dS^T Q
+    "dq": lambda hd: 6 * hd,      # S and dP recompute, dQ += dS K
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def visible_pairs(w, lengths=None):
+    """Exact number of visible (query, key) pairs summed over batch and heads."""
+    import numpy as np
+
+    p = np.arange(w.Tq, dtype=np.int64) + w.q_offset
+    lo = np.zeros_like(p)
+    hi = np.full_like(p, w.Tk)
+    if w.causal:
+        hi = np.minimum(hi, p + 1)
+    if w.window > 0:
+        lo = np.maximum(lo, p - w.window + 1)
+        if not w.causal:
+            hi = np.minimum(hi, p + w.window)
+    if lengths is None:
+        per_b = np.maximum(hi - lo, 0).sum() * np.ones(w.B, dtype=np.int64)
+    else:
+        per_b = np.array([np.maximum(np.minimum(hi, int(L)) - lo, 0).sum() for L in lengths], dtype=np.int64)
+    return int(per_b.sum()) * w.H
+
+
+def decode_bytes(w):
+    kv = 2 * w.B * w.Tk * w.Hkv * w.hd * 2
+    qo = 2 * w.B * w.Tq * w.H * w.hd * 2
+    return kv + qo + w.B * w.H * w.Tq * 4
+
+
+def src_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "attention_attn_fwd_08_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, sha):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(kernel)
+    if not d or d.get("source_sha") != sha:
+        return None
+    return d.get("bytes_per_launch")
+
+
+class Clocks:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.dev)], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]), hw=f[5], hwt=f[6],
+                                 swt=f[7], cap=f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = sorted({name for r in rows for name, key in (("hw_slowdown", "hw"), ("hw_thermal_slowdown", "hwt"),
+                                                                ("sw_thermal_slowdown", "swt"),
+                                                                ("sw_power_cap", "cap"))
+                          if r[key].lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------------- reference
+def oracle_sample(w, inp, groups, rows):
+    """Oracle fwd+bwd on `rows` trailing query rows of each (b, kv head) in `groups`.
+
+    Returns (seconds, algorithmic flops).  The groups are stacked as a batch of
+    independent problems (one KV head each), which is exact for attention."""
+    import numpy as np
+    import oracle
+
+    G, hd, T = w.H // w.Hkv, w.hd, w.Tq
+    r0 = T - rows
+    f = lambda t: t.to(dtype=__import__("torch").float64).numpy()
+    q = np.concatenate([f(inp["q"][b:b + 1, r0:, kvh * G * hd:(kvh + 1) * G * hd]) for b, kvh in groups])
+    do = np.concatenate([f(inp["do"][b:b + 1, r0:, kvh * G * hd:(kvh + 1) * G * hd]) for b, kvh in groups])
+    k = np.concatenate([f(inp["k"][b:b + 1, :, kvh * hd:(kvh + 1) * hd]) for b, kvh in groups])
+    v = np.concatenate([f(inp["v"][b:b + 1, :, kvh * hd:(kvh + 1) * hd]) for b, kvh in groups])
+    kw = dict(H=G, Hkv=1, scale=w.scale, causal=w.causal, window=w.window, softcap=w.softcap, q_offset=r0)
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, **kw)
+    oracle.bwd(q, k, v, do, **kw)
+    dt = time.perf_counter() - t0
+    pairs = sum(min(T, p + 1) - max(0, p - w.window + 1 if w.window else 0) for p in range(r0, T)) * G * len(groups)
+    return dt, 3.5 * FWD_FLOPS_PER_PAIR(hd) * pairs
+
+
+def oracle_groups(w, n):
+    return [(b, kvh) for b in range(w.B) for kvh in range(w.Hkv)][:n]
+
+
+def run_reference(args, rank):
+    from attention_attn_fwd_08_gb300 import synth
+    import oracle
+
+    if rank != 0:
+        return
+    oracle.build()
+    w = synth.WORKLOADS["gqa_prefill"]
+    inp = synth.make_inputs(w)
+    groups, rows = oracle_groups(w, 8), 64
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, groups, rows)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(w, inp, groups, rows)
+        times.append(dt)
+        flops = fl
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = "fwd+bwd of the last %d query rows of %d (batch, KV head) groups per step" % (rows, len(groups))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": "GQA causal prefill fwd+bwd, B=%d T=%d H=%d Hkv=%d hd=%d, bf16, LSE saved" % (
+        w.B, w.Tq, w.H, w.Hkv, w.hd), "B": w.B, "T": w.Tq, "H": w.H, "Hkv": w.Hkv, "hd": w.hd, "causal": True,
+            "parallelism": "replicas", "l2": "flushed between steps (512 MiB write), outside the timed events"}
+
+
+# --------------------------------------------------------------------- ours
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import attention_attn_fwd_08_gb300 as A
+    from attention_attn_fwd_08_gb300 import synth
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    A.lib()
+    peaks = load_peaks()
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS["gqa_prefill"]
+    inp = synth.make_inputs(w)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    kw = dict(H=w.H, Hkv=w.Hkv, scale=w.scale, causal=w.causal)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Tq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(A.attn_bwd_workspace_size(w.B, w.Tq, w.H), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    phases = [
+        ("fwd", lambda: A.attn_fwd(q, k, v, o=o, lse=lse, **kw)),
+        ("preprocess", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=1, **kw)),
+        ("dkdv", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=2, **kw)),
+        ("dq", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=4, **kw)),
+    ]
+
+    def step():
+        for _, fn in phases:
+            fn()
+
+    for _ in range(args.warmup):
+        flush_buf.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    if st != A.OK:
+        raise RuntimeError("device status word %#x after warm-up" % word)
+
+    stream = torch.cuda.current_stream()
+    per_phase = {n: [] for n, _ in phases}
+    steps_ms = []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = A.attn_launch_count()
+    wall0 = time.perf_counter()
+    with Clocks(local) as clk:
+        for _ in range(args.steps):
+            flush_buf.zero_()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+            evs[0].record(stream)
+            for i, (_, fn) in enumerate(phases):
+                fn()
+                evs[i + 1].record(stream)
+            torch.cuda.synchronize()
+            for i, (n, _) in enumerate(phases):
+                per_phase[n].append(evs[i].elapsed_time(evs[i + 1]))
+            steps_ms.append(evs[0].elapsed_time(evs[-1]))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = A.attn_launch_count() - n0
+    if world > 1:
+        dist.barrier()
+    st, word = A.attn_get_device_status()
+    if st != A.OK:
+        raise RuntimeError("device status word %#x after the timed steps" % word)
+
+    ms_step = statistics.mean(steps_ms)
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    pairs = visible_pairs(w)
+    step_flops = 3.5 * FWD_FLOPS_PER_PAIR(w.hd) * pairs
+    value = step_flops * world / (ms_step * 1e-3) / 1e12
+
+    comps = {}
+    for n in ("fwd", "dkdv", "dq"):
+        ms = statistics.mean(per_phase[n])
+        tf = KERNEL_FLOPS_PER_PAIR[n](w.hd) * pairs / (ms * 1e-3) / 1e12
+        comps[n] = {"ms": ms, "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                    "flops_per_launch": KERNEL_FLOPS_PER_PAIR[n](w.hd) * pairs}
+    pre_ms = statistics.mean(per_phase["preprocess"])
+    pre_bytes = 2 * w.B * w.Tq * w.H * w.hd * 2 + w.B * w.H * w.Tq * 4
+    comps["preprocess"] = {"ms": pre_ms, "GB/s": pre_bytes / (pre_ms * 1e-3) / 1e9}
+    comps["fwd_bwd_step"] = {"ms": ms_step, "TFLOP/s": value / world}
+
+    # ---------------------------------------------------------------- decode
+    del flush_buf
+    for name in ("decode_lq1", "decode_lq4"):
+        wd = synth.WORKLOADS[name]
+        di = synth.make_inputs(wd)
+        qd_, kd_, vd_ = (di[n].to(dev) for n in ("q", "k", "v"))
+        od_ = torch.empty_like(qd_)
+        lsed_ = torch.empty((wd.B, wd.H, wd.Tq), dtype=torch.float32, device=dev)
+        wsd = torch.empty(A.attn_decode_workspace_size(wd.B, wd.Tq, wd.Tk, wd.H, wd.Hkv, wd.hd), dtype=torch.uint8,
+                          device=dev)
+        fn = lambda: A.attn_decode(qd_, kd_, vd_, H=wd.H, Hkv=wd.Hkv, causal=True, q_offset=wd.q_offset, o=od_,
+                                   lse=lsed_, workspace=wsd)
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.mean(times)
+        gbs = decode_bytes(wd) / (ms * 1e-3) / 1e9
+        comps[name] = {"ms": ms, "GB/s": gbs, "frac_of_hbm_peak": gbs / peaks["hbm"], "bytes_per_call": decode_bytes(wd),
+                       "note": "K/V (2 GiB) exceed L2; split + combine kernels timed together"}
+        del qd_, kd_, vd_, od_, wsd
+    st, word = A.attn_get_device_status()
+    if st != A.OK:
+        raise RuntimeError("device status word %#x after decode" % word)
+
+    # ------------------------------------------------------ dominant kernel
+    dom = max(("fwd", "dkdv", "dq"), key=lambda n: comps[n]["ms"])
+    fam = A.attn_kernel_family("bfloat16", w.hd)
+    src = {"fwd": ("fwd_tc.cu",) if fam else ("simt.cu",), "dkdv": ("bwd_tc.cu",) if fam else ("simt.cu",),
+           "dq": ("bwd_tc.cu",) if fam else ("simt.cu",)}[dom]
+    ach = comps[dom]["TFLOP/s"]
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16"], "traffic": traffic_for(dom, src_sha(*src)),
+                "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peaks["source"],
+                "flops_per_launch": comps[dom]["flops_per_launch"], "ms_per_launch": comps[dom]["ms"]}
+
+    # ------------------------------------------------------------------ e2e
+    e2e = measure_e2e(A, w, inp, dev, stream, args, kw)
+
+    # ---------------------------------------------------------- cpu baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        groups, rows = oracle_groups(w, 16), 512
+        dt, fl = oracle_sample(w, inp, groups, rows)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": "fwd+bwd of the last %d query rows of %d (batch, KV head) groups, %.1f s" % (
+                   rows, len(groups), dt)}
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1))", "config": workload_config(w),
+            "kernel_family": "tcgen05" if fam else "simt", "components": components_round(comps),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk.summary(), "wall_s_timed_loop": wall}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def components_round(c):
+    return {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()} for k, v in c.items()}
+
+
+def measure_e2e(A, w, inp, dev, stream, args, kw):
+    """Same step through the public API from pinned host buffers: H2D of q,k,v,dO, fwd, bwd, D2H of o,dq,dk,dv."""
+    import torch
+
+    h_in = [inp[n].pin_memory() for n in ("q", "k", "v", "do")]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    h_out = [torch.empty_like(inp[n]).pin_memory() for n in ("q", "q", "k", "v")]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        q, k, v, do = d_in
+        o, lse = A.attn_fwd(q, k, v, **kw)
+        dq, dk, dv = A.attn_bwd(q, k, v, o, do, lse, **kw)
+        for h, d in zip(h_out, (o, dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.mean(times)
+    flops = 3.5 * FWD_FLOPS_PER_PAIR(w.hd) * visible_pairs(w)
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+if __name__ == "__main__":
+    main()

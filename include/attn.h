@@ -1,0 +1,194 @@
+/*
+ * attn.h -- C ABI of the GB300 fused-attention library (libattn_gb300.so).
+ *
+ * Scaled-dot-product attention with tiled online softmax on one GPU:
+ * forward with saved log-sum-exp, FlashAttention-2-style backward, and
+ * split-KV decode for a short query block over a long KV cache.
+ *
+ * What is computed (per batch b, query head h, query row i, key j):
+ *   kv     = h / (H / Hkv)      consecutive query heads share a KV head
+ *          (brotensor ops/flash_attention.h, flash_attention_decode: query head h
+ *           maps to KV head h/(num_q_heads/num_kv_heads))
+ *   p      = i + q_offset       absolute query position
+ *          (ferrotensor_backend engine/attention.rs, AttentionOptions.causal_offset)
+ *   s      = scale * q_i . k_j
+ *   st     = softcap > 0 ? softcap * tanh(s / softcap) : s
+ *          (brotensor ops/flash_attention.h, flash_attention_decode, Gemma-2
+ *           extensions: after the scale, before mask and softmax; 0 = off)
+ *   key j visible iff  (!causal || j <= p)
+ *                   && (window == 0 || |p - j| < window)
+ *                   && (key_mask == NULL || key_mask[b*stride + j] > 0.5)
+ *          (ferrotensor AttentionOptions for causal/window -- with causal this is
+ *           keys [max(0, p-window+1), p] as brotensor flash_attention_decode and
+ *           forge attention.metal AttnParams state; brotensor flash_attention_backward
+ *           for the 1/0 key mask with the 0.5 threshold)
+ *   O_i    = sum_j softmax_j(st_ij over visible j) v_j
+ *   LSE_i  = ln sum_{visible j} exp(st_ij)      natural log, capped scores
+ *          (vision_rs flash_attn2.rs, Forward: logsumexp saved for backward)
+ *   A row with no visible key gets O_i = 0 and LSE_i = -inf and adds nothing to
+ *   any gradient.
+ *
+ * Layouts (all row-major, contiguous, caller-owned device memory):
+ *   q, o, do, dq : [B][Tq][H*hd]     k, v, dk, dv : [B][Tk][Hkv*hd]
+ *   lse          : [B][H][Tq] fp32
+ *   key_mask     : fp32, key j of batch b at key_mask[b*key_mask_bstride + j];
+ *                  key_mask_bstride = 0 shares one length-Tk mask across batches.
+ *   (forge attention.metal: q/o [B,T,H*hd], k/v [B,T,Hkv*hd]; brotensor: a
+ *    length-Lk fp32 key mask, caller-owned.)
+ *
+ * Ownership and execution: the library never allocates, frees or synchronises.
+ * Every call validates its arguments on the host, then enqueues kernels on
+ * `stream` (a cudaStream_t passed as void*; NULL = legacy default stream) and
+ * returns.  Outputs and gradients are overwritten, never accumulated
+ * (ferrotensor flash_attention_backward: "Writes (does not accumulate into)").
+ * Pointers must be 16-byte aligned.  The device current on the calling thread
+ * must own every pointer.
+ *
+ * Errors: argument errors return ATTN_ERR_INVALID_ARG (or ATTN_ERR_UNSUPPORTED
+ * for a valid but unimplemented shape/dtype) before anything is enqueued and
+ * nothing is written.  A failed launch returns ATTN_ERR_CUDA.  Kernels never
+ * trap: every wait inside a kernel is bounded, and a wait that runs out sets a
+ * device status word that attn_get_device_status() reports as ATTN_ERR_TIMEOUT.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,
+    ATTN_ERR_UNSUPPORTED = 2,
+    ATTN_ERR_CUDA = 3,
+    ATTN_ERR_TIMEOUT = 4
+} attn_status;
+
+typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
+
+/*
+ * Forward.  O = softmax(st) V over the visible keys, LSE saved when lse != NULL.
+ * Source: vision_rs flash_attn2.rs, Forward (online softmax with saved
+ * logsumexp); ferrotensor flash_attention_v2_with (GQA, causal offset, window);
+ * brotensor flash_attention_gqa_forward / flash_attention_windowed_forward
+ * (key mask, softcap, bidirectional encoder case).
+ *   dt        : element type of q, k, v, o (fp32 math inside for every type).
+ *   q, k, v   : inputs, layouts above.          o : output [B][Tq][H*hd].
+ *   lse       : output [B][H][Tq] fp32, or NULL to skip.
+ *   B, Tq, Tk : batch, query rows, key rows (>= 0; B or Tq == 0 is a no-op,
+ *               Tk == 0 writes O = 0, LSE = -inf).
+ *   H, Hkv    : query / KV heads, Hkv >= 1 divides H.
+ *   hd        : head dim, 64 or 128.
+ *   scale     : > 0 and finite (1/sqrt(hd) in the usual case).
+ *   causal    : 0/1.   window : >= 0, 0 = unbounded.   softcap : >= 0, 0 = off.
+ *   q_offset  : >= 0, absolute position of query row 0.
+ *   key_mask  : NULL or fp32 mask as above; key_mask_bstride >= 0.
+ */
+ATTN_API attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
+                     float* lse, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
+                     int causal, int window, float softcap, int q_offset, const float* key_mask,
+                     long long key_mask_bstride, void* stream);
+
+/* Bytes of scratch attn_bwd needs: D = rowsum(dO * O), one fp32 per (b, h, i). */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Tq, int H);
+
+/*
+ * Backward (FlashAttention-2 style, deterministic, no atomics).
+ * Source: vision_rs flash_attn2.rs, "Backward - dQ" and "Backward - dK / dV";
+ * forge attention.metal, attention_bwd_d_f32 (D = dO.O), attention_bwd_dq_f32,
+ * attention_bwd_dkv_f32 (softcap derivative 1 - tanh^2, GQA group sums);
+ * ferrotensor flash_attention_v2_backward_with (separate dQ and dK/dV passes).
+ *   o, lse    : the forward's output and saved LSE for the same arguments.
+ *   dout      : upstream gradient of o, layout of q.
+ *   dq, dk, dv: outputs, layouts of q, k, v; overwritten.
+ *   workspace : device scratch of at least attn_bwd_workspace_size() bytes,
+ *               16-byte aligned; contents on entry are ignored.
+ *   Other arguments exactly as for attn_fwd (same values as the forward call).
+ */
+ATTN_API attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int B, int Tq, int Tk, int H,
+                     int Hkv, int hd, float scale, int causal, int window, float softcap,
+                     int q_offset, const float* key_mask, long long key_mask_bstride,
+                     void* stream);
+
+/*
+ * The three passes of attn_bwd, selectable one at a time (same arguments).
+ * phases is a bit set: 1 = D = rowsum(dO*O) into the workspace, 2 = dK/dV,
+ * 4 = dQ.  Passes 2 and 4 read the D that pass 1 wrote into the same
+ * workspace.  attn_bwd(...) is attn_bwd_phases(..., 7).
+ */
+ATTN_API attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const void* v,
+                     const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                     void* dv, void* workspace, size_t workspace_bytes, int B, int Tq, int Tk,
+                     int H, int Hkv, int hd, float scale, int causal, int window, float softcap,
+                     int q_offset, const float* key_mask, long long key_mask_bstride,
+                     void* stream, int phases);
+
+/* Bytes of scratch attn_decode needs (split-KV partials); 0 if the shape is invalid. */
+ATTN_API size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv, int hd);
+
+/*
+ * Split-KV decode: a block of Lq query rows (1 <= Lq <= 16) at positions
+ * q_offset .. q_offset+Lq-1 over a KV cache of Tk rows.  Each (b, KV head,
+ * key chunk) is one CTA that reads its K/V rows once for all (H/Hkv)*Lq query
+ * rows of the group; a second kernel merges the chunks by log-sum-exp.
+ * Source: brotensor ops/flash_attention.h, flash_attention_decode (query p =
+ * valid_len - L_q + q attends [0, p], GQA, softcap, window) and
+ * flash_attention_decode_len (work divided over the keys; split points change
+ * only the rounding; R > 1 rows each read the cache once).
+ *   dt        : ATTN_BF16 or ATTN_F16 (ATTN_F32 runs the fp32 forward kernel).
+ *   q, o      : [B][Lq][H*hd];  k, v : [B][Tk][Hkv*hd];  lse : [B][H][Lq] or NULL.
+ *   workspace : device scratch of at least attn_decode_workspace_size() bytes,
+ *               16-byte aligned.
+ *   (H/Hkv)*Lq <= 64, hd 64 or 128; the rest as for attn_fwd.  The usual KV-cache
+ *   call is causal with q_offset = Tk - Lq.
+ */
+ATTN_API attn_status attn_decode(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, int B, int Lq,
+                        int Tk, int H, int Hkv, int hd, float scale, int causal, int window,
+                        float softcap, int q_offset, const float* key_mask,
+                        long long key_mask_bstride, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+ATTN_API const char* attn_status_string(attn_status s);
+
+/*
+ * Reads and clears the device status word that bounded waits set when they
+ * run out.  Synchronises `stream` first.  Returns ATTN_OK, ATTN_ERR_TIMEOUT or
+ * ATTN_ERR_CUDA.  If `detail` is not NULL it receives the raw word (which wait
+ * gave up, as a bit set).
+ */
+ATTN_API attn_status attn_get_device_status(void* stream, unsigned int* detail);
+
+/*
+ * Self-test of the bounded-wait path: launches one CTA that waits on a
+ * barrier nothing will complete, for at most `timeout_us` microseconds
+ * (1 .. 2000000), then sets the status word and exits normally.  The caller
+ * then sees ATTN_ERR_TIMEOUT from attn_get_device_status().
+ */
+ATTN_API attn_status attn_selftest_bounded_wait(unsigned int timeout_us, void* stream);
+
+/* Which kernel family attn_fwd / attn_bwd use for (dt, hd): 0 = SIMT fp32, 1 = tcgen05. */
+ATTN_API int attn_kernel_family(attn_dtype dt, int hd);
+
+/* Running total of kernels this library has enqueued in this process. */
+ATTN_API unsigned long long attn_launch_count(void);
+
+/* ABI version, bumped on any signature change. */
+ATTN_API int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

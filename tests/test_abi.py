@@ -1,0 +1,103 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments synchronously (before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_attn_fwd_08_gb300 as A
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BAD = ctypes.c_void_p(0x1000)  # never dereferenced: every case fails validation first
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    L = A.lib()
+    names = declared_symbols()
+    assert {"attn_fwd", "attn_bwd", "attn_decode"} <= names
+    for n in sorted(names):
+        assert hasattr(L, n), n
+    assert L.attn_abi_version() == 1
+
+
+def test_status_strings():
+    L = A.lib()
+    for st in range(5):
+        assert L.attn_status_string(st)
+    assert b"invalid" in L.attn_status_string(1)
+
+
+def fwd(**kw):
+    args = dict(dt=2, q=BAD, k=BAD, v=BAD, o=BAD, lse=None, B=1, Tq=4, Tk=4, H=2, Hkv=1, hd=64, scale=0.125,
+                causal=1, window=0, softcap=0.0, q_offset=0, mask=None, mstride=0, stream=None)
+    args.update(kw)
+    return A.lib().attn_fwd(*args.values())
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(H=3, Hkv=2), A.ERR_INVALID_ARG),         # Hkv must divide H
+    (dict(Hkv=0), A.ERR_INVALID_ARG),
+    (dict(hd=96), A.ERR_UNSUPPORTED),
+    (dict(hd=256), A.ERR_UNSUPPORTED),
+    (dict(scale=0.0), A.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), A.ERR_INVALID_ARG),
+    (dict(softcap=-1.0), A.ERR_INVALID_ARG),
+    (dict(softcap=float("inf")), A.ERR_INVALID_ARG),
+    (dict(window=-1), A.ERR_INVALID_ARG),
+    (dict(q_offset=-1), A.ERR_INVALID_ARG),
+    (dict(causal=2), A.ERR_INVALID_ARG),
+    (dict(B=-1), A.ERR_INVALID_ARG),
+    (dict(Tq=-1), A.ERR_INVALID_ARG),
+    (dict(dt=7), A.ERR_INVALID_ARG),
+    (dict(q=ctypes.c_void_p(0x1001)), A.ERR_INVALID_ARG),   # misaligned
+    (dict(o=None), A.ERR_INVALID_ARG),                      # missing output
+    (dict(mstride=-5), A.ERR_INVALID_ARG),
+])
+def test_fwd_rejects_bad_arguments(kw, expect):
+    assert fwd(**kw) == expect
+
+
+def test_empty_batch_or_queries_is_a_noop():
+    assert fwd(B=0) == A.OK
+    assert fwd(Tq=0) == A.OK
+
+
+def test_bwd_and_decode_validation():
+    L = A.lib()
+    # bwd: workspace too small
+    st = L.attn_bwd(2, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, 4, 1, 8, 8, 2, 1, 64, 0.125, 1, 0, 0.0,
+                    0, None, 0, None)
+    assert st == A.ERR_INVALID_ARG
+    # decode: too many query rows per CTA group / too long a block
+    st = L.attn_decode(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 1, 17, 64, 2, 1, 64, 0.125, 1, 0, 0.0, 47,
+                       None, 0, None)
+    assert st == A.ERR_UNSUPPORTED
+    st = L.attn_decode(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 1, 16, 64, 8, 1, 64, 0.125, 1, 0, 0.0, 48,
+                       None, 0, None)
+    assert st == A.ERR_UNSUPPORTED
+    # decode: workspace too small
+    st = L.attn_decode(2, BAD, BAD, BAD, BAD, None, BAD, 16, 2, 4, 4096, 8, 2, 128, 0.1, 1, 0, 0.0, 4092,
+                       None, 0, None)
+    assert st == A.ERR_INVALID_ARG
+
+
+def test_workspace_sizes():
+    assert A.attn_bwd_workspace_size(4, 2048, 32) == 4 * 2048 * 32 * 4
+    n = A.attn_decode_workspace_size(16, 4, 32768, 32, 8, 128)
+    assert n > 0 and n % (16 * 32 * 4 * 130 * 4) == 0
+    assert A.attn_decode_workspace_size(1, 1, 100, 3, 2, 128) == 0  # Hkv does not divide H
+
+
+def test_kernel_family_is_reported():
+    assert A.attn_kernel_family("float32", 64) == 0
+    assert A.attn_kernel_family("bfloat16", 128) in (0, 1)

@@ -1,0 +1,166 @@
+"""GPU parity against the fp64 oracle at sizes the oracle finishes in seconds,
+spanning several 128-row tiles with ragged tails, every masking feature and
+the degenerate cases.  Every call goes through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import attention_attn_fwd_08_gb300 as A
+from helpers import f64, inputs, run_fwd_case
+
+pytestmark = pytest.mark.gpu
+
+FWD_FLAGS = [
+    dict(causal=False),
+    dict(causal=True),
+    dict(causal=True, window=100),
+    dict(causal=True, window=37, softcap=50.0),
+    dict(causal=False, softcap=5.0, mask="batch"),
+    dict(causal=False, window=64, mask="shared"),
+    dict(causal=True, mask="holes"),          # early rows fully masked
+    dict(causal=True, q_offset=77, window=150),
+]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("flags", FWD_FLAGS, ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_fwd_16bit(dt, hd, flags):
+    Tq = 300
+    Tk = Tq + flags.get("q_offset", 0)
+    run_fwd_case(dt, 2, Tq, Tk, 4, 2, hd, seed=100 + hd, **flags)
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("flags", FWD_FLAGS[:4] + FWD_FLAGS[6:], ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_fwd_fp32(hd, flags):
+    Tq = 200
+    Tk = Tq + flags.get("q_offset", 0)
+    run_fwd_case("f32", 1, Tq, Tk, 2, 1, hd, seed=200 + hd, **flags)
+
+
+def test_fp32_causal_workload_full():
+    """B=1, H=Hkv=1, T=128, hd=64, scale=1/8, causal, fp32."""
+    run_fwd_case("f32", 1, 128, 128, 1, 1, 64, causal=True, seed=0x5EED0001)
+
+
+BWD_FLAGS = [
+    dict(causal=True),
+    dict(causal=False, mask="batch"),
+    dict(causal=True, window=90, softcap=50.0),
+    dict(causal=True, mask="holes", softcap=3.0),
+    dict(causal=True, q_offset=40, window=130),
+]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("flags", BWD_FLAGS, ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_bwd_16bit(dt, hd, flags):
+    Tq = 260
+    Tk = Tq + flags.get("q_offset", 0)
+    run_fwd_case(dt, 2, Tq, Tk, 4, 2, hd, backward=True, seed=300 + hd, **flags)
+
+
+@pytest.mark.parametrize("flags", BWD_FLAGS[:3], ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_bwd_fp32(flags):
+    Tq = 150
+    Tk = Tq + flags.get("q_offset", 0)
+    run_fwd_case("f32", 1, Tq, Tk, 2, 1, 64, backward=True, seed=400, **flags)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("Lq,H,Hkv", [(1, 8, 2), (4, 8, 2), (16, 4, 4), (4, 32, 8), (3, 12, 1)])
+@pytest.mark.parametrize("hd", [64, 128])
+def test_decode(dt, Lq, H, Hkv, hd):
+    Tk = 1000
+    run_fwd_case(dt, 3, Lq, Tk, H, Hkv, hd, causal=True, q_offset=Tk - Lq, decode=True, seed=500 + Lq)
+
+
+@pytest.mark.parametrize("flags", [dict(window=200), dict(softcap=30.0, mask="holes"), dict(mask="shared"),
+                                   dict(window=5000, softcap=1.0)],
+                         ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_decode_features(flags):
+    Tk, Lq = 3333, 4
+    run_fwd_case("bf16", 2, Lq, Tk, 8, 2, 128, causal=True, q_offset=Tk - Lq, decode=True, seed=600, **flags)
+
+
+def test_decode_short_cache_and_noncausal():
+    run_fwd_case("bf16", 2, 2, 7, 4, 2, 64, causal=True, q_offset=5, decode=True, seed=700)
+    run_fwd_case("f16", 2, 2, 130, 4, 2, 64, causal=False, q_offset=0, decode=True, seed=701)
+
+
+def test_decode_fp32_routes_to_fp32_kernel():
+    run_fwd_case("f32", 1, 4, 300, 4, 2, 64, causal=True, q_offset=296, decode=True, seed=702)
+
+
+# ------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_single_query_single_key(dt):
+    run_fwd_case(dt, 1, 1, 1, 2, 1, 64, causal=True, backward=True, seed=800)
+
+
+def test_ragged_small_and_tq_ne_tk():
+    run_fwd_case("bf16", 3, 7, 5, 2, 2, 128, causal=False, seed=801)
+    run_fwd_case("bf16", 1, 129, 257, 2, 1, 64, causal=True, q_offset=128, backward=True, seed=802)
+    run_fwd_case("f16", 1, 5, 300, 2, 1, 64, causal=False, backward=True, seed=803)
+
+
+def test_window_larger_than_sequence_equals_unbounded():
+    q, k, v, _ = inputs("bf16", 1, 200, 200, 2, 1, 128, 900)
+    a, la = A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), H=2, Hkv=1, causal=True, window=0)
+    b, lb = A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), H=2, Hkv=1, causal=True, window=500)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_softcap_zero_is_off_on_gpu():
+    q, k, v, _ = inputs("bf16", 1, 150, 150, 2, 1, 64, 901)
+    a, la = A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), H=2, Hkv=1, causal=True)
+    b, lb = A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), H=2, Hkv=1, causal=True, softcap=0.0)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_no_keys_gives_zero_output_and_neg_inf_lse():
+    q = torch.randn(2, 5, 2 * 64, device="cuda").bfloat16()
+    k = torch.empty(2, 0, 64, device="cuda", dtype=torch.bfloat16)
+    o, lse = A.attn_fwd(q, k, k, H=2, Hkv=1)
+    torch.cuda.synchronize()
+    assert (o == 0).all() and torch.isneginf(lse).all()
+    o, lse = A.attn_decode(q[:, :1].contiguous(), k, k, H=2, Hkv=1, q_offset=0)
+    torch.cuda.synchronize()
+    assert (o == 0).all() and torch.isneginf(lse).all()
+
+
+def test_empty_batch_is_noop():
+    q = torch.empty(0, 4, 128, device="cuda", dtype=torch.bfloat16)
+    o = torch.full_like(q, 3.0)
+    A.attn_fwd(q, q, q, H=1, Hkv=1, o=o)
+    torch.cuda.synchronize()
+
+
+def test_outputs_are_overwritten_not_accumulated():
+    q, k, v, do = inputs("bf16", 1, 140, 140, 2, 1, 64, 902, backward=True)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = A.attn_fwd(qd, kd, vd, H=2, Hkv=1, causal=True)
+    g1 = A.attn_bwd(qd, kd, vd, o, dod, lse, H=2, Hkv=1, causal=True)
+    g1 = [t.clone() for t in g1]
+    dq, dk, dv = (torch.full_like(t, 7.0) for t in g1)
+    g2 = A.attn_bwd(qd, kd, vd, o, dod, lse, H=2, Hkv=1, causal=True, dq=dq, dk=dk, dv=dv)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_guard_bands_untouched():
+    """Outputs written inside larger buffers leave the surrounding canary bytes alone."""
+    B, T, H, hd = 1, 130, 2, 64
+    q, k, v, do = inputs("bf16", B, T, T, H, 1, hd, 903, backward=True)
+    n = B * T * H * hd
+    pad = 4096
+    big = torch.full((n + 2 * pad,), 9.0, device="cuda", dtype=torch.bfloat16)
+    o = big[pad:pad + n].view(B, T, H * hd)
+    A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), H=H, Hkv=1, causal=True, o=o)
+    torch.cuda.synchronize()
+    assert (big[:pad] == 9.0).all() and (big[pad + n:] == 9.0).all()
