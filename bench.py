@@ -376,7 +376,7 @@ def main():
         import oracle
 
         oracle.build()
-        groups, rows = oracle_groups(w, 16), 512
+        groups, rows = oracle_groups(w, w.B * w.Hkv), w.Tq
         dt, fl = oracle_sample(w, inp, groups, rows)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": "fwd+bwd of the last %d query rows of %d (batch, KV head) groups, %.1f s" % (
