@@ -21,6 +21,8 @@
 // would waste 3/4 of every MMA and the path is bound by HBM, not the MMA rate.
 #include <math.h>
 
+#include <mutex>
+
 #include "kernels.h"
 
 namespace attn {
@@ -335,6 +337,34 @@ cudaError_t decode_typed(const Params& p, const DecMaps& maps, cudaStream_t s) {
 }
 
 }  // namespace
+
+// ----------------------------------------------- scratch for the no-alloc call
+// attn_decode_noalloc keeps its split partials here instead of in a caller
+// workspace, for callers that cannot allocate device memory.  Every GPU that
+// loads the library holds these 32 MiB until the process exits.  Host code
+// must not pass the symbol itself to a kernel: on the host it names a
+// stand-in, not device memory, so the device address is looked up below.
+static __device__ __align__(256) float g_decode_scratch[kDecodeScratchBytes / sizeof(float)];
+
+cudaError_t decode_noalloc_scratch(float** out) {
+    constexpr int kMaxDevices = 64;
+    static float* addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        // first use on this device, with it current: resolve the array's device address
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<float*>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
 
 cudaError_t launch_decode(const Params& p, int dt, const DecMaps& maps, cudaStream_t s) {
     const bool bf16 = dt == 2;

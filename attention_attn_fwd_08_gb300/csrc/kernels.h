@@ -30,6 +30,11 @@ struct DecMaps {
 };
 cudaError_t launch_decode(const Params& p, int dt, const DecMaps& maps, cudaStream_t s);
 
+// Fixed scratch for attn_decode_noalloc (split partials), defined in decode.cu.
+constexpr size_t kDecodeScratchBytes = size_t(32) << 20;
+// Device address of that scratch on the current device (looked up once per device).
+cudaError_t decode_noalloc_scratch(float** out);
+
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned int timeout_us, cudaStream_t s);
 
 }  // namespace attn

@@ -159,6 +159,31 @@ ATTN_API attn_status attn_decode(attn_dtype dt, const void* q, const void* k, co
                         float softcap, int q_offset, const float* key_mask,
                         long long key_mask_bstride, void* stream);
 
+/*
+ * attn_decode without a workspace argument, for callers that cannot call
+ * cudaMalloc and have no scratch buffer to pass in: for example a plugin that
+ * is handed only its input and output buffers, a serving loop that forbids
+ * device allocation after start-up so that a request can never fail for lack
+ * of memory, or a C caller with no device allocator of its own.  The pages
+ * have no counterpart to this call; it exists for those callers.
+ *
+ * Same arguments, kernels and results as attn_decode.  The split partials
+ * live in one fixed array of 32 MiB that the library reserves in device
+ * memory on every GPU that loads it, held until the process exits; shapes
+ * whose attn_decode_workspace_size() exceeds 32 MiB return
+ * ATTN_ERR_UNSUPPORTED and launch nothing.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ * The first call on a device looks up the array's device address (a one-time
+ * set-up step), so make that first call before any stream capture.  All calls
+ * share the one array and it keeps the last call's contents (no entry needs to
+ * start at zero: each call writes every partial it later reads); calls that
+ * overlap on the GPU, for example on two streams, race on it.
+ */
+ATTN_API attn_status attn_decode_noalloc(attn_dtype dt, const void* q, const void* k, const void* v,
+                        void* o, float* lse, int B, int Lq, int Tk, int H, int Hkv, int hd,
+                        float scale, int causal, int window, float softcap, int q_offset,
+                        const float* key_mask, long long key_mask_bstride, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 ATTN_API const char* attn_status_string(attn_status s);
 
