@@ -19,7 +19,10 @@
 using namespace attn;
 
 #ifndef ATTN_USE_TCGEN05
-#define ATTN_USE_TCGEN05 0
+#define ATTN_USE_TCGEN05 1
+#endif
+#ifndef ATTN_USE_TCGEN05_BWD
+#define ATTN_USE_TCGEN05_BWD 1
 #endif
 
 namespace {
@@ -122,6 +125,10 @@ Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, i
 bool use_tcgen05(attn_dtype dt, int hd) {
     (void)hd;
     return dt != ATTN_F32 && ATTN_USE_TCGEN05;
+}
+bool use_tcgen05_bwd(attn_dtype dt, int hd) {
+    (void)hd;
+    return dt != ATTN_F32 && ATTN_USE_TCGEN05_BWD;
 }
 
 // Decode split plan: a deterministic function of the shape.  Aim for about
@@ -250,12 +257,16 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
     p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse_in = lse;
     p.dq = dq; p.dk = dk; p.dv = dv; p.delta = static_cast<float*>(workspace);
     const int nk = ((phases & 1) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
-    if (!use_tcgen05(dt, hd)) return counted(launch_simt_bwd(p, (int)dt, phases, s), nk);
+    if (!use_tcgen05_bwd(dt, hd)) return counted(launch_simt_bwd(p, (int)dt, phases, s), nk);
     BwdMaps maps;
     if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
         !make_map(&maps.dout, dt, dout, (long long)H * hd, Tq, B, 128) ||
         !make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 128) ||
-        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128))
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128) ||
+        !make_map(&maps.q64, dt, q, (long long)H * hd, Tq, B, 64) ||
+        !make_map(&maps.dout64, dt, dout, (long long)H * hd, Tq, B, 64) ||
+        !make_map(&maps.k64, dt, k, (long long)Hkv * hd, Tk, B, 64) ||
+        !make_map(&maps.v64, dt, v, (long long)Hkv * hd, Tk, B, 64))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_bwd(p, (int)dt, maps, phases, s), nk);
 }

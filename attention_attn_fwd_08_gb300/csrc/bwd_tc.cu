@@ -1,5 +1,618 @@
-// bwd_tc.cu -- placeholder until the tcgen05 backward lands.
+// bwd_tc.cu -- FlashAttention-2-style backward on the tcgen05 tensor cores.
+//
+// Deterministic and free of atomics: one kernel owns dK/dV of a 128-key block
+// (summing over the GQA group's query heads in TMEM), a second owns dQ of a
+// 128-row query block.  Both recompute P = exp(st - LSE) from the saved LSE.
+// Sources: vision_rs flash_attn2.rs, "Backward - dQ" and "Backward - dK / dV"
+// (p = exp(s*scale - L), dS = p (dO.V - D), dQ += dS K scale, dK += dS Q scale,
+// dV += p dO); forge attention.metal, attention_bwd_dq_f32 / attention_bwd_dkv_f32
+// (softcap derivative 1 - tanh^2 of the uncapped score, dK/dV summed over
+// the query heads sharing a KV head, no atomics); ferrotensor
+// engine/attention.rs, flash_attention_v2_backward_with (a dQ pass over query
+// tiles and a dK/dV pass over key tiles, 128 rows each).
+//
+// dK/dV kernel: CTA = 128 keys of one (b, kv head), 6 warps.
+//   warp 4  TMA: K and V once, then 64-row Q and dO tiles of every query head
+//           of the group into a ring.
+//   warp 5  MMA (one thread): S^T = K Q^T and dP^T = V dO^T into a double
+//           buffer; after the compute warps turn them into P^T and dS^T
+//           (16-bit, written over the first half of each buffer):
+//           dV += P^T dO and dK += dS^T Q, A operand from TMEM.
+//   warps 0-3  one thread per key row: P^T = exp2(st*log2e - LSE*log2e) on
+//           visible pairs, dS^T = P^T (dP^T - D) (* (1 - tanh^2)).
+//   TMEM: S^T 0/64, dP^T 128/192, dV 256, dK 256+hd.
+// dQ kernel: CTA = 128 query rows of one (b, h): S = Q K^T and dP = dO V^T
+//   over 64-key tiles (double buffer), dS written over S, dQ += dS K.
+//   TMEM: S 0/64, dP 128/192, dQ 256.
+#include <math.h>
+
 #include "kernels.h"
+
 namespace attn {
-cudaError_t launch_tc_bwd(const Params&, int, const BwdMaps&, int, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned int* status, unsigned int code,
+                                          volatile int* abort_flag) {
+    const bool r = mbar_wait(bar, parity, status, code, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+// =============================================================== dK / dV
+template <int HD>
+struct KVCfg {
+    static constexpr int BKV = 128;  // keys per CTA
+    static constexpr int BQ = 64;    // query rows per inner tile
+    static constexpr int kBoxes = HD / 64;
+    static constexpr int kStages = HD == 128 ? 3 : 4;
+    static constexpr int kKVBytes = BKV * HD * 2;
+    static constexpr int kQBytes = BQ * HD * 2;  // one Q (or dO) tile
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKVBytes;
+    static constexpr int kQOff = 2 * kKVBytes;
+    static constexpr int kGOff = kQOff + kStages * kQBytes;   // dO ring
+    static constexpr int kStatOff = kGOff + kStages * kQBytes;  // [4 warps][2][BQ] floats: lse2, D
+    static constexpr int kBarOff = kStatOff + 4 * 2 * BQ * 4;
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
+    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+template <bool BF16, int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG) {
+    using C = KVCfg<HD>;
+    constexpr int NS = C::kStages, BQ = C::BQ, BKV = C::BKV;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    float* stat = reinterpret_cast<float*>(smem + C::kStatOff);
+    __shared__ int abort_flag;
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int KV_FULL = 0;
+    auto Q_FULL = [&](int s) { return 1 + s; };
+    auto Q_EMPTY = [&](int s) { return 1 + NS + s; };
+    auto ST_FULL = [&](int b) { return 1 + 2 * NS + b; };
+    auto PT_FULL = [&](int b) { return 3 + 2 * NS + b; };
+    const int ACC_DONE = 5 + 2 * NS;
+    const int MMA_DONE = 6 + 2 * NS;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kvh = blockIdx.y, b = blockIdx.z;
+    const int j0 = blockIdx.x * BKV;
+    int qlo, qhi;
+    query_range(P.causal, P.window, P.Tq, P.q_offset, j0, min(j0 + BKV, P.Tk), &qlo, &qhi);
+    const int qt0 = qlo / BQ;
+    const int nqt = qhi > qlo ? (qhi + BQ - 1) / BQ - qt0 : 0;
+    const int ntiles = nqt * P.G;  // (head, query tile) pairs, head-major
+    auto tile_head = [&](int n) { return kvh * P.G + n / max(nqt, 1); };
+    auto tile_i0 = [&](int n) { return (qt0 + n % max(nqt, 1)) * BQ; };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) mbar_init(BAR(i), (i == PT_FULL(0) || i == PT_FULL(1)) ? 4 : 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t tDV = tbase + 256, tDK = tbase + 256 + HD;
+
+    if (warp == 4) {
+        if (lane == 0 && ntiles > 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmG);
+            mbar_expect_tx(BAR(KV_FULL), 2 * C::kKVBytes);
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+                tma_load_3d(sbase + C::kKOff + bx * (BKV * 128), &tmK, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
+                tma_load_3d(sbase + C::kVOff + bx * (BKV * 128), &tmV, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
+            }
+            int issued = 0;
+            for (int n = 0; n < ntiles; ++n) {
+                const int s = n % NS, use = n / NS;
+                if (use > 0 && !mbar_wait(BAR(Q_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
+                    break;
+                const int h = tile_head(n), i0 = tile_i0(n);
+                mbar_expect_tx(BAR(Q_FULL(s)), 2 * C::kQBytes);
+#pragma unroll
+                for (int bx = 0; bx < C::kBoxes; ++bx) {
+                    tma_load_3d(sbase + C::kQOff + s * C::kQBytes + bx * (BQ * 128), &tmQ, BAR(Q_FULL(s)),
+                                h * HD + bx * 64, i0, b);
+                    tma_load_3d(sbase + C::kGOff + s * C::kQBytes + bx * (BQ * 128), &tmG, BAR(Q_FULL(s)),
+                                h * HD + bx * 64, i0, b);
+                }
+                issued = n + 1;
+            }
+            mbar_wait(BAR(KV_FULL), 0, P.status, ST_TEARDOWN, nullptr);
+            for (int n = max(0, issued - NS); n < issued; ++n)
+                mbar_wait(BAR(Q_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
+        }
+    } else if (warp == 5) {
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idS = idesc_f16(BF16, BKV, BQ, false, false);
+            constexpr uint32_t idAcc = idesc_f16(BF16, BKV, HD, false, true);
+            bool ok = mbar_wait(BAR(KV_FULL), 0, P.status, ST_BWD_MMA, &abort_flag);
+            // S^T and dP^T of tile n into buffer n & 1
+            auto issue_sd = [&](int n) -> bool {
+                const int s = n % NS, bf = n & 1;
+                if (!mbar_wait(BAR(Q_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t qa = sbase + C::kQOff + s * C::kQBytes, ga = sbase + C::kGOff + s * C::kQBytes;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
+                    const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+                    mma_ss(tbase + bf * 64, sdesc_sw128(sbase + C::kKOff + aoff, 16, 1024),
+                           sdesc_sw128(qa + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
+                    const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+                    mma_ss(tbase + 128 + bf * 64, sdesc_sw128(sbase + C::kVOff + aoff, 16, 1024),
+                           sdesc_sw128(ga + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(BAR(ST_FULL(bf)));
+                return true;
+            };
+            if (ok) ok = issue_sd(0);
+            if (ok && ntiles > 1) ok = issue_sd(1);
+            for (int n = 0; ok && n < ntiles; ++n) {
+                const int s = n % NS, bf = n & 1;
+                if (!mbar_wait(BAR(PT_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t qa = sbase + C::kQOff + s * C::kQBytes, ga = sbase + C::kGOff + s * C::kQBytes;
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk) {
+                    mma_ts(tDV, tbase + bf * 64 + kk * 8, sdesc_sw128(ga + kk * 2048, BQ * 128, 1024), idAcc,
+                           (n > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk) {
+                    mma_ts(tDK, tbase + 128 + bf * 64 + kk * 8, sdesc_sw128(qa + kk * 2048, BQ * 128, 1024), idAcc,
+                           (n > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(BAR(Q_EMPTY(s)));
+                if (n + 2 < ntiles) ok = issue_sd(n + 2);
+            }
+            if (ok) mma_commit(BAR(ACC_DONE));
+            mma_commit(BAR(MMA_DONE));
+            mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
+        }
+    } else {
+        // ------------------------------------------------ compute: one key row per thread
+        const int r = warp * 32 + lane;
+        const int j = j0 + r;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const bool key_live = j < P.Tk && (!P.key_mask || P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f);
+        const bool cap = P.softcap > 0.f;
+        const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
+        bool ok = true;
+        for (int n = 0; n < ntiles; ++n) {
+            const int bf = n & 1;
+            const int h = tile_head(n), i0 = tile_i0(n);
+            // LSE (log2 units) and D of this query tile, staged per warp in shared memory
+            float* st_l = stat + warp * 2 * BQ;
+            float* st_d = st_l + BQ;
+            __syncwarp();  // the warp finished reading the previous tile's values
+#pragma unroll
+            for (int e = 0; e < BQ / 32; ++e) {
+                const int c = lane + 32 * e, i = i0 + c;
+                float lv = -INFINITY, dv = 0.f;
+                if (i < P.Tq) {
+                    lv = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
+                    dv = P.delta[((long long)b * P.H + h) * P.Tq + i];
+                }
+                st_l[c] = lv == -INFINITY ? INFINITY : lv * kLog2e;
+                st_d[c] = dv;
+            }
+            __syncwarp();
+            // visible query columns of this key row in the tile
+            int clo = 0, chi = min(BQ, P.Tq - i0);
+            if (P.causal) clo = max(clo, j - P.q_offset - i0);
+            if (P.window > 0) {
+                chi = min(chi, j + P.window - P.q_offset - i0);
+                if (!P.causal) clo = max(clo, j - P.window + 1 - P.q_offset - i0);
+            }
+            if (!key_live) chi = 0;
+            if (!warp_wait(BAR(ST_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[2][32], dp[2][32];
+            tmem_ld32(tbase + lane_off + bf * 64, sv[0]);
+            tmem_ld32(tbase + lane_off + bf * 64 + 32, sv[1]);
+            tmem_ld32(tbase + lane_off + 128 + bf * 64, dp[0]);
+            tmem_ld32(tbase + lane_off + 128 + bf * 64 + 32, dp[1]);
+            tmem_ld_wait_only();
+            tmem_pin(sv[0]);
+            tmem_pin(sv[1]);
+            tmem_pin(dp[0]);
+            tmem_pin(dp[1]);
+            uint32_t pk[32], dk[32];
+#pragma unroll
+            for (int c = 0; c < BQ; c += 2) {
+                float pv[2], dv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int cc = c + e;
+                    const float s = __uint_as_float(sv[cc >> 5][cc & 31]);
+                    float x, dcap = 1.f;
+                    if (cap) {
+                        const float t = tanh_accurate(s * cap_in);
+                        x = P.softcap * t * kLog2e;
+                        dcap = 1.f - t * t;
+                    } else {
+                        x = s * P.scale_log2;
+                    }
+                    const bool vis = cc >= clo && cc < chi;
+                    const float p = vis ? fast_exp2(x - st_l[cc]) : 0.f;
+                    pv[e] = p;
+                    dv[e] = p * (__uint_as_float(dp[cc >> 5][cc & 31]) - st_d[cc]) * dcap;
+                }
+                pk[c >> 1] = pack2<BF16>(pv[0], pv[1]);
+                dk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
+            }
+            tmem_st32(tbase + lane_off + bf * 64, pk);
+            tmem_st32(tbase + lane_off + 128 + bf * 64, dk);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(PT_FULL(bf)));
+        }
+        // epilogue: dV, dK (x scale) for this key row; zero when no query sees it
+        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+        const bool have = ok && ntiles > 0 && warp_wait(BAR(ACC_DONE), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
+        if (have) tc_fence_after();
+        if (ok) {
+            const long long off = ((long long)b * P.Tk + (j < P.Tk ? j : 0)) * (long long)P.Hkv * HD + (long long)kvh * HD;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                T* dst = reinterpret_cast<T*>(part == 0 ? P.dv : P.dk) + off;
+                const uint32_t tcol = part == 0 ? tDV : tDK;
+                const float mul = part == 0 ? 1.f : P.scale;
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t acc[32];
+                    if (have) {
+                        tmem_ld32(tcol + lane_off + c * 32, acc);
+                        tmem_ld_wait(acc);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[e] = 0u;
+                    }
+                    if (j < P.Tk && (have || ntiles == 0)) {
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            packed[e] = pack2<BF16>(__uint_as_float(acc[2 * e]) * mul, __uint_as_float(acc[2 * e + 1]) * mul);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+// ===================================================================== dQ
+template <int HD>
+struct QCfg {
+    static constexpr int BQ = 128;  // query rows per CTA
+    static constexpr int BK = 64;   // keys per inner tile
+    static constexpr int kBoxes = HD / 64;
+    static constexpr int kStages = HD == 128 ? 3 : 4;
+    static constexpr int kQBytes = BQ * HD * 2;
+    static constexpr int kKBytes = BK * HD * 2;  // one K (or V) tile
+    static constexpr int kQOff = 0;
+    static constexpr int kGOff = kQBytes;
+    static constexpr int kKOff = 2 * kQBytes;
+    static constexpr int kVOff = kKOff + kStages * kKBytes;
+    static constexpr int kBarOff = kVOff + kStages * kKBytes;
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
+    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+template <bool BF16, int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG) {
+    using C = QCfg<HD>;
+    constexpr int NS = C::kStages, BQ = C::BQ, BK = C::BK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    __shared__ int abort_flag;
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int QG_FULL = 0;
+    auto KV_FULL = [&](int s) { return 1 + s; };
+    auto KV_EMPTY = [&](int s) { return 1 + NS + s; };
+    auto ST_FULL = [&](int b) { return 1 + 2 * NS + b; };
+    auto DS_FULL = [&](int b) { return 3 + 2 * NS + b; };
+    const int ACC_DONE = 5 + 2 * NS;
+    const int MMA_DONE = 6 + 2 * NS;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nqb = (P.Tq + BQ - 1) / BQ;
+    const int qb = nqb - 1 - (int)blockIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z, kvh = h / P.G;
+    const int i0 = qb * BQ;
+    int lo, hi;
+    key_range(P.causal, P.window, P.Tk, i0 + P.q_offset, min(i0 + BQ, P.Tq) - 1 + P.q_offset, &lo, &hi);
+    const int kt0 = lo / BK;
+    const int ntiles = hi > lo ? (hi + BK - 1) / BK - kt0 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) mbar_init(BAR(i), (i == DS_FULL(0) || i == DS_FULL(1)) ? 4 : 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t tDQ = tbase + 256;
+
+    if (warp == 4) {
+        if (lane == 0 && ntiles > 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmG);
+            mbar_expect_tx(BAR(QG_FULL), 2 * C::kQBytes);
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx) {
+                tma_load_3d(sbase + C::kQOff + bx * (BQ * 128), &tmQ, BAR(QG_FULL), h * HD + bx * 64, i0, b);
+                tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), h * HD + bx * 64, i0, b);
+            }
+            int issued = 0;
+            for (int n = 0; n < ntiles; ++n) {
+                const int s = n % NS, use = n / NS;
+                if (use > 0 && !mbar_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
+                    break;
+                const int jt = (kt0 + n) * BK;
+                mbar_expect_tx(BAR(KV_FULL(s)), 2 * C::kKBytes);
+#pragma unroll
+                for (int bx = 0; bx < C::kBoxes; ++bx) {
+                    tma_load_3d(sbase + C::kKOff + s * C::kKBytes + bx * (BK * 128), &tmK, BAR(KV_FULL(s)),
+                                kvh * HD + bx * 64, jt, b);
+                    tma_load_3d(sbase + C::kVOff + s * C::kKBytes + bx * (BK * 128), &tmV, BAR(KV_FULL(s)),
+                                kvh * HD + bx * 64, jt, b);
+                }
+                issued = n + 1;
+            }
+            mbar_wait(BAR(QG_FULL), 0, P.status, ST_TEARDOWN, nullptr);
+            for (int n = max(0, issued - NS); n < issued; ++n)
+                mbar_wait(BAR(KV_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
+        }
+    } else if (warp == 5) {
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idS = idesc_f16(BF16, BQ, BK, false, false);
+            constexpr uint32_t idAcc = idesc_f16(BF16, BQ, HD, false, true);
+            bool ok = mbar_wait(BAR(QG_FULL), 0, P.status, ST_BWD_MMA, &abort_flag);
+            auto issue_sd = [&](int n) -> bool {
+                const int s = n % NS, bf = n & 1;
+                if (!mbar_wait(BAR(KV_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t ka = sbase + C::kKOff + s * C::kKBytes, va = sbase + C::kVOff + s * C::kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t aoff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+                    const uint32_t boff = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+                    mma_ss(tbase + bf * 64, sdesc_sw128(sbase + C::kQOff + aoff, 16, 1024),
+                           sdesc_sw128(ka + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t aoff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+                    const uint32_t boff = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
+                    mma_ss(tbase + 128 + bf * 64, sdesc_sw128(sbase + C::kGOff + aoff, 16, 1024),
+                           sdesc_sw128(va + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(BAR(ST_FULL(bf)));
+                return true;
+            };
+            if (ok) ok = issue_sd(0);
+            if (ok && ntiles > 1) ok = issue_sd(1);
+            for (int n = 0; ok && n < ntiles; ++n) {
+                const int s = n % NS, bf = n & 1;
+                if (!mbar_wait(BAR(DS_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ka = sbase + C::kKOff + s * C::kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_ts(tDQ, tbase + bf * 64 + kk * 8, sdesc_sw128(ka + kk * 2048, BK * 128, 1024), idAcc,
+                           (n > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(BAR(KV_EMPTY(s)));
+                if (n + 2 < ntiles) ok = issue_sd(n + 2);
+            }
+            if (ok) mma_commit(BAR(ACC_DONE));
+            mma_commit(BAR(MMA_DONE));
+            mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
+        }
+    } else {
+        // ----------------------------------------- compute: one query row per thread
+        const int r = warp * 32 + lane;
+        const int i = i0 + r;
+        const int p = i + P.q_offset;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const bool row_ok = i < P.Tq;
+        float lse2 = INFINITY, Dd = 0.f;
+        if (row_ok) {
+            const float lv = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
+            lse2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
+            Dd = P.delta[((long long)b * P.H + h) * P.Tq + i];
+        }
+        const bool cap = P.softcap > 0.f;
+        const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
+        bool ok = true;
+        for (int n = 0; n < ntiles; ++n) {
+            const int bf = n & 1;
+            const int jt = (kt0 + n) * BK;
+            uint32_t mbits[2] = {0xffffffffu, 0xffffffffu};
+            if (P.key_mask) {
+                const float* mrow = P.key_mask + (long long)b * P.mask_bstride;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int j = jt + c * 32 + lane;
+                    mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
+                }
+            }
+            int clo = 0, chi = min(BK, P.Tk - jt);
+            if (P.causal) chi = min(chi, p - jt + 1);
+            if (P.window > 0) {
+                clo = max(clo, p - P.window + 1 - jt);
+                if (!P.causal) chi = min(chi, p + P.window - jt);
+            }
+            if (!row_ok) chi = 0;
+            if (!warp_wait(BAR(ST_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sv[2][32], dp[2][32];
+            tmem_ld32(tbase + lane_off + bf * 64, sv[0]);
+            tmem_ld32(tbase + lane_off + bf * 64 + 32, sv[1]);
+            tmem_ld32(tbase + lane_off + 128 + bf * 64, dp[0]);
+            tmem_ld32(tbase + lane_off + 128 + bf * 64 + 32, dp[1]);
+            tmem_ld_wait_only();
+            tmem_pin(sv[0]);
+            tmem_pin(sv[1]);
+            tmem_pin(dp[0]);
+            tmem_pin(dp[1]);
+            uint32_t dsk[32];
+#pragma unroll
+            for (int c = 0; c < BK; c += 2) {
+                float dv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int cc = c + e;
+                    const float s = __uint_as_float(sv[cc >> 5][cc & 31]);
+                    float x, dcap = 1.f;
+                    if (cap) {
+                        const float t = tanh_accurate(s * cap_in);
+                        x = P.softcap * t * kLog2e;
+                        dcap = 1.f - t * t;
+                    } else {
+                        x = s * P.scale_log2;
+                    }
+                    const bool vis = cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u);
+                    const float pr = vis ? fast_exp2(x - lse2) : 0.f;
+                    dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
+                }
+                dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
+            }
+            tmem_st32(tbase + lane_off + bf * 64, dsk);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(DS_FULL(bf)));
+        }
+        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+        const bool have = ok && ntiles > 0 && warp_wait(BAR(ACC_DONE), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
+        if (have) tc_fence_after();
+        if (ok) {
+            T* dst = reinterpret_cast<T*>(P.dq) + ((long long)b * P.Tq + (row_ok ? i : 0)) * (long long)P.H * HD +
+                     (long long)h * HD;
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t acc[32];
+                if (have) {
+                    tmem_ld32(tDQ + lane_off + c * 32, acc);
+                    tmem_ld_wait(acc);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] = 0u;
+                }
+                if (row_ok && (have || ntiles == 0)) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        packed[e] = pack2<BF16>(__uint_as_float(acc[2 * e]) * P.scale,
+                                                __uint_as_float(acc[2 * e + 1]) * P.scale);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+template <bool BF16, int HD>
+cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_t s) {
+    cudaError_t e;
+    if (phases & 1) {
+        e = launch_bwd_preprocess(p, BF16 ? 2 : 1, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (phases & 2) {
+        auto k = bwd_dkdv_kernel<BF16, HD>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
+        if (e != cudaSuccess) return e;
+        k<<<dim3((p.Tk + 127) / 128, p.Hkv, p.B), kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (phases & 4) {
+        auto k = bwd_dq_kernel<BF16, HD>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
+        if (e != cudaSuccess) return e;
+        k<<<dim3((p.Tq + 127) / 128, p.H, p.B), kThreads, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bwd(const Params& p, int dt, const BwdMaps& maps, int phases, cudaStream_t s) {
+    const bool bf16 = dt == 2;
+    if (p.hd == 64) return bf16 ? bwd_typed<true, 64>(p, maps, phases, s) : bwd_typed<false, 64>(p, maps, phases, s);
+    return bf16 ? bwd_typed<true, 128>(p, maps, phases, s) : bwd_typed<false, 128>(p, maps, phases, s);
+}
+
 }  // namespace attn

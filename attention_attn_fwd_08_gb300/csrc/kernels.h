@@ -20,7 +20,8 @@ struct FwdMaps {
 };
 cudaError_t launch_tc_fwd(const Params& p, int dt, const FwdMaps& maps, cudaStream_t s);
 struct BwdMaps {
-    CUtensorMap q, k, v, dout;
+    CUtensorMap q, dout, k, v;          // 128-row boxes
+    CUtensorMap q64, dout64, k64, v64;  // 64-row boxes
 };
 cudaError_t launch_tc_bwd(const Params& p, int dt, const BwdMaps& maps, int phases, cudaStream_t s);
 

@@ -217,6 +217,23 @@ def workload_config(w):
 
 
 # --------------------------------------------------------------------- ours
+def max_over_ranks(ms, world, device):
+    """Slowest rank's step time: every rank's replica counts only once all finish."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_flops, world, ms_step):
+    """Whole-job TFLOP/s: every replica does step_flops in the slowest rank's time."""
+    return step_flops * world / (ms_step * 1e-3) / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -304,14 +321,10 @@ def main():
     if st != A.OK:
         raise RuntimeError("device status word %#x after the timed steps" % word)
 
-    ms_step = statistics.mean(steps_ms)
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(statistics.mean(steps_ms), world, dev)
     pairs = visible_pairs(w)
     step_flops = 3.5 * FWD_FLOPS_PER_PAIR(w.hd) * pairs
-    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(step_flops, world, ms_step)
 
     comps = {}
     for n in ("fwd", "dkdv", "dq"):
