@@ -217,7 +217,8 @@ attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v,
 
 size_t attn_bwd_workspace_size(int B, int Tq, int H) {
     if (B < 0 || Tq < 0 || H < 0) return 0;
-    return (size_t)B * Tq * H * sizeof(float);
+    const size_t tq_pad = ((size_t)Tq + 63) / 64 * 64;
+    return 2 * (size_t)B * H * tq_pad * sizeof(float);  // D and LSE*log2(e), rows padded to 64
 }
 
 attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
@@ -255,7 +256,10 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
                            key_mask_bstride);
     if (!p.status) return ATTN_ERR_CUDA;
     p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse_in = lse;
-    p.dq = dq; p.dk = dk; p.dv = dv; p.delta = static_cast<float*>(workspace);
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.tq_pad = (Tq + 63) / 64 * 64;
+    p.delta = static_cast<float*>(workspace);
+    p.lse2 = p.delta + (size_t)B * H * p.tq_pad;
     const int nk = ((phases & 1) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
     if (!use_tcgen05_bwd(dt, hd)) return counted(launch_simt_bwd(p, (int)dt, phases, s), nk);
     BwdMaps maps;

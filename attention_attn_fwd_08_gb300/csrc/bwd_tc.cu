@@ -26,6 +26,8 @@
 //   TMEM: S 0/64, dP 128/192, dQ 256.
 #include <math.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 
 namespace attn {
@@ -53,8 +55,9 @@ struct KVCfg {
     static constexpr int kVOff = kKVBytes;
     static constexpr int kQOff = 2 * kKVBytes;
     static constexpr int kGOff = kQOff + kStages * kQBytes;   // dO ring
-    static constexpr int kStatOff = kGOff + kStages * kQBytes;  // [4 warps][2][BQ] floats: lse2, D
-    static constexpr int kBarOff = kStatOff + 4 * 2 * BQ * 4;
+    static constexpr int kStatOff = kGOff + kStages * kQBytes;  // [stage][2][BQ] floats: lse2, D
+    static constexpr int kStatBytes = 2 * BQ * 4;
+    static constexpr int kBarOff = kStatOff + kStages * kStatBytes;
     static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (use > 0 && !mbar_wait(BAR(Q_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
                     break;
                 const int h = tile_head(n), i0 = tile_i0(n);
-                mbar_expect_tx(BAR(Q_FULL(s)), 2 * C::kQBytes);
+                mbar_expect_tx(BAR(Q_FULL(s)), 2 * C::kQBytes + C::kStatBytes);
 #pragma unroll
                 for (int bx = 0; bx < C::kBoxes; ++bx) {
                     tma_load_3d(sbase + C::kQOff + s * C::kQBytes + bx * (BQ * 128), &tmQ, BAR(Q_FULL(s)),
@@ -135,6 +138,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(sbase + C::kGOff + s * C::kQBytes + bx * (BQ * 128), &tmG, BAR(Q_FULL(s)),
                                 h * HD + bx * 64, i0, b);
                 }
+                // LSE*log2(e) and D of these 64 rows (padded rows: +inf and 0)
+                const long long srow = ((long long)b * P.H + h) * P.tq_pad + i0;
+                const uint32_t sdst = sbase + C::kStatOff + s * C::kStatBytes;
+                bulk_load(sdst, P.lse2 + srow, BQ * 4, BAR(Q_FULL(s)));
+                bulk_load(sdst + BQ * 4, P.delta + srow, BQ * 4, BAR(Q_FULL(s)));
                 issued = n + 1;
             }
             mbar_wait(BAR(KV_FULL), 0, P.status, ST_TEARDOWN, nullptr);
@@ -208,22 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = 0; n < ntiles; ++n) {
             const int bf = n & 1;
             const int h = tile_head(n), i0 = tile_i0(n);
-            // LSE (log2 units) and D of this query tile, staged per warp in shared memory
-            float* st_l = stat + warp * 2 * BQ;
-            float* st_d = st_l + BQ;
-            __syncwarp();  // the warp finished reading the previous tile's values
-#pragma unroll
-            for (int e = 0; e < BQ / 32; ++e) {
-                const int c = lane + 32 * e, i = i0 + c;
-                float lv = -INFINITY, dv = 0.f;
-                if (i < P.Tq) {
-                    lv = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
-                    dv = P.delta[((long long)b * P.H + h) * P.Tq + i];
-                }
-                st_l[c] = lv == -INFINITY ? INFINITY : lv * kLog2e;
-                st_d[c] = dv;
-            }
-            __syncwarp();
             // visible query columns of this key row in the tile
             int clo = 0, chi = min(BQ, P.Tq - i0);
             if (P.causal) clo = max(clo, j - P.q_offset - i0);
@@ -232,10 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!P.causal) clo = max(clo, j - P.window + 1 - P.q_offset - i0);
             }
             if (!key_live) chi = 0;
-            if (!warp_wait(BAR(ST_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
+            // the stats arrive with Q/dO of this tile; S^T/dP^T come from the MMA
+            const int s = n % NS;
+            if (!warp_wait(BAR(Q_FULL(s)), (n / NS) & 1, P.status, ST_BWD_COMPUTE, &abort_flag) ||
+                !warp_wait(BAR(ST_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
                 ok = false;
                 break;
             }
+            const float* st_l = stat + s * 2 * BQ;
+            const float* st_d = st_l + BQ;
             tc_fence_after();
             uint32_t sv[2][32], dp[2][32];
             tmem_ld32(tbase + lane_off + bf * 64, sv[0]);
@@ -248,29 +245,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
             uint32_t pk[32], dk[32];
+            // branch-free element loop; the softcap choice is made once per tile
+            auto elems = [&](auto capc) {
+                constexpr bool kCap = decltype(capc)::value;
 #pragma unroll
-            for (int c = 0; c < BQ; c += 2) {
-                float pv[2], dv[2];
+                for (int c = 0; c < BQ; c += 2) {
+                    float pv[2], dv[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int cc = c + e;
-                    const float s = __uint_as_float(sv[cc >> 5][cc & 31]);
-                    float x, dcap = 1.f;
-                    if (cap) {
-                        const float t = tanh_accurate(s * cap_in);
-                        x = P.softcap * t * kLog2e;
-                        dcap = 1.f - t * t;
-                    } else {
-                        x = s * P.scale_log2;
+                    for (int e = 0; e < 2; ++e) {
+                        const int cc = c + e;
+                        const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
+                        float x, dcap = 1.f;
+                        if constexpr (kCap) {
+                            const float t = tanh_accurate(sval * cap_in);
+                            x = P.softcap * t * kLog2e;
+                            dcap = 1.f - t * t;
+                        } else {
+                            x = sval * P.scale_log2;
+                        }
+                        const bool vis = cc >= clo && cc < chi;
+                        const float p = fast_exp2(vis ? x - st_l[cc] : -INFINITY);
+                        pv[e] = p;
+                        dv[e] = p * (__uint_as_float(dp[cc >> 5][cc & 31]) - st_d[cc]) * dcap;
                     }
-                    const bool vis = cc >= clo && cc < chi;
-                    const float p = vis ? fast_exp2(x - st_l[cc]) : 0.f;
-                    pv[e] = p;
-                    dv[e] = p * (__uint_as_float(dp[cc >> 5][cc & 31]) - st_d[cc]) * dcap;
+                    pk[c >> 1] = pack2<BF16>(pv[0], pv[1]);
+                    dk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
                 }
-                pk[c >> 1] = pack2<BF16>(pv[0], pv[1]);
-                dk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
-            }
+            };
+            if (cap)
+                elems(std::integral_constant<bool, true>());
+            else
+                elems(std::integral_constant<bool, false>());
             tmem_st32(tbase + lane_off + bf * 64, pk);
             tmem_st32(tbase + lane_off + 128 + bf * 64, dk);
             tmem_st_wait();
@@ -476,9 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = i < P.Tq;
         float lse2 = INFINITY, Dd = 0.f;
         if (row_ok) {
-            const float lv = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
-            lse2 = lv == -INFINITY ? INFINITY : lv * kLog2e;
-            Dd = P.delta[((long long)b * P.H + h) * P.Tq + i];
+            lse2 = P.lse2[((long long)b * P.H + h) * P.tq_pad + i];
+            Dd = P.delta[((long long)b * P.H + h) * P.tq_pad + i];
         }
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
@@ -518,27 +522,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
             uint32_t dsk[32];
+            auto elems = [&](auto capc) {
+                constexpr bool kCap = decltype(capc)::value;
 #pragma unroll
-            for (int c = 0; c < BK; c += 2) {
-                float dv[2];
+                for (int c = 0; c < BK; c += 2) {
+                    float dv[2];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int cc = c + e;
-                    const float s = __uint_as_float(sv[cc >> 5][cc & 31]);
-                    float x, dcap = 1.f;
-                    if (cap) {
-                        const float t = tanh_accurate(s * cap_in);
-                        x = P.softcap * t * kLog2e;
-                        dcap = 1.f - t * t;
-                    } else {
-                        x = s * P.scale_log2;
+                    for (int e = 0; e < 2; ++e) {
+                        const int cc = c + e;
+                        const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
+                        float x, dcap = 1.f;
+                        if constexpr (kCap) {
+                            const float t = tanh_accurate(sval * cap_in);
+                            x = P.softcap * t * kLog2e;
+                            dcap = 1.f - t * t;
+                        } else {
+                            x = sval * P.scale_log2;
+                        }
+                        const bool vis = cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u);
+                        const float pr = fast_exp2(vis ? x - lse2 : -INFINITY);
+                        dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
                     }
-                    const bool vis = cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u);
-                    const float pr = vis ? fast_exp2(x - lse2) : 0.f;
-                    dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
+                    dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
                 }
-                dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
-            }
+            };
+            if (cap)
+                elems(std::integral_constant<bool, true>());
+            else
+                elems(std::integral_constant<bool, false>());
             tmem_st32(tbase + lane_off + bf * 64, dsk);
             tmem_st_wait();
             tc_fence_before();

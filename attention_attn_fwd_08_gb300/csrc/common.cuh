@@ -28,7 +28,9 @@ struct Params {
     void* dq;
     void* dk;
     void* dv;
-    float* delta;        // backward: D = rowsum(dO*O)  [B][H][Tq]
+    float* delta;        // backward: D = rowsum(dO*O)       [B*H][tq_pad]
+    float* lse2;         // backward: LSE*log2(e), +inf where LSE = -inf  [B*H][tq_pad]
+    int tq_pad;          // backward: Tq rounded up to 64 (row stride of delta / lse2)
     float* ws;           // decode: split partials
     const float* key_mask;
     long long mask_bstride;
@@ -221,6 +223,12 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
         : "memory");
+}
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;

@@ -31,7 +31,7 @@
 #include "kernels.h"
 
 #ifndef ATTN_FWD_PINGPONG
-#define ATTN_FWD_PINGPONG 0
+#define ATTN_FWD_PINGPONG 1
 #endif
 
 namespace attn {
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const float alpha = lane_resc ? fast_exp2(m_used - mx) : 1.f;
+                const float alpha = fast_exp2(lane_resc ? m_used - mx : 0.f);
                 if (lane_resc) {
                     m_used = mx;
                     l *= alpha;
@@ -596,11 +596,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 tmem_pin(tb);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
+                    // branch-free: invisible columns become -inf through a select
                     const int ca = c2 * 32 + e, cb = ca + 32;
                     const bool va = full || (ca >= clo && ca < chi && ((mbits[c2] >> e) & 1u));
                     const bool vb = full || (cb >= clo && cb < chi && ((mbits[c2 + 1] >> e) & 1u));
-                    if (va) mr[e & 3] = fmaxf(mr[e & 3], __uint_as_float(ta[e]));
-                    if (vb) mr[e & 3] = fmaxf(mr[e & 3], __uint_as_float(tb[e]));
+                    mr[e & 3] = fmaxf(mr[e & 3], va ? __uint_as_float(ta[e]) : -INFINITY);
+                    mr[e & 3] = fmaxf(mr[e & 3], vb ? __uint_as_float(tb[e]) : -INFINITY);
                 }
             }
             const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const bool lane_resc = l > 0.f && mx > m_used + kRescaleThreshold;
             if (__any_sync(0xffffffffu, lane_resc)) {
                 // S_u(k) completed after P_u(k-1) V(k-1): O_u already holds it
-                const float alpha = lane_resc ? fast_exp2(m_used - mx) : 1.f;
+                const float alpha = fast_exp2(lane_resc ? m_used - mx : 0.f);
                 if (lane_resc) {
                     m_used = mx;
                     l *= alpha;
@@ -644,8 +645,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     const int c0 = c * 32 + 2 * e, c1 = c0 + 1;
                     const bool v0 = full || (c0 >= clo && c0 < chi && ((mbits[c] >> (2 * e)) & 1u));
                     const bool v1 = full || (c1 >= clo && c1 < chi && ((mbits[c] >> (2 * e + 1)) & 1u));
-                    const float p0 = v0 ? fast_exp2(x0 - ms) : 0.f;
-                    const float p1 = v1 ? fast_exp2(x1 - ms) : 0.f;
+                    // ex2(-inf) = 0: masking is a select of the argument, never a branch
+                    const float p0 = fast_exp2(v0 ? x0 - ms : -INFINITY);
+                    const float p1 = fast_exp2(v1 ? x1 - ms : -INFINITY);
                     rs4[e & 3] += p0 + p1;
                     pk[e] = pack2<BF16>(p0, p1);
                 }

@@ -137,21 +137,37 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
 }
 
 // ------------------------------------------------------- backward: D = dO.O
+// One warp per (b, i, h) row, i < tq_pad: D = dO.O and LSE*log2(e) into the
+// padded [B*H][tq_pad] workspace rows (padding rows get D = 0, LSE = +inf so
+// they contribute nothing).
 template <typename T>
 __global__ void bwd_preprocess_kernel(Params P) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const long long rows = (long long)P.B * P.Tq * P.H;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long rows = (long long)P.B * P.tq_pad * P.H;
     if (warp >= rows) return;
     // row order (b, i, h) so consecutive warps read consecutive memory
-    const int h = warp % P.H;
+    const int h = (int)(warp % P.H);
     const long long bi = warp / P.H;
-    const int i = (int)(bi % P.Tq), b = (int)(bi / P.Tq);
+    const int i = (int)(bi % P.tq_pad), b = (int)(bi / P.tq_pad);
+    const long long srow = ((long long)b * P.H + h) * P.tq_pad + i;
+    if (i >= P.Tq) {
+        if (lane == 0) {
+            P.delta[srow] = 0.f;
+            P.lse2[srow] = INFINITY;
+        }
+        return;
+    }
     const T* o = qrow<T>(P, P.o_in, b, i, h);
     const T* g = qrow<T>(P, P.dout, b, i, h);
     float acc = 0.f;
     for (int d = lane; d < P.hd; d += 32) acc = fmaf(Elem<T>::to_f(o[d]), Elem<T>::to_f(g[d]), acc);
     acc = warp_sum(acc);
-    if (lane == 0) P.delta[((long long)b * P.H + h) * P.Tq + i] = acc;
+    if (lane == 0) {
+        P.delta[srow] = acc;
+        const float l = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
+        P.lse2[srow] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+    }
 }
 
 // -------------------------------------------------------------- backward: dQ
@@ -178,7 +194,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
     }
     const long long srow = ((long long)b * P.H + h) * P.Tq + i;
     const float lse = row_ok ? P.lse_in[srow] : -INFINITY;
-    const float Dd = row_ok ? P.delta[srow] : 0.f;
+    const float Dd = row_ok ? P.delta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
     const bool live = row_ok && lse != -INFINITY;
     float acc[HD / 32];
 #pragma unroll
@@ -283,7 +299,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
                 const int i = i0 + ii;
                 const long long srow = ((long long)b * P.H + h) * P.Tq + i;
                 Ls[ii] = i < P.Tq ? P.lse_in[srow] : -INFINITY;
-                Ds[ii] = i < P.Tq ? P.delta[srow] : 0.f;
+                Ds[ii] = i < P.Tq ? P.delta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
             }
             __syncthreads();
 #pragma unroll
@@ -350,7 +366,7 @@ cudaError_t fwd_typed(const Params& p, cudaStream_t s) {
 
 template <typename T>
 cudaError_t preprocess_typed(const Params& p, cudaStream_t s) {
-    const long long rows = (long long)p.B * p.Tq * p.H;
+    const long long rows = (long long)p.B * p.tq_pad * p.H;
     const int threads = 256;
     const long long blocks = (rows * 32 + threads - 1) / threads;
     bwd_preprocess_kernel<T><<<(unsigned)blocks, threads, 0, s>>>(p);

@@ -98,7 +98,8 @@ ATTN_API attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const
                      int causal, int window, float softcap, int q_offset, const float* key_mask,
                      long long key_mask_bstride, void* stream);
 
-/* Bytes of scratch attn_bwd needs: D = rowsum(dO * O), one fp32 per (b, h, i). */
+/* Bytes of scratch attn_bwd needs: D = rowsum(dO * O) and LSE*log2(e), one fp32
+ * each per (b, h, i), rows padded to a multiple of 64 queries. */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Tq, int H);
 
 /*

@@ -92,7 +92,8 @@ def test_bwd_and_decode_validation():
 
 
 def test_workspace_sizes():
-    assert A.attn_bwd_workspace_size(4, 2048, 32) == 4 * 2048 * 32 * 4
+    assert A.attn_bwd_workspace_size(4, 2048, 32) == 2 * 4 * 2048 * 32 * 4
+    assert A.attn_bwd_workspace_size(1, 65, 2) == 2 * 1 * 128 * 2 * 4
     n = A.attn_decode_workspace_size(16, 4, 32768, 32, 8, 128)
     assert n > 0 and n % (16 * 32 * 4 * 130 * 4) == 0
     assert A.attn_decode_workspace_size(1, 1, 100, 3, 2, 128) == 0  # Hkv does not divide H
