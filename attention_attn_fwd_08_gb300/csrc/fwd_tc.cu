@@ -364,11 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // P.V and next S while the other warpgroup runs its softmax (ping-pong).
 //   warps 0-3  softmax of tile A (rows i0 .. i0+127)
 //   warps 4-7  softmax of tile B (rows i0+128 .. i0+255)
-//   warp 8     TMA producer     warp 9  TMEM owner + MMA issuer
+//   warp 8     TMA producer     warp 9  TMEM owner + MMA issuer   (10, 11 idle)
+// Registers: launched at 168 per thread (384 threads = 64512); the producer
+// warpgroup gives its share to the softmax warpgroups with setmaxnreg
+// (2*128*224 + 128*56 = 64512, never more than the launch total).
 // TMEM: S_A 0, S_B 128, O_A 256, O_B 256+hd (512 columns).  Each tile has a
 // single S buffer; S_u(n) is issued after P_u(n-1) V(n-1), so a completed
 // S_u(n) also means O_u is stable for a rescale.
-constexpr int kThreads2 = 320;
+constexpr int kThreads2 = 384;
+constexpr int kRegsSoftmax = 224, kRegsProducer = 56;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= kThreads2 * 168, "register split exceeds launch");
 
 template <int HD>
 struct Fwd2Cfg {
@@ -444,8 +449,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-
-    if (warp == 8) {
+    if (warp >= 8) {
+        regs_dec<kRegsProducer>();
+        if (warp == 8) {
         if (lane == 0 && ntiles > 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int n = max(0, issued_v - NS); n < issued_v; ++n)
                 mbar_wait(BAR(V_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
-    } else if (warp == 9) {
+        } else if (warp == 9) {
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
             constexpr uint32_t idPV = idesc_f16(BF16, BM, HD, false, true);
@@ -494,14 +500,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const int ks = n % NS;
                 if (!mbar_wait(BAR(K_FULL(ks)), (n / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t kaddr = sbase + C::kKOff + ks * C::kKVBytes;
-                const uint32_t qaddr = sbase + C::kQOff + u * C::kQBytes;
-#pragma unroll
+                // descriptor + (byte offset >> 4) moves the start address (no carry below 256 KB)
+                const uint64_t qdesc = sdesc_sw128(sbase + C::kQOff + u * C::kQBytes, 16, 1024);
+                const uint64_t kdesc = sdesc_sw128(sbase + C::kKOff + ks * C::kKVBytes, 16, 1024);
+#pragma unroll 1
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off_q = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    const uint32_t off_k = (kk >> 2) * (BN * 128) + (kk & 3) * 32;
-                    mma_ss(tbase + u * 128, sdesc_sw128(qaddr + off_q, 16, 1024), sdesc_sw128(kaddr + off_k, 16, 1024),
-                           idS, kk > 0 ? 1u : 0u);
+                    const uint32_t off_q = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+                    const uint32_t off_k = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
+                    mma_ss(tbase + u * 128, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(BAR(S_FULL(u)));
                 return true;
@@ -512,11 +518,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 if (!mbar_wait(BAR(P_FULL(u)), k & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
                 if (!mbar_wait(BAR(V_FULL(vs)), (n / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t vaddr = sbase + C::kVOff + vs * C::kKVBytes;
-#pragma unroll
+                const uint64_t vdesc = sdesc_sw128(sbase + C::kVOff + vs * C::kKVBytes, BN * 128, 1024);
+#pragma unroll 1
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tbase + 256 + u * HD, tbase + u * 128 + kk * 8,
-                           sdesc_sw128(vaddr + kk * 16 * 128, BN * 128, 1024), idPV, (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tbase + 256 + u * HD, tbase + u * 128 + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
+                           (k > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(BAR(O_DONE(u)));
                 return true;
             };
@@ -535,7 +541,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
             mma_commit(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
+        }  // warps 10 and 11 only fill the producer warpgroup
     } else {
+        regs_inc<kRegsSoftmax>();
         // -------------------------------------- softmax + epilogue of tile u
         const int u = warp >> 2, wq = warp & 3;
         const int r = wq * 32 + lane;
@@ -582,97 +590,137 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 break;
             }
             tc_fence_after();
-            // pass 1: row max of the raw scores over the visible columns.  s*scale and
-            // softcap*tanh(s*scale/softcap) both increase with s, so the transform is
-            // applied once, to the max.
-            float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c2 = 0; c2 < 4; c2 += 2) {
-                uint32_t ta[32], tb[32];
-                tmem_ld32(tS + lane_off + c2 * 32, ta);
-                tmem_ld32(tS + lane_off + (c2 + 1) * 32, tb);
-                tmem_ld_wait_only();
-                tmem_pin(ta);
-                tmem_pin(tb);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    // branch-free: invisible columns become -inf through a select
-                    const int ca = c2 * 32 + e, cb = ca + 32;
-                    const bool va = full || (ca >= clo && ca < chi && ((mbits[c2] >> e) & 1u));
-                    const bool vb = full || (cb >= clo && cb < chi && ((mbits[c2 + 1] >> e) & 1u));
-                    mr[e & 3] = fmaxf(mr[e & 3], va ? __uint_as_float(ta[e]) : -INFINITY);
-                    mr[e & 3] = fmaxf(mr[e & 3], vb ? __uint_as_float(tb[e]) : -INFINITY);
-                }
-            }
-            const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
-            const float mx = mraw == -INFINITY ? -INFINITY
-                                               : (cap ? cap_out * tanh_accurate(mraw * cap_in) : mraw * sl2);
-            if (l == 0.f) m_used = fmaxf(m_used, mx);
-            const bool lane_resc = l > 0.f && mx > m_used + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, lane_resc)) {
-                // S_u(k) completed after P_u(k-1) V(k-1): O_u already holds it
-                const float alpha = fast_exp2(lane_resc ? m_used - mx : 0.f);
-                if (lane_resc) {
-                    m_used = mx;
-                    l *= alpha;
-                }
-#pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t orr[32];
-                    tmem_ld32(tO + lane_off + c * 32, orr);
-                    tmem_ld_wait(orr);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st32(tO + lane_off + c * 32, orr);
-                }
-            }
-            // pass 2: P = exp2(x - m) chunk by chunk, written back over S as 16-bit pairs
-            const float ms = m_used == -INFINITY ? 0.f : m_used;
-            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-            auto p_chunk = [&](auto capc, int c, const uint32_t(&t)[32]) {
-                constexpr bool kCap = decltype(capc)::value;
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float x0 = __uint_as_float(t[2 * e]), x1 = __uint_as_float(t[2 * e + 1]);
-                    if constexpr (kCap) {
-                        x0 = cap_out * tanh_accurate(x0 * cap_in);
-                        x1 = cap_out * tanh_accurate(x1 * cap_in);
-                    } else {
-                        x0 *= sl2;
-                        x1 *= sl2;
-                    }
-                    const int c0 = c * 32 + 2 * e, c1 = c0 + 1;
-                    const bool v0 = full || (c0 >= clo && c0 < chi && ((mbits[c] >> (2 * e)) & 1u));
-                    const bool v1 = full || (c1 >= clo && c1 < chi && ((mbits[c] >> (2 * e + 1)) & 1u));
-                    // ex2(-inf) = 0: masking is a select of the argument, never a branch
-                    const float p0 = fast_exp2(v0 ? x0 - ms : -INFINITY);
-                    const float p1 = fast_exp2(v1 ? x1 - ms : -INFINITY);
-                    rs4[e & 3] += p0 + p1;
-                    pk[e] = pack2<BF16>(p0, p1);
-                }
-                tmem_st16(tS + lane_off + c * 16, pk);
+            // Visibility is evaluated only in tiles that some row does not see whole
+            // (kMask); s*scale and softcap*tanh(s*scale/softcap) both increase with s,
+            // so row maxima are taken over raw scores and transformed once.
+            auto vis_col = [&](int c) -> bool {
+                return c >= clo && c < chi && ((mbits[c >> 5] >> (c & 31)) & 1u);
             };
-            auto p_row = [&](auto capc) {
+            auto to_log2 = [&](auto capc, float raw) -> float {
+                if constexpr (decltype(capc)::value) return cap_out * tanh_accurate(raw * cap_in);
+                else return raw * sl2;
+            };
+            // raw-score row max of the tile (first tile a row sees)
+            auto max_pass = [&](auto capc, auto maskc) -> float {
+                constexpr bool kMask = decltype(maskc)::value;
+                float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c2 = 0; c2 < 4; c2 += 2) {
+                    uint32_t ta[32], tb[32];
+                    tmem_ld32(tS + lane_off + c2 * 32, ta);
+                    tmem_ld32(tS + lane_off + (c2 + 1) * 32, tb);
+                    tmem_ld_wait_only();
+                    tmem_pin(ta);
+                    tmem_pin(tb);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float a = __uint_as_float(ta[e]), bb = __uint_as_float(tb[e]);
+                        if constexpr (kMask) {
+                            a = vis_col(c2 * 32 + e) ? a : -INFINITY;
+                            bb = vis_col(c2 * 32 + 32 + e) ? bb : -INFINITY;
+                        }
+                        mr[e & 3] = fmaxf(mr[e & 3], fmaxf(a, bb));
+                    }
+                }
+                const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+                return mraw == -INFINITY ? -INFINITY : to_log2(capc, mraw);
+            };
+            // P = exp2(x - ms) over the tile as 16-bit pairs in registers (S stays intact in
+            // TMEM until the caller stores P over it); returns the row sum and the
+            // (log2-unit) row max seen along the way
+            uint32_t pk[4][16];
+            auto p_pass = [&](auto capc, auto maskc, float ms, float& rsum, float& mxo) {
+                constexpr bool kCap = decltype(capc)::value;
+                constexpr bool kMask = decltype(maskc)::value;
+                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+                float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                auto chunk = [&](int c, const uint32_t(&t)[32]) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float r0 = __uint_as_float(t[2 * e]), r1 = __uint_as_float(t[2 * e + 1]);
+                        float x0, x1;
+                        if constexpr (kCap) {
+                            x0 = fmaf(cap_out, tanh_accurate(r0 * cap_in), -ms);
+                            x1 = fmaf(cap_out, tanh_accurate(r1 * cap_in), -ms);
+                        } else {
+                            x0 = fmaf(r0, sl2, -ms);
+                            x1 = fmaf(r1, sl2, -ms);
+                        }
+                        if constexpr (kMask) {
+                            // the mask goes on the transformed argument: softcap*tanh(-inf) is finite
+                            const bool v0 = vis_col(c * 32 + 2 * e), v1 = vis_col(c * 32 + 2 * e + 1);
+                            r0 = v0 ? r0 : -INFINITY;
+                            r1 = v1 ? r1 : -INFINITY;
+                            x0 = v0 ? x0 : -INFINITY;
+                            x1 = v1 ? x1 : -INFINITY;
+                        }
+                        mr[e & 3] = fmaxf(mr[e & 3], fmaxf(r0, r1));
+                        const float p0 = fast_exp2(x0);  // masked: ex2(-inf) = 0
+                        const float p1 = fast_exp2(x1);
+                        rs4[e & 3] += p0 + p1;
+                        pk[c][e] = pack2<BF16>(p0, p1);
+                    }
+                };
                 uint32_t ta[32], tb[32];
                 tmem_ld32(tS + lane_off + 0 * 32, ta);
                 tmem_ld_wait(ta);
                 tmem_ld32(tS + lane_off + 1 * 32, tb);
-                p_chunk(capc, 0, ta);
+                chunk(0, ta);
                 tmem_ld_wait(tb);
                 tmem_ld32(tS + lane_off + 2 * 32, ta);
-                p_chunk(capc, 1, tb);
+                chunk(1, tb);
                 tmem_ld_wait(ta);
                 tmem_ld32(tS + lane_off + 3 * 32, tb);
-                p_chunk(capc, 2, ta);
+                chunk(2, ta);
                 tmem_ld_wait(tb);
-                p_chunk(capc, 3, tb);
+                chunk(3, tb);
+                rsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+                const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+                mxo = mraw == -INFINITY ? -INFINITY : to_log2(capc, mraw);
             };
-            if (cap)
-                p_row(std::integral_constant<bool, true>());
-            else
-                p_row(std::integral_constant<bool, false>());
-            l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+            auto run_tile = [&](auto capc, auto maskc) {
+                // rows that have seen no key yet take this tile's max as their reference
+                if (__any_sync(0xffffffffu, l == 0.f)) {
+                    const float mt = max_pass(capc, maskc);
+                    if (l == 0.f) m_used = fmaxf(m_used, mt);
+                }
+                // one pass against the running reference max; if some row's max grew
+                // by more than 2^8 (rare), rescale O, move the reference and redo the tile
+                float rs, mx;
+                p_pass(capc, maskc, m_used == -INFINITY ? 0.f : m_used, rs, mx);
+                const bool resc = l > 0.f && mx > m_used + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // S_u(k) completed after P_u(k-1) V(k-1): O_u already holds it
+                    const float alpha = fast_exp2(resc ? m_used - mx : 0.f);
+                    if (resc) {
+                        m_used = mx;
+                        l *= alpha;
+                    }
+#pragma unroll 1
+                    for (int c = 0; c < HD / 32; ++c) {
+                        uint32_t orr[32];
+                        tmem_ld32(tO + lane_off + c * 32, orr);
+                        tmem_ld_wait(orr);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st32(tO + lane_off + c * 32, orr);
+                    }
+                    // S is still intact in TMEM: recompute this tile's P against the new max
+                    p_pass(capc, maskc, m_used == -INFINITY ? 0.f : m_used, rs, mx);
+                }
+                l += rs;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_st16(tS + lane_off + c * 16, pk[c]);
+            };
+            using TT = std::integral_constant<bool, true>;
+            using FF = std::integral_constant<bool, false>;
+            if (cap) {
+                if (full) run_tile(TT(), FF());
+                else run_tile(TT(), TT());
+            } else {
+                if (full) run_tile(FF(), FF());
+                else run_tile(FF(), TT());
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
