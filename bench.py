@@ -241,6 +241,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["all", "prefill"], default="all",
+                    help="prefill: only the fwd+bwd step (no decode measurement), e.g. for profiler runs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -339,7 +341,7 @@ def main():
 
     # ---------------------------------------------------------------- decode
     del flush_buf
-    for name in ("decode_lq1", "decode_lq4"):
+    for name in (("decode_lq1", "decode_lq4") if args.workload == "all" else ()):
         wd = synth.WORKLOADS[name]
         di = synth.make_inputs(wd)
         qd_, kd_, vd_ = (di[n].to(dev) for n in ("q", "k", "v"))
