@@ -18,12 +18,6 @@
 
 using namespace attn;
 
-#ifndef ATTN_USE_TCGEN05
-#define ATTN_USE_TCGEN05 1
-#endif
-#ifndef ATTN_USE_TCGEN05_BWD
-#define ATTN_USE_TCGEN05_BWD 1
-#endif
 
 namespace {
 
@@ -122,13 +116,11 @@ Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, i
     return p;
 }
 
+// fp16/bf16 run on the tensor cores; fp32 stays on the CUDA-core kernels (no TF32,
+// no 16-bit P), which is what fp32 accuracy needs.
 bool use_tcgen05(attn_dtype dt, int hd) {
     (void)hd;
-    return dt != ATTN_F32 && ATTN_USE_TCGEN05;
-}
-bool use_tcgen05_bwd(attn_dtype dt, int hd) {
-    (void)hd;
-    return dt != ATTN_F32 && ATTN_USE_TCGEN05_BWD;
+    return dt != ATTN_F32;
 }
 
 // Decode split plan: a deterministic function of the shape.  Aim for about
@@ -261,7 +253,7 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
     p.delta = static_cast<float*>(workspace);
     p.lse2 = p.delta + (size_t)B * H * p.tq_pad;
     const int nk = ((phases & 1) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
-    if (!use_tcgen05_bwd(dt, hd)) return counted(launch_simt_bwd(p, (int)dt, phases, s), nk);
+    if (!use_tcgen05(dt, hd)) return counted(launch_simt_bwd(p, (int)dt, phases, s), nk);
     BwdMaps maps;
     if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
         !make_map(&maps.dout, dt, dout, (long long)H * hd, Tq, B, 128) ||

@@ -87,8 +87,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int MMA_DONE = 6 + 2 * NS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kvh = blockIdx.y, b = blockIdx.z;
-    const int j0 = blockIdx.x * BKV;
+    // 1-D grid, longest first: causally the first key blocks are seen by the most queries
+    const int kb = (int)(blockIdx.x % (unsigned)(P.Hkv * P.B));
+    const int kvh = kb % P.Hkv, b = kb / P.Hkv;
+    const int j0 = (int)(blockIdx.x / (unsigned)(P.Hkv * P.B)) * BKV;
     int qlo, qhi;
     query_range(P.causal, P.window, P.Tq, P.q_offset, j0, min(j0 + BKV, P.Tk), &qlo, &qhi);
     const int qt0 = qlo / BQ;
@@ -246,8 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(dp[1]);
             uint32_t pk[32], dk[32];
             // branch-free element loop; the softcap choice is made once per tile
-            auto elems = [&](auto capc) {
+            auto elems = [&](auto capc, auto maskc) {
                 constexpr bool kCap = decltype(capc)::value;
+                constexpr bool kMask = decltype(maskc)::value;
 #pragma unroll
                 for (int c = 0; c < BQ; c += 2) {
                     float pv[2], dv[2];
@@ -258,13 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float x, dcap = 1.f;
                         if constexpr (kCap) {
                             const float t = tanh_accurate(sval * cap_in);
-                            x = P.softcap * t * kLog2e;
+                            x = P.softcap * t * kLog2e - st_l[cc];
                             dcap = 1.f - t * t;
                         } else {
-                            x = sval * P.scale_log2;
+                            x = fmaf(sval, P.scale_log2, -st_l[cc]);
                         }
-                        const bool vis = cc >= clo && cc < chi;
-                        const float p = fast_exp2(vis ? x - st_l[cc] : -INFINITY);
+                        if constexpr (kMask) x = (cc >= clo && cc < chi) ? x : -INFINITY;
+                        const float p = fast_exp2(x);
                         pv[e] = p;
                         dv[e] = p * (__uint_as_float(dp[cc >> 5][cc & 31]) - st_d[cc]) * dcap;
                     }
@@ -272,10 +275,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
                 }
             };
-            if (cap)
-                elems(std::integral_constant<bool, true>());
-            else
-                elems(std::integral_constant<bool, false>());
+            // every (query, key) pair of the tile visible: skip the per-element tests
+            const bool full = key_live && clo <= 0 && chi >= BQ;
+            const bool full_w = __all_sync(0xffffffffu, full);
+            using TT = std::integral_constant<bool, true>;
+            using FF = std::integral_constant<bool, false>;
+            if (cap) {
+                if (full_w) elems(TT(), FF());
+                else elems(TT(), TT());
+            } else {
+                if (full_w) elems(FF(), FF());
+                else elems(FF(), TT());
+            }
             tmem_st32(tbase + lane_off + bf * 64, pk);
             tmem_st32(tbase + lane_off + 128 + bf * 64, dk);
             tmem_st_wait();
@@ -369,8 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nqb = (P.Tq + BQ - 1) / BQ;
-    const int qb = nqb - 1 - (int)blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z, kvh = h / P.G;
+    // 1-D grid, longest first: every head's last (causally heaviest) query block first
+    const int hb = (int)(blockIdx.x % (unsigned)(P.H * P.B));
+    const int qb = nqb - 1 - (int)(blockIdx.x / (unsigned)(P.H * P.B));
+    const int h = hb % P.H, b = hb / P.H, kvh = h / P.G;
     const int i0 = qb * BQ;
     int lo, hi;
     key_range(P.causal, P.window, P.Tk, i0 + P.q_offset, min(i0 + BQ, P.Tq) - 1 + P.q_offset, &lo, &hi);
@@ -522,8 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
             uint32_t dsk[32];
-            auto elems = [&](auto capc) {
+            auto elems = [&](auto capc, auto maskc) {
                 constexpr bool kCap = decltype(capc)::value;
+                constexpr bool kMask = decltype(maskc)::value;
 #pragma unroll
                 for (int c = 0; c < BK; c += 2) {
                     float dv[2];
@@ -534,22 +548,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float x, dcap = 1.f;
                         if constexpr (kCap) {
                             const float t = tanh_accurate(sval * cap_in);
-                            x = P.softcap * t * kLog2e;
+                            x = P.softcap * t * kLog2e - lse2;
                             dcap = 1.f - t * t;
                         } else {
-                            x = sval * P.scale_log2;
+                            x = fmaf(sval, P.scale_log2, -lse2);
                         }
-                        const bool vis = cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u);
-                        const float pr = fast_exp2(vis ? x - lse2 : -INFINITY);
+                        if constexpr (kMask)
+                            x = (cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u)) ? x : -INFINITY;
+                        const float pr = fast_exp2(x);
                         dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
                     }
                     dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
                 }
             };
-            if (cap)
-                elems(std::integral_constant<bool, true>());
-            else
-                elems(std::integral_constant<bool, false>());
+            // every (query, key) pair of the tile visible: skip the per-element tests
+            const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= BK;
+            const bool full_w = __all_sync(0xffffffffu, full);
+            using TT = std::integral_constant<bool, true>;
+            using FF = std::integral_constant<bool, false>;
+            if (cap) {
+                if (full_w) elems(TT(), FF());
+                else elems(TT(), TT());
+            } else {
+                if (full_w) elems(FF(), FF());
+                else elems(FF(), TT());
+            }
             tmem_st32(tbase + lane_off + bf * 64, dsk);
             tmem_st_wait();
             tc_fence_before();
@@ -605,14 +628,16 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         auto k = bwd_dkdv_kernel<BF16, HD>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
-        k<<<dim3((p.Tk + 127) / 128, p.Hkv, p.B), kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64);
+        const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;
+        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 4) {
         auto k = bwd_dq_kernel<BF16, HD>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
-        k<<<dim3((p.Tq + 127) / 128, p.H, p.B), kThreads, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout);
+        const unsigned grid = (unsigned)((p.Tq + 127) / 128) * p.H * p.B;
+        k<<<grid, kThreads, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -10,54 +10,23 @@
 // fully masked key tiles are skipped); ferrotensor engine/attention.rs,
 // flash_attention_v2_with (128 query rows per workgroup, GQA).
 //
-// CTA = one 128-row query tile of one (b, h); 6 warps:
-//   warps 0-3  softmax: one thread per query row (TMEM lane = row); reads S
-//              from TMEM, applies scale / softcap / mask, online softmax in
-//              exp2 units, writes P (16-bit) back over S's columns, rescales
-//              the O accumulator in TMEM when the row max grows by more than
-//              2^8, and runs the epilogue (O / l, LSE).
-//   warp 4     TMA producer: Q once, then 128-key K and V tiles into a
-//              2- or 3-stage ring (128-byte swizzle).
-//   warp 5     TMEM owner and single-thread MMA issuer:
-//              S[n%2] = Q K_n^T  (A, B from shared memory, K-major)
-//              O     += P_{n-1} V_{n-1}  (A = P from TMEM, B = V MN-major)
-// TMEM: S0 at column 0, S1 at 128, O at 256 (hd columns), 512 allocated.
-// Key tiles outside every row's visible range are never loaded; tiles that
-// every row sees entirely skip the per-element mask.
+// One kernel, fwd_tc2_kernel: two 128-row query tiles of one (b, h) per CTA
+// share every K/V tile; two softmax warpgroups alternate with the tensor core
+// (details at the kernel).  Key tiles outside every row's visible range are
+// never loaded; tiles that every row sees entirely skip the per-element mask.
 #include <math.h>
 
 #include <type_traits>
 
 #include "kernels.h"
 
-#ifndef ATTN_FWD_PINGPONG
-#define ATTN_FWD_PINGPONG 1
-#endif
-
 namespace attn {
 namespace {
 
-constexpr int BM = 128;      // query rows per CTA
+constexpr int BM = 128;      // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;      // keys per tile
-constexpr int kThreads = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 256x
-
-template <int HD>
-struct FwdCfg {
-    static constexpr int kBoxes = HD / 64;                  // 64-column TMA boxes per row
-    static constexpr int kStages = HD == 128 ? 2 : 3;
-    static constexpr int kQBytes = BM * HD * 2;
-    static constexpr int kKVBytes = BN * HD * 2;            // one K (or V) tile
-    static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQBytes;
-    static constexpr int kVOff = kKOff + kStages * kKVBytes;
-    static constexpr int kBarOff = kVOff + kStages * kKVBytes;
-    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2;
-    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
-    // at least this much dynamic smem so that one CTA (and its 512 TMEM columns) owns an SM
-    static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
-};
 
 struct TileInfo {
     int t0, ntiles;
@@ -72,290 +41,6 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0) {
     t.t0 = lo / BN;
     t.ntiles = hi > lo ? (hi + BN - 1) / BN - t.t0 : 0;
     return t;
-}
-
-template <bool BF16, int HD>
-__global__ void __launch_bounds__(kThreads, 1)
-    fwd_tc_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV) {
-    using C = FwdCfg<HD>;
-    constexpr int NS = C::kStages;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-    __shared__ int abort_flag;
-
-    // barrier indices
-    const uint32_t bar0 = smem_u32(bars);
-    auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    const int Q_FULL = 0;
-    auto K_FULL = [&](int s) { return 1 + s; };
-    auto K_EMPTY = [&](int s) { return 1 + NS + s; };
-    auto V_FULL = [&](int s) { return 1 + 2 * NS + s; };
-    auto V_EMPTY = [&](int s) { return 1 + 3 * NS + s; };
-    auto S_FULL = [&](int b) { return 1 + 4 * NS + b; };
-    auto P_FULL = [&](int b) { return 3 + 4 * NS + b; };
-    const int O_DONE = 5 + 4 * NS;
-    const int MMA_DONE = 6 + 4 * NS;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nqt = (P.Tq + BM - 1) / BM;
-    const int qt = nqt - 1 - (int)blockIdx.x;  // heaviest causal tiles first
-    const int h = blockIdx.y, b = blockIdx.z, kvh = h / P.G;
-    const int i0 = qt * BM;
-    const TileInfo ti = tile_range(P, i0);
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNumBars; ++i) mbar_init(BAR(i), (i == P_FULL(0) || i == P_FULL(1)) ? 4 : 1);
-        abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 5) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = *tmem_slot;
-
-    if (warp == 4) {
-        // ------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            int issued_k = 0, issued_v = 0;
-            if (ti.ntiles > 0) {
-                mbar_expect_tx(BAR(Q_FULL), C::kQBytes);
-#pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_3d(sbase + C::kQOff + bx * (BM * 128), &tmQ, BAR(Q_FULL), h * HD + bx * 64, i0, b);
-                for (int n = 0; n < ti.ntiles; ++n) {
-                    const int s = n % NS, use = n / NS;
-                    const int j0 = (ti.t0 + n) * BN;
-                    if (use > 0 &&
-                        !mbar_wait(BAR(K_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag))
-                        break;
-                    mbar_expect_tx(BAR(K_FULL(s)), C::kKVBytes);
-#pragma unroll
-                    for (int bx = 0; bx < C::kBoxes; ++bx)
-                        tma_load_3d(sbase + C::kKOff + s * C::kKVBytes + bx * (BN * 128), &tmK, BAR(K_FULL(s)),
-                                    kvh * HD + bx * 64, j0, b);
-                    issued_k = n + 1;
-                    if (use > 0 &&
-                        !mbar_wait(BAR(V_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag))
-                        break;
-                    mbar_expect_tx(BAR(V_FULL(s)), C::kKVBytes);
-#pragma unroll
-                    for (int bx = 0; bx < C::kBoxes; ++bx)
-                        tma_load_3d(sbase + C::kVOff + s * C::kKVBytes + bx * (BN * 128), &tmV, BAR(V_FULL(s)),
-                                    kvh * HD + bx * 64, j0, b);
-                    issued_v = n + 1;
-                }
-                // everything issued must land before the CTA's shared memory is released
-                mbar_wait(BAR(Q_FULL), 0, P.status, ST_TEARDOWN, nullptr);
-                for (int n = max(0, issued_k - NS); n < issued_k; ++n)
-                    mbar_wait(BAR(K_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
-                for (int n = max(0, issued_v - NS); n < issued_v; ++n)
-                    mbar_wait(BAR(V_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
-            }
-        }
-    } else if (warp == 5) {
-        // -------------------------------------------------------- MMA issuer
-        if (lane == 0 && ti.ntiles > 0) {
-            constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
-            constexpr uint32_t idPV = idesc_f16(BF16, BM, HD, false, true);
-            const uint32_t tO = tbase + 256;
-            bool ok = mbar_wait(BAR(Q_FULL), 0, P.status, ST_FWD_MMA, &abort_flag);
-            auto issue_pv = [&](int j) -> bool {
-                const int vs = j % NS, pb = j & 1;
-                if (!mbar_wait(BAR(P_FULL(pb)), (j >> 1) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
-                if (!mbar_wait(BAR(V_FULL(vs)), (j / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t vaddr = sbase + C::kVOff + vs * C::kKVBytes;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(vaddr + kk * 16 * 128, BN * 128, 1024);
-                    mma_ts(tO, tbase + pb * 128 + kk * 8, bdesc, idPV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(BAR(V_EMPTY(vs)));
-                mma_commit(BAR(O_DONE));
-                return true;
-            };
-            for (int n = 0; ok && n < ti.ntiles; ++n) {
-                const int ks = n % NS, sb = n & 1;
-                if (!mbar_wait(BAR(K_FULL(ks)), (n / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t kaddr = sbase + C::kKOff + ks * C::kKVBytes;
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-                    const uint64_t adesc = sdesc_sw128(sbase + C::kQOff + off, 16, 1024);
-                    const uint64_t bdesc = sdesc_sw128(kaddr + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tbase + sb * 128, adesc, bdesc, idS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(BAR(S_FULL(sb)));
-                mma_commit(BAR(K_EMPTY(ks)));
-                if (n > 0 && !issue_pv(n - 1)) ok = false;
-            }
-            if (ok) issue_pv(ti.ntiles - 1);
-            // all issued MMAs complete before TMEM is released
-            mma_commit(BAR(MMA_DONE));
-            mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
-        }
-    } else {
-        // ------------------------------------------------- softmax, epilogue
-        const int r = warp * 32 + lane;  // TMEM lane == row within the tile
-        const int i = i0 + r;
-        const int p = i + P.q_offset;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const float sl2 = P.scale_log2;
-        const bool cap = P.softcap > 0.f;
-        const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);  // s * scale / softcap
-        const float cap_out = P.softcap * kLog2e;
-        const int prow0 = i0 + P.q_offset, prow1 = min(i0 + BM, P.Tq) - 1 + P.q_offset;
-        float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
-        // every lane waits; the outcome is made warp-uniform before anyone acts on it
-        auto wait_warp = [&](int bar, uint32_t parity) -> bool {
-            const bool r = mbar_wait(BAR(bar), parity, P.status, ST_FWD_SOFTMAX, &abort_flag);
-            return __all_sync(0xffffffffu, r);
-        };
-        for (int n = 0; n < ti.ntiles; ++n) {
-            const int sb = n & 1;
-            const int j0 = (ti.t0 + n) * BN;
-            // visible columns of this row in the tile: [clo, chi) and the key-mask bits
-            const bool full = tile_full(P.causal, P.window, P.Tk, prow0, prow1, j0, j0 + BN) && !P.key_mask;
-            uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-            if (P.key_mask) {
-                const float* mrow = P.key_mask + (long long)b * P.mask_bstride;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int j = j0 + c * 32 + lane;
-                    mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
-                }
-            }
-            int clo = 0, chi = BN;
-            if (!full) {
-                chi = min(chi, P.Tk - j0);
-                if (P.causal) chi = min(chi, p - j0 + 1);
-                if (P.window > 0) {
-                    clo = max(clo, p - P.window + 1 - j0);
-                    if (!P.causal) chi = min(chi, p + P.window - j0);
-                }
-            }
-            if (!wait_warp(S_FULL(sb), (n >> 1) & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tbase + lane_off + sb * 128 + c * 32, sr[c]);
-            tmem_ld_wait_only();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_pin(sr[c]);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                float s = __uint_as_float(sr[c >> 5][c & 31]);
-                float v = cap ? cap_out * tanh_accurate(s * cap_in) : s * sl2;
-                if (!full) {
-                    const bool vis = c >= clo && c < chi && ((mbits[c >> 5] >> (c & 31)) & 1u);
-                    v = vis ? v : -INFINITY;
-                }
-                sr[c >> 5][c & 31] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
-            }
-            // online softmax with a lazily rescaled reference max
-            if (l == 0.f) m_used = fmaxf(m_used, mx);
-            const bool lane_resc = l > 0.f && mx > m_used + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, lane_resc)) {
-                // O must hold P_{n-1} V_{n-1} before it is rescaled
-                if (!wait_warp(O_DONE, (n - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const float alpha = fast_exp2(lane_resc ? m_used - mx : 0.f);
-                if (lane_resc) {
-                    m_used = mx;
-                    l *= alpha;
-                }
-#pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t orr[32];
-                    tmem_ld32(tbase + lane_off + 256 + c * 32, orr);
-                    tmem_ld_wait(orr);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st32(tbase + lane_off + 256 + c * 32, orr);
-                }
-                tmem_st_wait();
-            }
-            const float ms = m_used == -INFINITY ? 0.f : m_used;
-            float rs = 0.f;
-            uint32_t pk[2][32];
-#pragma unroll
-            for (int c = 0; c < BN; c += 2) {
-                const float p0 = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - ms);
-                const float p1 = fast_exp2(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]) - ms);
-                rs += p0 + p1;
-                pk[c >> 6][(c >> 1) & 31] = pack2<BF16>(p0, p1);
-            }
-            l += rs;
-            tmem_st32(tbase + lane_off + sb * 128, pk[0]);
-            tmem_st32(tbase + lane_off + sb * 128 + 32, pk[1]);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(P_FULL(sb)));
-        }
-        // epilogue: O / l, LSE in natural-log units
-        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-        const bool row_ok = i < P.Tq;
-        T* orow = reinterpret_cast<T*>(P.o) + ((long long)b * P.Tq + (row_ok ? i : 0)) * (long long)P.H * HD +
-                  (long long)h * HD;
-        const bool have_o = ok && ti.ntiles > 0 && wait_warp(O_DONE, (ti.ntiles - 1) & 1);
-        if (have_o) tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-            uint32_t orr[32];
-            if (have_o) {
-                tmem_ld32(tbase + lane_off + 256 + c * 32, orr);
-                tmem_ld_wait(orr);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) orr[e] = 0u;
-            }
-            if (row_ok && (have_o || ti.ntiles == 0)) {
-                uint32_t packed[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    packed[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
-                uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
-            }
-        }
-        if (row_ok && P.lse && (have_o || ti.ntiles == 0))
-            P.lse[((long long)b * P.H + h) * P.Tq + i] =
-                l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 5) {
-        tc_fence_after();
-        tmem_dealloc(tbase, 512);
-    }
 }
 
 // ------------------------------------------------------------------------
@@ -415,9 +100,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int MMA_DONE = 7 + 4 * NS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 1-D grid, longest first: every head's last (causally heaviest) query block
+    // comes before any head's next one
     const int ncta = (P.Tq + 2 * BM - 1) / (2 * BM);
-    const int cq = ncta - 1 - (int)blockIdx.x;  // heaviest causal blocks first
-    const int h = blockIdx.y, b = blockIdx.z, kvh = h / P.G;
+    const int hb = (int)(blockIdx.x % (unsigned)(P.H * P.B));
+    const int cq = ncta - 1 - (int)(blockIdx.x / (unsigned)(P.H * P.B));
+    const int h = hb % P.H, b = hb / P.H, kvh = h / P.G;
     const int i0 = cq * 2 * BM;
     const bool hasB = i0 + BM < P.Tq;
     TileInfo tu[2];
@@ -772,19 +460,8 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     auto kern = fwd_tc2_kernel<BF16, HD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.Tq + 2 * BM - 1) / (2 * BM), p.H, p.B);
+    const unsigned grid = (unsigned)((p.Tq + 2 * BM - 1) / (2 * BM)) * p.H * p.B;
     kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v);
-    return cudaGetLastError();
-}
-
-template <bool BF16, int HD>
-cudaError_t fwd_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
-    using C = FwdCfg<HD>;
-    auto kern = fwd_tc_kernel<BF16, HD>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
-    if (e != cudaSuccess) return e;
-    dim3 grid((p.Tq + BM - 1) / BM, p.H, p.B);
-    kern<<<grid, kThreads, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v);
     return cudaGetLastError();
 }
 
@@ -792,12 +469,8 @@ cudaError_t fwd_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
 
 cudaError_t launch_tc_fwd(const Params& p, int dt, const FwdMaps& maps, cudaStream_t s) {
     const bool bf16 = dt == 2;
-#if ATTN_FWD_PINGPONG
     if (p.hd == 64) return bf16 ? fwd2_typed<true, 64>(p, maps, s) : fwd2_typed<false, 64>(p, maps, s);
     return bf16 ? fwd2_typed<true, 128>(p, maps, s) : fwd2_typed<false, 128>(p, maps, s);
-#endif
-    if (p.hd == 64) return bf16 ? fwd_typed<true, 64>(p, maps, s) : fwd_typed<false, 64>(p, maps, s);
-    return bf16 ? fwd_typed<true, 128>(p, maps, s) : fwd_typed<false, 128>(p, maps, s);
 }
 
 }  // namespace attn
