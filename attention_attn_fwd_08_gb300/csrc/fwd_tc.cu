@@ -49,7 +49,8 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0) {
 // P.V and next S while the other warpgroup runs its softmax (ping-pong).
 //   warps 0-3  softmax of tile A (rows i0 .. i0+127)
 //   warps 4-7  softmax of tile B (rows i0+128 .. i0+255)
-//   warp 8     TMA producer     warp 9  TMEM owner + MMA issuer   (10, 11 idle)
+//   warp 8     TMA producer     warp 9  TMEM owner + MMA issuer of tile A
+//   warp 10    MMA issuer of tile B                                 (11 idle)
 // Registers: launched at 168 per thread (384 threads = 64512); the producer
 // warpgroup gives its share to the softmax warpgroups with setmaxnreg
 // (2*128*224 + 128*56 = 64512, never more than the launch total).
@@ -125,7 +126,16 @@ __global__ void __launch_bounds__(kThreads2, 1)
     auto has = [&](int u, int n) { return n >= tu[u].t0 && n < tu[u].t0 + tu[u].ntiles; };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNumBars; ++i) mbar_init(BAR(i), (i == P_FULL(0) || i == P_FULL(1)) ? 4 : 1);
+        // stage releases and the teardown barrier take one arrival per MMA issuer
+        const uint32_t issuers = hasB ? 2u : 1u;
+        for (int i = 0; i < C::kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == P_FULL(0) || i == P_FULL(1)) count = 4;
+            for (int s2 = 0; s2 < NS; ++s2)
+                if (i == K_EMPTY(s2) || i == V_EMPTY(s2)) count = issuers;
+            if (i == MMA_DONE) count = issuers;
+            mbar_init(BAR(i), count);
+        }
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -178,50 +188,52 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int n = max(0, issued_v - NS); n < issued_v; ++n)
                 mbar_wait(BAR(V_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
-        } else if (warp == 9) {
-        if (lane == 0 && ntiles > 0) {
+        } else if (warp == 9 || warp == 10) {
+        // Two MMA issuers, one per query tile (warp 9: A, warp 10: B), so that one
+        // tile's barrier waits overlap the other tile's MMA issue.  Each runs its own
+        // in-order chain; both commit the K/V stage releases of every tile in the
+        // union range (those barriers count one arrival per issuer).
+        const int u = warp - 9;
+        if (lane == 0 && ntiles > 0 && (u == 0 || hasB)) {
             constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
             constexpr uint32_t idPV = idesc_f16(BF16, BM, HD, false, true);
             bool ok = mbar_wait(BAR(Q_FULL), 0, P.status, ST_FWD_MMA, &abort_flag);
+            const uint64_t qdesc = sdesc_sw128(sbase + C::kQOff + u * C::kQBytes, 16, 1024);
+            const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
             // n is relative to t0 here
-            auto issue_s = [&](int u, int n) -> bool {
+            auto issue_s = [&](int n) -> bool {
                 const int ks = n % NS;
                 if (!mbar_wait(BAR(K_FULL(ks)), (n / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
                 // descriptor + (byte offset >> 4) moves the start address (no carry below 256 KB)
-                const uint64_t qdesc = sdesc_sw128(sbase + C::kQOff + u * C::kQBytes, 16, 1024);
                 const uint64_t kdesc = sdesc_sw128(sbase + C::kKOff + ks * C::kKVBytes, 16, 1024);
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off_q = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
                     const uint32_t off_k = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
-                    mma_ss(tbase + u * 128, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
+                    mma_ss(tS, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(BAR(S_FULL(u)));
                 return true;
             };
-            auto issue_pv = [&](int u, int n) -> bool {
+            auto issue_pv = [&](int n) -> bool {
                 const int vs = n % NS;
                 const int k = t0 + n - tu[u].t0;  // index of this tile in u's sequence
                 if (!mbar_wait(BAR(P_FULL(u)), k & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
                 if (!mbar_wait(BAR(V_FULL(vs)), (n / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
                 const uint64_t vdesc = sdesc_sw128(sbase + C::kVOff + vs * C::kKVBytes, BN * 128, 1024);
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tbase + 256 + u * HD, tbase + u * 128 + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
-                           (k > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV, (k > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(BAR(O_DONE(u)));
                 return true;
             };
-            for (int u = 0; ok && u < 2; ++u)
-                if (has(u, t0)) ok = issue_s(u, 0);
+            if (ok && has(u, t0)) ok = issue_s(0);
             if (ok) mma_commit(BAR(K_EMPTY(0)));
             for (int n = 0; ok && n < ntiles; ++n) {
-                for (int u = 0; ok && u < 2; ++u) {
-                    if (has(u, t0 + n)) ok = issue_pv(u, n);
-                    if (ok && n + 1 < ntiles && has(u, t0 + n + 1)) ok = issue_s(u, n + 1);
-                }
+                if (has(u, t0 + n)) ok = issue_pv(n);
+                if (ok && n + 1 < ntiles && has(u, t0 + n + 1)) ok = issue_s(n + 1);
                 if (!ok) break;
                 mma_commit(BAR(V_EMPTY(n % NS)));
                 if (n + 1 < ntiles) mma_commit(BAR(K_EMPTY((n + 1) % NS)));

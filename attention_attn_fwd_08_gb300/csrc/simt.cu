@@ -137,37 +137,43 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
 }
 
 // ------------------------------------------------------- backward: D = dO.O
-// One warp per (b, i, h) row, i < tq_pad: D = dO.O and LSE*log2(e) into the
-// padded [B*H][tq_pad] workspace rows (padding rows get D = 0, LSE = +inf so
-// they contribute nothing).
-template <typename T>
-__global__ void bwd_preprocess_kernel(Params P) {
-    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
+// D = dO.O and LSE*log2(e) for every (b, i, h) row, i < tq_pad, into the padded
+// [B*H][tq_pad] workspace rows (padding rows get D = 0, LSE = +inf so they
+// contribute nothing).  HBM-bound: each thread reads 16 bytes of O and of dO,
+// LPR = hd*sizeof(T)/16 lanes share a row, rows in (b, i, h) order so
+// consecutive lanes read consecutive memory.
+template <typename T, int LPR>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(Params P) {
+    constexpr int V = 16 / (int)sizeof(T);  // elements per 16-byte load
+    const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = gt / LPR;
+    const int sub = (int)(gt % LPR);
     const long long rows = (long long)P.B * P.tq_pad * P.H;
-    if (warp >= rows) return;
-    // row order (b, i, h) so consecutive warps read consecutive memory
-    const int h = (int)(warp % P.H);
-    const long long bi = warp / P.H;
+    const bool live = row < rows;
+    const int h = live ? (int)(row % P.H) : 0;
+    const long long bi = live ? row / P.H : 0;
     const int i = (int)(bi % P.tq_pad), b = (int)(bi / P.tq_pad);
+    float acc = 0.f;
+    if (live && i < P.Tq) {
+        const uint4 ov = reinterpret_cast<const uint4*>(qrow<T>(P, P.o_in, b, i, h))[sub];
+        const uint4 gv = reinterpret_cast<const uint4*>(qrow<T>(P, P.dout, b, i, h))[sub];
+        const T* oe = reinterpret_cast<const T*>(&ov);
+        const T* ge = reinterpret_cast<const T*>(&gv);
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc = fmaf(Elem<T>::to_f(oe[e]), Elem<T>::to_f(ge[e]), acc);
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, LPR);
+    if (!live || sub != 0) return;
     const long long srow = ((long long)b * P.H + h) * P.tq_pad + i;
     if (i >= P.Tq) {
-        if (lane == 0) {
-            P.delta[srow] = 0.f;
-            P.lse2[srow] = INFINITY;
-        }
+        P.delta[srow] = 0.f;
+        P.lse2[srow] = INFINITY;
         return;
     }
-    const T* o = qrow<T>(P, P.o_in, b, i, h);
-    const T* g = qrow<T>(P, P.dout, b, i, h);
-    float acc = 0.f;
-    for (int d = lane; d < P.hd; d += 32) acc = fmaf(Elem<T>::to_f(o[d]), Elem<T>::to_f(g[d]), acc);
-    acc = warp_sum(acc);
-    if (lane == 0) {
-        P.delta[srow] = acc;
-        const float l = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
-        P.lse2[srow] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
-    }
+    P.delta[srow] = acc;
+    const float l = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
+    P.lse2[srow] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
 }
 
 // -------------------------------------------------------------- backward: dQ
@@ -364,13 +370,21 @@ cudaError_t fwd_typed(const Params& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename T, int LPR>
+cudaError_t preprocess_launch(const Params& p, cudaStream_t s) {
+    const long long threads = (long long)p.B * p.tq_pad * p.H * LPR;
+    const int block = 256;
+    bwd_preprocess_kernel<T, LPR><<<(unsigned)((threads + block - 1) / block), block, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t preprocess_typed(const Params& p, cudaStream_t s) {
-    const long long rows = (long long)p.B * p.tq_pad * p.H;
-    const int threads = 256;
-    const long long blocks = (rows * 32 + threads - 1) / threads;
-    bwd_preprocess_kernel<T><<<(unsigned)blocks, threads, 0, s>>>(p);
-    return cudaGetLastError();
+    // lanes per row = hd * sizeof(T) / 16 (hd is 64 or 128)
+    const int lpr = p.hd * (int)sizeof(T) / 16;
+    if (lpr == 8) return preprocess_launch<T, 8>(p, s);
+    if (lpr == 16) return preprocess_launch<T, 16>(p, s);
+    return preprocess_launch<T, 32>(p, s);
 }
 
 template <typename T, int HD>
