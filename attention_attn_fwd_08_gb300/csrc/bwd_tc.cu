@@ -22,8 +22,9 @@
 //           visible pairs, dS^T = P^T (dP^T - D) (* (1 - tanh^2)).
 //   TMEM: S^T 0/64, dP^T 128/192, dV 256, dK 256+hd.
 // dQ kernel: CTA = 128 query rows of one (b, h): S = Q K^T and dP = dO V^T
-//   over 64-key tiles (double buffer), dS written over S, dQ += dS K.
-//   TMEM: S 0/64, dP 128/192, dQ 256.
+//   over 64-key tiles (double buffer), dS written over S, dQ += dS K.  Q and
+//   dO are copied once into TMEM so all three GEMMs take A from TMEM.
+//   TMEM: S 0/64, dP 128/192, dQ 256, Q 256+hd, dO 256+hd+hd/2.
 #include <math.h>
 
 #include <type_traits>
@@ -351,7 +352,7 @@ struct QCfg {
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKBytes;
     static constexpr int kBarOff = kVOff + kStages * kKBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1 + 1;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
@@ -376,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto ST_FULL = [&](int b) { return 1 + 2 * NS + b; };
     auto DS_FULL = [&](int b) { return 3 + 2 * NS + b; };
     const int ACC_DONE = 5 + 2 * NS;
+    const int QT_READY = 7 + 2 * NS;  // Q and dO copied into TMEM (A operands)
     const int MMA_DONE = 6 + 2 * NS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -391,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntiles = hi > lo ? (hi + BK - 1) / BK - kt0 : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNumBars; ++i) mbar_init(BAR(i), (i == DS_FULL(0) || i == DS_FULL(1)) ? 4 : 1);
+        for (int i = 0; i < C::kNumBars; ++i)
+            mbar_init(BAR(i), (i == DS_FULL(0) || i == DS_FULL(1) || i == QT_READY) ? 4 : 1);
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -404,6 +407,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
     const uint32_t tDQ = tbase + 256;
+    // Q and dO as 16-bit A operands in TMEM (row = lane, two elements per column):
+    // every GEMM here then reads only K or V from shared memory
+    const uint32_t tQ = tbase + 256 + HD, tG = tQ + HD / 2;
 
     if (warp == 4) {
         if (lane == 0 && ntiles > 0) {
@@ -441,25 +447,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idS = idesc_f16(BF16, BQ, BK, false, false);
             constexpr uint32_t idAcc = idesc_f16(BF16, BQ, HD, false, true);
-            bool ok = mbar_wait(BAR(QG_FULL), 0, P.status, ST_BWD_MMA, &abort_flag);
+            bool ok = mbar_wait(BAR(QT_READY), 0, P.status, ST_BWD_MMA, &abort_flag);
             auto issue_sd = [&](int n) -> bool {
                 const int s = n % NS, bf = n & 1;
                 if (!mbar_wait(BAR(KV_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t ka = sbase + C::kKOff + s * C::kKBytes, va = sbase + C::kVOff + s * C::kKBytes;
+                const uint64_t kdesc = sdesc_sw128(ka, 16, 1024), vdesc = sdesc_sw128(va, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                    const uint32_t boff = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-                    mma_ss(tbase + bf * 64, sdesc_sw128(sbase + C::kQOff + aoff, 16, 1024),
-                           sdesc_sw128(ka + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
+                    mma_ts(tbase + bf * 64, tQ + kk * 8, kdesc + boff, idS, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                    const uint32_t boff = (kk >> 2) * (BK * 128) + (kk & 3) * 32;
-                    mma_ss(tbase + 128 + bf * 64, sdesc_sw128(sbase + C::kGOff + aoff, 16, 1024),
-                           sdesc_sw128(va + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
+                    mma_ts(tbase + 128 + bf * 64, tG + kk * 8, vdesc + boff, idS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(BAR(ST_FULL(bf)));
                 return true;
@@ -500,7 +503,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         bool ok = true;
-        for (int n = 0; n < ntiles; ++n) {
+        if (ntiles > 0) {
+            // copy this thread's rows of Q and dO (128-byte-swizzled smem) into TMEM
+            ok = warp_wait(BAR(QG_FULL), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
+            if (ok) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const uint8_t* src = smem + (t == 0 ? C::kQOff : C::kGOff);
+#pragma unroll
+                    for (int half = 0; half < HD / 64; ++half) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const uint4 v4 = *reinterpret_cast<const uint4*>(
+                                src + half * (BQ * 128) + r * 128 + ((ch ^ (r & 7)) << 4));
+                            w[4 * ch] = v4.x;
+                            w[4 * ch + 1] = v4.y;
+                            w[4 * ch + 2] = v4.z;
+                            w[4 * ch + 3] = v4.w;
+                        }
+                        tmem_st32((t == 0 ? tQ : tG) + lane_off + half * 32, w);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(QT_READY));
+        }
+        for (int n = 0; ok && n < ntiles; ++n) {
             const int bf = n & 1;
             const int jt = (kt0 + n) * BK;
             uint32_t mbits[2] = {0xffffffffu, 0xffffffffu};
