@@ -34,7 +34,8 @@
 namespace attn {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;    // dK/dV: 4 compute warps, producer, MMA
+constexpr int kThreadsDQ = 224;  // dQ: 4 compute warps, producer, two MMA issuers
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned int* status, unsigned int code,
@@ -358,7 +359,7 @@ struct QCfg {
 };
 
 template <bool BF16, int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsDQ, 1)
     bwd_dq_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG) {
     using C = QCfg<HD>;
@@ -393,8 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntiles = hi > lo ? (hi + BK - 1) / BK - kt0 : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNumBars; ++i)
-            mbar_init(BAR(i), (i == DS_FULL(0) || i == DS_FULL(1) || i == QT_READY) ? 4 : 1);
+        for (int i = 0; i < C::kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == DS_FULL(0) || i == DS_FULL(1) || i == QT_READY) count = 4;
+            if (i == ST_FULL(0) || i == ST_FULL(1) || i == MMA_DONE) count = 2;  // two MMA issuers
+            for (int s2 = 0; s2 < NS; ++s2)
+                if (i == KV_EMPTY(s2)) count = 2;
+            mbar_init(BAR(i), count);
+        }
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -443,48 +450,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = max(0, issued - NS); n < issued; ++n)
                 mbar_wait(BAR(KV_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == 5 || warp == 6) {
+        // Two MMA issuers (one thread each issues at most one 128x64x16 MMA per ~44
+        // cycles, slower than the tensor core runs them): warp 5 issues S and dQ (the
+        // dS of tile n sits over S(n), so S(n+2) must follow dQ(n) in one stream),
+        // warp 6 issues dP.  ST_FULL, KV_EMPTY and MMA_DONE count both.
+        const bool issues_dp = warp == 6;
         if (lane == 0 && ntiles > 0) {
             constexpr uint32_t idS = idesc_f16(BF16, BQ, BK, false, false);
             constexpr uint32_t idAcc = idesc_f16(BF16, BQ, HD, false, true);
             bool ok = mbar_wait(BAR(QT_READY), 0, P.status, ST_BWD_MMA, &abort_flag);
-            auto issue_sd = [&](int n) -> bool {
+            // S(n) = Q K_n^T (warp 5) or dP(n) = dO V_n^T (warp 6) into buffer n & 1
+            auto issue_one = [&](int n) -> bool {
                 const int s = n % NS, bf = n & 1;
                 if (!mbar_wait(BAR(KV_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t ka = sbase + C::kKOff + s * C::kKBytes, va = sbase + C::kVOff + s * C::kKBytes;
-                const uint64_t kdesc = sdesc_sw128(ka, 16, 1024), vdesc = sdesc_sw128(va, 16, 1024);
+                const uint32_t src = sbase + (issues_dp ? C::kVOff : C::kKOff) + s * C::kKBytes;
+                const uint64_t bdesc = sdesc_sw128(src, 16, 1024);
+                const uint32_t d = tbase + (issues_dp ? 128 : 0) + bf * 64;
+                const uint32_t a = issues_dp ? tG : tQ;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
-                    mma_ts(tbase + bf * 64, tQ + kk * 8, kdesc + boff, idS, kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
-                    mma_ts(tbase + 128 + bf * 64, tG + kk * 8, vdesc + boff, idS, kk > 0 ? 1u : 0u);
+                    mma_ts(d, a + kk * 8, bdesc + boff, idS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(BAR(ST_FULL(bf)));
                 return true;
             };
-            if (ok) ok = issue_sd(0);
-            if (ok && ntiles > 1) ok = issue_sd(1);
+            if (ok) ok = issue_one(0);
+            if (ok && ntiles > 1) ok = issue_one(1);
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int s = n % NS, bf = n & 1;
+                // tile n's dS is written (and its S, dP read) once DS_FULL completes
                 if (!mbar_wait(BAR(DS_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ka = sbase + C::kKOff + s * C::kKBytes;
+                if (!issues_dp) {
+                    const uint32_t ka = sbase + C::kKOff + s * C::kKBytes;
+                    const uint64_t kdesc = sdesc_sw128(ka, BK * 128, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_ts(tDQ, tbase + bf * 64 + kk * 8, sdesc_sw128(ka + kk * 2048, BK * 128, 1024), idAcc,
-                           (n > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_ts(tDQ, tbase + bf * 64 + kk * 8, kdesc + ((kk * 2048) >> 4), idAcc,
+                               (n > 0 || kk > 0) ? 1u : 0u);
+                }
                 mma_commit(BAR(KV_EMPTY(s)));
-                if (n + 2 < ntiles) ok = issue_sd(n + 2);
+                if (n + 2 < ntiles) ok = issue_one(n + 2);
             }
-            if (ok) mma_commit(BAR(ACC_DONE));
+            if (ok && !issues_dp) mma_commit(BAR(ACC_DONE));
             mma_commit(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
@@ -668,7 +682,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         const unsigned grid = (unsigned)((p.Tq + 127) / 128) * p.H * p.B;
-        k<<<grid, kThreads, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout);
+        k<<<grid, kThreadsDQ, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
