@@ -38,12 +38,6 @@ constexpr int kThreads = 192;    // dK/dV: 4 compute warps, producer, MMA
 constexpr int kThreadsDQ = 224;  // dQ: 4 compute warps, producer, two MMA issuers
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned int* status, unsigned int code,
-                                          volatile int* abort_flag) {
-    const bool r = mbar_wait(bar, parity, status, code, abort_flag);
-    return __all_sync(0xffffffffu, r);
-}
-
 // =============================================================== dK / dV
 template <int HD>
 struct KVCfg {
@@ -117,36 +111,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tDV = tbase + 256, tDK = tbase + 256 + HD;
 
     if (warp == 4) {
-        if (lane == 0 && ntiles > 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            prefetch_tmap(&tmG);
-            mbar_expect_tx(BAR(KV_FULL), 2 * C::kKVBytes);
+        // producer and MMA issuer run as whole warps; one elected lane issues
+        if (ntiles > 0) {
+            if (elect_one()) {
+                prefetch_tmap(&tmQ);
+                prefetch_tmap(&tmK);
+                prefetch_tmap(&tmV);
+                prefetch_tmap(&tmG);
+            }
+            if (elect_one()) mbar_expect_tx(BAR(KV_FULL), 2 * C::kKVBytes);
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
-                tma_load_3d(sbase + C::kKOff + bx * (BKV * 128), &tmK, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
-                tma_load_3d(sbase + C::kVOff + bx * (BKV * 128), &tmV, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
+                if (elect_one())
+                    tma_load_3d(sbase + C::kKOff + bx * (BKV * 128), &tmK, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
+                if (elect_one())
+                    tma_load_3d(sbase + C::kVOff + bx * (BKV * 128), &tmV, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
             }
             int issued = 0;
             for (int n = 0; n < ntiles; ++n) {
                 const int s = n % NS, use = n / NS;
-                if (use > 0 && !mbar_wait(BAR(Q_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
+                if (use > 0 && !warp_wait(BAR(Q_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
                     break;
                 const int h = tile_head(n), i0 = tile_i0(n);
-                mbar_expect_tx(BAR(Q_FULL(s)), 2 * C::kQBytes + C::kStatBytes);
+                if (elect_one()) mbar_expect_tx(BAR(Q_FULL(s)), 2 * C::kQBytes + C::kStatBytes);
 #pragma unroll
                 for (int bx = 0; bx < C::kBoxes; ++bx) {
-                    tma_load_3d(sbase + C::kQOff + s * C::kQBytes + bx * (BQ * 128), &tmQ, BAR(Q_FULL(s)),
-                                h * HD + bx * 64, i0, b);
-                    tma_load_3d(sbase + C::kGOff + s * C::kQBytes + bx * (BQ * 128), &tmG, BAR(Q_FULL(s)),
-                                h * HD + bx * 64, i0, b);
+                    if (elect_one())
+                        tma_load_3d(sbase + C::kQOff + s * C::kQBytes + bx * (BQ * 128), &tmQ, BAR(Q_FULL(s)),
+                                    h * HD + bx * 64, i0, b);
+                    if (elect_one())
+                        tma_load_3d(sbase + C::kGOff + s * C::kQBytes + bx * (BQ * 128), &tmG, BAR(Q_FULL(s)),
+                                    h * HD + bx * 64, i0, b);
                 }
                 // LSE*log2(e) and D of these 64 rows (padded rows: +inf and 0)
                 const long long srow = ((long long)b * P.H + h) * P.tq_pad + i0;
                 const uint32_t sdst = sbase + C::kStatOff + s * C::kStatBytes;
-                bulk_load(sdst, P.lse2 + srow, BQ * 4, BAR(Q_FULL(s)));
-                bulk_load(sdst + BQ * 4, P.delta + srow, BQ * 4, BAR(Q_FULL(s)));
+                if (elect_one()) bulk_load(sdst, P.lse2 + srow, BQ * 4, BAR(Q_FULL(s)));
+                if (elect_one()) bulk_load(sdst + BQ * 4, P.delta + srow, BQ * 4, BAR(Q_FULL(s)));
                 issued = n + 1;
             }
             mbar_wait(BAR(KV_FULL), 0, P.status, ST_TEARDOWN, nullptr);
@@ -154,38 +155,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(BAR(Q_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
     } else if (warp == 5) {
-        if (lane == 0 && ntiles > 0) {
+        if (ntiles > 0) {
             constexpr uint32_t idS = idesc_f16(BF16, BKV, BQ, false, false);
             constexpr uint32_t idAcc = idesc_f16(BF16, BKV, HD, false, true);
-            bool ok = mbar_wait(BAR(KV_FULL), 0, P.status, ST_BWD_MMA, &abort_flag);
+            bool ok = warp_wait(BAR(KV_FULL), 0, P.status, ST_BWD_MMA, &abort_flag);
             // S^T and dP^T of tile n into buffer n & 1
             auto issue_sd = [&](int n) -> bool {
                 const int s = n % NS, bf = n & 1;
-                if (!mbar_wait(BAR(Q_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
+                if (!warp_wait(BAR(Q_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t qa = sbase + C::kQOff + s * C::kQBytes, ga = sbase + C::kGOff + s * C::kQBytes;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
                     const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                    mma_ss(tbase + bf * 64, sdesc_sw128(sbase + C::kKOff + aoff, 16, 1024),
-                           sdesc_sw128(qa + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    if (elect_one())
+                        mma_ss(tbase + bf * 64, sdesc_sw128(sbase + C::kKOff + aoff, 16, 1024),
+                               sdesc_sw128(qa + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
                     const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                    mma_ss(tbase + 128 + bf * 64, sdesc_sw128(sbase + C::kVOff + aoff, 16, 1024),
-                           sdesc_sw128(ga + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    if (elect_one())
+                        mma_ss(tbase + 128 + bf * 64, sdesc_sw128(sbase + C::kVOff + aoff, 16, 1024),
+                               sdesc_sw128(ga + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(BAR(ST_FULL(bf)));
+                if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
                 return true;
             };
             if (ok) ok = issue_sd(0);
             if (ok && ntiles > 1) ok = issue_sd(1);
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int s = n % NS, bf = n & 1;
-                if (!mbar_wait(BAR(PT_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
+                if (!warp_wait(BAR(PT_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -193,19 +196,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t qa = sbase + C::kQOff + s * C::kQBytes, ga = sbase + C::kGOff + s * C::kQBytes;
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk) {
-                    mma_ts(tDV, tbase + bf * 64 + kk * 8, sdesc_sw128(ga + kk * 2048, BQ * 128, 1024), idAcc,
-                           (n > 0 || kk > 0) ? 1u : 0u);
+                    if (elect_one())
+                        mma_ts(tDV, tbase + bf * 64 + kk * 8, sdesc_sw128(ga + kk * 2048, BQ * 128, 1024), idAcc,
+                               (n > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk) {
-                    mma_ts(tDK, tbase + 128 + bf * 64 + kk * 8, sdesc_sw128(qa + kk * 2048, BQ * 128, 1024), idAcc,
-                           (n > 0 || kk > 0) ? 1u : 0u);
+                    if (elect_one())
+                        mma_ts(tDK, tbase + 128 + bf * 64 + kk * 8, sdesc_sw128(qa + kk * 2048, BQ * 128, 1024),
+                               idAcc, (n > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(BAR(Q_EMPTY(s)));
+                if (elect_one()) mma_commit(BAR(Q_EMPTY(s)));
                 if (n + 2 < ntiles) ok = issue_sd(n + 2);
             }
-            if (ok) mma_commit(BAR(ACC_DONE));
-            mma_commit(BAR(MMA_DONE));
+            if (ok && elect_one()) mma_commit(BAR(ACC_DONE));
+            if (elect_one()) mma_commit(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
     } else {
@@ -419,30 +424,37 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     const uint32_t tQ = tbase + 256 + HD, tG = tQ + HD / 2;
 
     if (warp == 4) {
-        if (lane == 0 && ntiles > 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            prefetch_tmap(&tmG);
-            mbar_expect_tx(BAR(QG_FULL), 2 * C::kQBytes);
+        // producer and MMA issuers run as whole warps; one elected lane issues
+        if (ntiles > 0) {
+            if (elect_one()) {
+                prefetch_tmap(&tmQ);
+                prefetch_tmap(&tmK);
+                prefetch_tmap(&tmV);
+                prefetch_tmap(&tmG);
+            }
+            if (elect_one()) mbar_expect_tx(BAR(QG_FULL), 2 * C::kQBytes);
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
-                tma_load_3d(sbase + C::kQOff + bx * (BQ * 128), &tmQ, BAR(QG_FULL), h * HD + bx * 64, i0, b);
-                tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), h * HD + bx * 64, i0, b);
+                if (elect_one())
+                    tma_load_3d(sbase + C::kQOff + bx * (BQ * 128), &tmQ, BAR(QG_FULL), h * HD + bx * 64, i0, b);
+                if (elect_one())
+                    tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), h * HD + bx * 64, i0, b);
             }
             int issued = 0;
             for (int n = 0; n < ntiles; ++n) {
                 const int s = n % NS, use = n / NS;
-                if (use > 0 && !mbar_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
+                if (use > 0 && !warp_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
                     break;
                 const int jt = (kt0 + n) * BK;
-                mbar_expect_tx(BAR(KV_FULL(s)), 2 * C::kKBytes);
+                if (elect_one()) mbar_expect_tx(BAR(KV_FULL(s)), 2 * C::kKBytes);
 #pragma unroll
                 for (int bx = 0; bx < C::kBoxes; ++bx) {
-                    tma_load_3d(sbase + C::kKOff + s * C::kKBytes + bx * (BK * 128), &tmK, BAR(KV_FULL(s)),
-                                kvh * HD + bx * 64, jt, b);
-                    tma_load_3d(sbase + C::kVOff + s * C::kKBytes + bx * (BK * 128), &tmV, BAR(KV_FULL(s)),
-                                kvh * HD + bx * 64, jt, b);
+                    if (elect_one())
+                        tma_load_3d(sbase + C::kKOff + s * C::kKBytes + bx * (BK * 128), &tmK, BAR(KV_FULL(s)),
+                                    kvh * HD + bx * 64, jt, b);
+                    if (elect_one())
+                        tma_load_3d(sbase + C::kVOff + s * C::kKBytes + bx * (BK * 128), &tmV, BAR(KV_FULL(s)),
+                                    kvh * HD + bx * 64, jt, b);
                 }
                 issued = n + 1;
             }
@@ -451,19 +463,19 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 mbar_wait(BAR(KV_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
     } else if (warp == 5 || warp == 6) {
-        // Two MMA issuers (one thread each issues at most one 128x64x16 MMA per ~44
-        // cycles, slower than the tensor core runs them): warp 5 issues S and dQ (the
-        // dS of tile n sits over S(n), so S(n+2) must follow dQ(n) in one stream),
-        // warp 6 issues dP.  ST_FULL, KV_EMPTY and MMA_DONE count both.
+        // Two MMA issuers, so that one's barrier waits overlap the other's issue:
+        // warp 5 issues S and dQ (the dS of tile n sits over S(n), so S(n+2) must
+        // follow dQ(n) in one stream), warp 6 issues dP.  ST_FULL, KV_EMPTY and
+        // MMA_DONE count both.
         const bool issues_dp = warp == 6;
-        if (lane == 0 && ntiles > 0) {
+        if (ntiles > 0) {
             constexpr uint32_t idS = idesc_f16(BF16, BQ, BK, false, false);
             constexpr uint32_t idAcc = idesc_f16(BF16, BQ, HD, false, true);
-            bool ok = mbar_wait(BAR(QT_READY), 0, P.status, ST_BWD_MMA, &abort_flag);
+            bool ok = warp_wait(BAR(QT_READY), 0, P.status, ST_BWD_MMA, &abort_flag);
             // S(n) = Q K_n^T (warp 5) or dP(n) = dO V_n^T (warp 6) into buffer n & 1
             auto issue_one = [&](int n) -> bool {
                 const int s = n % NS, bf = n & 1;
-                if (!mbar_wait(BAR(KV_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
+                if (!warp_wait(BAR(KV_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t src = sbase + (issues_dp ? C::kVOff : C::kKOff) + s * C::kKBytes;
                 const uint64_t bdesc = sdesc_sw128(src, 16, 1024);
@@ -472,9 +484,9 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
-                    mma_ts(d, a + kk * 8, bdesc + boff, idS, kk > 0 ? 1u : 0u);
+                    if (elect_one()) mma_ts(d, a + kk * 8, bdesc + boff, idS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(BAR(ST_FULL(bf)));
+                if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
                 return true;
             };
             if (ok) ok = issue_one(0);
@@ -482,7 +494,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int s = n % NS, bf = n & 1;
                 // tile n's dS is written (and its S, dP read) once DS_FULL completes
-                if (!mbar_wait(BAR(DS_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
+                if (!warp_wait(BAR(DS_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -492,14 +504,15 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                     const uint64_t kdesc = sdesc_sw128(ka, BK * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_ts(tDQ, tbase + bf * 64 + kk * 8, kdesc + ((kk * 2048) >> 4), idAcc,
-                               (n > 0 || kk > 0) ? 1u : 0u);
+                        if (elect_one())
+                            mma_ts(tDQ, tbase + bf * 64 + kk * 8, kdesc + ((kk * 2048) >> 4), idAcc,
+                                   (n > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(BAR(KV_EMPTY(s)));
+                if (elect_one()) mma_commit(BAR(KV_EMPTY(s)));
                 if (n + 2 < ntiles) ok = issue_one(n + 2);
             }
-            if (ok && !issues_dp) mma_commit(BAR(ACC_DONE));
-            mma_commit(BAR(MMA_DONE));
+            if (ok && !issues_dp && elect_one()) mma_commit(BAR(ACC_DONE));
+            if (elect_one()) mma_commit(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
     } else {

@@ -220,6 +220,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// Bounded wait by a whole warp; true only when every lane saw the phase.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned int* status, unsigned int code,
+                                          volatile int* abort_flag) {
+    const bool r = mbar_wait(bar, parity, status, code, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+// True in exactly one lane of the (converged, full) warp, the same lane every
+// time.  Issuing tcgen05.mma / tcgen05.commit / TMA this way from a warp that
+// runs the issue loop together keeps the operand arithmetic warp-uniform; the
+// issue then costs about a third of the same loop run by a single lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2) {

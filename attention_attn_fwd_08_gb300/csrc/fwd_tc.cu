@@ -26,7 +26,8 @@ namespace {
 constexpr int BM = 128;      // query rows per tile (two tiles per CTA)
 constexpr int BN = 128;      // keys per tile
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale only when the max grows by > 256x
+constexpr float kRescaleHi = 8.0f;   // log2 units: the row max may reach 2^8 times the reference
+constexpr float kRescaleLo = -2.0f;  // a row's first visible tile may put its max at >= 2^-2
 
 struct TileInfo {
     int t0, ntiles;
@@ -44,9 +45,14 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0) {
 }
 
 // ------------------------------------------------------------------------
-// Two query tiles per CTA (256 rows of one head) sharing every K/V tile, with
+// Persistent: one CTA per SM walks work items blockIdx.x, +gridDim.x, ...; an
+// item is two query tiles (256 rows of one head) sharing every K/V tile, with
 // one softmax warpgroup per tile, so the tensor core works on one tile's
-// P.V and next S while the other warpgroup runs its softmax (ping-pong).
+// P.V and next S while the other warpgroup runs its softmax (ping-pong).  The
+// K/V ring and every barrier phase run on across items: the next item's Q tile
+// loads once the current item's last S of that tile completed, and its first
+// P.V waits only for the epilogue to have read O out of TMEM, so item
+// boundaries cost little more than a ring step.
 //   warps 0-3  softmax of tile A (rows i0 .. i0+127)
 //   warps 4-7  softmax of tile B (rows i0+128 .. i0+255)
 //   warp 8     TMA producer     warp 9  TMEM owner + MMA issuer of tile A
@@ -71,10 +77,48 @@ struct Fwd2Cfg {
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kStages * kKVBytes;
-    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
+    static constexpr int kNumBars = 13 + 4 * kStages;
     static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
+
+// One work item: 256 query rows (tiles A and B) of one (batch, head), and the
+// key tiles each tile sees.  Items are numbered longest first: every head's last
+// (causally heaviest) query block comes before any head's next one.
+struct FwdItem {
+    int b, h, kvh, i0;
+    bool hasB;
+    TileInfo tu[2];
+    int t0, ntiles;  // union key-tile range of the two tiles
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
+    FwdItem it;
+    const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
+    const int hb = w % (P.H * P.B);
+    const int cq = ncq - 1 - w / (P.H * P.B);
+    it.h = hb % P.H;
+    it.b = hb / P.H;
+    it.kvh = it.h / P.G;
+    it.i0 = cq * 2 * BM;
+    it.hasB = it.i0 + BM < P.Tq;
+    it.tu[0] = tile_range(P, it.i0);
+    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM) : TileInfo{0, 0};
+    int t0 = it.tu[0].t0, t1 = it.tu[0].t0 + it.tu[0].ntiles;
+    if (it.tu[1].ntiles > 0) {
+        if (it.tu[0].ntiles == 0) {
+            t0 = it.tu[1].t0;
+            t1 = it.tu[1].t0 + it.tu[1].ntiles;
+        } else {
+            t0 = min(t0, it.tu[1].t0);
+            t1 = max(t1, it.tu[1].t0 + it.tu[1].ntiles);
+        }
+    }
+    it.t0 = t0;
+    it.ntiles = t1 > t0 ? t1 - t0 : 0;
+    return it;
+}
+__device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * BM - 1) / (2 * BM) * P.H * P.B; }
 
 template <bool BF16, int HD>
 __global__ void __launch_bounds__(kThreads2, 1)
@@ -90,50 +134,32 @@ __global__ void __launch_bounds__(kThreads2, 1)
     __shared__ int abort_flag;
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    const int Q_FULL = 0;
-    auto K_FULL = [&](int s) { return 1 + s; };
-    auto K_EMPTY = [&](int s) { return 1 + NS + s; };
-    auto V_FULL = [&](int s) { return 1 + 2 * NS + s; };
-    auto V_EMPTY = [&](int s) { return 1 + 3 * NS + s; };
-    auto S_FULL = [&](int u) { return 1 + 4 * NS + u; };
-    auto P_FULL = [&](int u) { return 3 + 4 * NS + u; };
-    auto O_DONE = [&](int u) { return 5 + 4 * NS + u; };
-    const int MMA_DONE = 7 + 4 * NS;
+    auto Q_FULL = [&](int u) { return u; };
+    auto Q_EMPTY = [&](int u) { return 2 + u; };  // the item's last S of tile u completed
+    auto K_FULL = [&](int s) { return 4 + s; };
+    auto K_EMPTY = [&](int s) { return 4 + NS + s; };
+    auto V_FULL = [&](int s) { return 4 + 2 * NS + s; };
+    auto V_EMPTY = [&](int s) { return 4 + 3 * NS + s; };
+    auto S_FULL = [&](int u) { return 4 + 4 * NS + u; };
+    auto P_FULL = [&](int u) { return 6 + 4 * NS + u; };
+    auto O_DONE = [&](int u) { return 8 + 4 * NS + u; };   // the item's last P.V of tile u completed
+    auto O_EMPTY = [&](int u) { return 10 + 4 * NS + u; };  // the epilogue has read O_u out of TMEM
+    const int MMA_DONE = 12 + 4 * NS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // 1-D grid, longest first: every head's last (causally heaviest) query block
-    // comes before any head's next one
-    const int ncta = (P.Tq + 2 * BM - 1) / (2 * BM);
-    const int hb = (int)(blockIdx.x % (unsigned)(P.H * P.B));
-    const int cq = ncta - 1 - (int)(blockIdx.x / (unsigned)(P.H * P.B));
-    const int h = hb % P.H, b = hb / P.H, kvh = h / P.G;
-    const int i0 = cq * 2 * BM;
-    const bool hasB = i0 + BM < P.Tq;
-    TileInfo tu[2];
-    tu[0] = tile_range(P, i0);
-    tu[1] = hasB ? tile_range(P, i0 + BM) : TileInfo{0, 0};
-    int t0 = tu[0].t0, t1 = tu[0].t0 + tu[0].ntiles;
-    if (tu[1].ntiles > 0) {
-        if (tu[0].ntiles == 0) {
-            t0 = tu[1].t0;
-            t1 = tu[1].t0 + tu[1].ntiles;
-        } else {
-            t0 = min(t0, tu[1].t0);
-            t1 = max(t1, tu[1].t0 + tu[1].ntiles);
-        }
-    }
-    const int ntiles = t1 > t0 ? t1 - t0 : 0;
-    auto has = [&](int u, int n) { return n >= tu[u].t0 && n < tu[u].t0 + tu[u].ntiles; };
+    const int nitems = fwd_items(P);
+    // every role walks the same item sequence; a tile u is active in an item when
+    // it has rows and sees at least one key tile
+    auto active = [&](const FwdItem& it, int u) { return it.tu[u].ntiles > 0; };
 
     if (threadIdx.x == 0) {
-        // stage releases and the teardown barrier take one arrival per MMA issuer
-        const uint32_t issuers = hasB ? 2u : 1u;
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == P_FULL(0) || i == P_FULL(1)) count = 4;
+            if (i == P_FULL(0) || i == P_FULL(1) || i == O_EMPTY(0) || i == O_EMPTY(1)) count = 4;
+            // stage releases and the teardown barrier: one arrival per MMA issuer
             for (int s2 = 0; s2 < NS; ++s2)
-                if (i == K_EMPTY(s2) || i == V_EMPTY(s2)) count = issuers;
-            if (i == MMA_DONE) count = issuers;
+                if (i == K_EMPTY(s2) || i == V_EMPTY(s2)) count = 2;
+            if (i == MMA_DONE) count = 2;
             mbar_init(BAR(i), count);
         }
         abort_flag = 0;
@@ -149,253 +175,260 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const uint32_t tbase = *tmem_slot;
     if (warp >= 8) {
         regs_dec<kRegsProducer>();
+        // The producer and the MMA issuers run their loops as whole warps and issue
+        // each TMA copy, MMA and commit from one elected lane.
         if (warp == 8) {
-        if (lane == 0 && ntiles > 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            const int nq = hasB ? 2 : 1;
-            mbar_expect_tx(BAR(Q_FULL), nq * C::kQBytes);
-            for (int u = 0; u < nq; ++u)
-#pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_3d(sbase + C::kQOff + u * C::kQBytes + bx * (BM * 128), &tmQ, BAR(Q_FULL),
-                                h * HD + bx * 64, i0 + u * BM, b);
-            int issued_k = 0, issued_v = 0;
-            for (int n = 0; n < ntiles; ++n) {
-                const int s = n % NS, use = n / NS;
-                const int j0 = (t0 + n) * BN;
-                if (use > 0 && !mbar_wait(BAR(K_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag))
-                    break;
-                mbar_expect_tx(BAR(K_FULL(s)), C::kKVBytes);
-#pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_3d(sbase + C::kKOff + s * C::kKVBytes + bx * (BN * 128), &tmK, BAR(K_FULL(s)),
-                                kvh * HD + bx * 64, j0, b);
-                issued_k = n + 1;
-                if (use > 0 && !mbar_wait(BAR(V_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag))
-                    break;
-                mbar_expect_tx(BAR(V_FULL(s)), C::kKVBytes);
-#pragma unroll
-                for (int bx = 0; bx < C::kBoxes; ++bx)
-                    tma_load_3d(sbase + C::kVOff + s * C::kKVBytes + bx * (BN * 128), &tmV, BAR(V_FULL(s)),
-                                kvh * HD + bx * 64, j0, b);
-                issued_v = n + 1;
+            if (elect_one()) {
+                prefetch_tmap(&tmQ);
+                prefetch_tmap(&tmK);
+                prefetch_tmap(&tmV);
             }
-            mbar_wait(BAR(Q_FULL), 0, P.status, ST_TEARDOWN, nullptr);
-            for (int n = max(0, issued_k - NS); n < issued_k; ++n)
+            bool ok = true;
+            int gk = 0, gv = 0;   // K and V tiles loaded so far (ring positions)
+            int qn[2] = {0, 0};   // Q tiles loaded so far, per tile slot
+            for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+                const FwdItem it = fwd_item(P, w);
+                if (it.ntiles == 0) continue;
+                for (int u = 0; ok && u < 2; ++u) {
+                    if (!active(it, u)) continue;
+                    // the slot is free once the previous item's last S of this tile completed
+                    if (qn[u] > 0 && !warp_wait(BAR(Q_EMPTY(u)), (qn[u] - 1) & 1, P.status, ST_FWD_PRODUCER,
+                                                &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) mbar_expect_tx(BAR(Q_FULL(u)), C::kQBytes);
+#pragma unroll
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        if (elect_one())
+                            tma_load_3d(sbase + C::kQOff + u * C::kQBytes + bx * (BM * 128), &tmQ, BAR(Q_FULL(u)),
+                                        it.h * HD + bx * 64, it.i0 + u * BM, it.b);
+                    ++qn[u];
+                }
+                for (int n = 0; ok && n < it.ntiles; ++n) {
+                    const int s = gk % NS, use = gk / NS;
+                    const int j0 = (it.t0 + n) * BN;
+                    if (use > 0 && !warp_wait(BAR(K_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) mbar_expect_tx(BAR(K_FULL(s)), C::kKVBytes);
+#pragma unroll
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        if (elect_one())
+                            tma_load_3d(sbase + C::kKOff + s * C::kKVBytes + bx * (BN * 128), &tmK, BAR(K_FULL(s)),
+                                        it.kvh * HD + bx * 64, j0, it.b);
+                    ++gk;
+                    if (use > 0 && !warp_wait(BAR(V_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) mbar_expect_tx(BAR(V_FULL(s)), C::kKVBytes);
+#pragma unroll
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        if (elect_one())
+                            tma_load_3d(sbase + C::kVOff + s * C::kKVBytes + bx * (BN * 128), &tmV, BAR(V_FULL(s)),
+                                        it.kvh * HD + bx * 64, j0, it.b);
+                    ++gv;
+                }
+            }
+            // every copy in flight lands before the CTA exits
+            for (int u = 0; u < 2; ++u)
+                if (qn[u] > 0) mbar_wait(BAR(Q_FULL(u)), (qn[u] - 1) & 1, P.status, ST_TEARDOWN, nullptr);
+            for (int n = max(0, gk - NS); n < gk; ++n)
                 mbar_wait(BAR(K_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
-            for (int n = max(0, issued_v - NS); n < issued_v; ++n)
+            for (int n = max(0, gv - NS); n < gv; ++n)
                 mbar_wait(BAR(V_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
-        }
         } else if (warp == 9 || warp == 10) {
-        // Two MMA issuers, one per query tile (warp 9: A, warp 10: B), so that one
-        // tile's barrier waits overlap the other tile's MMA issue.  Each runs its own
-        // in-order chain; both commit the K/V stage releases of every tile in the
-        // union range (those barriers count one arrival per issuer).
-        const int u = warp - 9;
-        if (lane == 0 && ntiles > 0 && (u == 0 || hasB)) {
+            // Two MMA issuers, one per query tile (warp 9: A, warp 10: B), so that one
+            // tile's barrier waits overlap the other tile's MMA issue.  Each runs its own
+            // in-order chain over the same items; both commit the K/V stage releases of
+            // every tile (those barriers count one arrival per issuer).
+            const int u = warp - 9;
             constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
             constexpr uint32_t idPV = idesc_f16(BF16, BM, HD, false, true);
-            bool ok = mbar_wait(BAR(Q_FULL), 0, P.status, ST_FWD_MMA, &abort_flag);
+            auto wait_all = [&](int bar, uint32_t parity) -> bool {
+                return warp_wait(BAR(bar), parity, P.status, ST_FWD_MMA, &abort_flag);
+            };
             const uint64_t qdesc = sdesc_sw128(sbase + C::kQOff + u * C::kQBytes, 16, 1024);
             const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
-            // n is relative to t0 here
-            auto issue_s = [&](int n) -> bool {
-                const int ks = n % NS;
-                if (!mbar_wait(BAR(K_FULL(ks)), (n / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
-                tc_fence_after();
-                // descriptor + (byte offset >> 4) moves the start address (no carry below 256 KB)
-                const uint64_t kdesc = sdesc_sw128(sbase + C::kKOff + ks * C::kKVBytes, 16, 1024);
+            bool ok = true;
+            int g = 0;    // ring position of the item's first tile
+            int pc = 0;   // P_FULL(u) phases consumed
+            int act = 0;  // items in which this tile was active so far
+            for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+                const FwdItem it = fwd_item(P, w);
+                if (it.ntiles == 0) continue;
+                const TileInfo my = it.tu[u];
+                const bool on = active(it, u);
+                auto has = [&](int n) { return it.t0 + n >= my.t0 && it.t0 + n < my.t0 + my.ntiles; };
+                auto last_of_u = [&](int n) { return it.t0 + n == my.t0 + my.ntiles - 1; };
+                // S(n) = Q_u K(n)^T into S_u; the item's last S also frees the Q slot
+                auto issue_s = [&](int n) {
+                    const int gs = (g + n) % NS;
+                    const uint64_t kdesc = sdesc_sw128(sbase + C::kKOff + gs * C::kKVBytes, 16, 1024);
+                    // descriptor + (byte offset >> 4) moves the start address (no carry below 256 KB)
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off_q = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-                    const uint32_t off_k = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
-                    mma_ss(tS, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t off_q = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+                        const uint32_t off_k = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
+                        if (elect_one()) mma_ss(tS, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
+                    }
+                    if (elect_one()) mma_commit(BAR(S_FULL(u)));
+                    if (last_of_u(n) && elect_one()) mma_commit(BAR(Q_EMPTY(u)));
+                };
+                // O_u (+)= P_u V(n); the item's last one signals the epilogue
+                auto issue_pv = [&](int n, int k) {
+                    const int vs = (g + n) % NS;
+                    const uint64_t vdesc = sdesc_sw128(sbase + C::kVOff + vs * C::kKVBytes, BN * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        if (elect_one())
+                            mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
+                                   (k > 0 || kk > 0) ? 1u : 0u);
+                    if (k == my.ntiles - 1 && elect_one()) mma_commit(BAR(O_DONE(u)));
+                };
+                // Each step first waits for V(n) and K(n+1) (normally long resident), so
+                // that once P(n) arrives PV(n) and S(n+1) issue back to back.  The stage
+                // releases count arrivals, not issuers: a chain commits a tile's release
+                // only after it has waited for that tile's data phase (also for tiles it
+                // skips), so an arrival can never belong to a later use of the stage.
+                if (on && !wait_all(Q_FULL(u), act & 1)) {
+                    ok = false;
+                    break;
                 }
-                mma_commit(BAR(S_FULL(u)));
-                return true;
-            };
-            auto issue_pv = [&](int n) -> bool {
-                const int vs = n % NS;
-                const int k = t0 + n - tu[u].t0;  // index of this tile in u's sequence
-                if (!mbar_wait(BAR(P_FULL(u)), k & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
-                if (!mbar_wait(BAR(V_FULL(vs)), (n / NS) & 1, P.status, ST_FWD_MMA, &abort_flag)) return false;
+                if (!wait_all(K_FULL(g % NS), (g / NS) & 1)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const uint64_t vdesc = sdesc_sw128(sbase + C::kVOff + vs * C::kKVBytes, BN * 128, 1024);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV, (k > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(BAR(O_DONE(u)));
-                return true;
-            };
-            if (ok && has(u, t0)) ok = issue_s(0);
-            if (ok) mma_commit(BAR(K_EMPTY(0)));
-            for (int n = 0; ok && n < ntiles; ++n) {
-                if (has(u, t0 + n)) ok = issue_pv(n);
-                if (ok && n + 1 < ntiles && has(u, t0 + n + 1)) ok = issue_s(n + 1);
-                if (!ok) break;
-                mma_commit(BAR(V_EMPTY(n % NS)));
-                if (n + 1 < ntiles) mma_commit(BAR(K_EMPTY((n + 1) % NS)));
+                if (has(0)) issue_s(0);
+                if (elect_one()) mma_commit(BAR(K_EMPTY(g % NS)));
+                for (int n = 0; ok && n < it.ntiles; ++n) {
+                    const int gn = g + n;
+                    ok = wait_all(V_FULL(gn % NS), (gn / NS) & 1);
+                    if (ok && n + 1 < it.ntiles) ok = wait_all(K_FULL((gn + 1) % NS), ((gn + 1) / NS) & 1);
+                    const int k = it.t0 + n - my.t0;  // index of tile n in u's own sequence
+                    if (ok && has(n)) {
+                        ok = wait_all(P_FULL(u), pc & 1);
+                        ++pc;
+                        // the first P.V overwrites O_u: the previous item's epilogue must have read it
+                        if (ok && k == 0 && act > 0) ok = wait_all(O_EMPTY(u), (act - 1) & 1);
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (has(n)) issue_pv(n, k);
+                    if (n + 1 < it.ntiles && has(n + 1)) issue_s(n + 1);
+                    if (elect_one()) mma_commit(BAR(V_EMPTY(gn % NS)));
+                    if (n + 1 < it.ntiles && elect_one()) mma_commit(BAR(K_EMPTY((gn + 1) % NS)));
+                }
+                g += it.ntiles;
+                if (on) ++act;
             }
-            mma_commit(BAR(MMA_DONE));
+            if (elect_one()) mma_commit(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
-        }
-        }  // warps 10 and 11 only fill the producer warpgroup
+        }  // warp 11 only fills the producer warpgroup
     } else {
         regs_inc<kRegsSoftmax>();
         // -------------------------------------- softmax + epilogue of tile u
         const int u = warp >> 2, wq = warp & 3;
         const int r = wq * 32 + lane;
-        const int ib = i0 + u * BM;  // first row of this tile
-        const int i = ib + r;
-        const int p = i + P.q_offset;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
         const float sl2 = P.scale_log2;
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         const float cap_out = P.softcap * kLog2e;
-        const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, P.Tq) - 1 + P.q_offset;
-        const TileInfo my = tu[u];
-        float m_used = -INFINITY, l = 0.f;
-        bool ok = true;
         auto wait_warp = [&](int bar, uint32_t parity) -> bool {
             const bool rr = mbar_wait(BAR(bar), parity, P.status, ST_FWD_SOFTMAX, &abort_flag);
             return __all_sync(0xffffffffu, rr);
         };
-        for (int k = 0; k < my.ntiles; ++k) {
-            const int j0 = (my.t0 + k) * BN;
-            const bool full = tile_full(P.causal, P.window, P.Tk, prow0, prow1, j0, j0 + BN) && !P.key_mask;
-            uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-            if (P.key_mask) {
-                const float* mrow = P.key_mask + (long long)b * P.mask_bstride;
+        bool ok = true;
+        int sc = 0;   // S_FULL(u) phases consumed
+        int act = 0;  // items in which this tile was active so far (O_DONE phases)
+        // Masking: in a tile that some row does not see whole, the invisible scores
+        // are overwritten with -inf in TMEM first, so every tile then runs the same
+        // softmax code (one hot copy of the unrolled loop instead of one per case).
+        auto mask_tile = [&](int clo, int chi, const uint32_t(&mbits)[4]) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t t[32];
+                tmem_ld32(tS + lane_off + c * 32, t);
+                tmem_ld_wait(t);
+                const uint32_t mw = mbits[0] * (c == 0) | mbits[1] * (c == 1) | mbits[2] * (c == 2) | mbits[3] * (c == 3);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int j = j0 + c * 32 + lane;
-                    mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
+                for (int e = 0; e < 32; ++e) {
+                    const int col = c * 32 + e;
+                    const bool v = col >= clo && col < chi && ((mw >> e) & 1u);
+                    t[e] = v ? t[e] : 0xff800000u;  // -inf
                 }
+                tmem_st32(tS + lane_off + c * 32, t);
             }
-            int clo = 0, chi = BN;
-            if (!full) {
-                chi = min(chi, P.Tk - j0);
-                if (P.causal) chi = min(chi, p - j0 + 1);
-                if (P.window > 0) {
-                    clo = max(clo, p - P.window + 1 - j0);
-                    if (!P.causal) chi = min(chi, p + P.window - j0);
-                }
-            }
-            if (!wait_warp(S_FULL(u), k & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // Visibility is evaluated only in tiles that some row does not see whole
-            // (kMask); s*scale and softcap*tanh(s*scale/softcap) both increase with s,
-            // so row maxima are taken over raw scores and transformed once.
-            auto vis_col = [&](int c) -> bool {
-                return c >= clo && c < chi && ((mbits[c >> 5] >> (c & 31)) & 1u);
-            };
-            auto to_log2 = [&](auto capc, float raw) -> float {
-                if constexpr (decltype(capc)::value) return cap_out * tanh_accurate(raw * cap_in);
-                else return raw * sl2;
-            };
-            // raw-score row max of the tile (first tile a row sees)
-            auto max_pass = [&](auto capc, auto maskc) -> float {
-                constexpr bool kMask = decltype(maskc)::value;
-                float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            tmem_st_wait();
+        };
+        // P = exp2(x) with x = s*scale*log2(e) - ms (or softcap*tanh(s*scale/softcap)*log2(e)
+        // - ms), as 16-bit pairs in registers; S stays intact in TMEM until the caller
+        // stores P over it.  Returns the row sum and the row max of x (-inf: nothing seen).
+        uint32_t pk[4][16];
+        auto p_pass = [&](auto capc, float ms, float& rsum, float& xmax) {
+            constexpr bool kCap = decltype(capc)::value;
+            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+            float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            auto chunk = [&](int c, const uint32_t(&t)[32]) {
 #pragma unroll
-                for (int c2 = 0; c2 < 4; c2 += 2) {
-                    uint32_t ta[32], tb[32];
-                    tmem_ld32(tS + lane_off + c2 * 32, ta);
-                    tmem_ld32(tS + lane_off + (c2 + 1) * 32, tb);
-                    tmem_ld_wait_only();
-                    tmem_pin(ta);
-                    tmem_pin(tb);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float a = __uint_as_float(ta[e]), bb = __uint_as_float(tb[e]);
-                        if constexpr (kMask) {
-                            a = vis_col(c2 * 32 + e) ? a : -INFINITY;
-                            bb = vis_col(c2 * 32 + 32 + e) ? bb : -INFINITY;
-                        }
-                        mr[e & 3] = fmaxf(mr[e & 3], fmaxf(a, bb));
+                for (int e = 0; e < 16; ++e) {
+                    const float r0 = __uint_as_float(t[2 * e]), r1 = __uint_as_float(t[2 * e + 1]);
+                    float x0, x1;
+                    if constexpr (kCap) {
+                        // a masked score is -inf, and softcap*tanh(-inf) would be finite
+                        x0 = r0 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r0 * cap_in), -ms);
+                        x1 = r1 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r1 * cap_in), -ms);
+                    } else {
+                        x0 = fmaf(r0, sl2, -ms);
+                        x1 = fmaf(r1, sl2, -ms);
                     }
+                    mr[e & 3] = fmaxf(mr[e & 3], fmaxf(x0, x1));
+                    const float p0 = fast_exp2(x0);  // ex2(-inf) = 0
+                    const float p1 = fast_exp2(x1);
+                    rs4[e & 3] += p0 + p1;
+                    pk[c][e] = pack2<BF16>(p0, p1);
                 }
-                const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
-                return mraw == -INFINITY ? -INFINITY : to_log2(capc, mraw);
             };
-            // P = exp2(x - ms) over the tile as 16-bit pairs in registers (S stays intact in
-            // TMEM until the caller stores P over it); returns the row sum and the
-            // (log2-unit) row max seen along the way
-            uint32_t pk[4][16];
-            auto p_pass = [&](auto capc, auto maskc, float ms, float& rsum, float& mxo) {
-                constexpr bool kCap = decltype(capc)::value;
-                constexpr bool kMask = decltype(maskc)::value;
-                float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-                float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                auto chunk = [&](int c, const uint32_t(&t)[32]) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float r0 = __uint_as_float(t[2 * e]), r1 = __uint_as_float(t[2 * e + 1]);
-                        float x0, x1;
-                        if constexpr (kCap) {
-                            x0 = fmaf(cap_out, tanh_accurate(r0 * cap_in), -ms);
-                            x1 = fmaf(cap_out, tanh_accurate(r1 * cap_in), -ms);
-                        } else {
-                            x0 = fmaf(r0, sl2, -ms);
-                            x1 = fmaf(r1, sl2, -ms);
-                        }
-                        if constexpr (kMask) {
-                            // the mask goes on the transformed argument: softcap*tanh(-inf) is finite
-                            const bool v0 = vis_col(c * 32 + 2 * e), v1 = vis_col(c * 32 + 2 * e + 1);
-                            r0 = v0 ? r0 : -INFINITY;
-                            r1 = v1 ? r1 : -INFINITY;
-                            x0 = v0 ? x0 : -INFINITY;
-                            x1 = v1 ? x1 : -INFINITY;
-                        }
-                        mr[e & 3] = fmaxf(mr[e & 3], fmaxf(r0, r1));
-                        const float p0 = fast_exp2(x0);  // masked: ex2(-inf) = 0
-                        const float p1 = fast_exp2(x1);
-                        rs4[e & 3] += p0 + p1;
-                        pk[c][e] = pack2<BF16>(p0, p1);
-                    }
-                };
-                uint32_t ta[32], tb[32];
-                tmem_ld32(tS + lane_off + 0 * 32, ta);
-                tmem_ld_wait(ta);
-                tmem_ld32(tS + lane_off + 1 * 32, tb);
-                chunk(0, ta);
-                tmem_ld_wait(tb);
-                tmem_ld32(tS + lane_off + 2 * 32, ta);
-                chunk(1, tb);
-                tmem_ld_wait(ta);
-                tmem_ld32(tS + lane_off + 3 * 32, tb);
-                chunk(2, ta);
-                tmem_ld_wait(tb);
-                chunk(3, tb);
-                rsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-                const float mraw = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
-                mxo = mraw == -INFINITY ? -INFINITY : to_log2(capc, mraw);
-            };
-            auto run_tile = [&](auto capc, auto maskc) {
-                // rows that have seen no key yet take this tile's max as their reference
-                if (__any_sync(0xffffffffu, l == 0.f)) {
-                    const float mt = max_pass(capc, maskc);
-                    if (l == 0.f) m_used = fmaxf(m_used, mt);
+            uint32_t ta[32], tb[32];
+            tmem_ld32(tS + lane_off + 0 * 32, ta);
+            tmem_ld_wait(ta);
+            tmem_ld32(tS + lane_off + 1 * 32, tb);
+            chunk(0, ta);
+            tmem_ld_wait(tb);
+            tmem_ld32(tS + lane_off + 2 * 32, ta);
+            chunk(1, tb);
+            tmem_ld_wait(ta);
+            tmem_ld32(tS + lane_off + 3 * 32, tb);
+            chunk(2, ta);
+            tmem_ld_wait(tb);
+            chunk(3, tb);
+            rsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+            xmax = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+        };
+        // One pass against the row's reference m (log2 units, starting at 0).  The
+        // reference moves only when P would leave [2^-2, 2^8] at the row max: a max
+        // above 2^8 (any tile), or a first tile whose max is below 2^-2.  Then O is
+        // rescaled, the reference moved to the max and the tile redone from the
+        // scores still in TMEM; for ordinary inputs this never happens.
+        auto run_tile = [&](auto capc, float& m_used, float& l, int k) {
+            float rs, xm;
+            p_pass(capc, m_used, rs, xm);
+            const bool resc = xm > kRescaleHi || (l == 0.f && xm < kRescaleLo && xm != -INFINITY);
+            if (__any_sync(0xffffffffu, resc)) {
+                // S_u(k) completed after P_u(k-1) V(k-1): O_u holds every earlier tile.
+                // Rows that have seen nothing yet hold O = 0 and keep alpha = 1 (their
+                // reference may move down by any amount).
+                const float alpha = fast_exp2(resc && l > 0.f ? -xm : 0.f);
+                if (resc) {
+                    m_used += xm;
+                    l *= alpha;
                 }
-                // one pass against the running reference max; if some row's max grew
-                // by more than 2^8 (rare), rescale O, move the reference and redo the tile
-                float rs, mx;
-                p_pass(capc, maskc, m_used == -INFINITY ? 0.f : m_used, rs, mx);
-                const bool resc = l > 0.f && mx > m_used + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, resc)) {
-                    // S_u(k) completed after P_u(k-1) V(k-1): O_u already holds it
-                    const float alpha = fast_exp2(resc ? m_used - mx : 0.f);
-                    if (resc) {
-                        m_used = mx;
-                        l *= alpha;
-                    }
+                if (k > 0) {
 #pragma unroll 1
                     for (int c = 0; c < HD / 32; ++c) {
                         uint32_t orr[32];
@@ -405,58 +438,99 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
                         tmem_st32(tO + lane_off + c * 32, orr);
                     }
-                    // S is still intact in TMEM: recompute this tile's P against the new max
-                    p_pass(capc, maskc, m_used == -INFINITY ? 0.f : m_used, rs, mx);
                 }
-                l += rs;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_st16(tS + lane_off + c * 16, pk[c]);
-            };
-            using TT = std::integral_constant<bool, true>;
-            using FF = std::integral_constant<bool, false>;
-            if (cap) {
-                if (full) run_tile(TT(), FF());
-                else run_tile(TT(), TT());
-            } else {
-                if (full) run_tile(FF(), FF());
-                else run_tile(FF(), TT());
+                p_pass(capc, m_used, rs, xm);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(P_FULL(u)));
-        }
-        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-        const bool row_ok = i < P.Tq;
-        T* orow = reinterpret_cast<T*>(P.o) + ((long long)b * P.Tq + (row_ok ? i : 0)) * (long long)P.H * HD +
-                  (long long)h * HD;
-        const bool have_o = ok && my.ntiles > 0 && wait_warp(O_DONE(u), (my.ntiles - 1) & 1);
-        if (have_o) tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+            l += rs;
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-            uint32_t orr[32];
-            if (have_o) {
-                tmem_ld32(tO + lane_off + c * 32, orr);
-                tmem_ld_wait(orr);
-            } else {
+            for (int c = 0; c < 4; ++c) tmem_st16(tS + lane_off + c * 16, pk[c]);
+        };
+        for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
+            const FwdItem it = fwd_item(P, w);
+            const int ib = it.i0 + u * BM;  // first row of this tile
+            if (ib >= P.Tq) continue;
+            const int i = ib + r;
+            const int p = i + P.q_offset;
+            const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, P.Tq) - 1 + P.q_offset;
+            const TileInfo my = it.tu[u];
+            float m_used = 0.f, l = 0.f;
+            for (int k = 0; k < my.ntiles; ++k) {
+                const int j0 = (my.t0 + k) * BN;
+                const bool full = tile_full(P.causal, P.window, P.Tk, prow0, prow1, j0, j0 + BN) && !P.key_mask;
+                uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+                if (P.key_mask) {
+                    const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) orr[e] = 0u;
+                    for (int c = 0; c < 4; ++c) {
+                        const int j = j0 + c * 32 + lane;
+                        mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
+                    }
+                }
+                // this row's visible columns of the tile: [clo, chi), and the key-mask bits
+                int clo = 0, chi = BN;
+                if (!full) {
+                    chi = min(chi, P.Tk - j0);
+                    if (P.causal) chi = min(chi, p - j0 + 1);
+                    if (P.window > 0) {
+                        clo = max(clo, p - P.window + 1 - j0);
+                        if (!P.causal) chi = min(chi, p + P.window - j0);
+                    }
+                }
+                if (!wait_warp(S_FULL(u), sc & 1)) {
+                    ok = false;
+                    break;
+                }
+                ++sc;
+                tc_fence_after();
+                if (!full) mask_tile(clo, chi, mbits);
+                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k);
+                else run_tile(std::integral_constant<bool, false>(), m_used, l, k);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(P_FULL(u)));
             }
-            if (row_ok && (have_o || my.ntiles == 0)) {
-                uint32_t packed[16];
+            using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+            const bool row_ok = i < P.Tq;
+            T* orow = reinterpret_cast<T*>(P.o) + ((long long)it.b * P.Tq + (row_ok ? i : 0)) * (long long)P.H * HD +
+                      (long long)it.h * HD;
+            const bool have_o = ok && my.ntiles > 0 && wait_warp(O_DONE(u), act & 1);
+            if (my.ntiles > 0) ++act;
+            if (have_o) tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint32_t packed[HD / 2];
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                uint32_t orr[32];
+                if (have_o) {
+                    tmem_ld32(tO + lane_off + c * 32, orr);
+                    tmem_ld_wait(orr);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) orr[e] = 0u;
+                }
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    packed[e] = pack2<BF16>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
-                uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+                    packed[c * 16 + e] =
+                        pack2<BF16>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
             }
+            // O_u is in registers: the next item's first P.V may overwrite it
+            if (have_o) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(O_EMPTY(u)));
+            }
+            if (row_ok && (have_o || my.ntiles == 0)) {
+                uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+                for (int e = 0; e < HD / 8; ++e)
+                    dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+                if (P.lse)
+                    P.lse[((long long)it.b * P.H + it.h) * P.Tq + i] =
+                        l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            }
+            if (!ok) break;
         }
-        if (row_ok && P.lse && (have_o || my.ntiles == 0))
-            P.lse[((long long)b * P.H + h) * P.Tq + i] =
-                l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
     tc_fence_before();
     __syncthreads();
@@ -472,7 +546,12 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     auto kern = fwd_tc2_kernel<BF16, HD>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((p.Tq + 2 * BM - 1) / (2 * BM)) * p.H * p.B;
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // persistent: one CTA per SM (one fits), each walks items blockIdx.x, +grid, ...
+    const long long items = (long long)((p.Tq + 2 * BM - 1) / (2 * BM)) * p.H * p.B;
+    const unsigned grid = (unsigned)(items < nsm ? items : nsm);
     kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v);
     return cudaGetLastError();
 }

@@ -42,6 +42,28 @@ def test_fwd_fp32(hd, flags):
     run_fwd_case("f32", 1, Tq, Tk, 2, 1, hd, seed=200 + hd, **flags)
 
 
+# More work items (256-row query blocks x heads x batch) than the GPU has SMs, so
+# every CTA of the persistent forward runs several items back to back with
+# different key ranges, masks and tile activity.
+MULTI_ITEM_FLAGS = [
+    dict(causal=True),
+    dict(causal=True, window=200, softcap=30.0),
+    dict(causal=False, mask="holes"),
+    dict(causal=True, q_offset=100, window=300),
+]
+
+
+@pytest.mark.parametrize("flags", MULTI_ITEM_FLAGS, ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_fwd_many_items_per_cta(flags):
+    Tq = 520  # 3 query blocks, the last one ragged (8 rows, tile B empty)
+    Tk = Tq + flags.get("q_offset", 0)
+    run_fwd_case("bf16", 4, Tq, Tk, 32, 8, 128, seed=150, **flags)
+
+
+def test_fwd_many_items_hd64_f16():
+    run_fwd_case("f16", 3, 700, 700, 24, 4, 64, causal=True, window=333, seed=151)
+
+
 def test_fp32_causal_workload_full():
     """B=1, H=Hkv=1, T=128, hd=64, scale=1/8, causal, fp32."""
     run_fwd_case("f32", 1, 128, 128, 1, 1, 64, causal=True, seed=0x5EED0001)
