@@ -202,7 +202,8 @@ attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v,
     FwdMaps maps;
     if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
         !make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 128) ||
-        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128))
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128) ||
+        !make_map(&maps.o, dt, o, (long long)H * hd, Tq, B, 32))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_fwd(p, (int)dt, maps, s), 1);
 }

@@ -254,10 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
             uint32_t pk[32], dk[32];
-            // branch-free element loop; the softcap choice is made once per tile
-            auto elems = [&](auto capc, auto maskc) {
+            // In a tile where some pair is invisible, those scores become -inf first, so
+            // every tile runs one copy of the element loop (a rarely run second copy
+            // would be fetched into the instruction cache cold each time).
+            const bool full = key_live && clo <= 0 && chi >= BQ;
+            if (!__all_sync(0xffffffffu, full)) {
+#pragma unroll
+                for (int cc = 0; cc < BQ; ++cc)
+                    sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi) ? sv[cc >> 5][cc & 31] : 0xff800000u;
+            }
+            auto elems = [&](auto capc) {
                 constexpr bool kCap = decltype(capc)::value;
-                constexpr bool kMask = decltype(maskc)::value;
 #pragma unroll
                 for (int c = 0; c < BQ; c += 2) {
                     float pv[2], dv[2];
@@ -267,13 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
                         float x, dcap = 1.f;
                         if constexpr (kCap) {
+                            // softcap*tanh(-inf) would be finite: keep a masked score at -inf
                             const float t = tanh_accurate(sval * cap_in);
-                            x = P.softcap * t * kLog2e - st_l[cc];
+                            x = sval == -INFINITY ? -INFINITY : P.softcap * t * kLog2e - st_l[cc];
                             dcap = 1.f - t * t;
                         } else {
                             x = fmaf(sval, P.scale_log2, -st_l[cc]);
                         }
-                        if constexpr (kMask) x = (cc >= clo && cc < chi) ? x : -INFINITY;
                         const float p = fast_exp2(x);
                         pv[e] = p;
                         dv[e] = p * (__uint_as_float(dp[cc >> 5][cc & 31]) - st_d[cc]) * dcap;
@@ -282,18 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
                 }
             };
-            // every (query, key) pair of the tile visible: skip the per-element tests
-            const bool full = key_live && clo <= 0 && chi >= BQ;
-            const bool full_w = __all_sync(0xffffffffu, full);
-            using TT = std::integral_constant<bool, true>;
-            using FF = std::integral_constant<bool, false>;
-            if (cap) {
-                if (full_w) elems(TT(), FF());
-                else elems(TT(), TT());
-            } else {
-                if (full_w) elems(FF(), FF());
-                else elems(FF(), TT());
-            }
+            if (cap) elems(std::integral_constant<bool, true>());
+            else elems(std::integral_constant<bool, false>());
             tmem_st32(tbase + lane_off + bf * 64, pk);
             tmem_st32(tbase + lane_off + 128 + bf * 64, dk);
             tmem_st_wait();
@@ -593,9 +590,17 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
             uint32_t dsk[32];
-            auto elems = [&](auto capc, auto maskc) {
+            // invisible pairs become -inf scores first: one copy of the element loop
+            const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= BK;
+            if (!__all_sync(0xffffffffu, full)) {
+#pragma unroll
+                for (int cc = 0; cc < BK; ++cc)
+                    sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u))
+                                               ? sv[cc >> 5][cc & 31]
+                                               : 0xff800000u;
+            }
+            auto elems = [&](auto capc) {
                 constexpr bool kCap = decltype(capc)::value;
-                constexpr bool kMask = decltype(maskc)::value;
 #pragma unroll
                 for (int c = 0; c < BK; c += 2) {
                     float dv[2];
@@ -605,32 +610,21 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                         const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
                         float x, dcap = 1.f;
                         if constexpr (kCap) {
+                            // softcap*tanh(-inf) would be finite: keep a masked score at -inf
                             const float t = tanh_accurate(sval * cap_in);
-                            x = P.softcap * t * kLog2e - lse2;
+                            x = sval == -INFINITY ? -INFINITY : P.softcap * t * kLog2e - lse2;
                             dcap = 1.f - t * t;
                         } else {
                             x = fmaf(sval, P.scale_log2, -lse2);
                         }
-                        if constexpr (kMask)
-                            x = (cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u)) ? x : -INFINITY;
                         const float pr = fast_exp2(x);
                         dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
                     }
                     dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
                 }
             };
-            // every (query, key) pair of the tile visible: skip the per-element tests
-            const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= BK;
-            const bool full_w = __all_sync(0xffffffffu, full);
-            using TT = std::integral_constant<bool, true>;
-            using FF = std::integral_constant<bool, false>;
-            if (cap) {
-                if (full_w) elems(TT(), FF());
-                else elems(TT(), TT());
-            } else {
-                if (full_w) elems(FF(), FF());
-                else elems(FF(), TT());
-            }
+            if (cap) elems(std::integral_constant<bool, true>());
+            else elems(std::integral_constant<bool, false>());
             tmem_st32(tbase + lane_off + bf * 64, dsk);
             tmem_st_wait();
             tc_fence_before();

@@ -78,7 +78,10 @@ struct Fwd2Cfg {
     static constexpr int kVOff = kKOff + kStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kStages * kKVBytes;
     static constexpr int kNumBars = 13 + 4 * kStages;
-    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+    // epilogue staging: one 32-row x 64-column slice (4 KB) per softmax warp
+    static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
+    static constexpr int kStgBytes = 8 * 32 * 128;
+    static constexpr int kBytes = kStgOff + kStgBytes;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
@@ -123,7 +126,7 @@ __device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * B
 template <bool BF16, int HD>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
     using C = Fwd2Cfg<HD>;
     constexpr int NS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -350,19 +353,32 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // are overwritten with -inf in TMEM first, so every tile then runs the same
         // softmax code (one hot copy of the unrolled loop instead of one per case).
         auto mask_tile = [&](int clo, int chi, const uint32_t(&mbits)[4]) {
-#pragma unroll 1
+            // visibility bits of columns 32c .. 32c+31: [clo, chi) and the key mask
+            uint32_t vw[4];
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t t[32];
-                tmem_ld32(tS + lane_off + c * 32, t);
-                tmem_ld_wait(t);
-                const uint32_t mw = mbits[0] * (c == 0) | mbits[1] * (c == 1) | mbits[2] * (c == 2) | mbits[3] * (c == 3);
+                const int lo = min(max(clo - 32 * c, 0), 32), hi = min(max(chi - 32 * c, 0), 32);
+                const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+                const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
+                vw[c] = below_hi & ~below_lo & mbits[c];
+            }
+            // two 32-column chunks per step, both loads in flight together
+#pragma unroll 1
+            for (int c = 0; c < 4; c += 2) {
+                uint32_t t0[32], t1[32];
+                tmem_ld32(tS + lane_off + c * 32, t0);
+                tmem_ld32(tS + lane_off + c * 32 + 32, t1);
+                tmem_ld_wait_only();
+                tmem_pin(t0);
+                tmem_pin(t1);
+                const uint32_t w0 = c == 0 ? vw[0] : vw[2], w1 = c == 0 ? vw[1] : vw[3];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int col = c * 32 + e;
-                    const bool v = col >= clo && col < chi && ((mw >> e) & 1u);
-                    t[e] = v ? t[e] : 0xff800000u;  // -inf
+                    t0[e] = ((w0 >> e) & 1u) ? t0[e] : 0xff800000u;  // -inf
+                    t1[e] = ((w1 >> e) & 1u) ? t1[e] : 0xff800000u;
                 }
-                tmem_st32(tS + lane_off + c * 32, t);
+                tmem_st32(tS + lane_off + c * 32, t0);
+                tmem_st32(tS + lane_off + c * 32 + 32, t1);
             }
             tmem_st_wait();
         };
@@ -490,10 +506,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(P_FULL(u)));
             }
-            using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-            const bool row_ok = i < P.Tq;
-            T* orow = reinterpret_cast<T*>(P.o) + ((long long)it.b * P.Tq + (row_ok ? i : 0)) * (long long)P.H * HD +
-                      (long long)it.h * HD;
             const bool have_o = ok && my.ntiles > 0 && wait_warp(O_DONE(u), act & 1);
             if (my.ntiles > 0) ++act;
             if (have_o) tc_fence_after();
@@ -520,17 +532,37 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(O_EMPTY(u)));
             }
-            if (row_ok && (have_o || my.ntiles == 0)) {
-                uint4* dst = reinterpret_cast<uint4*>(orow);
+            if (ok && (have_o || my.ntiles == 0)) {
+                // This warp's 32 rows go out through its 4 KB staging slice, 64 columns
+                // at a time, in the 128-byte-swizzled layout of the tensor map's box;
+                // one lane issues the tiled store (rows past Tq are not written).
+                const uint32_t slice = sbase + C::kStgOff + (u * 4 + wq) * 4096;
 #pragma unroll
-                for (int e = 0; e < HD / 8; ++e)
-                    dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
-                if (P.lse)
+                for (int half = 0; half < HD / 64; ++half) {
+                    if (elect_one()) bulk_wait_read_all();  // the slice's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int w4 = half * 32 + 4 * j;
+                        st_shared_v4(slice + lane * 128 + ((j ^ (lane & 7)) << 4), packed[w4], packed[w4 + 1],
+                                     packed[w4 + 2], packed[w4 + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (elect_one()) {
+                        tma_store_3d(&tmO, slice, it.h * HD + half * 64, ib + wq * 32, it.b);
+                        bulk_commit_group();
+                    }
+                }
+                if (P.lse && i < P.Tq)
                     P.lse[((long long)it.b * P.H + it.h) * P.Tq + i] =
                         l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
             }
             if (!ok) break;
         }
+        // the staging slice must stay until this warp's last store has read it
+        if (elect_one()) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -552,7 +584,7 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     // persistent: one CTA per SM (one fits), each walks items blockIdx.x, +grid, ...
     const long long items = (long long)((p.Tq + 2 * BM - 1) / (2 * BM)) * p.H * p.B;
     const unsigned grid = (unsigned)(items < nsm ? items : nsm);
-    kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v);
+    kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v, m.o);
     return cudaGetLastError();
 }
 

@@ -17,6 +17,7 @@ cudaError_t launch_bwd_preprocess(const Params& p, int dt, cudaStream_t s);
 // maps are built by the caller.
 struct FwdMaps {
     CUtensorMap q, k, v;
+    CUtensorMap o;  // 32-row boxes, for the epilogue's stores
 };
 cudaError_t launch_tc_fwd(const Params& p, int dt, const FwdMaps& maps, cudaStream_t s);
 struct BwdMaps {
