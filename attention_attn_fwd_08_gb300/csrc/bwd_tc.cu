@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===================================================================== dQ
 template <int HD>
 struct QCfg {
-    static constexpr int BQ = 128;  // query rows per CTA
+    static constexpr int BQ = 128;  // query rows per item
     static constexpr int BK = 64;   // keys per inner tile
     static constexpr int kBoxes = HD / 64;
     static constexpr int kStages = HD == 128 ? 3 : 4;
@@ -355,15 +355,45 @@ struct QCfg {
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKBytes;
     static constexpr int kBarOff = kVOff + kStages * kKBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1 + 1;
-    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kNumBars = 8 + 2 * kStages + 4;
+    // epilogue staging: one 32-row x 64-column slice (4 KB) per compute warp
+    static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
+    static constexpr int kBytes = kStgOff + 4 * 4096;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
+// One dQ work item: 128 query rows of one (batch, head) and the key tiles they
+// see.  Items are numbered longest first (every head's last query block first).
+struct DqItem {
+    int b, h, kvh, i0, kt0, ntiles;
+};
+template <int BQ, int BK>
+__device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
+    DqItem it;
+    const int nqb = (P.Tq + BQ - 1) / BQ;
+    const int hb = w % (P.H * P.B);
+    const int qb = nqb - 1 - w / (P.H * P.B);
+    it.h = hb % P.H;
+    it.b = hb / P.H;
+    it.kvh = it.h / P.G;
+    it.i0 = qb * BQ;
+    int lo, hi;
+    key_range(P.causal, P.window, P.Tk, it.i0 + P.q_offset, min(it.i0 + BQ, P.Tq) - 1 + P.q_offset, &lo, &hi);
+    it.kt0 = lo / BK;
+    it.ntiles = hi > lo ? (hi + BK - 1) / BK - it.kt0 : 0;
+    return it;
+}
+
+// Persistent: one CTA per SM walks the items blockIdx.x, +gridDim.x, ...  The
+// K/V ring and every barrier phase run on across items.  The next item's Q and dO
+// are loaded into shared memory once the current ones are in TMEM, and copied
+// into TMEM right after the current item's last dS, so its first S and dP run
+// while the current item's epilogue reads dQ out.
 template <bool BF16, int HD>
 __global__ void __launch_bounds__(kThreadsDQ, 1)
     bwd_dq_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                  const __grid_constant__ CUtensorMap tmDQ) {
     using C = QCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BK = C::BK;
     extern __shared__ uint8_t smem_raw[];
@@ -374,31 +404,24 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     __shared__ int abort_flag;
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    const int QG_FULL = 0;
-    auto KV_FULL = [&](int s) { return 1 + s; };
-    auto KV_EMPTY = [&](int s) { return 1 + NS + s; };
-    auto ST_FULL = [&](int b) { return 1 + 2 * NS + b; };
-    auto DS_FULL = [&](int b) { return 3 + 2 * NS + b; };
-    const int ACC_DONE = 5 + 2 * NS;
-    const int QT_READY = 7 + 2 * NS;  // Q and dO copied into TMEM (A operands)
-    const int MMA_DONE = 6 + 2 * NS;
+    const int QG_FULL = 0;   // Q and dO of an item in shared memory
+    const int QG_EMPTY = 1;  // ... copied into TMEM (4 compute warps)
+    const int QT_READY = 2;  // Q and dO of an item in TMEM (A operands; 4 warps)
+    const int DQ_DONE = 3;   // the item's last dQ MMA completed
+    const int DQ_EMPTY = 4;  // the epilogue has read dQ out of TMEM (4 warps)
+    const int MMA_DONE = 5;
+    auto ST_FULL = [&](int b) { return 6 + b; };  // S and dP of a tile (two issuers)
+    auto DS_FULL = [&](int b) { return 8 + b; };  // dS of a tile (4 warps)
+    auto KV_FULL = [&](int s) { return 10 + s; };
+    auto KV_EMPTY = [&](int s) { return 10 + NS + s; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nqb = (P.Tq + BQ - 1) / BQ;
-    // 1-D grid, longest first: every head's last (causally heaviest) query block first
-    const int hb = (int)(blockIdx.x % (unsigned)(P.H * P.B));
-    const int qb = nqb - 1 - (int)(blockIdx.x / (unsigned)(P.H * P.B));
-    const int h = hb % P.H, b = hb / P.H, kvh = h / P.G;
-    const int i0 = qb * BQ;
-    int lo, hi;
-    key_range(P.causal, P.window, P.Tk, i0 + P.q_offset, min(i0 + BQ, P.Tq) - 1 + P.q_offset, &lo, &hi);
-    const int kt0 = lo / BK;
-    const int ntiles = hi > lo ? (hi + BK - 1) / BK - kt0 : 0;
+    const int nitems = (P.Tq + BQ - 1) / BQ * P.H * P.B;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == DS_FULL(0) || i == DS_FULL(1) || i == QT_READY) count = 4;
+            if (i == DS_FULL(0) || i == DS_FULL(1) || i == QT_READY || i == QG_EMPTY || i == DQ_EMPTY) count = 4;
             if (i == ST_FULL(0) || i == ST_FULL(1) || i == MMA_DONE) count = 2;  // two MMA issuers
             for (int s2 = 0; s2 < NS; ++s2)
                 if (i == KV_EMPTY(s2)) count = 2;
@@ -422,221 +445,272 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 
     if (warp == 4) {
         // producer and MMA issuers run as whole warps; one elected lane issues
-        if (ntiles > 0) {
-            if (elect_one()) {
-                prefetch_tmap(&tmQ);
-                prefetch_tmap(&tmK);
-                prefetch_tmap(&tmV);
-                prefetch_tmap(&tmG);
-            }
+        if (elect_one()) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            prefetch_tmap(&tmG);
+        }
+        bool ok = true;
+        int qn = 0, g = 0;  // Q/dO loads and K/V tiles loaded so far
+        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+            const DqItem it = dq_item<BQ, BK>(P, w);
+            if (it.ntiles == 0) continue;
+            if (qn > 0 && !warp_wait(BAR(QG_EMPTY), (qn - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) break;
             if (elect_one()) mbar_expect_tx(BAR(QG_FULL), 2 * C::kQBytes);
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
                 if (elect_one())
-                    tma_load_3d(sbase + C::kQOff + bx * (BQ * 128), &tmQ, BAR(QG_FULL), h * HD + bx * 64, i0, b);
+                    tma_load_3d(sbase + C::kQOff + bx * (BQ * 128), &tmQ, BAR(QG_FULL), it.h * HD + bx * 64, it.i0,
+                                it.b);
                 if (elect_one())
-                    tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), h * HD + bx * 64, i0, b);
+                    tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), it.h * HD + bx * 64, it.i0,
+                                it.b);
             }
-            int issued = 0;
-            for (int n = 0; n < ntiles; ++n) {
-                const int s = n % NS, use = n / NS;
-                if (use > 0 && !warp_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
+            ++qn;
+            for (int n = 0; n < it.ntiles; ++n) {
+                const int s = g % NS, use = g / NS;
+                if (use > 0 && !warp_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) {
+                    ok = false;
                     break;
-                const int jt = (kt0 + n) * BK;
+                }
+                const int jt = (it.kt0 + n) * BK;
                 if (elect_one()) mbar_expect_tx(BAR(KV_FULL(s)), 2 * C::kKBytes);
 #pragma unroll
                 for (int bx = 0; bx < C::kBoxes; ++bx) {
                     if (elect_one())
                         tma_load_3d(sbase + C::kKOff + s * C::kKBytes + bx * (BK * 128), &tmK, BAR(KV_FULL(s)),
-                                    kvh * HD + bx * 64, jt, b);
+                                    it.kvh * HD + bx * 64, jt, it.b);
                     if (elect_one())
                         tma_load_3d(sbase + C::kVOff + s * C::kKBytes + bx * (BK * 128), &tmV, BAR(KV_FULL(s)),
-                                    kvh * HD + bx * 64, jt, b);
+                                    it.kvh * HD + bx * 64, jt, it.b);
                 }
-                issued = n + 1;
+                ++g;
             }
-            mbar_wait(BAR(QG_FULL), 0, P.status, ST_TEARDOWN, nullptr);
-            for (int n = max(0, issued - NS); n < issued; ++n)
-                mbar_wait(BAR(KV_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
+        // every copy in flight lands before the CTA exits
+        if (qn > 0) mbar_wait(BAR(QG_FULL), (qn - 1) & 1, P.status, ST_TEARDOWN, nullptr);
+        for (int n = max(0, g - NS); n < g; ++n)
+            mbar_wait(BAR(KV_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
     } else if (warp == 5 || warp == 6) {
         // Two MMA issuers, so that one's barrier waits overlap the other's issue:
         // warp 5 issues S and dQ (the dS of tile n sits over S(n), so S(n+2) must
         // follow dQ(n) in one stream), warp 6 issues dP.  ST_FULL, KV_EMPTY and
-        // MMA_DONE count both.
+        // MMA_DONE count both.  Tiles are numbered across items (gt): ring slot
+        // gt % NS, S/dP buffer gt & 1.
         const bool issues_dp = warp == 6;
-        if (ntiles > 0) {
-            constexpr uint32_t idS = idesc_f16(BF16, BQ, BK, false, false);
-            constexpr uint32_t idAcc = idesc_f16(BF16, BQ, HD, false, true);
-            bool ok = warp_wait(BAR(QT_READY), 0, P.status, ST_BWD_MMA, &abort_flag);
-            // S(n) = Q K_n^T (warp 5) or dP(n) = dO V_n^T (warp 6) into buffer n & 1
-            auto issue_one = [&](int n) -> bool {
-                const int s = n % NS, bf = n & 1;
-                if (!warp_wait(BAR(KV_FULL(s)), (n / NS) & 1, P.status, ST_BWD_MMA, &abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t src = sbase + (issues_dp ? C::kVOff : C::kKOff) + s * C::kKBytes;
-                const uint64_t bdesc = sdesc_sw128(src, 16, 1024);
-                const uint32_t d = tbase + (issues_dp ? 128 : 0) + bf * 64;
-                const uint32_t a = issues_dp ? tG : tQ;
+        constexpr uint32_t idS = idesc_f16(BF16, BQ, BK, false, false);
+        constexpr uint32_t idAcc = idesc_f16(BF16, BQ, HD, false, true);
+        auto wait_all = [&](int bar, uint32_t parity) -> bool {
+            return warp_wait(BAR(bar), parity, P.status, ST_BWD_MMA, &abort_flag);
+        };
+        // S(t) = Q K_t^T (warp 5) or dP(t) = dO V_t^T (warp 6) into buffer t & 1
+        auto issue_one = [&](int t) -> bool {
+            const int s = t % NS, bf = t & 1;
+            if (!wait_all(KV_FULL(s), (t / NS) & 1)) return false;
+            tc_fence_after();
+            const uint32_t src = sbase + (issues_dp ? C::kVOff : C::kKOff) + s * C::kKBytes;
+            const uint64_t bdesc = sdesc_sw128(src, 16, 1024);
+            const uint32_t d = tbase + (issues_dp ? 128 : 0) + bf * 64;
+            const uint32_t a = issues_dp ? tG : tQ;
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
-                    if (elect_one()) mma_ts(d, a + kk * 8, bdesc + boff, idS, kk > 0 ? 1u : 0u);
-                }
-                if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
-                return true;
-            };
-            if (ok) ok = issue_one(0);
-            if (ok && ntiles > 1) ok = issue_one(1);
-            for (int n = 0; ok && n < ntiles; ++n) {
-                const int s = n % NS, bf = n & 1;
-                // tile n's dS is written (and its S, dP read) once DS_FULL completes
-                if (!warp_wait(BAR(DS_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_MMA, &abort_flag)) {
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
+                if (elect_one()) mma_ts(d, a + kk * 8, bdesc + boff, idS, kk > 0 ? 1u : 0u);
+            }
+            if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
+            return true;
+        };
+        bool ok = true;
+        int gt = 0, act = 0;
+        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+            const DqItem it = dq_item<BQ, BK>(P, w);
+            if (it.ntiles == 0) continue;
+            ok = wait_all(QT_READY, act & 1);
+            if (ok) ok = issue_one(gt);
+            if (ok && it.ntiles > 1) ok = issue_one(gt + 1);
+            for (int n = 0; ok && n < it.ntiles; ++n) {
+                const int t = gt + n, s = t % NS, bf = t & 1;
+                // tile t's dS is written (and its S, dP read) once DS_FULL completes
+                if (!wait_all(DS_FULL(bf), (t >> 1) & 1)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 if (!issues_dp) {
-                    const uint32_t ka = sbase + C::kKOff + s * C::kKBytes;
-                    const uint64_t kdesc = sdesc_sw128(ka, BK * 128, 1024);
+                    // the first dQ MMA overwrites the accumulator: the previous item's
+                    // epilogue must have read it
+                    if (n == 0 && act > 0 && !wait_all(DQ_EMPTY, (act - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t kdesc = sdesc_sw128(sbase + C::kKOff + s * C::kKBytes, BK * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         if (elect_one())
                             mma_ts(tDQ, tbase + bf * 64 + kk * 8, kdesc + ((kk * 2048) >> 4), idAcc,
                                    (n > 0 || kk > 0) ? 1u : 0u);
+                } else {
+                    tc_fence_after();
                 }
                 if (elect_one()) mma_commit(BAR(KV_EMPTY(s)));
-                if (n + 2 < ntiles) ok = issue_one(n + 2);
+                if (n + 2 < it.ntiles) ok = issue_one(t + 2);
             }
-            if (ok && !issues_dp && elect_one()) mma_commit(BAR(ACC_DONE));
-            if (elect_one()) mma_commit(BAR(MMA_DONE));
-            mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
+            if (ok && !issues_dp && elect_one()) mma_commit(BAR(DQ_DONE));
+            gt += it.ntiles;
+            ++act;
         }
+        if (elect_one()) mma_commit(BAR(MMA_DONE));
+        mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
     } else {
         // ----------------------------------------- compute: one query row per thread
         const int r = warp * 32 + lane;
-        const int i = i0 + r;
-        const int p = i + P.q_offset;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const bool row_ok = i < P.Tq;
-        float lse2 = INFINITY, Dd = 0.f;
-        if (row_ok) {
-            lse2 = P.lse2[((long long)b * P.H + h) * P.tq_pad + i];
-            Dd = P.delta[((long long)b * P.H + h) * P.tq_pad + i];
-        }
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         bool ok = true;
-        if (ntiles > 0) {
-            // copy this thread's rows of Q and dO (128-byte-swizzled smem) into TMEM
-            ok = warp_wait(BAR(QG_FULL), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
-            if (ok) {
+        int gt = 0, act = 0, qc = 0;  // tiles, active items and Q/dO copies so far
+        int copied = -1;              // item whose Q and dO are in TMEM
+        // copy this thread's rows of Q and dO (128-byte-swizzled smem) into TMEM
+        auto copy_q = [&](int w2) -> bool {
+            if (!warp_wait(BAR(QG_FULL), qc & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) return false;
+            ++qc;
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const uint8_t* src = smem + (t == 0 ? C::kQOff : C::kGOff);
+            for (int t = 0; t < 2; ++t) {
+                const uint8_t* src = smem + (t == 0 ? C::kQOff : C::kGOff);
 #pragma unroll
-                    for (int half = 0; half < HD / 64; ++half) {
-                        uint32_t w[32];
+                for (int half = 0; half < HD / 64; ++half) {
+                    uint32_t wv[32];
 #pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            const uint4 v4 = *reinterpret_cast<const uint4*>(
-                                src + half * (BQ * 128) + r * 128 + ((ch ^ (r & 7)) << 4));
-                            w[4 * ch] = v4.x;
-                            w[4 * ch + 1] = v4.y;
-                            w[4 * ch + 2] = v4.z;
-                            w[4 * ch + 3] = v4.w;
-                        }
-                        tmem_st32((t == 0 ? tQ : tG) + lane_off + half * 32, w);
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(src + half * (BQ * 128) + r * 128 +
+                                                                         ((ch ^ (r & 7)) << 4));
+                        wv[4 * ch] = v4.x;
+                        wv[4 * ch + 1] = v4.y;
+                        wv[4 * ch + 2] = v4.z;
+                        wv[4 * ch + 3] = v4.w;
                     }
-                }
-                tmem_st_wait();
-                tc_fence_before();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(QT_READY));
-        }
-        for (int n = 0; ok && n < ntiles; ++n) {
-            const int bf = n & 1;
-            const int jt = (kt0 + n) * BK;
-            uint32_t mbits[2] = {0xffffffffu, 0xffffffffu};
-            if (P.key_mask) {
-                const float* mrow = P.key_mask + (long long)b * P.mask_bstride;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int j = jt + c * 32 + lane;
-                    mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
+                    tmem_st32((t == 0 ? tQ : tG) + lane_off + half * 32, wv);
                 }
             }
-            int clo = 0, chi = min(BK, P.Tk - jt);
-            if (P.causal) chi = min(chi, p - jt + 1);
-            if (P.window > 0) {
-                clo = max(clo, p - P.window + 1 - jt);
-                if (!P.causal) chi = min(chi, p + P.window - jt);
-            }
-            if (!row_ok) chi = 0;
-            if (!warp_wait(BAR(ST_FULL(bf)), (n >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sv[2][32], dp[2][32];
-            tmem_ld32(tbase + lane_off + bf * 64, sv[0]);
-            tmem_ld32(tbase + lane_off + bf * 64 + 32, sv[1]);
-            tmem_ld32(tbase + lane_off + 128 + bf * 64, dp[0]);
-            tmem_ld32(tbase + lane_off + 128 + bf * 64 + 32, dp[1]);
-            tmem_ld_wait_only();
-            tmem_pin(sv[0]);
-            tmem_pin(sv[1]);
-            tmem_pin(dp[0]);
-            tmem_pin(dp[1]);
-            uint32_t dsk[32];
-            // invisible pairs become -inf scores first: one copy of the element loop
-            const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= BK;
-            if (!__all_sync(0xffffffffu, full)) {
-#pragma unroll
-                for (int cc = 0; cc < BK; ++cc)
-                    sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u))
-                                               ? sv[cc >> 5][cc & 31]
-                                               : 0xff800000u;
-            }
-            auto elems = [&](auto capc) {
-                constexpr bool kCap = decltype(capc)::value;
-#pragma unroll
-                for (int c = 0; c < BK; c += 2) {
-                    float dv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int cc = c + e;
-                        const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
-                        float x, dcap = 1.f;
-                        if constexpr (kCap) {
-                            // softcap*tanh(-inf) would be finite: keep a masked score at -inf
-                            const float t = tanh_accurate(sval * cap_in);
-                            x = sval == -INFINITY ? -INFINITY : P.softcap * t * kLog2e - lse2;
-                            dcap = 1.f - t * t;
-                        } else {
-                            x = fmaf(sval, P.scale_log2, -lse2);
-                        }
-                        const float pr = fast_exp2(x);
-                        dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
-                    }
-                    dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
-                }
-            };
-            if (cap) elems(std::integral_constant<bool, true>());
-            else elems(std::integral_constant<bool, false>());
-            tmem_st32(tbase + lane_off + bf * 64, dsk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(DS_FULL(bf)));
-        }
-        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-        const bool have = ok && ntiles > 0 && warp_wait(BAR(ACC_DONE), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
-        if (have) tc_fence_after();
-        if (ok) {
-            T* dst = reinterpret_cast<T*>(P.dq) + ((long long)b * P.Tq + (row_ok ? i : 0)) * (long long)P.H * HD +
-                     (long long)h * HD;
+            if (lane == 0) {
+                mbar_arrive(BAR(QG_EMPTY));
+                mbar_arrive(BAR(QT_READY));
+            }
+            copied = w2;
+            return true;
+        };
+        for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
+            const DqItem it = dq_item<BQ, BK>(P, w);
+            const int i = it.i0 + r;
+            const int p = i + P.q_offset;
+            const bool row_ok = i < P.Tq;
+            const int ntiles = it.ntiles;
+            float lse2 = INFINITY, Dd = 0.f;
+            if (row_ok && ntiles > 0) {
+                lse2 = P.lse2[((long long)it.b * P.H + it.h) * P.tq_pad + i];
+                Dd = P.delta[((long long)it.b * P.H + it.h) * P.tq_pad + i];
+            }
+            if (ntiles > 0 && copied != w) ok = copy_q(w);
+            for (int n = 0; ok && n < ntiles; ++n) {
+                const int t = gt + n, bf = t & 1;
+                const int jt = (it.kt0 + n) * BK;
+                uint32_t mbits[2] = {0xffffffffu, 0xffffffffu};
+                if (P.key_mask) {
+                    const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int j = jt + c * 32 + lane;
+                        mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
+                    }
+                }
+                int clo = 0, chi = min(BK, P.Tk - jt);
+                if (P.causal) chi = min(chi, p - jt + 1);
+                if (P.window > 0) {
+                    clo = max(clo, p - P.window + 1 - jt);
+                    if (!P.causal) chi = min(chi, p + P.window - jt);
+                }
+                if (!row_ok) chi = 0;
+                if (!warp_wait(BAR(ST_FULL(bf)), (t >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sv[2][32], dp[2][32];
+                tmem_ld32(tbase + lane_off + bf * 64, sv[0]);
+                tmem_ld32(tbase + lane_off + bf * 64 + 32, sv[1]);
+                tmem_ld32(tbase + lane_off + 128 + bf * 64, dp[0]);
+                tmem_ld32(tbase + lane_off + 128 + bf * 64 + 32, dp[1]);
+                tmem_ld_wait_only();
+                tmem_pin(sv[0]);
+                tmem_pin(sv[1]);
+                tmem_pin(dp[0]);
+                tmem_pin(dp[1]);
+                uint32_t dsk[32];
+                // invisible pairs become -inf scores first: one copy of the element loop
+                const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= BK;
+                if (!__all_sync(0xffffffffu, full)) {
+#pragma unroll
+                    for (int cc = 0; cc < BK; ++cc)
+                        sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u))
+                                                   ? sv[cc >> 5][cc & 31]
+                                                   : 0xff800000u;
+                }
+                auto elems = [&](auto capc) {
+                    constexpr bool kCap = decltype(capc)::value;
+#pragma unroll
+                    for (int c = 0; c < BK; c += 2) {
+                        float dv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int cc = c + e;
+                            const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
+                            float x, dcap = 1.f;
+                            if constexpr (kCap) {
+                                // softcap*tanh(-inf) would be finite: keep a masked score at -inf
+                                const float t = tanh_accurate(sval * cap_in);
+                                x = sval == -INFINITY ? -INFINITY : P.softcap * t * kLog2e - lse2;
+                                dcap = 1.f - t * t;
+                            } else {
+                                x = fmaf(sval, P.scale_log2, -lse2);
+                            }
+                            const float pr = fast_exp2(x);
+                            dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
+                        }
+                        dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
+                    }
+                };
+                if (cap) elems(std::integral_constant<bool, true>());
+                else elems(std::integral_constant<bool, false>());
+                tmem_st32(tbase + lane_off + bf * 64, dsk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(DS_FULL(bf)));
+            }
+            if (!ok) break;
+            // every S and dP of this item completed (their results were read above):
+            // put the next active item's Q and dO into TMEM before this epilogue
+            for (int w2 = w + (int)gridDim.x; ntiles > 0 && w2 < nitems; w2 += gridDim.x) {
+                if (dq_item<BQ, BK>(P, w2).ntiles == 0) continue;
+                ok = copy_q(w2);
+                break;
+            }
+            if (!ok) break;
+            // epilogue: dQ (x scale) of this row, zero when it sees no key
+            const bool have = ntiles > 0 && warp_wait(BAR(DQ_DONE), act & 1, P.status, ST_BWD_COMPUTE, &abort_flag);
+            if (ntiles > 0) {
+                if (!have) {
+                    ok = false;
+                    break;
+                }
+                ++act;
+                tc_fence_after();
+            }
+            uint32_t packed[HD / 2];
 #pragma unroll
             for (int c = 0; c < HD / 32; ++c) {
                 uint32_t acc[32];
@@ -647,19 +721,39 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) acc[e] = 0u;
                 }
-                if (row_ok && (have || ntiles == 0)) {
-                    uint32_t packed[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        packed[e] = pack2<BF16>(__uint_as_float(acc[2 * e]) * P.scale,
-                                                __uint_as_float(acc[2 * e + 1]) * P.scale);
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+                for (int e = 0; e < 16; ++e)
+                    packed[c * 16 + e] = pack2<BF16>(__uint_as_float(acc[2 * e]) * P.scale,
+                                                     __uint_as_float(acc[2 * e + 1]) * P.scale);
+            }
+            if (have) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(DQ_EMPTY));
+            }
+            // this warp's 32 rows leave through its staging slice, 64 columns at a time
+            const uint32_t slice = sbase + C::kStgOff + warp * 4096;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+            for (int half = 0; half < HD / 64; ++half) {
+                if (elect_one()) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int w4 = half * 32 + 4 * j;
+                    st_shared_v4(slice + lane * 128 + ((j ^ (lane & 7)) << 4), packed[w4], packed[w4 + 1],
+                                 packed[w4 + 2], packed[w4 + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (elect_one()) {
+                    tma_store_3d(&tmDQ, slice, it.h * HD + half * 64, it.i0 + warp * 32, it.b);
+                    bulk_commit_group();
                 }
             }
+            gt += ntiles;
         }
+        if (elect_one()) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -688,8 +782,13 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         auto k = bwd_dq_kernel<BF16, HD>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
-        const unsigned grid = (unsigned)((p.Tq + 127) / 128) * p.H * p.B;
-        k<<<grid, kThreadsDQ, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout);
+        int dev = 0, nsm = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        // persistent: one CTA per SM (one fits), each walks items blockIdx.x, +grid, ...
+        const long long items = (long long)((p.Tq + 127) / 128) * p.H * p.B;
+        const unsigned grid = (unsigned)(items < nsm ? items : nsm);
+        k<<<grid, kThreadsDQ, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout, m.dq32);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

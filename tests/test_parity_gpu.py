@@ -87,6 +87,15 @@ def test_bwd_16bit(dt, hd, flags):
     run_fwd_case(dt, 2, Tq, Tk, 4, 2, hd, backward=True, seed=300 + hd, **flags)
 
 
+# More dQ work items (128-row query blocks x heads x batch) than SMs: every CTA of
+# the persistent dQ kernel runs several items with different key ranges.
+@pytest.mark.parametrize("flags", [dict(causal=True), dict(causal=True, window=150, softcap=20.0),
+                                   dict(causal=False, mask="holes")],
+                         ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_bwd_many_items_per_cta(flags):
+    run_fwd_case("bf16", 4, 300, 300, 32, 8, 128, backward=True, seed=310, **flags)
+
+
 @pytest.mark.parametrize("flags", BWD_FLAGS[:3], ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
 def test_bwd_fp32(flags):
     Tq = 150
