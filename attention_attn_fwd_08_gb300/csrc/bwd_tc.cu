@@ -384,7 +384,7 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
     return it;
 }
 
-// Persistent: one CTA per SM walks the items blockIdx.x, +gridDim.x, ...  The
+// Persistent: one CTA per SM walks its items in snake order (snake_item).  The
 // K/V ring and every barrier phase run on across items.  The next item's Q and dO
 // are loaded into shared memory once the current ones are in TMEM, and copied
 // into TMEM right after the current item's last dS, so its first S and dP run
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         }
         bool ok = true;
         int qn = 0, g = 0;  // Q/dO loads and K/V tiles loaded so far
-        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+        for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
             const DqItem it = dq_item<BQ, BK>(P, w);
             if (it.ntiles == 0) continue;
             if (qn > 0 && !warp_wait(BAR(QG_EMPTY), (qn - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) break;
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         };
         bool ok = true;
         int gt = 0, act = 0;
-        for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
+        for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
             const DqItem it = dq_item<BQ, BK>(P, w);
             if (it.ntiles == 0) continue;
             ok = wait_all(QT_READY, act & 1);
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             copied = w2;
             return true;
         };
-        for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
+        for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
             const DqItem it = dq_item<BQ, BK>(P, w);
             const int i = it.i0 + r;
             const int p = i + P.q_offset;
@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             if (!ok) break;
             // every S and dP of this item completed (their results were read above):
             // put the next active item's Q and dO into TMEM before this epilogue
-            for (int w2 = w + (int)gridDim.x; ntiles > 0 && w2 < nitems; w2 += gridDim.x) {
+            for (int k2 = k_ + 1, w2 = snake_item(k2); ntiles > 0 && w2 < nitems; w2 = snake_item(++k2)) {
                 if (dq_item<BQ, BK>(P, w2).ntiles == 0) continue;
                 ok = copy_q(w2);
                 break;
@@ -785,7 +785,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         int dev = 0, nsm = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        // persistent: one CTA per SM (one fits), each walks items blockIdx.x, +grid, ...
+        // persistent: one CTA per SM (one fits); each walks its items in snake order
         const long long items = (long long)((p.Tq + 127) / 128) * p.H * p.B;
         const unsigned grid = (unsigned)(items < nsm ? items : nsm);
         k<<<grid, kThreadsDQ, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout, m.dq32);

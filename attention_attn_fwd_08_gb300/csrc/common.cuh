@@ -220,6 +220,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// The k-th work item of this CTA in a persistent kernel: rounds of gridDim.x
+// items taken alternately in CTA order and reversed, so that with items numbered
+// longest first each CTA pairs heavier items with lighter ones.
+__device__ __forceinline__ int snake_item(int k) {
+    const int g = (int)gridDim.x, c = (int)blockIdx.x;
+    return k * g + ((k & 1) ? g - 1 - c : c);
+}
+
 // Bounded wait by a whole warp; true only when every lane saw the phase.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned int* status, unsigned int code,
                                           volatile int* abort_flag) {
