@@ -35,8 +35,13 @@ namespace attn {
 namespace {
 
 constexpr int kThreads = 192;    // dK/dV: 4 compute warps, producer, MMA
-constexpr int kThreadsDQ = 224;  // dQ: 4 compute warps, producer, two MMA issuers
+constexpr int kThreadsDQ = 352;  // dQ: 8 compute warps, producer, two MMA issuers
 constexpr float kLog2e = 1.4426950408889634f;
+
+// TMEM column (within a 64-column tile buffer) of K-step kk's 16-bit dS operand
+// in the dQ kernel: the two compute warps of a row each pack their 32 columns
+// into the first 16 of them, so the 32 operand columns sit at 0..15 and 32..47.
+__device__ __forceinline__ uint32_t pcol(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
 
 // =============================================================== dK / dV
 template <int HD>
@@ -356,9 +361,9 @@ struct QCfg {
     static constexpr int kVOff = kKOff + kStages * kKBytes;
     static constexpr int kBarOff = kVOff + kStages * kKBytes;
     static constexpr int kNumBars = 8 + 2 * kStages + 4;
-    // epilogue staging: one 32-row x 64-column slice (4 KB) per compute warp
+    // epilogue staging: one 32-row x 64-column slice (4 KB) per compute warp (8)
     static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
-    static constexpr int kBytes = kStgOff + 4 * 4096;
+    static constexpr int kBytes = kStgOff + 8 * 4096;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
@@ -405,13 +410,13 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int QG_FULL = 0;   // Q and dO of an item in shared memory
-    const int QG_EMPTY = 1;  // ... copied into TMEM (4 compute warps)
-    const int QT_READY = 2;  // Q and dO of an item in TMEM (A operands; 4 warps)
+    const int QG_EMPTY = 1;  // ... copied into TMEM (8 compute warps)
+    const int QT_READY = 2;  // Q and dO of an item in TMEM (A operands; 8 warps)
     const int DQ_DONE = 3;   // the item's last dQ MMA completed
-    const int DQ_EMPTY = 4;  // the epilogue has read dQ out of TMEM (4 warps)
+    const int DQ_EMPTY = 4;  // the epilogue has read dQ out of TMEM (8 warps)
     const int MMA_DONE = 5;
     auto ST_FULL = [&](int b) { return 6 + b; };  // S and dP of a tile (two issuers)
-    auto DS_FULL = [&](int b) { return 8 + b; };  // dS of a tile (4 warps)
+    auto DS_FULL = [&](int b) { return 8 + b; };  // dS of a tile (8 warps)
     auto KV_FULL = [&](int s) { return 10 + s; };
     auto KV_EMPTY = [&](int s) { return 10 + NS + s; };
 
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == DS_FULL(0) || i == DS_FULL(1) || i == QT_READY || i == QG_EMPTY || i == DQ_EMPTY) count = 4;
+            if (i == DS_FULL(0) || i == DS_FULL(1) || i == QT_READY || i == QG_EMPTY || i == DQ_EMPTY) count = 8;
             if (i == ST_FULL(0) || i == ST_FULL(1) || i == MMA_DONE) count = 2;  // two MMA issuers
             for (int s2 = 0; s2 < NS; ++s2)
                 if (i == KV_EMPTY(s2)) count = 2;
@@ -430,7 +435,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     // every GEMM here then reads only K or V from shared memory
     const uint32_t tQ = tbase + 256 + HD, tG = tQ + HD / 2;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // producer and MMA issuers run as whole warps; one elected lane issues
         if (elect_one()) {
             prefetch_tmap(&tmQ);
@@ -492,13 +497,13 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         if (qn > 0) mbar_wait(BAR(QG_FULL), (qn - 1) & 1, P.status, ST_TEARDOWN, nullptr);
         for (int n = max(0, g - NS); n < g; ++n)
             mbar_wait(BAR(KV_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
-    } else if (warp == 5 || warp == 6) {
+    } else if (warp == 9 || warp == 10) {
         // Two MMA issuers, so that one's barrier waits overlap the other's issue:
-        // warp 5 issues S and dQ (the dS of tile n sits over S(n), so S(n+2) must
-        // follow dQ(n) in one stream), warp 6 issues dP.  ST_FULL, KV_EMPTY and
+        // warp 9 issues S and dQ (the dS of tile n sits over S(n), so S(n+2) must
+        // follow dQ(n) in one stream), warp 10 issues dP.  ST_FULL, KV_EMPTY and
         // MMA_DONE count both.  Tiles are numbered across items (gt): ring slot
         // gt % NS, S/dP buffer gt & 1.
-        const bool issues_dp = warp == 6;
+        const bool issues_dp = warp == 10;
         constexpr uint32_t idS = idesc_f16(BF16, BQ, BK, false, false);
         constexpr uint32_t idAcc = idesc_f16(BF16, BQ, HD, false, true);
         auto wait_all = [&](int bar, uint32_t parity) -> bool {
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         if (elect_one())
-                            mma_ts(tDQ, tbase + bf * 64 + kk * 8, kdesc + ((kk * 2048) >> 4), idAcc,
+                            mma_ts(tDQ, tbase + bf * 64 + pcol(kk), kdesc + ((kk * 2048) >> 4), idAcc,
                                    (n > 0 || kk > 0) ? 1u : 0u);
                 } else {
                     tc_fence_after();
@@ -562,21 +567,23 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         }
         if (elect_one()) mma_commit(BAR(MMA_DONE));
         mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
-    } else {
-        // ----------------------------------------- compute: one query row per thread
-        const int r = warp * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    } else if (warp < 8) {
+        // ------------------- compute: warps w and w+4 share rows (TMEM lane quarter
+        // w % 4, one query row per thread) and split each tile's 64 key columns (hf)
+        const int wq = warp & 3, hf = warp >> 2;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         bool ok = true;
         int gt = 0, act = 0, qc = 0;  // tiles, active items and Q/dO copies so far
         int copied = -1;              // item whose Q and dO are in TMEM
-        // copy this thread's rows of Q and dO (128-byte-swizzled smem) into TMEM
+        // copy this thread's row of Q (hf 0) or dO (hf 1), 128-byte-swizzled smem, into TMEM
         auto copy_q = [&](int w2) -> bool {
             if (!warp_wait(BAR(QG_FULL), qc & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) return false;
             ++qc;
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
+            {
+                const int t = hf;
                 const uint8_t* src = smem + (t == 0 ? C::kQOff : C::kGOff);
 #pragma unroll
                 for (int half = 0; half < HD / 64; ++half) {
@@ -618,20 +625,19 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int t = gt + n, bf = t & 1;
                 const int jt = (it.kt0 + n) * BK;
-                uint32_t mbits[2] = {0xffffffffu, 0xffffffffu};
+                // this warp's 32 key columns: jt + 32 hf + [0, 32)
+                const int jc = jt + 32 * hf;
+                uint32_t mbits = 0xffffffffu;
                 if (P.key_mask) {
                     const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int j = jt + c * 32 + lane;
-                        mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
-                    }
+                    const int j = jc + lane;
+                    mbits = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
                 }
-                int clo = 0, chi = min(BK, P.Tk - jt);
-                if (P.causal) chi = min(chi, p - jt + 1);
+                int clo = 0, chi = min(32, P.Tk - jc);
+                if (P.causal) chi = min(chi, p - jc + 1);
                 if (P.window > 0) {
-                    clo = max(clo, p - P.window + 1 - jt);
-                    if (!P.causal) chi = min(chi, p + P.window - jt);
+                    clo = max(clo, p - P.window + 1 - jc);
+                    if (!P.causal) chi = min(chi, p + P.window - jc);
                 }
                 if (!row_ok) chi = 0;
                 if (!warp_wait(BAR(ST_FULL(bf)), (t >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
@@ -639,35 +645,29 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                     break;
                 }
                 tc_fence_after();
-                uint32_t sv[2][32], dp[2][32];
-                tmem_ld32(tbase + lane_off + bf * 64, sv[0]);
-                tmem_ld32(tbase + lane_off + bf * 64 + 32, sv[1]);
-                tmem_ld32(tbase + lane_off + 128 + bf * 64, dp[0]);
-                tmem_ld32(tbase + lane_off + 128 + bf * 64 + 32, dp[1]);
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tbase + lane_off + bf * 64 + 32 * hf, sv);
+                tmem_ld32(tbase + lane_off + 128 + bf * 64 + 32 * hf, dp);
                 tmem_ld_wait_only();
-                tmem_pin(sv[0]);
-                tmem_pin(sv[1]);
-                tmem_pin(dp[0]);
-                tmem_pin(dp[1]);
-                uint32_t dsk[32];
+                tmem_pin(sv);
+                tmem_pin(dp);
+                uint32_t dsk[16];
                 // invisible pairs become -inf scores first: one copy of the element loop
-                const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= BK;
+                const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= 32;
                 if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
-                    for (int cc = 0; cc < BK; ++cc)
-                        sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi && ((mbits[cc >> 5] >> (cc & 31)) & 1u))
-                                                   ? sv[cc >> 5][cc & 31]
-                                                   : 0xff800000u;
+                    for (int cc = 0; cc < 32; ++cc)
+                        sv[cc] = (cc >= clo && cc < chi && ((mbits >> cc) & 1u)) ? sv[cc] : 0xff800000u;
                 }
                 auto elems = [&](auto capc) {
                     constexpr bool kCap = decltype(capc)::value;
 #pragma unroll
-                    for (int c = 0; c < BK; c += 2) {
+                    for (int c = 0; c < 32; c += 2) {
                         float dv[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int cc = c + e;
-                            const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
+                            const float sval = __uint_as_float(sv[cc]);
                             float x, dcap = 1.f;
                             if constexpr (kCap) {
                                 // softcap*tanh(-inf) would be finite: keep a masked score at -inf
@@ -678,14 +678,16 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                                 x = fmaf(sval, P.scale_log2, -lse2);
                             }
                             const float pr = fast_exp2(x);
-                            dv[e] = pr * (__uint_as_float(dp[cc >> 5][cc & 31]) - Dd) * dcap;
+                            dv[e] = pr * (__uint_as_float(dp[cc]) - Dd) * dcap;
                         }
                         dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
                     }
                 };
                 if (cap) elems(std::integral_constant<bool, true>());
                 else elems(std::integral_constant<bool, false>());
-                tmem_st32(tbase + lane_off + bf * 64, dsk);
+                // packed into the first 16 of the 32 columns this warp read (the partner
+                // warp may still be loading the other 32)
+                tmem_st16(tbase + lane_off + bf * 64 + 32 * hf, dsk);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -710,12 +712,17 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 ++act;
                 tc_fence_after();
             }
-            uint32_t packed[HD / 2];
+            // columns of dQ this warp writes: 64 * hf + [0, 64) (hd 128); the whole row
+            // by hf 0 (hd 64)
+            constexpr int kCols = 64;
+            const bool writes = HD == 128 || hf == 0;
+            const int c0 = HD == 128 ? 64 * hf : 0;
+            uint32_t packed[kCols / 2];
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int c = 0; c < kCols / 32; ++c) {
                 uint32_t acc[32];
-                if (have) {
-                    tmem_ld32(tDQ + lane_off + c * 32, acc);
+                if (have && writes) {
+                    tmem_ld32(tDQ + lane_off + c0 + c * 32, acc);
                     tmem_ld_wait(acc);
                 } else {
 #pragma unroll
@@ -731,22 +738,19 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(DQ_EMPTY));
             }
-            // this warp's 32 rows leave through its staging slice, 64 columns at a time
-            const uint32_t slice = sbase + C::kStgOff + warp * 4096;
-#pragma unroll
-            for (int half = 0; half < HD / 64; ++half) {
+            // this warp's 32 rows x 64 columns leave through its staging slice
+            if (writes) {
+                const uint32_t slice = sbase + C::kStgOff + warp * 4096;
                 if (elect_one()) bulk_wait_read_all();
                 __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int w4 = half * 32 + 4 * j;
-                    st_shared_v4(slice + lane * 128 + ((j ^ (lane & 7)) << 4), packed[w4], packed[w4 + 1],
-                                 packed[w4 + 2], packed[w4 + 3]);
-                }
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(slice + lane * 128 + ((j ^ (lane & 7)) << 4), packed[4 * j], packed[4 * j + 1],
+                                 packed[4 * j + 2], packed[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (elect_one()) {
-                    tma_store_3d(&tmDQ, slice, it.h * HD + half * 64, it.i0 + warp * 32, it.b);
+                    tma_store_3d(&tmDQ, slice, it.h * HD + c0, it.i0 + wq * 32, it.b);
                     bulk_commit_group();
                 }
             }
@@ -757,7 +761,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
