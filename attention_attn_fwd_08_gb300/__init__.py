@@ -175,8 +175,9 @@ def attn_bwd(q, k, v, o, do, lse, *, H, Hkv, scale=None, causal=False, window=0,
              key_mask=None, dq=None, dk=None, dv=None, workspace=None, stream=None, phases=7):
     """Backward attention; returns (dq, dk, dv), overwritten.
 
-    phases selects passes (1 = D = rowsum(dO*O), 2 = dK/dV, 4 = dQ); passes 2 and 4
-    read the D that pass 1 left in `workspace`, so pass the same workspace."""
+    phases selects passes (1 = D = rowsum(dO*O), 2 = dK/dV, 4 = dQ, which forms D
+    itself); pass 2 alone reads the D that an earlier pass 1 or 4 left in
+    `workspace`, so pass the same workspace."""
     torch = _torch()
     _contig(q, k, v, o, do, lse, dq, dk, dv)
     B, Tq, Tk, hd = _dims(q, k, H, Hkv)

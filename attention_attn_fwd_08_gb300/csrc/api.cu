@@ -253,8 +253,14 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
     p.tq_pad = (Tq + 63) / 64 * 64;
     p.delta = static_cast<float*>(workspace);
     p.lse2 = p.delta + (size_t)B * H * p.tq_pad;
-    const int nk = ((phases & 1) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
-    if (!use_tcgen05(dt, hd)) return counted(launch_simt_bwd(p, (int)dt, phases, s), nk);
+    if (!use_tcgen05(dt, hd)) {
+        // the fp32 dQ pass reads D from the workspace: pass 4 implies pass 1 there
+        const int ph = (phases & 4) ? (phases | 1) : phases;
+        const int nks = ((ph & 1) ? 1 : 0) + ((ph & 2) ? 1 : 0) + ((ph & 4) ? 1 : 0);
+        return counted(launch_simt_bwd(p, (int)dt, ph, s), nks);
+    }
+    // the tensor-core dQ pass forms D itself: pass 1 is then not run separately
+    const int nk = ((phases & 1) && !(phases & 4) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
     BwdMaps maps;
     if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
         !make_map(&maps.dout, dt, dout, (long long)H * hd, Tq, B, 128) ||
@@ -264,7 +270,8 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
         !make_map(&maps.dout64, dt, dout, (long long)H * hd, Tq, B, 64) ||
         !make_map(&maps.k64, dt, k, (long long)Hkv * hd, Tk, B, 64) ||
         !make_map(&maps.v64, dt, v, (long long)Hkv * hd, Tk, B, 64) ||
-        ((phases & 4) && !make_map(&maps.dq32, dt, dq, (long long)H * hd, Tq, B, 32)))
+        ((phases & 4) && (!make_map(&maps.dq32, dt, dq, (long long)H * hd, Tq, B, 32) ||
+                          !make_map(&maps.o, dt, o, (long long)H * hd, Tq, B, 128))))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_bwd(p, (int)dt, maps, phases, s), nk);
 }

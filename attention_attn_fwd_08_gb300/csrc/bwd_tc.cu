@@ -35,7 +35,7 @@ namespace attn {
 namespace {
 
 constexpr int kThreads = 192;    // dK/dV: 4 compute warps, producer, MMA
-constexpr int kThreadsDQ = 352;  // dQ: 8 compute warps, producer, two MMA issuers
+constexpr int kThreadsDQ = 384;  // dQ: 8 compute warps, K/V producer, two MMA issuers, Q/dO/O producer
 constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM column (within a 64-column tile buffer) of K-step kk's 16-bit dS operand
@@ -356,11 +356,12 @@ struct QCfg {
     static constexpr int kQBytes = BQ * HD * 2;
     static constexpr int kKBytes = BK * HD * 2;  // one K (or V) tile
     static constexpr int kQOff = 0;
-    static constexpr int kGOff = kQBytes;
-    static constexpr int kKOff = 2 * kQBytes;
+    static constexpr int kGOff = kQBytes;      // dO
+    static constexpr int kOOff = 2 * kQBytes;  // O (for D = rowsum(dO*O))
+    static constexpr int kKOff = 3 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKBytes;
     static constexpr int kBarOff = kVOff + kStages * kKBytes;
-    static constexpr int kNumBars = 8 + 2 * kStages + 4;
+    static constexpr int kNumBars = 11 + 2 * kStages;
     // epilogue staging: one 32-row x 64-column slice (4 KB) per compute warp (8)
     static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
     static constexpr int kBytes = kStgOff + 8 * 4096;
@@ -390,6 +391,9 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
 }
 
 // Persistent: one CTA per SM walks its items in snake order (snake_item).  The
+// kernel also computes D = rowsum(dO*O) and LSE*log2(e) of its rows from the O
+// and dO tiles it loads, uses them, and writes them into the workspace for the
+// dK/dV pass (which therefore runs after this one).  The
 // K/V ring and every barrier phase run on across items.  The next item's Q and dO
 // are loaded into shared memory once the current ones are in TMEM, and copied
 // into TMEM right after the current item's last dS, so its first S and dP run
@@ -398,7 +402,7 @@ template <bool BF16, int HD>
 __global__ void __launch_bounds__(kThreadsDQ, 1)
     bwd_dq_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                  const __grid_constant__ CUtensorMap tmDQ) {
+                  const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDQ) {
     using C = QCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BK = C::BK;
     extern __shared__ uint8_t smem_raw[];
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     __shared__ int abort_flag;
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    const int QG_FULL = 0;   // Q and dO of an item in shared memory
+    const int QG_FULL = 0;   // Q, dO and O of an item in shared memory
     const int QG_EMPTY = 1;  // ... copied into TMEM (8 compute warps)
     const int QT_READY = 2;  // Q and dO of an item in TMEM (A operands; 8 warps)
     const int DQ_DONE = 3;   // the item's last dQ MMA completed
@@ -419,6 +423,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     auto DS_FULL = [&](int b) { return 8 + b; };  // dS of a tile (8 warps)
     auto KV_FULL = [&](int s) { return 10 + s; };
     auto KV_EMPTY = [&](int s) { return 10 + NS + s; };
+    const int D_FULL = 10 + 2 * NS;  // D of an item's rows in shared memory (the Q/dO/O producer)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nitems = (P.Tq + BQ - 1) / BQ * P.H * P.B;
@@ -448,21 +453,39 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     // every GEMM here then reads only K or V from shared memory
     const uint32_t tQ = tbase + 256 + HD, tG = tQ + HD / 2;
 
-    if (warp == 8) {
-        // producer and MMA issuers run as whole warps; one elected lane issues
+    if (warp == 11) {
+        // ------------------------------- Q/dO/O producer and D (whole warp)
+        // Loads the next item's tiles as soon as the current ones are in TMEM, then
+        // forms D = rowsum(dO*O) of its 128 rows (lane l: rows l, l+32, l+64, l+96)
+        // into the first 512 bytes of the O tile, and writes D and LSE*log2(e) of
+        // every row into the workspace for the dK/dV pass (rows that see no key and
+        // padding rows: D = 0, LSE = +inf).
         if (elect_one()) {
             prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
             prefetch_tmap(&tmG);
+            prefetch_tmap(&tmO);
         }
-        bool ok = true;
-        int qn = 0, g = 0;  // Q/dO loads and K/V tiles loaded so far
-        for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
+        auto stats = [&](const DqItem& it, int i2, float dval) {
+            if (i2 >= P.tq_pad) return;
+            const long long srow = ((long long)it.b * P.H + it.h) * P.tq_pad + i2;
+            float l2 = INFINITY;
+            if (i2 < P.Tq) {
+                const float l = P.lse_in[((long long)it.b * P.H + it.h) * P.Tq + i2];
+                l2 = l == -INFINITY ? INFINITY : l * kLog2e;
+            }
+            P.delta[srow] = i2 < P.Tq ? dval : 0.f;
+            P.lse2[srow] = l2;
+        };
+        int qn = 0;  // Q/dO/O loads so far
+        for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
             const DqItem it = dq_item<BQ, BK>(P, w);
-            if (it.ntiles == 0) continue;
+            if (it.ntiles == 0) {
+#pragma unroll
+                for (int m = 0; m < BQ / 32; ++m) stats(it, it.i0 + m * 32 + lane, 0.f);
+                continue;
+            }
             if (qn > 0 && !warp_wait(BAR(QG_EMPTY), (qn - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) break;
-            if (elect_one()) mbar_expect_tx(BAR(QG_FULL), 2 * C::kQBytes);
+            if (elect_one()) mbar_expect_tx(BAR(QG_FULL), 3 * C::kQBytes);
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
                 if (elect_one())
@@ -471,8 +494,51 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 if (elect_one())
                     tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), it.h * HD + bx * 64, it.i0,
                                 it.b);
+                if (elect_one())
+                    tma_load_3d(sbase + C::kOOff + bx * (BQ * 128), &tmO, BAR(QG_FULL), it.h * HD + bx * 64, it.i0,
+                                it.b);
             }
             ++qn;
+            if (!warp_wait(BAR(QG_FULL), (qn - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) break;
+            float dv[BQ / 32];
+#pragma unroll
+            for (int m = 0; m < BQ / 32; ++m) {
+                const int rr = m * 32 + lane;
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int half = 0; half < HD / 64; ++half) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const int off = half * (BQ * 128) + rr * 128 + ((ch ^ (rr & 7)) << 4);
+                        const uint4 g4 = *reinterpret_cast<const uint4*>(smem + C::kGOff + off);
+                        const uint4 o4 = *reinterpret_cast<const uint4*>(smem + C::kOOff + off);
+                        a0 += dot2<BF16>(g4.x, o4.x) + dot2<BF16>(g4.y, o4.y);
+                        a1 += dot2<BF16>(g4.z, o4.z) + dot2<BF16>(g4.w, o4.w);
+                    }
+                }
+                dv[m] = a0 + a1;
+            }
+            __syncwarp();  // every lane has read its O rows
+            float* d_smem = reinterpret_cast<float*>(smem + C::kOOff);
+#pragma unroll
+            for (int m = 0; m < BQ / 32; ++m) d_smem[m * 32 + lane] = dv[m];
+            fence_proxy_async_smem();  // before the next TMA load overwrites it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(D_FULL));
+#pragma unroll
+            for (int m = 0; m < BQ / 32; ++m) stats(it, it.i0 + m * 32 + lane, dv[m]);
+        }
+        if (qn > 0) mbar_wait(BAR(QG_FULL), (qn - 1) & 1, P.status, ST_TEARDOWN, nullptr);
+    } else if (warp == 8) {
+        // ------------------------------------------- K/V producer (whole warp)
+        if (elect_one()) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+        }
+        bool ok = true;
+        int g = 0;  // K/V tiles loaded so far
+        for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
+            const DqItem it = dq_item<BQ, BK>(P, w);
             for (int n = 0; n < it.ntiles; ++n) {
                 const int s = g % NS, use = g / NS;
                 if (use > 0 && !warp_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) {
@@ -494,7 +560,6 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             }
         }
         // every copy in flight lands before the CTA exits
-        if (qn > 0) mbar_wait(BAR(QG_FULL), (qn - 1) & 1, P.status, ST_TEARDOWN, nullptr);
         for (int n = max(0, g - NS); n < g; ++n)
             mbar_wait(BAR(KV_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
     } else if (warp == 9 || warp == 10) {
@@ -578,13 +643,20 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         bool ok = true;
         int gt = 0, act = 0, qc = 0;  // tiles, active items and Q/dO copies so far
         int copied = -1;              // item whose Q and dO are in TMEM
-        // copy this thread's row of Q (hf 0) or dO (hf 1), 128-byte-swizzled smem, into TMEM
+        float d_copied = 0.f;         // D = rowsum(dO*O) of this thread's row of that item
+        float l_copied = -INFINITY;   // its LSE, loaded with the copy (used at the item's start)
+        auto load_lse = [&](const DqItem& it2) -> float {
+            const int i2 = it2.i0 + r;
+            return i2 < P.Tq ? P.lse_in[((long long)it2.b * P.H + it2.h) * P.Tq + i2] : -INFINITY;
+        };
+        // copy this thread's row of Q (hf 0) or dO (hf 1), 128-byte-swizzled smem, into
+        // TMEM; both halves also form D of the row from dO and O in shared memory
+        // Copy this thread's row of Q (hf 0) or dO (hf 1), 128-byte-swizzled smem,
+        // into TMEM; read the row's D that the producer warp formed.
         auto copy_q = [&](int w2) -> bool {
             if (!warp_wait(BAR(QG_FULL), qc & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) return false;
-            ++qc;
             {
-                const int t = hf;
-                const uint8_t* src = smem + (t == 0 ? C::kQOff : C::kGOff);
+                const uint8_t* src = smem + (hf == 0 ? C::kQOff : C::kGOff);
 #pragma unroll
                 for (int half = 0; half < HD / 64; ++half) {
                     uint32_t wv[32];
@@ -597,16 +669,22 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                         wv[4 * ch + 2] = v4.z;
                         wv[4 * ch + 3] = v4.w;
                     }
-                    tmem_st32((t == 0 ? tQ : tG) + lane_off + half * 32, wv);
+                    tmem_st32((hf == 0 ? tQ : tG) + lane_off + half * 32, wv);
                 }
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(BAR(QG_EMPTY));
-                mbar_arrive(BAR(QT_READY));
-            }
+            // the MMA warps may start on this item now
+            if (lane == 0) mbar_arrive(BAR(QT_READY));
+            // issued here, consumed at the item's start: the latency hides behind
+            // the current item's epilogue
+            l_copied = load_lse(dq_item<BQ, BK>(P, w2));
+            if (!warp_wait(BAR(D_FULL), qc & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) return false;
+            d_copied = reinterpret_cast<const float*>(smem + C::kOOff)[r];
+            ++qc;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(QG_EMPTY));  // Q, dO, O and D in shared memory are free
             copied = w2;
             return true;
         };
@@ -617,11 +695,11 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             const bool row_ok = i < P.Tq;
             const int ntiles = it.ntiles;
             float lse2 = INFINITY, Dd = 0.f;
-            if (row_ok && ntiles > 0) {
-                lse2 = P.lse2[((long long)it.b * P.H + it.h) * P.tq_pad + i];
-                Dd = P.delta[((long long)it.b * P.H + it.h) * P.tq_pad + i];
-            }
             if (ntiles > 0 && copied != w) ok = copy_q(w);
+            if (row_ok && ntiles > 0) {
+                lse2 = l_copied == -INFINITY ? INFINITY : l_copied * kLog2e;
+                Dd = d_copied;
+            }
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int t = gt + n, bf = t & 1;
                 const int jt = (it.kt0 + n) * BK;
@@ -767,20 +845,15 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     }
 }
 
+// Pass 4 (dQ) forms D and LSE*log2(e) itself and writes them into the
+// workspace, so with pass 4 requested pass 1 is not run separately, and dQ goes
+// before dK/dV, which reads them.
 template <bool BF16, int HD>
 cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_t s) {
     cudaError_t e;
-    if (phases & 1) {
+    if ((phases & 1) && !(phases & 4)) {
         e = launch_bwd_preprocess(p, BF16 ? 2 : 1, s);
         if (e != cudaSuccess) return e;
-    }
-    if (phases & 2) {
-        auto k = bwd_dkdv_kernel<BF16, HD>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
-        if (e != cudaSuccess) return e;
-        const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;
-        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 4) {
         auto k = bwd_dq_kernel<BF16, HD>;
@@ -792,7 +865,15 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         // persistent: one CTA per SM (one fits); each walks its items in snake order
         const long long items = (long long)((p.Tq + 127) / 128) * p.H * p.B;
         const unsigned grid = (unsigned)(items < nsm ? items : nsm);
-        k<<<grid, kThreadsDQ, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout, m.dq32);
+        k<<<grid, kThreadsDQ, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout, m.o, m.dq32);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (phases & 2) {
+        auto k = bwd_dkdv_kernel<BF16, HD>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
+        if (e != cudaSuccess) return e;
+        const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;
+        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -84,6 +84,18 @@ template <> __device__ __forceinline__ uint32_t pack2<false>(float lo, float hi)
     __half2 t = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&t);
 }
+// dot product of two words of two 16-bit values each, in fp32
+template <bool BF16> __device__ __forceinline__ float dot2(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ float dot2<true>(uint32_t a, uint32_t b) {
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
+    return fmaf(x.x, y.x, x.y * y.y);
+}
+template <> __device__ __forceinline__ float dot2<false>(uint32_t a, uint32_t b) {
+    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&a));
+    const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&b));
+    return fmaf(x.x, y.x, x.y * y.y);
+}
 
 // ------------------------------------------------------------ visibility
 // Key j visible to the query at absolute position p (see include/attn.h).

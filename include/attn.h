@@ -124,9 +124,12 @@ ATTN_API attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const
 
 /*
  * The three passes of attn_bwd, selectable one at a time (same arguments).
- * phases is a bit set: 1 = D = rowsum(dO*O) into the workspace, 2 = dK/dV,
- * 4 = dQ.  Passes 2 and 4 read the D that pass 1 wrote into the same
- * workspace.  attn_bwd(...) is attn_bwd_phases(..., 7).
+ * phases is a bit set: 1 = D = rowsum(dO*O) and LSE*log2(e) into the
+ * workspace, 2 = dK/dV, 4 = dQ.  Pass 4 forms D and LSE*log2(e) itself and
+ * leaves them in the workspace (so with 4 set, 1 is implied and, on the
+ * 16-bit path, not run as a pass of its own); pass 2 alone reads the workspace
+ * an earlier pass 1 or 4 with the same arguments wrote.  Requested passes run
+ * as 1, 4, 2.  attn_bwd(...) is attn_bwd_phases(..., 7).
  */
 ATTN_API attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const void* v,
                      const void* o, const void* dout, const float* lse, void* dq, void* dk,

@@ -184,6 +184,32 @@ def test_outputs_are_overwritten_not_accumulated():
         assert torch.equal(a, b)
 
 
+def test_bwd_passes_run_separately():
+    """dQ (pass 4) then dK/dV (pass 2) into a workspace of garbage equals the full
+    backward bit for bit; pass 1 then 2 (D from the standalone pass) agrees within
+    rounding."""
+    B, T, H, Hkv, hd = 2, 300, 4, 2, 128
+    q, k, v, do = inputs("bf16", B, T, T, H, Hkv, hd, 904, backward=True)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    kw = dict(H=H, Hkv=Hkv, causal=True)
+    o, lse = A.attn_fwd(qd, kd, vd, **kw)
+    n = A.attn_bwd_workspace_size(B, T, H)
+    full = [t.clone() for t in A.attn_bwd(qd, kd, vd, o, dod, lse, **kw)]
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
+    dq4, _, _ = A.attn_bwd(qd, kd, vd, o, dod, lse, workspace=ws, phases=4, **kw)
+    dq4 = dq4.clone()
+    _, dk2, dv2 = A.attn_bwd(qd, kd, vd, o, dod, lse, workspace=ws, phases=2, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(dq4, full[0]) and torch.equal(dk2, full[1]) and torch.equal(dv2, full[2])
+    ws.fill_(0xFF)
+    A.attn_bwd(qd, kd, vd, o, dod, lse, workspace=ws, phases=1, **kw)
+    _, dk1, dv1 = A.attn_bwd(qd, kd, vd, o, dod, lse, workspace=ws, phases=2, **kw)
+    torch.cuda.synchronize()
+    for a, b in ((dk1, full[1]), (dv1, full[2])):
+        err = (a.float() - b.float()).norm() / b.float().norm()
+        assert err < 1e-2, err
+
+
 def test_guard_bands_untouched():
     """Outputs written inside larger buffers leave the surrounding canary bytes alone."""
     B, T, H, hd = 1, 130, 2, 64
