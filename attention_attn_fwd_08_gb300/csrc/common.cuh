@@ -240,6 +240,27 @@ __device__ __forceinline__ int snake_item(int k) {
     return k * g + ((k & 1) ? g - 1 - c : c);
 }
 
+// Bounded wait until a shared counter reaches target (an execution order only:
+// no data is published through it).  Sleeps briefly between polls so that the
+// waiting warps leave issue slots to the warps they wait for.
+__device__ __forceinline__ bool count_wait(const int* counter, int target, unsigned int* status, unsigned int code,
+                                           volatile int* abort_flag) {
+    const volatile int* cc = counter;
+    if (*cc >= target) return true;
+    const unsigned long long t0 = globaltimer();
+#pragma unroll 1
+    while (true) {
+        __nanosleep(20);
+        if (*cc >= target) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(status, code);
+            if (abort_flag) *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
 // Bounded wait by a whole warp; true only when every lane saw the phase.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned int* status, unsigned int code,
                                           volatile int* abort_flag) {

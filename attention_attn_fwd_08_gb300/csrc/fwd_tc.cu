@@ -148,6 +148,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
     auto O_DONE = [&](int u) { return 8 + 4 * NS + u; };   // the item's last P.V of tile u completed
     auto O_EMPTY = [&](int u) { return 10 + 4 * NS + u; };  // the epilogue has read O_u out of TMEM
     const int MMA_DONE = 12 + 4 * NS;
+    // softmaxes finished by tile u, counted per warp (exact counts: a tile with no work
+    // in an item lets the other run several softmaxes ahead, which mbarrier parity
+    // could not tell apart)
+    __shared__ int done_count[2];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nitems = fwd_items(P);
@@ -166,6 +170,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             mbar_init(BAR(i), count);
         }
         abort_flag = 0;
+        done_count[0] = done_count[1] = 0;
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -461,8 +466,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_st16(tS + lane_off + c * 16, pk[c]);
         };
+        // The two tiles' softmaxes alternate A(k), B(k), A(k+1), ... within an item, so
+        // each runs while the tensor core works on the other tile's P.V and next S;
+        // left alone they fall into lockstep and the tensor core idles during both.
+        // base[u] counts tile u's softmaxes in earlier items.
+        int base[2] = {0, 0};
         for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
             const FwdItem it = fwd_item(P, w);
+            const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
+            const int bA = base[0], bB = base[1];
+            base[0] += nA;
+            base[1] += nB;
             const int ib = it.i0 + u * BM;  // first row of this tile
             if (ib >= P.Tq) continue;
             const int i = ib + r;
@@ -497,6 +511,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     break;
                 }
                 ++sc;
+                if (u == 0 ? (k >= 1 && k - 1 < nB) : (k < nA)) {
+                    const int need = 4 * (u == 0 ? bB + k : bA + k + 1);  // warp arrivals
+                    const bool rr = count_wait(&done_count[u ^ 1], need, P.status, ST_FWD_SOFTMAX, &abort_flag);
+                    if (!__all_sync(0xffffffffu, rr)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 tc_fence_after();
                 if (!full) mask_tile(clo, chi, mbits);
                 if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k);
@@ -504,27 +526,37 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(P_FULL(u)));
+                if (lane == 0) {
+                    mbar_arrive(BAR(P_FULL(u)));
+                    atomicAdd(&done_count[u], 1);
+                }
             }
             const bool have_o = ok && my.ntiles > 0 && wait_warp(O_DONE(u), act & 1);
             if (my.ntiles > 0) ++act;
             if (have_o) tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint32_t packed[HD / 2];
-#pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-                uint32_t orr[32];
+            {
+                // all of the row's O columns in flight at once, one wait
+                uint32_t orr[HD / 32][32];
                 if (have_o) {
-                    tmem_ld32(tO + lane_off + c * 32, orr);
-                    tmem_ld_wait(orr);
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c) tmem_ld32(tO + lane_off + c * 32, orr[c]);
+                    tmem_ld_wait_only();
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c) tmem_pin(orr[c]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) orr[e] = 0u;
+                    for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orr[c][e] = 0u;
                 }
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    packed[c * 16 + e] =
-                        pack2<BF16>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
+                for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        packed[c * 16 + e] = pack2<BF16>(__uint_as_float(orr[c][2 * e]) * inv,
+                                                         __uint_as_float(orr[c][2 * e + 1]) * inv);
             }
             // O_u is in registers: the next item's first P.V may overwrite it
             if (have_o) {
