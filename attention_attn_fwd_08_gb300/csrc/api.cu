@@ -271,7 +271,9 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
         !make_map(&maps.k64, dt, k, (long long)Hkv * hd, Tk, B, 64) ||
         !make_map(&maps.v64, dt, v, (long long)Hkv * hd, Tk, B, 64) ||
         ((phases & 4) && (!make_map(&maps.dq32, dt, dq, (long long)H * hd, Tq, B, 32) ||
-                          !make_map(&maps.o, dt, o, (long long)H * hd, Tq, B, 128))))
+                          !make_map(&maps.o, dt, o, (long long)H * hd, Tq, B, 128))) ||
+        ((phases & 2) && (!make_map(&maps.dk32, dt, dk, (long long)Hkv * hd, Tk, B, 32) ||
+                          !make_map(&maps.dv32, dt, dv, (long long)Hkv * hd, Tk, B, 32))))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_bwd(p, (int)dt, maps, phases, s), nk);
 }

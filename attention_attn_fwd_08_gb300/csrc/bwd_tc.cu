@@ -60,14 +60,17 @@ struct KVCfg {
     static constexpr int kStatBytes = 2 * BQ * 4;
     static constexpr int kBarOff = kStatOff + kStages * kStatBytes;
     static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
-    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+    // epilogue staging: two 32-row x 64-column slices (4 KB each) per compute warp
+    static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
+    static constexpr int kBytes = kStgOff + 4 * 8192;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
 template <bool BF16, int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                    const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV) {
     using C = KVCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BKV = C::BKV;
     extern __shared__ uint8_t smem_raw[];
@@ -303,40 +306,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(PT_FULL(bf)));
         }
-        // epilogue: dV, dK (x scale) for this key row; zero when no query sees it
-        using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+        // epilogue: dV, dK (x scale) for this key row; zero when no query sees it.  Each
+        // warp's 32 rows leave through two alternating 4 KB staging slices, 64 columns
+        // per tiled store (rows past Tk are not written).
         const bool have = ok && ntiles > 0 && warp_wait(BAR(ACC_DONE), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
         if (have) tc_fence_after();
-        if (ok) {
-            const long long off = ((long long)b * P.Tk + (j < P.Tk ? j : 0)) * (long long)P.Hkv * HD + (long long)kvh * HD;
+        if (have || (ok && ntiles == 0)) {
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
-                T* dst = reinterpret_cast<T*>(part == 0 ? P.dv : P.dk) + off;
                 const uint32_t tcol = part == 0 ? tDV : tDK;
                 const float mul = part == 0 ? 1.f : P.scale;
+                uint32_t acc[HD / 32][32];
+                if (have) {
 #pragma unroll
-                for (int c = 0; c < HD / 32; ++c) {
-                    uint32_t acc[32];
-                    if (have) {
-                        tmem_ld32(tcol + lane_off + c * 32, acc);
-                        tmem_ld_wait(acc);
-                    } else {
+                    for (int c = 0; c < HD / 32; ++c) tmem_ld32(tcol + lane_off + c * 32, acc[c]);
+                    tmem_ld_wait_only();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] = 0u;
+                    for (int c = 0; c < HD / 32; ++c) tmem_pin(acc[c]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[c][e] = 0u;
+                }
+#pragma unroll
+                for (int half = 0; half < HD / 64; ++half) {
+                    const int q = part * (HD / 64) + half;
+                    const uint32_t slice = sbase + C::kStgOff + warp * 8192 + (q & 1) * 4096;
+                    // the slices alternate: this one's last store is the older of the
+                    // two most recent groups
+                    if (elect_one()) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const int col = half * 64 + j * 8 + 2 * t;  // element column
+                            w4[t] = pack2<BF16>(__uint_as_float(acc[col >> 5][col & 31]) * mul,
+                                                __uint_as_float(acc[col >> 5][(col & 31) + 1]) * mul);
+                        }
+                        st_shared_v4(slice + lane * 128 + ((j ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
                     }
-                    if (j < P.Tk && (have || ntiles == 0)) {
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            packed[e] = pack2<BF16>(__uint_as_float(acc[2 * e]) * mul, __uint_as_float(acc[2 * e + 1]) * mul);
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (elect_one()) {
+                        tma_store_3d(part == 0 ? &tmDV : &tmDK, slice, kvh * HD + half * 64, j0 + warp * 32, b);
+                        bulk_commit_group();
                     }
                 }
             }
         }
+        if (elect_one()) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -873,7 +895,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;
-        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64);
+        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64, m.dk32, m.dv32);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -24,7 +24,7 @@ struct BwdMaps {
     CUtensorMap q, dout, k, v;          // 128-row boxes
     CUtensorMap q64, dout64, k64, v64;  // 64-row boxes
     CUtensorMap o;                      // 128-row boxes (D = rowsum(dO*O) in the dQ pass)
-    CUtensorMap dq32;                   // 32-row boxes, for the dQ epilogue's stores
+    CUtensorMap dq32, dk32, dv32;       // 32-row boxes, for the epilogues' stores
 };
 cudaError_t launch_tc_bwd(const Params& p, int dt, const BwdMaps& maps, int phases, cudaStream_t s);
 
