@@ -20,7 +20,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_bwd_workspace_size", "attn_decode_workspace_size",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_bwd_workspace_size", "attn_decode_workspace_size",
            "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_launch_count", "AttnError", "lib",
            "library_path"]
 
@@ -68,6 +68,8 @@ def lib():
         L.attn_decode_workspace_size.restype = sz
         L.attn_decode.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + tail
         L.attn_decode.restype = i
+        L.attn_decode_len.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + [i] * 6 + [f, i, i, f, vp, vp, ll, vp]
+        L.attn_decode_len.restype = i
         L.attn_status_string.argtypes = [i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -222,6 +224,35 @@ def attn_decode(q, k, v, *, H, Hkv, scale=None, causal=True, window=0, softcap=0
                            int(bool(causal)), int(window), float(softcap), int(q_offset), _ptr(m), int(ms),
                            _stream(stream))
     _check(st, "attn_decode")
+    return o, lse
+
+
+def attn_decode_len(q, k, v, lengths, *, H, Hkv, scale=None, causal=True, window=0, softcap=0.0, key_mask=None,
+                    o=None, lse=None, want_lse=True, workspace=None, stream=None):
+    """Split-KV decode over a cache of capacity k.shape[1] whose per-sequence valid
+    length is read on the device from `lengths` (int32 [B]); the Lq query rows of
+    sequence b sit at positions lengths[b] - Lq .. lengths[b] - 1.  Returns (o, lse).
+    The launch depends on the capacity only, so it can be captured in a CUDA graph
+    and replayed after `lengths` changes."""
+    torch = _torch()
+    _contig(q, k, v, o, lse, lengths)
+    B, Lq, Tk, hd = _dims(q, k, H, Hkv)
+    if lengths.dtype != torch.int32 or lengths.numel() != B:
+        raise ValueError("lengths must be int32 with one entry per batch")
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    nbytes = attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    st = lib().attn_decode_len(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), B, Lq, Tk, H, Hkv, hd, float(scale),
+                               int(bool(causal)), int(window), float(softcap), _ptr(lengths), _ptr(m), int(ms),
+                               _stream(stream))
+    _check(st, "attn_decode_len")
     return o, lse
 
 

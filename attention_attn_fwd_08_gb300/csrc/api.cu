@@ -328,6 +328,41 @@ attn_status attn_decode(attn_dtype dt, const void* q, const void* k, const void*
     return counted(launch_decode(p, (int)dt, maps, s), 2);
 }
 
+attn_status attn_decode_len(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                            void* workspace, size_t workspace_bytes, int B, int Lq, int Tk, int H, int Hkv,
+                            int hd, float scale, int causal, int window, float softcap, const int* lengths,
+                            const float* key_mask, long long key_mask_bstride, void* stream) {
+    attn_status st = check_common(dt, B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, 0, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    if (!lengths || (reinterpret_cast<uintptr_t>(lengths) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if (dt == ATTN_F32) return ATTN_ERR_UNSUPPORTED;  // the 16-bit split kernels only
+    if (Lq > 16 || (H / Hkv) * Lq > 64) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || Lq == 0) return ATTN_OK;
+    if (!q || !o || (Tk > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+        return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fill_empty(dt, o, (long long)B * Lq * H * hd, lse, lse ? (long long)B * H * Lq : 0, s);
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd))
+        return ATTN_ERR_INVALID_ARG;
+    Params p = base_params(B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, 0, key_mask,
+                           key_mask_bstride);
+    if (!p.status) return ATTN_ERR_CUDA;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.ws = static_cast<float*>(workspace);
+    p.lengths = lengths;
+    // the plan depends on the capacity only, so a captured launch stays valid as lengths change
+    decode_plan(B, Lq, Tk, H, Hkv, &p.splits, &p.chunk);
+    DecMaps maps;
+    if (!make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 64) ||
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 64))
+        return ATTN_ERR_CUDA;
+    return counted(launch_decode(p, (int)dt, maps, s), 2);
+}
+
+
 attn_status attn_decode_noalloc(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
                                 int B, int Lq, int Tk, int H, int Hkv, int hd, float scale, int causal, int window,
                                 float softcap, int q_offset, const float* key_mask, long long key_mask_bstride,

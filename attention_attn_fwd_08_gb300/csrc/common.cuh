@@ -41,6 +41,7 @@ struct Params {
     float softcap;       // 0 = off
     int q_offset;
     int splits, chunk;   // decode
+    const int* lengths;  // decode: per-batch valid cache length on the device, or NULL (Tk for all)
     unsigned int* status;
 };
 

@@ -66,10 +66,18 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Params P,
     const int b = y / P.Hkv;
     const int split = blockIdx.x;
 
+    // This sequence's cache length: Tk, or its device-resident valid length (the
+    // query block then sits at positions len - Lq .. len - 1 and keys from len on
+    // are not visible), so a captured launch serves whatever lengths the buffer holds.
+    int tk_b = P.Tk, qoff = P.q_offset;
+    if (P.lengths) {
+        tk_b = min(max(P.lengths[b], 0), P.Tk);
+        qoff = tk_b - P.Tq;
+    }
     // keys this CTA reads: its chunk, cut to what any of its rows can see
     int lo, hi;
-    key_range(P.causal, P.window, P.Tk, P.q_offset, P.q_offset + P.Tq - 1, &lo, &hi);
-    const int c0 = split * P.chunk, c1 = min(P.Tk, c0 + P.chunk);
+    key_range(P.causal, P.window, tk_b, qoff, qoff + P.Tq - 1, &lo, &hi);
+    const int c0 = split * P.chunk, c1 = min(tk_b, c0 + P.chunk);
     lo = max(lo, c0);
     hi = min(hi, c1);
     const int t0 = lo / kKeys;
@@ -125,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Params P,
             const int gg = rok[r] ? rr / P.Tq : 0, lq = rok[r] ? rr % P.Tq : 0;
             hq[r] = kvh * P.G + gg;
             lqq[r] = lq;
-            pos[r] = P.q_offset + lq;
+            pos[r] = qoff + lq;
             qp[r] = reinterpret_cast<const uint16_t*>(P.q) + ((long long)b * P.Tq + lq) * (long long)P.H * HD +
                     (long long)hq[r] * HD;
         }
@@ -179,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Params P,
                     const int j = j0 + kb + nt * 8 + 2 * t + (e & 1);
                     float x = sc[nt][e] * P.scale;
                     if (P.softcap > 0.f) x = P.softcap * tanh_accurate(x / P.softcap);
-                    const bool vis = rok[r] && visible(P, b, pos[r], j);
+                    const bool vis = rok[r] && j < tk_b && visible(P, b, pos[r], j);
                     x = vis ? x * kLog2e : -INFINITY;
                     sc[nt][e] = x;
                     mx[r] = fmaxf(mx[r], x);

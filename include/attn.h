@@ -164,6 +164,30 @@ ATTN_API attn_status attn_decode(attn_dtype dt, const void* q, const void* k, co
                         long long key_mask_bstride, void* stream);
 
 /*
+ * Split-KV decode over a fixed-capacity KV cache whose valid length per
+ * sequence lives in device memory, so that a captured CUDA graph can be
+ * replayed as the cache grows without any host-side change.
+ * Source: brotensor ops/flash_attention.h, flash_attention_decode_len (the
+ * valid length is read on the device; query row q of an L_q block sits at
+ * position valid_len - L_q + q and attends [0, p]).
+ *   lengths : device array of B int32, 4-byte aligned; sequence b holds
+ *             L_b = min(max(lengths[b], 0), Tk) valid keys (rows 0 .. L_b-1 of
+ *             its cache); keys from L_b on are not visible.  Its Lq query rows
+ *             sit at positions L_b - Lq .. L_b - 1 (no q_offset argument);
+ *             with causal masking a row at a negative position sees no key
+ *             (O = 0, LSE = -inf), as does every row of a sequence with L_b = 0.
+ *   Tk      : the cache capacity (rows allocated per sequence); the split plan
+ *             and the workspace size depend on it alone.
+ *   dt      : ATTN_BF16 or ATTN_F16 (ATTN_F32 returns ATTN_ERR_UNSUPPORTED).
+ *   The rest, key_mask included, as for attn_decode.
+ */
+ATTN_API attn_status attn_decode_len(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, int B, int Lq,
+                        int Tk, int H, int Hkv, int hd, float scale, int causal, int window,
+                        float softcap, const int* lengths, const float* key_mask,
+                        long long key_mask_bstride, void* stream);
+
+/*
  * attn_decode without a workspace argument, for callers that cannot call
  * cudaMalloc and have no scratch buffer to pass in: for example a plugin that
  * is handed only its input and output buffers, a serving loop that forbids

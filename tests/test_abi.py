@@ -91,6 +91,31 @@ def test_bwd_and_decode_validation():
     assert st == A.ERR_INVALID_ARG
 
 
+def test_decode_len_validation():
+    """Argument errors of the device-length decode come back before any launch."""
+    L = A.lib()
+    # NULL lengths
+    st = L.attn_decode_len(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 128, 0.1, 1, 0, 0.0, None,
+                           None, 0, None)
+    assert st == A.ERR_INVALID_ARG
+    # lengths not 4-byte aligned
+    st = L.attn_decode_len(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 128, 0.1, 1, 0, 0.0, ctypes.c_void_p(0x1002),
+                           None, 0, None)
+    assert st == A.ERR_INVALID_ARG
+    # fp32 has no split kernel
+    st = L.attn_decode_len(0, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 128, 0.1, 1, 0, 0.0, BAD,
+                           None, 0, None)
+    assert st == A.ERR_UNSUPPORTED
+    # too long a query block
+    st = L.attn_decode_len(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 17, 256, 8, 2, 128, 0.1, 1, 0, 0.0, BAD,
+                           None, 0, None)
+    assert st == A.ERR_UNSUPPORTED
+    # workspace too small for the capacity
+    st = L.attn_decode_len(2, BAD, BAD, BAD, BAD, None, BAD, 16, 2, 4, 4096, 8, 2, 128, 0.1, 1, 0, 0.0, BAD,
+                           None, 0, None)
+    assert st == A.ERR_INVALID_ARG
+
+
 def test_workspace_sizes():
     assert A.attn_bwd_workspace_size(4, 2048, 32) == 2 * 4 * 2048 * 32 * 4
     assert A.attn_bwd_workspace_size(1, 65, 2) == 2 * 1 * 128 * 2 * 4

@@ -119,6 +119,76 @@ def test_decode_features(flags):
     run_fwd_case("bf16", 2, Lq, Tk, 8, 2, 128, causal=True, q_offset=Tk - Lq, decode=True, seed=600, **flags)
 
 
+def _decode_len_reference(q, k, v, lengths, H, Hkv, hd, km=None, **flags):
+    """Per sequence b: the oracle on its first L_b keys, query rows at positions
+    L_b - Lq .. L_b - 1 (rows at negative positions see nothing: O = 0, LSE = -inf)."""
+    B, Lq = q.shape[0], q.shape[1]
+    o_ref = np.zeros((B, Lq, H * hd))
+    lse_ref = np.full((B, H, Lq), -np.inf)
+    for b in range(B):
+        L = int(lengths[b])
+        first = max(Lq - L, 0)  # first query row at a position >= 0
+        if L == 0 or first >= Lq:
+            continue
+        kb = f64(k[b:b + 1, :L])
+        vb = f64(v[b:b + 1, :L])
+        mb = None if km is None else f64(km[b:b + 1, :L])
+        o_b, l_b = oracle.fwd(f64(q[b:b + 1, first:]), kb, vb, H=H, Hkv=Hkv, scale=1.0 / math.sqrt(hd), causal=True,
+                              q_offset=L - Lq + first, key_mask=mb, **flags)
+        o_ref[b, first:] = o_b[0]
+        lse_ref[b, :, first:] = l_b[0]
+    return o_ref, lse_ref
+
+
+@pytest.mark.parametrize("flags", [dict(), dict(window=300, softcap=25.0), dict(mask=True)],
+                         ids=["plain", "window-softcap", "keymask"])
+def test_decode_len_matches_oracle(flags):
+    """Device-resident lengths, including L < Lq and L = 0, against the oracle."""
+    from helpers import compare_o_lse, make_mask
+    B, Lq, Tk, H, Hkv, hd = 6, 4, 700, 8, 2, 128
+    q, k, v, _ = inputs("bf16", B, Lq, Tk, H, Hkv, hd, 905)
+    lengths = torch.tensor([700, 333, 4, 2, 0, 65], dtype=torch.int32)
+    flags = dict(flags)
+    km = make_mask("batch", B, Tk, 906) if flags.pop("mask", False) else None
+    o, lse = A.attn_decode_len(q.cuda(), k.cuda(), v.cuda(), lengths.cuda(), H=H, Hkv=Hkv,
+                               key_mask=None if km is None else km.cuda(), **flags)
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    assert st == A.OK, "device status word %#x" % word
+    o_ref, lse_ref = _decode_len_reference(q, k, v, lengths, H, Hkv, hd, km=km, **flags)
+    compare_o_lse(o, lse, o_ref, lse_ref, "bf16", "decode_len %s" % flags)
+
+
+def test_decode_len_graph_replay_follows_lengths():
+    """One captured launch, replayed after the device lengths change, matches the
+    oracle for each set of lengths."""
+    from helpers import compare_o_lse
+    B, Lq, Tk, H, Hkv, hd = 3, 2, 1500, 8, 2, 128
+    q, k, v, _ = inputs("bf16", B, Lq, Tk, H, Hkv, hd, 907)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    lengths = torch.tensor([100, 100, 100], dtype=torch.int32, device="cuda")
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, Lq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(A.attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first call outside the capture (one-time set-up)
+        A.attn_decode_len(qd, kd, vd, lengths, H=H, Hkv=Hkv, o=o, lse=lse, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        A.attn_decode_len(qd, kd, vd, lengths, H=H, Hkv=Hkv, o=o, lse=lse, workspace=ws)
+    for lens in ([1500, 777, 1], [64, 1499, 300]):
+        lengths.copy_(torch.tensor(lens, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        st, word = A.attn_get_device_status()
+        assert st == A.OK, "device status word %#x" % word
+        o_ref, lse_ref = _decode_len_reference(q, k, v, lens, H, Hkv, hd)
+        compare_o_lse(o, lse, o_ref, lse_ref, "bf16", "graph replay lengths %s" % lens)
+
+
 def test_decode_short_cache_and_noncausal():
     run_fwd_case("bf16", 2, 2, 7, 4, 2, 64, causal=True, q_offset=5, decode=True, seed=700)
     run_fwd_case("f16", 2, 2, 130, 4, 2, 64, causal=False, q_offset=0, decode=True, seed=701)
