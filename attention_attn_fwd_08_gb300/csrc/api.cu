@@ -86,8 +86,11 @@ bool make_map(CUtensorMap* m, int dt, const void* base, long long inner, long lo
 // ------------------------------------------------------------- validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// decode_hd: the decode entry points also take hd 256 (16-bit types; their split kernel
+// is the only one built for it)
 attn_status check_common(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal,
-                         int window, float softcap, int q_offset, const float* key_mask, long long mstride) {
+                         int window, float softcap, int q_offset, const float* key_mask, long long mstride,
+                         bool decode_hd = false) {
     if (dt != ATTN_F32 && dt != ATTN_F16 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
     if (B < 0 || Tq < 0 || Tk < 0) return ATTN_ERR_INVALID_ARG;
     if (B > 65535) return ATTN_ERR_INVALID_ARG;
@@ -99,7 +102,7 @@ attn_status check_common(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, i
     if (mstride < 0) return ATTN_ERR_INVALID_ARG;
     if (key_mask && (reinterpret_cast<uintptr_t>(key_mask) & 3u)) return ATTN_ERR_INVALID_ARG;
     if ((long long)Tq + q_offset > INT32_MAX - 1) return ATTN_ERR_INVALID_ARG;
-    if (hd != 64 && hd != 128) return ATTN_ERR_UNSUPPORTED;
+    if (hd != 64 && hd != 128 && !(decode_hd && hd == 256 && dt != ATTN_F32)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
@@ -289,7 +292,7 @@ attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const void* v,
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv, int hd) {
-    if (B <= 0 || Lq <= 0 || Tk < 0 || H <= 0 || Hkv <= 0 || H % Hkv || (hd != 64 && hd != 128)) return 0;
+    if (B <= 0 || Lq <= 0 || Tk < 0 || H <= 0 || Hkv <= 0 || H % Hkv || (hd != 64 && hd != 128 && hd != 256)) return 0;
     int splits, chunk;
     decode_plan(B, Lq, Tk, H, Hkv, &splits, &chunk);
     return (size_t)B * H * Lq * splits * (hd + 2) * sizeof(float);
@@ -300,7 +303,7 @@ attn_status attn_decode(attn_dtype dt, const void* q, const void* k, const void*
                         float scale, int causal, int window, float softcap, int q_offset, const float* key_mask,
                         long long key_mask_bstride, void* stream) {
     attn_status st = check_common(dt, B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
-                                  key_mask_bstride);
+                                  key_mask_bstride, true);
     if (st != ATTN_OK) return st;
     if (Lq > 16 || (H / Hkv) * Lq > 64) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || Lq == 0) return ATTN_OK;
@@ -333,7 +336,7 @@ attn_status attn_decode_len(attn_dtype dt, const void* q, const void* k, const v
                             int hd, float scale, int causal, int window, float softcap, const int* lengths,
                             const float* key_mask, long long key_mask_bstride, void* stream) {
     attn_status st = check_common(dt, B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, 0, key_mask,
-                                  key_mask_bstride);
+                                  key_mask_bstride, true);
     if (st != ATTN_OK) return st;
     if (!lengths || (reinterpret_cast<uintptr_t>(lengths) & 3u)) return ATTN_ERR_INVALID_ARG;
     if (dt == ATTN_F32) return ATTN_ERR_UNSUPPORTED;  // the 16-bit split kernels only
@@ -368,7 +371,7 @@ attn_status attn_decode_noalloc(attn_dtype dt, const void* q, const void* k, con
                                 float softcap, int q_offset, const float* key_mask, long long key_mask_bstride,
                                 void* stream) {
     attn_status st = check_common(dt, B, Lq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
-                                  key_mask_bstride);
+                                  key_mask_bstride, true);
     if (st != ATTN_OK) return st;
     if (Lq > 16 || (H / Hkv) * Lq > 64) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || Lq == 0) return ATTN_OK;

@@ -377,6 +377,7 @@ cudaError_t decode_noalloc_scratch(float** out) {
 cudaError_t launch_decode(const Params& p, int dt, const DecMaps& maps, cudaStream_t s) {
     const bool bf16 = dt == 2;
     if (p.hd == 64) return bf16 ? decode_typed<true, 64>(p, maps, s) : decode_typed<false, 64>(p, maps, s);
+    if (p.hd == 256) return bf16 ? decode_typed<true, 256>(p, maps, s) : decode_typed<false, 256>(p, maps, s);
     return bf16 ? decode_typed<true, 128>(p, maps, s) : decode_typed<false, 128>(p, maps, s);
 }
 

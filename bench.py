@@ -366,6 +366,28 @@ def main():
         gbs = decode_bytes(wd) / (ms * 1e-3) / 1e9
         comps[name] = {"ms": ms, "GB/s": gbs, "frac_of_hbm_peak": gbs / peaks["hbm"], "bytes_per_call": decode_bytes(wd),
                        "note": "K/V (2 GiB) exceed L2; split + combine kernels timed together"}
+        if name == "decode_lq4":
+            # the same call with the cache lengths read on the device (all full here, so
+            # the bytes are the same): what a captured serving loop runs
+            lens = torch.full((wd.B,), wd.Tk, dtype=torch.int32, device=dev)
+            fl = lambda: A.attn_decode_len(qd_, kd_, vd_, lens, H=wd.H, Hkv=wd.Hkv, causal=True, o=od_, lse=lsed_,
+                                           workspace=wsd)
+            for _ in range(args.warmup):
+                fl()
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(args.steps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fl()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.mean(times)
+            gbs = decode_bytes(wd) / (ms * 1e-3) / 1e9
+            comps["decode_len_lq4"] = {"ms": ms, "GB/s": gbs, "frac_of_hbm_peak": gbs / peaks["hbm"],
+                                       "bytes_per_call": decode_bytes(wd),
+                                       "note": "attn_decode_len with every length = Tk (device-resident lengths)"}
         del qd_, kd_, vd_, od_, wsd
     st, word = A.attn_get_device_status()
     if st != A.OK:

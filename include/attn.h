@@ -154,8 +154,9 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv
  *   q, o      : [B][Lq][H*hd];  k, v : [B][Tk][Hkv*hd];  lse : [B][H][Lq] or NULL.
  *   workspace : device scratch of at least attn_decode_workspace_size() bytes,
  *               16-byte aligned.
- *   (H/Hkv)*Lq <= 64, hd 64 or 128; the rest as for attn_fwd.  The usual KV-cache
- *   call is causal with q_offset = Tk - Lq.
+ *   (H/Hkv)*Lq <= 64, hd 64, 128 or 256 (256: ATTN_BF16 / ATTN_F16 only); the
+ *   rest as for attn_fwd.  The usual KV-cache call is causal with q_offset =
+ *   Tk - Lq.
  */
 ATTN_API attn_status attn_decode(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
                         float* lse, void* workspace, size_t workspace_bytes, int B, int Lq,

@@ -106,6 +106,12 @@ def test_decode_len_validation():
     st = L.attn_decode_len(0, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 128, 0.1, 1, 0, 0.0, BAD,
                            None, 0, None)
     assert st == A.ERR_UNSUPPORTED
+    # hd 256: decode only, 16-bit only
+    st = L.attn_decode(0, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 256, 0.1, 1, 0, 0.0, 252,
+                       None, 0, None)
+    assert st == A.ERR_UNSUPPORTED
+    st = L.attn_fwd(2, BAD, BAD, BAD, BAD, None, 2, 4, 256, 8, 2, 256, 0.1, 1, 0, 0.0, 0, None, 0, None)
+    assert st == A.ERR_UNSUPPORTED
     # too long a query block
     st = L.attn_decode_len(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 17, 256, 8, 2, 128, 0.1, 1, 0, 0.0, BAD,
                            None, 0, None)
@@ -122,6 +128,7 @@ def test_workspace_sizes():
     n = A.attn_decode_workspace_size(16, 4, 32768, 32, 8, 128)
     assert n > 0 and n % (16 * 32 * 4 * 130 * 4) == 0
     assert A.attn_decode_workspace_size(1, 1, 100, 3, 2, 128) == 0  # Hkv does not divide H
+    assert A.attn_decode_workspace_size(2, 4, 1000, 8, 2, 256) > 0  # decode also takes hd 256
 
 
 def test_kernel_family_is_reported():

@@ -105,7 +105,7 @@ def test_bwd_fp32(flags):
 
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
 @pytest.mark.parametrize("Lq,H,Hkv", [(1, 8, 2), (4, 8, 2), (16, 4, 4), (4, 32, 8), (3, 12, 1)])
-@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("hd", [64, 128, 256])
 def test_decode(dt, Lq, H, Hkv, hd):
     Tk = 1000
     run_fwd_case(dt, 3, Lq, Tk, H, Hkv, hd, causal=True, q_offset=Tk - Lq, decode=True, seed=500 + Lq)
@@ -157,6 +157,19 @@ def test_decode_len_matches_oracle(flags):
     assert st == A.OK, "device status word %#x" % word
     o_ref, lse_ref = _decode_len_reference(q, k, v, lengths, H, Hkv, hd, km=km, **flags)
     compare_o_lse(o, lse, o_ref, lse_ref, "bf16", "decode_len %s" % flags)
+
+
+def test_decode_len_hd256_window_softcap():
+    from helpers import compare_o_lse
+    B, Lq, Tk, H, Hkv, hd = 3, 2, 900, 4, 2, 256
+    q, k, v, _ = inputs("f16", B, Lq, Tk, H, Hkv, hd, 908)
+    lengths = torch.tensor([900, 411, 1], dtype=torch.int32)
+    o, lse = A.attn_decode_len(q.cuda(), k.cuda(), v.cuda(), lengths.cuda(), H=H, Hkv=Hkv, window=200, softcap=30.0)
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    assert st == A.OK, "device status word %#x" % word
+    o_ref, lse_ref = _decode_len_reference(q, k, v, lengths, H, Hkv, hd, window=200, softcap=30.0)
+    compare_o_lse(o, lse, o_ref, lse_ref, "f16", "decode_len hd256")
 
 
 def test_decode_len_graph_replay_follows_lengths():
