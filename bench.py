@@ -2,11 +2,13 @@
 """Throughput of the fused-attention hot path on GB300.
 
 One step = one pass of the whole path over the GQA causal prefill workload
-(B=4, T=2048, H=32, Hkv=8, hd=128, bf16, LSE saved): attn_fwd, then the
-backward's three passes (D, dK/dV, dQ).  `value` is that step's algorithmic
-TFLOP/s (fwd 4*hd flops per visible (query,key) pair per head, fwd+bwd 3.5x
-that).  Decode (B=16, H=32, Hkv=8, hd=128, Lk=32768, Lq=1 and 4) is measured in
-the same run and reported in GB/s under "components".
+(B=4, T=2048, H=32, Hkv=8, hd=128, bf16, LSE saved), as a training step
+calls it: attn_fwd, then attn_bwd with its default passes (dQ, which forms D
+itself, then dK/dV).  `value` is that step's algorithmic TFLOP/s (fwd 4*hd
+flops per visible (query,key) pair per head, fwd+bwd 3.5x that).  Per-pass
+times, the sliding-window + softcap fwd/bwd, the key-masked encoder forward
+and decode (B=16, H=32, Hkv=8, hd=128, Lk=32768, Lq=1 and 4, in GB/s) are
+measured in the same run and reported under "components".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -275,16 +277,11 @@ def main():
     ws = torch.empty(A.attn_bwd_workspace_size(w.B, w.Tq, w.H), dtype=torch.uint8, device=dev)
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
-    phases = [
-        ("fwd", lambda: A.attn_fwd(q, k, v, o=o, lse=lse, **kw)),
-        ("preprocess", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=1, **kw)),
-        ("dkdv", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=2, **kw)),
-        ("dq", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=4, **kw)),
-    ]
-
     def step():
-        for _, fn in phases:
-            fn()
+        # what a training step calls: the forward, then the backward's default
+        # passes (dQ, which forms D itself, then dK/dV)
+        A.attn_fwd(q, k, v, o=o, lse=lse, **kw)
+        A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
 
     for _ in range(args.warmup):
         flush_buf.zero_()
@@ -295,7 +292,6 @@ def main():
         raise RuntimeError("device status word %#x after warm-up" % word)
 
     stream = torch.cuda.current_stream()
-    per_phase = {n: [] for n, _ in phases}
     steps_ms = []
     if world > 1:
         dist.barrier()
@@ -305,15 +301,12 @@ def main():
     with Clocks(local) as clk:
         for _ in range(args.steps):
             flush_buf.zero_()
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
-            evs[0].record(stream)
-            for i, (_, fn) in enumerate(phases):
-                fn()
-                evs[i + 1].record(stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
             torch.cuda.synchronize()
-            for i, (n, _) in enumerate(phases):
-                per_phase[n].append(evs[i].elapsed_time(evs[i + 1]))
-            steps_ms.append(evs[0].elapsed_time(evs[-1]))
+            steps_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     launches = A.attn_launch_count() - n0
@@ -328,16 +321,30 @@ def main():
     step_flops = 3.5 * FWD_FLOPS_PER_PAIR(w.hd) * pairs
     value = job_throughput(step_flops, world, ms_step)
 
+    # per-pass times, outside the step: the same passes in the step's order,
+    # one event between each, plus the standalone D pass (not part of the step)
+    passes = [
+        ("fwd", lambda: A.attn_fwd(q, k, v, o=o, lse=lse, **kw)),
+        ("dq", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=4, **kw)),
+        ("dkdv", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=2, **kw)),
+        ("preprocess", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=1, **kw)),
+    ]
+    per_pass = time_passes(torch, stream, passes, args, flush_buf)
     comps = {}
     for n in ("fwd", "dkdv", "dq"):
-        ms = statistics.mean(per_phase[n])
+        ms = per_pass[n]
         tf = KERNEL_FLOPS_PER_PAIR[n](w.hd) * pairs / (ms * 1e-3) / 1e12
         comps[n] = {"ms": ms, "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
                     "flops_per_launch": KERNEL_FLOPS_PER_PAIR[n](w.hd) * pairs}
-    pre_ms = statistics.mean(per_phase["preprocess"])
+    comps["dq"]["note"] = "includes D = rowsum(dO*O), formed inside the dQ kernel"
     pre_bytes = 2 * w.B * w.Tq * w.H * w.hd * 2 + w.B * w.H * w.Tq * 4
-    comps["preprocess"] = {"ms": pre_ms, "GB/s": pre_bytes / (pre_ms * 1e-3) / 1e9}
+    comps["preprocess"] = {"ms": per_pass["preprocess"], "GB/s": pre_bytes / (per_pass["preprocess"] * 1e-3) / 1e9,
+                           "note": "standalone D pass (attn_bwd phases=1); not run by the default backward"}
     comps["fwd_bwd_step"] = {"ms": ms_step, "TFLOP/s": value / world}
+
+    # ------------------------------------------- sliding window + softcap, key mask
+    if args.workload == "all":
+        comps.update(masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks))
 
     # ---------------------------------------------------------------- decode
     del flush_buf
@@ -429,6 +436,66 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def time_passes(torch, stream, passes, args, flush_buf):
+    """Mean ms of each pass, run back to back in order after an L2 flush, one event between each."""
+    for _ in range(args.warmup):
+        flush_buf.zero_()
+        for _, fn in passes:
+            fn()
+    torch.cuda.synchronize()
+    acc = {n: [] for n, _ in passes}
+    for _ in range(args.steps):
+        flush_buf.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
+        evs[0].record(stream)
+        for i, (_, fn) in enumerate(passes):
+            fn()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        for i, (n, _) in enumerate(passes):
+            acc[n].append(evs[i].elapsed_time(evs[i + 1]))
+    return {n: statistics.mean(t) for n, t in acc.items()}
+
+
+def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
+    """Sliding-window + softcap fwd/bwd (B=2 T=8192 H=16 Hkv=4 hd=128 window=1024 softcap=50, bf16) and the
+    bidirectional key-masked encoder forward (B=8 T=1024 H=Hkv=12 hd=64, fp16), flops over visible pairs."""
+    out = {}
+    ws_ = synth.WORKLOADS["swa_softcap"]
+    si = synth.make_inputs(ws_)
+    q, k, v, do = (si[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((ws_.B, ws_.H, ws_.Tq), dtype=torch.float32, device=dev)
+    wsb = torch.empty(A.attn_bwd_workspace_size(ws_.B, ws_.Tq, ws_.H), dtype=torch.uint8, device=dev)
+    kw = dict(H=ws_.H, Hkv=ws_.Hkv, scale=ws_.scale, causal=True, window=ws_.window, softcap=ws_.softcap)
+    t = time_passes(torch, stream, [
+        ("fwd", lambda: A.attn_fwd(q, k, v, o=o, lse=lse, **kw)),
+        ("bwd", lambda: A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=wsb, **kw))], args, flush_buf)
+    pairs = visible_pairs(ws_)
+    for n, fl in (("fwd", 4), ("bwd", 10)):
+        tf = fl * ws_.hd * pairs / (t[n] * 1e-3) / 1e12
+        out["swa_softcap_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                   "visible_pairs": pairs}
+    del q, k, v, do, o, dq, dk, dv, lse, wsb
+
+    we = synth.WORKLOADS["encoder_mask"]
+    ei = synth.make_inputs(we)
+    q, k, v = (ei[n].to(dev) for n in ("q", "k", "v"))
+    km = ei["key_mask"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((we.B, we.H, we.Tq), dtype=torch.float32, device=dev)
+    kw = dict(H=we.H, Hkv=we.Hkv, scale=we.scale, causal=False, key_mask=km)
+    t = time_passes(torch, stream, [("fwd", lambda: A.attn_fwd(q, k, v, o=o, lse=lse, **kw))], args, flush_buf)
+    pairs = visible_pairs(we, lengths=ei["lengths"].tolist())
+    tf = 4 * we.hd * pairs / (t["fwd"] * 1e-3) / 1e12
+    out["encoder_mask_fwd"] = {"ms": t["fwd"], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                               "visible_pairs": pairs, "note": "fp16; flops over unmasked keys only"}
+    st, word = A.attn_get_device_status()
+    if st != A.OK:
+        raise RuntimeError("device status word %#x after the masked workloads" % word)
+    return out
 
 
 def components_round(c):
