@@ -254,8 +254,8 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
     p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse_in = lse;
     p.dq = dq; p.dk = dk; p.dv = dv;
     p.tq_pad = (Tq + 63) / 64 * 64;
-    p.delta = static_cast<float*>(workspace);
-    p.lse2 = p.delta + (size_t)B * H * p.tq_pad;
+    p.ndelta = static_cast<float*>(workspace);
+    p.nlse2 = p.ndelta + (size_t)B * H * p.tq_pad;
     if (!use_tcgen05(dt, hd)) {
         // the fp32 dQ pass reads D from the workspace: pass 4 implies pass 1 there
         const int ph = (phases & 4) ? (phases | 1) : phases;

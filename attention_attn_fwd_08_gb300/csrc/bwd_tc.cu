@@ -56,7 +56,7 @@ struct KVCfg {
     static constexpr int kVOff = kKVBytes;
     static constexpr int kQOff = 2 * kKVBytes;
     static constexpr int kGOff = kQOff + kStages * kQBytes;   // dO ring
-    static constexpr int kStatOff = kGOff + kStages * kQBytes;  // [stage][2][BQ] floats: lse2, D
+    static constexpr int kStatOff = kGOff + kStages * kQBytes;  // [stage][2][BQ] floats: -LSE*log2e, -D
     static constexpr int kStatBytes = 2 * BQ * 4;
     static constexpr int kBarOff = kStatOff + kStages * kStatBytes;
     static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
@@ -151,11 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(sbase + C::kGOff + s * C::kQBytes + bx * (BQ * 128), &tmG, BAR(Q_FULL(s)),
                                     h * HD + bx * 64, i0, b);
                 }
-                // LSE*log2(e) and D of these 64 rows (padded rows: +inf and 0)
+                // -LSE*log2(e) and -D of these 64 rows (padded rows: -inf and 0)
                 const long long srow = ((long long)b * P.H + h) * P.tq_pad + i0;
                 const uint32_t sdst = sbase + C::kStatOff + s * C::kStatBytes;
-                if (elect_one()) bulk_load(sdst, P.lse2 + srow, BQ * 4, BAR(Q_FULL(s)));
-                if (elect_one()) bulk_load(sdst + BQ * 4, P.delta + srow, BQ * 4, BAR(Q_FULL(s)));
+                if (elect_one()) bulk_load(sdst, P.nlse2 + srow, BQ * 4, BAR(Q_FULL(s)));
+                if (elect_one()) bulk_load(sdst + BQ * 4, P.ndelta + srow, BQ * 4, BAR(Q_FULL(s)));
                 issued = n + 1;
             }
             mbar_wait(BAR(KV_FULL), 0, P.status, ST_TEARDOWN, nullptr);
@@ -229,6 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool key_live = j < P.Tk && (!P.key_mask || P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f);
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
+        const CapPoly cp = cap_poly(P.scale, P.softcap);
+        const uint64_t sl2_2 = f2_make(P.scale_log2, P.scale_log2), one2 = f2_make(1.f, 1.f);
         bool ok = true;
         for (int n = 0; n < ntiles; ++n) {
             const int bf = n & 1;
@@ -262,6 +264,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
             uint32_t pk[32], dk[32];
+            // With a softcap, the polynomial serves the tile unless a raw score of the
+            // row lies outside its range (checked before masking)
+            bool poly = false;
+            if (cap) {
+                float amax = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < BQ; cc += 2)
+                    amax = max3f(amax, fabsf(__uint_as_float(sv[cc >> 5][cc & 31])),
+                                 fabsf(__uint_as_float(sv[cc >> 5][(cc & 31) + 1])));
+                poly = __all_sync(0xffffffffu, amax <= cp.r_max);
+            }
             // In a tile where some pair is invisible, those scores become -inf first, so
             // every tile runs one copy of the element loop (a rarely run second copy
             // would be fetched into the instruction cache cold each time).
@@ -270,35 +283,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < BQ; ++cc)
                     sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi) ? sv[cc >> 5][cc & 31] : 0xff800000u;
+                poly = poly && cp.inf_ok;
             }
-            auto elems = [&](auto capc) {
-                constexpr bool kCap = decltype(capc)::value;
+            // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate.
+            // Pairs of columns go through the f32x2 unit together; the stats hold -LSE*log2e
+            // and -D, so x = st*log2e + nl and dS = P*(dP + nd)*(1 - tanh^2).
+            auto elems = [&](auto modec) {
+                constexpr int kMode = decltype(modec)::value;
 #pragma unroll
                 for (int c = 0; c < BQ; c += 2) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int cc = c + e;
-                        const float sval = __uint_as_float(sv[cc >> 5][cc & 31]);
-                        float x, dcap = 1.f;
-                        if constexpr (kCap) {
-                            // softcap*tanh(-inf) would be finite: keep a masked score at -inf
-                            const float t = tanh_accurate(sval * cap_in);
-                            x = sval == -INFINITY ? -INFINITY : P.softcap * t * kLog2e - st_l[cc];
-                            dcap = 1.f - t * t;
-                        } else {
-                            x = fmaf(sval, P.scale_log2, -st_l[cc]);
+                    const uint64_t nl = *reinterpret_cast<const uint64_t*>(st_l + c);
+                    const uint64_t nd = *reinterpret_cast<const uint64_t*>(st_d + c);
+                    const float s0 = __uint_as_float(sv[c >> 5][c & 31]), s1 = __uint_as_float(sv[c >> 5][(c & 31) + 1]);
+                    const uint64_t dp2 = f2_make(__uint_as_float(dp[c >> 5][c & 31]), __uint_as_float(dp[c >> 5][(c & 31) + 1]));
+                    float p0, p1, x0, x1;
+                    uint64_t dcap = one2;
+                    if constexpr (kMode == 2) {
+                        // softcap*tanh(-inf) would be finite: keep a masked score at -inf
+                        float l0, l1;
+                        f2_split(nl, l0, l1);
+                        const float t0 = tanh_accurate(s0 * cap_in), t1 = tanh_accurate(s1 * cap_in);
+                        x0 = s0 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t0, l0);
+                        x1 = s1 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t1, l1);
+                        dcap = f2_make(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
+                    } else {
+                        uint64_t g = f2_make(s0, s1);
+                        if constexpr (kMode == 1) {
+                            uint64_t uu;
+                            g = cap_g(cp, g, uu);
+                            // 1 - tanh^2; a masked score gives g = -inf and -inf here, with P = 0
+                            float d0, d1;
+                            f2_split(f2_fma(f2_mul(g, g), cp.nc2, one2), d0, d1);
+                            dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
                         }
-                        const float p = fast_exp2(x);
-                        pv[e] = p;
-                        dv[e] = p * (__uint_as_float(dp[cc >> 5][cc & 31]) - st_d[cc]) * dcap;
+                        f2_split(f2_fma(g, sl2_2, nl), x0, x1);
                     }
-                    pk[c >> 1] = pack2<BF16>(pv[0], pv[1]);
-                    dk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
+                    p0 = fast_exp2(x0);
+                    p1 = fast_exp2(x1);
+                    const uint64_t pp = f2_make(p0, p1);
+                    uint64_t ds = f2_mul(pp, f2_add(dp2, nd));
+                    if constexpr (kMode != 0) ds = f2_mul(ds, dcap);
+                    float q0, q1;
+                    f2_split(ds, q0, q1);
+                    pk[c >> 1] = pack2<BF16>(p0, p1);
+                    dk[c >> 1] = pack2<BF16>(q0, q1);
                 }
             };
-            if (cap) elems(std::integral_constant<bool, true>());
-            else elems(std::integral_constant<bool, false>());
+            if (!cap) elems(std::integral_constant<int, 0>());
+            else if (poly) elems(std::integral_constant<int, 1>());
+            else elems(std::integral_constant<int, 2>());
             tmem_st32(tbase + lane_off + bf * 64, pk);
             tmem_st32(tbase + lane_off + 128 + bf * 64, dk);
             tmem_st_wait();
@@ -479,9 +512,9 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         // ------------------------------- Q/dO/O producer and D (whole warp)
         // Loads the next item's tiles as soon as the current ones are in TMEM, then
         // forms D = rowsum(dO*O) of its 128 rows (lane l: rows l, l+32, l+64, l+96)
-        // into the first 512 bytes of the O tile, and writes D and LSE*log2(e) of
+        // into the first 512 bytes of the O tile, and writes -D and -LSE*log2(e) of
         // every row into the workspace for the dK/dV pass (rows that see no key and
-        // padding rows: D = 0, LSE = +inf).
+        // padding rows: D = 0, LSE = -inf).
         if (elect_one()) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmG);
@@ -490,13 +523,13 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         auto stats = [&](const DqItem& it, int i2, float dval) {
             if (i2 >= P.tq_pad) return;
             const long long srow = ((long long)it.b * P.H + it.h) * P.tq_pad + i2;
-            float l2 = INFINITY;
+            float nl2 = -INFINITY;
             if (i2 < P.Tq) {
                 const float l = P.lse_in[((long long)it.b * P.H + it.h) * P.Tq + i2];
-                l2 = l == -INFINITY ? INFINITY : l * kLog2e;
+                nl2 = l == -INFINITY ? -INFINITY : -l * kLog2e;
             }
-            P.delta[srow] = i2 < P.Tq ? dval : 0.f;
-            P.lse2[srow] = l2;
+            P.ndelta[srow] = i2 < P.Tq ? -dval : 0.f;
+            P.nlse2[srow] = nl2;
         };
         int qn = 0;  // Q/dO/O loads so far
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
@@ -662,6 +695,8 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
+        const CapPoly cp = cap_poly(P.scale, P.softcap);
+        const uint64_t sl2_2 = f2_make(P.scale_log2, P.scale_log2), one2 = f2_make(1.f, 1.f);
         bool ok = true;
         int gt = 0, act = 0, qc = 0;  // tiles, active items and Q/dO copies so far
         int copied = -1;              // item whose Q and dO are in TMEM
@@ -722,6 +757,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 lse2 = l_copied == -INFINITY ? INFINITY : l_copied * kLog2e;
                 Dd = d_copied;
             }
+            const uint64_t nl2 = f2_make(-lse2, -lse2), nd2 = f2_make(-Dd, -Dd);
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int t = gt + n, bf = t & 1;
                 const int jt = (it.kt0 + n) * BK;
@@ -752,39 +788,63 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 tmem_pin(sv);
                 tmem_pin(dp);
                 uint32_t dsk[16];
+                // with a softcap, the polynomial serves the tile unless a raw score of the
+                // row lies outside its range (checked before masking)
+                bool poly = false;
+                if (cap) {
+                    float amax = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < 32; cc += 2)
+                        amax = max3f(amax, fabsf(__uint_as_float(sv[cc])), fabsf(__uint_as_float(sv[cc + 1])));
+                    poly = __all_sync(0xffffffffu, amax <= cp.r_max);
+                }
                 // invisible pairs become -inf scores first: one copy of the element loop
                 const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= 32;
                 if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc)
                         sv[cc] = (cc >= clo && cc < chi && ((mbits >> cc) & 1u)) ? sv[cc] : 0xff800000u;
+                    poly = poly && cp.inf_ok;
                 }
-                auto elems = [&](auto capc) {
-                    constexpr bool kCap = decltype(capc)::value;
+                // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate.
+                // Pairs of columns go through the f32x2 unit together.
+                auto elems = [&](auto modec) {
+                    constexpr int kMode = decltype(modec)::value;
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
-                        float dv[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int cc = c + e;
-                            const float sval = __uint_as_float(sv[cc]);
-                            float x, dcap = 1.f;
-                            if constexpr (kCap) {
-                                // softcap*tanh(-inf) would be finite: keep a masked score at -inf
-                                const float t = tanh_accurate(sval * cap_in);
-                                x = sval == -INFINITY ? -INFINITY : P.softcap * t * kLog2e - lse2;
-                                dcap = 1.f - t * t;
-                            } else {
-                                x = fmaf(sval, P.scale_log2, -lse2);
+                        const float s0 = __uint_as_float(sv[c]), s1 = __uint_as_float(sv[c + 1]);
+                        const uint64_t dp2 = f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
+                        float x0, x1;
+                        uint64_t dcap = one2;
+                        if constexpr (kMode == 2) {
+                            // softcap*tanh(-inf) would be finite: keep a masked score at -inf
+                            const float t0 = tanh_accurate(s0 * cap_in), t1 = tanh_accurate(s1 * cap_in);
+                            x0 = s0 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t0, -lse2);
+                            x1 = s1 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t1, -lse2);
+                            dcap = f2_make(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
+                        } else {
+                            uint64_t g = f2_make(s0, s1);
+                            if constexpr (kMode == 1) {
+                                uint64_t uu;
+                                g = cap_g(cp, g, uu);
+                                // 1 - tanh^2; a masked score gives g = -inf and -inf here, with P = 0
+                                float d0, d1;
+                                f2_split(f2_fma(f2_mul(g, g), cp.nc2, one2), d0, d1);
+                                dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
                             }
-                            const float pr = fast_exp2(x);
-                            dv[e] = pr * (__uint_as_float(dp[cc]) - Dd) * dcap;
+                            f2_split(f2_fma(g, sl2_2, nl2), x0, x1);
                         }
-                        dsk[c >> 1] = pack2<BF16>(dv[0], dv[1]);
+                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                        uint64_t ds = f2_mul(f2_make(p0, p1), f2_add(dp2, nd2));
+                        if constexpr (kMode != 0) ds = f2_mul(ds, dcap);
+                        float q0, q1;
+                        f2_split(ds, q0, q1);
+                        dsk[c >> 1] = pack2<BF16>(q0, q1);
                     }
                 };
-                if (cap) elems(std::integral_constant<bool, true>());
-                else elems(std::integral_constant<bool, false>());
+                if (!cap) elems(std::integral_constant<int, 0>());
+                else if (poly) elems(std::integral_constant<int, 1>());
+                else elems(std::integral_constant<int, 2>());
                 // packed into the first 16 of the 32 columns this warp read (the partner
                 // warp may still be loading the other 32)
                 tmem_st16(tbase + lane_off + bf * 64 + 32 * hf, dsk);
@@ -867,7 +927,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     }
 }
 
-// Pass 4 (dQ) forms D and LSE*log2(e) itself and writes them into the
+// Pass 4 (dQ) forms D and LSE*log2(e) itself and writes them (negated) into the
 // workspace, so with pass 4 requested pass 1 is not run separately, and dQ goes
 // before dK/dV, which reads them.
 template <bool BF16, int HD>

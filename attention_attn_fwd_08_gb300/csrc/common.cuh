@@ -28,9 +28,9 @@ struct Params {
     void* dq;
     void* dk;
     void* dv;
-    float* delta;        // backward: D = rowsum(dO*O)       [B*H][tq_pad]
-    float* lse2;         // backward: LSE*log2(e), +inf where LSE = -inf  [B*H][tq_pad]
-    int tq_pad;          // backward: Tq rounded up to 64 (row stride of delta / lse2)
+    float* ndelta;       // backward: -D = -rowsum(dO*O)     [B*H][tq_pad]
+    float* nlse2;        // backward: -LSE*log2(e), -inf where LSE = -inf  [B*H][tq_pad]
+    int tq_pad;          // backward: Tq rounded up to 64 (row stride of ndelta / nlse2)
     float* ws;           // decode: split partials
     const float* key_mask;
     long long mask_bstride;
@@ -143,7 +143,6 @@ __host__ __device__ __forceinline__ bool tile_full(int causal, int window, int T
     return true;
 }
 
-// Capped score in log2 units: x = s*scale (natural), returns st*log2(e).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -160,6 +159,83 @@ __device__ __forceinline__ float fast_rcp(float x) {
 __device__ __forceinline__ float tanh_accurate(float x) {
     float e = fast_exp2(x * 2.8853900817779268f);  // 2*log2(e)
     return 1.0f - 2.0f * fast_rcp(e + 1.0f);
+}
+
+// softcap * tanh(y) for small |y| without the two MUFU operations of
+// tanh_accurate: tanh(y) = y * (1 + t * R(t)), t = y^2, R a cubic fitted to
+// (tanh(y)/y - 1)/t on |y| <= kTanhPolyY (weighted least squares on Chebyshev
+// nodes, weights chosen for the relative error of tanh; that error stays below
+// 2e-8 there, under fp32 rounding).  Callers check the range and fall back to
+// tanh_accurate for larger |y|.  The leading coefficient is positive, so a
+// score of -inf still maps to -inf through every form built on it below.
+constexpr float kTanhPolyY = 0.5f;
+constexpr float kTanhR0 = -0.3333313623f, kTanhR1 = 0.1332571191f, kTanhR2 = -0.0530346934f,
+                kTanhR3 = 0.0172199592f;
+
+// ------------------------------------------------- packed fp32 pairs (f32x2)
+// The sm_100 family issues add/mul/fma on two fp32 values held in one 64-bit
+// register as one instruction.
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t a, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Per-launch constants of the softcapped score for a raw score r = q.k, with
+// c = scale/softcap: tanh(c*r) = c*g, g = r + r*u*S(u), u = r^2 and
+// S(u) = c^2*R(c^2*u).  The capped score in log2 units is then sl2*g
+// (sl2 = scale*log2 e) and the softcap derivative 1 - c^2*g^2.
+struct CapPoly {
+    uint64_t s0, s1, s2, s3;  // S's coefficients, both halves equal
+    uint64_t nc2;             // -c^2, both halves
+    float u_max, r_max;       // the polynomial serves u <= u_max, i.e. |r| <= r_max
+    bool inf_ok;              // S(+inf) = +inf, so a -inf score stays -inf through g
+};
+__device__ __forceinline__ CapPoly cap_poly(float scale, float softcap) {
+    const float c = scale / fmaxf(softcap, 1e-30f), c2 = c * c;
+    const float k0 = c2 * kTanhR0, k1 = c2 * c2 * kTanhR1, k2 = c2 * c2 * c2 * kTanhR2,
+                k3 = c2 * c2 * c2 * c2 * kTanhR3;
+    CapPoly cp;
+    cp.s0 = f2_make(k0, k0);
+    cp.s1 = f2_make(k1, k1);
+    cp.s2 = f2_make(k2, k2);
+    cp.s3 = f2_make(k3, k3);
+    cp.nc2 = f2_make(-c2, -c2);
+    cp.r_max = fminf(kTanhPolyY / c, 1e18f);
+    cp.u_max = cp.r_max * cp.r_max;
+    cp.inf_ok = k3 > 0.f;
+    return cp;
+}
+// g of a pair of raw scores (see CapPoly)
+__device__ __forceinline__ uint64_t cap_g(const CapPoly& cp, uint64_t r, uint64_t& u) {
+    u = f2_mul(r, r);
+    uint64_t sp = f2_fma(u, cp.s3, cp.s2);
+    sp = f2_fma(u, sp, cp.s1);
+    sp = f2_fma(u, sp, cp.s0);
+    return f2_fma(r, f2_mul(u, sp), r);
 }
 
 // --------------------------------------------------------------- timing

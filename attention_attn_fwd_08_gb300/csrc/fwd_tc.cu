@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
         const float sl2 = P.scale_log2;
+        const uint64_t sl2_2 = f2_make(sl2, sl2);
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         const float cap_out = P.softcap * kLog2e;
@@ -357,7 +358,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // Masking: in a tile that some row does not see whole, the invisible scores
         // are overwritten with -inf in TMEM first, so every tile then runs the same
         // softmax code (one hot copy of the unrolled loop instead of one per case).
-        auto mask_tile = [&](int clo, int chi, const uint32_t(&mbits)[4]) {
+        auto mask_tile = [&](int clo, int chi, const uint32_t(&mbits)[4]) -> bool {
             // visibility bits of columns 32c .. 32c+31: [clo, chi) and the key mask
             uint32_t vw[4];
 #pragma unroll
@@ -367,7 +368,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
                 vw[c] = below_hi & ~below_lo & mbits[c];
             }
-            // two 32-column chunks per step, both loads in flight together
+            // two 32-column chunks per step, both loads in flight together; with a
+            // softcap also the largest raw |score| (before masking) of the row
+            float amax = 0.f;
 #pragma unroll 1
             for (int c = 0; c < 4; c += 2) {
                 uint32_t t0[32], t1[32];
@@ -376,6 +379,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 tmem_ld_wait_only();
                 tmem_pin(t0);
                 tmem_pin(t1);
+                if (cap) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2)
+                        amax = max3f(amax, max3f(fabsf(__uint_as_float(t0[e])), fabsf(__uint_as_float(t0[e + 1])),
+                                                 fabsf(__uint_as_float(t1[e]))),
+                                     fabsf(__uint_as_float(t1[e + 1])));
+                }
                 const uint32_t w0 = c == 0 ? vw[0] : vw[2], w1 = c == 0 ? vw[1] : vw[3];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
@@ -386,32 +396,48 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 tmem_st32(tS + lane_off + c * 32 + 32, t1);
             }
             tmem_st_wait();
+            const CapPoly cp = cap_poly(P.scale, P.softcap);
+            return !cp.inf_ok || !(amax <= cp.r_max);
         };
-        // P = exp2(x) with x = s*scale*log2(e) - ms (or softcap*tanh(s*scale/softcap)*log2(e)
-        // - ms), as 16-bit pairs in registers; S stays intact in TMEM until the caller
-        // stores P over it.  Returns the row sum and the row max of x (-inf: nothing seen).
+        // P = exp2(x) with x = s*scale*log2(e) - ms, or with the capped score
+        // softcap*tanh(s*scale/softcap)*log2(e) in place of s*scale*log2(e), as 16-bit
+        // pairs in registers; S stays intact in TMEM until the caller stores P over it.
+        // Mode 0: no softcap; 1: softcap by the polynomial (umax returns the largest
+        // squared raw score, which must lie in its range); 2: softcap by tanh_accurate.
+        // Pairs of scores go through the f32x2 unit together.  Returns the row sum and
+        // the row max of x (-inf: nothing seen).
         uint32_t pk[4][16];
-        auto p_pass = [&](auto capc, float ms, float& rsum, float& xmax) {
-            constexpr bool kCap = decltype(capc)::value;
-            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+        auto p_pass = [&](auto modec, float ms, float& rsum, float& xmax, float& umax) {
+            constexpr int kMode = decltype(modec)::value;
+            const CapPoly cp = cap_poly(P.scale, P.softcap);
+            const uint64_t nms = f2_make(-ms, -ms);
+            uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
             float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float um[2] = {0.f, 0.f};
             auto chunk = [&](int c, const uint32_t(&t)[32]) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float r0 = __uint_as_float(t[2 * e]), r1 = __uint_as_float(t[2 * e + 1]);
                     float x0, x1;
-                    if constexpr (kCap) {
+                    if constexpr (kMode == 2) {
                         // a masked score is -inf, and softcap*tanh(-inf) would be finite
                         x0 = r0 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r0 * cap_in), -ms);
                         x1 = r1 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r1 * cap_in), -ms);
                     } else {
-                        x0 = fmaf(r0, sl2, -ms);
-                        x1 = fmaf(r1, sl2, -ms);
+                        uint64_t rr = f2_make(r0, r1);
+                        if constexpr (kMode == 1) {
+                            uint64_t uu;
+                            rr = cap_g(cp, rr, uu);
+                            float u0, u1;
+                            f2_split(uu, u0, u1);
+                            um[e & 1] = max3f(um[e & 1], u0, u1);
+                        }
+                        f2_split(f2_fma(rr, sl2_2, nms), x0, x1);
                     }
-                    mr[e & 3] = fmaxf(mr[e & 3], fmaxf(x0, x1));
+                    mr[e & 3] = max3f(mr[e & 3], x0, x1);
                     const float p0 = fast_exp2(x0);  // ex2(-inf) = 0
                     const float p1 = fast_exp2(x1);
-                    rs4[e & 3] += p0 + p1;
+                    rs2[e & 1] = f2_add(rs2[e & 1], f2_make(p0, p1));
                     pk[c][e] = pack2<BF16>(p0, p1);
                 }
             };
@@ -428,19 +454,39 @@ __global__ void __launch_bounds__(kThreads2, 1)
             chunk(2, ta);
             tmem_ld_wait(tb);
             chunk(3, tb);
-            rsum = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+            float a0, a1, b0, b1;
+            f2_split(rs2[0], a0, a1);
+            f2_split(rs2[1], b0, b1);
+            rsum = (a0 + b0) + (a1 + b1);
             xmax = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+            umax = fmaxf(um[0], um[1]);
         };
         // One pass against the row's reference m (log2 units, starting at 0).  The
         // reference moves only when P would leave [2^-2, 2^8] at the row max: a max
         // above 2^8 (any tile), or a first tile whose max is below 2^-2.  Then O is
         // rescaled, the reference moved to the max and the tile redone from the
-        // scores still in TMEM; for ordinary inputs this never happens.
-        auto run_tile = [&](auto capc, float& m_used, float& l, int k) {
-            float rs, xm;
-            p_pass(capc, m_used, rs, xm);
-            const bool resc = xm > kRescaleHi || (l == 0.f && xm < kRescaleLo && xm != -INFINITY);
-            if (__any_sync(0xffffffffu, resc)) {
+        // scores still in TMEM; for ordinary inputs this never happens.  With a
+        // softcap the polynomial pass is redone by tanh_accurate when a raw score of
+        // the row lies outside its range (raw_big: found by the mask pass of a masked
+        // tile, whose -inf scores say nothing about the range).
+        auto run_tile = [&](auto capc, float& m_used, float& l, int k, bool masked, bool raw_big) {
+            constexpr bool kCap = decltype(capc)::value;
+            const float u_max = kCap ? cap_poly(P.scale, P.softcap).u_max : 0.f;
+            float rs, xm, um;
+            bool accurate = false;
+#pragma unroll 1
+            for (int pass = 0; pass < 3; ++pass) {
+                if (kCap && accurate) p_pass(std::integral_constant<int, 2>(), m_used, rs, xm, um);
+                else p_pass(std::integral_constant<int, kCap ? 1 : 0>(), m_used, rs, xm, um);
+                if (kCap && !accurate) {
+                    const bool big = masked ? raw_big : !(um <= u_max);
+                    if (__any_sync(0xffffffffu, big)) {
+                        accurate = true;
+                        continue;
+                    }
+                }
+                const bool resc = xm > kRescaleHi || (l == 0.f && xm < kRescaleLo && xm != -INFINITY);
+                if (!__any_sync(0xffffffffu, resc)) break;
                 // S_u(k) completed after P_u(k-1) V(k-1): O_u holds every earlier tile.
                 // Rows that have seen nothing yet hold O = 0 and keep alpha = 1 (their
                 // reference may move down by any amount).
@@ -460,7 +506,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         tmem_st32(tO + lane_off + c * 32, orr);
                     }
                 }
-                p_pass(capc, m_used, rs, xm);
             }
             l += rs;
 #pragma unroll
@@ -486,7 +531,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
             float m_used = 0.f, l = 0.f;
             for (int k = 0; k < my.ntiles; ++k) {
                 const int j0 = (my.t0 + k) * BN;
-                const bool full = tile_full(P.causal, P.window, P.Tk, prow0, prow1, j0, j0 + BN) && !P.key_mask;
                 uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
                 if (P.key_mask) {
                     const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
@@ -496,6 +540,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
                     }
                 }
+                // a tile whose keys the mask keeps whole needs no mask pass
+                const bool full = tile_full(P.causal, P.window, P.Tk, prow0, prow1, j0, j0 + BN) &&
+                                  (mbits[0] & mbits[1] & mbits[2] & mbits[3]) == 0xffffffffu;
                 // this row's visible columns of the tile: [clo, chi), and the key-mask bits
                 int clo = 0, chi = BN;
                 if (!full) {
@@ -520,9 +567,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                 }
                 tc_fence_after();
-                if (!full) mask_tile(clo, chi, mbits);
-                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k);
-                else run_tile(std::integral_constant<bool, false>(), m_used, l, k);
+                const bool raw_big = full ? false : mask_tile(clo, chi, mbits);
+                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, !full, raw_big);
+                else run_tile(std::integral_constant<bool, false>(), m_used, l, k, !full, raw_big);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();

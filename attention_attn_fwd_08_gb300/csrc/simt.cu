@@ -167,13 +167,13 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(Params P) {
     if (!live || sub != 0) return;
     const long long srow = ((long long)b * P.H + h) * P.tq_pad + i;
     if (i >= P.Tq) {
-        P.delta[srow] = 0.f;
-        P.lse2[srow] = INFINITY;
+        P.ndelta[srow] = 0.f;
+        P.nlse2[srow] = -INFINITY;
         return;
     }
-    P.delta[srow] = acc;
+    P.ndelta[srow] = -acc;
     const float l = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
-    P.lse2[srow] = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+    P.nlse2[srow] = l == -INFINITY ? -INFINITY : -l * 1.4426950408889634f;
 }
 
 // -------------------------------------------------------------- backward: dQ
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
     }
     const long long srow = ((long long)b * P.H + h) * P.Tq + i;
     const float lse = row_ok ? P.lse_in[srow] : -INFINITY;
-    const float Dd = row_ok ? P.delta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
+    const float Dd = row_ok ? -P.ndelta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
     const bool live = row_ok && lse != -INFINITY;
     float acc[HD / 32];
 #pragma unroll
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
                 const int i = i0 + ii;
                 const long long srow = ((long long)b * P.H + h) * P.Tq + i;
                 Ls[ii] = i < P.Tq ? P.lse_in[srow] : -INFINITY;
-                Ds[ii] = i < P.Tq ? P.delta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
+                Ds[ii] = i < P.Tq ? -P.ndelta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
             }
             __syncthreads();
 #pragma unroll

@@ -98,8 +98,8 @@ ATTN_API attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const
                      int causal, int window, float softcap, int q_offset, const float* key_mask,
                      long long key_mask_bstride, void* stream);
 
-/* Bytes of scratch attn_bwd needs: D = rowsum(dO * O) and LSE*log2(e), one fp32
- * each per (b, h, i), rows padded to a multiple of 64 queries. */
+/* Bytes of scratch attn_bwd needs: -D = -rowsum(dO * O) and -LSE*log2(e), one
+ * fp32 each per (b, h, i), rows padded to a multiple of 64 queries. */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Tq, int H);
 
 /*
@@ -125,7 +125,7 @@ ATTN_API attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const
 /*
  * The three passes of attn_bwd, selectable one at a time (same arguments).
  * phases is a bit set: 1 = D = rowsum(dO*O) and LSE*log2(e) into the
- * workspace, 2 = dK/dV, 4 = dQ.  Pass 4 forms D and LSE*log2(e) itself and
+ * workspace (stored negated), 2 = dK/dV, 4 = dQ.  Pass 4 forms D and LSE*log2(e) itself and
  * leaves them in the workspace (so with 4 set, 1 is implied and, on the
  * 16-bit path, not run as a pass of its own); pass 2 alone reads the workspace
  * an earlier pass 1 or 4 with the same arguments wrote.  Requested passes run

@@ -96,6 +96,14 @@ def test_bwd_many_items_per_cta(flags):
     run_fwd_case("bf16", 4, 300, 300, 32, 8, 128, backward=True, seed=310, **flags)
 
 
+@pytest.mark.parametrize("dt,hd", [("bf16", 128), ("f16", 64)])
+def test_softcap_polynomial_and_fallback_mix(dt, hd):
+    """A softcap of 8 puts about one raw score q.k in 10^4 outside the range of the
+    kernels' tanh polynomial (|q.k| * scale / softcap > 1/2), so within one call
+    some warps' tiles take the exp-based tanh and the rest the polynomial."""
+    run_fwd_case(dt, 2, 390, 390, 4, 2, hd, backward=True, causal=True, window=300, softcap=8.0, seed=320)
+
+
 @pytest.mark.parametrize("flags", BWD_FLAGS[:3], ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
 def test_bwd_fp32(flags):
     Tq = 150
