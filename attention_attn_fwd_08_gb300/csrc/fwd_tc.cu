@@ -355,138 +355,90 @@ __global__ void __launch_bounds__(kThreads2, 1)
         bool ok = true;
         int sc = 0;   // S_FULL(u) phases consumed
         int act = 0;  // items in which this tile was active so far (O_DONE phases)
-        // Masking: in a tile that some row does not see whole, the invisible scores
-        // are overwritten with -inf in TMEM first, so every tile then runs the same
-        // softmax code (one hot copy of the unrolled loop instead of one per case).
-        auto mask_tile = [&](int clo, int chi, const uint32_t(&mbits)[4]) -> bool {
-            // visibility bits of columns 32c .. 32c+31: [clo, chi) and the key mask
-            uint32_t vw[4];
+        // One tile's softmax, one thread per row.  The row's 128 scores come out of
+        // TMEM into registers in one go (four loads in flight), so P can be written
+        // over S chunk by chunk as it is formed.  Pass 1 takes the row max (after the
+        // invisible scores are set to -inf, in tiles that some row does not see
+        // whole); pass 2 forms P = exp2(x) with x = s*scale*log2(e) - m, or with the
+        // capped score softcap*tanh(s*scale/softcap)*log2(e) in place of
+        // s*scale*log2(e), pairs of scores through the f32x2 unit together.
+        //   The reference m (log2 units, starting at 0) moves only when P would leave
+        // [2^-2, 2^8] at the row max: a max above 2^8 (any tile), or a first tile whose
+        // max is below 2^-2; then O is rescaled in TMEM first.  For ordinary inputs
+        // this never happens.  The softcap takes the fitted tanh polynomial unless a
+        // raw score of the warp's rows lies outside its range (mode 2: tanh_accurate).
+        auto run_tile = [&](auto capc, float& m_used, float& l, int k, bool full, int clo, int chi,
+                            const uint32_t(&mbits)[4]) {
+            constexpr bool kCap = decltype(capc)::value;
+            uint32_t sv[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int lo = min(max(clo - 32 * c, 0), 32), hi = min(max(chi - 32 * c, 0), 32);
-                const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
-                const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
-                vw[c] = below_hi & ~below_lo & mbits[c];
-            }
-            // two 32-column chunks per step, both loads in flight together; with a
-            // softcap also the largest raw |score| (before masking) of the row
-            float amax = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < 4; c += 2) {
-                uint32_t t0[32], t1[32];
-                tmem_ld32(tS + lane_off + c * 32, t0);
-                tmem_ld32(tS + lane_off + c * 32 + 32, t1);
-                tmem_ld_wait_only();
-                tmem_pin(t0);
-                tmem_pin(t1);
-                if (cap) {
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sv[c]);
+            tmem_ld_wait_only();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
+            bool accurate = false;
+            if constexpr (kCap) {
+                // largest raw |score| of the row, before masking
+                float amax = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2)
-                        amax = max3f(amax, max3f(fabsf(__uint_as_float(t0[e])), fabsf(__uint_as_float(t0[e + 1])),
-                                                 fabsf(__uint_as_float(t1[e]))),
-                                     fabsf(__uint_as_float(t1[e + 1])));
-                }
-                const uint32_t w0 = c == 0 ? vw[0] : vw[2], w1 = c == 0 ? vw[1] : vw[3];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    t0[e] = ((w0 >> e) & 1u) ? t0[e] : 0xff800000u;  // -inf
-                    t1[e] = ((w1 >> e) & 1u) ? t1[e] : 0xff800000u;
-                }
-                tmem_st32(tS + lane_off + c * 32, t0);
-                tmem_st32(tS + lane_off + c * 32 + 32, t1);
+                        amax = max3f(amax, fabsf(__uint_as_float(sv[c][e])), fabsf(__uint_as_float(sv[c][e + 1])));
+                const CapPoly cp = cap_poly(P.scale, P.softcap);
+                accurate = __any_sync(0xffffffffu, !(amax <= cp.r_max)) || (!full && !cp.inf_ok);
             }
-            tmem_st_wait();
-            const CapPoly cp = cap_poly(P.scale, P.softcap);
-            return !cp.inf_ok || !(amax <= cp.r_max);
-        };
-        // P = exp2(x) with x = s*scale*log2(e) - ms, or with the capped score
-        // softcap*tanh(s*scale/softcap)*log2(e) in place of s*scale*log2(e), as 16-bit
-        // pairs in registers; S stays intact in TMEM until the caller stores P over it.
-        // Mode 0: no softcap; 1: softcap by the polynomial (umax returns the largest
-        // squared raw score, which must lie in its range); 2: softcap by tanh_accurate.
-        // Pairs of scores go through the f32x2 unit together.  Returns the row sum and
-        // the row max of x (-inf: nothing seen).
-        uint32_t pk[4][16];
-        auto p_pass = [&](auto modec, float ms, float& rsum, float& xmax, float& umax) {
-            constexpr int kMode = decltype(modec)::value;
-            const CapPoly cp = cap_poly(P.scale, P.softcap);
-            const uint64_t nms = f2_make(-ms, -ms);
-            uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
-            float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            float um[2] = {0.f, 0.f};
-            auto chunk = [&](int c, const uint32_t(&t)[32]) {
+            if (!full) {
+                // visibility bits of columns 32c .. 32c+31: [clo, chi) and the key mask
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float r0 = __uint_as_float(t[2 * e]), r1 = __uint_as_float(t[2 * e + 1]);
-                    float x0, x1;
-                    if constexpr (kMode == 2) {
-                        // a masked score is -inf, and softcap*tanh(-inf) would be finite
-                        x0 = r0 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r0 * cap_in), -ms);
-                        x1 = r1 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r1 * cap_in), -ms);
-                    } else {
-                        uint64_t rr = f2_make(r0, r1);
-                        if constexpr (kMode == 1) {
-                            uint64_t uu;
-                            rr = cap_g(cp, rr, uu);
-                            float u0, u1;
-                            f2_split(uu, u0, u1);
-                            um[e & 1] = max3f(um[e & 1], u0, u1);
-                        }
-                        f2_split(f2_fma(rr, sl2_2, nms), x0, x1);
+                for (int c = 0; c < 4; ++c) {
+                    const int lo = min(max(clo - 32 * c, 0), 32), hi = min(max(chi - 32 * c, 0), 32);
+                    const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+                    const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
+                    const uint32_t vw = below_hi & ~below_lo & mbits[c];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sv[c][e] = ((vw >> e) & 1u) ? sv[c][e] : 0xff800000u;  // -inf
+                }
+            }
+            // pass 1: the row max of the scores, as x against the current reference
+            float rmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; e += 2)
+                    rmax = max3f(rmax, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+            // x is increasing in the score, so its row max is x(rmax)
+            auto to_x = [&](auto modec, uint64_t rr, uint64_t nms) -> uint64_t {
+                constexpr int kMode = decltype(modec)::value;
+                if constexpr (kMode == 2) {
+                    float r0, r1;
+                    f2_split(rr, r0, r1);
+                    float m0, m1;
+                    f2_split(nms, m0, m1);
+                    // a masked score is -inf, and softcap*tanh(-inf) would be finite
+                    return f2_make(r0 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r0 * cap_in), m0),
+                                   r1 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r1 * cap_in), m1));
+                } else {
+                    if constexpr (kMode == 1) {
+                        const CapPoly cp = cap_poly(P.scale, P.softcap);
+                        uint64_t uu;
+                        rr = cap_g(cp, rr, uu);
                     }
-                    mr[e & 3] = max3f(mr[e & 3], x0, x1);
-                    const float p0 = fast_exp2(x0);  // ex2(-inf) = 0
-                    const float p1 = fast_exp2(x1);
-                    rs2[e & 1] = f2_add(rs2[e & 1], f2_make(p0, p1));
-                    pk[c][e] = pack2<BF16>(p0, p1);
+                    return f2_fma(rr, sl2_2, nms);
                 }
             };
-            uint32_t ta[32], tb[32];
-            tmem_ld32(tS + lane_off + 0 * 32, ta);
-            tmem_ld_wait(ta);
-            tmem_ld32(tS + lane_off + 1 * 32, tb);
-            chunk(0, ta);
-            tmem_ld_wait(tb);
-            tmem_ld32(tS + lane_off + 2 * 32, ta);
-            chunk(1, tb);
-            tmem_ld_wait(ta);
-            tmem_ld32(tS + lane_off + 3 * 32, tb);
-            chunk(2, ta);
-            tmem_ld_wait(tb);
-            chunk(3, tb);
-            float a0, a1, b0, b1;
-            f2_split(rs2[0], a0, a1);
-            f2_split(rs2[1], b0, b1);
-            rsum = (a0 + b0) + (a1 + b1);
-            xmax = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
-            umax = fmaxf(um[0], um[1]);
-        };
-        // One pass against the row's reference m (log2 units, starting at 0).  The
-        // reference moves only when P would leave [2^-2, 2^8] at the row max: a max
-        // above 2^8 (any tile), or a first tile whose max is below 2^-2.  Then O is
-        // rescaled, the reference moved to the max and the tile redone from the
-        // scores still in TMEM; for ordinary inputs this never happens.  With a
-        // softcap the polynomial pass is redone by tanh_accurate when a raw score of
-        // the row lies outside its range (raw_big: found by the mask pass of a masked
-        // tile, whose -inf scores say nothing about the range).
-        auto run_tile = [&](auto capc, float& m_used, float& l, int k, bool masked, bool raw_big) {
-            constexpr bool kCap = decltype(capc)::value;
-            const float u_max = kCap ? cap_poly(P.scale, P.softcap).u_max : 0.f;
-            float rs, xm, um;
-            bool accurate = false;
-#pragma unroll 1
-            for (int pass = 0; pass < 3; ++pass) {
-                if (kCap && accurate) p_pass(std::integral_constant<int, 2>(), m_used, rs, xm, um);
-                else p_pass(std::integral_constant<int, kCap ? 1 : 0>(), m_used, rs, xm, um);
-                if (kCap && !accurate) {
-                    const bool big = masked ? raw_big : !(um <= u_max);
-                    if (__any_sync(0xffffffffu, big)) {
-                        accurate = true;
-                        continue;
-                    }
-                }
-                const bool resc = xm > kRescaleHi || (l == 0.f && xm < kRescaleLo && xm != -INFINITY);
-                if (!__any_sync(0xffffffffu, resc)) break;
+            float xm, xm_;
+            {
+                const uint64_t r2 = f2_make(rmax, rmax), n2 = f2_make(-m_used, -m_used);
+                uint64_t x2;
+                if (!kCap) x2 = to_x(std::integral_constant<int, 0>(), r2, n2);
+                else if (!accurate) x2 = to_x(std::integral_constant<int, 1>(), r2, n2);
+                else x2 = to_x(std::integral_constant<int, 2>(), r2, n2);
+                f2_split(x2, xm, xm_);
+            }
+            if (rmax == -INFINITY) xm = -INFINITY;
+            const bool resc = xm > kRescaleHi || (l == 0.f && xm < kRescaleLo && xm != -INFINITY);
+            if (__any_sync(0xffffffffu, resc)) {
                 // S_u(k) completed after P_u(k-1) V(k-1): O_u holds every earlier tile.
                 // Rows that have seen nothing yet hold O = 0 and keep alpha = 1 (their
                 // reference may move down by any amount).
@@ -507,9 +459,33 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                 }
             }
-            l += rs;
+            // pass 2: P chunk by chunk, each 16-bit chunk stored over S as soon as formed
+            auto p_pass = [&](auto modec) {
+                const uint64_t nms = f2_make(-m_used, -m_used);
+                uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_st16(tS + lane_off + c * 16, pk[c]);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float x0, x1;
+                        f2_split(to_x(modec, f2_make(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), nms),
+                                 x0, x1);
+                        const float p0 = fast_exp2(x0);  // ex2(-inf) = 0
+                        const float p1 = fast_exp2(x1);
+                        rs2[e & 1] = f2_add(rs2[e & 1], f2_make(p0, p1));
+                        pk[e] = pack2<BF16>(p0, p1);
+                    }
+                    tmem_st16(tS + lane_off + c * 16, pk);
+                }
+                float a0, a1, b0, b1;
+                f2_split(rs2[0], a0, a1);
+                f2_split(rs2[1], b0, b1);
+                l += (a0 + b0) + (a1 + b1);
+            };
+            if (!kCap) p_pass(std::integral_constant<int, 0>());
+            else if (!accurate) p_pass(std::integral_constant<int, 1>());
+            else p_pass(std::integral_constant<int, 2>());
         };
         // The two tiles' softmaxes alternate A(k), B(k), A(k+1), ... within an item, so
         // each runs while the tensor core works on the other tile's P.V and next S;
@@ -567,9 +543,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                 }
                 tc_fence_after();
-                const bool raw_big = full ? false : mask_tile(clo, chi, mbits);
-                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, !full, raw_big);
-                else run_tile(std::integral_constant<bool, false>(), m_used, l, k, !full, raw_big);
+                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits);
+                else run_tile(std::integral_constant<bool, false>(), m_used, l, k, full, clo, chi, mbits);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
