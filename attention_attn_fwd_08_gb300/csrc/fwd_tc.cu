@@ -368,14 +368,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // this never happens.  The softcap takes the fitted tanh polynomial unless a
         // raw score of the warp's rows lies outside its range (mode 2: tanh_accurate).
         auto run_tile = [&](auto capc, float& m_used, float& l, int k, bool full, int clo, int chi,
-                            const uint32_t(&mbits)[4]) {
+                            const uint32_t(&mbits)[4], uint32_t(&sv)[4][32]) {
             constexpr bool kCap = decltype(capc)::value;
-            uint32_t sv[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sv[c]);
-            tmem_ld_wait_only();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
             bool accurate = false;
             if constexpr (kCap) {
                 // largest raw |score| of the row, before masking
@@ -487,10 +481,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
             else if (!accurate) p_pass(std::integral_constant<int, 1>());
             else p_pass(std::integral_constant<int, 2>());
         };
-        // The two tiles' softmaxes alternate A(k), B(k), A(k+1), ... within an item, so
-        // each runs while the tensor core works on the other tile's P.V and next S;
-        // left alone they fall into lockstep and the tensor core idles during both.
+        // Without a softcap at hd 128 the two tiles' softmaxes alternate A(k), B(k),
+        // A(k+1), ... within an item, so each runs while the tensor core works on the
+        // other tile's P.V and next S; left alone they fall into lockstep and the
+        // tensor core idles during both.  The longer softcap softmax (and the shorter
+        // MMAs of hd 64) do better with both warpgroups issuing at once (measured).
         // base[u] counts tile u's softmaxes in earlier items.
+        const bool alternate = !cap && HD == 128;
         int base[2] = {0, 0};
         for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
             const FwdItem it = fwd_item(P, w);
@@ -534,17 +531,25 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     break;
                 }
                 ++sc;
-                if (u == 0 ? (k >= 1 && k - 1 < nB) : (k < nA)) {
+                tc_fence_after();
+                // the row's 128 scores, loaded while this tile waits for its turn
+                uint32_t sv[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sv[c]);
+                if (alternate && (u == 0 ? (k >= 1 && k - 1 < nB) : (k < nA))) {
                     const int need = 4 * (u == 0 ? bB + k : bA + k + 1);  // warp arrivals
                     const bool rr = count_wait(&done_count[u ^ 1], need, P.status, ST_FWD_SOFTMAX, &abort_flag);
                     if (!__all_sync(0xffffffffu, rr)) {
+                        tmem_ld_wait_only();
                         ok = false;
                         break;
                     }
                 }
-                tc_fence_after();
-                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits);
-                else run_tile(std::integral_constant<bool, false>(), m_used, l, k, full, clo, chi, mbits);
+                tmem_ld_wait_only();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
+                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits, sv);
+                else run_tile(std::integral_constant<bool, false>(), m_used, l, k, full, clo, chi, mbits, sv);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
