@@ -166,3 +166,45 @@ def bwd(q, k, v, do, *, H, Hkv, scale, causal=False, window=0, softcap=0.0, q_of
     if rc != 0:
         raise ValueError("oracle_attn_bwd rejected its arguments")
     return dq, dk, dv
+
+
+def varlen_fwd(q, k, v, cu_q, cu_k, *, H, Hkv, scale, causal=False, window=0, softcap=0.0):
+    """Packed variable-length forward (brotensor ops/flash_attention.h,
+    flash_attention_varlen_forward): sequence b is rows cu_q[b] .. cu_q[b+1]-1 of
+    q [total_q, H*hd] and rows cu_k[b] .. cu_k[b+1]-1 of k/v, attended to as its
+    own batch of one with query positions counted from its first row; nothing
+    crosses sequences.  Returns O [total_q, H*hd] (zero on rows outside every
+    sequence) and LSE as a list of [H, Tq_b] arrays, one per sequence."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    hd = q.shape[1] // H
+    o = np.zeros_like(q)
+    lses = []
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if q1 == q0:
+            lses.append(np.zeros((H, 0)))
+            continue
+        if k1 == k0:  # no key at all: every row fully masked (O = 0, LSE = -inf)
+            lses.append(np.full((H, q1 - q0), -np.inf))
+            continue
+        ob, lb = fwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], H=H, Hkv=Hkv, scale=scale, causal=causal,
+                     window=window, softcap=softcap)
+        o[q0:q1] = ob[0]
+        lses.append(lb[0])
+    return o, lses
+
+
+def varlen_bwd(q, k, v, do, cu_q, cu_k, *, H, Hkv, scale, causal=False, window=0, softcap=0.0):
+    """Backward of varlen_fwd (brotensor flash_attention_varlen_backward: the
+    per-sequence backward; excluded positions contribute nothing).  Returns dQ,
+    dK, dV on the packed rows, zero outside every sequence."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if q1 == q0 or k1 == k0:
+            continue
+        gq, gk, gv = bwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], do[None, q0:q1], H=H, Hkv=Hkv, scale=scale,
+                         causal=causal, window=window, softcap=softcap)
+        dq[q0:q1], dk[k0:k1], dv[k0:k1] = gq[0], gk[0], gv[0]
+    return dq, dk, dv
