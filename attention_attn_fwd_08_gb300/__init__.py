@@ -20,7 +20,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_bwd_workspace_size", "attn_decode_workspace_size",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_bwd_workspace_size", "attn_decode_workspace_size",
            "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_launch_count", "AttnError", "lib",
            "library_path"]
 
@@ -70,6 +70,10 @@ def lib():
         L.attn_decode.restype = i
         L.attn_decode_len.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + [i] * 6 + [f, i, i, f, vp, vp, ll, vp]
         L.attn_decode_len.restype = i
+        L.attn_varlen_fwd.argtypes = [i] + [vp] * 7 + [i] * 8 + [f, i, i, f, vp]
+        L.attn_varlen_fwd.restype = i
+        L.attn_varlen_bwd.argtypes = [i] + [vp] * 10 + [sz, vp, vp] + [i] * 8 + [f, i, i, f, vp]
+        L.attn_varlen_bwd.restype = i
         L.attn_status_string.argtypes = [i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -254,6 +258,64 @@ def attn_decode_len(q, k, v, lengths, *, H, Hkv, scale=None, causal=True, window
                                _stream(stream))
     _check(st, "attn_decode_len")
     return o, lse
+
+
+def _varlen_dims(q, k, cu_q, cu_k, H, Hkv):
+    torch = _torch()
+    if q.dim() != 2 or k.dim() != 2:
+        raise ValueError("packed q must be [total_q, H*hd] and k/v [total_k, Hkv*hd]")
+    if q.shape[1] % H or k.shape[1] % Hkv or q.shape[1] // H != k.shape[1] // Hkv:
+        raise ValueError("inconsistent shapes: q %s, k %s, H=%d, Hkv=%d" % (tuple(q.shape), tuple(k.shape), H, Hkv))
+    for c in (cu_q, cu_k):
+        if c.dtype != torch.int32 or c.dim() != 1 or not c.is_contiguous():
+            raise ValueError("cu_seqlens must be contiguous int32 [batch+1]")
+    if cu_q.numel() != cu_k.numel() or cu_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have batch+1 entries")
+    return cu_q.numel() - 1, q.shape[0], k.shape[0], q.shape[1] // H
+
+
+def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, H, Hkv, scale=None,
+                    causal=False, window=0, softcap=0.0, o=None, lse=None, want_lse=True, stream=None):
+    """Packed variable-length forward: sequence b owns rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+    of q/o and cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k/v (int32 device prefix sums); no
+    attention across sequences.  Returns (o, lse), lse [batch, H, max_seqlen_q].  Rows of o
+    outside every sequence are left as they were."""
+    torch = _torch()
+    _contig(q, k, v, o, lse)
+    batch, total_q, total_k, hd = _varlen_dims(q, k, cu_seqlens_q, cu_seqlens_k, H, Hkv)
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((batch, H, max_seqlen_q), dtype=torch.float32, device=q.device)
+    st = lib().attn_varlen_fwd(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                               _ptr(cu_seqlens_k), batch, int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, H,
+                               Hkv, hd, float(scale), int(bool(causal)), int(window), float(softcap), _stream(stream))
+    _check(st, "attn_varlen_fwd")
+    return o, lse
+
+
+def attn_varlen_bwd(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, H, Hkv,
+                    scale=None, causal=False, window=0, softcap=0.0, dq=None, dk=None, dv=None, workspace=None,
+                    stream=None):
+    """Backward of attn_varlen_fwd; returns (dq, dk, dv), overwritten on every sequence's rows."""
+    torch = _torch()
+    _contig(q, k, v, o, do, lse, dq, dk, dv)
+    batch, total_q, total_k, hd = _varlen_dims(q, k, cu_seqlens_q, cu_seqlens_k, H, Hkv)
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = attn_bwd_workspace_size(batch, int(max_seqlen_q), H)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = lib().attn_varlen_bwd(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), batch, int(max_seqlen_q), int(max_seqlen_k),
+                               total_q, total_k, H, Hkv, hd, float(scale), int(bool(causal)), int(window),
+                               float(softcap), _stream(stream))
+    _check(st, "attn_varlen_bwd")
+    return dq, dk, dv
 
 
 def attn_get_device_status(stream=None):

@@ -289,6 +289,110 @@ attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const void* v,
                            hd, scale, causal, window, softcap, q_offset, key_mask, key_mask_bstride, stream, 7);
 }
 
+// ------------------------------------------------------ packed sequences
+// The dense kernels run on the packed tensors as one batch of total rows; each
+// work item reads its sequence's bounds from cu_seqlens on the device (Seq in
+// common.cuh).  Launch shapes come from batch and the max_seqlen bounds.
+namespace {
+
+attn_status check_varlen(attn_dtype dt, const int* cu_q, const int* cu_k, int batch, int max_q, int max_k,
+                         int total_q, int total_k, int H, int Hkv, int hd, float scale, int causal, int window,
+                         float softcap) {
+    attn_status st = check_common(dt, batch, max_q, max_k, H, Hkv, hd, scale, causal, window, softcap, 0, nullptr, 0);
+    if (st != ATTN_OK) return st;
+    if (total_q < 0 || total_k < 0 || max_q > total_q || max_k > total_k) return ATTN_ERR_INVALID_ARG;
+    if (batch > 0 && (!cu_q || !cu_k)) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_k) & 3u))
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+Params varlen_params(const int* cu_q, const int* cu_k, int batch, int max_q, int max_k, int total_q, int total_k,
+                     int H, int Hkv, int hd, float scale, int causal, int window, float softcap) {
+    Params p = base_params(batch, max_q, max_k, H, Hkv, hd, scale, causal, window, softcap, 0, nullptr, 0);
+    p.cu_q = cu_q;
+    p.cu_k = cu_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    return p;
+}
+
+}  // namespace
+
+attn_status attn_varlen_fwd(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int max_seqlen_q,
+                            int max_seqlen_k, int total_q, int total_k, int H, int Hkv, int hd, float scale,
+                            int causal, int window, float softcap, void* stream) {
+    attn_status st = check_varlen(dt, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k, total_q,
+                                  total_k, H, Hkv, hd, scale, causal, window, softcap);
+    if (st != ATTN_OK) return st;
+    if (batch == 0 || max_seqlen_q == 0 || total_q == 0) return ATTN_OK;
+    if (!q || !o || (total_k > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
+        return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Params p = varlen_params(cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k, total_q, total_k, H,
+                             Hkv, hd, scale, causal, window, softcap);
+    if (!p.status) return ATTN_ERR_CUDA;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    // no keys anywhere: the CUDA-core kernel writes O = 0 and LSE = -inf per row
+    if (!use_tcgen05(dt, hd) || max_seqlen_k == 0 || total_k == 0)
+        return counted(launch_simt_fwd(p, (int)dt, s), 1);
+    FwdMaps maps;
+    if (!make_map(&maps.q, dt, q, (long long)H * hd, total_q, 1, 128) ||
+        !make_map(&maps.k, dt, k, (long long)Hkv * hd, total_k, 1, 128) ||
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, total_k, 1, 128) ||
+        !make_map(&maps.o, dt, o, (long long)H * hd, total_q, 1, 32))
+        return ATTN_ERR_CUDA;
+    return counted(launch_tc_fwd(p, (int)dt, maps, s), 1);
+}
+
+attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                            int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int H, int Hkv, int hd,
+                            float scale, int causal, int window, float softcap, void* stream) {
+    attn_status st = check_varlen(dt, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k, total_q,
+                                  total_k, H, Hkv, hd, scale, causal, window, softcap);
+    if (st != ATTN_OK) return st;
+    if (batch == 0 || (total_q == 0 && total_k == 0)) return ATTN_OK;
+    const size_t ws_need = attn_bwd_workspace_size(batch, max_seqlen_q, H);
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || (!workspace && ws_need > 0))
+        return ATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_need) return ATTN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    for (const void* x : ptrs)
+        if (!aligned16(x)) return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Params p = varlen_params(cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, max_seqlen_k, total_q, total_k, H,
+                             Hkv, hd, scale, causal, window, softcap);
+    if (!p.status) return ATTN_ERR_CUDA;
+    p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse_in = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.tq_pad = (max_seqlen_q + 63) / 64 * 64;
+    p.ndelta = static_cast<float*>(workspace);
+    p.nlse2 = p.ndelta + (size_t)batch * H * p.tq_pad;
+    // with no query rows or no key rows anywhere, the CUDA-core kernels write the
+    // zero gradients of whatever rows the sequences have
+    if (!use_tcgen05(dt, hd) || max_seqlen_q == 0 || max_seqlen_k == 0 || total_q == 0 || total_k == 0)
+        return counted(launch_simt_bwd(p, (int)dt, 7, s), 3);
+    BwdMaps maps;
+    if (!make_map(&maps.q, dt, q, (long long)H * hd, total_q, 1, 128) ||
+        !make_map(&maps.dout, dt, dout, (long long)H * hd, total_q, 1, 128) ||
+        !make_map(&maps.k, dt, k, (long long)Hkv * hd, total_k, 1, 128) ||
+        !make_map(&maps.v, dt, v, (long long)Hkv * hd, total_k, 1, 128) ||
+        !make_map(&maps.q64, dt, q, (long long)H * hd, total_q, 1, 64) ||
+        !make_map(&maps.dout64, dt, dout, (long long)H * hd, total_q, 1, 64) ||
+        !make_map(&maps.k64, dt, k, (long long)Hkv * hd, total_k, 1, 64) ||
+        !make_map(&maps.v64, dt, v, (long long)Hkv * hd, total_k, 1, 64) ||
+        !make_map(&maps.dq32, dt, dq, (long long)H * hd, total_q, 1, 32) ||
+        !make_map(&maps.o, dt, o, (long long)H * hd, total_q, 1, 128) ||
+        !make_map(&maps.dk32, dt, dk, (long long)Hkv * hd, total_k, 1, 32) ||
+        !make_map(&maps.dv32, dt, dv, (long long)Hkv * hd, total_k, 1, 32))
+        return ATTN_ERR_CUDA;
+    return counted(launch_tc_bwd(p, (int)dt, maps, 7, s), 2);
+}
+
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv, int hd) {
@@ -409,7 +513,8 @@ attn_status attn_get_device_status(void* stream, unsigned int* detail) {
     const unsigned int zero = 0;
     if (cudaMemcpy(ptr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return ATTN_ERR_CUDA;
     if (detail) *detail = word;
-    return word ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    if (word & ~(unsigned int)ST_VARLEN_BOUNDS) return ATTN_ERR_TIMEOUT;
+    return word ? ATTN_ERR_INVALID_ARG : ATTN_OK;
 }
 
 attn_status attn_selftest_bounded_wait(unsigned int timeout_us, void* stream) {

@@ -66,7 +66,9 @@ struct KVCfg {
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
-template <bool BF16, int HD>
+// VL: packed variable-length sequences (cu_seqlens); the dense instantiation
+// carries none of their bookkeeping.
+template <bool BF16, int HD, bool VL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -95,8 +97,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kb = (int)(blockIdx.x % (unsigned)(P.Hkv * P.B));
     const int kvh = kb % P.Hkv, b = kb / P.Hkv;
     const int j0 = (int)(blockIdx.x / (unsigned)(P.Hkv * P.B)) * BKV;
+    const Seq sq = seq_of<VL>(P, b);
+    if (j0 >= sq.tk) return;  // (packed) past this sequence's keys: nothing to write
     int qlo, qhi;
-    query_range(P.causal, P.window, P.Tq, P.q_offset, j0, min(j0 + BKV, P.Tk), &qlo, &qhi);
+    query_range(P.causal, P.window, sq.tq, P.q_offset, j0, min(j0 + BKV, sq.tk), &qlo, &qhi);
     const int qt0 = qlo / BQ;
     const int nqt = qhi > qlo ? (qhi + BQ - 1) / BQ - qt0 : 0;
     const int ntiles = nqt * P.G;  // (head, query tile) pairs, head-major
@@ -131,9 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
                 if (elect_one())
-                    tma_load_3d(sbase + C::kKOff + bx * (BKV * 128), &tmK, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
+                    tma_load_3d(sbase + C::kKOff + bx * (BKV * 128), &tmK, BAR(KV_FULL), kvh * HD + bx * 64,
+                                sq.k0 + j0, sq.zb);
                 if (elect_one())
-                    tma_load_3d(sbase + C::kVOff + bx * (BKV * 128), &tmV, BAR(KV_FULL), kvh * HD + bx * 64, j0, b);
+                    tma_load_3d(sbase + C::kVOff + bx * (BKV * 128), &tmV, BAR(KV_FULL), kvh * HD + bx * 64,
+                                sq.k0 + j0, sq.zb);
             }
             int issued = 0;
             for (int n = 0; n < ntiles; ++n) {
@@ -146,10 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int bx = 0; bx < C::kBoxes; ++bx) {
                     if (elect_one())
                         tma_load_3d(sbase + C::kQOff + s * C::kQBytes + bx * (BQ * 128), &tmQ, BAR(Q_FULL(s)),
-                                    h * HD + bx * 64, i0, b);
+                                    h * HD + bx * 64, sq.q0 + i0, sq.zb);
                     if (elect_one())
                         tma_load_3d(sbase + C::kGOff + s * C::kQBytes + bx * (BQ * 128), &tmG, BAR(Q_FULL(s)),
-                                    h * HD + bx * 64, i0, b);
+                                    h * HD + bx * 64, sq.q0 + i0, sq.zb);
                 }
                 // -LSE*log2(e) and -D of these 64 rows (padded rows: -inf and 0)
                 const long long srow = ((long long)b * P.H + h) * P.tq_pad + i0;
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = warp * 32 + lane;
         const int j = j0 + r;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        const bool key_live = j < P.Tk && (!P.key_mask || P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f);
+        const bool key_live = j < sq.tk && (!P.key_mask || P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f);
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         const CapPoly cp = cap_poly(P.scale, P.softcap);
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int bf = n & 1;
             const int h = tile_head(n), i0 = tile_i0(n);
             // visible query columns of this key row in the tile
-            int clo = 0, chi = min(BQ, P.Tq - i0);
+            int clo = 0, chi = min(BQ, sq.tq - i0);
             if (P.causal) clo = max(clo, j - P.q_offset - i0);
             if (P.window > 0) {
                 chi = min(chi, j + P.window - P.q_offset - i0);
@@ -344,6 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // per tiled store (rows past Tk are not written).
         const bool have = ok && ntiles > 0 && warp_wait(BAR(ACC_DONE), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
         if (have) tc_fence_after();
+        // A packed sequence's last keys may share a 32-row slice with the next
+        // sequence's first: such a slice goes out row by row (this sequence's rows
+        // only).  Dense tensors end where the maps end, which clips the tiled store.
+        const bool whole = !VL || j0 + warp * 32 + 32 <= sq.tk;
         if (have || (ok && ntiles == 0)) {
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
@@ -361,6 +371,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < HD / 32; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) acc[c][e] = 0u;
+                }
+                if (!whole) {
+                    if (j < sq.tk) {
+                        uint4* row = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(part == 0 ? P.dv : P.dk) +
+                                                              ((long long)sq.k0 + j) * P.Hkv * HD + (long long)kvh * HD);
+#pragma unroll
+                        for (int w4 = 0; w4 < HD / 8; ++w4) {
+                            uint32_t q4[4];
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int col = w4 * 8 + 2 * t;
+                                q4[t] = pack2<BF16>(__uint_as_float(acc[col >> 5][col & 31]) * mul,
+                                                    __uint_as_float(acc[col >> 5][(col & 31) + 1]) * mul);
+                            }
+                            row[w4] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+                        }
+                    }
+                    continue;
                 }
 #pragma unroll
                 for (int half = 0; half < HD / 64; ++half) {
@@ -384,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (elect_one()) {
-                        tma_store_3d(part == 0 ? &tmDV : &tmDK, slice, kvh * HD + half * 64, j0 + warp * 32, b);
+                        tma_store_3d(part == 0 ? &tmDV : &tmDK, slice, kvh * HD + half * 64, sq.k0 + j0 + warp * 32,
+                                     sq.zb);
                         bulk_commit_group();
                     }
                 }
@@ -427,8 +456,9 @@ struct QCfg {
 // see.  Items are numbered longest first (every head's last query block first).
 struct DqItem {
     int b, h, kvh, i0, kt0, ntiles;
+    Seq sq;
 };
-template <int BQ, int BK>
+template <int BQ, int BK, bool VL>
 __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
     DqItem it;
     const int nqb = (P.Tq + BQ - 1) / BQ;
@@ -438,8 +468,11 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
     it.b = hb / P.H;
     it.kvh = it.h / P.G;
     it.i0 = qb * BQ;
-    int lo, hi;
-    key_range(P.causal, P.window, P.Tk, it.i0 + P.q_offset, min(it.i0 + BQ, P.Tq) - 1 + P.q_offset, &lo, &hi);
+    it.sq = seq_of<VL>(P, it.b);
+    int lo = 0, hi = 0;
+    if (it.i0 < it.sq.tq)  // (packed) items past a sequence's rows have no tiles
+        key_range(P.causal, P.window, it.sq.tk, it.i0 + P.q_offset, min(it.i0 + BQ, it.sq.tq) - 1 + P.q_offset, &lo,
+                  &hi);
     it.kt0 = lo / BK;
     it.ntiles = hi > lo ? (hi + BK - 1) / BK - it.kt0 : 0;
     return it;
@@ -453,7 +486,7 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
 // are loaded into shared memory once the current ones are in TMEM, and copied
 // into TMEM right after the current item's last dS, so its first S and dP run
 // while the current item's epilogue reads dQ out.
-template <bool BF16, int HD>
+template <bool BF16, int HD, bool VL>
 __global__ void __launch_bounds__(kThreadsDQ, 1)
     bwd_dq_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -524,16 +557,16 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             if (i2 >= P.tq_pad) return;
             const long long srow = ((long long)it.b * P.H + it.h) * P.tq_pad + i2;
             float nl2 = -INFINITY;
-            if (i2 < P.Tq) {
+            if (i2 < it.sq.tq) {
                 const float l = P.lse_in[((long long)it.b * P.H + it.h) * P.Tq + i2];
                 nl2 = l == -INFINITY ? -INFINITY : -l * kLog2e;
             }
-            P.ndelta[srow] = i2 < P.Tq ? -dval : 0.f;
+            P.ndelta[srow] = i2 < it.sq.tq ? -dval : 0.f;
             P.nlse2[srow] = nl2;
         };
         int qn = 0;  // Q/dO/O loads so far
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w);
             if (it.ntiles == 0) {
 #pragma unroll
                 for (int m = 0; m < BQ / 32; ++m) stats(it, it.i0 + m * 32 + lane, 0.f);
@@ -544,14 +577,14 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
                 if (elect_one())
-                    tma_load_3d(sbase + C::kQOff + bx * (BQ * 128), &tmQ, BAR(QG_FULL), it.h * HD + bx * 64, it.i0,
-                                it.b);
+                    tma_load_3d(sbase + C::kQOff + bx * (BQ * 128), &tmQ, BAR(QG_FULL), it.h * HD + bx * 64,
+                                it.sq.q0 + it.i0, it.sq.zb);
                 if (elect_one())
-                    tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), it.h * HD + bx * 64, it.i0,
-                                it.b);
+                    tma_load_3d(sbase + C::kGOff + bx * (BQ * 128), &tmG, BAR(QG_FULL), it.h * HD + bx * 64,
+                                it.sq.q0 + it.i0, it.sq.zb);
                 if (elect_one())
-                    tma_load_3d(sbase + C::kOOff + bx * (BQ * 128), &tmO, BAR(QG_FULL), it.h * HD + bx * 64, it.i0,
-                                it.b);
+                    tma_load_3d(sbase + C::kOOff + bx * (BQ * 128), &tmO, BAR(QG_FULL), it.h * HD + bx * 64,
+                                it.sq.q0 + it.i0, it.sq.zb);
             }
             ++qn;
             if (!warp_wait(BAR(QG_FULL), (qn - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) break;
@@ -593,7 +626,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         bool ok = true;
         int g = 0;  // K/V tiles loaded so far
         for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w);
             for (int n = 0; n < it.ntiles; ++n) {
                 const int s = g % NS, use = g / NS;
                 if (use > 0 && !warp_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) {
@@ -606,10 +639,10 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 for (int bx = 0; bx < C::kBoxes; ++bx) {
                     if (elect_one())
                         tma_load_3d(sbase + C::kKOff + s * C::kKBytes + bx * (BK * 128), &tmK, BAR(KV_FULL(s)),
-                                    it.kvh * HD + bx * 64, jt, it.b);
+                                    it.kvh * HD + bx * 64, it.sq.k0 + jt, it.sq.zb);
                     if (elect_one())
                         tma_load_3d(sbase + C::kVOff + s * C::kKBytes + bx * (BK * 128), &tmV, BAR(KV_FULL(s)),
-                                    it.kvh * HD + bx * 64, jt, it.b);
+                                    it.kvh * HD + bx * 64, it.sq.k0 + jt, it.sq.zb);
                 }
                 ++g;
             }
@@ -649,7 +682,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         bool ok = true;
         int gt = 0, act = 0;
         for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w);
             if (it.ntiles == 0) continue;
             ok = wait_all(QT_READY, act & 1);
             if (ok) ok = issue_one(gt);
@@ -704,7 +737,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         float l_copied = -INFINITY;   // its LSE, loaded with the copy (used at the item's start)
         auto load_lse = [&](const DqItem& it2) -> float {
             const int i2 = it2.i0 + r;
-            return i2 < P.Tq ? P.lse_in[((long long)it2.b * P.H + it2.h) * P.Tq + i2] : -INFINITY;
+            return i2 < it2.sq.tq ? P.lse_in[((long long)it2.b * P.H + it2.h) * P.Tq + i2] : -INFINITY;
         };
         // copy this thread's row of Q (hf 0) or dO (hf 1), 128-byte-swizzled smem, into
         // TMEM; both halves also form D of the row from dO and O in shared memory
@@ -736,7 +769,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             if (lane == 0) mbar_arrive(BAR(QT_READY));
             // issued here, consumed at the item's start: the latency hides behind
             // the current item's epilogue
-            l_copied = load_lse(dq_item<BQ, BK>(P, w2));
+            l_copied = load_lse(dq_item<BQ, BK, VL>(P, w2));
             if (!warp_wait(BAR(D_FULL), qc & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) return false;
             d_copied = reinterpret_cast<const float*>(smem + C::kOOff)[r];
             ++qc;
@@ -746,10 +779,11 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             return true;
         };
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w);
             const int i = it.i0 + r;
             const int p = i + P.q_offset;
-            const bool row_ok = i < P.Tq;
+            const int tq = it.sq.tq, tk = it.sq.tk;
+            const bool row_ok = i < tq;
             const int ntiles = it.ntiles;
             float lse2 = INFINITY, Dd = 0.f;
             if (ntiles > 0 && copied != w) ok = copy_q(w);
@@ -767,9 +801,9 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 if (P.key_mask) {
                     const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
                     const int j = jc + lane;
-                    mbits = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
+                    mbits = __ballot_sync(0xffffffffu, j < tk && mrow[j] > 0.5f);
                 }
-                int clo = 0, chi = min(32, P.Tk - jc);
+                int clo = 0, chi = min(32, tk - jc);
                 if (P.causal) chi = min(chi, p - jc + 1);
                 if (P.window > 0) {
                     clo = max(clo, p - P.window + 1 - jc);
@@ -857,7 +891,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             // every S and dP of this item completed (their results were read above):
             // put the next active item's Q and dO into TMEM before this epilogue
             for (int k2 = k_ + 1, w2 = snake_item(k2); ntiles > 0 && w2 < nitems; w2 = snake_item(++k2)) {
-                if (dq_item<BQ, BK>(P, w2).ntiles == 0) continue;
+                if (dq_item<BQ, BK, VL>(P, w2).ntiles == 0) continue;
                 ok = copy_q(w2);
                 break;
             }
@@ -898,8 +932,19 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(DQ_EMPTY));
             }
+            // A packed sequence's last rows may share a 32-row slice with the next
+            // sequence's first (or lie past its end): such a slice goes out row by row,
+            // this sequence's rows only.  Dense tensors end where the map ends.
+            const bool whole = !VL || it.i0 + wq * 32 + 32 <= tq;
+            if (writes && !whole && row_ok) {
+                uint4* row = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(P.dq) +
+                                                      ((long long)it.sq.q0 + i) * P.H * HD + (long long)it.h * HD + c0);
+#pragma unroll
+                for (int w4 = 0; w4 < kCols / 8; ++w4)
+                    row[w4] = make_uint4(packed[4 * w4], packed[4 * w4 + 1], packed[4 * w4 + 2], packed[4 * w4 + 3]);
+            }
             // this warp's 32 rows x 64 columns leave through its staging slice
-            if (writes) {
+            if (writes && whole) {
                 const uint32_t slice = sbase + C::kStgOff + warp * 4096;
                 if (elect_one()) bulk_wait_read_all();
                 __syncwarp();
@@ -910,7 +955,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (elect_one()) {
-                    tma_store_3d(&tmDQ, slice, it.h * HD + c0, it.i0 + wq * 32, it.b);
+                    tma_store_3d(&tmDQ, slice, it.h * HD + c0, it.sq.q0 + it.i0 + wq * 32, it.sq.zb);
                     bulk_commit_group();
                 }
             }
@@ -938,7 +983,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         if (e != cudaSuccess) return e;
     }
     if (phases & 4) {
-        auto k = bwd_dq_kernel<BF16, HD>;
+        auto k = p.cu_q ? bwd_dq_kernel<BF16, HD, true> : bwd_dq_kernel<BF16, HD, false>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         int dev = 0, nsm = 0;
@@ -951,7 +996,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
-        auto k = bwd_dkdv_kernel<BF16, HD>;
+        auto k = p.cu_q ? bwd_dkdv_kernel<BF16, HD, true> : bwd_dkdv_kernel<BF16, HD, false>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;

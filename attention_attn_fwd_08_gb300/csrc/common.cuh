@@ -42,6 +42,12 @@ struct Params {
     int q_offset;
     int splits, chunk;   // decode
     const int* lengths;  // decode: per-batch valid cache length on the device, or NULL (Tk for all)
+    // Packed variable-length batches: sequence b owns query rows [cu_q[b], cu_q[b+1])
+    // and key rows [cu_k[b], cu_k[b+1]) of one packed tensor (device int32 prefix
+    // sums, B+1 each); Tq and Tk then bound the sequence lengths.  NULL: dense [B][T].
+    const int* cu_q;
+    const int* cu_k;
+    int total_q, total_k;  // packed: rows of q/o and of k/v (no access goes past them)
     unsigned int* status;
 };
 
@@ -56,6 +62,7 @@ enum : unsigned int {
     ST_DEC_WAIT = 1u << 6,
     ST_SELFTEST = 1u << 7,
     ST_TEARDOWN = 1u << 8,
+    ST_VARLEN_BOUNDS = 1u << 9,  // a packed sequence longer than the bound, or cu_seqlens decreasing
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: no wait is ever that long
@@ -98,10 +105,48 @@ template <> __device__ __forceinline__ float dot2<false>(uint32_t a, uint32_t b)
     return fmaf(x.x, y.x, x.y * y.y);
 }
 
+// --------------------------------------------------------------- sequences
+// Where sequence b's rows live.  Dense: batch b of [B][T] tensors.  Packed:
+// rows q0 .. q0+tq-1 (queries) and k0 .. k0+tk-1 (keys) of the single packed
+// batch.  zb is the batch coordinate of the 3-D tensor maps; the linear row of
+// query i is zb*Tq + q0 + i (keys: zb*Tk + k0 + j).  A packed sequence longer
+// than the launch bound or running past the tensor's rows (or a decreasing or
+// negative prefix sum) is cut to what fits (or to nothing) and flags
+// ST_VARLEN_BOUNDS, so that no access leaves the caller's buffers.
+struct Seq {
+    int q0, tq, k0, tk, zb;
+};
+template <bool kPacked>
+__device__ __forceinline__ Seq seq_of(const Params& P, int b) {
+    Seq s;
+    if constexpr (kPacked) {
+        const int a0 = __ldg(P.cu_q + b), a1 = __ldg(P.cu_q + b + 1);
+        const int c0 = __ldg(P.cu_k + b), c1 = __ldg(P.cu_k + b + 1);
+        const bool start_ok = a0 >= 0 && c0 >= 0 && a0 <= P.total_q && c0 <= P.total_k;
+        s.q0 = start_ok ? a0 : 0;
+        s.k0 = start_ok ? c0 : 0;
+        s.tq = start_ok ? min(min(max(a1 - a0, 0), P.Tq), P.total_q - a0) : 0;
+        s.tk = start_ok ? min(min(max(c1 - c0, 0), P.Tk), P.total_k - c0) : 0;
+        s.zb = 0;
+        if ((a1 - a0 != s.tq || c1 - c0 != s.tk) && P.status) atomicOr(P.status, ST_VARLEN_BOUNDS);
+    } else {
+        s.q0 = 0;
+        s.k0 = 0;
+        s.tq = P.Tq;
+        s.tk = P.Tk;
+        s.zb = b;
+    }
+    return s;
+}
+// the same, choosing the layout at run time (the CUDA-core kernels)
+__device__ __forceinline__ Seq seq_any(const Params& P, int b) {
+    return P.cu_q ? seq_of<true>(P, b) : seq_of<false>(P, b);
+}
+
 // ------------------------------------------------------------ visibility
-// Key j visible to the query at absolute position p (see include/attn.h).
-__device__ __forceinline__ bool visible(const Params& P, int b, int p, int j) {
-    if (j < 0 || j >= P.Tk) return false;
+// Key j (of tk) visible to the query at absolute position p (see include/attn.h).
+__device__ __forceinline__ bool visible(const Params& P, int b, int p, int j, int tk) {
+    if (j < 0 || j >= tk) return false;
     if (P.causal && j > p) return false;
     if (P.window > 0) {
         int gap = p - j;

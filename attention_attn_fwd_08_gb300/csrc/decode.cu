@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Params P,
                     const int j = j0 + kb + nt * 8 + 2 * t + (e & 1);
                     float x = sc[nt][e] * P.scale;
                     if (P.softcap > 0.f) x = P.softcap * tanh_accurate(x / P.softcap);
-                    const bool vis = rok[r] && j < tk_b && visible(P, b, pos[r], j);
+                    const bool vis = rok[r] && visible(P, b, pos[r], j, tk_b);
                     x = vis ? x * kLog2e : -INFINITY;
                     sc[nt][e] = x;
                     mx[r] = fmaxf(mx[r], x);

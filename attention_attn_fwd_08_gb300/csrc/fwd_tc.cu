@@ -33,11 +33,12 @@ struct TileInfo {
     int t0, ntiles;
 };
 
-__device__ __forceinline__ TileInfo tile_range(const Params& P, int i0) {
+// key tiles the query tile at rows i0 .. of a sequence of tq queries and tk keys sees
+__device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, int tk) {
     const int p0 = i0 + P.q_offset;
-    const int p1 = min(i0 + BM, P.Tq) - 1 + P.q_offset;
+    const int p1 = min(i0 + BM, tq) - 1 + P.q_offset;
     int lo, hi;
-    key_range(P.causal, P.window, P.Tk, p0, p1, &lo, &hi);
+    key_range(P.causal, P.window, tk, p0, p1, &lo, &hi);
     TileInfo t;
     t.t0 = lo / BN;
     t.ntiles = hi > lo ? (hi + BN - 1) / BN - t.t0 : 0;
@@ -87,14 +88,18 @@ struct Fwd2Cfg {
 
 // One work item: 256 query rows (tiles A and B) of one (batch, head), and the
 // key tiles each tile sees.  Items are numbered longest first: every head's last
-// (causally heaviest) query block comes before any head's next one.
+// (causally heaviest) query block comes before any head's next one.  With packed
+// sequences the items cover the longest sequence; a shorter one's surplus items
+// have no tiles.
 struct FwdItem {
     int b, h, kvh, i0;
+    Seq sq;
     bool hasB;
     TileInfo tu[2];
     int t0, ntiles;  // union key-tile range of the two tiles
 };
 
+template <bool VL>
 __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
     FwdItem it;
     const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
@@ -104,9 +109,10 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
     it.b = hb / P.H;
     it.kvh = it.h / P.G;
     it.i0 = cq * 2 * BM;
-    it.hasB = it.i0 + BM < P.Tq;
-    it.tu[0] = tile_range(P, it.i0);
-    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM) : TileInfo{0, 0};
+    it.sq = seq_of<VL>(P, it.b);
+    it.hasB = it.i0 + BM < it.sq.tq;
+    it.tu[0] = it.i0 < it.sq.tq ? tile_range(P, it.i0, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
+    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
     int t0 = it.tu[0].t0, t1 = it.tu[0].t0 + it.tu[0].ntiles;
     if (it.tu[1].ntiles > 0) {
         if (it.tu[0].ntiles == 0) {
@@ -123,7 +129,9 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
 }
 __device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * BM - 1) / (2 * BM) * P.H * P.B; }
 
-template <bool BF16, int HD>
+// VL: packed variable-length sequences (cu_seqlens); the dense instantiation
+// carries none of their bookkeeping.
+template <bool BF16, int HD, bool VL>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
@@ -195,7 +203,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int gk = 0, gv = 0;   // K and V tiles loaded so far (ring positions)
             int qn[2] = {0, 0};   // Q tiles loaded so far, per tile slot
             for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
-                const FwdItem it = fwd_item(P, w);
+                const FwdItem it = fwd_item<VL>(P, w);
                 if (it.ntiles == 0) continue;
                 for (int u = 0; ok && u < 2; ++u) {
                     if (!active(it, u)) continue;
@@ -210,7 +218,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     for (int bx = 0; bx < C::kBoxes; ++bx)
                         if (elect_one())
                             tma_load_3d(sbase + C::kQOff + u * C::kQBytes + bx * (BM * 128), &tmQ, BAR(Q_FULL(u)),
-                                        it.h * HD + bx * 64, it.i0 + u * BM, it.b);
+                                        it.h * HD + bx * 64, it.sq.q0 + it.i0 + u * BM, it.sq.zb);
                     ++qn[u];
                 }
                 for (int n = 0; ok && n < it.ntiles; ++n) {
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     for (int bx = 0; bx < C::kBoxes; ++bx)
                         if (elect_one())
                             tma_load_3d(sbase + C::kKOff + s * C::kKVBytes + bx * (BN * 128), &tmK, BAR(K_FULL(s)),
-                                        it.kvh * HD + bx * 64, j0, it.b);
+                                        it.kvh * HD + bx * 64, it.sq.k0 + j0, it.sq.zb);
                     ++gk;
                     if (use > 0 && !warp_wait(BAR(V_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag)) {
                         ok = false;
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     for (int bx = 0; bx < C::kBoxes; ++bx)
                         if (elect_one())
                             tma_load_3d(sbase + C::kVOff + s * C::kKVBytes + bx * (BN * 128), &tmV, BAR(V_FULL(s)),
-                                        it.kvh * HD + bx * 64, j0, it.b);
+                                        it.kvh * HD + bx * 64, it.sq.k0 + j0, it.sq.zb);
                     ++gv;
                 }
             }
@@ -265,7 +273,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int pc = 0;   // P_FULL(u) phases consumed
             int act = 0;  // items in which this tile was active so far
             for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
-                const FwdItem it = fwd_item(P, w);
+                const FwdItem it = fwd_item<VL>(P, w);
                 if (it.ntiles == 0) continue;
                 const TileInfo my = it.tu[u];
                 const bool on = active(it, u);
@@ -490,16 +498,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const bool alternate = !cap && HD == 128;
         int base[2] = {0, 0};
         for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
-            const FwdItem it = fwd_item(P, w);
+            const FwdItem it = fwd_item<VL>(P, w);
             const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
             const int bA = base[0], bB = base[1];
             base[0] += nA;
             base[1] += nB;
             const int ib = it.i0 + u * BM;  // first row of this tile
-            if (ib >= P.Tq) continue;
+            if (ib >= it.sq.tq) continue;
+            const int tq = it.sq.tq, tk = it.sq.tk;
             const int i = ib + r;
             const int p = i + P.q_offset;
-            const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, P.Tq) - 1 + P.q_offset;
+            const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, tq) - 1 + P.q_offset;
             const TileInfo my = it.tu[u];
             float m_used = 0.f, l = 0.f;
             for (int k = 0; k < my.ntiles; ++k) {
@@ -510,16 +519,16 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int j = j0 + c * 32 + lane;
-                        mbits[c] = __ballot_sync(0xffffffffu, j < P.Tk && mrow[j] > 0.5f);
+                        mbits[c] = __ballot_sync(0xffffffffu, j < tk && mrow[j] > 0.5f);
                     }
                 }
                 // a tile whose keys the mask keeps whole needs no mask pass
-                const bool full = tile_full(P.causal, P.window, P.Tk, prow0, prow1, j0, j0 + BN) &&
+                const bool full = tile_full(P.causal, P.window, tk, prow0, prow1, j0, j0 + BN) &&
                                   (mbits[0] & mbits[1] & mbits[2] & mbits[3]) == 0xffffffffu;
                 // this row's visible columns of the tile: [clo, chi), and the key-mask bits
                 int clo = 0, chi = BN;
                 if (!full) {
-                    chi = min(chi, P.Tk - j0);
+                    chi = min(chi, tk - j0);
                     if (P.causal) chi = min(chi, p - j0 + 1);
                     if (P.window > 0) {
                         clo = max(clo, p - P.window + 1 - j0);
@@ -591,7 +600,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(O_EMPTY(u)));
             }
-            if (ok && (have_o || my.ntiles == 0)) {
+            // A packed sequence's last rows may share a 32-row slice with the next
+            // sequence's first: such a slice goes out row by row (rows of this sequence
+            // only).  Dense tensors end where the map ends, which clips the tiled store.
+            const bool whole = !VL || ib + wq * 32 + 32 <= tq;
+            if (ok && (have_o || my.ntiles == 0) && !whole && i < tq) {
+                uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(P.o) +
+                                                       ((long long)it.sq.q0 + i) * P.H * HD + (long long)it.h * HD);
+#pragma unroll
+                for (int w4 = 0; w4 < HD / 8; ++w4)
+                    orow[w4] = make_uint4(packed[4 * w4], packed[4 * w4 + 1], packed[4 * w4 + 2], packed[4 * w4 + 3]);
+            }
+            if (ok && (have_o || my.ntiles == 0) && whole) {
                 // This warp's 32 rows go out through its 4 KB staging slice, 64 columns
                 // at a time, in the 128-byte-swizzled layout of the tensor map's box;
                 // one lane issues the tiled store (rows past Tq are not written).
@@ -609,14 +629,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (elect_one()) {
-                        tma_store_3d(&tmO, slice, it.h * HD + half * 64, ib + wq * 32, it.b);
+                        tma_store_3d(&tmO, slice, it.h * HD + half * 64, it.sq.q0 + ib + wq * 32, it.sq.zb);
                         bulk_commit_group();
                     }
                 }
-                if (P.lse && i < P.Tq)
-                    P.lse[((long long)it.b * P.H + it.h) * P.Tq + i] =
-                        l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
             }
+            if (ok && (have_o || my.ntiles == 0) && P.lse && i < tq)
+                P.lse[((long long)it.b * P.H + it.h) * P.Tq + i] =
+                    l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
             if (!ok) break;
         }
         // the staging slice must stay until this warp's last store has read it
@@ -634,7 +654,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
 template <bool BF16, int HD>
 cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     using C = Fwd2Cfg<HD>;
-    auto kern = fwd_tc2_kernel<BF16, HD>;
+    auto kern = p.cu_q ? fwd_tc2_kernel<BF16, HD, true> : fwd_tc2_kernel<BF16, HD, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
     if (e != cudaSuccess) return e;
     int dev = 0, nsm = 0;

@@ -44,15 +44,20 @@ __device__ __forceinline__ float capped(float s, float softcap) {
     return softcap > 0.f ? softcap * tanhf(s / softcap) : s;
 }
 
-template <typename T>
-__device__ __forceinline__ const T* qrow(const Params& P, const void* base, int b, int i, int h) {
-    return reinterpret_cast<const T*>(base) + ((long long)b * P.Tq + i) * (long long)P.H * P.hd +
-           (long long)h * P.hd;
+// head h of query row i (key row j) of sequence sq
+__device__ __forceinline__ long long qoff(const Params& P, const Seq& sq, int i, int h) {
+    return ((long long)sq.zb * P.Tq + sq.q0 + i) * (long long)P.H * P.hd + (long long)h * P.hd;
+}
+__device__ __forceinline__ long long kvoff(const Params& P, const Seq& sq, int j, int kvh) {
+    return ((long long)sq.zb * P.Tk + sq.k0 + j) * (long long)P.Hkv * P.hd + (long long)kvh * P.hd;
 }
 template <typename T>
-__device__ __forceinline__ const T* kvrow(const Params& P, const void* base, int b, int j, int kvh) {
-    return reinterpret_cast<const T*>(base) + ((long long)b * P.Tk + j) * (long long)P.Hkv * P.hd +
-           (long long)kvh * P.hd;
+__device__ __forceinline__ const T* qrow(const Params& P, const void* base, const Seq& sq, int i, int h) {
+    return reinterpret_cast<const T*>(base) + qoff(P, sq, i, h);
+}
+template <typename T>
+__device__ __forceinline__ const T* kvrow(const Params& P, const void* base, const Seq& sq, int j, int kvh) {
+    return reinterpret_cast<const T*>(base) + kvoff(P, sq, j, kvh);
 }
 
 // ------------------------------------------------------------------ forward
@@ -64,17 +69,19 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
     float* Qs = Vs + kTile * HD;             // [kRows][HD]
     float* Ps = Qs + kRows * HD;             // [kRows][kTile]
     const int b = blockIdx.z, h = blockIdx.y, kvh = h / P.G;
+    const Seq sq = seq_any(P, b);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i0 = blockIdx.x * kRows;
+    if (i0 >= sq.tq) return;  // (packed) past this sequence's rows
     const int i = i0 + warp;
-    const bool row_ok = i < P.Tq;
+    const bool row_ok = i < sq.tq;
     const int p = i + P.q_offset;
-    const int ilast = min(i0 + kRows, P.Tq) - 1;
+    const int ilast = min(i0 + kRows, sq.tq) - 1;
     int lo, hi;
-    key_range(P.causal, P.window, P.Tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+    key_range(P.causal, P.window, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
 
     for (int d = lane; d < HD; d += 32)
-        Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, b, i, h)[d]) : 0.f;
+        Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, sq, i, h)[d]) : 0.f;
 
     float m = -INFINITY, l = 0.f;
     float acc[HD / 32];
@@ -86,9 +93,9 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
         for (int e = threadIdx.x; e < kTile * HD; e += blockDim.x) {
             const int jj = e / HD, d = e % HD, j = j0 + jj;
             float kv = 0.f, vv = 0.f;
-            if (j < P.Tk) {
-                kv = Elem<T>::to_f(kvrow<T>(P, P.k, b, j, kvh)[d]);
-                vv = Elem<T>::to_f(kvrow<T>(P, P.v, b, j, kvh)[d]);
+            if (j < sq.tk) {
+                kv = Elem<T>::to_f(kvrow<T>(P, P.k, sq, j, kvh)[d]);
+                vv = Elem<T>::to_f(kvrow<T>(P, P.v, sq, j, kvh)[d]);
             }
             Ks[jj * (HD + 1) + d] = kv;
             Vs[jj * HD + d] = vv;
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
             float dot = 0.f;
 #pragma unroll 8
             for (int d = 0; d < HD; ++d) dot = fmaf(Qs[warp * HD + d], Ks[jj * (HD + 1) + d], dot);
-            vis[t] = row_ok && visible(P, b, p, j);
+            vis[t] = row_ok && visible(P, b, p, j, sq.tk);
             s[t] = vis[t] ? capped(dot * P.scale, P.softcap) : -INFINITY;
         }
         const float m_new = fmaxf(m, warp_max(fmaxf(s[0], s[1])));
@@ -127,8 +134,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
         m = m_new;
     }
     if (!row_ok) return;
-    T* orow = reinterpret_cast<T*>(P.o) + ((long long)b * P.Tq + i) * (long long)P.H * P.hd +
-              (long long)h * P.hd;
+    T* orow = reinterpret_cast<T*>(P.o) + qoff(P, sq, i, h);
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) orow[lane + 32 * c] = Elem<T>::from_f(acc[c] * inv);
@@ -153,10 +159,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(Params P) {
     const int h = live ? (int)(row % P.H) : 0;
     const long long bi = live ? row / P.H : 0;
     const int i = (int)(bi % P.tq_pad), b = (int)(bi / P.tq_pad);
+    const Seq sq = seq_any(P, live ? b : 0);
     float acc = 0.f;
-    if (live && i < P.Tq) {
-        const uint4 ov = reinterpret_cast<const uint4*>(qrow<T>(P, P.o_in, b, i, h))[sub];
-        const uint4 gv = reinterpret_cast<const uint4*>(qrow<T>(P, P.dout, b, i, h))[sub];
+    if (live && i < sq.tq) {
+        const uint4 ov = reinterpret_cast<const uint4*>(qrow<T>(P, P.o_in, sq, i, h))[sub];
+        const uint4 gv = reinterpret_cast<const uint4*>(qrow<T>(P, P.dout, sq, i, h))[sub];
         const T* oe = reinterpret_cast<const T*>(&ov);
         const T* ge = reinterpret_cast<const T*>(&gv);
 #pragma unroll
@@ -166,7 +173,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(Params P) {
     for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, LPR);
     if (!live || sub != 0) return;
     const long long srow = ((long long)b * P.H + h) * P.tq_pad + i;
-    if (i >= P.Tq) {
+    if (i >= sq.tq) {
         P.ndelta[srow] = 0.f;
         P.nlse2[srow] = -INFINITY;
         return;
@@ -186,17 +193,19 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
     float* Gs = Qs + kRows * HD;         // [kRows][HD]  dO
     float* Ss = Gs + kRows * HD;         // [kRows][kTile] dS
     const int b = blockIdx.z, h = blockIdx.y, kvh = h / P.G;
+    const Seq sq = seq_any(P, b);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int i0 = blockIdx.x * kRows;
+    if (i0 >= sq.tq) return;  // (packed) past this sequence's rows
     const int i = i0 + warp;
-    const bool row_ok = i < P.Tq;
+    const bool row_ok = i < sq.tq;
     const int p = i + P.q_offset;
-    const int ilast = min(i0 + kRows, P.Tq) - 1;
+    const int ilast = min(i0 + kRows, sq.tq) - 1;
     int lo, hi;
-    key_range(P.causal, P.window, P.Tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+    key_range(P.causal, P.window, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
     for (int d = lane; d < HD; d += 32) {
-        Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, b, i, h)[d]) : 0.f;
-        Gs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.dout, b, i, h)[d]) : 0.f;
+        Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, sq, i, h)[d]) : 0.f;
+        Gs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.dout, sq, i, h)[d]) : 0.f;
     }
     const long long srow = ((long long)b * P.H + h) * P.Tq + i;
     const float lse = row_ok ? P.lse_in[srow] : -INFINITY;
@@ -211,9 +220,9 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
         for (int e = threadIdx.x; e < kTile * HD; e += blockDim.x) {
             const int jj = e / HD, d = e % HD, j = j0 + jj;
             float kv = 0.f, vv = 0.f;
-            if (j < P.Tk) {
-                kv = Elem<T>::to_f(kvrow<T>(P, P.k, b, j, kvh)[d]);
-                vv = Elem<T>::to_f(kvrow<T>(P, P.v, b, j, kvh)[d]);
+            if (j < sq.tk) {
+                kv = Elem<T>::to_f(kvrow<T>(P, P.k, sq, j, kvh)[d]);
+                vv = Elem<T>::to_f(kvrow<T>(P, P.v, sq, j, kvh)[d]);
             }
             Ks[jj * (HD + 1) + d] = kv;
             Vs[jj * (HD + 1) + d] = vv;
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
         for (int t = 0; t < 2; ++t) {
             const int jj = lane + 32 * t, j = j0 + jj;
             float ds = 0.f;
-            if (live && visible(P, b, p, j)) {
+            if (live && visible(P, b, p, j, sq.tk)) {
                 float qk = 0.f, gv = 0.f;
 #pragma unroll 8
                 for (int d = 0; d < HD; ++d) {
@@ -254,8 +263,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
         __syncwarp();
     }
     if (!row_ok) return;
-    T* out = reinterpret_cast<T*>(P.dq) + ((long long)b * P.Tq + i) * (long long)P.H * P.hd +
-             (long long)h * P.hd;
+    T* out = reinterpret_cast<T*>(P.dq) + qoff(P, sq, i, h);
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) out[lane + 32 * c] = Elem<T>::from_f(acc[c] * P.scale);
 }
@@ -273,16 +281,18 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
     float* Pw = Ds + kTile;              // [kRows][kTile] P
     float* Sw = Pw + kRows * kTile;      // [kRows][kTile] dS
     const int b = blockIdx.z, kvh = blockIdx.y;
+    const Seq sq = seq_any(P, b);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j0 = blockIdx.x * kRows;
+    if (j0 >= sq.tk) return;  // (packed) past this sequence's keys
     const int j = j0 + warp;
-    const bool key_ok = j < P.Tk;
-    const int jlast = min(j0 + kRows, P.Tk);
+    const bool key_ok = j < sq.tk;
+    const int jlast = min(j0 + kRows, sq.tk);
     int qlo, qhi;
-    query_range(P.causal, P.window, P.Tq, P.q_offset, j0, jlast, &qlo, &qhi);
+    query_range(P.causal, P.window, sq.tq, P.q_offset, j0, jlast, &qlo, &qhi);
     for (int d = lane; d < HD; d += 32) {
-        Ks[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.k, b, j, kvh)[d]) : 0.f;
-        Vs[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.v, b, j, kvh)[d]) : 0.f;
+        Ks[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.k, sq, j, kvh)[d]) : 0.f;
+        Vs[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.v, sq, j, kvh)[d]) : 0.f;
     }
     float dk[HD / 32], dv[HD / 32];
 #pragma unroll
@@ -294,9 +304,9 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
             for (int e = threadIdx.x; e < kTile * HD; e += blockDim.x) {
                 const int ii = e / HD, d = e % HD, i = i0 + ii;
                 float qv = 0.f, gv = 0.f;
-                if (i < P.Tq) {
-                    qv = Elem<T>::to_f(qrow<T>(P, P.q, b, i, h)[d]);
-                    gv = Elem<T>::to_f(qrow<T>(P, P.dout, b, i, h)[d]);
+                if (i < sq.tq) {
+                    qv = Elem<T>::to_f(qrow<T>(P, P.q, sq, i, h)[d]);
+                    gv = Elem<T>::to_f(qrow<T>(P, P.dout, sq, i, h)[d]);
                 }
                 Qs[ii * (HD + 1) + d] = qv;
                 Gs[ii * (HD + 1) + d] = gv;
@@ -304,15 +314,15 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
             for (int ii = threadIdx.x; ii < kTile; ii += blockDim.x) {
                 const int i = i0 + ii;
                 const long long srow = ((long long)b * P.H + h) * P.Tq + i;
-                Ls[ii] = i < P.Tq ? P.lse_in[srow] : -INFINITY;
-                Ds[ii] = i < P.Tq ? -P.ndelta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
+                Ls[ii] = i < sq.tq ? P.lse_in[srow] : -INFINITY;
+                Ds[ii] = i < sq.tq ? -P.ndelta[((long long)b * P.H + h) * P.tq_pad + i] : 0.f;
             }
             __syncthreads();
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const int ii = lane + 32 * t, i = i0 + ii;
                 float pr = 0.f, ds = 0.f;
-                if (key_ok && i < P.Tq && Ls[ii] != -INFINITY && visible(P, b, i + P.q_offset, j)) {
+                if (key_ok && i < sq.tq && Ls[ii] != -INFINITY && visible(P, b, i + P.q_offset, j, sq.tk)) {
                     float qk = 0.f, gv = 0.f;
 #pragma unroll 8
                     for (int d = 0; d < HD; ++d) {
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
         }
     }
     if (!key_ok) return;
-    const long long off = ((long long)b * P.Tk + j) * (long long)P.Hkv * P.hd + (long long)kvh * P.hd;
+    const long long off = kvoff(P, sq, j, kvh);
     T* dkp = reinterpret_cast<T*>(P.dk) + off;
     T* dvp = reinterpret_cast<T*>(P.dv) + off;
 #pragma unroll
@@ -390,11 +400,12 @@ cudaError_t preprocess_typed(const Params& p, cudaStream_t s) {
 template <typename T, int HD>
 cudaError_t bwd_typed(const Params& p, int phases, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
-    if (phases & 1) {
+    // (packed sequences: a zero bound leaves nothing to launch for that pass)
+    if ((phases & 1) && p.tq_pad > 0) {
         e = preprocess_typed<T>(p, s);
         if (e != cudaSuccess) return e;
     }
-    if (phases & 2) {
+    if ((phases & 2) && p.Tk > 0) {
         const size_t smem_kv =
             sizeof(float) * (2 * kTile * (HD + 1) + 2 * kRows * HD + 2 * kTile + 2 * kRows * kTile);
         auto kkv = simt_dkdv_kernel<T, HD>;
@@ -403,7 +414,7 @@ cudaError_t bwd_typed(const Params& p, int phases, cudaStream_t s) {
         kkv<<<dim3((p.Tk + kRows - 1) / kRows, p.Hkv, p.B), kRows * 32, smem_kv, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (!(phases & 4)) return cudaSuccess;
+    if (!(phases & 4) || p.Tq == 0) return cudaSuccess;
     const size_t smem_dq =
         sizeof(float) * (2 * kTile * (HD + 1) + 2 * kRows * HD + kRows * kTile);
     auto kdq = simt_dq_kernel<T, HD>;

@@ -189,6 +189,51 @@ ATTN_API attn_status attn_decode_len(attn_dtype dt, const void* q, const void* k
                         long long key_mask_bstride, void* stream);
 
 /*
+ * Packed variable-length attention: the batch's sequences stored back to back
+ * in one tensor, no padding, no attention across sequences.
+ * Source: brotensor ops/flash_attention.h, flash_attention_varlen_forward and
+ * flash_attention_varlen_backward (cu_seqlens prefix sums on the device;
+ * sequence b covers query rows [cu_q[b], cu_q[b+1]) and key rows
+ * [cu_k[b], cu_k[b+1]); causal: key j of the sequence is visible to its query
+ * i when j <= i, both counted from the sequence's first row).
+ *   q, o          : [total_q, H*hd]; k, v : [total_k, Hkv*hd]; 16-byte aligned.
+ *   cu_seqlens_q, cu_seqlens_k : device arrays of batch+1 int32 (4-byte aligned),
+ *                   non-decreasing, cu[0] >= 0 and cu[batch] <= total.
+ *   max_seqlen_q, max_seqlen_k : bounds on every sequence's query / key count;
+ *                   the launch shape depends on them (and on batch) alone, so one
+ *                   captured graph serves every packing within the bounds.  A
+ *                   sequence above the bound or past total (or a decreasing or
+ *                   negative prefix sum) is cut to what fits (or to nothing), so no
+ *                   access leaves the buffers, and attn_get_device_status() then
+ *                   returns ATTN_ERR_INVALID_ARG.
+ *   lse           : [batch, H, max_seqlen_q] fp32 or NULL; entry (b, h, i) for
+ *                   i < the length of sequence b.
+ *   window, softcap, scale, dt, H, Hkv, hd : as for attn_fwd, applied within each
+ *                   sequence (query positions from 0, no q_offset, no key mask).
+ *   Rows of o outside every sequence are not written.
+ */
+ATTN_API attn_status attn_varlen_fwd(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
+                        float* lse, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int H,
+                        int Hkv, int hd, float scale, int causal, int window, float softcap,
+                        void* stream);
+
+/*
+ * Backward of attn_varlen_fwd (same arguments; o and lse from that call).
+ * dq [total_q, H*hd], dk and dv [total_k, Hkv*hd] are overwritten on the rows
+ * of every sequence (zero where nothing is visible); rows outside every
+ * sequence are not written.  workspace: at least
+ * attn_bwd_workspace_size(batch, max_seqlen_q, H) bytes, 16-byte aligned.
+ */
+ATTN_API attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k, const void* v,
+                        const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                        void* dv, void* workspace, size_t workspace_bytes,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                        int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int H,
+                        int Hkv, int hd, float scale, int causal, int window, float softcap,
+                        void* stream);
+
+/*
  * attn_decode without a workspace argument, for callers that cannot call
  * cudaMalloc and have no scratch buffer to pass in: for example a plugin that
  * is handed only its input and output buffers, a serving loop that forbids
@@ -218,9 +263,11 @@ ATTN_API const char* attn_status_string(attn_status s);
 
 /*
  * Reads and clears the device status word that bounded waits set when they
- * run out.  Synchronises `stream` first.  Returns ATTN_OK, ATTN_ERR_TIMEOUT or
+ * run out (and that packed-sequence calls set when cu_seqlens break their
+ * bounds).  Synchronises `stream` first.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a
+ * wait ran out), ATTN_ERR_INVALID_ARG (only the cu_seqlens bit is set) or
  * ATTN_ERR_CUDA.  If `detail` is not NULL it receives the raw word (which wait
- * gave up, as a bit set).
+ * gave up, as a bit set; bit 9: cu_seqlens out of bounds).
  */
 ATTN_API attn_status attn_get_device_status(void* stream, unsigned int* detail);
 

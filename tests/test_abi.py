@@ -122,6 +122,40 @@ def test_decode_len_validation():
     assert st == A.ERR_INVALID_ARG
 
 
+def test_varlen_validation():
+    """Argument errors of the packed-sequence calls come back before any launch."""
+    L = A.lib()
+    tail = [0.1, 1, 0, 0.0, None]
+    # batch > 0 without cu_seqlens
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, None, None, 2, 64, 64, 100, 100, 8, 2, 128, *tail)
+    assert st == A.ERR_INVALID_ARG
+    # cu_seqlens not 4-byte aligned
+    odd = ctypes.c_void_p(0x1002)
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, odd, BAD, 2, 64, 64, 100, 100, 8, 2, 128, *tail)
+    assert st == A.ERR_INVALID_ARG
+    # a bound above the packed row count
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 101, 64, 100, 100, 8, 2, 128, *tail)
+    assert st == A.ERR_INVALID_ARG
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, -1, 8, 2, 128, *tail)
+    assert st == A.ERR_INVALID_ARG
+    # head dim, GQA divisibility, softcap
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, 100, 8, 2, 96, *tail)
+    assert st == A.ERR_UNSUPPORTED
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, 100, 8, 3, 128, *tail)
+    assert st == A.ERR_INVALID_ARG
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, 100, 8, 2, 128, 0.1, 1, 0, -1.0,
+                           None)
+    assert st == A.ERR_INVALID_ARG
+    # nothing to do: no sequences, or no query rows
+    assert L.attn_varlen_fwd(2, None, None, None, None, None, None, None, 0, 0, 0, 0, 0, 8, 2, 128, *tail) == A.OK
+    assert L.attn_varlen_fwd(2, None, None, None, None, None, BAD, BAD, 3, 0, 5, 0, 5, 8, 2, 128, *tail) == A.OK
+    # backward: workspace too small for batch x max_seqlen_q
+    st = L.attn_varlen_bwd(2, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, 16, BAD, BAD, 2, 64, 64, 100, 100, 8,
+                           2, 128, *tail)
+    assert st == A.ERR_INVALID_ARG
+    assert A.attn_bwd_workspace_size(2, 64, 8) > 16
+
+
 def test_workspace_sizes():
     assert A.attn_bwd_workspace_size(4, 2048, 32) == 2 * 4 * 2048 * 32 * 4
     assert A.attn_bwd_workspace_size(1, 65, 2) == 2 * 1 * 128 * 2 * 4
