@@ -12,6 +12,7 @@ Workloads (shapes of the attention settings the pages describe):
   swa_softcap     B=2  Tq=Tk=8192  H=16 Hkv=4 hd=128 causal window=1024 softcap=50  bf16 fwd+bwd
   encoder_mask    B=8  Tq=Tk=1024  H=Hkv=12  hd=64  bidirectional, per-sequence key mask, fp16 fwd
   decode_lq1/lq4  B=16 Lk=32768 Lq in {1,4} H=32 Hkv=8 hd=128 causal q_offset=Lk-Lq  bf16 decode
+  varlen_packed   8 sequences of U{256..2048} rows packed back to back, H=32 Hkv=8 hd=128 causal bf16 fwd+bwd
 """
 from __future__ import annotations
 
@@ -65,6 +66,9 @@ WORKLOADS = {
                            decode=True, seed=0x5EED0005),
     "decode_lq4": Workload("decode_lq4", "bf16", 16, 4, 32768, 32, 8, 128, True, q_offset=32764,
                            decode=True, seed=0x5EED0006),
+    # Tq/Tk: the bound on a sequence's length (max_seqlen)
+    "varlen_packed": Workload("varlen_packed", "bf16", 8, 2048, 2048, 32, 8, 128, True, backward=True,
+                              seed=0x5EED0007),
 }
 
 
@@ -103,3 +107,20 @@ def make_inputs(w: Workload) -> dict:
         out["lengths"] = lens
         out["key_mask"] = prefix_mask(lens, w.Tk)
     return out
+
+
+def make_packed_inputs(w: Workload) -> dict:
+    """Packed q, k, v, dO ([total, heads*hd], CPU) for w: w.B sequences with lengths
+    drawn uniformly from [256, w.Tq], and their int64 prefix sums ``cu`` (B+1)."""
+    lens = mask_lengths(w.B, 256, w.Tq, w.seed + 4)
+    cu = torch.zeros(w.B + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(lens, 0)
+    total = int(cu[-1])
+    return {
+        "q": normal((total, w.H * w.hd), w.seed + 0, w.dtype),
+        "k": normal((total, w.Hkv * w.hd), w.seed + 1, w.dtype),
+        "v": normal((total, w.Hkv * w.hd), w.seed + 2, w.dtype),
+        "do": normal((total, w.H * w.hd), w.seed + 3, w.dtype),
+        "lengths": lens,
+        "cu": cu,
+    }

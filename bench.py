@@ -460,8 +460,9 @@ def time_passes(torch, stream, passes, args, flush_buf):
 
 
 def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
-    """Sliding-window + softcap fwd/bwd (B=2 T=8192 H=16 Hkv=4 hd=128 window=1024 softcap=50, bf16) and the
-    bidirectional key-masked encoder forward (B=8 T=1024 H=Hkv=12 hd=64, fp16), flops over visible pairs."""
+    """Sliding-window + softcap fwd/bwd (B=2 T=8192 H=16 Hkv=4 hd=128 window=1024 softcap=50, bf16), the
+    bidirectional key-masked encoder forward (B=8 T=1024 H=Hkv=12 hd=64, fp16) and packed variable-length
+    causal fwd/bwd (8 sequences of U{256..2048} rows, H=32 Hkv=8 hd=128, bf16), flops over visible pairs."""
     out = {}
     ws_ = synth.WORKLOADS["swa_softcap"]
     si = synth.make_inputs(ws_)
@@ -492,6 +493,25 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
     tf = 4 * we.hd * pairs / (t["fwd"] * 1e-3) / 1e12
     out["encoder_mask_fwd"] = {"ms": t["fwd"], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
                                "visible_pairs": pairs, "note": "fp16; flops over unmasked keys only"}
+    # packed variable-length sequences (cu_seqlens), causal, fwd and bwd
+    wv = synth.WORKLOADS["varlen_packed"]
+    vi = synth.make_packed_inputs(wv)
+    q, k, v, do = (vi[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu = vi["cu"].to(device=dev, dtype=torch.int32)
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((wv.B, wv.H, wv.Tq), dtype=torch.float32, device=dev)
+    wsv = torch.empty(A.attn_bwd_workspace_size(wv.B, wv.Tq, wv.H), dtype=torch.uint8, device=dev)
+    kw = dict(H=wv.H, Hkv=wv.Hkv, scale=wv.scale, causal=True)
+    t = time_passes(torch, stream, [
+        ("fwd", lambda: A.attn_varlen_fwd(q, k, v, cu, cu, wv.Tq, wv.Tk, o=o, lse=lse, **kw)),
+        ("bwd", lambda: A.attn_varlen_bwd(q, k, v, o, do, lse, cu, cu, wv.Tq, wv.Tk, dq=dq, dk=dk, dv=dv,
+                                          workspace=wsv, **kw))], args, flush_buf)
+    pairs = sum(int(L) * (int(L) + 1) // 2 for L in vi["lengths"]) * wv.H
+    for n, fl in (("fwd", 4), ("bwd", 10)):
+        tf = fl * wv.hd * pairs / (t[n] * 1e-3) / 1e12
+        out["varlen_packed_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                     "visible_pairs": pairs, "tokens": int(vi["cu"][-1]),
+                                     "note": "8 causal sequences of U{256..2048} rows packed back to back"}
     st, word = A.attn_get_device_status()
     if st != A.OK:
         raise RuntimeError("device status word %#x after the masked workloads" % word)
