@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int nitems = fwd_items(P);
     // every role walks the same item sequence; a tile u is active in an item when
     // it has rows and sees at least one key tile
-    auto active = [&](const FwdItem& it, int u) { return it.tu[u].ntiles > 0; };
+    // (tile u is a run-time value: select, so that the item stays in registers)
+    auto active = [&](const FwdItem& it, int u) { return (u == 0 ? it.tu[0].ntiles : it.tu[1].ntiles) > 0; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
                 const FwdItem it = fwd_item<VL>(P, w);
                 if (it.ntiles == 0) continue;
-                const TileInfo my = it.tu[u];
+                const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
                 const bool on = active(it, u);
                 auto has = [&](int n) { return it.t0 + n >= my.t0 && it.t0 + n < my.t0 + my.ntiles; };
                 auto last_of_u = [&](int n) { return it.t0 + n == my.t0 + my.ntiles - 1; };
@@ -509,7 +510,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const int i = ib + r;
             const int p = i + P.q_offset;
             const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, tq) - 1 + P.q_offset;
-            const TileInfo my = it.tu[u];
+            const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
             float m_used = 0.f, l = 0.f;
             for (int k = 0; k < my.ntiles; ++k) {
                 const int j0 = (my.t0 + k) * BN;
