@@ -68,6 +68,15 @@ def _load():
         lib.oracle_attn_probs.restype = ctypes.c_int
         lib.oracle_attn_bwd.argtypes = [dp] * 7 + common
         lib.oracle_attn_bwd.restype = ctypes.c_int
+        llp = ctypes.POINTER(ctypes.c_longlong)
+        common_ex = [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_double,
+                                          ctypes.c_longlong, dp, ctypes.c_longlong, dp, llp]
+        lib.oracle_attn_fwd_ex.argtypes = [dp, dp, dp, dp, dp] + common_ex
+        lib.oracle_attn_fwd_ex.restype = ctypes.c_int
+        lib.oracle_attn_probs_ex.argtypes = [dp, dp, dp, dp, ctypes.c_int, ctypes.c_int] + common_ex
+        lib.oracle_attn_probs_ex.restype = ctypes.c_int
+        lib.oracle_attn_bwd_ex.argtypes = [dp] * 7 + common_ex
+        lib.oracle_attn_bwd_ex.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -165,6 +174,77 @@ def bwd(q, k, v, do, *, H, Hkv, scale, causal=False, window=0, softcap=0.0, q_of
                                           q_offset, m, ms))
     if rc != 0:
         raise ValueError("oracle_attn_bwd rejected its arguments")
+    return dq, dk, dv
+
+
+def _bias(bias, B, H, Tq, Tk):
+    """(array or None, 4 strides): an additive bias broadcastable to [B, H, Tq, Tk],
+    size-1 dimensions read with stride 0 (ferrotensor engine/attention.rs, mask_strides)."""
+    if bias is None:
+        return None, None
+    a = _f64(bias)
+    if a.ndim != 4:
+        raise ValueError("bias must be 4-D [B|1, H|1, Tq|1, Tk|1]")
+    full = (B, H, Tq, Tk)
+    st = []
+    for dim, n, sb in zip(a.shape, full, a.strides):
+        if dim not in (1, n):
+            raise ValueError("bias shape %s does not broadcast to %s" % (a.shape, full))
+        st.append(0 if dim == 1 else sb // 8)
+    return a, (ctypes.c_longlong * 4)(*st)
+
+
+def _common_ex(B, Tq, Tk, H, Hkv, hd, scale, wl, wr, softcap, q_offset, m, ms, bias, bs):
+    return [B, Tq, Tk, H, Hkv, hd, float(scale), int(wl), int(wr), float(softcap), int(q_offset), _ptr(m), int(ms),
+            _ptr(bias), bs]
+
+
+def fwd_ex(q, k, v, *, H, Hkv, scale, window_left=-1, window_right=-1, softcap=0.0, q_offset=0, key_mask=None,
+           bias=None):
+    """O and LSE with the two-sided window [p - window_left, p + window_right]
+    (negative = unbounded) and an optional additive bias (see attn_oracle.c)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Tq, Tk, hd = _shapes(q, k, H, Hkv)
+    m, ms = _mask(key_mask, B, Tk)
+    bb, bs = _bias(bias, B, H, Tq, Tk)
+    o = np.zeros((B, Tq, H * hd), np.float64)
+    lse = np.zeros((B, H, Tq), np.float64)
+    rc = _load().oracle_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                    *_common_ex(B, Tq, Tk, H, Hkv, hd, scale, window_left, window_right, softcap,
+                                                q_offset, m, ms, bb, bs))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd_ex rejected its arguments")
+    return o, lse
+
+
+def probs_ex(q, k, v, b, h, *, H, Hkv, scale, window_left=-1, window_right=-1, softcap=0.0, q_offset=0,
+             key_mask=None, bias=None):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Tq, Tk, hd = _shapes(q, k, H, Hkv)
+    m, ms = _mask(key_mask, B, Tk)
+    bb, bs = _bias(bias, B, H, Tq, Tk)
+    P = np.zeros((Tq, Tk), np.float64)
+    rc = _load().oracle_attn_probs_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(P), int(b), int(h),
+                                      *_common_ex(B, Tq, Tk, H, Hkv, hd, scale, window_left, window_right, softcap,
+                                                  q_offset, m, ms, bb, bs))
+    if rc != 0:
+        raise ValueError("oracle_attn_probs_ex rejected its arguments")
+    return P
+
+
+def bwd_ex(q, k, v, do, *, H, Hkv, scale, window_left=-1, window_right=-1, softcap=0.0, q_offset=0, key_mask=None,
+           bias=None):
+    """dQ, dK, dV of fwd_ex (the bias is a constant: it enters through P only)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Tq, Tk, hd = _shapes(q, k, H, Hkv)
+    m, ms = _mask(key_mask, B, Tk)
+    bb, bs = _bias(bias, B, H, Tq, Tk)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    rc = _load().oracle_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                                    *_common_ex(B, Tq, Tk, H, Hkv, hd, scale, window_left, window_right, softcap,
+                                                q_offset, m, ms, bb, bs))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_ex rejected its arguments")
     return dq, dk, dv
 
 

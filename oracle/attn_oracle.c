@@ -54,6 +54,21 @@
  *    flash_attention.h: excluded positions "contribute nothing", a zero-length
  *    decode "writes zeros").  This is a reading; the pages do not define LSE there.
  *
+ * The "_ex" entry points generalise two terms (the survey's next row on masks):
+ *
+ *   vis    = (wl < 0 || j >= p - wl) && (wr < 0 || j <= p + wr) && (key mask)
+ *   st_ij  = (softcap > 0 ? softcap * tanh(s_ij / softcap) : s_ij) + bias[b,h,i,j]
+ *
+ * A two-sided window [p - wl, p + wr] (negative = unbounded on that side) holds
+ * every window the pages write: ferrotensor's |p - j| < w is (w-1, w-1), with
+ * causal (w-1, 0); brotensor flash_attention_windowed_forward's bidirectional
+ * window |r - j| <= w/2 is (w/2, w/2); forge attention.metal's one-sided window
+ * (keys from i+1-window on) is (w-1, -1); causal alone is (-1, 0).  The bias is
+ * ferrotensor's additive mask [batch, heads, seq_q, seq_k] with size-1
+ * dimensions broadcast (stride 0; ferrotensor engine/attention.rs,
+ * mask_strides), added to the scaled score; -inf entries drop the pair.  It
+ * enters the backward only through P (dS has no bias term).
+ *
  * Layouts: q, o, do, dq are [B][Tq][H*hd]; k, v, dk, dv are [B][Tk][Hkv*hd];
  * lse is [B][H][Tq]; key_mask (optional) is key_mask[b*mask_bstride + j].
  * All arrays are row-major fp64.  Functions return 0, or -1 on bad arguments.
@@ -73,6 +88,10 @@ typedef struct {
     long long q_offset;
     const double* key_mask;
     long long mask_bstride;
+    int ext;             /* 1: the two-sided window and the bias below */
+    long long wl, wr;    /* window [p - wl, p + wr]; negative = unbounded */
+    const double* bias;  /* bias[b*bs[0] + h*bs[1] + i*bs[2] + j*bs[3]] or NULL */
+    long long bs[4];
 } attn_dims;
 
 static int dims_ok(const attn_dims* d)
@@ -86,11 +105,16 @@ static int dims_ok(const attn_dims* d)
 /* visibility of key j to the query at absolute position p (see header). */
 static int visible(const attn_dims* d, int b, long long p, long long j)
 {
-    if (d->causal && j > p) return 0;
-    if (d->window > 0) {
-        long long gap = p - j;
-        if (gap < 0) gap = -gap;
-        if (gap >= d->window) return 0;
+    if (d->ext) {
+        if (d->wl >= 0 && j < p - d->wl) return 0;
+        if (d->wr >= 0 && j > p + d->wr) return 0;
+    } else {
+        if (d->causal && j > p) return 0;
+        if (d->window > 0) {
+            long long gap = p - j;
+            if (gap < 0) gap = -gap;
+            if (gap >= d->window) return 0;
+        }
     }
     if (d->key_mask && !(d->key_mask[(long long)b * d->mask_bstride + j] > 0.5)) return 0;
     return 1;
@@ -126,6 +150,9 @@ static double attend_row(const attn_dims* d, const double* q, const double* k, c
         raw[j] = s;
         if (visible(d, b, p, j)) {
             double st = d->softcap > 0 ? d->softcap * tanh(s / d->softcap) : s;
+            if (d->bias)
+                st += d->bias[(long long)b * d->bs[0] + (long long)h * d->bs[1] + (long long)i * d->bs[2] +
+                              (long long)j * d->bs[3]];
             prob[j] = st;
             if (st > m) m = st;
         } else {
@@ -160,17 +187,26 @@ static attn_dims make_dims(int B, int Tq, int Tk, int H, int Hkv, int hd, double
     d.B = B; d.Tq = Tq; d.Tk = Tk; d.H = H; d.Hkv = Hkv; d.hd = hd;
     d.scale = scale; d.causal = causal; d.window = window; d.softcap = softcap;
     d.q_offset = q_offset; d.key_mask = key_mask; d.mask_bstride = mask_bstride;
+    d.ext = 0; d.wl = d.wr = -1; d.bias = NULL;
+    d.bs[0] = d.bs[1] = d.bs[2] = d.bs[3] = 0;
     return d;
 }
 
-/* Forward: o [B][Tq][H*hd], lse [B][H][Tq] (lse may be NULL). */
-int oracle_attn_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
-                    int B, int Tq, int Tk, int H, int Hkv, int hd, double scale, int causal,
-                    int window, double softcap, long long q_offset, const double* key_mask,
-                    long long mask_bstride)
+static attn_dims make_dims_ex(int B, int Tq, int Tk, int H, int Hkv, int hd, double scale, long long wl,
+                              long long wr, double softcap, long long q_offset, const double* key_mask,
+                              long long mask_bstride, const double* bias, const long long* bs)
 {
-    attn_dims d = make_dims(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset,
-                            key_mask, mask_bstride);
+    attn_dims d = make_dims(B, Tq, Tk, H, Hkv, hd, scale, 0, 0, softcap, q_offset, key_mask, mask_bstride);
+    d.ext = 1; d.wl = wl; d.wr = wr; d.bias = bias;
+    for (int e = 0; e < 4; ++e) d.bs[e] = bias ? bs[e] : 0;
+    return d;
+}
+
+static int fwd_dims(const attn_dims* dp, const double* q, const double* k, const double* v, double* o,
+                    double* lse)
+{
+    const attn_dims d = *dp;
+    const int B = d.B, Tq = d.Tq, Tk = d.Tk, H = d.H, hd = d.hd;
     if (!dims_ok(&d)) return -1;
     int failed = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic)
@@ -195,14 +231,33 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v, double* o
     return failed ? -1 : 0;
 }
 
-/* The probability matrix P [Tq][Tk] of one (b, h), for invariant checks. */
-int oracle_attn_probs(const double* q, const double* k, const double* v, double* P, int b, int h,
-                      int B, int Tq, int Tk, int H, int Hkv, int hd, double scale, int causal,
-                      int window, double softcap, long long q_offset, const double* key_mask,
-                      long long mask_bstride)
+/* Forward: o [B][Tq][H*hd], lse [B][H][Tq] (lse may be NULL). */
+int oracle_attn_fwd(const double* q, const double* k, const double* v, double* o, double* lse,
+                    int B, int Tq, int Tk, int H, int Hkv, int hd, double scale, int causal,
+                    int window, double softcap, long long q_offset, const double* key_mask,
+                    long long mask_bstride)
 {
     attn_dims d = make_dims(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset,
                             key_mask, mask_bstride);
+    return fwd_dims(&d, q, k, v, o, lse);
+}
+
+/* The same with the two-sided window and the additive bias (see header). */
+int oracle_attn_fwd_ex(const double* q, const double* k, const double* v, double* o, double* lse,
+                       int B, int Tq, int Tk, int H, int Hkv, int hd, double scale, long long wl,
+                       long long wr, double softcap, long long q_offset, const double* key_mask,
+                       long long mask_bstride, const double* bias, const long long* bs)
+{
+    attn_dims d = make_dims_ex(B, Tq, Tk, H, Hkv, hd, scale, wl, wr, softcap, q_offset, key_mask,
+                               mask_bstride, bias, bs);
+    return fwd_dims(&d, q, k, v, o, lse);
+}
+
+static int probs_dims(const attn_dims* dp, const double* q, const double* k, const double* v, double* P,
+                      int b, int h)
+{
+    const attn_dims d = *dp;
+    const int B = d.B, Tq = d.Tq, Tk = d.Tk, H = d.H, hd = d.hd;
     if (!dims_ok(&d) || b < 0 || b >= B || h < 0 || h >= H) return -1;
     double* raw = (double*)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
     double* oi = (double*)malloc(sizeof(double) * (size_t)hd);
@@ -213,19 +268,39 @@ int oracle_attn_probs(const double* q, const double* k, const double* v, double*
     return 0;
 }
 
+/* The probability matrix P [Tq][Tk] of one (b, h), for invariant checks. */
+int oracle_attn_probs(const double* q, const double* k, const double* v, double* P, int b, int h,
+                      int B, int Tq, int Tk, int H, int Hkv, int hd, double scale, int causal,
+                      int window, double softcap, long long q_offset, const double* key_mask,
+                      long long mask_bstride)
+{
+    attn_dims d = make_dims(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset,
+                            key_mask, mask_bstride);
+    return probs_dims(&d, q, k, v, P, b, h);
+}
+
+int oracle_attn_probs_ex(const double* q, const double* k, const double* v, double* P, int b, int h,
+                         int B, int Tq, int Tk, int H, int Hkv, int hd, double scale, long long wl,
+                         long long wr, double softcap, long long q_offset, const double* key_mask,
+                         long long mask_bstride, const double* bias, const long long* bs)
+{
+    attn_dims d = make_dims_ex(B, Tq, Tk, H, Hkv, hd, scale, wl, wr, softcap, q_offset, key_mask,
+                               mask_bstride, bias, bs);
+    return probs_dims(&d, q, k, v, P, b, h);
+}
+
 /*
  * Backward straight from the definition: P is rebuilt row by row from the
  * inputs (not from a saved LSE), O and D come from that P.  dq/dk/dv are
  * overwritten.  Parallel over (b, kv head) so that each thread owns its dK/dV
  * rows (the GQA group sum of forge attention.metal, attention_bwd_dkv_f32).
  */
-int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
-                    double* dq, double* dk, double* dv, int B, int Tq, int Tk, int H, int Hkv,
-                    int hd, double scale, int causal, int window, double softcap,
-                    long long q_offset, const double* key_mask, long long mask_bstride)
+static int bwd_dims(const attn_dims* dp, const double* q, const double* k, const double* v,
+                    const double* dout, double* dq, double* dk, double* dv)
 {
-    attn_dims d = make_dims(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset,
-                            key_mask, mask_bstride);
+    const attn_dims d = *dp;
+    const int B = d.B, Tq = d.Tq, Tk = d.Tk, H = d.H, Hkv = d.Hkv, hd = d.hd;
+    const double scale = d.scale, softcap = d.softcap;
     if (!dims_ok(&d)) return -1;
     const int G = H / Hkv;
     int failed = 0;
@@ -284,6 +359,27 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
             free(oi);
         }
     return failed ? -1 : 0;
+}
+
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv, int B, int Tq, int Tk, int H, int Hkv,
+                    int hd, double scale, int causal, int window, double softcap,
+                    long long q_offset, const double* key_mask, long long mask_bstride)
+{
+    attn_dims d = make_dims(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset,
+                            key_mask, mask_bstride);
+    return bwd_dims(&d, q, k, v, dout, dq, dk, dv);
+}
+
+int oracle_attn_bwd_ex(const double* q, const double* k, const double* v, const double* dout,
+                       double* dq, double* dk, double* dv, int B, int Tq, int Tk, int H, int Hkv,
+                       int hd, double scale, long long wl, long long wr, double softcap,
+                       long long q_offset, const double* key_mask, long long mask_bstride,
+                       const double* bias, const long long* bs)
+{
+    attn_dims d = make_dims_ex(B, Tq, Tk, H, Hkv, hd, scale, wl, wr, softcap, q_offset, key_mask,
+                               mask_bstride, bias, bs);
+    return bwd_dims(&d, q, k, v, dout, dq, dk, dv);
 }
 
 /* Threads the OpenMP runtime will use (reported next to oracle timings). */
