@@ -20,7 +20,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_bwd_workspace_size", "attn_decode_workspace_size",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_bwd_workspace_size", "attn_decode_workspace_size",
            "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_launch_count", "AttnError", "lib",
            "library_path"]
 
@@ -70,6 +70,11 @@ def lib():
         L.attn_decode.restype = i
         L.attn_decode_len.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + [i] * 6 + [f, i, i, f, vp, vp, ll, vp]
         L.attn_decode_len.restype = i
+        tail_ex = [i, i, i, i, i, i, f, i, i, f, i, vp, ll, vp, ll, ll, ll, ll, vp]
+        L.attn_fwd_ex.argtypes = [i, vp, vp, vp, vp, vp] + tail_ex
+        L.attn_fwd_ex.restype = i
+        L.attn_bwd_ex.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz] + tail_ex
+        L.attn_bwd_ex.restype = i
         L.attn_varlen_fwd.argtypes = [i] + [vp] * 7 + [i] * 8 + [f, i, i, f, vp]
         L.attn_varlen_fwd.restype = i
         L.attn_varlen_bwd.argtypes = [i] + [vp] * 10 + [sz, vp, vp] + [i] * 8 + [f, i, i, f, vp]
@@ -258,6 +263,65 @@ def attn_decode_len(q, k, v, lengths, *, H, Hkv, scale=None, causal=True, window
                                _stream(stream))
     _check(st, "attn_decode_len")
     return o, lse
+
+
+def _bias(bias, B, H, Tq, Tk):
+    """(tensor or None, 4 strides in elements) of a bias broadcastable to [B, H, Tq, Tk]."""
+    if bias is None:
+        return None, (0, 0, 0, 0)
+    torch = _torch()
+    if bias.dtype != torch.float32 or bias.dim() != 4:
+        raise ValueError("bias must be a 4-D fp32 tensor [B|1, H|1, Tq|1, Tk|1]")
+    st = []
+    for dim, n, s in zip(bias.shape, (B, H, Tq, Tk), bias.stride()):
+        if dim not in (1, n):
+            raise ValueError("bias shape %s does not broadcast to %s" % (tuple(bias.shape), (B, H, Tq, Tk)))
+        st.append(0 if dim == 1 else s)
+    return bias, tuple(st)
+
+
+def attn_fwd_ex(q, k, v, *, H, Hkv, scale=None, window_left=-1, window_right=-1, softcap=0.0, q_offset=0,
+                key_mask=None, bias=None, o=None, lse=None, want_lse=True, stream=None):
+    """Forward with the two-sided window [p - window_left, p + window_right] (negative:
+    unbounded) and an optional fp32 additive bias broadcastable to [B, H, Tq, Tk]."""
+    torch = _torch()
+    _contig(q, k, v, o, lse)
+    B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    bt, bs = _bias(bias, B, H, Tq, Tk)
+    st = lib().attn_fwd_ex(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Tq, Tk, H, Hkv, hd, float(scale),
+                           int(window_left), int(window_right), float(softcap), int(q_offset), _ptr(m), int(ms),
+                           _ptr(bt), *bs, _stream(stream))
+    _check(st, "attn_fwd_ex")
+    return o, lse
+
+
+def attn_bwd_ex(q, k, v, o, do, lse, *, H, Hkv, scale=None, window_left=-1, window_right=-1, softcap=0.0,
+                q_offset=0, key_mask=None, bias=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of attn_fwd_ex (same window and bias); returns (dq, dk, dv), overwritten."""
+    torch = _torch()
+    _contig(q, k, v, o, do, lse, dq, dk, dv)
+    B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nbytes = attn_bwd_workspace_size(B, Tq, H)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    bt, bs = _bias(bias, B, H, Tq, Tk)
+    st = lib().attn_bwd_ex(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                           _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, Tq, Tk, H, Hkv,
+                           hd, float(scale), int(window_left), int(window_right), float(softcap), int(q_offset),
+                           _ptr(m), int(ms), _ptr(bt), *bs, _stream(stream))
+    _check(st, "attn_bwd_ex")
+    return dq, dk, dv
 
 
 def _varlen_dims(q, k, cu_q, cu_k, H, Hkv):

@@ -113,7 +113,10 @@ Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, i
     p.B = B; p.Tq = Tq; p.Tk = Tk; p.H = H; p.Hkv = Hkv; p.hd = hd; p.G = H / Hkv;
     p.scale = scale;
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.causal = causal; p.window = window; p.softcap = softcap; p.q_offset = q_offset;
+    // causal, window (ferrotensor's |p - j| < window) as the two-sided window
+    p.wl = window > 0 ? window - 1 : -1;
+    p.wr = causal ? 0 : (window > 0 ? window - 1 : -1);
+    p.softcap = softcap; p.q_offset = q_offset;
     p.key_mask = key_mask; p.mask_bstride = mstride;
     p.status = status_ptr();
     return p;
@@ -141,8 +144,6 @@ void decode_plan(int B, int Lq, int Tk, int H, int Hkv, int* splits, int* chunk)
     *chunk = (int)c;
     *splits = Tk > 0 ? (int)((Tk + c - 1) / c) : 1;
 }
-
-attn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 // O = 0, LSE = -inf for every row (Tk == 0: no key is visible).
 template <typename T>
@@ -184,12 +185,14 @@ const char* attn_status_string(attn_status s) {
 
 int attn_kernel_family(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) ? 1 : 0; }
 
-attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                     int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal, int window, float softcap,
-                     int q_offset, const float* key_mask, long long key_mask_bstride, void* stream) {
-    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
-                                  key_mask_bstride);
-    if (st != ATTN_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// The forward once the arguments are checked and the window set in p.
+attn_status fwd_launch(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, Params p,
+                       void* stream) {
+    const int B = p.B, Tq = p.Tq, Tk = p.Tk, H = p.H, Hkv = p.Hkv, hd = p.hd;
     if (B == 0 || Tq == 0) return ATTN_OK;
     if (!q || !o || (Tk > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (lse && !aligned16(lse)))
@@ -197,11 +200,11 @@ attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (Tk == 0)
         return fill_empty(dt, o, (long long)B * Tq * H * hd, lse, lse ? (long long)B * H * Tq : 0, s);
-    Params p = base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
-                           key_mask_bstride);
     if (!p.status) return ATTN_ERR_CUDA;
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
-    if (!use_tcgen05(dt, hd)) return counted(launch_simt_fwd(p, (int)dt, s), 1);
+    // a bias with a softcap has no tensor-core form (the cap is not linear in the raw
+    // score): those calls take the CUDA-core kernels
+    if (!use_tcgen05(dt, hd) || (p.bias && p.softcap > 0.f)) return counted(launch_simt_fwd(p, (int)dt, s), 1);
     FwdMaps maps;
     if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
         !make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 128) ||
@@ -211,20 +214,37 @@ attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v,
     return counted(launch_tc_fwd(p, (int)dt, maps, s), 1);
 }
 
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal, int window, float softcap,
+                     int q_offset, const float* key_mask, long long key_mask_bstride, void* stream) {
+    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    return fwd_launch(dt, q, k, v, o, lse,
+                      base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride),
+                      stream);
+}
+
 size_t attn_bwd_workspace_size(int B, int Tq, int H) {
     if (B < 0 || Tq < 0 || H < 0) return 0;
     const size_t tq_pad = ((size_t)Tq + 63) / 64 * 64;
     return 2 * (size_t)B * H * tq_pad * sizeof(float);  // D and LSE*log2(e), rows padded to 64
 }
 
-attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
-                            const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
-                            size_t workspace_bytes, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
-                            int causal, int window, float softcap, int q_offset, const float* key_mask,
-                            long long key_mask_bstride, void* stream, int phases) {
-    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
-                                  key_mask_bstride);
-    if (st != ATTN_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// The backward once the arguments are checked and the window set in p.
+attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                       Params p, void* stream, int phases) {
+    const int B = p.B, Tq = p.Tq, Tk = p.Tk, H = p.H, Hkv = p.Hkv, hd = p.hd;
     if (phases <= 0 || phases > 7) return ATTN_ERR_INVALID_ARG;
     if (B == 0) return ATTN_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -248,15 +268,13 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
     const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
     for (const void* x : ptrs)
         if (!aligned16(x)) return ATTN_ERR_INVALID_ARG;
-    Params p = base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
-                           key_mask_bstride);
     if (!p.status) return ATTN_ERR_CUDA;
     p.q = q; p.k = k; p.v = v; p.o_in = o; p.dout = dout; p.lse_in = lse;
     p.dq = dq; p.dk = dk; p.dv = dv;
     p.tq_pad = (Tq + 63) / 64 * 64;
     p.ndelta = static_cast<float*>(workspace);
     p.nlse2 = p.ndelta + (size_t)B * H * p.tq_pad;
-    if (!use_tcgen05(dt, hd)) {
+    if (!use_tcgen05(dt, hd) || (p.bias && p.softcap > 0.f)) {
         // the fp32 dQ pass reads D from the workspace: pass 4 implies pass 1 there
         const int ph = (phases & 4) ? (phases | 1) : phases;
         const int nks = ((ph & 1) ? 1 : 0) + ((ph & 2) ? 1 : 0) + ((ph & 4) ? 1 : 0);
@@ -279,6 +297,24 @@ attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const v
                           !make_map(&maps.dv32, dt, dv, (long long)Hkv * hd, Tk, B, 32))))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_bwd(p, (int)dt, maps, phases, s), nk);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
+                            int causal, int window, float softcap, int q_offset, const float* key_mask,
+                            long long key_mask_bstride, void* stream, int phases) {
+    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    return bwd_launch(dt, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                      base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride),
+                      stream, phases);
 }
 
 attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -391,6 +427,57 @@ attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k, const v
         !make_map(&maps.dv32, dt, dv, (long long)Hkv * hd, total_k, 1, 32))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_bwd(p, (int)dt, maps, 7, s), 2);
+}
+
+// ----------------------------------------- two-sided window, additive bias
+}  // extern "C"
+
+namespace {
+
+// Params of an _ex call: the window sides (negative = unbounded) and the bias.
+attn_status ex_params(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, int window_left,
+                      int window_right, float softcap, int q_offset, const float* key_mask, long long mstride,
+                      const float* bias, long long sb, long long sh, long long sq, long long sk, Params* out) {
+    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, 0, 0, softcap, q_offset, key_mask, mstride);
+    if (st != ATTN_OK) return st;
+    if (bias && ((reinterpret_cast<uintptr_t>(bias) & 3u) || sb < 0 || sh < 0 || sq < 0 || sk < 0))
+        return ATTN_ERR_INVALID_ARG;
+    Params p = base_params(B, Tq, Tk, H, Hkv, hd, scale, 0, 0, softcap, q_offset, key_mask, mstride);
+    p.wl = window_left < 0 ? -1 : window_left;
+    p.wr = window_right < 0 ? -1 : window_right;
+    p.bias = bias;
+    p.bias_sb = sb; p.bias_sh = sh; p.bias_sq = sq; p.bias_sk = sk;
+    *out = p;
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd_ex(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Tq, int Tk, int H, int Hkv, int hd, float scale, int window_left, int window_right,
+                        float softcap, int q_offset, const float* key_mask, long long key_mask_bstride,
+                        const float* bias, long long bias_sb, long long bias_sh, long long bias_sq,
+                        long long bias_sk, void* stream) {
+    Params p;
+    attn_status st = ex_params(dt, B, Tq, Tk, H, Hkv, hd, scale, window_left, window_right, softcap, q_offset,
+                               key_mask, key_mask_bstride, bias, bias_sb, bias_sh, bias_sq, bias_sk, &p);
+    if (st != ATTN_OK) return st;
+    return fwd_launch(dt, q, k, v, o, lse, p, stream);
+}
+
+attn_status attn_bwd_ex(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                        size_t workspace_bytes, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
+                        int window_left, int window_right, float softcap, int q_offset, const float* key_mask,
+                        long long key_mask_bstride, const float* bias, long long bias_sb, long long bias_sh,
+                        long long bias_sq, long long bias_sk, void* stream) {
+    Params p;
+    attn_status st = ex_params(dt, B, Tq, Tk, H, Hkv, hd, scale, window_left, window_right, softcap, q_offset,
+                               key_mask, key_mask_bstride, bias, bias_sb, bias_sh, bias_sq, bias_sk, &p);
+    if (st != ATTN_OK) return st;
+    return bwd_launch(dt, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, p, stream, 7);
 }
 
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

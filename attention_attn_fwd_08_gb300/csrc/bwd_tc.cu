@@ -66,15 +66,16 @@ struct KVCfg {
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
-// VL: packed variable-length sequences (cu_seqlens); the dense instantiation
-// carries none of their bookkeeping.
-template <bool BF16, int HD, bool VL>
+// MODE 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with an
+// additive score bias.  Each instantiation carries only its own bookkeeping.
+template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV) {
     using C = KVCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BKV = C::BKV;
+    constexpr bool VL = MODE == 1, BIAS = MODE == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -100,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Seq sq = seq_of<VL>(P, b);
     if (j0 >= sq.tk) return;  // (packed) past this sequence's keys: nothing to write
     int qlo, qhi;
-    query_range(P.causal, P.window, sq.tq, P.q_offset, j0, min(j0 + BKV, sq.tk), &qlo, &qhi);
+    query_range(P.wl, P.wr, sq.tq, P.q_offset, j0, min(j0 + BKV, sq.tk), &qlo, &qhi);
     const int qt0 = qlo / BQ;
     const int nqt = qhi > qlo ? (qhi + BQ - 1) / BQ - qt0 : 0;
     const int ntiles = nqt * P.G;  // (head, query tile) pairs, head-major
@@ -243,11 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int h = tile_head(n), i0 = tile_i0(n);
             // visible query columns of this key row in the tile
             int clo = 0, chi = min(BQ, sq.tq - i0);
-            if (P.causal) clo = max(clo, j - P.q_offset - i0);
-            if (P.window > 0) {
-                chi = min(chi, j + P.window - P.q_offset - i0);
-                if (!P.causal) clo = max(clo, j - P.window + 1 - P.q_offset - i0);
-            }
+            // query position p sees key j when p - wl <= j <= p + wr
+            if (P.wr >= 0) clo = max(clo, j - P.wr - P.q_offset - i0);
+            if (P.wl >= 0) chi = min(chi, j + P.wl - P.q_offset - i0 + 1);
             if (!key_live) chi = 0;
             // the stats arrive with Q/dO of this tile; S^T/dP^T come from the MMA
             const int s = n % NS;
@@ -269,6 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(sv[1]);
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
+            if (BIAS && key_live) {  // additive score bias of (query i0 + cc, key j); never with softcap here
+                const float* col = P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh +
+                                   (long long)i0 * P.bias_sq + (long long)j * P.bias_sk;
+                const float inv = 1.f / P.scale;
+#pragma unroll
+                for (int cc = 0; cc < BQ; ++cc)
+                    if (i0 + cc < sq.tq)
+                        sv[cc >> 5][cc & 31] = __float_as_uint(
+                            fmaf(__ldg(col + (long long)cc * P.bias_sq), inv, __uint_as_float(sv[cc >> 5][cc & 31])));
+            }
             uint32_t pk[32], dk[32];
             // With a softcap, the polynomial serves the tile unless a raw score of the
             // row lies outside its range (checked before masking)
@@ -471,7 +480,7 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
     it.sq = seq_of<VL>(P, it.b);
     int lo = 0, hi = 0;
     if (it.i0 < it.sq.tq)  // (packed) items past a sequence's rows have no tiles
-        key_range(P.causal, P.window, it.sq.tk, it.i0 + P.q_offset, min(it.i0 + BQ, it.sq.tq) - 1 + P.q_offset, &lo,
+        key_range(P.wl, P.wr, it.sq.tk, it.i0 + P.q_offset, min(it.i0 + BQ, it.sq.tq) - 1 + P.q_offset, &lo,
                   &hi);
     it.kt0 = lo / BK;
     it.ntiles = hi > lo ? (hi + BK - 1) / BK - it.kt0 : 0;
@@ -486,13 +495,14 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
 // are loaded into shared memory once the current ones are in TMEM, and copied
 // into TMEM right after the current item's last dS, so its first S and dP run
 // while the current item's epilogue reads dQ out.
-template <bool BF16, int HD, bool VL>
+template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreadsDQ, 1)
     bwd_dq_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                   const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDQ) {
     using C = QCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BK = C::BK;
+    constexpr bool VL = MODE == 1, BIAS = MODE == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -804,11 +814,8 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                     mbits = __ballot_sync(0xffffffffu, j < tk && mrow[j] > 0.5f);
                 }
                 int clo = 0, chi = min(32, tk - jc);
-                if (P.causal) chi = min(chi, p - jc + 1);
-                if (P.window > 0) {
-                    clo = max(clo, p - P.window + 1 - jc);
-                    if (!P.causal) chi = min(chi, p + P.window - jc);
-                }
+                if (P.wr >= 0) chi = min(chi, p + P.wr - jc + 1);
+                if (P.wl >= 0) clo = max(clo, p - P.wl - jc);
                 if (!row_ok) chi = 0;
                 if (!warp_wait(BAR(ST_FULL(bf)), (t >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
                     ok = false;
@@ -821,6 +828,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 tmem_ld_wait_only();
                 tmem_pin(sv);
                 tmem_pin(dp);
+                if (BIAS && row_ok) add_bias32(P, it.b, it.h, i, jc, tk, sv);  // (never with softcap here)
                 uint32_t dsk[16];
                 // with a softcap, the polynomial serves the tile unless a raw score of the
                 // row lies outside its range (checked before masking)
@@ -983,7 +991,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         if (e != cudaSuccess) return e;
     }
     if (phases & 4) {
-        auto k = p.cu_q ? bwd_dq_kernel<BF16, HD, true> : bwd_dq_kernel<BF16, HD, false>;
+        auto k = p.cu_q ? bwd_dq_kernel<BF16, HD, 1> : p.bias ? bwd_dq_kernel<BF16, HD, 2> : bwd_dq_kernel<BF16, HD, 0>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         int dev = 0, nsm = 0;
@@ -996,7 +1004,8 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
-        auto k = p.cu_q ? bwd_dkdv_kernel<BF16, HD, true> : bwd_dkdv_kernel<BF16, HD, false>;
+        auto k = p.cu_q ? bwd_dkdv_kernel<BF16, HD, 1>
+                        : p.bias ? bwd_dkdv_kernel<BF16, HD, 2> : bwd_dkdv_kernel<BF16, HD, 0>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;

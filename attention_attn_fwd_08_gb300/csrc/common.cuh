@@ -37,7 +37,10 @@ struct Params {
     int B, Tq, Tk, H, Hkv, hd, G;
     float scale;         // softmax scale (natural units)
     float scale_log2;    // scale * log2(e)
-    int causal, window;
+    int wl, wr;          // visible keys [p - wl, p + wr] for the query at position p; -1: unbounded side
+    // additive score bias, bias[b*bias_sb + h*bias_sh + i*bias_sq + j*bias_sk], or NULL
+    const float* bias;
+    long long bias_sb, bias_sh, bias_sq, bias_sk;
     float softcap;       // 0 = off
     int q_offset;
     int splits, chunk;   // decode
@@ -143,48 +146,57 @@ __device__ __forceinline__ Seq seq_any(const Params& P, int b) {
     return P.cu_q ? seq_of<true>(P, b) : seq_of<false>(P, b);
 }
 
+// ------------------------------------------------------------ score bias
+// Adds bias(b, h, i, j) / scale to 32 raw scores q.k of row i, keys j0 .. j0+31
+// (so that the scaled score gains the bias); keys from tk on get nothing (they
+// are invisible).  Contiguous 16-byte-aligned rows load as float4.
+__device__ __forceinline__ void add_bias32(const Params& P, int b, int h, int i, int j0, int tk, uint32_t (&s)[32]) {
+    const float* row = P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh + (long long)i * P.bias_sq;
+    const float inv = 1.f / P.scale;
+    if (P.bias_sk == 1 && j0 + 32 <= tk && ((reinterpret_cast<uintptr_t>(row + j0) & 15u) == 0)) {
+        const float4* r4 = reinterpret_cast<const float4*>(row + j0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 v = __ldg(r4 + e);
+            s[4 * e + 0] = __float_as_uint(fmaf(v.x, inv, __uint_as_float(s[4 * e + 0])));
+            s[4 * e + 1] = __float_as_uint(fmaf(v.y, inv, __uint_as_float(s[4 * e + 1])));
+            s[4 * e + 2] = __float_as_uint(fmaf(v.z, inv, __uint_as_float(s[4 * e + 2])));
+            s[4 * e + 3] = __float_as_uint(fmaf(v.w, inv, __uint_as_float(s[4 * e + 3])));
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            if (j0 + e < tk)
+                s[e] = __float_as_uint(fmaf(__ldg(row + (long long)(j0 + e) * P.bias_sk), inv, __uint_as_float(s[e])));
+    }
+}
+
 // ------------------------------------------------------------ visibility
 // Key j (of tk) visible to the query at absolute position p (see include/attn.h).
 __device__ __forceinline__ bool visible(const Params& P, int b, int p, int j, int tk) {
     if (j < 0 || j >= tk) return false;
-    if (P.causal && j > p) return false;
-    if (P.window > 0) {
-        int gap = p - j;
-        gap = gap < 0 ? -gap : gap;
-        if (gap >= P.window) return false;
-    }
+    if (P.wr >= 0 && j > p + P.wr) return false;
+    if (P.wl >= 0 && j < p - P.wl) return false;
     if (P.key_mask && !(P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f)) return false;
     return true;
 }
 
 // Range of keys [lo, hi) that any query with position in [p0, p1] can see,
-// before the key mask.  Empty when lo >= hi.
-__host__ __device__ __forceinline__ void key_range(int causal, int window, int Tk, int p0, int p1,
-                                                   int* lo, int* hi) {
+// before the key mask: the window [p - wl, p + wr] (-1 = unbounded side).
+__host__ __device__ __forceinline__ void key_range(int wl, int wr, int Tk, int p0, int p1, int* lo, int* hi) {
     long long l = 0, h = Tk;
-    if (causal) h = (long long)p1 + 1 < h ? (long long)p1 + 1 : h;
-    if (window > 0) {
-        long long wl = (long long)p0 - window + 1;
-        l = wl > l ? wl : l;
-        if (!causal) {
-            long long wh = (long long)p1 + window;
-            h = wh < h ? wh : h;
-        }
-    }
+    if (wr >= 0 && (long long)p1 + wr + 1 < h) h = (long long)p1 + wr + 1;
+    if (wl >= 0 && (long long)p0 - wl > l) l = (long long)p0 - wl;
     if (h < l) h = l;
     *lo = (int)l;
     *hi = (int)h;
 }
 
 // True when every query in [p0, p1] sees every key in [j0, j1) (ignoring the key mask).
-__host__ __device__ __forceinline__ bool tile_full(int causal, int window, int Tk, int p0, int p1,
-                                                   int j0, int j1) {
+__host__ __device__ __forceinline__ bool tile_full(int wl, int wr, int Tk, int p0, int p1, int j0, int j1) {
     if (j1 > Tk) return false;
-    if (causal && j1 - 1 > p0) return false;
-    if (window > 0) {
-        if (p1 - j0 >= window) return false;               // oldest key too old for the newest query
-        if (!causal && (j1 - 1) - p0 >= window) return false;  // newest key too far ahead
-    }
+    if (wr >= 0 && (long long)j1 - 1 > (long long)p0 + wr) return false;  // newest key ahead of the oldest query
+    if (wl >= 0 && (long long)j0 < (long long)p1 - wl) return false;      // oldest key behind the newest query
     return true;
 }
 
@@ -648,22 +660,12 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) {
 
 namespace attn {
 // Queries [lo, hi) (row indices) that can see at least one key of [j0, j1),
-// before the key mask.
-__host__ __device__ __forceinline__ void query_range(int causal, int window, int Tq, int q_offset,
-                                                     int j0, int j1, int* lo, int* hi) {
+// before the key mask: position p = i + q_offset with j0 - wr <= p <= j1 - 1 + wl.
+__host__ __device__ __forceinline__ void query_range(int wl, int wr, int Tq, int q_offset, int j0, int j1, int* lo,
+                                                     int* hi) {
     long long l = 0, h = Tq;
-    if (causal) {
-        long long c = (long long)j0 - q_offset;
-        l = c > l ? c : l;
-    }
-    if (window > 0) {
-        long long wh = (long long)j1 - 1 + window - 1 - q_offset + 1;  // p <= j1-1 + window-1
-        h = wh < h ? wh : h;
-        if (!causal) {
-            long long wl = (long long)j0 - window + 1 - q_offset;
-            l = wl > l ? wl : l;
-        }
-    }
+    if (wr >= 0 && (long long)j0 - wr - q_offset > l) l = (long long)j0 - wr - q_offset;
+    if (wl >= 0 && (long long)j1 - 1 + wl - q_offset + 1 < h) h = (long long)j1 - 1 + wl - q_offset + 1;
     if (h < l) h = l;
     *lo = (int)l;
     *hi = (int)h;

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Params P,
     }
     // keys this CTA reads: its chunk, cut to what any of its rows can see
     int lo, hi;
-    key_range(P.causal, P.window, tk_b, qoff, qoff + P.Tq - 1, &lo, &hi);
+    key_range(P.wl, P.wr, tk_b, qoff, qoff + P.Tq - 1, &lo, &hi);
     const int c0 = split * P.chunk, c1 = min(tk_b, c0 + P.chunk);
     lo = max(lo, c0);
     hi = min(hi, c1);

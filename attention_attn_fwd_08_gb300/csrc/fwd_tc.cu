@@ -38,7 +38,7 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, 
     const int p0 = i0 + P.q_offset;
     const int p1 = min(i0 + BM, tq) - 1 + P.q_offset;
     int lo, hi;
-    key_range(P.causal, P.window, tk, p0, p1, &lo, &hi);
+    key_range(P.wl, P.wr, tk, p0, p1, &lo, &hi);
     TileInfo t;
     t.t0 = lo / BN;
     t.ntiles = hi > lo ? (hi + BN - 1) / BN - t.t0 : 0;
@@ -129,12 +129,13 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
 }
 __device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * BM - 1) / (2 * BM) * P.H * P.B; }
 
-// VL: packed variable-length sequences (cu_seqlens); the dense instantiation
-// carries none of their bookkeeping.
-template <bool BF16, int HD, bool VL>
+// MODE 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with an
+// additive score bias.  Each instantiation carries only its own bookkeeping.
+template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
+    constexpr bool VL = MODE == 1, BIAS = MODE == 2;
     using C = Fwd2Cfg<HD>;
     constexpr int NS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -524,17 +525,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     }
                 }
                 // a tile whose keys the mask keeps whole needs no mask pass
-                const bool full = tile_full(P.causal, P.window, tk, prow0, prow1, j0, j0 + BN) &&
+                const bool full = tile_full(P.wl, P.wr, tk, prow0, prow1, j0, j0 + BN) &&
                                   (mbits[0] & mbits[1] & mbits[2] & mbits[3]) == 0xffffffffu;
                 // this row's visible columns of the tile: [clo, chi), and the key-mask bits
                 int clo = 0, chi = BN;
                 if (!full) {
                     chi = min(chi, tk - j0);
-                    if (P.causal) chi = min(chi, p - j0 + 1);
-                    if (P.window > 0) {
-                        clo = max(clo, p - P.window + 1 - j0);
-                        if (!P.causal) chi = min(chi, p + P.window - j0);
-                    }
+                    if (P.wr >= 0) chi = min(chi, p + P.wr - j0 + 1);
+                    if (P.wl >= 0) clo = max(clo, p - P.wl - j0);
                 }
                 if (!wait_warp(S_FULL(u), sc & 1)) {
                     ok = false;
@@ -558,6 +556,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 tmem_ld_wait_only();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
+                if (BIAS && i < tq) {  // additive score bias (never with softcap here)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) add_bias32(P, it.b, it.h, i, j0 + 32 * c, tk, sv[c]);
+                }
                 if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits, sv);
                 else run_tile(std::integral_constant<bool, false>(), m_used, l, k, full, clo, chi, mbits, sv);
                 tmem_st_wait();
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
 template <bool BF16, int HD>
 cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     using C = Fwd2Cfg<HD>;
-    auto kern = p.cu_q ? fwd_tc2_kernel<BF16, HD, true> : fwd_tc2_kernel<BF16, HD, false>;
+    auto kern = p.cu_q ? fwd_tc2_kernel<BF16, HD, 1> : p.bias ? fwd_tc2_kernel<BF16, HD, 2> : fwd_tc2_kernel<BF16, HD, 0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
     if (e != cudaSuccess) return e;
     int dev = 0, nsm = 0;

@@ -43,6 +43,12 @@ __device__ __forceinline__ float warp_sum(float x) {
 __device__ __forceinline__ float capped(float s, float softcap) {
     return softcap > 0.f ? softcap * tanhf(s / softcap) : s;
 }
+// additive score bias of (b, h, i, j), or 0
+__device__ __forceinline__ float bias_at(const Params& P, int b, int h, int i, int j) {
+    return P.bias ? P.bias[(long long)b * P.bias_sb + (long long)h * P.bias_sh + (long long)i * P.bias_sq +
+                           (long long)j * P.bias_sk]
+                  : 0.f;
+}
 
 // head h of query row i (key row j) of sequence sq
 __device__ __forceinline__ long long qoff(const Params& P, const Seq& sq, int i, int h) {
@@ -78,7 +84,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
     const int p = i + P.q_offset;
     const int ilast = min(i0 + kRows, sq.tq) - 1;
     int lo, hi;
-    key_range(P.causal, P.window, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+    key_range(P.wl, P.wr, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
 
     for (int d = lane; d < HD; d += 32)
         Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, sq, i, h)[d]) : 0.f;
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
 #pragma unroll 8
             for (int d = 0; d < HD; ++d) dot = fmaf(Qs[warp * HD + d], Ks[jj * (HD + 1) + d], dot);
             vis[t] = row_ok && visible(P, b, p, j, sq.tk);
-            s[t] = vis[t] ? capped(dot * P.scale, P.softcap) : -INFINITY;
+            s[t] = vis[t] ? capped(dot * P.scale, P.softcap) + bias_at(P, b, h, i, j) : -INFINITY;
         }
         const float m_new = fmaxf(m, warp_max(fmaxf(s[0], s[1])));
         if (m_new == -INFINITY) continue;  // nothing visible yet for this row (warp-uniform)
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
     const int p = i + P.q_offset;
     const int ilast = min(i0 + kRows, sq.tq) - 1;
     int lo, hi;
-    key_range(P.causal, P.window, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+    key_range(P.wl, P.wr, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
     for (int d = lane; d < HD; d += 32) {
         Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, sq, i, h)[d]) : 0.f;
         Gs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.dout, sq, i, h)[d]) : 0.f;
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
                     st = P.softcap * th;
                     dcap = 1.f - th * th;
                 }
-                const float pr = expf(st - lse);
+                const float pr = expf(st + bias_at(P, b, h, i, j) - lse);
                 ds = pr * (gv - Dd) * dcap;
             }
             Ss[warp * kTile + jj] = ds;
@@ -289,7 +295,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
     const bool key_ok = j < sq.tk;
     const int jlast = min(j0 + kRows, sq.tk);
     int qlo, qhi;
-    query_range(P.causal, P.window, sq.tq, P.q_offset, j0, jlast, &qlo, &qhi);
+    query_range(P.wl, P.wr, sq.tq, P.q_offset, j0, jlast, &qlo, &qhi);
     for (int d = lane; d < HD; d += 32) {
         Ks[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.k, sq, j, kvh)[d]) : 0.f;
         Vs[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.v, sq, j, kvh)[d]) : 0.f;
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
                         st = P.softcap * th;
                         dcap = 1.f - th * th;
                     }
-                    pr = expf(st - Ls[ii]);
+                    pr = expf(st + bias_at(P, b, h, i, j) - Ls[ii]);
                     ds = pr * (gv - Ds[ii]) * dcap;
                 }
                 Pw[warp * kTile + ii] = pr;

@@ -462,7 +462,8 @@ def time_passes(torch, stream, passes, args, flush_buf):
 def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
     """Sliding-window + softcap fwd/bwd (B=2 T=8192 H=16 Hkv=4 hd=128 window=1024 softcap=50, bf16), the
     bidirectional key-masked encoder forward (B=8 T=1024 H=Hkv=12 hd=64, fp16) and packed variable-length
-    causal fwd/bwd (8 sequences of U{256..2048} rows, H=32 Hkv=8 hd=128, bf16), flops over visible pairs."""
+    causal fwd/bwd (8 sequences of U{256..2048} rows, H=32 Hkv=8 hd=128, bf16) and the GQA causal prefill with
+    an additive [1, 1, T, T] fp32 score bias (fwd/bwd), flops over visible pairs."""
     out = {}
     ws_ = synth.WORKLOADS["swa_softcap"]
     si = synth.make_inputs(ws_)
@@ -512,6 +513,23 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
         out["varlen_packed_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
                                      "visible_pairs": pairs, "tokens": int(vi["cu"][-1]),
                                      "note": "8 causal sequences of U{256..2048} rows packed back to back"}
+    # additive score bias [1, 1, T, T] (fp32, L2-resident) on the GQA causal prefill shape
+    wb = synth.WORKLOADS["gqa_prefill"]
+    bi = synth.make_inputs(wb)
+    q, k, v, do = (bi[n].to(dev) for n in ("q", "k", "v", "do"))
+    bias = synth.normal((1, 1, wb.Tq, wb.Tk), wb.seed + 5, "f32").to(dev)
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((wb.B, wb.H, wb.Tq), dtype=torch.float32, device=dev)
+    wsb = torch.empty(A.attn_bwd_workspace_size(wb.B, wb.Tq, wb.H), dtype=torch.uint8, device=dev)
+    kw = dict(H=wb.H, Hkv=wb.Hkv, scale=wb.scale, window_left=-1, window_right=0, bias=bias)
+    t = time_passes(torch, stream, [
+        ("fwd", lambda: A.attn_fwd_ex(q, k, v, o=o, lse=lse, **kw)),
+        ("bwd", lambda: A.attn_bwd_ex(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=wsb, **kw))], args, flush_buf)
+    pairs = visible_pairs(wb)
+    for n, fl in (("fwd", 4), ("bwd", 10)):
+        tf = fl * wb.hd * pairs / (t[n] * 1e-3) / 1e12
+        out["bias_prefill_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                    "visible_pairs": pairs, "note": "GQA causal prefill with a [1,1,T,T] fp32 bias"}
     st, word = A.attn_get_device_status()
     if st != A.OK:
         raise RuntimeError("device status word %#x after the masked workloads" % word)

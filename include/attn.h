@@ -189,6 +189,43 @@ ATTN_API attn_status attn_decode_len(attn_dtype dt, const void* q, const void* k
                         long long key_mask_bstride, void* stream);
 
 /*
+ * Forward and backward with a general two-sided window and an additive score
+ * bias.
+ * Source: ferrotensor engine/attention.rs (flash_attention_v2_with: additive mask
+ * [batch, heads, seq_q, seq_k], size-1 dimensions broadcast with stride 0 by
+ * mask_strides; AttentionOptions window |p - j| < window), brotensor
+ * ops/flash_attention.h, flash_attention_windowed_forward (bidirectional window:
+ * keys [p - window/2, p + window/2]) and forge attention.metal, attention_fwd_f32
+ * (one-sided window: keys from i + 1 - window on).
+ *   window_left, window_right : the query at absolute position p = i + q_offset
+ *                sees keys j with p - window_left <= j <= p + window_right; a
+ *                negative side is unbounded.  causal = (-1, 0); ferrotensor's
+ *                window w = (w-1, w-1), with causal (w-1, 0); brotensor's
+ *                bidirectional window w = (w/2, w/2); forge's one-sided window w =
+ *                (w-1, -1).
+ *   bias       : fp32 added to the (capped) scaled score of (b, h, i, j):
+ *                bias[b*bias_sb + h*bias_sh + i*bias_sq + j*bias_sk], strides in
+ *                elements (0 broadcasts a dimension), 4-byte aligned; NULL for none.
+ *                A -inf entry drops that pair.  The gradient treats it as a constant.
+ *   Everything else as attn_fwd / attn_bwd (key mask included).  16-bit calls with
+ *   both a bias and a softcap run on the CUDA-core kernels (same results, slower).
+ */
+ATTN_API attn_status attn_fwd_ex(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
+                        float* lse, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
+                        int window_left, int window_right, float softcap, int q_offset,
+                        const float* key_mask, long long key_mask_bstride, const float* bias,
+                        long long bias_sb, long long bias_sh, long long bias_sq, long long bias_sk,
+                        void* stream);
+
+ATTN_API attn_status attn_bwd_ex(attn_dtype dt, const void* q, const void* k, const void* v,
+                        const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                        void* dv, void* workspace, size_t workspace_bytes, int B, int Tq, int Tk,
+                        int H, int Hkv, int hd, float scale, int window_left, int window_right,
+                        float softcap, int q_offset, const float* key_mask,
+                        long long key_mask_bstride, const float* bias, long long bias_sb,
+                        long long bias_sh, long long bias_sq, long long bias_sk, void* stream);
+
+/*
  * Packed variable-length attention: the batch's sequences stored back to back
  * in one tensor, no padding, no attention across sequences.
  * Source: brotensor ops/flash_attention.h, flash_attention_varlen_forward and

@@ -156,6 +156,24 @@ def test_varlen_validation():
     assert A.attn_bwd_workspace_size(2, 64, 8) > 16
 
 
+def test_ex_validation():
+    """Argument errors of the window/bias calls come back before any launch."""
+    L = A.lib()
+    args = [2, BAD, BAD, BAD, BAD, None, 2, 64, 64, 8, 2, 128, 0.1, 10, 0, 0.0, 0, None, 0]
+    # bias not 4-byte aligned, negative bias stride
+    assert L.attn_fwd_ex(*args, ctypes.c_void_p(0x1002), 0, 0, 64, 1, None) == A.ERR_INVALID_ARG
+    assert L.attn_fwd_ex(*args, BAD, 0, 0, -64, 1, None) == A.ERR_INVALID_ARG
+    # the usual shape rules
+    bad_hd = [2, BAD, BAD, BAD, BAD, None, 2, 64, 64, 8, 2, 96, 0.1, 10, 0, 0.0, 0, None, 0]
+    assert L.attn_fwd_ex(*bad_hd, None, 0, 0, 0, 0, None) == A.ERR_UNSUPPORTED
+    st = L.attn_bwd_ex(2, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, 16, 2, 64, 64, 8, 2, 128, 0.1, 10, 0,
+                       0.0, 0, None, 0, None, 0, 0, 0, 0, None)
+    assert st == A.ERR_INVALID_ARG  # workspace too small
+    # nothing to do
+    zero = [2, None, None, None, None, None, 0, 64, 64, 8, 2, 128, 0.1, -1, -1, 0.0, 0, None, 0]
+    assert L.attn_fwd_ex(*zero, None, 0, 0, 0, 0, None) == A.OK
+
+
 def test_workspace_sizes():
     assert A.attn_bwd_workspace_size(4, 2048, 32) == 2 * 4 * 2048 * 32 * 4
     assert A.attn_bwd_workspace_size(1, 65, 2) == 2 * 1 * 128 * 2 * 4
