@@ -383,12 +383,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
             bool accurate = false;
             if constexpr (kCap) {
                 // largest raw |score| of the row, before masking
-                float amax = 0.f;
+                float am[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2)
-                        amax = max3f(amax, fabsf(__uint_as_float(sv[c][e])), fabsf(__uint_as_float(sv[c][e + 1])));
+                        am[c] = max3f(am[c], fabsf(__uint_as_float(sv[c][e])), fabsf(__uint_as_float(sv[c][e + 1])));
+                const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
                 const CapPoly cp = cap_poly(P.scale, P.softcap);
                 accurate = __any_sync(0xffffffffu, !(amax <= cp.r_max)) || (!full && !cp.inf_ok);
             }
@@ -405,12 +406,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 }
             }
             // pass 1: the row max of the scores, as x against the current reference
-            float rmax = -INFINITY;
+            float rm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
                 for (int e = 0; e < 32; e += 2)
-                    rmax = max3f(rmax, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+                    rm[c] = max3f(rm[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+            const float rmax = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
             // x is increasing in the score, so its row max is x(rmax)
             auto to_x = [&](auto modec, uint64_t rr, uint64_t nms) -> uint64_t {
                 constexpr int kMode = decltype(modec)::value;
