@@ -288,3 +288,31 @@ def varlen_bwd(q, k, v, do, cu_q, cu_k, *, H, Hkv, scale, causal=False, window=0
                          causal=causal, window=window, softcap=softcap)
         dq[q0:q1], dk[k0:k1], dv[k0:k1] = gq[0], gk[0], gv[0]
     return dq, dk, dv
+
+
+def rope(x, *, head_dim, pos=0, theta=10000.0):
+    """Rotate-half rotary embedding (ferrotensor engine/attention.rs, rope /
+    rope_theta): x is [batch, seq, heads*head_dim]; every head vector of token s
+    (counted within its sequence) gets position pos + s, and its pair
+    (x[i], x[i + head_dim/2]), i < head_dim/2, turns by the angle
+    (pos + s) * theta**(-2i/head_dim):
+        x'[i]          = x[i] cos - x[i + head_dim/2] sin
+        x'[i + hd/2]   = x[i + head_dim/2] cos + x[i] sin
+    Returns a new fp64 array (the page rotates in place)."""
+    x = _f64(x)
+    B, T, C = x.shape
+    hd = int(head_dim)
+    if hd % 2 or C % hd:
+        raise ValueError("head_dim must be even and divide the row")
+    half = hd // 2
+    out = x.copy().reshape(B, T, C // hd, hd)
+    xin = x.reshape(B, T, C // hd, hd)
+    for s in range(T):
+        p = float(pos + s)
+        for i in range(half):
+            ang = p * float(theta) ** (-2.0 * i / hd)
+            c, sn = np.cos(ang), np.sin(ang)
+            a, b = xin[:, s, :, i], xin[:, s, :, i + half]
+            out[:, s, :, i] = a * c - b * sn
+            out[:, s, :, i + half] = b * c + a * sn
+    return out.reshape(B, T, C)
