@@ -20,7 +20,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_bwd_workspace_size", "attn_decode_workspace_size",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_rope", "attn_bwd_workspace_size", "attn_decode_workspace_size",
            "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_launch_count", "AttnError", "lib",
            "library_path"]
 
@@ -75,6 +75,8 @@ def lib():
         L.attn_fwd_ex.restype = i
         L.attn_bwd_ex.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz] + tail_ex
         L.attn_bwd_ex.restype = i
+        L.attn_rope.argtypes = [i, vp, i, i, i, i, i, f, vp]
+        L.attn_rope.restype = i
         L.attn_varlen_fwd.argtypes = [i] + [vp] * 7 + [i] * 8 + [f, i, i, f, vp]
         L.attn_varlen_fwd.restype = i
         L.attn_varlen_bwd.argtypes = [i] + [vp] * 10 + [sz, vp, vp] + [i] * 8 + [f, i, i, f, vp]
@@ -322,6 +324,18 @@ def attn_bwd_ex(q, k, v, o, do, lse, *, H, Hkv, scale=None, window_left=-1, wind
                            _ptr(m), int(ms), _ptr(bt), *bs, _stream(stream))
     _check(st, "attn_bwd_ex")
     return dq, dk, dv
+
+
+def attn_rope(x, *, H, pos=0, theta=10000.0, stream=None):
+    """Rotate-half rotary embedding of x [B, T, H*hd] in place (every head vector of
+    token s at position pos + s); returns x."""
+    _contig(x)
+    if x.dim() != 3 or x.shape[2] % H:
+        raise ValueError("x must be [B, T, H*hd]")
+    B, T, C = x.shape
+    st = lib().attn_rope(_dt(x), _ptr(x), B, T, H, C // H, int(pos), float(theta), _stream(stream))
+    _check(st, "attn_rope")
+    return x
 
 
 def _varlen_dims(q, k, cu_q, cu_k, H, Hkv):

@@ -86,8 +86,7 @@ bool make_map(CUtensorMap* m, int dt, const void* base, long long inner, long lo
 // ------------------------------------------------------------- validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// decode_hd: the decode entry points also take hd 256 (16-bit types; their split kernel
-// is the only one built for it)
+// decode_hd: a decode entry point, whose 16-bit split kernel is built for hd 64, 128, 256
 attn_status check_common(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, int causal,
                          int window, float softcap, int q_offset, const float* key_mask, long long mstride,
                          bool decode_hd = false) {
@@ -102,7 +101,10 @@ attn_status check_common(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, i
     if (mstride < 0) return ATTN_ERR_INVALID_ARG;
     if (key_mask && (reinterpret_cast<uintptr_t>(key_mask) & 3u)) return ATTN_ERR_INVALID_ARG;
     if ((long long)Tq + q_offset > INT32_MAX - 1) return ATTN_ERR_INVALID_ARG;
-    if (hd != 64 && hd != 128 && !(decode_hd && hd == 256 && dt != ATTN_F32)) return ATTN_ERR_UNSUPPORTED;
+    // head sizes: 64 and 128 on the tensor cores (16-bit); 32, 96 and 256 also on the
+    // CUDA-core kernels; the 16-bit decode split kernel takes 64, 128 and 256
+    if (hd != 32 && hd != 64 && hd != 96 && hd != 128 && hd != 256) return ATTN_ERR_UNSUPPORTED;
+    if (decode_hd && dt != ATTN_F32 && hd != 64 && hd != 128 && hd != 256) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
 
@@ -122,12 +124,10 @@ Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, i
     return p;
 }
 
-// fp16/bf16 run on the tensor cores; fp32 stays on the CUDA-core kernels (no TF32,
-// no 16-bit P), which is what fp32 accuracy needs.
-bool use_tcgen05(attn_dtype dt, int hd) {
-    (void)hd;
-    return dt != ATTN_F32;
-}
+// fp16/bf16 at hd 64 / 128 run on the tensor cores; fp32 stays on the CUDA-core
+// kernels (no TF32, no 16-bit P), which is what fp32 accuracy needs, and so do
+// the head sizes without a tensor-core kernel (32, 96, 256: correct, not fast).
+bool use_tcgen05(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 64 || hd == 128); }
 
 // Decode split plan: a deterministic function of the shape.  Aim for about
 // eight waves of two resident CTAs on each of GB300's 152 SMs.
@@ -478,6 +478,16 @@ attn_status attn_bwd_ex(attn_dtype dt, const void* q, const void* k, const void*
                                key_mask, key_mask_bstride, bias, bias_sb, bias_sh, bias_sq, bias_sk, &p);
     if (st != ATTN_OK) return st;
     return bwd_launch(dt, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, p, stream, 7);
+}
+
+attn_status attn_rope(attn_dtype dt, void* x, int B, int T, int H, int hd, int pos, float theta, void* stream) {
+    if (dt != ATTN_F32 && dt != ATTN_F16 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || T < 0 || H <= 0 || pos < 0 || !(theta > 0.f) || !isfinite(theta)) return ATTN_ERR_INVALID_ARG;
+    if (hd < 4 || hd > 256 || hd % 4) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || T == 0) return ATTN_OK;
+    if (!x || !aligned16(x)) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * T > (long long)INT32_MAX * 8) return ATTN_ERR_UNSUPPORTED;
+    return counted(launch_rope(x, (int)dt, B, T, H, hd, pos, (double)theta, static_cast<cudaStream_t>(stream)), 1);
 }
 
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -41,4 +41,7 @@ cudaError_t decode_noalloc_scratch(float** out);
 
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned int timeout_us, cudaStream_t s);
 
+// rotate-half rotary embedding in place over [B][T][H*hd] (hd 8 .. 256, a multiple of 4)
+cudaError_t launch_rope(void* x, int dt, int B, int T, int H, int hd, int pos, double theta, cudaStream_t s);
+
 }  // namespace attn

@@ -394,13 +394,49 @@ cudaError_t preprocess_launch(const Params& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The same D pass for any head size: one warp per (b, i, h) row, lanes striding
+// over its hd elements.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_preprocess_any_kernel(Params P) {
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long rows = (long long)P.B * P.tq_pad * P.H;
+    if (row >= rows) return;  // whole warps leave together
+    const int h = (int)(row % P.H);
+    const long long bi = row / P.H;
+    const int i = (int)(bi % P.tq_pad), b = (int)(bi / P.tq_pad);
+    const Seq sq = seq_any(P, b);
+    float acc = 0.f;
+    if (i < sq.tq) {
+        const T* o = qrow<T>(P, P.o_in, sq, i, h);
+        const T* g = qrow<T>(P, P.dout, sq, i, h);
+        for (int d = lane; d < P.hd; d += 32) acc = fmaf(Elem<T>::to_f(o[d]), Elem<T>::to_f(g[d]), acc);
+    }
+    acc = warp_sum(acc);
+    if (lane != 0) return;
+    const long long srow = ((long long)b * P.H + h) * P.tq_pad + i;
+    if (i >= sq.tq) {
+        P.ndelta[srow] = 0.f;
+        P.nlse2[srow] = -INFINITY;
+        return;
+    }
+    P.ndelta[srow] = -acc;
+    const float l = P.lse_in[((long long)b * P.H + h) * P.Tq + i];
+    P.nlse2[srow] = l == -INFINITY ? -INFINITY : -l * 1.4426950408889634f;
+}
+
 template <typename T>
 cudaError_t preprocess_typed(const Params& p, cudaStream_t s) {
-    // lanes per row = hd * sizeof(T) / 16 (hd is 64 or 128)
+    // lanes per row = hd * sizeof(T) / 16 for hd 64 or 128; a warp per row otherwise
     const int lpr = p.hd * (int)sizeof(T) / 16;
-    if (lpr == 8) return preprocess_launch<T, 8>(p, s);
-    if (lpr == 16) return preprocess_launch<T, 16>(p, s);
-    return preprocess_launch<T, 32>(p, s);
+    if (p.hd == 64 || p.hd == 128) {
+        if (lpr == 8) return preprocess_launch<T, 8>(p, s);
+        if (lpr == 16) return preprocess_launch<T, 16>(p, s);
+        return preprocess_launch<T, 32>(p, s);
+    }
+    const long long threads = (long long)p.B * p.tq_pad * p.H * 32;
+    bwd_preprocess_any_kernel<T><<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 template <typename T, int HD>
@@ -432,15 +468,28 @@ cudaError_t bwd_typed(const Params& p, int phases, cudaStream_t s) {
 
 }  // namespace
 
+template <int HD>
+cudaError_t fwd_hd(const Params& p, int dt, cudaStream_t s) {
+    if (dt == 0) return fwd_typed<float, HD>(p, s);
+    if (dt == 1) return fwd_typed<__half, HD>(p, s);
+    return fwd_typed<__nv_bfloat16, HD>(p, s);
+}
+template <int HD>
+cudaError_t bwd_hd(const Params& p, int dt, int phases, cudaStream_t s) {
+    if (dt == 0) return bwd_typed<float, HD>(p, phases, s);
+    if (dt == 1) return bwd_typed<__half, HD>(p, phases, s);
+    return bwd_typed<__nv_bfloat16, HD>(p, phases, s);
+}
+
+// head sizes 32, 64, 96, 128, 256 (the caller has checked)
 cudaError_t launch_simt_fwd(const Params& p, int dt, cudaStream_t s) {
-    if (p.hd == 64) {
-        if (dt == 0) return fwd_typed<float, 64>(p, s);
-        if (dt == 1) return fwd_typed<__half, 64>(p, s);
-        return fwd_typed<__nv_bfloat16, 64>(p, s);
+    switch (p.hd) {
+        case 32: return fwd_hd<32>(p, dt, s);
+        case 64: return fwd_hd<64>(p, dt, s);
+        case 96: return fwd_hd<96>(p, dt, s);
+        case 128: return fwd_hd<128>(p, dt, s);
+        default: return fwd_hd<256>(p, dt, s);
     }
-    if (dt == 0) return fwd_typed<float, 128>(p, s);
-    if (dt == 1) return fwd_typed<__half, 128>(p, s);
-    return fwd_typed<__nv_bfloat16, 128>(p, s);
 }
 
 cudaError_t launch_bwd_preprocess(const Params& p, int dt, cudaStream_t s) {
@@ -450,14 +499,13 @@ cudaError_t launch_bwd_preprocess(const Params& p, int dt, cudaStream_t s) {
 }
 
 cudaError_t launch_simt_bwd(const Params& p, int dt, int phases, cudaStream_t s) {
-    if (p.hd == 64) {
-        if (dt == 0) return bwd_typed<float, 64>(p, phases, s);
-        if (dt == 1) return bwd_typed<__half, 64>(p, phases, s);
-        return bwd_typed<__nv_bfloat16, 64>(p, phases, s);
+    switch (p.hd) {
+        case 32: return bwd_hd<32>(p, dt, phases, s);
+        case 64: return bwd_hd<64>(p, dt, phases, s);
+        case 96: return bwd_hd<96>(p, dt, phases, s);
+        case 128: return bwd_hd<128>(p, dt, phases, s);
+        default: return bwd_hd<256>(p, dt, phases, s);
     }
-    if (dt == 0) return bwd_typed<float, 128>(p, phases, s);
-    if (dt == 1) return bwd_typed<__half, 128>(p, phases, s);
-    return bwd_typed<__nv_bfloat16, 128>(p, phases, s);
 }
 
 }  // namespace attn

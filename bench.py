@@ -530,6 +530,14 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
         tf = fl * wb.hd * pairs / (t[n] * 1e-3) / 1e12
         out["bias_prefill_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
                                     "visible_pairs": pairs, "note": "GQA causal prefill with a [1,1,T,T] fp32 bias"}
+    # rotary embedding of the GQA prefill q and k (HBM-bound: each element read and written once)
+    rq, rk = q.clone(), k.clone()
+    t = time_passes(torch, stream, [("rope", lambda: (A.attn_rope(rq, H=wb.H, pos=0), A.attn_rope(rk, H=wb.Hkv, pos=0)))],
+                    args, flush_buf)
+    nbytes = 2 * (rq.numel() + rk.numel()) * rq.element_size()
+    out["rope_qk"] = {"ms": t["rope"], "GB/s": nbytes / (t["rope"] * 1e-3) / 1e9,
+                      "frac_of_hbm_peak": nbytes / (t["rope"] * 1e-3) / 1e9 / peaks["hbm"], "bytes_per_call": nbytes,
+                      "note": "rotate-half RoPE of q [4,2048,32*128] and k [4,2048,8*128] bf16, in place (two launches)"}
     st, word = A.attn_get_device_status()
     if st != A.OK:
         raise RuntimeError("device status word %#x after the masked workloads" % word)

@@ -295,6 +295,21 @@ ATTN_API attn_status attn_decode_noalloc(attn_dtype dt, const void* q, const voi
                         float scale, int causal, int window, float softcap, int q_offset,
                         const float* key_mask, long long key_mask_bstride, void* stream);
 
+/*
+ * Rotate-half rotary embedding, in place, for the q or k given to the calls
+ * above (a separate HBM-bound pass: the attention kernels read the rotated rows).
+ * Source: ferrotensor engine/attention.rs, rope / rope_theta ("rotate-half RoPE
+ * (theta 10000) applied in place"; every head vector of token s gets position
+ * pos + s).
+ *   x     : [B, T, H*hd] of dtype dt, 16-byte aligned; overwritten.
+ *   pos   : position of token 0 of every sequence (>= 0).
+ *   theta : base frequency (10000 in the page's default, > 0).
+ *   Pair (x[i], x[i + hd/2]) of each head vector, i < hd/2, turns by
+ *   (pos + s) * theta^(-2i/hd).  hd a multiple of 4 in [4, 256].
+ */
+ATTN_API attn_status attn_rope(attn_dtype dt, void* x, int B, int T, int H, int hd, int pos, float theta,
+                        void* stream);
+
 /* Human-readable name of a status code (static storage). */
 ATTN_API const char* attn_status_string(attn_status s);
 

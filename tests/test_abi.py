@@ -47,8 +47,8 @@ def fwd(**kw):
 @pytest.mark.parametrize("kw,expect", [
     (dict(H=3, Hkv=2), A.ERR_INVALID_ARG),         # Hkv must divide H
     (dict(Hkv=0), A.ERR_INVALID_ARG),
-    (dict(hd=96), A.ERR_UNSUPPORTED),
-    (dict(hd=256), A.ERR_UNSUPPORTED),
+    (dict(hd=48), A.ERR_UNSUPPORTED),           # head sizes: 32, 64, 96, 128, 256
+    (dict(hd=512), A.ERR_UNSUPPORTED),
     (dict(scale=0.0), A.ERR_INVALID_ARG),
     (dict(scale=float("nan")), A.ERR_INVALID_ARG),
     (dict(softcap=-1.0), A.ERR_INVALID_ARG),
@@ -106,11 +106,14 @@ def test_decode_len_validation():
     st = L.attn_decode_len(0, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 128, 0.1, 1, 0, 0.0, BAD,
                            None, 0, None)
     assert st == A.ERR_UNSUPPORTED
-    # hd 256: decode only, 16-bit only
-    st = L.attn_decode(0, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 256, 0.1, 1, 0, 0.0, 252,
+    # the 16-bit split kernel takes hd 64, 128, 256 (96 runs only through attn_fwd)
+    st = L.attn_decode(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 96, 0.1, 1, 0, 0.0, 252,
                        None, 0, None)
     assert st == A.ERR_UNSUPPORTED
-    st = L.attn_fwd(2, BAD, BAD, BAD, BAD, None, 2, 4, 256, 8, 2, 256, 0.1, 1, 0, 0.0, 0, None, 0, None)
+    st = L.attn_decode(0, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 4, 256, 8, 2, 48, 0.1, 1, 0, 0.0, 252,
+                       None, 0, None)
+    assert st == A.ERR_UNSUPPORTED
+    st = L.attn_fwd(2, BAD, BAD, BAD, BAD, None, 2, 4, 256, 8, 2, 512, 0.1, 1, 0, 0.0, 0, None, 0, None)
     assert st == A.ERR_UNSUPPORTED
     # too long a query block
     st = L.attn_decode_len(2, BAD, BAD, BAD, BAD, None, BAD, 1 << 20, 2, 17, 256, 8, 2, 128, 0.1, 1, 0, 0.0, BAD,
@@ -139,7 +142,7 @@ def test_varlen_validation():
     st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, -1, 8, 2, 128, *tail)
     assert st == A.ERR_INVALID_ARG
     # head dim, GQA divisibility, softcap
-    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, 100, 8, 2, 96, *tail)
+    st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, 100, 8, 2, 48, *tail)
     assert st == A.ERR_UNSUPPORTED
     st = L.attn_varlen_fwd(2, BAD, BAD, BAD, BAD, None, BAD, BAD, 2, 64, 64, 100, 100, 8, 3, 128, *tail)
     assert st == A.ERR_INVALID_ARG
@@ -164,7 +167,7 @@ def test_ex_validation():
     assert L.attn_fwd_ex(*args, ctypes.c_void_p(0x1002), 0, 0, 64, 1, None) == A.ERR_INVALID_ARG
     assert L.attn_fwd_ex(*args, BAD, 0, 0, -64, 1, None) == A.ERR_INVALID_ARG
     # the usual shape rules
-    bad_hd = [2, BAD, BAD, BAD, BAD, None, 2, 64, 64, 8, 2, 96, 0.1, 10, 0, 0.0, 0, None, 0]
+    bad_hd = [2, BAD, BAD, BAD, BAD, None, 2, 64, 64, 8, 2, 48, 0.1, 10, 0, 0.0, 0, None, 0]
     assert L.attn_fwd_ex(*bad_hd, None, 0, 0, 0, 0, None) == A.ERR_UNSUPPORTED
     st = L.attn_bwd_ex(2, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, 16, 2, 64, 64, 8, 2, 128, 0.1, 10, 0,
                        0.0, 0, None, 0, None, 0, 0, 0, 0, None)

@@ -312,3 +312,28 @@ def test_guard_bands_untouched():
     A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), H=H, Hkv=1, causal=True, o=o)
     torch.cuda.synchronize()
     assert (big[:pad] == 9.0).all() and (big[pad + n:] == 9.0).all()
+
+
+# Head sizes without a tensor-core kernel run on the CUDA-core kernels (16-bit included).
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("hd", [32, 96, 256])
+def test_other_head_sizes_fwd_bwd(dt, hd):
+    assert A.attn_kernel_family({"bf16": "bfloat16", "f32": "float32"}[dt], hd) == 0
+    run_fwd_case(dt, 2, 150, 150, 4, 2, hd, causal=True, window=60, softcap=20.0, backward=True, seed=950 + hd)
+
+
+@pytest.mark.parametrize("hd", [32, 96, 256])
+def test_other_head_sizes_packed(hd):
+    from attention_attn_fwd_08_gb300 import synth
+
+    lens = [70, 0, 130, 1]
+    cu = torch.tensor([0] + [int(x) for x in np.cumsum(lens)], dtype=torch.int32, device="cuda")
+    tot = int(cu[-1])
+    q = synth.normal((tot, 2 * hd), 960 + hd, "bf16")
+    k = synth.normal((tot, hd), 961 + hd, "bf16")
+    v = synth.normal((tot, hd), 962 + hd, "bf16")
+    o, _ = A.attn_varlen_fwd(q.cuda(), k.cuda(), v.cuda(), cu, cu, 130, 130, H=2, Hkv=1, causal=True)
+    torch.cuda.synchronize()
+    ref, _ = oracle.varlen_fwd(f64(q), f64(k), f64(v), cu.tolist(), cu.tolist(), H=2, Hkv=1,
+                               scale=1.0 / math.sqrt(hd), causal=True)
+    assert np.abs(f64(o) - ref).max() <= 2e-2
