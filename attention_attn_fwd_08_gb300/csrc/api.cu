@@ -482,7 +482,8 @@ attn_status attn_bwd_ex(attn_dtype dt, const void* q, const void* k, const void*
 
 attn_status attn_rope(attn_dtype dt, void* x, int B, int T, int H, int hd, int pos, float theta, void* stream) {
     if (dt != ATTN_F32 && dt != ATTN_F16 && dt != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-    if (B < 0 || T < 0 || H <= 0 || pos < 0 || !(theta > 0.f) || !isfinite(theta)) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || T < 0 || H <= 0 || H > 65535 || pos < 0 || !(theta > 0.f) || !isfinite(theta))
+        return ATTN_ERR_INVALID_ARG;
     if (hd < 4 || hd > 256 || hd % 4) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || T == 0) return ATTN_OK;
     if (!x || !aligned16(x)) return ATTN_ERR_INVALID_ARG;

@@ -137,6 +137,15 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Params P,
             qp[r] = reinterpret_cast<const uint16_t*>(P.q) + ((long long)b * P.Tq + lq) * (long long)P.H * HD +
                     (long long)hq[r] * HD;
         }
+        // each row's visible keys [vlo, vhi) before the key mask (the window around its position)
+        int vlo[2], vhi[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            vlo[r] = P.wl >= 0 ? max(0, pos[r] - P.wl) : 0;
+            vhi[r] = P.wr >= 0 ? min(tk_b, pos[r] + P.wr + 1) : tk_b;
+            if (!rok[r]) vhi[r] = vlo[r];
+        }
+        const float* mrow = P.key_mask ? P.key_mask + (long long)b * P.mask_bstride : nullptr;
         uint32_t qa[HD / 16][4];
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Params P,
                     const int j = j0 + kb + nt * 8 + 2 * t + (e & 1);
                     float x = sc[nt][e] * P.scale;
                     if (P.softcap > 0.f) x = P.softcap * tanh_accurate(x / P.softcap);
-                    const bool vis = rok[r] && visible(P, b, pos[r], j, tk_b);
+                    const bool vis = j >= vlo[r] && j < vhi[r] && (!mrow || mrow[j] > 0.5f);
                     x = vis ? x * kLog2e : -INFINITY;
                     sc[nt][e] = x;
                     mx[r] = fmaxf(mx[r], x);

@@ -13,8 +13,8 @@ from helpers import f64
 
 pytestmark = pytest.mark.gpu
 
-# max-abs error allowed on N(0,1) inputs: rounding of the output dtype (fp32: accurate angle)
-TOL = {"f32": 2e-5, "f16": 2e-3, "bf16": 1.6e-2}
+# max-abs error allowed on N(0,1) inputs: rounding of the output dtype (16-bit also the fp32 angle)
+TOL = {"f32": 2e-5, "f16": 4e-3, "bf16": 2.5e-2}
 
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
