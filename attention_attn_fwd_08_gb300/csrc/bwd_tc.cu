@@ -66,8 +66,10 @@ struct KVCfg {
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
-// MODE 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with an
-// additive score bias.  Each instantiation carries only its own bookkeeping.
+// MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
+// an additive score bias; MODE & 4: softcap.  Each instantiation carries only its own
+// bookkeeping (the softcap's registers, live through the tile loop, made the plain
+// path spill when it was a run-time branch).
 template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV) {
     using C = KVCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BKV = C::BKV;
-    constexpr bool VL = MODE == 1, BIAS = MODE == 2;
+    constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -234,9 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = j0 + r;
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const bool key_live = j < sq.tk && (!P.key_mask || P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f);
-        const bool cap = P.softcap > 0.f;
+        constexpr bool cap = (MODE & 4) != 0;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
-        const CapPoly cp = cap_poly(P.scale, P.softcap);
         const uint64_t sl2_2 = f2_make(P.scale_log2, P.scale_log2), one2 = f2_make(1.f, 1.f);
         bool ok = true;
         for (int n = 0; n < ntiles; ++n) {
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < BQ; cc += 2)
                     amax = max3f(amax, fabsf(__uint_as_float(sv[cc >> 5][cc & 31])),
                                  fabsf(__uint_as_float(sv[cc >> 5][(cc & 31) + 1])));
-                poly = __all_sync(0xffffffffu, amax <= cp.r_max);
+                poly = __all_sync(0xffffffffu, amax <= cap_poly(P.scale, P.softcap).r_max);
             }
             // In a tile where some pair is invisible, those scores become -inf first, so
             // every tile runs one copy of the element loop (a rarely run second copy
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < BQ; ++cc)
                     sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi) ? sv[cc >> 5][cc & 31] : 0xff800000u;
-                poly = poly && cp.inf_ok;
+                poly = poly && cap_poly(P.scale, P.softcap).inf_ok;
             }
             // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate.
             // Pairs of columns go through the f32x2 unit together; the stats hold -LSE*log2e
@@ -325,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint64_t g = f2_make(s0, s1);
                         if constexpr (kMode == 1) {
                             uint64_t uu;
+                            const CapPoly cp = cap_poly(P.scale, P.softcap);
                             g = cap_g(cp, g, uu);
                             // 1 - tanh^2; a masked score gives g = -inf and -inf here, with P = 0
                             float d0, d1;
@@ -738,7 +740,6 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const bool cap = P.softcap > 0.f;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
-        const CapPoly cp = cap_poly(P.scale, P.softcap);
         const uint64_t sl2_2 = f2_make(P.scale_log2, P.scale_log2), one2 = f2_make(1.f, 1.f);
         bool ok = true;
         int gt = 0, act = 0, qc = 0;  // tiles, active items and Q/dO copies so far
@@ -838,7 +839,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 #pragma unroll
                     for (int cc = 0; cc < 32; cc += 2)
                         amax = max3f(amax, fabsf(__uint_as_float(sv[cc])), fabsf(__uint_as_float(sv[cc + 1])));
-                    poly = __all_sync(0xffffffffu, amax <= cp.r_max);
+                    poly = __all_sync(0xffffffffu, amax <= cap_poly(P.scale, P.softcap).r_max);
                 }
                 // invisible pairs become -inf scores first: one copy of the element loop
                 const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= 32;
@@ -846,7 +847,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc)
                         sv[cc] = (cc >= clo && cc < chi && ((mbits >> cc) & 1u)) ? sv[cc] : 0xff800000u;
-                    poly = poly && cp.inf_ok;
+                    poly = poly && cap_poly(P.scale, P.softcap).inf_ok;
                 }
                 // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate.
                 // Pairs of columns go through the f32x2 unit together.
@@ -868,6 +869,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                             uint64_t g = f2_make(s0, s1);
                             if constexpr (kMode == 1) {
                                 uint64_t uu;
+                                const CapPoly cp = cap_poly(P.scale, P.softcap);
                                 g = cap_g(cp, g, uu);
                                 // 1 - tanh^2; a masked score gives g = -inf and -inf here, with P = 0
                                 float d0, d1;
@@ -1004,8 +1006,10 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
-        auto k = p.cu_q ? bwd_dkdv_kernel<BF16, HD, 1>
-                        : p.bias ? bwd_dkdv_kernel<BF16, HD, 2> : bwd_dkdv_kernel<BF16, HD, 0>;
+        const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
+        auto k = p.cu_q ? (c ? bwd_dkdv_kernel<BF16, HD, 5> : bwd_dkdv_kernel<BF16, HD, 1>)
+                 : p.bias ? bwd_dkdv_kernel<BF16, HD, 2>
+                          : (c ? bwd_dkdv_kernel<BF16, HD, 4> : bwd_dkdv_kernel<BF16, HD, 0>);
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;

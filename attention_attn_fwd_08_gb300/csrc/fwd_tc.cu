@@ -60,12 +60,12 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, 
 //   warp 10    MMA issuer of tile B                                 (11 idle)
 // Registers: launched at 168 per thread (384 threads = 64512); the producer
 // warpgroup gives its share to the softmax warpgroups with setmaxnreg
-// (2*128*224 + 128*56 = 64512, never more than the launch total).
+// (2*128*216 + 128*72 = 64512, never more than the launch total).
 // TMEM: S_A 0, S_B 128, O_A 256, O_B 256+hd (512 columns).  Each tile has a
 // single S buffer; S_u(n) is issued after P_u(n-1) V(n-1), so a completed
 // S_u(n) also means O_u is stable for a rescale.
 constexpr int kThreads2 = 384;
-constexpr int kRegsSoftmax = 224, kRegsProducer = 56;
+constexpr int kRegsSoftmax = 216, kRegsProducer = 72;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= kThreads2 * 168, "register split exceeds launch");
 
 template <int HD>
@@ -129,13 +129,14 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
 }
 __device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * BM - 1) / (2 * BM) * P.H * P.B; }
 
-// MODE 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with an
-// additive score bias.  Each instantiation carries only its own bookkeeping.
+// MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
+// an additive score bias; MODE & 4: softcap.  Each instantiation carries only its own
+// bookkeeping.
 template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
-    constexpr bool VL = MODE == 1, BIAS = MODE == 2;
+    constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2;
     using C = Fwd2Cfg<HD>;
     constexpr int NS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
         const float sl2 = P.scale_log2;
         const uint64_t sl2_2 = f2_make(sl2, sl2);
-        const bool cap = P.softcap > 0.f;
+        constexpr bool cap = (MODE & 4) != 0;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         const float cap_out = P.softcap * kLog2e;
         auto wait_warp = [&](int bar, uint32_t parity) -> bool {
@@ -659,7 +660,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
 template <bool BF16, int HD>
 cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     using C = Fwd2Cfg<HD>;
-    auto kern = p.cu_q ? fwd_tc2_kernel<BF16, HD, 1> : p.bias ? fwd_tc2_kernel<BF16, HD, 2> : fwd_tc2_kernel<BF16, HD, 0>;
+    const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
+    auto kern = p.cu_q ? (c ? fwd_tc2_kernel<BF16, HD, 5> : fwd_tc2_kernel<BF16, HD, 1>)
+                : p.bias ? fwd_tc2_kernel<BF16, HD, 2>
+                         : (c ? fwd_tc2_kernel<BF16, HD, 4> : fwd_tc2_kernel<BF16, HD, 0>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
     if (e != cudaSuccess) return e;
     int dev = 0, nsm = 0;

@@ -116,3 +116,75 @@ def test_decode_full(name):
     gpu = run_gpu(w, inp)
     for b, kvh in ((0, 0), (7, 3), (15, 7)):
         sample_block(w, inp, gpu, b, kvh, 0, w.Tq, 0, w.Tk)
+
+
+def test_varlen_packed_fwd_bwd_full():
+    """The bench's packed batch (8 causal sequences of U{256..2048} rows): whole
+    shortest sequence and the tail of the longest, one KV group each."""
+    w = synth.WORKLOADS["varlen_packed"]
+    inp = synth.make_packed_inputs(w)
+    dev = "cuda"
+    cu = inp["cu"].to(device=dev, dtype=torch.int32)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    kw = dict(H=w.H, Hkv=w.Hkv, scale=w.scale, causal=True)
+    o, lse = A.attn_varlen_fwd(q, k, v, cu, cu, w.Tq, w.Tk, **kw)
+    dq, dk, dv = A.attn_varlen_bwd(q, k, v, o, do, lse, cu, cu, w.Tq, w.Tk, **kw)
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    assert st == A.OK, "device status word %#x" % word
+    G, hd = w.H // w.Hkv, w.hd
+    lens = [int(x) for x in inp["lengths"]]
+    cuh = [int(x) for x in inp["cu"]]
+    for b, kvh, tail in ((int(np.argmin(lens)), 5, None), (int(np.argmax(lens)), 2, 128)):
+        L, s0 = lens[b], cuh[b]
+        r0 = 0 if tail is None else L - tail
+        sl = lambda x, h0, h1: f64(x[s0:s0 + L, h0 * hd:h1 * hd])[None]
+        qs = sl(inp["q"], kvh * G, (kvh + 1) * G)[:, r0:]
+        ks, vs = sl(inp["k"], kvh, kvh + 1), sl(inp["v"], kvh, kvh + 1)
+        okw = dict(H=G, Hkv=1, scale=w.scale, causal=True, q_offset=r0)
+        o_ref, lse_ref = oracle.fwd(qs, ks, vs, **okw)
+        og = o[s0 + r0:s0 + L, kvh * G * hd:(kvh + 1) * G * hd][None]
+        lg = lse[b:b + 1, kvh * G:(kvh + 1) * G, r0:L]
+        what = "varlen b%d kvh%d rows[%d,%d)" % (b, kvh, r0, L)
+        compare_o_lse(og, lg, o_ref, lse_ref, w.dtype, what)
+        dos = sl(inp["do"], kvh * G, (kvh + 1) * G)[:, r0:]
+        gq, gk, gv = oracle.bwd(qs, ks, vs, dos, **okw)
+        # dK/dV of the last `tail` keys are seen only by the sampled rows
+        g0 = r0
+        compare_grads((dq[s0 + r0:s0 + L, kvh * G * hd:(kvh + 1) * G * hd][None],
+                       dk[s0 + g0:s0 + L, kvh * hd:(kvh + 1) * hd][None],
+                       dv[s0 + g0:s0 + L, kvh * hd:(kvh + 1) * hd][None]),
+                      (gq, gk[:, g0:], gv[:, g0:]), w.dtype, what)
+
+
+def test_bias_prefill_fwd_bwd_full():
+    """The bench's biased GQA prefill: causal (window_right 0) with a [1, 1, T, T] fp32 bias."""
+    w = synth.WORKLOADS["gqa_prefill"]
+    inp = synth.make_inputs(w)
+    bias = synth.normal((1, 1, w.Tq, w.Tk), w.seed + 5, "f32")
+    dev = "cuda"
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    kw = dict(H=w.H, Hkv=w.Hkv, scale=w.scale, window_left=-1, window_right=0)
+    o, lse = A.attn_fwd_ex(q, k, v, bias=bias.to(dev), **kw)
+    dq, dk, dv = A.attn_bwd_ex(q, k, v, o, do, lse, bias=bias.to(dev), **kw)
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    assert st == A.OK, "device status word %#x" % word
+    G, hd, T = w.H // w.Hkv, w.hd, w.Tq
+    for b, kvh, r0 in ((1, 3, T - 128), (3, 6, 0)):
+        r1 = r0 + 128
+        qs = f64(inp["q"][b:b + 1, r0:r1, kvh * G * hd:(kvh + 1) * G * hd])
+        ks = f64(inp["k"][b:b + 1, :r1, kvh * hd:(kvh + 1) * hd])
+        vs = f64(inp["v"][b:b + 1, :r1, kvh * hd:(kvh + 1) * hd])
+        bs = f64(bias[:, :, r0:r1, :r1])
+        okw = dict(H=G, Hkv=1, scale=w.scale, window_left=-1, window_right=0, q_offset=r0, bias=bs)
+        o_ref, lse_ref = oracle.fwd_ex(qs, ks, vs, **okw)
+        what = "bias b%d kvh%d rows[%d,%d)" % (b, kvh, r0, r1)
+        compare_o_lse(o[b:b + 1, r0:r1, kvh * G * hd:(kvh + 1) * G * hd], lse[b:b + 1, kvh * G:(kvh + 1) * G, r0:r1],
+                      o_ref, lse_ref, w.dtype, what)
+        if r1 == T:  # keys [T-128, T) are seen only by the sampled rows
+            dos = f64(inp["do"][b:b + 1, r0:r1, kvh * G * hd:(kvh + 1) * G * hd])
+            gq, gk, gv = oracle.bwd_ex(qs, ks, vs, dos, **okw)
+            compare_grads((dq[b:b + 1, r0:r1, kvh * G * hd:(kvh + 1) * G * hd], dk[b:b + 1, r0:r1, kvh * hd:(kvh + 1) * hd],
+                           dv[b:b + 1, r0:r1, kvh * hd:(kvh + 1) * hd]),
+                          (gq, gk[:, r0:r1], gv[:, r0:r1]), w.dtype, what)
