@@ -270,14 +270,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_pin(dp[0]);
             tmem_pin(dp[1]);
             if (BIAS && key_live) {  // additive score bias of (query i0 + cc, key j); never with softcap here
+                // rows past the last query read the last row (finite; those columns are masked
+                // below), so each half's 32 loads issue back to back without a branch
                 const float* col = P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh +
-                                   (long long)i0 * P.bias_sq + (long long)j * P.bias_sk;
+                                   (long long)j * P.bias_sk;
                 const float inv = 1.f / P.scale;
+                const int ilast = max(sq.tq - 1, 0);
 #pragma unroll
-                for (int cc = 0; cc < BQ; ++cc)
-                    if (i0 + cc < sq.tq)
-                        sv[cc >> 5][cc & 31] = __float_as_uint(
-                            fmaf(__ldg(col + (long long)cc * P.bias_sq), inv, __uint_as_float(sv[cc >> 5][cc & 31])));
+                for (int half = 0; half < 2; ++half) {
+                    float bv[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        bv[e] = __ldg(col + (long long)min(i0 + 32 * half + e, ilast) * P.bias_sq);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        sv[half][e] = __float_as_uint(fmaf(bv[e], inv, __uint_as_float(sv[half][e])));
+                }
             }
             uint32_t pk[32], dk[32];
             // With a softcap, the polynomial serves the tile unless a raw score of the
