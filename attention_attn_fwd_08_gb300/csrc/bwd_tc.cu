@@ -35,7 +35,11 @@ namespace attn {
 namespace {
 
 constexpr int kThreads = 192;    // dK/dV: 4 compute warps, producer, MMA
-constexpr int kThreadsDQ = 384;  // dQ: 8 compute warps, K/V producer, two MMA issuers, Q/dO/O producer
+constexpr int kThreadsDQ = 384;
+// dQ registers: the eight compute warps take 184, the producers and MMA issuers 136
+// (256*184 + 128*136 = 64512 = 384 threads at launch * 168)
+constexpr int kDqRegsCompute = 184, kDqRegsAux = 136;
+static_assert(256 * kDqRegsCompute + 128 * kDqRegsAux <= kThreadsDQ * 168, "register split exceeds launch");  // dQ: 8 compute warps, K/V producer, two MMA issuers, Q/dO/O producer
 constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM column (within a 64-column tile buffer) of K-step kk's 16-bit dS operand
@@ -561,6 +565,8 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     // every GEMM here then reads only K or V from shared memory
     const uint32_t tQ = tbase + 256 + HD, tG = tQ + HD / 2;
 
+    if (warp >= 8) {
+    regs_dec<kDqRegsAux>();
     if (warp == 11) {
         // ------------------------------- Q/dO/O producer and D (whole warp)
         // Loads the next item's tiles as soon as the current ones are in TMEM, then
@@ -740,7 +746,9 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         }
         if (elect_one()) mma_commit(BAR(MMA_DONE));
         mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
-    } else if (warp < 8) {
+    }
+    } else {
+        regs_inc<kDqRegsCompute>();
         // ------------------- compute: warps w and w+4 share rows (TMEM lane quarter
         // w % 4, one query row per thread) and split each tile's 64 key columns (hf)
         const int wq = warp & 3, hf = warp >> 2;
