@@ -87,7 +87,9 @@ typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
  *   B, Tq, Tk : batch, query rows, key rows (>= 0; B or Tq == 0 is a no-op,
  *               Tk == 0 writes O = 0, LSE = -inf).
  *   H, Hkv    : query / KV heads, Hkv >= 1 divides H.
- *   hd        : head dim, 64 or 128.
+ *   hd        : head dim 32, 64, 96, 128 or 256.  16-bit types at 64 and 128 run on
+ *               the tensor cores; fp32 and the other sizes on CUDA-core kernels
+ *               (same results, no tensor-core speed).
  *   scale     : > 0 and finite (1/sqrt(hd) in the usual case).
  *   causal    : 0/1.   window : >= 0, 0 = unbounded.   softcap : >= 0, 0 = off.
  *   q_offset  : >= 0, absolute position of query row 0.
@@ -154,8 +156,8 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv
  *   q, o      : [B][Lq][H*hd];  k, v : [B][Tk][Hkv*hd];  lse : [B][H][Lq] or NULL.
  *   workspace : device scratch of at least attn_decode_workspace_size() bytes,
  *               16-byte aligned.
- *   (H/Hkv)*Lq <= 64, hd 64, 128 or 256 (256: ATTN_BF16 / ATTN_F16 only); the
- *   rest as for attn_fwd.  The usual KV-cache call is causal with q_offset =
+ *   (H/Hkv)*Lq <= 64; 16-bit types take hd 64, 128 or 256 (the split kernel's
+ *   sizes), fp32 any attn_fwd head size; the rest as for attn_fwd.  The usual KV-cache call is causal with q_offset =
  *   Tk - Lq.
  */
 ATTN_API attn_status attn_decode(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
