@@ -54,7 +54,7 @@
  *    flash_attention.h: excluded positions "contribute nothing", a zero-length
  *    decode "writes zeros").  This is a reading; the pages do not define LSE there.
  *
- * The "_ex" entry points generalise two terms (the survey's next row on masks):
+ * The "_ex" entry points generalise two terms (every page's window, an additive mask):
  *
  *   vis    = (wl < 0 || j >= p - wl) && (wr < 0 || j <= p + wr) && (key mask)
  *   st_ij  = (softcap > 0 ? softcap * tanh(s_ij / softcap) : s_ij) + bias[b,h,i,j]
