@@ -403,8 +403,9 @@ def main():
     # ------------------------------------------------------ dominant kernel
     dom = max(("fwd", "dkdv", "dq"), key=lambda n: comps[n]["ms"])
     fam = A.attn_kernel_family("bfloat16", w.hd)
+    # the kernel's own source plus the shared device helpers it compiles with
     src = {"fwd": ("fwd_tc.cu",) if fam else ("simt.cu",), "dkdv": ("bwd_tc.cu",) if fam else ("simt.cu",),
-           "dq": ("bwd_tc.cu",) if fam else ("simt.cu",)}[dom]
+           "dq": ("bwd_tc.cu",) if fam else ("simt.cu",)}[dom] + ("common.cuh",)
     ach = comps[dom]["TFLOP/s"]
     roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s",
                 "frac": ach / peaks["bf16"], "traffic": traffic_for(dom, src_sha(*src)),
