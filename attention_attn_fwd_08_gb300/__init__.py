@@ -20,7 +20,7 @@ import math
 import os
 import threading
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_rope", "attn_bwd_workspace_size", "attn_decode_workspace_size",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_rope", "attn_bwd_workspace_size", "attn_decode_workspace_size", "attn_decode_plan",
            "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_launch_count", "AttnError", "lib",
            "library_path"]
 
@@ -66,6 +66,8 @@ def lib():
         L.attn_launch_count.restype = ctypes.c_ulonglong
         L.attn_decode_workspace_size.argtypes = [i, i, i, i, i, i]
         L.attn_decode_workspace_size.restype = sz
+        L.attn_decode_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+        L.attn_decode_plan.restype = i
         L.attn_decode.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + tail
         L.attn_decode.restype = i
         L.attn_decode_len.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + [i] * 6 + [f, i, i, f, vp, vp, ll, vp]
@@ -212,6 +214,13 @@ def attn_bwd(q, k, v, o, do, lse, *, H, Hkv, scale=None, causal=False, window=0,
 
 def attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd) -> int:
     return int(lib().attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd))
+
+
+def attn_decode_plan(B, Lq, Tk, H, Hkv):
+    """(splits, chunk): the decode calls' key split for this shape (host only)."""
+    splits, chunk = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().attn_decode_plan(B, Lq, Tk, H, Hkv, ctypes.byref(splits), ctypes.byref(chunk)), "attn_decode_plan")
+    return splits.value, chunk.value
 
 
 def attn_decode(q, k, v, *, H, Hkv, scale=None, causal=True, window=0, softcap=0.0, q_offset=None, key_mask=None,

@@ -493,6 +493,12 @@ attn_status attn_rope(attn_dtype dt, void* x, int B, int T, int H, int hd, int p
 
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+attn_status attn_decode_plan(int B, int Lq, int Tk, int H, int Hkv, int* splits, int* chunk) {
+    if (!splits || !chunk || B <= 0 || Lq <= 0 || Tk < 0 || H <= 0 || Hkv <= 0 || H % Hkv) return ATTN_ERR_INVALID_ARG;
+    decode_plan(B, Lq, Tk, H, Hkv, splits, chunk);
+    return ATTN_OK;
+}
+
 size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv, int hd) {
     if (B <= 0 || Lq <= 0 || Tk < 0 || H <= 0 || Hkv <= 0 || H % Hkv || (hd != 64 && hd != 128 && hd != 256)) return 0;
     int splits, chunk;

@@ -144,6 +144,19 @@ ATTN_API attn_status attn_bwd_phases(attn_dtype dt, const void* q, const void* k
 ATTN_API size_t attn_decode_workspace_size(int B, int Lq, int Tk, int H, int Hkv, int hd);
 
 /*
+ * The key split attn_decode, attn_decode_len (with Tk = the capacity) and
+ * attn_decode_noalloc use for a shape: the cache rows [0, Tk) fall into
+ * *splits chunks of *chunk rows (a multiple of 64; the last chunk may be
+ * shorter), one CTA per (b, KV head, 16 query rows of the group, chunk).  The
+ * split is a deterministic function of the shape (it changes only the
+ * rounding of the result: brotensor ops/flash_attention.h,
+ * flash_attention_decode_len).  Host only, no CUDA call.  Returns
+ * ATTN_ERR_INVALID_ARG (outputs untouched) when a pointer is NULL, B, Lq, H or
+ * Hkv is not positive, Tk is negative or Hkv does not divide H.
+ */
+ATTN_API attn_status attn_decode_plan(int B, int Lq, int Tk, int H, int Hkv, int* splits, int* chunk);
+
+/*
  * Split-KV decode: a block of Lq query rows (1 <= Lq <= 16) at positions
  * q_offset .. q_offset+Lq-1 over a KV cache of Tk rows.  Each (b, KV head,
  * key chunk) is one CTA that reads its K/V rows once for all (H/Hkv)*Lq query

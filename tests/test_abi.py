@@ -189,3 +189,43 @@ def test_workspace_sizes():
 def test_kernel_family_is_reported():
     assert A.attn_kernel_family("float32", 64) == 0
     assert A.attn_kernel_family("bfloat16", 128) in (0, 1)
+
+
+@pytest.mark.parametrize("B,Lq,Tk,H,Hkv", [
+    (16, 1, 32768, 32, 8), (16, 4, 32768, 32, 8),   # the long-cache decode shapes
+    (1, 1, 1, 1, 1), (1, 1, 63, 8, 8), (1, 1, 64, 8, 8), (1, 1, 65, 8, 8),
+    (2, 16, 4096, 32, 8), (64, 16, 100000, 64, 1), (1, 3, 1 << 20, 8, 2), (3, 2, 777, 6, 3),
+])
+def test_decode_plan_partitions_the_cache(B, Lq, Tk, H, Hkv):
+    """Host planning of the split-KV decode: the chunks tile [0, Tk) exactly, start on
+    64-row boundaries, leave none empty, and the workspace holds one partial per
+    (b, query head, row, chunk)."""
+    splits, chunk = A.attn_decode_plan(B, Lq, Tk, H, Hkv)
+    assert chunk > 0 and chunk % 64 == 0
+    assert splits >= 1
+    assert (splits - 1) * chunk < Tk <= splits * chunk  # every key in one chunk, the last chunk non-empty
+    assert A.attn_decode_plan(B, Lq, Tk, H, Hkv) == (splits, chunk)  # deterministic
+    for hd in (64, 128, 256):
+        assert A.attn_decode_workspace_size(B, Lq, Tk, H, Hkv, hd) == B * H * Lq * splits * (hd + 2) * 4
+
+
+def test_decode_plan_fills_the_gpu_on_long_caches():
+    """A long cache with few (b, KV head) groups is split until the grid covers the
+    152 SMs many times over; a large batch needs no split at all."""
+    for B, Hkv in ((1, 1), (1, 8), (16, 8)):
+        splits, chunk = A.attn_decode_plan(B, 1, 1 << 17, 8 * Hkv, Hkv)
+        assert B * Hkv * splits >= 4 * 152, (B, Hkv, splits)
+    splits, _ = A.attn_decode_plan(4096, 1, 1024, 32, 8)
+    assert splits == 1
+    # splitting stops at 64-row chunks
+    assert A.attn_decode_plan(1, 1, 640, 1, 1) == (10, 64)
+
+
+def test_decode_plan_validation():
+    L = A.lib()
+    one = ctypes.c_int(0)
+    assert L.attn_decode_plan(1, 1, 16, 8, 2, None, ctypes.byref(one)) == A.ERR_INVALID_ARG
+    for args in ((0, 1, 16, 8, 2), (1, 0, 16, 8, 2), (1, 1, -1, 8, 2), (1, 1, 16, 8, 3), (1, 1, 16, 0, 1)):
+        with pytest.raises(A.AttnError):
+            A.attn_decode_plan(*args)
+    assert A.attn_decode_plan(2, 1, 0, 8, 2)[0] == 1  # an empty cache: one (empty) chunk
