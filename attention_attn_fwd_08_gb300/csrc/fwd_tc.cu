@@ -33,6 +33,35 @@ struct TileInfo {
     int t0, ntiles;
 };
 
+// A shorter softcap polynomial for tiles whose scores all lie well inside the
+// fitted polynomial's range: tanh(y) = y * (1 + t * (kTanhS0 + kTanhS1 * t)),
+// t = y^2, for |y| <= kTanhShortY (weighted least squares on Chebyshev nodes for
+// the relative error of tanh, below 1e-8 there in exact arithmetic).  Two
+// fewer packed operations per pair of scores than the cubic R.  The leading
+// coefficient is positive, so a score of -inf still maps to -inf.
+constexpr float kTanhShortY = 0.125f;
+constexpr float kTanhS0 = -0.3333277106f, kTanhS1 = 0.1321673691f;
+struct CapShort {
+    uint64_t s0, s1;  // S(u) = c^2*kTanhS0 + c^4*kTanhS1*u, both halves equal (c = scale/softcap)
+    float r_max;      // the polynomial serves raw scores |r| <= r_max
+    bool inf_ok;      // -inf maps to -inf (c^4*kTanhS1 did not underflow)
+};
+__device__ __forceinline__ CapShort cap_short(float scale, float softcap) {
+    const float c = scale / fmaxf(softcap, 1e-30f), c2 = c * c;
+    const float k0 = c2 * kTanhS0, k1 = c2 * c2 * kTanhS1;
+    CapShort cs;
+    cs.s0 = f2_make(k0, k0);
+    cs.s1 = f2_make(k1, k1);
+    cs.r_max = fminf(kTanhShortY / c, 1e18f);
+    cs.inf_ok = k1 > 0.f;
+    return cs;
+}
+// g = r + r*u*S(u), u = r^2, of a pair of raw scores: tanh(c*r) = c*g
+__device__ __forceinline__ uint64_t cap_g_short(const CapShort& cs, uint64_t r) {
+    const uint64_t u = f2_mul(r, r);
+    return f2_fma(r, f2_mul(u, f2_fma(u, cs.s1, cs.s0)), r);
+}
+
 // key tiles the query tile at rows i0 .. of a sequence of tq queries and tk keys sees
 __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, int tk) {
     const int p0 = i0 + P.q_offset;
@@ -46,8 +75,9 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, 
 }
 
 // ------------------------------------------------------------------------
-// Persistent: one CTA per SM walks work items blockIdx.x, +gridDim.x, ...; an
-// item is two query tiles (256 rows of one head) sharing every K/V tile, with
+// Persistent: one CTA per SM walks work items in snake order (items c, 2g-1-c,
+// 2g+c, ... for CTA c of g), so that the heavy first items and the light last
+// ones even out across the CTAs; an item is two query tiles (256 rows of one head) sharing every K/V tile, with
 // one softmax warpgroup per tile, so the tensor core works on one tile's
 // P.V and next S while the other warpgroup runs its softmax (ping-pong).  The
 // K/V ring and every barrier phase run on across items: the next item's Q tile
@@ -88,9 +118,7 @@ struct Fwd2Cfg {
 
 // One work item: 256 query rows (tiles A and B) of one (batch, head), and the
 // key tiles each tile sees.  Items are numbered longest first: every head's last
-// (causally heaviest) query block comes before any head's next one.  With packed
-// sequences the items cover the longest sequence; a shorter one's surplus items
-// have no tiles.
+// (causally heaviest) query block comes before any head's next one.
 struct FwdItem {
     int b, h, kvh, i0;
     Seq sq;
@@ -99,17 +127,17 @@ struct FwdItem {
     int t0, ntiles;  // union key-tile range of the two tiles
 };
 
+// The item of query block cq (rows 256*cq ..) of head h in sequence b; an item
+// that is not valid has no rows.
 template <bool VL>
-__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
+__device__ __forceinline__ FwdItem make_item(const Params& P, int b, int h, int cq, bool valid) {
     FwdItem it;
-    const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
-    const int hb = w % (P.H * P.B);
-    const int cq = ncq - 1 - w / (P.H * P.B);
-    it.h = hb % P.H;
-    it.b = hb / P.H;
+    it.h = h;
+    it.b = b;
     it.kvh = it.h / P.G;
     it.i0 = cq * 2 * BM;
     it.sq = seq_of<VL>(P, it.b);
+    if (!valid) it.sq.tq = 0;
     it.hasB = it.i0 + BM < it.sq.tq;
     it.tu[0] = it.i0 < it.sq.tq ? tile_range(P, it.i0, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
     it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
@@ -128,6 +156,55 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w) {
     return it;
 }
 __device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * BM - 1) / (2 * BM) * P.H * P.B; }
+
+// Packed sequences, at most 32 of them (kVlCompact): only the query blocks that
+// hold rows of their own sequence become items, so no CTA is dealt empty items
+// in place of work.  Items run from the highest block index down (the heaviest
+// under a causal mask first); a level holds H items for every sequence that
+// reaches it, sequences in order, heads innermost.  Lane b of a warp reads
+// sequence b's block count, and a cursor walks the levels once per CTA, as the
+// CTA's item numbers only grow.  Every call is made by whole warps.  More
+// sequences keep the plain numbering (a sequence's surplus items have no rows).
+constexpr int kVlCompact = 32;
+struct VlCursor {
+    int level;      // the block index the cursor is at
+    int first;      // number of that level's first item
+    unsigned seqs;  // the sequences that reach that level
+};
+// query blocks of 2*BM rows of sequence b (0 past the batch)
+__device__ __forceinline__ int vl_blocks(const Params& P, int b) {
+    return b < P.B ? (seq_of<true>(P, b).tq + 2 * BM - 1) / (2 * BM) : 0;
+}
+__device__ __forceinline__ int vl_init(const Params& P, VlCursor& c, int lane) {
+    const int nb = vl_blocks(P, lane);
+    c.level = (int)__reduce_max_sync(0xffffffffu, (unsigned)nb) - 1;
+    c.first = 0;
+    c.seqs = __ballot_sync(0xffffffffu, nb > 0 && nb > c.level);
+    return (int)__reduce_add_sync(0xffffffffu, (unsigned)nb) * P.H;
+}
+// item w (not below any earlier call's w, and below the item count)
+__device__ __forceinline__ FwdItem vl_item(const Params& P, VlCursor& c, int w) {
+    while (w >= c.first + __popc(c.seqs) * P.H && c.level > 0) {
+        c.first += __popc(c.seqs) * P.H;
+        --c.level;
+        c.seqs = __ballot_sync(0xffffffffu, vl_blocks(P, threadIdx.x & 31) > c.level);
+    }
+    const int r = w - c.first, j = r / P.H;
+    unsigned m = c.seqs;
+    for (int t = 0; t < j && m; ++t) m &= m - 1;
+    const bool valid = r >= 0 && r < __popc(c.seqs) * P.H && m != 0u;
+    return make_item<true>(P, valid ? __ffs(m) - 1 : 0, valid ? r - j * P.H : 0, c.level, valid);
+}
+
+template <bool VL>
+__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c) {
+    if constexpr (VL) {
+        if (P.B <= kVlCompact) return vl_item(P, c, w);
+    }
+    const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
+    const int hb = w % (P.H * P.B);
+    return make_item<VL>(P, hb / P.H, hb % P.H, ncq - 1 - w / (P.H * P.B), true);
+}
 
 // MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
 // an additive score bias; MODE & 4: softcap.  Each instantiation carries only its own
@@ -164,7 +241,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
     __shared__ int done_count[2];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nitems = fwd_items(P);
+    VlCursor vcur = {};
+    int nitems = fwd_items(P);
+    if constexpr (VL) {
+        if (P.B <= kVlCompact) nitems = vl_init(P, vcur, lane);
+    }
     // every role walks the same item sequence; a tile u is active in an item when
     // it has rows and sees at least one key tile
     // (tile u is a run-time value: select, so that the item stays in registers)
@@ -205,8 +286,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
             bool ok = true;
             int gk = 0, gv = 0;   // K and V tiles loaded so far (ring positions)
             int qn[2] = {0, 0};   // Q tiles loaded so far, per tile slot
-            for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
-                const FwdItem it = fwd_item<VL>(P, w);
+            for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
+                const FwdItem it = fwd_item<VL>(P, w, vcur);
                 if (it.ntiles == 0) continue;
                 for (int u = 0; ok && u < 2; ++u) {
                     if (!active(it, u)) continue;
@@ -275,8 +356,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int g = 0;    // ring position of the item's first tile
             int pc = 0;   // P_FULL(u) phases consumed
             int act = 0;  // items in which this tile was active so far
-            for (int w = blockIdx.x; ok && w < nitems; w += gridDim.x) {
-                const FwdItem it = fwd_item<VL>(P, w);
+            for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
+                const FwdItem it = fwd_item<VL>(P, w, vcur);
                 if (it.ntiles == 0) continue;
                 const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
                 const bool on = active(it, u);
@@ -377,11 +458,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // [2^-2, 2^8] at the row max: a max above 2^8 (any tile), or a first tile whose
         // max is below 2^-2; then O is rescaled in TMEM first.  For ordinary inputs
         // this never happens.  The softcap takes the fitted tanh polynomial unless a
-        // raw score of the warp's rows lies outside its range (mode 2: tanh_accurate).
+        // raw score of the warp's rows lies outside its range (mode 2: tanh_accurate),
+        // and the shorter one when every raw score lies inside its range (mode 3).
         auto run_tile = [&](auto capc, float& m_used, float& l, int k, bool full, int clo, int chi,
                             const uint32_t(&mbits)[4], uint32_t(&sv)[4][32]) {
             constexpr bool kCap = decltype(capc)::value;
-            bool accurate = false;
+            bool accurate = false, shorter = false;
             if constexpr (kCap) {
                 // largest raw |score| of the row, before masking
                 float am[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
@@ -393,6 +475,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
                 const CapPoly cp = cap_poly(P.scale, P.softcap);
                 accurate = __any_sync(0xffffffffu, !(amax <= cp.r_max)) || (!full && !cp.inf_ok);
+                const CapShort cs = cap_short(P.scale, P.softcap);
+                shorter = !accurate && __all_sync(0xffffffffu, amax <= cs.r_max) && (full || cs.inf_ok);
             }
             if (!full) {
                 // visibility bits of columns 32c .. 32c+31: [clo, chi) and the key mask
@@ -430,6 +514,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         const CapPoly cp = cap_poly(P.scale, P.softcap);
                         uint64_t uu;
                         rr = cap_g(cp, rr, uu);
+                    } else if constexpr (kMode == 3) {
+                        rr = cap_g_short(cap_short(P.scale, P.softcap), rr);
                     }
                     return f2_fma(rr, sl2_2, nms);
                 }
@@ -439,6 +525,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const uint64_t r2 = f2_make(rmax, rmax), n2 = f2_make(-m_used, -m_used);
                 uint64_t x2;
                 if (!kCap) x2 = to_x(std::integral_constant<int, 0>(), r2, n2);
+                else if (shorter) x2 = to_x(std::integral_constant<int, 3>(), r2, n2);
                 else if (!accurate) x2 = to_x(std::integral_constant<int, 1>(), r2, n2);
                 else x2 = to_x(std::integral_constant<int, 2>(), r2, n2);
                 f2_split(x2, xm, xm_);
@@ -491,6 +578,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 l += (a0 + b0) + (a1 + b1);
             };
             if (!kCap) p_pass(std::integral_constant<int, 0>());
+            else if (shorter) p_pass(std::integral_constant<int, 3>());
             else if (!accurate) p_pass(std::integral_constant<int, 1>());
             else p_pass(std::integral_constant<int, 2>());
         };
@@ -502,8 +590,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // base[u] counts tile u's softmaxes in earlier items.
         const bool alternate = !cap && HD == 128;
         int base[2] = {0, 0};
-        for (int w = blockIdx.x; w < nitems; w += gridDim.x) {
-            const FwdItem it = fwd_item<VL>(P, w);
+        for (int kw = 0, w = snake_item(0); w < nitems; w = snake_item(++kw)) {
+            const FwdItem it = fwd_item<VL>(P, w, vcur);
             const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
             const int bA = base[0], bB = base[1];
             base[0] += nA;
@@ -669,7 +757,8 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    // persistent: one CTA per SM (one fits), each walks items blockIdx.x, +grid, ...
+    // persistent: one CTA per SM (one fits), each walks its items in snake order
+    // (packed sequences may have fewer items than this bound: those CTAs exit at once)
     const long long items = (long long)((p.Tq + 2 * BM - 1) / (2 * BM)) * p.H * p.B;
     const unsigned grid = (unsigned)(items < nsm ? items : nsm);
     kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v, m.o);

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import attention_attn_fwd_08_gb300 as A
-from helpers import f64, inputs, run_fwd_case
+from helpers import compare_o_lse, f64, inputs, run_fwd_case
 
 pytestmark = pytest.mark.gpu
 
@@ -102,6 +102,36 @@ def test_softcap_polynomial_and_fallback_mix(dt, hd):
     kernels' tanh polynomial (|q.k| * scale / softcap > 1/2), so within one call
     some warps' tiles take the exp-based tanh and the rest the polynomial."""
     run_fwd_case(dt, 2, 390, 390, 4, 2, hd, backward=True, causal=True, window=300, softcap=8.0, seed=320)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("hd", [64, 128])
+def test_softcap_three_tiers(dt, hd):
+    """The forward picks, per warp and key tile, the short tanh polynomial (every
+    |scale*q.k/softcap| <= 1/8), the cubic one (<= 1/2) or the exp-based tanh.
+    With softcap 30 about half the warps' tiles of N(0,1) data fit the short one,
+    and a few query rows scaled by 8 push their warps past the cubic's range: the
+    input check below confirms that one call meets all three."""
+    B, T, H, Hkv, cap = 1, 384, 2, 1, 30.0
+    q, k, v, _ = inputs(dt, B, T, T, H, Hkv, hd, seed=330)
+    q[:, 300:304] = (q[:, 300:304].float() * 8).to(q.dtype)
+    scale = 1.0 / math.sqrt(hd)
+    y = np.einsum("bihd,bjhd->bhij", f64(q).reshape(B, T, H, hd),
+                  np.repeat(f64(k).reshape(B, T, Hkv, hd), H // Hkv, axis=2)) * scale / cap
+    tiers = set()
+    for h in range(H):
+        for i0 in range(0, T, 32):             # one warp's 32 rows
+            for j0 in range(0, i0 + 32, 128):  # the key tiles of its 128-row query tile
+                a = np.abs(y[:, h, i0:i0 + 32, j0:j0 + 128]).max()
+                tiers.add(0 if a <= 0.125 else 1 if a <= 0.5 else 2)
+    assert tiers == {0, 1, 2}, tiers
+    kw = dict(H=H, Hkv=Hkv, scale=scale, causal=True, softcap=cap)
+    o, lse = A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), **kw)
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    assert st == A.OK, "device status word %#x" % word
+    o_ref, lse_ref = oracle.fwd(f64(q), f64(k), f64(v), **kw)
+    compare_o_lse(o, lse, o_ref, lse_ref, dt, "softcap tiers %s hd%d" % (dt, hd))
 
 
 @pytest.mark.parametrize("flags", BWD_FLAGS[:3], ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))

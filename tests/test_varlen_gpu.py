@@ -107,6 +107,16 @@ def test_varlen_many_items_per_cta():
     run_varlen("bf16", lens, lens, 16, 4, 128, seed=730, causal=True)
 
 
+def test_varlen_more_sequences_than_a_warp():
+    """Up to 32 sequences, the forward deals out only the query blocks that hold rows;
+    with more it numbers every sequence's blocks up to the longest (the surplus ones
+    empty).  Both numberings must cover every row exactly once."""
+    lens = [int(x) for x in np.random.default_rng(6).integers(0, 400, size=40)]
+    lens[7] = 600
+    run_varlen("bf16", lens, lens, 4, 2, 128, seed=735, backward=False, causal=True)
+    run_varlen("bf16", lens[:32], lens[:32], 4, 2, 128, seed=736, backward=False, causal=True)
+
+
 @pytest.mark.parametrize("hd", [64, 128])
 def test_varlen_fp32(hd):
     run_varlen("f32", [40, 0, 97, 1, 130], [40, 0, 97, 1, 130], 2, 1, hd, seed=740, causal=True, window=50)
