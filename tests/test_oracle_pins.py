@@ -190,6 +190,23 @@ def test_prefix_mask_equals_truncated_cache(oracle):
         assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+def test_mask_keeps_a_key_only_above_one_half(oracle):
+    """A key is valid iff its mask entry is > 0.5 (brotensor ops/flash_attention.h,
+    flash_attention_forward and _backward contracts): entries of exactly 0.5 drop the
+    key like 0 does, entries just above keep it like 1 does, bit for bit."""
+    B, Tq, Tk, H, hd = 2, 6, 10, 2, 8
+    q, k, v, do = problem(B, Tq, Tk, H, H, hd, seed=95)
+    soft = np.array([[0.5, 1.0, 0.5000001, 0.0, 0.75, 0.5, 2.0, 0.49, 1.0, 0.5]] * B)
+    hard = (soft > 0.5).astype(np.float64)
+    assert 0 < hard.sum() < soft.size
+    kw = dict(H=H, Hkv=H, scale=0.4, causal=False)
+    o1, l1 = oracle.fwd(q, k, v, key_mask=soft, **kw)
+    o2, l2 = oracle.fwd(q, k, v, key_mask=hard, **kw)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    for g1, g2 in zip(oracle.bwd(q, k, v, do, key_mask=soft, **kw), oracle.bwd(q, k, v, do, key_mask=hard, **kw)):
+        assert np.array_equal(g1, g2)
+
+
 def test_decode_rows_equal_prefill_tail(oracle):
     """Lq rows at q_offset = Tk - Lq equal the last Lq rows of causal prefill."""
     B, T, H, Hkv, hd = 2, 13, 4, 2, 8
