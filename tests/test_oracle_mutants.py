@@ -14,7 +14,8 @@ from concurrent.futures import ThreadPoolExecutor
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_ext_pins.py", "tests/test_oracle_varlen_pins.py"]
+PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_ext_pins.py", "tests/test_oracle_varlen_pins.py",
+        "tests/test_oracle_rope_pins.py"]
 
 C, PY = "attn_oracle.c", "__init__.py"
 WORKERS = min(8, os.cpu_count() or 2)
@@ -49,6 +50,9 @@ MUTANTS = [
     ("packed sequences read the first sequence's keys", PY,
      "ob, lb = fwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1]",
      "ob, lb = fwd(q[None, q0:q1], k[None, 0:k1 - k0], v[None, 0:k1 - k0]"),
+    ("rotary turn in the wrong direction", PY, "= a * c - b * sn", "= a * c + b * sn"),
+    ("rotary frequency exponent", PY, "(-2.0 * i / hd)", "(-1.0 * i / hd)"),
+    ("rotary position without the token index", PY, "p = float(pos + s)", "p = float(pos)"),
 ]
 
 
