@@ -163,12 +163,41 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def _placed(q, like_q=(), like_k=(), k=None, f32=(), device=()):
+    """Checks, before any pointer reaches the library, what it cannot check itself:
+    every tensor in like_q / like_k is on q's device with q's dtype and the shape of
+    q / k; every (name, tensor, shape) in f32 is an fp32 tensor of that shape on q's
+    device; every tensor in device is on q's device; and that device is a GPU (a host
+    pointer would reach the kernels as a device address).  Entries may be None."""
+    for group, ref in ((like_q, q), (like_k, k)):
+        for name, t in group:
+            if t is None:
+                continue
+            if t.device != q.device or t.dtype != q.dtype:
+                raise ValueError("%s must be a %s tensor on %s (got %s on %s)" % (name, q.dtype, q.device, t.dtype,
+                                                                                t.device))
+            if tuple(t.shape) != tuple(ref.shape):
+                raise ValueError("%s must have shape %s (got %s)" % (name, tuple(ref.shape), tuple(t.shape)))
+    for name, t, shape in f32:
+        if t is None:
+            continue
+        if t.device != q.device or t.dtype != _torch().float32 or tuple(t.shape) != tuple(shape):
+            raise ValueError("%s must be an fp32 tensor of shape %s on %s" % (name, tuple(shape), q.device))
+    for name, t in device:
+        if t is not None and t.device != q.device:
+            raise ValueError("%s must be on %s (got %s)" % (name, q.device, t.device))
+    if q.device.type != "cuda":
+        raise ValueError("the library takes CUDA tensors; q is on %s" % q.device)
+
+
 def attn_fwd(q, k, v, *, H, Hkv, scale=None, causal=False, window=0, softcap=0.0, q_offset=0, key_mask=None,
              o=None, lse=None, want_lse=True, stream=None):
     """Forward attention; returns (o, lse).  lse is None when want_lse is False."""
     torch = _torch()
     _contig(q, k, v, o, lse)
     B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o)], like_k=[("k", k), ("v", v)], k=k, f32=[("lse", lse, (B, H, Tq))],
+            device=[("key_mask", key_mask)])
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
     if o is None:
         o = torch.empty_like(q)
@@ -196,6 +225,8 @@ def attn_bwd(q, k, v, o, do, lse, *, H, Hkv, scale=None, causal=False, window=0,
     torch = _torch()
     _contig(q, k, v, o, do, lse, dq, dk, dv)
     B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o), ("do", do), ("dq", dq)], like_k=[("k", k), ("v", v), ("dk", dk), ("dv", dv)], k=k,
+            f32=[("lse", lse, (B, H, Tq))], device=[("key_mask", key_mask), ("workspace", workspace)])
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -229,6 +260,8 @@ def attn_decode(q, k, v, *, H, Hkv, scale=None, causal=True, window=0, softcap=0
     torch = _torch()
     _contig(q, k, v, o, lse)
     B, Lq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o)], like_k=[("k", k), ("v", v)], k=k, f32=[("lse", lse, (B, H, Lq))],
+            device=[("key_mask", key_mask), ("workspace", workspace)])
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
     q_offset = Tk - Lq if q_offset is None else q_offset
     if o is None:
@@ -257,6 +290,8 @@ def attn_decode_len(q, k, v, lengths, *, H, Hkv, scale=None, causal=True, window
     torch = _torch()
     _contig(q, k, v, o, lse, lengths)
     B, Lq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o)], like_k=[("k", k), ("v", v)], k=k, f32=[("lse", lse, (B, H, Lq))],
+            device=[("key_mask", key_mask), ("workspace", workspace), ("lengths", lengths)])
     if lengths.dtype != torch.int32 or lengths.numel() != B:
         raise ValueError("lengths must be int32 with one entry per batch")
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
@@ -298,6 +333,8 @@ def attn_fwd_ex(q, k, v, *, H, Hkv, scale=None, window_left=-1, window_right=-1,
     torch = _torch()
     _contig(q, k, v, o, lse)
     B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o)], like_k=[("k", k), ("v", v)], k=k, f32=[("lse", lse, (B, H, Tq))],
+            device=[("key_mask", key_mask), ("bias", bias)])
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
     if o is None:
         o = torch.empty_like(q)
@@ -318,6 +355,8 @@ def attn_bwd_ex(q, k, v, o, do, lse, *, H, Hkv, scale=None, window_left=-1, wind
     torch = _torch()
     _contig(q, k, v, o, do, lse, dq, dk, dv)
     B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o), ("do", do), ("dq", dq)], like_k=[("k", k), ("v", v), ("dk", dk), ("dv", dv)], k=k,
+            f32=[("lse", lse, (B, H, Tq))], device=[("key_mask", key_mask), ("bias", bias), ("workspace", workspace)])
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -339,6 +378,7 @@ def attn_rope(x, *, H, pos=0, theta=10000.0, stream=None):
     """Rotate-half rotary embedding of x [B, T, H*hd] in place (every head vector of
     token s at position pos + s); returns x."""
     _contig(x)
+    _placed(x)
     if x.dim() != 3 or x.shape[2] % H:
         raise ValueError("x must be [B, T, H*hd]")
     B, T, C = x.shape
@@ -370,6 +410,8 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqle
     torch = _torch()
     _contig(q, k, v, o, lse)
     batch, total_q, total_k, hd = _varlen_dims(q, k, cu_seqlens_q, cu_seqlens_k, H, Hkv)
+    _placed(q, like_q=[("o", o)], like_k=[("k", k), ("v", v)], k=k, f32=[("lse", lse, (batch, H, max_seqlen_q))],
+            device=[("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)])
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
     if o is None:
         o = torch.empty_like(q)
@@ -389,6 +431,9 @@ def attn_varlen_bwd(q, k, v, o, do, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_
     torch = _torch()
     _contig(q, k, v, o, do, lse, dq, dk, dv)
     batch, total_q, total_k, hd = _varlen_dims(q, k, cu_seqlens_q, cu_seqlens_k, H, Hkv)
+    _placed(q, like_q=[("o", o), ("do", do), ("dq", dq)], like_k=[("k", k), ("v", v), ("dk", dk), ("dv", dv)], k=k,
+            f32=[("lse", lse, (batch, H, max_seqlen_q))],
+            device=[("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k), ("workspace", workspace)])
     scale = 1.0 / math.sqrt(hd) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
