@@ -101,7 +101,9 @@ ATTN_API attn_status attn_fwd(attn_dtype dt, const void* q, const void* k, const
                      long long key_mask_bstride, void* stream);
 
 /* Bytes of scratch attn_bwd needs: -D = -rowsum(dO * O) and -LSE*log2(e), one
- * fp32 each per (b, h, i), rows padded to a multiple of 64 queries. */
+ * fp32 each per (b, h, i), rows padded to a multiple of 64 queries (D is forge
+ * attention.metal's attention_bwd_d_f32 quantity).  Host only; 0 for B, Tq or H
+ * below 1. */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Tq, int H);
 
 /*
@@ -126,6 +128,9 @@ ATTN_API attn_status attn_bwd(attn_dtype dt, const void* q, const void* k, const
 
 /*
  * The three passes of attn_bwd, selectable one at a time (same arguments).
+ * Source: ferrotensor engine/attention.rs, flash_attention_v2_backward_with (a
+ * dQ dispatch over query tiles and a dK/dV dispatch over key tiles); forge
+ * attention.metal, attention_bwd_d_f32 (the D pass).
  * phases is a bit set: 1 = D = rowsum(dO*O) and LSE*log2(e) into the
  * workspace (stored negated), 2 = dK/dV, 4 = dQ.  Pass 4 forms D and LSE*log2(e) itself and
  * leaves them in the workspace (so with 4 set, 1 is implied and, on the
@@ -272,6 +277,8 @@ ATTN_API attn_status attn_varlen_fwd(attn_dtype dt, const void* q, const void* k
 
 /*
  * Backward of attn_varlen_fwd (same arguments; o and lse from that call).
+ * Source: brotensor ops/flash_attention.h, flash_attention_varlen_backward
+ * (per-sequence recompute, gradients overwritten).
  * dq [total_q, H*hd], dk and dv [total_k, Hkv*hd] are overwritten on the rows
  * of every sequence (zero where nothing is visible); rows outside every
  * sequence are not written.  workspace: at least
@@ -286,7 +293,8 @@ ATTN_API attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k
                         void* stream);
 
 /*
- * attn_decode without a workspace argument, for callers that cannot call
+ * attn_decode without a workspace argument (the computation is brotensor
+ * ops/flash_attention.h, flash_attention_decode / _decode_len), for callers that cannot call
  * cudaMalloc and have no scratch buffer to pass in: for example a plugin that
  * is handed only its input and output buffers, a serving loop that forbids
  * device allocation after start-up so that a request can never fail for lack
