@@ -133,3 +133,29 @@ def test_bias_matches_torch_fp64_with_autograd(oracle, bshape, wl, wr, softcap):
     g = oracle.bwd_ex(q, k, v, do, window_left=wl, window_right=wr, bias=bias, **kw)
     for a, t in zip(g, (tq, tk, tv)):
         np.testing.assert_allclose(a, t.grad.numpy(), atol=1e-11)
+
+
+@pytest.mark.parametrize("wl,wr,softcap,q_offset", [(2, 1, 0.0, 0), (-1, 0, 1.3, 2), (3, -1, 0.9, 1)])
+def test_ex_gradients_match_finite_differences(oracle, wl, wr, softcap, q_offset):
+    """Central differences (h = 1e-6) of sum(O * dO) through fwd_ex, with a
+    broadcast bias holding a -inf entry, against bwd_ex."""
+    B, Tq, H, Hkv, hd = 1, 5, 2, 1, 4
+    Tk = Tq + q_offset
+    q, k, v, do = rnd((B, Tq, H * hd), 31), rnd((B, Tk, Hkv * hd), 32), rnd((B, Tk, Hkv * hd), 33), rnd((B, Tq, H * hd), 34)
+    bias = rnd((1, H, Tq, Tk), 35)
+    bias[0, 1, 3, 0] = -np.inf
+    kw = dict(H=H, Hkv=Hkv, scale=0.5, window_left=wl, window_right=wr, softcap=softcap, q_offset=q_offset, bias=bias)
+    loss = lambda q_, k_, v_: float((oracle.fwd_ex(q_, k_, v_, **kw)[0] * do).sum())
+    grads = oracle.bwd_ex(q, k, v, do, **kw)
+    h = 1e-6
+    for idx, x in enumerate((q, k, v)):
+        num = np.zeros_like(x)
+        for mi in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[mi] += h
+            xm[mi] -= h
+            ap, am = [q, k, v], [q, k, v]
+            ap[idx], am[idx] = xp, xm
+            num[mi] = (loss(*ap) - loss(*am)) / (2 * h)
+        err = np.linalg.norm(num - grads[idx]) / max(np.linalg.norm(num), 1e-30)
+        assert err <= 1e-6, (idx, err)
