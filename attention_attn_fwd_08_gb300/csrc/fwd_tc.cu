@@ -77,8 +77,9 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, 
 // ------------------------------------------------------------------------
 // Persistent: one CTA per SM walks work items in snake order (items c, 2g-1-c,
 // 2g+c, ... for CTA c of g), so that the heavy first items and the light last
-// ones even out across the CTAs; an item is two query tiles (256 rows of one head) sharing every K/V tile, with
-// one softmax warpgroup per tile, so the tensor core works on one tile's
+// ones even out across the CTAs.  An item is two query tiles (256 rows of one
+// head) sharing every K/V tile, with one softmax warpgroup per tile, so the
+// tensor core works on one tile's
 // P.V and next S while the other warpgroup runs its softmax (ping-pong).  The
 // K/V ring and every barrier phase run on across items: the next item's Q tile
 // loads once the current item's last S of that tile completed, and its first
