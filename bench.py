@@ -550,7 +550,13 @@ def components_round(c):
 
 
 def measure_e2e(A, w, inp, dev, stream, args, kw):
-    """Same step through the public API from pinned host buffers: H2D of q,k,v,dO, fwd, bwd, D2H of o,dq,dk,dv."""
+    """Same step through the public API from pinned host buffers: H2D of q,k,v,dO, fwd, bwd,
+    D2H of o,dq,dk,dv, every copy inside the timed region.  The copies that no later call
+    waits for run on a second stream under the kernels: dO's upload under the forward, O's
+    and dQ's downloads under the dK/dV pass (the backward is called as its two passes, dQ
+    then dK/dV, with one workspace).  Before timing, one overlapped step's downloads are
+    compared bit for bit with the serial order's (the kernels are deterministic); on a
+    mismatch or an error the serial order is timed instead, and `mode` says which ran."""
     import torch
 
     h_in = [inp[n].pin_memory() for n in ("q", "k", "v", "do")]
@@ -558,8 +564,9 @@ def measure_e2e(A, w, inp, dev, stream, args, kw):
     h_out = [torch.empty_like(inp[n]).pin_memory() for n in ("q", "q", "k", "v")]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
+    ws = torch.empty(A.attn_bwd_workspace_size(w.B, w.Tq, w.H), dtype=torch.uint8, device=dev)
 
-    def step():
+    def serial_step():
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
         q, k, v, do = d_in
@@ -567,6 +574,46 @@ def measure_e2e(A, w, inp, dev, stream, args, kw):
         dq, dk, dv = A.attn_bwd(q, k, v, o, do, lse, **kw)
         for h, d in zip(h_out, (o, dq, dk, dv)):
             h.copy_(d, non_blocking=True)
+
+    side = []  # the second stream, made inside the guarded block below
+
+    def overlapped_step():
+        main, s2 = torch.cuda.current_stream(), side[0]
+        q, k, v, do = d_in
+        s2.wait_stream(main)  # the previous step is done with dO and the host buffers
+        with torch.cuda.stream(s2):
+            do.copy_(h_in[3], non_blocking=True)
+        do_ready = s2.record_event()
+        for h, d in zip(h_in[:3], (q, k, v)):
+            d.copy_(h, non_blocking=True)
+        o, lse = A.attn_fwd(q, k, v, **kw)
+        main.wait_event(do_ready)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=4, **kw)
+        s2.wait_stream(main)  # O and dQ are final
+        with torch.cuda.stream(s2):
+            h_out[0].copy_(o, non_blocking=True)
+            h_out[1].copy_(dq, non_blocking=True)
+        A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, phases=2, **kw)
+        h_out[2].copy_(dk, non_blocking=True)
+        h_out[3].copy_(dv, non_blocking=True)
+        main.wait_stream(s2)  # the step ends when every download has landed
+
+    mode, step = "serial", serial_step
+    try:
+        side.append(torch.cuda.Stream(device=dev))
+        serial_step()
+        torch.cuda.synchronize()
+        want = [t.clone() for t in h_out]
+        for t in h_out:
+            t.zero_()
+        overlapped_step()
+        torch.cuda.synchronize()
+        if all(torch.equal(a, b) for a, b in zip(want, h_out)):
+            mode, step = "overlapped", overlapped_step
+    except Exception as e:  # keep the serial order; the bench line says so
+        mode = "serial (overlapped order failed: %s)" % type(e).__name__
+    torch.cuda.synchronize()
 
     for _ in range(args.warmup):
         step()
@@ -582,7 +629,7 @@ def measure_e2e(A, w, inp, dev, stream, args, kw):
     ms = statistics.mean(times)
     flops = 3.5 * FWD_FLOPS_PER_PAIR(w.hd) * visible_pairs(w)
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "mode": mode}
 
 
 if __name__ == "__main__":
