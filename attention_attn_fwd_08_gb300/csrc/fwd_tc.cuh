@@ -1,0 +1,813 @@
+// fwd_tc.cuh -- prefill forward on the 5th-generation tensor cores (sm_103a).
+//
+// Computes O = softmax(st) V and LSE for fp16/bf16 inputs with fp32
+// accumulation, hd 64 or 128, with causal / sliding-window / key-mask
+// visibility, softcap, GQA and a query offset.
+// Sources: vision_rs flash_attn2.rs, Forward (online-softmax recurrence,
+// logsumexp saved for the backward); brotensor ops/flash_attention.h,
+// flash_attention_decode (softcap before masking; window keys
+// [p-window+1, p]) and flash_attention_forward (key mask > 0.5 keeps a key,
+// fully masked key tiles are skipped); ferrotensor engine/attention.rs,
+// flash_attention_v2_with (128 query rows per workgroup, GQA).
+//
+// One kernel, fwd_tc2_kernel: two 128-row query tiles of one (b, h) per CTA
+// share every K/V tile; two softmax warpgroups alternate with the tensor core
+// (details at the kernel).  Key tiles outside every row's visible range are
+// never loaded; tiles that every row sees entirely skip the per-element mask.
+#include <math.h>
+
+#include <type_traits>
+
+#pragma once
+
+#include "kernels.h"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;      // query rows per tile (two tiles per CTA)
+constexpr int BN = 128;      // keys per tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleHi = 8.0f;   // log2 units: the row max may reach 2^8 times the reference
+constexpr float kRescaleLo = -2.0f;  // a row's first visible tile may put its max at >= 2^-2
+
+struct TileInfo {
+    int t0, ntiles;
+};
+
+// A shorter softcap polynomial for tiles whose scores all lie well inside the
+// fitted polynomial's range: tanh(y) = y * (1 + t * (kTanhS0 + kTanhS1 * t)),
+// t = y^2, for |y| <= kTanhShortY (weighted least squares on Chebyshev nodes for
+// the relative error of tanh, below 1e-8 there in exact arithmetic).  Two
+// fewer packed operations per pair of scores than the cubic R.  The leading
+// coefficient is positive, so a score of -inf still maps to -inf.
+constexpr float kTanhShortY = 0.125f;
+constexpr float kTanhS0 = -0.3333277106f, kTanhS1 = 0.1321673691f;
+struct CapShort {
+    uint64_t s0, s1;  // S(u) = c^2*kTanhS0 + c^4*kTanhS1*u, both halves equal (c = scale/softcap)
+    float r_max;      // the polynomial serves raw scores |r| <= r_max
+    bool inf_ok;      // -inf maps to -inf (c^4*kTanhS1 did not underflow)
+};
+__device__ __forceinline__ CapShort cap_short(float scale, float softcap) {
+    const float c = scale / fmaxf(softcap, 1e-30f), c2 = c * c;
+    const float k0 = c2 * kTanhS0, k1 = c2 * c2 * kTanhS1;
+    CapShort cs;
+    cs.s0 = f2_make(k0, k0);
+    cs.s1 = f2_make(k1, k1);
+    cs.r_max = fminf(kTanhShortY / c, 1e18f);
+    cs.inf_ok = k1 > 0.f;
+    return cs;
+}
+// g = r + r*u*S(u), u = r^2, of a pair of raw scores: tanh(c*r) = c*g
+__device__ __forceinline__ uint64_t cap_g_short(const CapShort& cs, uint64_t r) {
+    const uint64_t u = f2_mul(r, r);
+    return f2_fma(r, f2_mul(u, f2_fma(u, cs.s1, cs.s0)), r);
+}
+
+// key tiles the query tile at rows i0 .. of a sequence of tq queries and tk keys sees
+__device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, int tk) {
+    const int p0 = i0 + P.q_offset;
+    const int p1 = min(i0 + BM, tq) - 1 + P.q_offset;
+    int lo, hi;
+    key_range(P.wl, P.wr, tk, p0, p1, &lo, &hi);
+    TileInfo t;
+    t.t0 = lo / BN;
+    t.ntiles = hi > lo ? (hi + BN - 1) / BN - t.t0 : 0;
+    return t;
+}
+
+// ------------------------------------------------------------------------
+// Persistent: one CTA per SM walks work items in snake order (items c, 2g-1-c,
+// 2g+c, ... for CTA c of g), so that the heavy first items and the light last
+// ones even out across the CTAs.  An item is two query tiles (256 rows of one
+// head) sharing every K/V tile, with two softmax warpgroups per tile, so the
+// tensor core works on one tile's P.V and next S while the other tile's
+// softmax runs (ping-pong).  The K/V ring and every barrier phase run on across
+// items: the next item's Q tile loads once the current item's last S of that
+// tile completed, and its first P.V waits only for the epilogue to have read O
+// out of TMEM, so item boundaries cost little more than a ring step.
+//   warps 0-7   softmax: warp w owns TMEM lane quarter w % 4 (32 rows of each
+//               tile, one per thread) and key columns 64*(w/4) .. +63 of every
+//               score tile, and the same half of the O columns.  Each warp
+//               takes the tiles in the order A(n), B(n), A(n+1), ... so that the
+//               tensor core works on one tile while the warps run the other's
+//               softmax.  The two warps of a quarter exchange their rows' partial
+//               maxima once per tile (and partial sums once per tile per item)
+//               through shared memory, paced by an mbarrier of the pair.
+//   warp 8      TMA producer     warp 9  TMEM owner + MMA issuer of tile A
+//   warp 10     MMA issuer of tile B                                 (11 idle)
+// Splitting each row over two threads halves the chain of dependent work per
+// tile (TMEM load, row max, exponentials, P store) that the tensor core waits
+// for, and two warps per SM sub-partition issue it.
+// Registers: launched at 168 per thread (384 threads = 64512); the producer
+// warpgroup gives part of its share to the softmax warpgroups with setmaxnreg
+// (2*128*192 + 128*112 = 63488, within the launch total; at 200/96 and below
+// the producer and MMA warps spill, and the softmax's 64 scores per thread fit
+// 192 in every instantiation but packed sequences with a softcap).
+// TMEM: S_A 0, S_B 128, O_A 256, O_B 256+hd (512 columns).  Each tile has a
+// single S buffer; S_u(n) is issued after P_u(n-1) V(n-1), so a completed
+// S_u(n) also means O_u is stable for a rescale.  P_u (16-bit) is written over
+// the first 64 columns of S_u: the warp of key half 1 writes its P into columns
+// that held half 0's scores, which half 0 has read by the time the pair's
+// exchange of that tile completes.
+constexpr int kThreads2 = 384;
+constexpr int kRegsSoftmax = 192, kRegsProducer = 112;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= kThreads2 * 168, "register split exceeds launch");
+
+template <int HD>
+struct Fwd2Cfg {
+    static constexpr int kBoxes = HD / 64;
+    static constexpr int kStages = HD == 128 ? 2 : 3;
+    static constexpr int kQBytes = BM * HD * 2;
+    static constexpr int kKVBytes = BN * HD * 2;
+    static constexpr int kQOff = 0;  // Q_A, Q_B
+    static constexpr int kKOff = 2 * kQBytes;
+    static constexpr int kVOff = kKOff + kStages * kKVBytes;
+    static constexpr int kBarOff = kVOff + kStages * kKVBytes;
+    static constexpr int kNumBars = 17 + 4 * kStages;
+    // pair exchanges: [parity][key half][128 rows] fp32
+    static constexpr int kXOff = (kBarOff + kNumBars * 8 + 16 + 15) / 16 * 16;
+    static constexpr int kXBytes = 2 * 2 * 128 * 4;
+    static constexpr int kBytes = kXOff + kXBytes;
+    static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+// One work item: 256 query rows (tiles A and B) of one (batch, head), and the
+// key tiles each tile sees.  Items are numbered longest first: every head's last
+// (causally heaviest) query block comes before any head's next one.
+struct FwdItem {
+    int b, h, kvh, i0;
+    Seq sq;
+    bool hasB;
+    TileInfo tu[2];
+    int t0, ntiles;  // union key-tile range of the two tiles
+};
+
+// The item of query block cq (rows 256*cq ..) of head h in sequence b; an item
+// that is not valid has no rows.
+template <bool VL>
+__device__ __forceinline__ FwdItem make_item(const Params& P, int b, int h, int cq, bool valid) {
+    FwdItem it;
+    it.h = h;
+    it.b = b;
+    it.kvh = it.h / P.G;
+    it.i0 = cq * 2 * BM;
+    it.sq = seq_of<VL>(P, it.b);
+    if (!valid) it.sq.tq = 0;
+    it.hasB = it.i0 + BM < it.sq.tq;
+    it.tu[0] = it.i0 < it.sq.tq ? tile_range(P, it.i0, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
+    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
+    int t0 = it.tu[0].t0, t1 = it.tu[0].t0 + it.tu[0].ntiles;
+    if (it.tu[1].ntiles > 0) {
+        if (it.tu[0].ntiles == 0) {
+            t0 = it.tu[1].t0;
+            t1 = it.tu[1].t0 + it.tu[1].ntiles;
+        } else {
+            t0 = min(t0, it.tu[1].t0);
+            t1 = max(t1, it.tu[1].t0 + it.tu[1].ntiles);
+        }
+    }
+    it.t0 = t0;
+    it.ntiles = t1 > t0 ? t1 - t0 : 0;
+    return it;
+}
+__device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * BM - 1) / (2 * BM) * P.H * P.B; }
+
+// Packed sequences, at most 32 of them (kVlCompact): only the query blocks that
+// hold rows of their own sequence become items, so no CTA is dealt empty items
+// in place of work.  Items run from the highest block index down (the heaviest
+// under a causal mask first); a level holds H items for every sequence that
+// reaches it, sequences in order, heads innermost.  Lane b of a warp reads
+// sequence b's block count, and a cursor walks the levels once per CTA, as the
+// CTA's item numbers only grow.  Every call is made by whole warps.  More
+// sequences keep the plain numbering (a sequence's surplus items have no rows).
+constexpr int kVlCompact = 32;
+struct VlCursor {
+    int level;      // the block index the cursor is at
+    int first;      // number of that level's first item
+    unsigned seqs;  // the sequences that reach that level
+};
+// query blocks of 2*BM rows of sequence b (0 past the batch)
+__device__ __forceinline__ int vl_blocks(const Params& P, int b) {
+    return b < P.B ? (seq_of<true>(P, b).tq + 2 * BM - 1) / (2 * BM) : 0;
+}
+__device__ __forceinline__ int vl_init(const Params& P, VlCursor& c, int lane) {
+    const int nb = vl_blocks(P, lane);
+    c.level = (int)__reduce_max_sync(0xffffffffu, (unsigned)nb) - 1;
+    c.first = 0;
+    c.seqs = __ballot_sync(0xffffffffu, nb > 0 && nb > c.level);
+    return (int)__reduce_add_sync(0xffffffffu, (unsigned)nb) * P.H;
+}
+// item w (not below any earlier call's w, and below the item count)
+__device__ __forceinline__ FwdItem vl_item(const Params& P, VlCursor& c, int w) {
+    while (w >= c.first + __popc(c.seqs) * P.H && c.level > 0) {
+        c.first += __popc(c.seqs) * P.H;
+        --c.level;
+        c.seqs = __ballot_sync(0xffffffffu, vl_blocks(P, threadIdx.x & 31) > c.level);
+    }
+    const int r = w - c.first, j = r / P.H;
+    unsigned m = c.seqs;
+    for (int t = 0; t < j && m; ++t) m &= m - 1;
+    const bool valid = r >= 0 && r < __popc(c.seqs) * P.H && m != 0u;
+    return make_item<true>(P, valid ? __ffs(m) - 1 : 0, valid ? r - j * P.H : 0, c.level, valid);
+}
+
+template <bool VL>
+__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c) {
+    if constexpr (VL) {
+        if (P.B <= kVlCompact) return vl_item(P, c, w);
+    }
+    const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
+    const int hb = w % (P.H * P.B);
+    return make_item<VL>(P, hb / P.H, hb % P.H, ncq - 1 - w / (P.H * P.B), true);
+}
+
+// MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
+// an additive score bias; MODE & 4: softcap; MODE & 8: a head size below HD (96 in a
+// 128 kernel, 32 in a 64 kernel) read and written through 4-D maps whose boxes reach
+// past the head (the extra columns load as zeros, add nothing to q.k or P.V, and are
+// never stored).  Each instantiation carries only its own bookkeeping.
+template <bool BF16, int HD, int MODE>
+__global__ void __launch_bounds__(kThreads2, 1)
+    fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV) {
+    constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
+    static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
+    using C = Fwd2Cfg<HD>;
+    constexpr int NS = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    __shared__ int abort_flag;
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    auto Q_FULL = [&](int u) { return u; };
+    auto Q_EMPTY = [&](int u) { return 2 + u; };  // the item's last S of tile u completed
+    auto K_FULL = [&](int s) { return 4 + s; };
+    auto K_EMPTY = [&](int s) { return 4 + NS + s; };
+    auto V_FULL = [&](int s) { return 4 + 2 * NS + s; };
+    auto V_EMPTY = [&](int s) { return 4 + 3 * NS + s; };
+    auto S_FULL = [&](int u) { return 4 + 4 * NS + u; };
+    auto P_FULL = [&](int u) { return 6 + 4 * NS + u; };
+    auto O_DONE = [&](int u) { return 8 + 4 * NS + u; };   // the item's last P.V of tile u completed
+    auto O_EMPTY = [&](int u) { return 10 + 4 * NS + u; };  // the epilogue has read O_u out of TMEM
+    const int MMA_DONE = 12 + 4 * NS;
+    // the two softmax warps of lane quarter q: one exchange per phase
+    auto XCH = [&](int q) { return 13 + 4 * NS + q; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    VlCursor vcur = {};
+    int nitems = fwd_items(P);
+    if constexpr (VL) {
+        if (P.B <= kVlCompact) nitems = vl_init(P, vcur, lane);
+    }
+    // every role walks the same item sequence; a tile u is active in an item when
+    // it has rows and sees at least one key tile
+    // (tile u is a run-time value: select, so that the item stays in registers)
+    auto active = [&](const FwdItem& it, int u) { return (u == 0 ? it.tu[0].ntiles : it.tu[1].ntiles) > 0; };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) {
+            uint32_t count = 1;
+            // one arrival per softmax warp of the tile
+            if (i == P_FULL(0) || i == P_FULL(1) || i == O_EMPTY(0) || i == O_EMPTY(1)) count = 8;
+            for (int q = 0; q < 4; ++q)
+                if (i == XCH(q)) count = 2;
+            // stage releases and the teardown barrier: one arrival per MMA issuer
+            for (int s2 = 0; s2 < NS; ++s2)
+                if (i == K_EMPTY(s2) || i == V_EMPTY(s2)) count = 2;
+            if (i == MMA_DONE) count = 2;
+            mbar_init(BAR(i), count);
+        }
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    if (warp >= 8) {
+        regs_dec<kRegsProducer>();
+        // The producer and the MMA issuers run their loops as whole warps and issue
+        // each TMA copy, MMA and commit from one elected lane.
+        if (warp == 8) {
+            if (elect_one()) {
+                prefetch_tmap(&tmQ);
+                prefetch_tmap(&tmK);
+                prefetch_tmap(&tmV);
+            }
+            bool ok = true;
+            int gk = 0, gv = 0;   // K and V tiles loaded so far (ring positions)
+            int qn[2] = {0, 0};   // Q tiles loaded so far, per tile slot
+            for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
+                const FwdItem it = fwd_item<VL>(P, w, vcur);
+                if (it.ntiles == 0) continue;
+                for (int u = 0; ok && u < 2; ++u) {
+                    if (!active(it, u)) continue;
+                    // the slot is free once the previous item's last S of this tile completed
+                    if (qn[u] > 0 && !warp_wait(BAR(Q_EMPTY(u)), (qn[u] - 1) & 1, P.status, ST_FWD_PRODUCER,
+                                                &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) mbar_expect_tx(BAR(Q_FULL(u)), C::kQBytes);
+#pragma unroll
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        if (elect_one())
+                            tile_load<PADH, HD>(sbase + C::kQOff + u * C::kQBytes + bx * (BM * 128), &tmQ,
+                                                BAR(Q_FULL(u)), it.h, bx, it.sq.q0 + it.i0 + u * BM, it.sq.zb);
+                    ++qn[u];
+                }
+                for (int n = 0; ok && n < it.ntiles; ++n) {
+                    const int s = gk % NS, use = gk / NS;
+                    const int j0 = (it.t0 + n) * BN;
+                    if (use > 0 && !warp_wait(BAR(K_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) mbar_expect_tx(BAR(K_FULL(s)), C::kKVBytes);
+#pragma unroll
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        if (elect_one())
+                            tile_load<PADH, HD>(sbase + C::kKOff + s * C::kKVBytes + bx * (BN * 128), &tmK,
+                                                BAR(K_FULL(s)), it.kvh, bx, it.sq.k0 + j0, it.sq.zb);
+                    ++gk;
+                    if (use > 0 && !warp_wait(BAR(V_EMPTY(s)), (use - 1) & 1, P.status, ST_FWD_PRODUCER, &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) mbar_expect_tx(BAR(V_FULL(s)), C::kKVBytes);
+#pragma unroll
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        if (elect_one())
+                            tile_load<PADH, HD>(sbase + C::kVOff + s * C::kKVBytes + bx * (BN * 128), &tmV,
+                                                BAR(V_FULL(s)), it.kvh, bx, it.sq.k0 + j0, it.sq.zb);
+                    ++gv;
+                }
+            }
+            // every copy in flight lands before the CTA exits
+            for (int u = 0; u < 2; ++u)
+                if (qn[u] > 0) mbar_wait(BAR(Q_FULL(u)), (qn[u] - 1) & 1, P.status, ST_TEARDOWN, nullptr);
+            for (int n = max(0, gk - NS); n < gk; ++n)
+                mbar_wait(BAR(K_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
+            for (int n = max(0, gv - NS); n < gv; ++n)
+                mbar_wait(BAR(V_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
+        } else if (warp == 9 || warp == 10) {
+            // Two MMA issuers, one per query tile (warp 9: A, warp 10: B), so that one
+            // tile's barrier waits overlap the other tile's MMA issue.  Each runs its own
+            // in-order chain over the same items; both commit the K/V stage releases of
+            // every tile (those barriers count one arrival per issuer).
+            const int u = warp - 9;
+            constexpr uint32_t idS = idesc_f16(BF16, BM, BN, false, false);
+            constexpr uint32_t idPV = idesc_f16(BF16, BM, HD, false, true);
+            auto wait_all = [&](int bar, uint32_t parity) -> bool {
+                return warp_wait(BAR(bar), parity, P.status, ST_FWD_MMA, &abort_flag);
+            };
+            const uint64_t qdesc = sdesc_sw128(sbase + C::kQOff + u * C::kQBytes, 16, 1024);
+            const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
+            bool ok = true;
+            int g = 0;    // ring position of the item's first tile
+            int pc = 0;   // P_FULL(u) phases consumed
+            int act = 0;  // items in which this tile was active so far
+            for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
+                const FwdItem it = fwd_item<VL>(P, w, vcur);
+                if (it.ntiles == 0) continue;
+                const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
+                const bool on = active(it, u);
+                auto has = [&](int n) { return it.t0 + n >= my.t0 && it.t0 + n < my.t0 + my.ntiles; };
+                auto last_of_u = [&](int n) { return it.t0 + n == my.t0 + my.ntiles - 1; };
+                // S(n) = Q_u K(n)^T into S_u; the item's last S also frees the Q slot
+                auto issue_s = [&](int n) {
+                    const int gs = (g + n) % NS;
+                    const uint64_t kdesc = sdesc_sw128(sbase + C::kKOff + gs * C::kKVBytes, 16, 1024);
+                    // descriptor + (byte offset >> 4) moves the start address (no carry below 256 KB)
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t off_q = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+                        const uint32_t off_k = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
+                        if (elect_one()) mma_ss(tS, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
+                    }
+                    if (elect_one()) mma_commit(BAR(S_FULL(u)));
+                    if (last_of_u(n) && elect_one()) mma_commit(BAR(Q_EMPTY(u)));
+                };
+                // O_u (+)= P_u V(n); the item's last one signals the epilogue
+                auto issue_pv = [&](int n, int k) {
+                    const int vs = (g + n) % NS;
+                    const uint64_t vdesc = sdesc_sw128(sbase + C::kVOff + vs * C::kKVBytes, BN * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        if (elect_one())
+                            mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
+                                   (k > 0 || kk > 0) ? 1u : 0u);
+                    if (k == my.ntiles - 1 && elect_one()) mma_commit(BAR(O_DONE(u)));
+                };
+                // Each step first waits for V(n) and K(n+1) (normally long resident), so
+                // that once P(n) arrives PV(n) and S(n+1) issue back to back.  The stage
+                // releases count arrivals, not issuers: a chain commits a tile's release
+                // only after it has waited for that tile's data phase (also for tiles it
+                // skips), so an arrival can never belong to a later use of the stage.
+                if (on && !wait_all(Q_FULL(u), act & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!wait_all(K_FULL(g % NS), (g / NS) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (has(0)) issue_s(0);
+                if (elect_one()) mma_commit(BAR(K_EMPTY(g % NS)));
+                for (int n = 0; ok && n < it.ntiles; ++n) {
+                    const int gn = g + n;
+                    ok = wait_all(V_FULL(gn % NS), (gn / NS) & 1);
+                    if (ok && n + 1 < it.ntiles) ok = wait_all(K_FULL((gn + 1) % NS), ((gn + 1) / NS) & 1);
+                    const int k = it.t0 + n - my.t0;  // index of tile n in u's own sequence
+                    if (ok && has(n)) {
+                        ok = wait_all(P_FULL(u), pc & 1);
+                        ++pc;
+                        // the first P.V overwrites O_u: the previous item's epilogue must have read it
+                        if (ok && k == 0 && act > 0) ok = wait_all(O_EMPTY(u), (act - 1) & 1);
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (has(n)) issue_pv(n, k);
+                    if (n + 1 < it.ntiles && has(n + 1)) issue_s(n + 1);
+                    if (elect_one()) mma_commit(BAR(V_EMPTY(gn % NS)));
+                    if (n + 1 < it.ntiles && elect_one()) mma_commit(BAR(K_EMPTY((gn + 1) % NS)));
+                }
+                g += it.ntiles;
+                if (on) ++act;
+            }
+            if (elect_one()) mma_commit(BAR(MMA_DONE));
+            mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
+        }  // warp 11 only fills the producer warpgroup
+    } else {
+        regs_inc<kRegsSoftmax>();
+        // ------------- softmax + epilogue of both tiles, lane quarter wq, key half hf
+        const int hf = warp >> 2, wq = warp & 3;
+        const int r = wq * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        constexpr int kOC = HD / 2;  // O columns of this thread's half
+        const float sl2 = P.scale_log2;
+        const uint64_t sl2_2 = f2_make(sl2, sl2);
+        constexpr bool cap = (MODE & 4) != 0;
+        const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
+        const float cap_out = P.softcap * kLog2e;
+        float* xbuf = reinterpret_cast<float*>(smem + C::kXOff);
+        auto wait_warp = [&](int bar, uint32_t parity) -> bool {
+            const bool rr = mbar_wait(BAR(bar), parity, P.status, ST_FWD_SOFTMAX, &abort_flag);
+            return __all_sync(0xffffffffu, rr);
+        };
+        bool ok = true;
+        int scA = 0, scB = 0;    // S_FULL phases consumed, per tile
+        int actA = 0, actB = 0;  // items in which the tile was active so far (O_DONE phases)
+        int xc = 0;              // exchanges with the other half's warp so far
+        // The other half's value of this thread's row: each warp of the pair writes its
+        // value into the slot of the exchange's parity, arrives on the pair's barrier and
+        // waits for the partner's arrival.  A slot is written again two exchanges later,
+        // by which time the partner has read it (it arrived at the exchange in between
+        // only after reading).  A wait that runs out clears ok (and the partner's next
+        // wait ends on the abort flag), so neither warp can be left waiting.
+        // The fences order this warp's completed TMEM reads of the tile before the
+        // partner's P stores into the same columns, which follow the exchange.
+        auto exchange = [&](float v) -> float {
+            xbuf[((xc & 1) * 2 + hf) * 128 + r] = v;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(XCH(wq)));
+            ok = wait_warp(XCH(wq), xc & 1) && ok;
+            tc_fence_after();
+            const float o = xbuf[((xc & 1) * 2 + (hf ^ 1)) * 128 + r];
+            ++xc;
+            return o;
+        };
+        // One tile's softmax for this thread's 64 columns of tile u.  The 64 scores come
+        // out of TMEM into registers in one go (two loads in flight), so P can be written
+        // over S chunk by chunk as it is formed.  Pass 1 takes the row max (after the
+        // invisible scores are set to -inf, in tiles that some row does not see whole)
+        // and combines it with the other half's; pass 2 forms P = exp2(x) with
+        // x = s*scale*log2(e) - m, or with the capped score
+        // softcap*tanh(s*scale/softcap)*log2(e) in place of s*scale*log2(e), pairs of
+        // scores through the f32x2 unit together.
+        //   The reference m (log2 units, starting at 0) moves only when P would leave
+        // [2^-2, 2^8] at the row max: a max above 2^8 (any tile), or a first visible
+        // tile whose max is below 2^-2; then O is rescaled in TMEM first (each thread
+        // its half of the columns).  For ordinary inputs this never happens.  Both
+        // threads of a row take these decisions from the same combined max (x of it
+        // through the accurate tanh), so their references stay equal.  The softcap
+        // takes the fitted tanh polynomial unless a raw score of the warp's rows and
+        // columns lies outside its range (mode 2: tanh_accurate), and the shorter one
+        // when every raw score lies inside its range (mode 3).
+        auto run_tile = [&](auto capc, int u, float& m_used, float& l, bool& seen, int k, bool full, int clo,
+                            int chi, const uint32_t(&mbits)[2], uint32_t(&sv)[2][32]) {
+            constexpr bool kCap = decltype(capc)::value;
+            const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
+            bool accurate = false, shorter = false;
+            if constexpr (kCap) {
+                // largest raw |score| of the row's 64 columns, before masking
+                float am[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const int t = 2 * c + ((e >> 2) & 1);
+                        am[t] = max3f(am[t], fabsf(__uint_as_float(sv[c][e])), fabsf(__uint_as_float(sv[c][e + 1])));
+                        am[t] = max3f(am[t], fabsf(__uint_as_float(sv[c][e + 2])), fabsf(__uint_as_float(sv[c][e + 3])));
+                    }
+                const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+                const CapPoly cp = cap_poly(P.scale, P.softcap);
+                accurate = __any_sync(0xffffffffu, !(amax <= cp.r_max)) || (!full && !cp.inf_ok);
+                const CapShort cs = cap_short(P.scale, P.softcap);
+                shorter = !accurate && __all_sync(0xffffffffu, amax <= cs.r_max) && (full || cs.inf_ok);
+            }
+            if (!full) {
+                // visibility bits of tile columns 64*hf + 32c .. +31: [clo, chi) and the key mask
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int cg = 64 * hf + 32 * c;
+                    const int lo = min(max(clo - cg, 0), 32), hi = min(max(chi - cg, 0), 32);
+                    const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+                    const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
+                    const uint32_t vw = below_hi & ~below_lo & mbits[c];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sv[c][e] = ((vw >> e) & 1u) ? sv[c][e] : 0xff800000u;  // -inf
+                }
+            }
+            // pass 1: the row max of this half's scores, then of the whole row
+            float rm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const int t = 2 * c + ((e >> 2) & 1);
+                    rm[t] = max3f(rm[t], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+                    rm[t] = max3f(rm[t], __uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3]));
+                }
+            float rmax = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
+            rmax = fmaxf(rmax, exchange(rmax));
+            // x is increasing in the score, so its row max is x(rmax)
+            auto to_x = [&](auto modec, uint64_t rr, uint64_t nms) -> uint64_t {
+                constexpr int kMode = decltype(modec)::value;
+                if constexpr (kMode == 2) {
+                    float r0, r1;
+                    f2_split(rr, r0, r1);
+                    float m0, m1;
+                    f2_split(nms, m0, m1);
+                    // a masked score is -inf, and softcap*tanh(-inf) would be finite
+                    return f2_make(r0 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r0 * cap_in), m0),
+                                   r1 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r1 * cap_in), m1));
+                } else {
+                    if constexpr (kMode == 1) {
+                        const CapPoly cp = cap_poly(P.scale, P.softcap);
+                        uint64_t uu;
+                        rr = cap_g(cp, rr, uu);
+                    } else if constexpr (kMode == 3) {
+                        rr = cap_g_short(cap_short(P.scale, P.softcap), rr);
+                    }
+                    return f2_fma(rr, sl2_2, nms);
+                }
+            };
+            float xm, xm_;
+            {
+                const uint64_t r2 = f2_make(rmax, rmax), n2 = f2_make(-m_used, -m_used);
+                uint64_t x2;
+                if (!kCap) x2 = to_x(std::integral_constant<int, 0>(), r2, n2);
+                else x2 = to_x(std::integral_constant<int, 2>(), r2, n2);
+                f2_split(x2, xm, xm_);
+            }
+            if (rmax == -INFINITY) xm = -INFINITY;
+            const bool resc = xm > kRescaleHi || (!seen && xm < kRescaleLo && xm != -INFINITY);
+            if (__any_sync(0xffffffffu, resc)) {
+                // S_u(k) completed after P_u(k-1) V(k-1): O_u holds every earlier tile.
+                // Rows that have seen nothing yet hold O = 0 and keep alpha = 1 (their
+                // reference may move down by any amount).
+                const float alpha = fast_exp2(resc && seen ? -xm : 0.f);
+                if (resc) {
+                    m_used += xm;
+                    l *= alpha;
+                }
+                if (k > 0) {
+#pragma unroll 1
+                    for (int c = 0; c < kOC / 32; ++c) {
+                        uint32_t orr[32];
+                        tmem_ld32(tO + lane_off + hf * kOC + c * 32, orr);
+                        tmem_ld_wait(orr);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st32(tO + lane_off + hf * kOC + c * 32, orr);
+                    }
+                }
+            }
+            seen = seen || rmax != -INFINITY;
+            // pass 2: P chunk by chunk, each 16-bit chunk stored over S as soon as formed
+            // (this half's 64 keys go to TMEM columns 32*hf .. 32*hf+31)
+            auto p_pass = [&](auto modec) {
+                const uint64_t nms = f2_make(-m_used, -m_used);
+                uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float x0, x1;
+                        f2_split(to_x(modec, f2_make(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), nms),
+                                 x0, x1);
+                        const float p0 = fast_exp2(x0);  // ex2(-inf) = 0
+                        const float p1 = fast_exp2(x1);
+                        rs2[e & 1] = f2_add(rs2[e & 1], f2_make(p0, p1));
+                        pk[e] = pack2<BF16>(p0, p1);
+                    }
+                    tmem_st16(tS + lane_off + 32 * hf + 16 * c, pk);
+                }
+                float a0, a1, b0, b1;
+                f2_split(rs2[0], a0, a1);
+                f2_split(rs2[1], b0, b1);
+                l += (a0 + b0) + (a1 + b1);
+            };
+            if (!kCap) p_pass(std::integral_constant<int, 0>());
+            else if (shorter) p_pass(std::integral_constant<int, 3>());
+            else if (!accurate) p_pass(std::integral_constant<int, 1>());
+            else p_pass(std::integral_constant<int, 2>());
+        };
+        for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
+            const FwdItem it = fwd_item<VL>(P, w, vcur);
+            const int tq = it.sq.tq, tk = it.sq.tk;
+            // per-tile running state of this thread's row (selected by the run-time tile
+            // index, so that it stays in registers)
+            float mA = 0.f, mB = 0.f, lA = 0.f, lB = 0.f;
+            bool seenA = false, seenB = false;
+            for (int n = 0; ok && n < it.ntiles; ++n) {
+#pragma unroll 1
+                for (int u = 0; u < 2; ++u) {
+                    const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
+                    const int k = it.t0 + n - my.t0;  // index of union tile n in u's own sequence
+                    if (k < 0 || k >= my.ntiles) continue;
+                    const int ib = it.i0 + u * BM;  // first row of tile u
+                    const int i = ib + r;
+                    const int p = i + P.q_offset;
+                    const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, tq) - 1 + P.q_offset;
+                    const int j0 = (my.t0 + k) * BN;
+                    uint32_t mbits[2] = {0xffffffffu, 0xffffffffu};
+                    if (P.key_mask) {
+                        const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int j = j0 + 64 * hf + c * 32 + lane;
+                            mbits[c] = __ballot_sync(0xffffffffu, j < tk && mrow[j] > 0.5f);
+                        }
+                    }
+                    // a half tile whose keys the mask keeps whole needs no mask pass
+                    const bool full = tile_full(P.wl, P.wr, tk, prow0, prow1, j0, j0 + BN) &&
+                                      (mbits[0] & mbits[1]) == 0xffffffffu;
+                    // this row's visible columns of the tile: [clo, chi)
+                    int clo = 0, chi = BN;
+                    if (!full) {
+                        chi = min(chi, tk - j0);
+                        if (P.wr >= 0) chi = min(chi, p + P.wr - j0 + 1);
+                        if (P.wl >= 0) clo = max(clo, p - P.wl - j0);
+                    }
+                    const int sc = u == 0 ? scA++ : scB++;
+                    ok = wait_warp(S_FULL(u), sc & 1) && ok;
+                    tc_fence_after();
+                    uint32_t sv[2][32];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) tmem_ld32(tbase + u * 128 + lane_off + 64 * hf + c * 32, sv[c]);
+                    tmem_ld_wait_only();
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) tmem_pin(sv[c]);
+                    if (BIAS && i < tq) {  // additive score bias (never with softcap here)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) add_bias32(P, it.b, it.h, i, j0 + 64 * hf + 32 * c, tk, sv[c]);
+                    }
+                    float m_used = u == 0 ? mA : mB, l = u == 0 ? lA : lB;
+                    bool seen = u == 0 ? seenA : seenB;
+                    // a failed wait still takes part in the pair's exchange (inside
+                    // run_tile), so that the partner is never left waiting; both then stop
+                    if (cap)
+                        run_tile(std::integral_constant<bool, true>(), u, m_used, l, seen, k, full, clo, chi, mbits, sv);
+                    else
+                        run_tile(std::integral_constant<bool, false>(), u, m_used, l, seen, k, full, clo, chi, mbits, sv);
+                    if (u == 0) {
+                        mA = m_used;
+                        lA = l;
+                        seenA = seen;
+                    } else {
+                        mB = m_used;
+                        lB = l;
+                        seenB = seen;
+                    }
+                    if (!ok) break;
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(P_FULL(u)));
+                }
+            }
+            if (!ok) break;
+            // epilogues: tile A, then tile B (whose last P.V completes meanwhile)
+#pragma unroll 1
+            for (int u = 0; u < 2; ++u) {
+                const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
+                const int ib = it.i0 + u * BM;
+                if (ib >= tq) continue;
+                const int i = ib + r;
+                const uint32_t tO = tbase + 256 + u * HD;
+                bool have_o = false;
+                if (my.ntiles > 0) {
+                    const int a = u == 0 ? actA++ : actB++;
+                    have_o = ok = wait_warp(O_DONE(u), a & 1) && ok;
+                }
+                if (have_o) tc_fence_after();
+                // the row's sum over both halves
+                const float lu = u == 0 ? lA : lB;
+                const float lt = lu + exchange(lu);
+                if (!ok) break;
+                const float m_used = u == 0 ? mA : mB;
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                uint32_t packed[kOC / 2];
+                {
+                    // this half's O columns in flight at once, one wait
+                    uint32_t orr[kOC / 32][32];
+                    if (have_o) {
+#pragma unroll
+                        for (int c = 0; c < kOC / 32; ++c) tmem_ld32(tO + lane_off + hf * kOC + c * 32, orr[c]);
+                        tmem_ld_wait_only();
+#pragma unroll
+                        for (int c = 0; c < kOC / 32; ++c) tmem_pin(orr[c]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kOC / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) orr[c][e] = 0u;
+                    }
+#pragma unroll
+                    for (int c = 0; c < kOC / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            packed[c * 16 + e] = pack2<BF16>(__uint_as_float(orr[c][2 * e]) * inv,
+                                                             __uint_as_float(orr[c][2 * e + 1]) * inv);
+                }
+                // O_u is in registers: the next item's first P.V may overwrite it
+                if (have_o) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(BAR(O_EMPTY(u)));
+                }
+                // Each thread writes its row's half of O (16-byte stores; a padded head
+                // writes only its real columns); rows past the sequence's end are not written.
+                if (i < tq) {
+                    const int ncol = min(kOC, P.hd - hf * kOC);
+                    uint4* orow = reinterpret_cast<uint4*>(
+                        reinterpret_cast<uint16_t*>(P.o) +
+                        (((long long)it.sq.zb * P.Tq + it.sq.q0 + i) * P.H + it.h) * P.hd + hf * kOC);
+#pragma unroll
+                    for (int w4 = 0; w4 < kOC / 8; ++w4)
+                        if (w4 * 8 < ncol)
+                            orow[w4] =
+                                make_uint4(packed[4 * w4], packed[4 * w4 + 1], packed[4 * w4 + 2], packed[4 * w4 + 3]);
+                    if (P.lse && hf == 0)
+                        P.lse[((long long)it.b * P.H + it.h) * P.Tq + i] =
+                            lt > 0.f ? (m_used + log2f(lt)) * 0.6931471805599453f : -INFINITY;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+template <bool BF16, int HD>
+cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
+    using C = Fwd2Cfg<HD>;
+    const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
+    // a head size below HD (dense batches without a bias only) runs the padded instantiations
+    auto kern = p.hd != HD ? (c ? fwd_tc2_kernel<BF16, HD, 12> : fwd_tc2_kernel<BF16, HD, 8>)
+                : p.cu_q   ? (c ? fwd_tc2_kernel<BF16, HD, 5> : fwd_tc2_kernel<BF16, HD, 1>)
+                : p.bias   ? fwd_tc2_kernel<BF16, HD, 2>
+                           : (c ? fwd_tc2_kernel<BF16, HD, 4> : fwd_tc2_kernel<BF16, HD, 0>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
+    if (e != cudaSuccess) return e;
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // persistent: one CTA per SM (one fits), each walks its items in snake order
+    // (packed sequences may have fewer items than this bound: those CTAs exit at once)
+    const long long items = (long long)((p.Tq + 2 * BM - 1) / (2 * BM)) * p.H * p.B;
+    const unsigned grid = (unsigned)(items < nsm ? items : nsm);
+    kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+}  // namespace attn

@@ -40,7 +40,8 @@
  * Every call validates its arguments on the host, then enqueues kernels on
  * `stream` (a cudaStream_t passed as void*; NULL = legacy default stream) and
  * returns.  Outputs and gradients are overwritten, never accumulated
- * (ferrotensor flash_attention_backward: "Writes (does not accumulate into)").
+ * (ferrotensor engine/attention.rs, flash_attention_backward: gradients are
+ * stored over the buffers' contents).
  * Pointers must be 16-byte aligned.  The device current on the calling thread
  * must own every pointer.
  *
@@ -87,9 +88,11 @@ typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
  *   B, Tq, Tk : batch, query rows, key rows (>= 0; B or Tq == 0 is a no-op,
  *               Tk == 0 writes O = 0, LSE = -inf).
  *   H, Hkv    : query / KV heads, Hkv >= 1 divides H.
- *   hd        : head dim 32, 64, 96, 128 or 256.  16-bit types at 64 and 128 run on
- *               the tensor cores; fp32 and the other sizes on CUDA-core kernels
- *               (same results, no tensor-core speed).
+ *   hd        : head dim 32, 64, 96, 128 or 256.  16-bit types at 32, 64, 96 and 128
+ *               run on the tensor cores (32 and 96 as 64 and 128 with the columns past
+ *               the head read as zeros; with an additive bias or in packed sequences
+ *               they take the CUDA-core kernels); fp32 and hd 256 run on CUDA-core
+ *               kernels (same results, no tensor-core speed).
  *   scale     : > 0 and finite (1/sqrt(hd) in the usual case).
  *   causal    : 0/1.   window : >= 0, 0 = unbounded.   softcap : >= 0, 0 = off.
  *   q_offset  : >= 0, absolute position of query row 0.
@@ -293,13 +296,12 @@ ATTN_API attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k
                         void* stream);
 
 /*
- * attn_decode without a workspace argument (the computation is brotensor
- * ops/flash_attention.h, flash_attention_decode / _decode_len), for callers that cannot call
+ * attn_decode without a workspace argument, for callers that cannot call
  * cudaMalloc and have no scratch buffer to pass in: for example a plugin that
  * is handed only its input and output buffers, a serving loop that forbids
  * device allocation after start-up so that a request can never fail for lack
- * of memory, or a C caller with no device allocator of its own.  The pages
- * have no counterpart to this call; it exists for those callers.
+ * of memory, or a C caller with no device allocator of its own.  The paper
+ * has no counterpart to this call; it exists for those callers.
  *
  * Same arguments, kernels and results as attn_decode.  The split partials
  * live in one fixed array of 32 MiB that the library reserves in device
@@ -321,9 +323,9 @@ ATTN_API attn_status attn_decode_noalloc(attn_dtype dt, const void* q, const voi
 /*
  * Rotate-half rotary embedding, in place, for the q or k given to the calls
  * above (a separate HBM-bound pass: the attention kernels read the rotated rows).
- * Source: ferrotensor engine/attention.rs, rope / rope_theta ("rotate-half RoPE
- * (theta 10000) applied in place"; every head vector of token s gets position
- * pos + s).
+ * Source: ferrotensor engine/attention.rs, rope / rope_theta (the rotate-half
+ * form, done in place, with base 10000 unless set; every head vector of token s
+ * gets position pos + s).
  *   x     : [B, T, H*hd] of dtype dt, 16-byte aligned; overwritten.
  *   pos   : position of token 0 of every sequence (>= 0).
  *   theta : base frequency (10000 in the page's default, > 0).
