@@ -32,6 +32,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd & fwd+bwd TFLOP/s vs BF16 peak; decode HBM GB/s vs peak"
 FWD_FLOPS_PER_PAIR = lambda hd: 4 * hd
+SOAK_S = 1.0  # seconds of untimed steps after the timed ones, for the clock record
+SLEEP_CYCLES = 1_000_000  # GPU sleep (about 0.5 ms) in front of timed calls that have no L2 flush before them
 KERNEL_FLOPS_PER_PAIR = {  # algorithmic GEMM flops per visible pair per head, by kernel
     "fwd": lambda hd: 4 * hd,     # S = QK^T, O += PV
     "dkdv": lambda hd: 8 * hd,    # S^T and dP^T recompute, dV += P^T dO, dK += dS^T Q
@@ -143,14 +145,16 @@ class Clocks:
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        load = [r for r in rows if r["power"] > 200.0] or rows
+        # a sample counts as under load when the board draws more than 200 W; with
+        # none, the median is over every sample and samples_under_load says 0
+        load = [r for r in rows if r["power"] > 200.0]
         reasons = sorted({name for r in rows for name, key in (("hw_slowdown", "hw"), ("hw_thermal_slowdown", "hwt"),
                                                                 ("sw_thermal_slowdown", "swt"),
                                                                 ("sw_power_cap", "cap"))
                           if r[key].lower() == "active"})
-        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["smax"] for r in rows),
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(load),
-                "power_w_max": max(r["power"] for r in rows)}
+        return {"sm_mhz": statistics.median(r["sm"] for r in (load or rows)),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": reasons, "samples": len(rows),
+                "samples_under_load": len(load), "power_w_max": max(r["power"] for r in rows)}
 
 
 # --------------------------------------------------------------- reference
@@ -164,12 +168,15 @@ def oracle_sample(w, inp, groups, rows):
 
     G, hd, T = w.H // w.Hkv, w.hd, w.Tq
     r0 = T - rows
+    # keys below the window of the first sampled row are visible to no sampled row:
+    # they are left out (the rows' positions shift with them, so nothing changes)
+    k0 = max(0, r0 - w.window + 1) if w.window else 0
     f = lambda t: t.to(dtype=__import__("torch").float64).numpy()
     q = np.concatenate([f(inp["q"][b:b + 1, r0:, kvh * G * hd:(kvh + 1) * G * hd]) for b, kvh in groups])
     do = np.concatenate([f(inp["do"][b:b + 1, r0:, kvh * G * hd:(kvh + 1) * G * hd]) for b, kvh in groups])
-    k = np.concatenate([f(inp["k"][b:b + 1, :, kvh * hd:(kvh + 1) * hd]) for b, kvh in groups])
-    v = np.concatenate([f(inp["v"][b:b + 1, :, kvh * hd:(kvh + 1) * hd]) for b, kvh in groups])
-    kw = dict(H=G, Hkv=1, scale=w.scale, causal=w.causal, window=w.window, softcap=w.softcap, q_offset=r0)
+    k = np.concatenate([f(inp["k"][b:b + 1, k0:, kvh * hd:(kvh + 1) * hd]) for b, kvh in groups])
+    v = np.concatenate([f(inp["v"][b:b + 1, k0:, kvh * hd:(kvh + 1) * hd]) for b, kvh in groups])
+    kw = dict(H=G, Hkv=1, scale=w.scale, causal=w.causal, window=w.window, softcap=w.softcap, q_offset=r0 - k0)
     t0 = time.perf_counter()
     oracle.fwd(q, k, v, **kw)
     oracle.bwd(q, k, v, do, **kw)
@@ -180,6 +187,61 @@ def oracle_sample(w, inp, groups, rows):
 
 def oracle_groups(w, n):
     return [(b, kvh) for b in range(w.B) for kvh in range(w.Hkv)][:n]
+
+
+def oracle_components(synth):
+    """The fp64 oracle timed on this host's cores, once per workload, in the units of
+    that workload's GPU figure: the fp32 causal forward (whole), the window+softcap
+    fwd+bwd and the key-masked encoder forward (samples stated below), and decode
+    (two of the sixteen sequences).  The oracle runs as it stands."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    oracle.build()
+    f = lambda t: t.to(dtype=torch.float64).numpy()
+    out = {}
+    cores = oracle.num_threads()
+    # fp32 causal forward, whole
+    w = synth.WORKLOADS["fp32_causal"]
+    inp = synth.make_inputs(w)
+    t0 = time.perf_counter()
+    oracle.fwd(f(inp["q"]), f(inp["k"]), f(inp["v"]), H=w.H, Hkv=w.Hkv, scale=w.scale, causal=True)
+    dt = time.perf_counter() - t0
+    fl = 4 * w.hd * visible_pairs(w)
+    out["fp32_causal_fwd"] = {"s": dt, "TFLOP/s": fl / dt / 1e12, "cores": cores, "sample": "the whole workload"}
+    # window + softcap fwd+bwd: the last 1024 query rows of 8 (batch, KV head) groups
+    w = synth.WORKLOADS["swa_softcap"]
+    inp = synth.make_inputs(w)
+    dt, fl = oracle_sample(w, inp, oracle_groups(w, 8), 1024)
+    out["swa_softcap_fwd_bwd"] = {"s": dt, "TFLOP/s": fl / dt / 1e12, "cores": cores,
+                                  "sample": "fwd+bwd of the last 1024 query rows of 8 of 8 (batch, KV head) groups "
+                                            "over the 2047 keys they can see"}
+    # key-masked encoder forward, whole
+    w = synth.WORKLOADS["encoder_mask"]
+    inp = synth.make_inputs(w)
+    t0 = time.perf_counter()
+    oracle.fwd(f(inp["q"]), f(inp["k"]), f(inp["v"]), H=w.H, Hkv=w.Hkv, scale=w.scale, causal=False,
+               key_mask=f(inp["key_mask"]))
+    dt = time.perf_counter() - t0
+    fl = 4 * w.hd * visible_pairs(w, lengths=inp["lengths"].tolist())
+    out["encoder_mask_fwd"] = {"s": dt, "TFLOP/s": fl / dt / 1e12, "cores": cores, "sample": "the whole workload"}
+    # decode: 2 of the 16 sequences (every head, the whole cache)
+    for name in ("decode_lq1", "decode_lq4"):
+        w = synth.WORKLOADS[name]
+        nb = 2
+        q = f(synth.normal((w.B, w.Tq, w.H * w.hd), w.seed + 0, w.dtype)[:nb])
+        k = f(synth.normal((w.B, w.Tk, w.Hkv * w.hd), w.seed + 1, w.dtype)[:nb])
+        v = f(synth.normal((w.B, w.Tk, w.Hkv * w.hd), w.seed + 2, w.dtype)[:nb])
+        t0 = time.perf_counter()
+        oracle.fwd(q, k, v, H=w.H, Hkv=w.Hkv, scale=w.scale, causal=True, q_offset=w.q_offset)
+        dt = time.perf_counter() - t0
+        nbytes = decode_bytes(w.with_(B=nb))
+        out[name] = {"s": dt, "GB/s": nbytes / dt / 1e9, "cores": cores,
+                     "sample": "%d of %d sequences (%d algorithmic bytes)" % (nb, w.B, nbytes)}
+        del q, k, v
+    return out
 
 
 def run_reference(args, rank):
@@ -218,6 +280,91 @@ def workload_config(w):
             "parallelism": "replicas", "l2": "flushed between steps (512 MiB write), outside the timed events"}
 
 
+# ------------------------------------------------------------- profile cases
+# Each case makes one workload's inputs on cuda:0 and returns the calls of one
+# repetition, in order.  Kernel launches per repetition (for a profiler's
+# --launch-skip): gqa_prefill 3 (fwd, dQ, dK/dV); swa_softcap, varlen_packed and
+# bias_prefill 3 (fwd, dQ, dK/dV); encoder_mask 1; decode_lq4 2 (split, combine).
+def _case_dense(A, synth, torch, dev, name, fwd_only=False, bias=False):
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    kw = dict(H=w.H, Hkv=w.Hkv, scale=w.scale)
+    if bias:
+        kw.update(window_left=-1, window_right=0,
+                  bias=synth.normal((1, 1, w.Tq, w.Tk), w.seed + 5, "f32").to(dev))
+    else:
+        kw.update(causal=w.causal, window=w.window, softcap=w.softcap)
+        if w.key_mask:
+            kw["key_mask"] = inp["key_mask"].to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Tq), dtype=torch.float32, device=dev)
+    fwd, bwd = (A.attn_fwd_ex, A.attn_bwd_ex) if bias else (A.attn_fwd, A.attn_bwd)
+    calls = [lambda: fwd(q, k, v, o=o, lse=lse, **kw)]
+    if not fwd_only:
+        do = inp["do"].to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(A.attn_bwd_workspace_size(w.B, w.Tq, w.H), dtype=torch.uint8, device=dev)
+        calls.append(lambda: bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=ws, **kw))
+    return calls
+
+
+def _case_varlen(A, synth, torch, dev):
+    w = synth.WORKLOADS["varlen_packed"]
+    vi = synth.make_packed_inputs(w)
+    q, k, v, do = (vi[n].to(dev) for n in ("q", "k", "v", "do"))
+    cu = vi["cu"].to(device=dev, dtype=torch.int32)
+    o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    lse = torch.empty((w.B, w.H, w.Tq), dtype=torch.float32, device=dev)
+    ws = torch.empty(A.attn_bwd_workspace_size(w.B, w.Tq, w.H), dtype=torch.uint8, device=dev)
+    kw = dict(H=w.H, Hkv=w.Hkv, scale=w.scale, causal=True)
+    return [lambda: A.attn_varlen_fwd(q, k, v, cu, cu, w.Tq, w.Tk, o=o, lse=lse, **kw),
+            lambda: A.attn_varlen_bwd(q, k, v, o, do, lse, cu, cu, w.Tq, w.Tk, dq=dq, dk=dk, dv=dv, workspace=ws,
+                                      **kw)]
+
+
+def _case_decode(A, synth, torch, dev):
+    w = synth.WORKLOADS["decode_lq4"]
+    di = synth.make_inputs(w)
+    q, k, v = (di[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Tq), dtype=torch.float32, device=dev)
+    ws = torch.empty(A.attn_decode_workspace_size(w.B, w.Tq, w.Tk, w.H, w.Hkv, w.hd), dtype=torch.uint8, device=dev)
+    return [lambda: A.attn_decode(q, k, v, H=w.H, Hkv=w.Hkv, causal=True, q_offset=w.q_offset, o=o, lse=lse,
+                                  workspace=ws)]
+
+
+PROFILE_CASES = {
+    "gqa_prefill": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill"),
+    "swa_softcap": lambda A, s, t, d: _case_dense(A, s, t, d, "swa_softcap"),
+    "encoder_mask": lambda A, s, t, d: _case_dense(A, s, t, d, "encoder_mask", fwd_only=True),
+    "bias_prefill": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill", bias=True),
+    "varlen_packed": lambda A, s, t, d: _case_varlen(A, s, t, d),
+    "decode_lq4": lambda A, s, t, d: _case_decode(A, s, t, d),
+}
+
+
+def run_profile_case(name, reps):
+    """Run one workload's calls `reps` times on cuda:0 (no timing, no JSON line) and check the
+    device status word afterwards."""
+    import torch
+
+    import attention_attn_fwd_08_gb300 as A
+    from attention_attn_fwd_08_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    calls = PROFILE_CASES[name](A, synth, torch, dev)
+    for _ in range(reps):
+        for fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    if st != A.OK:
+        raise RuntimeError("device status word %#x" % word)
+    print("profile case %s: %d repetitions, %d launches" % (name, reps, A.attn_launch_count()))
+
+
 # --------------------------------------------------------------------- ours
 def max_over_ranks(ms, world, device):
     """Slowest rank's step time: every rank's replica counts only once all finish."""
@@ -245,6 +392,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["all", "prefill"], default="all",
                     help="prefill: only the fwd+bwd step (no decode measurement), e.g. for profiler runs")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run only this workload's calls --reps times, untimed and without a JSON line "
+                         "(the command a profiler wraps)")
+    ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -253,6 +404,9 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.reps)
         return
 
     import torch
@@ -307,9 +461,18 @@ def main():
             e1.record(stream)
             torch.cuda.synchronize()
             steps_ms.append(e0.elapsed_time(e1))
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
-    launches = A.attn_launch_count() - n0
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        launches = A.attn_launch_count() - n0
+        # The timed steps last milliseconds, shorter than the sampler's 200 ms period:
+        # the same step keeps running, untimed, for SOAK_S more seconds inside the
+        # sampling window, so that the clock record sees this work under load.
+        soak0, soak_steps = time.perf_counter(), 0
+        while time.perf_counter() - soak0 < SOAK_S:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize()
+            soak_steps += 50
     if world > 1:
         dist.barrier()
     st, word = A.attn_get_device_status()
@@ -364,6 +527,9 @@ def main():
         times = []
         for _ in range(args.steps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            # the GPU sleeps while the host enqueues the call, so that the events time the
+            # kernels and not the host's launch latency (decode has no L2 flush in front)
+            torch.cuda._sleep(SLEEP_CYCLES)
             e0.record(stream)
             fn()
             e1.record(stream)
@@ -385,6 +551,7 @@ def main():
             times = []
             for _ in range(args.steps):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda._sleep(SLEEP_CYCLES)
                 e0.record(stream)
                 fl()
                 e1.record(stream)
@@ -404,8 +571,8 @@ def main():
     dom = max(("fwd", "dkdv", "dq"), key=lambda n: comps[n]["ms"])
     fam = A.attn_kernel_family("bfloat16", w.hd)
     # the kernel's own source plus the shared device helpers it compiles with
-    src = {"fwd": ("fwd_tc.cu",) if fam else ("simt.cu",), "dkdv": ("bwd_tc.cu",) if fam else ("simt.cu",),
-           "dq": ("bwd_tc.cu",) if fam else ("simt.cu",)}[dom] + ("common.cuh",)
+    src = {"fwd": ("fwd_tc.cuh",) if fam else ("simt.cu",), "dkdv": ("bwd_tc.cuh",) if fam else ("simt.cu",),
+           "dq": ("bwd_tc.cuh",) if fam else ("simt.cu",)}[dom] + ("common.cuh",)
     ach = comps[dom]["TFLOP/s"]
     roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s",
                 "frac": ach / peaks["bf16"], "traffic": traffic_for(dom, src_sha(*src)),
@@ -414,6 +581,19 @@ def main():
 
     # ------------------------------------------------------------------ e2e
     e2e = measure_e2e(A, w, inp, dev, stream, args, kw)
+
+    # ------------------------------------------------------- fp32 causal forward
+    if args.workload == "all":
+        w1 = synth.WORKLOADS["fp32_causal"]
+        i1 = synth.make_inputs(w1)
+        q1, k1, v1 = (i1[n].to(dev) for n in ("q", "k", "v"))
+        o1 = torch.empty_like(q1)
+        l1 = torch.empty((w1.B, w1.H, w1.Tq), dtype=torch.float32, device=dev)
+        t = time_passes(torch, stream, [("fwd", lambda: A.attn_fwd(q1, k1, v1, o=o1, lse=l1, H=w1.H, Hkv=w1.Hkv,
+                                                                     scale=w1.scale, causal=True))], args, None)
+        fl = 4 * w1.hd * visible_pairs(w1)
+        comps["fp32_causal_fwd"] = {"ms": t["fwd"], "TFLOP/s": fl / (t["fwd"] * 1e-3) / 1e12,
+                                    "note": "fp32 CUDA-core kernel; one CTA-sized problem, launch-bound"}
 
     # ---------------------------------------------------------- cpu baseline
     cpu = None
@@ -426,13 +606,18 @@ def main():
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": "fwd+bwd of the last %d query rows of %d (batch, KV head) groups, %.1f s" % (
                    rows, len(groups), dt)}
+        if args.workload == "all":
+            for name, rec in oracle_components(synth).items():
+                comps.setdefault(name, {})["cpu_oracle"] = rec
+            comps.setdefault("fwd_bwd_step", {})["cpu_oracle"] = {"s": dt, "TFLOP/s": fl / dt / 1e12,
+                                                                  "cores": cpu["cores"], "sample": cpu["sample"]}
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1))", "config": workload_config(w),
             "kernel_family": "tcgen05" if fam else "simt", "components": components_round(comps),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk.summary(), "wall_s_timed_loop": wall}
+            "clocks": dict(clk.summary(), soak_s=SOAK_S, soak_steps=soak_steps), "wall_s_timed_loop": wall}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -442,13 +627,17 @@ def main():
 def time_passes(torch, stream, passes, args, flush_buf):
     """Mean ms of each pass, run back to back in order after an L2 flush, one event between each."""
     for _ in range(args.warmup):
-        flush_buf.zero_()
+        if flush_buf is not None:
+            flush_buf.zero_()
         for _, fn in passes:
             fn()
     torch.cuda.synchronize()
     acc = {n: [] for n, _ in passes}
     for _ in range(args.steps):
-        flush_buf.zero_()
+        if flush_buf is not None:
+            flush_buf.zero_()
+        else:
+            torch.cuda._sleep(SLEEP_CYCLES)  # covers the host's enqueue of the passes
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(passes) + 1)]
         evs[0].record(stream)
         for i, (_, fn) in enumerate(passes):
@@ -546,7 +735,9 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
 
 
 def components_round(c):
-    return {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()} for k, v in c.items()}
+    if isinstance(c, dict):
+        return {k: components_round(v) for k, v in c.items()}
+    return round(c, 4) if isinstance(c, float) else c
 
 
 def measure_e2e(A, w, inp, dev, stream, args, kw):
