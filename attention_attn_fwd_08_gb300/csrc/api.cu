@@ -83,6 +83,23 @@ bool make_map(CUtensorMap* m, int dt, const void* base, long long inner, long lo
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over a [batches][rows][heads][hd] 16-bit tensor, box {64, 1, box_rows, 1},
+// 128-byte swizzle: for a head size below the kernel's (32 in a 64 kernel, 96 in a
+// 128 kernel), the box's columns past hd load as zeros and are never stored.
+bool make_map4(CUtensorMap* m, int dt, const void* base, int hd, long long heads, long long rows,
+               long long batches, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const CUtensorMapDataType t = dt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)heads, (cuuint64_t)rows, (cuuint64_t)batches};
+    cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)heads * hd * 2, (cuuint64_t)rows * heads * hd * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, t, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------- validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -124,10 +141,21 @@ Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, i
     return p;
 }
 
-// fp16/bf16 at hd 64 / 128 run on the tensor cores; fp32 stays on the CUDA-core
-// kernels (no TF32, no 16-bit P), which is what fp32 accuracy needs, and so do
-// the head sizes without a tensor-core kernel (32, 96, 256: correct, not fast).
-bool use_tcgen05(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 64 || hd == 128); }
+// fp16/bf16 at hd 64 / 128 run on the tensor cores, and so do hd 32 and 96 as 64 and
+// 128 with the columns past the head read as zeros (dense batches; packed sequences
+// and a score bias at those sizes take the CUDA-core kernels).  fp32 stays on the
+// CUDA-core kernels (no TF32, no 16-bit P), which is what fp32 accuracy needs, and so
+// does hd 256 (correct, not fast).
+bool padded_head(int hd) { return hd == 32 || hd == 96; }
+bool use_tcgen05(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 32 || hd == 64 || hd == 96 || hd == 128); }
+
+// Tensor map of one activation for the tensor-core kernels: 3-D at hd 64 / 128, 4-D
+// (zero-filled past the head) at hd 32 / 96.
+bool act_map(CUtensorMap* m, attn_dtype dt, const void* base, int hd, long long heads, long long rows,
+             long long batches, int box_rows) {
+    if (padded_head(hd)) return make_map4(m, (int)dt, base, hd, heads, rows, batches, box_rows);
+    return make_map(m, (int)dt, base, heads * hd, rows, batches, box_rows);
+}
 
 // Decode split plan: a deterministic function of the shape.  Aim for about
 // eight waves of two resident CTAs on each of GB300's 152 SMs.
@@ -204,12 +232,11 @@ attn_status fwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     // a bias with a softcap has no tensor-core form (the cap is not linear in the raw
     // score): those calls take the CUDA-core kernels
-    if (!use_tcgen05(dt, hd) || (p.bias && p.softcap > 0.f)) return counted(launch_simt_fwd(p, (int)dt, s), 1);
+    if (!use_tcgen05(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd))))
+        return counted(launch_simt_fwd(p, (int)dt, s), 1);
     FwdMaps maps;
-    if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
-        !make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 128) ||
-        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128) ||
-        !make_map(&maps.o, dt, o, (long long)H * hd, Tq, B, 32))
+    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128) || !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, 128) ||
+        !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, 128) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 32))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_fwd(p, (int)dt, maps, s), 1);
 }
@@ -274,7 +301,7 @@ attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     p.tq_pad = (Tq + 63) / 64 * 64;
     p.ndelta = static_cast<float*>(workspace);
     p.nlse2 = p.ndelta + (size_t)B * H * p.tq_pad;
-    if (!use_tcgen05(dt, hd) || (p.bias && p.softcap > 0.f)) {
+    if (!use_tcgen05(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd)))) {
         // the fp32 dQ pass reads D from the workspace: pass 4 implies pass 1 there
         const int ph = (phases & 4) ? (phases | 1) : phases;
         const int nks = ((ph & 1) ? 1 : 0) + ((ph & 2) ? 1 : 0) + ((ph & 4) ? 1 : 0);
@@ -283,18 +310,14 @@ attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     // the tensor-core dQ pass forms D itself: pass 1 is then not run separately
     const int nk = ((phases & 1) && !(phases & 4) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
     BwdMaps maps;
-    if (!make_map(&maps.q, dt, q, (long long)H * hd, Tq, B, 128) ||
-        !make_map(&maps.dout, dt, dout, (long long)H * hd, Tq, B, 128) ||
-        !make_map(&maps.k, dt, k, (long long)Hkv * hd, Tk, B, 128) ||
-        !make_map(&maps.v, dt, v, (long long)Hkv * hd, Tk, B, 128) ||
-        !make_map(&maps.q64, dt, q, (long long)H * hd, Tq, B, 64) ||
-        !make_map(&maps.dout64, dt, dout, (long long)H * hd, Tq, B, 64) ||
-        !make_map(&maps.k64, dt, k, (long long)Hkv * hd, Tk, B, 64) ||
-        !make_map(&maps.v64, dt, v, (long long)Hkv * hd, Tk, B, 64) ||
-        ((phases & 4) && (!make_map(&maps.dq32, dt, dq, (long long)H * hd, Tq, B, 32) ||
-                          !make_map(&maps.o, dt, o, (long long)H * hd, Tq, B, 128))) ||
-        ((phases & 2) && (!make_map(&maps.dk32, dt, dk, (long long)Hkv * hd, Tk, B, 32) ||
-                          !make_map(&maps.dv32, dt, dv, (long long)Hkv * hd, Tk, B, 32))))
+    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128) || !act_map(&maps.dout, dt, dout, hd, H, Tq, B, 128) ||
+        !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, 128) || !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, 128) ||
+        !act_map(&maps.q64, dt, q, hd, H, Tq, B, 64) || !act_map(&maps.dout64, dt, dout, hd, H, Tq, B, 64) ||
+        !act_map(&maps.k64, dt, k, hd, Hkv, Tk, B, 64) || !act_map(&maps.v64, dt, v, hd, Hkv, Tk, B, 64) ||
+        ((phases & 4) &&
+         (!act_map(&maps.dq32, dt, dq, hd, H, Tq, B, 32) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 128))) ||
+        ((phases & 2) &&
+         (!act_map(&maps.dk32, dt, dk, hd, Hkv, Tk, B, 32) || !act_map(&maps.dv32, dt, dv, hd, Hkv, Tk, B, 32))))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_bwd(p, (int)dt, maps, phases, s), nk);
 }
@@ -372,7 +395,7 @@ attn_status attn_varlen_fwd(attn_dtype dt, const void* q, const void* k, const v
     if (!p.status) return ATTN_ERR_CUDA;
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     // no keys anywhere: the CUDA-core kernel writes O = 0 and LSE = -inf per row
-    if (!use_tcgen05(dt, hd) || max_seqlen_k == 0 || total_k == 0)
+    if (!use_tcgen05(dt, hd) || padded_head(hd) || max_seqlen_k == 0 || total_k == 0)
         return counted(launch_simt_fwd(p, (int)dt, s), 1);
     FwdMaps maps;
     if (!make_map(&maps.q, dt, q, (long long)H * hd, total_q, 1, 128) ||
@@ -410,7 +433,8 @@ attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k, const v
     p.nlse2 = p.ndelta + (size_t)batch * H * p.tq_pad;
     // with no query rows or no key rows anywhere, the CUDA-core kernels write the
     // zero gradients of whatever rows the sequences have
-    if (!use_tcgen05(dt, hd) || max_seqlen_q == 0 || max_seqlen_k == 0 || total_q == 0 || total_k == 0)
+    if (!use_tcgen05(dt, hd) || padded_head(hd) || max_seqlen_q == 0 || max_seqlen_k == 0 || total_q == 0 ||
+        total_k == 0)
         return counted(launch_simt_bwd(p, (int)dt, 7, s), 3);
     BwdMaps maps;
     if (!make_map(&maps.q, dt, q, (long long)H * hd, total_q, 1, 128) ||

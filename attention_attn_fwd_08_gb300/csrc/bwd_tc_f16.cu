@@ -1,0 +1,11 @@
+// bwd_tc_f16.cu -- the tensor-core backward (bwd_tc.cuh) instantiated for f16.
+#include "bwd_tc.cuh"
+
+namespace attn {
+
+cudaError_t launch_tc_bwd_f16(const Params& p, const BwdMaps& maps, int phases, cudaStream_t s) {
+    if (p.hd <= 64) return bwd_typed<false, 64>(p, maps, phases, s);
+    return bwd_typed<false, 128>(p, maps, phases, s);
+}
+
+}  // namespace attn

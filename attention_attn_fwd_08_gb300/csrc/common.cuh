@@ -440,6 +440,36 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                  "r"(src), "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// 4-D forms, for maps over [batches][rows][heads][hd] (padded head sizes: the
+// box's 64 columns reach past hd, those columns load as zeros and are not stored)
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+// Activation tiles: box bx (64 columns) of head h, rows from `row`, batch zb.  With
+// kPad the map is 4-D ([zb][row][h][col], hd < the kernel's padded head size), else
+// 3-D ([zb][row][h*HD + col]).
+template <bool kPad, int HD>
+__device__ __forceinline__ void tile_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, int h, int bx, int row,
+                                          int zb) {
+    if constexpr (kPad) tma_load_4d(dst, map, bar, bx * 64, h, row, zb);
+    else tma_load_3d(dst, map, bar, h * HD + bx * 64, row, zb);
+}
+template <bool kPad, int HD>
+__device__ __forceinline__ void tile_store(const CUtensorMap* map, uint32_t src, int h, int col, int row, int zb) {
+    if constexpr (kPad) tma_store_4d(map, src, col, h, row, zb);
+    else tma_store_3d(map, src, h * HD + col, row, zb);
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // this thread's bulk stores have finished reading shared memory
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

@@ -80,38 +80,25 @@ __device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, 
 // Persistent: one CTA per SM walks work items in snake order (items c, 2g-1-c,
 // 2g+c, ... for CTA c of g), so that the heavy first items and the light last
 // ones even out across the CTAs.  An item is two query tiles (256 rows of one
-// head) sharing every K/V tile, with two softmax warpgroups per tile, so the
-// tensor core works on one tile's P.V and next S while the other tile's
-// softmax runs (ping-pong).  The K/V ring and every barrier phase run on across
-// items: the next item's Q tile loads once the current item's last S of that
-// tile completed, and its first P.V waits only for the epilogue to have read O
-// out of TMEM, so item boundaries cost little more than a ring step.
-//   warps 0-7   softmax: warp w owns TMEM lane quarter w % 4 (32 rows of each
-//               tile, one per thread) and key columns 64*(w/4) .. +63 of every
-//               score tile, and the same half of the O columns.  Each warp
-//               takes the tiles in the order A(n), B(n), A(n+1), ... so that the
-//               tensor core works on one tile while the warps run the other's
-//               softmax.  The two warps of a quarter exchange their rows' partial
-//               maxima once per tile (and partial sums once per tile per item)
-//               through shared memory, paced by an mbarrier of the pair.
-//   warp 8      TMA producer     warp 9  TMEM owner + MMA issuer of tile A
-//   warp 10     MMA issuer of tile B                                 (11 idle)
-// Splitting each row over two threads halves the chain of dependent work per
-// tile (TMEM load, row max, exponentials, P store) that the tensor core waits
-// for, and two warps per SM sub-partition issue it.
+// head) sharing every K/V tile, with one softmax warpgroup per tile, so the
+// tensor core works on one tile's
+// P.V and next S while the other warpgroup runs its softmax (ping-pong).  The
+// K/V ring and every barrier phase run on across items: the next item's Q tile
+// loads once the current item's last S of that tile completed, and its first
+// P.V waits only for the epilogue to have read O out of TMEM, so item
+// boundaries cost little more than a ring step.
+//   warps 0-3  softmax of tile A (rows i0 .. i0+127)
+//   warps 4-7  softmax of tile B (rows i0+128 .. i0+255)
+//   warp 8     TMA producer     warp 9  TMEM owner + MMA issuer of tile A
+//   warp 10    MMA issuer of tile B                                 (11 idle)
 // Registers: launched at 168 per thread (384 threads = 64512); the producer
-// warpgroup gives part of its share to the softmax warpgroups with setmaxnreg
-// (2*128*192 + 128*112 = 63488, within the launch total; at 200/96 and below
-// the producer and MMA warps spill, and the softmax's 64 scores per thread fit
-// 192 in every instantiation but packed sequences with a softcap).
+// warpgroup gives its share to the softmax warpgroups with setmaxnreg
+// (2*128*216 + 128*72 = 64512, never more than the launch total).
 // TMEM: S_A 0, S_B 128, O_A 256, O_B 256+hd (512 columns).  Each tile has a
 // single S buffer; S_u(n) is issued after P_u(n-1) V(n-1), so a completed
-// S_u(n) also means O_u is stable for a rescale.  P_u (16-bit) is written over
-// the first 64 columns of S_u: the warp of key half 1 writes its P into columns
-// that held half 0's scores, which half 0 has read by the time the pair's
-// exchange of that tile completes.
+// S_u(n) also means O_u is stable for a rescale.
 constexpr int kThreads2 = 384;
-constexpr int kRegsSoftmax = 192, kRegsProducer = 112;
+constexpr int kRegsSoftmax = 216, kRegsProducer = 72;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= kThreads2 * 168, "register split exceeds launch");
 
 template <int HD>
@@ -124,11 +111,11 @@ struct Fwd2Cfg {
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kStages * kKVBytes;
-    static constexpr int kNumBars = 17 + 4 * kStages;
-    // pair exchanges: [parity][key half][128 rows] fp32
-    static constexpr int kXOff = (kBarOff + kNumBars * 8 + 16 + 15) / 16 * 16;
-    static constexpr int kXBytes = 2 * 2 * 128 * 4;
-    static constexpr int kBytes = kXOff + kXBytes;
+    static constexpr int kNumBars = 13 + 4 * kStages;
+    // epilogue staging: one 32-row x 64-column slice (4 KB) per softmax warp
+    static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
+    static constexpr int kStgBytes = 8 * 32 * 128;
+    static constexpr int kBytes = kStgOff + kStgBytes;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
@@ -230,7 +217,7 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c)
 template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
     using C = Fwd2Cfg<HD>;
@@ -254,8 +241,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
     auto O_DONE = [&](int u) { return 8 + 4 * NS + u; };   // the item's last P.V of tile u completed
     auto O_EMPTY = [&](int u) { return 10 + 4 * NS + u; };  // the epilogue has read O_u out of TMEM
     const int MMA_DONE = 12 + 4 * NS;
-    // the two softmax warps of lane quarter q: one exchange per phase
-    auto XCH = [&](int q) { return 13 + 4 * NS + q; };
+    // softmaxes finished by tile u, counted per warp (exact counts: a tile with no work
+    // in an item lets the other run several softmaxes ahead, which mbarrier parity
+    // could not tell apart)
+    __shared__ int done_count[2];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     VlCursor vcur = {};
@@ -271,10 +260,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            // one arrival per softmax warp of the tile
-            if (i == P_FULL(0) || i == P_FULL(1) || i == O_EMPTY(0) || i == O_EMPTY(1)) count = 8;
-            for (int q = 0; q < 4; ++q)
-                if (i == XCH(q)) count = 2;
+            if (i == P_FULL(0) || i == P_FULL(1) || i == O_EMPTY(0) || i == O_EMPTY(1)) count = 4;
             // stage releases and the teardown barrier: one arrival per MMA issuer
             for (int s2 = 0; s2 < NS; ++s2)
                 if (i == K_EMPTY(s2) || i == V_EMPTY(s2)) count = 2;
@@ -282,6 +268,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             mbar_init(BAR(i), count);
         }
         abort_flag = 0;
+        done_count[0] = done_count[1] = 0;
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -449,77 +436,48 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }  // warp 11 only fills the producer warpgroup
     } else {
         regs_inc<kRegsSoftmax>();
-        // ------------- softmax + epilogue of both tiles, lane quarter wq, key half hf
-        const int hf = warp >> 2, wq = warp & 3;
+        // -------------------------------------- softmax + epilogue of tile u
+        const int u = warp >> 2, wq = warp & 3;
         const int r = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        constexpr int kOC = HD / 2;  // O columns of this thread's half
+        const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
         const float sl2 = P.scale_log2;
         const uint64_t sl2_2 = f2_make(sl2, sl2);
         constexpr bool cap = (MODE & 4) != 0;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         const float cap_out = P.softcap * kLog2e;
-        float* xbuf = reinterpret_cast<float*>(smem + C::kXOff);
         auto wait_warp = [&](int bar, uint32_t parity) -> bool {
             const bool rr = mbar_wait(BAR(bar), parity, P.status, ST_FWD_SOFTMAX, &abort_flag);
             return __all_sync(0xffffffffu, rr);
         };
         bool ok = true;
-        int scA = 0, scB = 0;    // S_FULL phases consumed, per tile
-        int actA = 0, actB = 0;  // items in which the tile was active so far (O_DONE phases)
-        int xc = 0;              // exchanges with the other half's warp so far
-        // The other half's value of this thread's row: each warp of the pair writes its
-        // value into the slot of the exchange's parity, arrives on the pair's barrier and
-        // waits for the partner's arrival.  A slot is written again two exchanges later,
-        // by which time the partner has read it (it arrived at the exchange in between
-        // only after reading).  A wait that runs out clears ok (and the partner's next
-        // wait ends on the abort flag), so neither warp can be left waiting.
-        // The fences order this warp's completed TMEM reads of the tile before the
-        // partner's P stores into the same columns, which follow the exchange.
-        auto exchange = [&](float v) -> float {
-            xbuf[((xc & 1) * 2 + hf) * 128 + r] = v;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(XCH(wq)));
-            ok = wait_warp(XCH(wq), xc & 1) && ok;
-            tc_fence_after();
-            const float o = xbuf[((xc & 1) * 2 + (hf ^ 1)) * 128 + r];
-            ++xc;
-            return o;
-        };
-        // One tile's softmax for this thread's 64 columns of tile u.  The 64 scores come
-        // out of TMEM into registers in one go (two loads in flight), so P can be written
+        int sc = 0;   // S_FULL(u) phases consumed
+        int act = 0;  // items in which this tile was active so far (O_DONE phases)
+        // One tile's softmax, one thread per row.  The row's 128 scores come out of
+        // TMEM into registers in one go (four loads in flight), so P can be written
         // over S chunk by chunk as it is formed.  Pass 1 takes the row max (after the
-        // invisible scores are set to -inf, in tiles that some row does not see whole)
-        // and combines it with the other half's; pass 2 forms P = exp2(x) with
-        // x = s*scale*log2(e) - m, or with the capped score
-        // softcap*tanh(s*scale/softcap)*log2(e) in place of s*scale*log2(e), pairs of
-        // scores through the f32x2 unit together.
+        // invisible scores are set to -inf, in tiles that some row does not see
+        // whole); pass 2 forms P = exp2(x) with x = s*scale*log2(e) - m, or with the
+        // capped score softcap*tanh(s*scale/softcap)*log2(e) in place of
+        // s*scale*log2(e), pairs of scores through the f32x2 unit together.
         //   The reference m (log2 units, starting at 0) moves only when P would leave
-        // [2^-2, 2^8] at the row max: a max above 2^8 (any tile), or a first visible
-        // tile whose max is below 2^-2; then O is rescaled in TMEM first (each thread
-        // its half of the columns).  For ordinary inputs this never happens.  Both
-        // threads of a row take these decisions from the same combined max (x of it
-        // through the accurate tanh), so their references stay equal.  The softcap
-        // takes the fitted tanh polynomial unless a raw score of the warp's rows and
-        // columns lies outside its range (mode 2: tanh_accurate), and the shorter one
-        // when every raw score lies inside its range (mode 3).
-        auto run_tile = [&](auto capc, int u, float& m_used, float& l, bool& seen, int k, bool full, int clo,
-                            int chi, const uint32_t(&mbits)[2], uint32_t(&sv)[2][32]) {
+        // [2^-2, 2^8] at the row max: a max above 2^8 (any tile), or a first tile whose
+        // max is below 2^-2; then O is rescaled in TMEM first.  For ordinary inputs
+        // this never happens.  The softcap takes the fitted tanh polynomial unless a
+        // raw score of the warp's rows lies outside its range (mode 2: tanh_accurate),
+        // and the shorter one when every raw score lies inside its range (mode 3).
+        auto run_tile = [&](auto capc, float& m_used, float& l, int k, bool full, int clo, int chi,
+                            const uint32_t(&mbits)[4], uint32_t(&sv)[4][32]) {
             constexpr bool kCap = decltype(capc)::value;
-            const uint32_t tS = tbase + u * 128, tO = tbase + 256 + u * HD;
             bool accurate = false, shorter = false;
             if constexpr (kCap) {
-                // largest raw |score| of the row's 64 columns, before masking
+                // largest raw |score| of the row, before masking
                 float am[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const int t = 2 * c + ((e >> 2) & 1);
-                        am[t] = max3f(am[t], fabsf(__uint_as_float(sv[c][e])), fabsf(__uint_as_float(sv[c][e + 1])));
-                        am[t] = max3f(am[t], fabsf(__uint_as_float(sv[c][e + 2])), fabsf(__uint_as_float(sv[c][e + 3])));
-                    }
+                    for (int e = 0; e < 32; e += 2)
+                        am[c] = max3f(am[c], fabsf(__uint_as_float(sv[c][e])), fabsf(__uint_as_float(sv[c][e + 1])));
                 const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
                 const CapPoly cp = cap_poly(P.scale, P.softcap);
                 accurate = __any_sync(0xffffffffu, !(amax <= cp.r_max)) || (!full && !cp.inf_ok);
@@ -527,11 +485,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 shorter = !accurate && __all_sync(0xffffffffu, amax <= cs.r_max) && (full || cs.inf_ok);
             }
             if (!full) {
-                // visibility bits of tile columns 64*hf + 32c .. +31: [clo, chi) and the key mask
+                // visibility bits of columns 32c .. 32c+31: [clo, chi) and the key mask
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int cg = 64 * hf + 32 * c;
-                    const int lo = min(max(clo - cg, 0), 32), hi = min(max(chi - cg, 0), 32);
+                for (int c = 0; c < 4; ++c) {
+                    const int lo = min(max(clo - 32 * c, 0), 32), hi = min(max(chi - 32 * c, 0), 32);
                     const uint32_t below_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
                     const uint32_t below_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
                     const uint32_t vw = below_hi & ~below_lo & mbits[c];
@@ -539,18 +496,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     for (int e = 0; e < 32; ++e) sv[c][e] = ((vw >> e) & 1u) ? sv[c][e] : 0xff800000u;  // -inf
                 }
             }
-            // pass 1: the row max of this half's scores, then of the whole row
+            // pass 1: the row max of the scores, as x against the current reference
             float rm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const int t = 2 * c + ((e >> 2) & 1);
-                    rm[t] = max3f(rm[t], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
-                    rm[t] = max3f(rm[t], __uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3]));
-                }
-            float rmax = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
-            rmax = fmaxf(rmax, exchange(rmax));
+                for (int e = 0; e < 32; e += 2)
+                    rm[c] = max3f(rm[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+            const float rmax = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
             // x is increasing in the score, so its row max is x(rmax)
             auto to_x = [&](auto modec, uint64_t rr, uint64_t nms) -> uint64_t {
                 constexpr int kMode = decltype(modec)::value;
@@ -578,40 +531,40 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 const uint64_t r2 = f2_make(rmax, rmax), n2 = f2_make(-m_used, -m_used);
                 uint64_t x2;
                 if (!kCap) x2 = to_x(std::integral_constant<int, 0>(), r2, n2);
+                else if (shorter) x2 = to_x(std::integral_constant<int, 3>(), r2, n2);
+                else if (!accurate) x2 = to_x(std::integral_constant<int, 1>(), r2, n2);
                 else x2 = to_x(std::integral_constant<int, 2>(), r2, n2);
                 f2_split(x2, xm, xm_);
             }
             if (rmax == -INFINITY) xm = -INFINITY;
-            const bool resc = xm > kRescaleHi || (!seen && xm < kRescaleLo && xm != -INFINITY);
+            const bool resc = xm > kRescaleHi || (l == 0.f && xm < kRescaleLo && xm != -INFINITY);
             if (__any_sync(0xffffffffu, resc)) {
                 // S_u(k) completed after P_u(k-1) V(k-1): O_u holds every earlier tile.
                 // Rows that have seen nothing yet hold O = 0 and keep alpha = 1 (their
                 // reference may move down by any amount).
-                const float alpha = fast_exp2(resc && seen ? -xm : 0.f);
+                const float alpha = fast_exp2(resc && l > 0.f ? -xm : 0.f);
                 if (resc) {
                     m_used += xm;
                     l *= alpha;
                 }
                 if (k > 0) {
 #pragma unroll 1
-                    for (int c = 0; c < kOC / 32; ++c) {
+                    for (int c = 0; c < HD / 32; ++c) {
                         uint32_t orr[32];
-                        tmem_ld32(tO + lane_off + hf * kOC + c * 32, orr);
+                        tmem_ld32(tO + lane_off + c * 32, orr);
                         tmem_ld_wait(orr);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                        tmem_st32(tO + lane_off + hf * kOC + c * 32, orr);
+                        tmem_st32(tO + lane_off + c * 32, orr);
                     }
                 }
             }
-            seen = seen || rmax != -INFINITY;
             // pass 2: P chunk by chunk, each 16-bit chunk stored over S as soon as formed
-            // (this half's 64 keys go to TMEM columns 32*hf .. 32*hf+31)
             auto p_pass = [&](auto modec) {
                 const uint64_t nms = f2_make(-m_used, -m_used);
                 uint64_t rs2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -623,7 +576,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                         rs2[e & 1] = f2_add(rs2[e & 1], f2_make(p0, p1));
                         pk[e] = pack2<BF16>(p0, p1);
                     }
-                    tmem_st16(tS + lane_off + 32 * hf + 16 * c, pk);
+                    tmem_st16(tS + lane_off + c * 16, pk);
                 }
                 float a0, a1, b0, b1;
                 f2_split(rs2[0], a0, a1);
@@ -635,148 +588,160 @@ __global__ void __launch_bounds__(kThreads2, 1)
             else if (!accurate) p_pass(std::integral_constant<int, 1>());
             else p_pass(std::integral_constant<int, 2>());
         };
-        for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
+        // Without a softcap at hd 128 the two tiles' softmaxes alternate A(k), B(k),
+        // A(k+1), ... within an item, so each runs while the tensor core works on the
+        // other tile's P.V and next S; left alone they fall into lockstep and the
+        // tensor core idles during both.  The longer softcap softmax (and the shorter
+        // MMAs of hd 64) do better with both warpgroups issuing at once (measured).
+        // base[u] counts tile u's softmaxes in earlier items.
+        const bool alternate = !cap && HD == 128;
+        int base[2] = {0, 0};
+        for (int kw = 0, w = snake_item(0); w < nitems; w = snake_item(++kw)) {
             const FwdItem it = fwd_item<VL>(P, w, vcur);
+            const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
+            const int bA = base[0], bB = base[1];
+            base[0] += nA;
+            base[1] += nB;
+            const int ib = it.i0 + u * BM;  // first row of this tile
+            if (ib >= it.sq.tq) continue;
             const int tq = it.sq.tq, tk = it.sq.tk;
-            // per-tile running state of this thread's row (selected by the run-time tile
-            // index, so that it stays in registers)
-            float mA = 0.f, mB = 0.f, lA = 0.f, lB = 0.f;
-            bool seenA = false, seenB = false;
-            for (int n = 0; ok && n < it.ntiles; ++n) {
-#pragma unroll 1
-                for (int u = 0; u < 2; ++u) {
-                    const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
-                    const int k = it.t0 + n - my.t0;  // index of union tile n in u's own sequence
-                    if (k < 0 || k >= my.ntiles) continue;
-                    const int ib = it.i0 + u * BM;  // first row of tile u
-                    const int i = ib + r;
-                    const int p = i + P.q_offset;
-                    const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, tq) - 1 + P.q_offset;
-                    const int j0 = (my.t0 + k) * BN;
-                    uint32_t mbits[2] = {0xffffffffu, 0xffffffffu};
-                    if (P.key_mask) {
-                        const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
+            const int i = ib + r;
+            const int p = i + P.q_offset;
+            const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, tq) - 1 + P.q_offset;
+            const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
+            float m_used = 0.f, l = 0.f;
+            for (int k = 0; k < my.ntiles; ++k) {
+                const int j0 = (my.t0 + k) * BN;
+                uint32_t mbits[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+                if (P.key_mask) {
+                    const float* mrow = P.key_mask + (long long)it.b * P.mask_bstride;
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const int j = j0 + 64 * hf + c * 32 + lane;
-                            mbits[c] = __ballot_sync(0xffffffffu, j < tk && mrow[j] > 0.5f);
-                        }
+                    for (int c = 0; c < 4; ++c) {
+                        const int j = j0 + c * 32 + lane;
+                        mbits[c] = __ballot_sync(0xffffffffu, j < tk && mrow[j] > 0.5f);
                     }
-                    // a half tile whose keys the mask keeps whole needs no mask pass
-                    const bool full = tile_full(P.wl, P.wr, tk, prow0, prow1, j0, j0 + BN) &&
-                                      (mbits[0] & mbits[1]) == 0xffffffffu;
-                    // this row's visible columns of the tile: [clo, chi)
-                    int clo = 0, chi = BN;
-                    if (!full) {
-                        chi = min(chi, tk - j0);
-                        if (P.wr >= 0) chi = min(chi, p + P.wr - j0 + 1);
-                        if (P.wl >= 0) clo = max(clo, p - P.wl - j0);
-                    }
-                    const int sc = u == 0 ? scA++ : scB++;
-                    ok = wait_warp(S_FULL(u), sc & 1) && ok;
-                    tc_fence_after();
-                    uint32_t sv[2][32];
+                }
+                // a tile whose keys the mask keeps whole needs no mask pass
+                const bool full = tile_full(P.wl, P.wr, tk, prow0, prow1, j0, j0 + BN) &&
+                                  (mbits[0] & mbits[1] & mbits[2] & mbits[3]) == 0xffffffffu;
+                // this row's visible columns of the tile: [clo, chi), and the key-mask bits
+                int clo = 0, chi = BN;
+                if (!full) {
+                    chi = min(chi, tk - j0);
+                    if (P.wr >= 0) chi = min(chi, p + P.wr - j0 + 1);
+                    if (P.wl >= 0) clo = max(clo, p - P.wl - j0);
+                }
+                if (!wait_warp(S_FULL(u), sc & 1)) {
+                    ok = false;
+                    break;
+                }
+                ++sc;
+                tc_fence_after();
+                // the row's 128 scores, loaded while this tile waits for its turn
+                uint32_t sv[4][32];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) tmem_ld32(tbase + u * 128 + lane_off + 64 * hf + c * 32, sv[c]);
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sv[c]);
+                if (alternate && (u == 0 ? (k >= 1 && k - 1 < nB) : (k < nA))) {
+                    const int need = 4 * (u == 0 ? bB + k : bA + k + 1);  // warp arrivals
+                    const bool rr = count_wait(&done_count[u ^ 1], need, P.status, ST_FWD_SOFTMAX, &abort_flag);
+                    if (!__all_sync(0xffffffffu, rr)) {
+                        tmem_ld_wait_only();
+                        ok = false;
+                        break;
+                    }
+                }
+                tmem_ld_wait_only();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
+                if (BIAS && i < tq) {  // additive score bias (never with softcap here)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) add_bias32(P, it.b, it.h, i, j0 + 32 * c, tk, sv[c]);
+                }
+                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits, sv);
+                else run_tile(std::integral_constant<bool, false>(), m_used, l, k, full, clo, chi, mbits, sv);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(BAR(P_FULL(u)));
+                    atomicAdd(&done_count[u], 1);
+                }
+            }
+            const bool have_o = ok && my.ntiles > 0 && wait_warp(O_DONE(u), act & 1);
+            if (my.ntiles > 0) ++act;
+            if (have_o) tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint32_t packed[HD / 2];
+            {
+                // all of the row's O columns in flight at once, one wait
+                uint32_t orr[HD / 32][32];
+                if (have_o) {
+#pragma unroll
+                    for (int c = 0; c < HD / 32; ++c) tmem_ld32(tO + lane_off + c * 32, orr[c]);
                     tmem_ld_wait_only();
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) tmem_pin(sv[c]);
-                    if (BIAS && i < tq) {  // additive score bias (never with softcap here)
+                    for (int c = 0; c < HD / 32; ++c) tmem_pin(orr[c]);
+                } else {
 #pragma unroll
-                        for (int c = 0; c < 2; ++c) add_bias32(P, it.b, it.h, i, j0 + 64 * hf + 32 * c, tk, sv[c]);
-                    }
-                    float m_used = u == 0 ? mA : mB, l = u == 0 ? lA : lB;
-                    bool seen = u == 0 ? seenA : seenB;
-                    // a failed wait still takes part in the pair's exchange (inside
-                    // run_tile), so that the partner is never left waiting; both then stop
-                    if (cap)
-                        run_tile(std::integral_constant<bool, true>(), u, m_used, l, seen, k, full, clo, chi, mbits, sv);
-                    else
-                        run_tile(std::integral_constant<bool, false>(), u, m_used, l, seen, k, full, clo, chi, mbits, sv);
-                    if (u == 0) {
-                        mA = m_used;
-                        lA = l;
-                        seenA = seen;
-                    } else {
-                        mB = m_used;
-                        lB = l;
-                        seenB = seen;
-                    }
-                    if (!ok) break;
-                    tmem_st_wait();
-                    tc_fence_before();
+                    for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) orr[c][e] = 0u;
+                }
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        packed[c * 16 + e] = pack2<BF16>(__uint_as_float(orr[c][2 * e]) * inv,
+                                                         __uint_as_float(orr[c][2 * e + 1]) * inv);
+            }
+            // O_u is in registers: the next item's first P.V may overwrite it
+            if (have_o) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(O_EMPTY(u)));
+            }
+            // A packed sequence's last rows may share a 32-row slice with the next
+            // sequence's first: such a slice goes out row by row (rows of this sequence
+            // only).  Dense tensors end where the map ends, which clips the tiled store.
+            const bool whole = !VL || ib + wq * 32 + 32 <= tq;
+            if (ok && (have_o || my.ntiles == 0) && !whole && i < tq) {
+                uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(P.o) +
+                                                       ((long long)it.sq.q0 + i) * P.H * HD + (long long)it.h * HD);
+#pragma unroll
+                for (int w4 = 0; w4 < HD / 8; ++w4)
+                    orow[w4] = make_uint4(packed[4 * w4], packed[4 * w4 + 1], packed[4 * w4 + 2], packed[4 * w4 + 3]);
+            }
+            if (ok && (have_o || my.ntiles == 0) && whole) {
+                // This warp's 32 rows go out through its 4 KB staging slice, 64 columns
+                // at a time, in the 128-byte-swizzled layout of the tensor map's box;
+                // one lane issues the tiled store (rows past Tq are not written).
+                const uint32_t slice = sbase + C::kStgOff + (u * 4 + wq) * 4096;
+#pragma unroll
+                for (int half = 0; half < HD / 64; ++half) {
+                    if (elect_one()) bulk_wait_read_all();  // the slice's previous store has read it
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(BAR(P_FULL(u)));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int w4 = half * 32 + 4 * j;
+                        st_shared_v4(slice + lane * 128 + ((j ^ (lane & 7)) << 4), packed[w4], packed[w4 + 1],
+                                     packed[w4 + 2], packed[w4 + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (elect_one()) {
+                        tile_store<PADH, HD>(&tmO, slice, it.h, half * 64, it.sq.q0 + ib + wq * 32, it.sq.zb);
+                        bulk_commit_group();
+                    }
                 }
             }
+            if (ok && (have_o || my.ntiles == 0) && P.lse && i < tq)
+                P.lse[((long long)it.b * P.H + it.h) * P.Tq + i] =
+                    l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
             if (!ok) break;
-            // epilogues: tile A, then tile B (whose last P.V completes meanwhile)
-#pragma unroll 1
-            for (int u = 0; u < 2; ++u) {
-                const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
-                const int ib = it.i0 + u * BM;
-                if (ib >= tq) continue;
-                const int i = ib + r;
-                const uint32_t tO = tbase + 256 + u * HD;
-                bool have_o = false;
-                if (my.ntiles > 0) {
-                    const int a = u == 0 ? actA++ : actB++;
-                    have_o = ok = wait_warp(O_DONE(u), a & 1) && ok;
-                }
-                if (have_o) tc_fence_after();
-                // the row's sum over both halves
-                const float lu = u == 0 ? lA : lB;
-                const float lt = lu + exchange(lu);
-                if (!ok) break;
-                const float m_used = u == 0 ? mA : mB;
-                const float inv = lt > 0.f ? 1.f / lt : 0.f;
-                uint32_t packed[kOC / 2];
-                {
-                    // this half's O columns in flight at once, one wait
-                    uint32_t orr[kOC / 32][32];
-                    if (have_o) {
-#pragma unroll
-                        for (int c = 0; c < kOC / 32; ++c) tmem_ld32(tO + lane_off + hf * kOC + c * 32, orr[c]);
-                        tmem_ld_wait_only();
-#pragma unroll
-                        for (int c = 0; c < kOC / 32; ++c) tmem_pin(orr[c]);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < kOC / 32; ++c)
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) orr[c][e] = 0u;
-                    }
-#pragma unroll
-                    for (int c = 0; c < kOC / 32; ++c)
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            packed[c * 16 + e] = pack2<BF16>(__uint_as_float(orr[c][2 * e]) * inv,
-                                                             __uint_as_float(orr[c][2 * e + 1]) * inv);
-                }
-                // O_u is in registers: the next item's first P.V may overwrite it
-                if (have_o) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(BAR(O_EMPTY(u)));
-                }
-                // Each thread writes its row's half of O (16-byte stores; a padded head
-                // writes only its real columns); rows past the sequence's end are not written.
-                if (i < tq) {
-                    const int ncol = min(kOC, P.hd - hf * kOC);
-                    uint4* orow = reinterpret_cast<uint4*>(
-                        reinterpret_cast<uint16_t*>(P.o) +
-                        (((long long)it.sq.zb * P.Tq + it.sq.q0 + i) * P.H + it.h) * P.hd + hf * kOC);
-#pragma unroll
-                    for (int w4 = 0; w4 < kOC / 8; ++w4)
-                        if (w4 * 8 < ncol)
-                            orow[w4] =
-                                make_uint4(packed[4 * w4], packed[4 * w4 + 1], packed[4 * w4 + 2], packed[4 * w4 + 3]);
-                    if (P.lse && hf == 0)
-                        P.lse[((long long)it.b * P.H + it.h) * P.Tq + i] =
-                            lt > 0.f ? (m_used + log2f(lt)) * 0.6931471805599453f : -INFINITY;
-                }
-            }
         }
+        // the staging slice must stay until this warp's last store has read it
+        if (elect_one()) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -804,7 +769,7 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     // (packed sequences may have fewer items than this bound: those CTAs exit at once)
     const long long items = (long long)((p.Tq + 2 * BM - 1) / (2 * BM)) * p.H * p.B;
     const unsigned grid = (unsigned)(items < nsm ? items : nsm);
-    kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v);
+    kern<<<grid, kThreads2, C::kLaunchBytes, s>>>(p, m.q, m.k, m.v, m.o);
     return cudaGetLastError();
 }
 

@@ -13,20 +13,28 @@ cudaError_t launch_simt_fwd(const Params& p, int dt, cudaStream_t s);
 cudaError_t launch_simt_bwd(const Params& p, int dt, int phases, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const Params& p, int dt, cudaStream_t s);
 
-// tcgen05 prefill forward / backward (fp16 / bf16, hd 64 or 128).  The tensor
-// maps are built by the caller.
+// tcgen05 prefill forward / backward (fp16 / bf16; hd 64 or 128, and 32 / 96 through
+// 4-D maps padded to 64 / 128).  The tensor maps are built by the caller.
 struct FwdMaps {
     CUtensorMap q, k, v;
     CUtensorMap o;  // 32-row boxes, for the epilogue's stores
 };
-cudaError_t launch_tc_fwd(const Params& p, int dt, const FwdMaps& maps, cudaStream_t s);
+cudaError_t launch_tc_fwd_bf16(const Params& p, const FwdMaps& maps, cudaStream_t s);  // fwd_tc_bf16.cu
+cudaError_t launch_tc_fwd_f16(const Params& p, const FwdMaps& maps, cudaStream_t s);   // fwd_tc_f16.cu
+inline cudaError_t launch_tc_fwd(const Params& p, int dt, const FwdMaps& maps, cudaStream_t s) {
+    return dt == 2 ? launch_tc_fwd_bf16(p, maps, s) : launch_tc_fwd_f16(p, maps, s);
+}
 struct BwdMaps {
     CUtensorMap q, dout, k, v;          // 128-row boxes
     CUtensorMap q64, dout64, k64, v64;  // 64-row boxes
     CUtensorMap o;                      // 128-row boxes (D = rowsum(dO*O) in the dQ pass)
     CUtensorMap dq32, dk32, dv32;       // 32-row boxes, for the epilogues' stores
 };
-cudaError_t launch_tc_bwd(const Params& p, int dt, const BwdMaps& maps, int phases, cudaStream_t s);
+cudaError_t launch_tc_bwd_bf16(const Params& p, const BwdMaps& maps, int phases, cudaStream_t s);  // bwd_tc_bf16.cu
+cudaError_t launch_tc_bwd_f16(const Params& p, const BwdMaps& maps, int phases, cudaStream_t s);   // bwd_tc_f16.cu
+inline cudaError_t launch_tc_bwd(const Params& p, int dt, const BwdMaps& maps, int phases, cudaStream_t s) {
+    return dt == 2 ? launch_tc_bwd_bf16(p, maps, phases, s) : launch_tc_bwd_f16(p, maps, phases, s);
+}
 
 // split-KV decode (fp16 / bf16, hd 64 or 128).
 struct DecMaps {

@@ -59,6 +59,14 @@ def test_two_sided_windows(dt, hd, wl, wr):
     run_ex(dt, 2, 300, 300, 4, 2, hd, seed=800 + hd, wl=wl, wr=wr, softcap=20.0 if wr == -1 else 0.0)
 
 
+@pytest.mark.parametrize("hd", [32, 96])
+def test_two_sided_windows_padded_heads(hd):
+    """hd 32 / 96 take the padded tensor-core kernels with a two-sided window; with a
+    bias they take the CUDA-core kernels."""
+    run_ex("bf16", 2, 300, 300, 4, 2, hd, seed=805 + hd, wl=50, wr=30)
+    run_ex("f16", 1, 200, 230, 4, 2, hd, seed=806 + hd, wl=-1, wr=20, bias=bias_of((1, 4, 200, 230), 807))
+
+
 def test_two_sided_window_with_q_offset_fp32():
     run_ex("f32", 1, 150, 190, 2, 1, 64, seed=810, wl=40, wr=10, q_offset=40)
 
