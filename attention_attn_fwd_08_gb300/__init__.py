@@ -21,7 +21,7 @@ import os
 import threading
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_rope", "attn_bwd_workspace_size", "attn_decode_workspace_size", "attn_decode_plan",
-           "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_launch_count", "AttnError", "lib",
+           "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_kernel_family_bwd", "attn_launch_count", "AttnError", "lib",
            "library_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -91,6 +91,8 @@ def lib():
         L.attn_selftest_bounded_wait.restype = i
         L.attn_kernel_family.argtypes = [i, i]
         L.attn_kernel_family.restype = i
+        L.attn_kernel_family_bwd.argtypes = [i, i]
+        L.attn_kernel_family_bwd.restype = i
         L.attn_abi_version.argtypes = []
         L.attn_abi_version.restype = i
         _lib = L
@@ -467,4 +469,10 @@ def attn_launch_count() -> int:
 
 
 def attn_kernel_family(dtype: str, hd: int) -> int:
+    """1 when attn_fwd runs (dtype, hd) on the tensor cores, 0 on the CUDA-core kernels."""
     return int(lib().attn_kernel_family(_DT[dtype], int(hd)))
+
+
+def attn_kernel_family_bwd(dtype: str, hd: int) -> int:
+    """1 when attn_bwd runs (dtype, hd) on the tensor cores, 0 on the CUDA-core kernels."""
+    return int(lib().attn_kernel_family_bwd(_DT[dtype], int(hd)))

@@ -149,6 +149,10 @@ Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, i
 bool padded_head(int hd) { return hd == 32 || hd == 96; }
 bool use_tcgen05(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 32 || hd == 64 || hd == 96 || hd == 128); }
 
+// The forward also runs 16-bit hd 256 on the tensor cores (one query tile per work
+// item, dense batches without a bias); its backward stays on the CUDA-core kernels.
+bool use_tc_fwd(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) || (dt != ATTN_F32 && hd == 256); }
+
 // Tensor map of one activation for the tensor-core kernels: 3-D at hd 64 / 128, 4-D
 // (zero-filled past the head) at hd 32 / 96.
 bool act_map(CUtensorMap* m, attn_dtype dt, const void* base, int hd, long long heads, long long rows,
@@ -211,7 +215,9 @@ const char* attn_status_string(attn_status s) {
     return "unknown status";
 }
 
-int attn_kernel_family(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) ? 1 : 0; }
+int attn_kernel_family(attn_dtype dt, int hd) { return use_tc_fwd(dt, hd) ? 1 : 0; }
+
+int attn_kernel_family_bwd(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) ? 1 : 0; }
 
 }  // extern "C"
 
@@ -232,11 +238,12 @@ attn_status fwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
     // a bias with a softcap has no tensor-core form (the cap is not linear in the raw
     // score): those calls take the CUDA-core kernels
-    if (!use_tcgen05(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd))))
+    if (!use_tc_fwd(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd) || hd == 256)))
         return counted(launch_simt_fwd(p, (int)dt, s), 1);
     FwdMaps maps;
-    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128) || !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, 128) ||
-        !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, 128) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 32))
+    const int kv_rows = hd == 256 ? 64 : 128;  // keys per tile
+    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128) || !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, kv_rows) ||
+        !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, kv_rows) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 32))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_fwd(p, (int)dt, maps, s), 1);
 }

@@ -720,6 +720,20 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
         tf = fl * wb.hd * pairs / (t[n] * 1e-3) / 1e12
         out["bias_prefill_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
                                     "visible_pairs": pairs, "note": "GQA causal prefill with a [1,1,T,T] fp32 bias"}
+    # the GQA causal prefill's width at head size 256 (forward on the tensor cores)
+    w2 = synth.WORKLOADS["gqa_prefill_hd256"]
+    i2 = synth.make_inputs(w2)
+    q2, k2, v2 = (i2[n].to(dev) for n in ("q", "k", "v"))
+    o2 = torch.empty_like(q2)
+    l2 = torch.empty((w2.B, w2.H, w2.Tq), dtype=torch.float32, device=dev)
+    kw2 = dict(H=w2.H, Hkv=w2.Hkv, scale=w2.scale, causal=True)
+    t = time_passes(torch, stream, [("fwd", lambda: A.attn_fwd(q2, k2, v2, o=o2, lse=l2, **kw2))], args, flush_buf)
+    pairs = visible_pairs(w2)
+    tf = 4 * w2.hd * pairs / (t["fwd"] * 1e-3) / 1e12
+    out["hd256_prefill_fwd"] = {"ms": t["fwd"], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                "visible_pairs": pairs,
+                                "note": "B=4 T=2048 H=16 Hkv=4 hd=256 causal bf16 forward (tensor cores)"}
+    del q2, k2, v2, o2, l2
     # rotary embedding of the GQA prefill q and k (HBM-bound: each element read and written once)
     rq, rk = q.clone(), k.clone()
     t = time_passes(torch, stream, [("rope", lambda: (A.attn_rope(rq, H=wb.H, pos=0), A.attn_rope(rk, H=wb.Hkv, pos=0)))],

@@ -88,11 +88,12 @@ typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
  *   B, Tq, Tk : batch, query rows, key rows (>= 0; B or Tq == 0 is a no-op,
  *               Tk == 0 writes O = 0, LSE = -inf).
  *   H, Hkv    : query / KV heads, Hkv >= 1 divides H.
- *   hd        : head dim 32, 64, 96, 128 or 256.  16-bit types at 32, 64, 96 and 128
- *               run on the tensor cores (32 and 96 as 64 and 128 with the columns past
- *               the head read as zeros; with an additive bias or in packed sequences
- *               they take the CUDA-core kernels); fp32 and hd 256 run on CUDA-core
- *               kernels (same results, no tensor-core speed).
+ *   hd        : head dim 32, 64, 96, 128 or 256.  16-bit types run on the tensor
+ *               cores (32 and 96 as 64 and 128 with the columns past the head read as
+ *               zeros; 256 with one 128-row query tile per work item; with an additive
+ *               bias, or in packed sequences, 32, 96 and 256 take the CUDA-core
+ *               kernels); fp32 runs on CUDA-core kernels (same results, no tensor-core
+ *               speed).  attn_bwd at hd 256 runs on the CUDA-core kernels.
  *   scale     : > 0 and finite (1/sqrt(hd) in the usual case).
  *   causal    : 0/1.   window : >= 0, 0 = unbounded.   softcap : >= 0, 0 = off.
  *   q_offset  : >= 0, absolute position of query row 0.
@@ -356,8 +357,14 @@ ATTN_API attn_status attn_get_device_status(void* stream, unsigned int* detail);
  */
 ATTN_API attn_status attn_selftest_bounded_wait(unsigned int timeout_us, void* stream);
 
-/* Which kernel family attn_fwd / attn_bwd use for (dt, hd): 0 = SIMT fp32, 1 = tcgen05. */
+/* Which kernel family attn_fwd (and attn_fwd_ex without a bias) uses for (dt, hd):
+ * 0 = CUDA-core kernels, 1 = tcgen05 tensor cores.  16-bit hd 32, 64, 96, 128 and 256
+ * run on the tensor cores. */
 ATTN_API int attn_kernel_family(attn_dtype dt, int hd);
+
+/* The same for attn_bwd: 16-bit hd 32, 64, 96 and 128 run on the tensor cores, hd 256
+ * on the CUDA-core kernels. */
+ATTN_API int attn_kernel_family_bwd(attn_dtype dt, int hd);
 
 /* Running total of kernels this library has enqueued in this process. */
 ATTN_API unsigned long long attn_launch_count(void);

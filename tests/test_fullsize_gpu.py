@@ -188,3 +188,13 @@ def test_bias_prefill_fwd_bwd_full():
             compare_grads((dq[b:b + 1, r0:r1, kvh * G * hd:(kvh + 1) * G * hd], dk[b:b + 1, r0:r1, kvh * hd:(kvh + 1) * hd],
                            dv[b:b + 1, r0:r1, kvh * hd:(kvh + 1) * hd]),
                           (gq, gk[:, r0:r1], gv[:, r0:r1]), w.dtype, what)
+
+
+def test_gqa_prefill_hd256_fwd_full():
+    """The hd 256 forward at its benchmark size: sampled blocks of two groups."""
+    w = synth.WORKLOADS["gqa_prefill_hd256"]
+    inp = synth.make_inputs(w)
+    gpu = run_gpu(w, inp)
+    T = w.Tq
+    sample_block(w, inp, gpu, 0, 0, 0, 200, 0, 200)
+    sample_block(w, inp, gpu, 3, 3, T - 300, T, 0, T)

@@ -346,14 +346,39 @@ def test_guard_bands_untouched():
     assert (big[:pad] == 9.0).all() and (big[pad + n:] == 9.0).all()
 
 
-# hd 32 and 96 run on the tensor cores in 16 bits (padded), hd 256 and fp32 on the
-# CUDA-core kernels.
+# In 16 bits hd 32 and 96 run on the tensor cores (padded), hd 256's forward too (one
+# query tile per work item) and its backward on the CUDA-core kernels; fp32 runs on
+# the CUDA-core kernels.
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("hd", [32, 96, 256])
 def test_other_head_sizes_fwd_bwd(dt, hd):
-    tc = dt != "f32" and hd != 256
-    assert A.attn_kernel_family({"bf16": "bfloat16", "f32": "float32"}[dt], hd) == (1 if tc else 0)
+    name = {"bf16": "bfloat16", "f32": "float32"}[dt]
+    assert A.attn_kernel_family(name, hd) == (1 if dt != "f32" else 0)
+    assert A.attn_kernel_family_bwd(name, hd) == (1 if dt != "f32" and hd != 256 else 0)
     run_fwd_case(dt, 2, 150, 150, 4, 2, hd, causal=True, window=60, softcap=20.0, backward=True, seed=950 + hd)
+
+
+HD256_FLAGS = [
+    dict(causal=True),
+    dict(causal=False),
+    dict(causal=True, window=100, softcap=30.0),
+    dict(causal=False, softcap=3.0, mask="batch"),
+    dict(causal=True, mask="holes"),
+    dict(causal=True, q_offset=90, window=200),
+]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("flags", HD256_FLAGS, ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_fwd_hd256_tensor_core(dt, flags):
+    """The hd 256 forward: several 64-key tiles and 128-row items, ragged tails, GQA."""
+    Tq = 333
+    run_fwd_case(dt, 2, Tq, Tq + flags.get("q_offset", 0), 4, 2, 256, seed=990, **flags)
+
+
+def test_fwd_hd256_many_items_per_cta():
+    # more 128-row items (3 x 32 x 3) than SMs: every CTA of the persistent kernel runs several
+    run_fwd_case("bf16", 3, 300, 300, 32, 8, 256, causal=True, seed=995)
 
 
 @pytest.mark.parametrize("hd", [32, 96])
