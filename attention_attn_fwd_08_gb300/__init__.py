@@ -21,7 +21,7 @@ import os
 import threading
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_rope", "attn_bwd_workspace_size", "attn_decode_workspace_size", "attn_decode_plan",
-           "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_kernel_family_bwd", "attn_launch_count", "AttnError", "lib",
+           "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_kernel_family_bwd", "attn_fwd_rope", "attn_bwd_rope", "attn_fwd_rope_workspace_size", "attn_bwd_rope_workspace_size", "attn_launch_count", "AttnError", "lib",
            "library_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -93,6 +93,15 @@ def lib():
         L.attn_kernel_family.restype = i
         L.attn_kernel_family_bwd.argtypes = [i, i]
         L.attn_kernel_family_bwd.restype = i
+        L.attn_fwd_rope_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+        L.attn_fwd_rope_workspace_size.restype = sz
+        L.attn_fwd_rope.argtypes = [i, vp, vp, vp, vp, vp, vp, sz] + [i] * 6 + [f, i, i, f, i, vp, ll, i, f, vp]
+        L.attn_fwd_rope.restype = i
+        L.attn_bwd_rope_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        L.attn_bwd_rope_workspace_size.restype = sz
+        L.attn_bwd_rope.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz] + [i] * 6 + [f, i, i, f, i, vp, ll,
+                                                                                           i, f, vp]
+        L.attn_bwd_rope.restype = i
         L.attn_abi_version.argtypes = []
         L.attn_abi_version.restype = i
         _lib = L
@@ -242,6 +251,69 @@ def attn_bwd(q, k, v, o, do, lse, *, H, Hkv, scale=None, causal=False, window=0,
                                B, Tq, Tk, H, Hkv, hd, float(scale), int(bool(causal)), int(window), float(softcap),
                                int(q_offset), _ptr(m), int(ms), _stream(stream), int(phases))
     _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_fwd_rope_workspace_size(dtype, B, Tq, Tk, H, Hkv, hd, q_offset=0) -> int:
+    return int(lib().attn_fwd_rope_workspace_size(_DT[dtype], B, Tq, Tk, H, Hkv, hd, int(q_offset)))
+
+
+def attn_fwd_rope(q, k, v, *, H, Hkv, scale=None, causal=False, window=0, softcap=0.0, q_offset=0, key_mask=None,
+                  rope_pos=0, rope_theta=10000.0, o=None, lse=None, want_lse=True, workspace=None, stream=None):
+    """Forward attention on the rotary-embedded q and k (q and k are passed unrotated and
+    left unchanged): query row i turns at position rope_pos + q_offset + i, key j at
+    rope_pos + j.  Returns (o, lse)."""
+    torch = _torch()
+    _contig(q, k, v, o, lse)
+    B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o)], like_k=[("k", k), ("v", v)], k=k, f32=[("lse", lse, (B, H, Tq))],
+            device=[("key_mask", key_mask), ("workspace", workspace)])
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    name = str(q.dtype).split(".")[-1]
+    if workspace is None:
+        nbytes = attn_fwd_rope_workspace_size(name, B, Tq, Tk, H, Hkv, hd, q_offset)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    st = lib().attn_fwd_rope(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), B, Tq, Tk, H, Hkv, hd, float(scale),
+                             int(bool(causal)), int(window), float(softcap), int(q_offset), _ptr(m), int(ms),
+                             int(rope_pos), float(rope_theta), _stream(stream))
+    _check(st, "attn_fwd_rope")
+    return o, lse
+
+
+def attn_bwd_rope_workspace_size(dtype, B, Tq, Tk, H, Hkv, hd) -> int:
+    return int(lib().attn_bwd_rope_workspace_size(_DT[dtype], B, Tq, Tk, H, Hkv, hd))
+
+
+def attn_bwd_rope(q, k, v, o, do, lse, *, H, Hkv, scale=None, causal=False, window=0, softcap=0.0, q_offset=0,
+                  key_mask=None, rope_pos=0, rope_theta=10000.0, dq=None, dk=None, dv=None, workspace=None,
+                  stream=None):
+    """Backward of attn_fwd_rope (same arguments; o and lse from that call): returns
+    (dq, dk, dv), the gradients of the unrotated q and k, overwritten."""
+    torch = _torch()
+    _contig(q, k, v, o, do, lse, dq, dk, dv)
+    B, Tq, Tk, hd = _dims(q, k, H, Hkv)
+    _placed(q, like_q=[("o", o), ("do", do), ("dq", dq)], like_k=[("k", k), ("v", v), ("dk", dk), ("dv", dv)], k=k,
+            f32=[("lse", lse, (B, H, Tq))], device=[("key_mask", key_mask), ("workspace", workspace)])
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    name = str(q.dtype).split(".")[-1]
+    if workspace is None:
+        nbytes = attn_bwd_rope_workspace_size(name, B, Tq, Tk, H, Hkv, hd)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    m, ms = _mask(key_mask, B, Tk)
+    st = lib().attn_bwd_rope(_dt(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, Tq, Tk, H,
+                             Hkv, hd, float(scale), int(bool(causal)), int(window), float(softcap), int(q_offset),
+                             _ptr(m), int(ms), int(rope_pos), float(rope_theta), _stream(stream))
+    _check(st, "attn_bwd_rope")
     return dq, dk, dv
 
 

@@ -519,7 +519,137 @@ attn_status attn_rope(attn_dtype dt, void* x, int B, int T, int H, int hd, int p
     if (B == 0 || T == 0) return ATTN_OK;
     if (!x || !aligned16(x)) return ATTN_ERR_INVALID_ARG;
     if ((long long)B * T > (long long)INT32_MAX * 8) return ATTN_ERR_UNSUPPORTED;
-    return counted(launch_rope(x, (int)dt, B, T, H, hd, pos, (double)theta, static_cast<cudaStream_t>(stream)), 1);
+    return counted(
+        launch_rope(x, x, (int)dt, B, T, H, hd, pos, (double)theta, false, static_cast<cudaStream_t>(stream)), 1);
+}
+
+}  // extern "C"
+
+// --------------------------------------------------- rotary embedding fused
+namespace {
+
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// rotary positions the table covers: query row i sits at q_offset + i, key j at j
+long long rope_npos(int Tq, int Tk, int q_offset) {
+    const long long a = (long long)q_offset + Tq;
+    return a > Tk ? a : Tk;
+}
+
+// the forward turns the query tiles inside the kernel (16-bit, hd 64 / 128); other
+// types and head sizes turn q into the workspace first
+bool rope_in_kernel(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 64 || hd == 128); }
+
+bool rope_args_ok(attn_dtype dt, int hd, int rope_pos, float theta) {
+    if (rope_pos < 0 || !(theta > 0.f) || !isfinite(theta)) return false;
+    (void)dt;
+    return hd % 4 == 0 && hd >= 4 && hd <= 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_fwd_rope_workspace_size(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd, int q_offset) {
+    if (B < 0 || Tq < 0 || Tk < 0 || H <= 0 || Hkv <= 0 || hd <= 0 || q_offset < 0) return 0;
+    const size_t es = elem_size(dt);
+    size_t n = align256((size_t)B * Tk * Hkv * hd * es);  // rotated k
+    if (rope_in_kernel(dt, hd)) n += align256((size_t)rope_npos(Tq, Tk, q_offset) * hd * sizeof(float));
+    else n += align256((size_t)B * Tq * H * hd * es);  // rotated q
+    return n;
+}
+
+attn_status attn_fwd_rope(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse,
+                          void* workspace, size_t workspace_bytes, int B, int Tq, int Tk, int H, int Hkv, int hd,
+                          float scale, int causal, int window, float softcap, int q_offset, const float* key_mask,
+                          long long key_mask_bstride, int rope_pos, float rope_theta, void* stream) {
+    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    if (!rope_args_ok(dt, hd, rope_pos, rope_theta)) return ATTN_ERR_INVALID_ARG;
+    if ((long long)rope_pos + rope_npos(Tq, Tk, q_offset) > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    if (B == 0 || Tq == 0) return ATTN_OK;
+    Params p = base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                           key_mask_bstride);
+    if (Tk == 0) return fwd_launch(dt, q, k, v, o, lse, p, stream);
+    if (!workspace || !aligned16(workspace) || !k || !q ||
+        workspace_bytes < attn_fwd_rope_workspace_size(dt, B, Tq, Tk, H, Hkv, hd, q_offset))
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k)) return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t es = elem_size(dt);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* k_rot = ws;
+    uint8_t* rest = ws + align256((size_t)B * Tk * Hkv * hd * es);
+    // keys at rotary positions rope_pos + j
+    if (launch_rope(k, k_rot, (int)dt, B, Tk, Hkv, hd, rope_pos, (double)rope_theta, false, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (rope_in_kernel(dt, hd)) {
+        float* tab = reinterpret_cast<float*>(rest);
+        const int npos = (int)rope_npos(Tq, Tk, q_offset);
+        if (launch_rope_table(tab, npos, hd, rope_pos, (double)rope_theta, s) != cudaSuccess) return ATTN_ERR_CUDA;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        p.rope_tab = tab;
+        p.rope_npos = npos;
+        return fwd_launch(dt, q, k_rot, v, o, lse, p, stream);
+    }
+    // queries at rotary positions rope_pos + q_offset + i, turned into the workspace
+    void* q_rot = rest;
+    if (launch_rope(q, q_rot, (int)dt, B, Tq, H, hd, rope_pos + q_offset, (double)rope_theta, false, s) !=
+        cudaSuccess)
+        return ATTN_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return fwd_launch(dt, q_rot, k_rot, v, o, lse, p, stream);
+}
+
+size_t attn_bwd_rope_workspace_size(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd) {
+    if (B < 0 || Tq < 0 || Tk < 0 || H <= 0 || Hkv <= 0 || hd <= 0) return 0;
+    const size_t es = elem_size(dt);
+    return align256((size_t)B * Tq * H * hd * es) + align256((size_t)B * Tk * Hkv * hd * es) +
+           align256(attn_bwd_workspace_size(B, Tq, H));
+}
+
+attn_status attn_bwd_rope(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                          size_t workspace_bytes, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
+                          int causal, int window, float softcap, int q_offset, const float* key_mask,
+                          long long key_mask_bstride, int rope_pos, float rope_theta, void* stream) {
+    attn_status st = check_common(dt, B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                                  key_mask_bstride);
+    if (st != ATTN_OK) return st;
+    if (!rope_args_ok(dt, hd, rope_pos, rope_theta)) return ATTN_ERR_INVALID_ARG;
+    if ((long long)rope_pos + rope_npos(Tq, Tk, q_offset) > INT32_MAX) return ATTN_ERR_INVALID_ARG;
+    if (B == 0) return ATTN_OK;
+    Params p = base_params(B, Tq, Tk, H, Hkv, hd, scale, causal, window, softcap, q_offset, key_mask,
+                           key_mask_bstride);
+    if (Tq == 0 || Tk == 0)  // no visible pair: zero gradients, nothing to turn
+        return bwd_launch(dt, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, p, stream, 7);
+    if (!workspace || !aligned16(workspace) || !q || !k || !dq || !dk ||
+        workspace_bytes < attn_bwd_rope_workspace_size(dt, B, Tq, Tk, H, Hkv, hd))
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(dq) || !aligned16(dk)) return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t es = elem_size(dt);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* q_rot = ws;
+    void* k_rot = ws + align256((size_t)B * Tq * H * hd * es);
+    void* ws_bwd = static_cast<uint8_t*>(k_rot) + align256((size_t)B * Tk * Hkv * hd * es);
+    // the forward's rotated operands, the backward on them, then the gradients turned
+    // back (dL/dq = R^T dL/d(Rq): the inverse turn at the same positions)
+    if (launch_rope(q, q_rot, (int)dt, B, Tq, H, hd, rope_pos + q_offset, (double)rope_theta, false, s) !=
+            cudaSuccess ||
+        launch_rope(k, k_rot, (int)dt, B, Tk, Hkv, hd, rope_pos, (double)rope_theta, false, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    g_launches.fetch_add(2, std::memory_order_relaxed);
+    st = bwd_launch(dt, q_rot, k_rot, v, o, dout, lse, dq, dk, dv, ws_bwd, attn_bwd_workspace_size(B, Tq, H), p,
+                    stream, 7);
+    if (st != ATTN_OK) return st;
+    if (launch_rope(dq, dq, (int)dt, B, Tq, H, hd, rope_pos + q_offset, (double)rope_theta, true, s) != cudaSuccess ||
+        launch_rope(dk, dk, (int)dt, B, Tk, Hkv, hd, rope_pos, (double)rope_theta, true, s) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    g_launches.fetch_add(2, std::memory_order_relaxed);
+    return ATTN_OK;
 }
 
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

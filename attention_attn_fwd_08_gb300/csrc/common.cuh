@@ -51,6 +51,11 @@ struct Params {
     const int* cu_q;
     const int* cu_k;
     int total_q, total_k;  // packed: rows of q/o and of k/v (no access goes past them)
+    // rotary embedding of the query tiles inside the forward (or NULL): cosine and
+    // sine of rotary position s (query row i sits at s = q_offset + i) and pair
+    // index c at rope_tab[2 * (c * rope_npos + s)], [+1]; rope_npos positions
+    const float* rope_tab;
+    int rope_npos;
     unsigned int* status;
 };
 
@@ -169,6 +174,16 @@ __device__ __forceinline__ void add_bias32(const Params& P, int b, int h, int i,
             if (j0 + e < tk)
                 s[e] = __float_as_uint(fmaf(__ldg(row + (long long)(j0 + e) * P.bias_sk), inv, __uint_as_float(s[e])));
     }
+}
+
+// ------------------------------------------------------------ rotary turn
+// Rotate-half RoPE turn of the pair (a, b) = (x[i], x[i + hd/2]) by the angle whose
+// cosine and sine are c and s (the inverse turn passes -s).  Written out with fmaf
+// so that every kernel that rotates (the standalone pass, the forward's Q tiles)
+// rounds alike.
+__device__ __forceinline__ void rope_turn(float a, float b, float c, float s, float& lo, float& hi) {
+    lo = fmaf(a, c, -(b * s));
+    hi = fmaf(b, c, a * s);
 }
 
 // ------------------------------------------------------------ visibility

@@ -111,7 +111,7 @@ struct Fwd2Cfg {
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKVBytes;
     static constexpr int kBarOff = kVOff + kStages * kKVBytes;
-    static constexpr int kNumBars = 13 + 4 * kStages;
+    static constexpr int kNumBars = 15 + 4 * kStages;
     // epilogue staging: one 32-row x 64-column slice (4 KB) per softmax warp
     static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
     static constexpr int kStgBytes = 8 * 32 * 128;
@@ -213,13 +213,18 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c)
 // an additive score bias; MODE & 4: softcap; MODE & 8: a head size below HD (96 in a
 // 128 kernel, 32 in a 64 kernel) read and written through 4-D maps whose boxes reach
 // past the head (the extra columns load as zeros, add nothing to q.k or P.V, and are
-// never stored).  Each instantiation carries only its own bookkeeping.
+// never stored); MODE & 16: rotary embedding of the query tiles in shared memory
+// (dense batches): the softmax warps of a tile turn their rows' pairs (x[c],
+// x[c + hd/2]) by the angles of P.rope_tab once the tile lands, and the MMA warp
+// waits for that (Q_ROT) instead of the load.  Each instantiation carries only its
+// own bookkeeping.
 template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
-    constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
+    constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0, ROPE = (MODE & 16) != 0;
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
+    static_assert(!(ROPE && (VL || BIAS || PADH)), "the fused rotation is built for dense batches at hd 64 / 128");
     using C = Fwd2Cfg<HD>;
     constexpr int NS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     auto O_DONE = [&](int u) { return 8 + 4 * NS + u; };   // the item's last P.V of tile u completed
     auto O_EMPTY = [&](int u) { return 10 + 4 * NS + u; };  // the epilogue has read O_u out of TMEM
     const int MMA_DONE = 12 + 4 * NS;
+    auto Q_ROT = [&](int u) { return 13 + 4 * NS + u; };  // Q tile u rotated in shared memory (4 warps)
     // softmaxes finished by tile u, counted per warp (exact counts: a tile with no work
     // in an item lets the other run several softmaxes ahead, which mbarrier parity
     // could not tell apart)
@@ -260,7 +266,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == P_FULL(0) || i == P_FULL(1) || i == O_EMPTY(0) || i == O_EMPTY(1)) count = 4;
+            if (i == P_FULL(0) || i == P_FULL(1) || i == O_EMPTY(0) || i == O_EMPTY(1) || i == Q_ROT(0) ||
+                i == Q_ROT(1))
+                count = 4;
             // stage releases and the teardown barrier: one arrival per MMA issuer
             for (int s2 = 0; s2 < NS; ++s2)
                 if (i == K_EMPTY(s2) || i == V_EMPTY(s2)) count = 2;
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 // releases count arrivals, not issuers: a chain commits a tile's release
                 // only after it has waited for that tile's data phase (also for tiles it
                 // skips), so an arrival can never belong to a later use of the stage.
-                if (on && !wait_all(Q_FULL(u), act & 1)) {
+                if (on && !wait_all(ROPE ? Q_ROT(u) : Q_FULL(u), act & 1)) {
                     ok = false;
                     break;
                 }
@@ -596,7 +604,62 @@ __global__ void __launch_bounds__(kThreads2, 1)
         // base[u] counts tile u's softmaxes in earlier items.
         const bool alternate = !cap && HD == 128;
         int base[2] = {0, 0};
-        for (int kw = 0, w = snake_item(0); w < nitems; w = snake_item(++kw)) {
+        // Fused rotary embedding: turn this thread's row of tile u's Q in shared memory
+        // once the tile of item w2 has landed, then release it to the MMA warp.  Pairs
+        // (c, c + hd/2) sit in the same 16-byte chunk slot of the two 64-column boxes
+        // (hd 128) or four chunks apart in the one box (hd 64).
+        int qr = 0;        // Q tiles of this tile slot rotated so far
+        int rot_kw = -1;   // position (in this CTA's item sequence) of the last rotated item
+        auto rotate_q = [&](int kw2) -> bool {
+            const FwdItem it2 = fwd_item<VL>(P, snake_item(kw2), vcur);
+            const TileInfo my2 = u == 0 ? it2.tu[0] : it2.tu[1];
+            if (it2.ntiles == 0 || my2.ntiles == 0) return true;  // the tile is not loaded for this item
+            if (!wait_warp(Q_FULL(u), qr & 1)) return false;
+            ++qr;
+            const int i2 = it2.i0 + u * BM + r;
+            if (i2 < it2.sq.tq) {
+                // cosine and sine of pair c at this row's position: tab2[c * npos + s]
+                const float2* tcol = reinterpret_cast<const float2*>(P.rope_tab) + (P.q_offset + i2);
+                uint8_t* qrow = smem + C::kQOff + u * C::kQBytes + r * 128;
+#pragma unroll
+                for (int j = 0; j < HD / 16; ++j) {
+                    uint4* pa = reinterpret_cast<uint4*>(qrow + ((j ^ (r & 7)) << 4));
+                    uint4* pb = reinterpret_cast<uint4*>(HD == 128 ? qrow + BM * 128 + ((j ^ (r & 7)) << 4)
+                                                                   : qrow + (((j + 4) ^ (r & 7)) << 4));
+                    uint4 a = *pa, b = *pb;
+                    uint32_t* aw = reinterpret_cast<uint32_t*>(&a);
+                    uint32_t* bw = reinterpret_cast<uint32_t*>(&b);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 c0 = __ldg(tcol + (long long)(8 * j + 2 * e) * P.rope_npos);
+                        const float2 c1 = __ldg(tcol + (long long)(8 * j + 2 * e + 1) * P.rope_npos);
+                        const float4 cs = make_float4(c0.x, c0.y, c1.x, c1.y);  // pairs 8j+2e and 8j+2e+1
+                        float a0, a1, b0, b1, ra0, ra1, rb0, rb1;
+                        if constexpr (BF16) {
+                            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+                            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
+                            a0 = fa.x; a1 = fa.y; b0 = fb.x; b1 = fb.y;
+                        } else {
+                            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&aw[e]));
+                            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&bw[e]));
+                            a0 = fa.x; a1 = fa.y; b0 = fb.x; b1 = fb.y;
+                        }
+                        rope_turn(a0, b0, cs.x, cs.y, ra0, rb0);
+                        rope_turn(a1, b1, cs.z, cs.w, ra1, rb1);
+                        aw[e] = pack2<BF16>(ra0, ra1);
+                        bw[e] = pack2<BF16>(rb0, rb1);
+                    }
+                    *pa = a;
+                    *pb = b;
+                }
+            }
+            fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(Q_ROT(u)));
+            rot_kw = kw2;
+            return true;
+        };
+        for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
             const FwdItem it = fwd_item<VL>(P, w, vcur);
             const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
             const int bA = base[0], bB = base[1];
@@ -609,6 +672,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const int p = i + P.q_offset;
             const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, tq) - 1 + P.q_offset;
             const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
+            if constexpr (ROPE) {
+                // this item's Q, unless the previous item's end already turned it
+                if (my.ntiles > 0 && rot_kw != kw && !rotate_q(kw)) {
+                    ok = false;
+                    break;
+                }
+            }
             float m_used = 0.f, l = 0.f;
             for (int k = 0; k < my.ntiles; ++k) {
                 const int j0 = (my.t0 + k) * BN;
@@ -666,6 +736,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     mbar_arrive(BAR(P_FULL(u)));
                     atomicAdd(&done_count[u], 1);
                 }
+            }
+            if constexpr (ROPE) {
+                // the next item's Q lands once this item's last S of the tile completed:
+                // turn it now, so that its first S need not wait for this epilogue
+                if (ok && snake_item(kw + 1) < nitems && !rotate_q(kw + 1)) ok = false;
             }
             const bool have_o = ok && my.ntiles > 0 && wait_warp(O_DONE(u), act & 1);
             if (my.ntiles > 0) ++act;
@@ -756,7 +831,9 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     using C = Fwd2Cfg<HD>;
     const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
     // a head size below HD (dense batches without a bias only) runs the padded instantiations
-    auto kern = p.hd != HD ? (c ? fwd_tc2_kernel<BF16, HD, 12> : fwd_tc2_kernel<BF16, HD, 8>)
+    // the rotary query turn (dense batches at hd 64 / 128) runs the MODE & 16 instantiations
+    auto kern = p.rope_tab  ? (c ? fwd_tc2_kernel<BF16, HD, 20> : fwd_tc2_kernel<BF16, HD, 16>)
+                : p.hd != HD ? (c ? fwd_tc2_kernel<BF16, HD, 12> : fwd_tc2_kernel<BF16, HD, 8>)
                 : p.cu_q   ? (c ? fwd_tc2_kernel<BF16, HD, 5> : fwd_tc2_kernel<BF16, HD, 1>)
                 : p.bias   ? fwd_tc2_kernel<BF16, HD, 2>
                            : (c ? fwd_tc2_kernel<BF16, HD, 4> : fwd_tc2_kernel<BF16, HD, 0>);

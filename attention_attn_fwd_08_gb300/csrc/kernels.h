@@ -49,7 +49,11 @@ cudaError_t decode_noalloc_scratch(float** out);
 
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned int timeout_us, cudaStream_t s);
 
-// rotate-half rotary embedding in place over [B][T][H*hd] (hd 8 .. 256, a multiple of 4)
-cudaError_t launch_rope(void* x, int dt, int B, int T, int H, int hd, int pos, double theta, cudaStream_t s);
+// rotate-half rotary embedding of src [B][T][H*hd] into dst (src == dst: in place), hd 8 .. 256
+// a multiple of 4; inverse turns every pair the other way
+cudaError_t launch_rope(const void* src, void* dst, int dt, int B, int T, int H, int hd, int pos, double theta,
+                        bool inverse, cudaStream_t s);
+// cosine/sine table of rotary positions pos .. pos+npos-1 for the forward's fused rotation
+cudaError_t launch_rope_table(float* tab, int npos, int hd, int pos, double theta, cudaStream_t s);
 
 }  // namespace attn

@@ -1,4 +1,5 @@
-// rope.cu -- rotate-half rotary embedding, applied in place before attention.
+// rope.cu -- rotate-half rotary embedding, applied before attention (in place, or
+// into another buffer), and the cosine/sine table the forward's fused rotation reads.
 //
 // Source: ferrotensor engine/attention.rs, rope / rope_theta: every head vector
 // of token s (counted within its sequence) gets position pos + s, and its pair
@@ -53,9 +54,10 @@ __device__ __forceinline__ void pair_sincos(double p, double f, float* s, float*
 }
 constexpr int kHeadsPerThread = 4;
 
-// grid.x: blocks of blockDim.y tokens; threadIdx.x: pair index / 2
+// grid.x: blocks of blockDim.y tokens; threadIdx.x: pair index / 2.  Reads src and
+// writes dst (the same array for the in-place pass); sgn = -1 turns the other way.
 template <typename T>
-__global__ void rope_kernel(T* x, long long tokens, int T_, int H, int hd, int pos,
+__global__ void rope_kernel(const T* src, T* dst, long long tokens, int T_, int H, int hd, int pos, float sgn,
                             const __grid_constant__ RopeFreqs fr) {
     using P2 = Pair2<T>;
     const long long tok = (long long)blockIdx.x * blockDim.y + threadIdx.y;
@@ -66,22 +68,27 @@ __global__ void rope_kernel(T* x, long long tokens, int T_, int H, int hd, int p
     float s0, c0, s1, c1;
     pair_sincos<T>(p, fr.inv_freq[i], &s0, &c0);
     pair_sincos<T>(p, fr.inv_freq[i + 1], &s1, &c1);
-    typename P2::V* row = reinterpret_cast<typename P2::V*>(x + tok * (long long)H * hd);
+    s0 *= sgn;
+    s1 *= sgn;
+    const typename P2::V* irow = reinterpret_cast<const typename P2::V*>(src + tok * (long long)H * hd);
+    typename P2::V* orow = reinterpret_cast<typename P2::V*>(dst + tok * (long long)H * hd);
     const int h1 = min(H, (int)(blockIdx.y + 1) * kHeadsPerThread);
 #pragma unroll 4
     for (int h = blockIdx.y * kHeadsPerThread; h < h1; ++h) {
-        typename P2::V* lo = row + (h * hd + i) / 2;
-        typename P2::V* hi = row + (h * hd + i + half) / 2;
-        const float2 a = P2::to_f2(*lo), b = P2::to_f2(*hi);
-        *lo = P2::from_f2(make_float2(a.x * c0 - b.x * s0, a.y * c1 - b.y * s1));
-        *hi = P2::from_f2(make_float2(b.x * c0 + a.x * s0, b.y * c1 + a.y * s1));
+        const int lo = (h * hd + i) / 2, hi = (h * hd + i + half) / 2;
+        const float2 a = P2::to_f2(irow[lo]), b = P2::to_f2(irow[hi]);
+        float2 ra, rb;
+        rope_turn(a.x, b.x, c0, s0, ra.x, rb.x);
+        rope_turn(a.y, b.y, c1, s1, ra.y, rb.y);
+        orow[lo] = P2::from_f2(ra);
+        orow[hi] = P2::from_f2(rb);
     }
 }
 
 // The same with 16-byte accesses: a thread owns VEC consecutive pairs indices i0 ..
 // (used when hd/2 is a multiple of VEC, so both halves stay 16-byte aligned).
 template <typename T>
-__global__ void rope_vec_kernel(T* x, long long tokens, int T_, int H, int hd, int pos,
+__global__ void rope_vec_kernel(const T* src, T* dst, long long tokens, int T_, int H, int hd, int pos, float sgn,
                                 const __grid_constant__ RopeFreqs fr) {
     using P2 = Pair2<T>;
     constexpr int VEC = 16 / (int)sizeof(T);
@@ -91,55 +98,91 @@ __global__ void rope_vec_kernel(T* x, long long tokens, int T_, int H, int hd, i
     const double p = (double)pos + (int)(tok % T_);
     float sn[VEC], cs[VEC];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) pair_sincos<T>(p, fr.inv_freq[i0 + e], &sn[e], &cs[e]);
-    T* row = x + tok * (long long)H * hd;
+    for (int e = 0; e < VEC; ++e) {
+        pair_sincos<T>(p, fr.inv_freq[i0 + e], &sn[e], &cs[e]);
+        sn[e] *= sgn;
+    }
+    const T* irow = src + tok * (long long)H * hd;
+    T* orow = dst + tok * (long long)H * hd;
     const int h1 = min(H, (int)(blockIdx.y + 1) * kHeadsPerThread);
 #pragma unroll 2
     for (int h = blockIdx.y * kHeadsPerThread; h < h1; ++h) {
-        uint4* lo = reinterpret_cast<uint4*>(row + h * hd + i0);
-        uint4* hi = reinterpret_cast<uint4*>(row + h * hd + i0 + half);
         union U {
             uint4 u;
             typename P2::V v[VEC / 2];
         } ua, ub;
-        ua.u = *lo;
-        ub.u = *hi;
+        ua.u = *reinterpret_cast<const uint4*>(irow + h * hd + i0);
+        ub.u = *reinterpret_cast<const uint4*>(irow + h * hd + i0 + half);
 #pragma unroll
         for (int e = 0; e < VEC / 2; ++e) {
             const float2 a = P2::to_f2(ua.v[e]), b = P2::to_f2(ub.v[e]);
-            const float c0 = cs[2 * e], s0 = sn[2 * e], c1 = cs[2 * e + 1], s1 = sn[2 * e + 1];
-            ua.v[e] = P2::from_f2(make_float2(a.x * c0 - b.x * s0, a.y * c1 - b.y * s1));
-            ub.v[e] = P2::from_f2(make_float2(b.x * c0 + a.x * s0, b.y * c1 + a.y * s1));
+            float2 ra, rb;
+            rope_turn(a.x, b.x, cs[2 * e], sn[2 * e], ra.x, rb.x);
+            rope_turn(a.y, b.y, cs[2 * e + 1], sn[2 * e + 1], ra.y, rb.y);
+            ua.v[e] = P2::from_f2(ra);
+            ub.v[e] = P2::from_f2(rb);
         }
-        *lo = ua.u;
-        *hi = ub.u;
+        *reinterpret_cast<uint4*>(orow + h * hd + i0) = ua.u;
+        *reinterpret_cast<uint4*>(orow + h * hd + i0 + half) = ub.u;
     }
 }
 
-template <typename T>
-cudaError_t rope_typed(void* x, int B, int T_, int H, int hd, int pos, double theta, cudaStream_t st) {
+// Cosine and sine of rotary position s (angle (pos + s) * theta^(-2c/hd)) for every
+// pair index c < hd/2: tab[2 * (c * npos + s)] = cos, [+1] = sin (consecutive
+// positions adjacent, so that threads holding consecutive rows read one line); the
+// angle is formed exactly as the 16-bit pass forms it, so that a table-driven turn
+// equals that pass.
+__global__ void rope_table_kernel(float* tab, int npos, int half, int pos, const __grid_constant__ RopeFreqs fr) {
+    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= (long long)npos * half) return;
+    const int c = (int)(e / npos), s = (int)(e % npos);
+    float sn, cs;
+    pair_sincos<__half>((double)pos + s, fr.inv_freq[c], &sn, &cs);
+    tab[2 * e] = cs;
+    tab[2 * e + 1] = sn;
+}
+
+RopeFreqs freqs(int hd, double theta) {
     RopeFreqs fr;
     for (int i = 0; i < hd / 2; ++i) fr.inv_freq[i] = pow(theta, -2.0 * i / hd);
+    return fr;
+}
+
+template <typename T>
+cudaError_t rope_typed(const void* src, void* dst, int B, int T_, int H, int hd, int pos, double theta, float sgn,
+                       cudaStream_t st) {
+    const RopeFreqs fr = freqs(hd, theta);
     const long long tokens = (long long)B * T_;
     constexpr int VEC = 16 / (int)sizeof(T);
     if ((hd / 2) % VEC == 0) {
         const dim3 block(hd / 2 / VEC, 256 / (hd / 2 / VEC));
         const dim3 grid((unsigned)((tokens + block.y - 1) / block.y), (H + kHeadsPerThread - 1) / kHeadsPerThread);
-        rope_vec_kernel<T><<<grid, block, 0, st>>>(static_cast<T*>(x), tokens, T_, H, hd, pos, fr);
+        rope_vec_kernel<T><<<grid, block, 0, st>>>(static_cast<const T*>(src), static_cast<T*>(dst), tokens, T_, H,
+                                                    hd, pos, sgn, fr);
     } else {
         const dim3 block(hd / 4, 256 / (hd / 4));
         const dim3 grid((unsigned)((tokens + block.y - 1) / block.y), (H + kHeadsPerThread - 1) / kHeadsPerThread);
-        rope_kernel<T><<<grid, block, 0, st>>>(static_cast<T*>(x), tokens, T_, H, hd, pos, fr);
+        rope_kernel<T><<<grid, block, 0, st>>>(static_cast<const T*>(src), static_cast<T*>(dst), tokens, T_, H, hd,
+                                               pos, sgn, fr);
     }
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_rope(void* x, int dt, int B, int T_, int H, int hd, int pos, double theta, cudaStream_t s) {
-    if (dt == 0) return rope_typed<float>(x, B, T_, H, hd, pos, theta, s);
-    if (dt == 1) return rope_typed<__half>(x, B, T_, H, hd, pos, theta, s);
-    return rope_typed<__nv_bfloat16>(x, B, T_, H, hd, pos, theta, s);
+cudaError_t launch_rope(const void* src, void* dst, int dt, int B, int T_, int H, int hd, int pos, double theta,
+                        bool inverse, cudaStream_t s) {
+    const float sgn = inverse ? -1.f : 1.f;
+    if (dt == 0) return rope_typed<float>(src, dst, B, T_, H, hd, pos, theta, sgn, s);
+    if (dt == 1) return rope_typed<__half>(src, dst, B, T_, H, hd, pos, theta, sgn, s);
+    return rope_typed<__nv_bfloat16>(src, dst, B, T_, H, hd, pos, theta, sgn, s);
+}
+
+cudaError_t launch_rope_table(float* tab, int npos, int hd, int pos, double theta, cudaStream_t s) {
+    const long long n = (long long)npos * (hd / 2);
+    if (n == 0) return cudaSuccess;
+    rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(tab, npos, hd / 2, pos, freqs(hd, theta));
+    return cudaGetLastError();
 }
 
 }  // namespace attn

@@ -742,6 +742,21 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
     out["rope_qk"] = {"ms": t["rope"], "GB/s": nbytes / (t["rope"] * 1e-3) / 1e9,
                       "frac_of_hbm_peak": nbytes / (t["rope"] * 1e-3) / 1e9 / peaks["hbm"], "bytes_per_call": nbytes,
                       "note": "rotate-half RoPE of q [4,2048,32*128] and k [4,2048,8*128] bf16, in place (two launches)"}
+    # rotary embedding fused into the forward against the standalone turn of q and k then the forward
+    wsr = torch.empty(A.attn_fwd_rope_workspace_size("bfloat16", wb.B, wb.Tq, wb.Tk, wb.H, wb.Hkv, wb.hd),
+                      dtype=torch.uint8, device=dev)
+    kwr = dict(H=wb.H, Hkv=wb.Hkv, scale=wb.scale, causal=True)
+    t = time_passes(torch, stream, [
+        ("fused", lambda: A.attn_fwd_rope(q, k, v, o=o, lse=lse, workspace=wsr, rope_pos=0, **kwr)),
+        ("split", lambda: (A.attn_rope(rq, H=wb.H, pos=0), A.attn_rope(rk, H=wb.Hkv, pos=0),
+                           A.attn_fwd(rq, rk, v, o=o, lse=lse, **kwr)))], args, flush_buf)
+    pairs = visible_pairs(wb)
+    for n in ("fused", "split"):
+        tf = 4 * wb.hd * pairs / (t[n] * 1e-3) / 1e12
+        out["rope_fwd_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                "note": "GQA causal prefill with rotate-half RoPE of q and k: " +
+                                        ("attn_fwd_rope (query tiles turned in the forward, keys in one pass)"
+                                         if n == "fused" else "attn_rope of q and k, then attn_fwd (three launches)")}
     st, word = A.attn_get_device_status()
     if st != A.OK:
         raise RuntimeError("device status word %#x after the masked workloads" % word)

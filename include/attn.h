@@ -336,6 +336,44 @@ ATTN_API attn_status attn_decode_noalloc(attn_dtype dt, const void* q, const voi
 ATTN_API attn_status attn_rope(attn_dtype dt, void* x, int B, int T, int H, int hd, int pos, float theta,
                         void* stream);
 
+/*
+ * Attention on rotary-embedded queries and keys, for callers that keep q and k
+ * unrotated.  Source: ferrotensor engine/attention.rs, rope / rope_theta (the
+ * rotate-half turn applied to q and k before flash attention), with the turn of
+ * attn_rope: pair (x[c], x[c + hd/2]) of a head vector at rotary position t turns
+ * by t * rope_theta^(-2c/hd).  Query row i sits at rotary position
+ * rope_pos + q_offset + i and key j at rope_pos + j, the positions the causal and
+ * window rules use, shifted by rope_pos >= 0.
+ *   attn_fwd_rope : O and LSE of attention on the turned q and k; q and k are not
+ *                   modified.  16-bit hd 64 / 128 turn the query tiles inside the
+ *                   forward kernel (from a cosine/sine table in the workspace);
+ *                   the keys are turned into the workspace first (one pass over k).
+ *                   Other types and head sizes turn q into the workspace too.  The
+ *                   result equals attn_rope on q and k followed by attn_fwd, bit for
+ *                   bit.  workspace: at least attn_fwd_rope_workspace_size() bytes,
+ *                   16-byte aligned; contents on entry are ignored.
+ *   attn_bwd_rope : the gradients of the unrotated q and k (dq = R^T dq', dk =
+ *                   R^T dk' for the turned operands' gradients dq', dk') and dv,
+ *                   overwritten; o and lse come from attn_fwd_rope with the same
+ *                   arguments.  It turns q and k into the workspace, runs the
+ *                   backward on them and turns dq and dk back in place.  workspace:
+ *                   at least attn_bwd_rope_workspace_size() bytes, 16-byte aligned.
+ *   rope_theta > 0 and finite; hd a multiple of 4.  The rest as attn_fwd / attn_bwd.
+ */
+ATTN_API size_t attn_fwd_rope_workspace_size(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd,
+                        int q_offset);
+ATTN_API attn_status attn_fwd_rope(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, int B, int Tq, int Tk, int H,
+                        int Hkv, int hd, float scale, int causal, int window, float softcap, int q_offset,
+                        const float* key_mask, long long key_mask_bstride, int rope_pos, float rope_theta,
+                        void* stream);
+ATTN_API size_t attn_bwd_rope_workspace_size(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, int hd);
+ATTN_API attn_status attn_bwd_rope(attn_dtype dt, const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                        size_t workspace_bytes, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,
+                        int causal, int window, float softcap, int q_offset, const float* key_mask,
+                        long long key_mask_bstride, int rope_pos, float rope_theta, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 ATTN_API const char* attn_status_string(attn_status s);
 
