@@ -196,6 +196,34 @@ __device__ __forceinline__ bool visible(const Params& P, int b, int p, int j, in
     return true;
 }
 
+// Keys of batch b that a key mask can keep: [lo, hi) covers every key j < tk with
+// mask > 0.5 (lo = hi when there is none).  Called by a whole warp: lane l scans its
+// own stretch of ceil(tk/32) keys, and the stretches holding a kept key bound the
+// span, so the result may include masked keys at its ends but never leaves a kept
+// key out.  Kernels use it to skip key tiles a prefix (or suffix) mask removes.
+__device__ __forceinline__ int2 mask_span(const Params& P, int b, int tk) {
+    const int lane = threadIdx.x & 31;
+    const int seg = (tk + 127) / 128 * 4;  // a multiple of 4 keys per lane
+    const float* row = P.key_mask + (long long)b * P.mask_bstride;
+    bool any = false;
+    const int j0 = lane * seg, j1 = min(tk, j0 + seg);
+    // independent loads (no early exit), four keys at a time when the row allows
+    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && j1 - j0 == seg) {
+        const float4* r4 = reinterpret_cast<const float4*>(row + j0);
+        for (int e = 0; e < seg / 4; ++e) {
+            const float4 m = __ldg(r4 + e);
+            any = any || (m.x > 0.5f) || (m.y > 0.5f) || (m.z > 0.5f) || (m.w > 0.5f);
+        }
+    } else {
+        for (int j = j0; j < j1; ++j) any = any || (__ldg(row + j) > 0.5f);
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, any);
+    if (bal == 0u) return make_int2(0, 0);
+    const int first = __ffs(bal) - 1, last = 31 - __clz(bal);
+    return make_int2(first * seg, min(tk, (last + 1) * seg));
+}
+constexpr int kMaskSpanMax = 64;  // batches whose spans a kernel keeps in shared memory
+
 // Range of keys [lo, hi) that any query with position in [p0, p1] can see,
 // before the key mask: the window [p - wl, p + wr] (-1 = unbounded side).
 __host__ __device__ __forceinline__ void key_range(int wl, int wr, int Tk, int p0, int p1, int* lo, int* hi) {

@@ -64,12 +64,15 @@ __device__ __forceinline__ uint64_t cap_g_short(const CapShort& cs, uint64_t r) 
     return f2_fma(r, f2_mul(u, f2_fma(u, cs.s1, cs.s0)), r);
 }
 
-// key tiles the query tile at rows i0 .. of a sequence of tq queries and tk keys sees
-__device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, int tk) {
+// key tiles the query tile at rows i0 .. of a sequence of tq queries and tk keys sees,
+// within the span of keys the key mask keeps (span.y <= span.x: none)
+__device__ __forceinline__ TileInfo tile_range(const Params& P, int i0, int tq, int tk, int2 span) {
     const int p0 = i0 + P.q_offset;
     const int p1 = min(i0 + BM, tq) - 1 + P.q_offset;
     int lo, hi;
     key_range(P.wl, P.wr, tk, p0, p1, &lo, &hi);
+    lo = max(lo, span.x);
+    hi = min(hi, span.y);
     TileInfo t;
     t.t0 = lo / BN;
     t.ntiles = hi > lo ? (hi + BN - 1) / BN - t.t0 : 0;
@@ -132,8 +135,9 @@ struct FwdItem {
 
 // The item of query block cq (rows 256*cq ..) of head h in sequence b; an item
 // that is not valid has no rows.
+// kspan: the key-mask spans of the batches (shared memory), or NULL for none
 template <bool VL>
-__device__ __forceinline__ FwdItem make_item(const Params& P, int b, int h, int cq, bool valid) {
+__device__ __forceinline__ FwdItem make_item(const Params& P, int b, int h, int cq, bool valid, const int2* kspan) {
     FwdItem it;
     it.h = h;
     it.b = b;
@@ -142,8 +146,9 @@ __device__ __forceinline__ FwdItem make_item(const Params& P, int b, int h, int 
     it.sq = seq_of<VL>(P, it.b);
     if (!valid) it.sq.tq = 0;
     it.hasB = it.i0 + BM < it.sq.tq;
-    it.tu[0] = it.i0 < it.sq.tq ? tile_range(P, it.i0, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
-    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM, it.sq.tq, it.sq.tk) : TileInfo{0, 0};
+    const int2 span = kspan ? kspan[b] : make_int2(0, it.sq.tk);
+    it.tu[0] = it.i0 < it.sq.tq ? tile_range(P, it.i0, it.sq.tq, it.sq.tk, span) : TileInfo{0, 0};
+    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM, it.sq.tq, it.sq.tk, span) : TileInfo{0, 0};
     int t0 = it.tu[0].t0, t1 = it.tu[0].t0 + it.tu[0].ntiles;
     if (it.tu[1].ntiles > 0) {
         if (it.tu[0].ntiles == 0) {
@@ -196,17 +201,17 @@ __device__ __forceinline__ FwdItem vl_item(const Params& P, VlCursor& c, int w) 
     unsigned m = c.seqs;
     for (int t = 0; t < j && m; ++t) m &= m - 1;
     const bool valid = r >= 0 && r < __popc(c.seqs) * P.H && m != 0u;
-    return make_item<true>(P, valid ? __ffs(m) - 1 : 0, valid ? r - j * P.H : 0, c.level, valid);
+    return make_item<true>(P, valid ? __ffs(m) - 1 : 0, valid ? r - j * P.H : 0, c.level, valid, nullptr);
 }
 
 template <bool VL>
-__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c) {
+__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c, const int2* kspan) {
     if constexpr (VL) {
         if (P.B <= kVlCompact) return vl_item(P, c, w);
     }
     const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
     const int hb = w % (P.H * P.B);
-    return make_item<VL>(P, hb / P.H, hb % P.H, ncq - 1 - w / (P.H * P.B), true);
+    return make_item<VL>(P, hb / P.H, hb % P.H, ncq - 1 - w / (P.H * P.B), true, kspan);
 }
 
 // MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
@@ -253,6 +258,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
     __shared__ int done_count[2];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Key-mask spans per batch (dense batches of at most kMaskSpanMax): key tiles a
+    // mask removes entirely at the ends of a row are never loaded or multiplied.  Each
+    // warp scans the batches w, w + 12, ...; the spans are read after the block-wide
+    // barrier below.
+    __shared__ int2 kspan_s[kMaskSpanMax];
+    const int2* kspan = (!VL && P.key_mask && P.B <= kMaskSpanMax) ? kspan_s : nullptr;
+    if (kspan)
+        for (int b = warp; b < P.B; b += kThreads2 / 32) {
+            const int2 sp = mask_span(P, b, P.Tk);
+            if (lane == 0) kspan_s[b] = sp;
+        }
     VlCursor vcur = {};
     int nitems = fwd_items(P);
     if constexpr (VL) {
@@ -301,7 +317,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int gk = 0, gv = 0;   // K and V tiles loaded so far (ring positions)
             int qn[2] = {0, 0};   // Q tiles loaded so far, per tile slot
             for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-                const FwdItem it = fwd_item<VL>(P, w, vcur);
+                const FwdItem it = fwd_item<VL>(P, w, vcur, kspan);
                 if (it.ntiles == 0) continue;
                 for (int u = 0; ok && u < 2; ++u) {
                     if (!active(it, u)) continue;
@@ -371,7 +387,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int pc = 0;   // P_FULL(u) phases consumed
             int act = 0;  // items in which this tile was active so far
             for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-                const FwdItem it = fwd_item<VL>(P, w, vcur);
+                const FwdItem it = fwd_item<VL>(P, w, vcur, kspan);
                 if (it.ntiles == 0) continue;
                 const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
                 const bool on = active(it, u);
@@ -611,7 +627,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         int qr = 0;        // Q tiles of this tile slot rotated so far
         int rot_kw = -1;   // position (in this CTA's item sequence) of the last rotated item
         auto rotate_q = [&](int kw2) -> bool {
-            const FwdItem it2 = fwd_item<VL>(P, snake_item(kw2), vcur);
+            const FwdItem it2 = fwd_item<VL>(P, snake_item(kw2), vcur, kspan);
             const TileInfo my2 = u == 0 ? it2.tu[0] : it2.tu[1];
             if (it2.ntiles == 0 || my2.ntiles == 0) return true;  // the tile is not loaded for this item
             if (!wait_warp(Q_FULL(u), qr & 1)) return false;
@@ -660,7 +676,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             return true;
         };
         for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-            const FwdItem it = fwd_item<VL>(P, w, vcur);
+            const FwdItem it = fwd_item<VL>(P, w, vcur, kspan);
             const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
             const int bA = base[0], bB = base[1];
             base[0] += nA;
