@@ -27,6 +27,7 @@
 //   TMEM: S 0/64, dP 128/192, dQ 256, Q 256+hd, dO 256+hd+hd/2.
 #include <math.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #pragma once
@@ -104,10 +105,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int MMA_DONE = 6 + 2 * NS;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // 1-D grid, longest first: causally the first key blocks are seen by the most queries
-    const int kb = (int)(blockIdx.x % (unsigned)(P.Hkv * P.B));
-    const int kvh = kb % P.Hkv, b = kb / P.Hkv;
-    const int j0 = (int)(blockIdx.x / (unsigned)(P.Hkv * P.B)) * BKV;
+    // 1-D grid over chunks of kv_chunk (batch, KV head) pairs, and inside a chunk key
+    // blocks longest first (causally the first key blocks are seen by the most
+    // queries): the CTAs that stream the same Q and dO tiles run together while L2
+    // still holds them, and the light blocks of one chunk overlap the next chunk
+    const int ng = P.Hkv * P.B, nkb = (int)gridDim.x / ng;
+    const int CH = P.kv_chunk > 0 ? min(P.kv_chunk, ng) : ng;
+    const int cidx = (int)blockIdx.x / (nkb * CH), ch = min(CH, ng - cidx * CH);
+    const int within = (int)blockIdx.x - cidx * nkb * CH;
+    const int kg = cidx * CH + within % ch;
+    const int kvh = kg % P.Hkv, b = kg / P.Hkv;
+    const int j0 = (within / ch) * BKV;
     const Seq sq = seq_of<VL>(P, b);
     if (j0 >= sq.tk) return;  // (packed) past this sequence's keys: nothing to write
     int qlo, qhi;
@@ -1040,7 +1048,12 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         const unsigned grid = (unsigned)((p.Tk + 127) / 128) * p.Hkv * p.B;
-        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(p, m.q64, m.k, m.v, m.dout64, m.dk32, m.dv32);
+        // about 32 MB of Q and dO per chunk of (batch, KV head) pairs
+        Params pc = p;
+        const long long per = 2LL * p.G * p.Tq * p.hd * 2;
+        // (packed sequences differ in length: their key blocks keep one global order)
+        pc.kv_chunk = p.cu_q ? 0 : (int)std::max(1LL, std::min<long long>(p.Hkv * p.B, (32LL << 20) / std::max(per, 1LL)));
+        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(pc, m.q64, m.k, m.v, m.dout64, m.dk32, m.dv32);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

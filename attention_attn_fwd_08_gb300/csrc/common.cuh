@@ -31,6 +31,7 @@ struct Params {
     float* ndelta;       // backward: -D = -rowsum(dO*O)     [B*H][tq_pad]
     float* nlse2;        // backward: -LSE*log2(e), -inf where LSE = -inf  [B*H][tq_pad]
     int tq_pad;          // backward: Tq rounded up to 64 (row stride of ndelta / nlse2)
+    int kv_chunk;        // backward dK/dV: (batch, KV head) pairs whose key blocks are numbered together (0: all)
     float* ws;           // decode: split partials
     const float* key_mask;
     long long mask_bstride;

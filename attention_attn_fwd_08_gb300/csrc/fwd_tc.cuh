@@ -204,12 +204,25 @@ __device__ __forceinline__ FwdItem vl_item(const Params& P, VlCursor& c, int w) 
     return make_item<true>(P, valid ? __ffs(m) - 1 : 0, valid ? r - j * P.H : 0, c.level, valid, nullptr);
 }
 
-template <bool VL>
-__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c, const int2* kspan) {
+// KORD: dense key-masked batches with their spans in kspan and kord the batches by
+// kept span, longest first.  Without a window every query block of a batch sees
+// the same key tiles, so a batch's items run together, the longest spans first;
+// otherwise each level of query blocks takes its batches in that order.
+template <bool VL, bool KORD = false>
+__device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c, const int2* kspan,
+                                            const unsigned char* kord = nullptr) {
     if constexpr (VL) {
         if (P.B <= kVlCompact) return vl_item(P, c, w);
     }
     const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
+    if constexpr (KORD) {
+        if (P.wl < 0 && P.wr < 0) {
+            const int per = P.H * ncq, rem = w % per;
+            return make_item<VL>(P, kord[w / per], rem % P.H, rem / P.H, true, kspan);
+        }
+        const int hb = w % (P.H * P.B);
+        return make_item<VL>(P, kord[hb / P.H], hb % P.H, ncq - 1 - w / (P.H * P.B), true, kspan);
+    }
     const int hb = w % (P.H * P.B);
     return make_item<VL>(P, hb / P.H, hb % P.H, ncq - 1 - w / (P.H * P.B), true, kspan);
 }
@@ -222,12 +235,15 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c,
 // (dense batches): the softmax warps of a tile turn their rows' pairs (x[c],
 // x[c + hd/2]) by the angles of P.rope_tab once the tile lands, and the MMA warp
 // waits for that (Q_ROT) instead of the load.  Each instantiation carries only its
-// own bookkeeping.
+// own bookkeeping.  MODE & 32: dense key-masked batches (at most kMaskSpanMax of
+// them), the items numbered by the batches' kept key spans, longest first.
 template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0, ROPE = (MODE & 16) != 0;
+    constexpr bool KORD = (MODE & 32) != 0;
+    static_assert(!(KORD && (MODE & 31) != 0), "the span order is built for plain dense key-masked batches");
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
     static_assert(!(ROPE && (VL || BIAS || PADH)), "the fused rotation is built for dense batches at hd 64 / 128");
     using C = Fwd2Cfg<HD>;
@@ -262,7 +278,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
     // mask removes entirely at the ends of a row are never loaded or multiplied.  Each
     // warp scans the batches w, w + 12, ...; the spans are read after the block-wide
     // barrier below.
-    __shared__ int2 kspan_s[kMaskSpanMax];
+    // (KORD: the batch order in the 64 bytes past the spans)
+    __shared__ int2 kspan_s[kMaskSpanMax + (KORD ? kMaskSpanMax / 8 : 0)];
+    unsigned char* kord_s = reinterpret_cast<unsigned char*>(kspan_s + kMaskSpanMax);
     const int2* kspan = (!VL && P.key_mask && P.B <= kMaskSpanMax) ? kspan_s : nullptr;
     if (kspan)
         for (int b = warp; b < P.B; b += kThreads2 / 32) {
@@ -302,6 +320,19 @@ __global__ void __launch_bounds__(kThreads2, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (KORD) {
+        // rank the batches by kept span, longest first (ties by index)
+        if ((int)threadIdx.x < P.B) {
+            const int b = threadIdx.x, len = kspan_s[b].y - kspan_s[b].x;
+            int rank = 0;
+            for (int b2 = 0; b2 < P.B; ++b2) {
+                const int l2 = kspan_s[b2].y - kspan_s[b2].x;
+                rank += (l2 > len || (l2 == len && b2 < b)) ? 1 : 0;
+            }
+            kord_s[rank] = (unsigned char)b;
+        }
+        __syncthreads();
+    }
     const uint32_t tbase = *tmem_slot;
     if (warp >= 8) {
         regs_dec<kRegsProducer>();
@@ -317,7 +348,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int gk = 0, gv = 0;   // K and V tiles loaded so far (ring positions)
             int qn[2] = {0, 0};   // Q tiles loaded so far, per tile slot
             for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-                const FwdItem it = fwd_item<VL>(P, w, vcur, kspan);
+                const FwdItem it = fwd_item<VL, KORD>(P, w, vcur, kspan, kord_s);
                 if (it.ntiles == 0) continue;
                 for (int u = 0; ok && u < 2; ++u) {
                     if (!active(it, u)) continue;
@@ -387,7 +418,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int pc = 0;   // P_FULL(u) phases consumed
             int act = 0;  // items in which this tile was active so far
             for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-                const FwdItem it = fwd_item<VL>(P, w, vcur, kspan);
+                const FwdItem it = fwd_item<VL, KORD>(P, w, vcur, kspan, kord_s);
                 if (it.ntiles == 0) continue;
                 const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
                 const bool on = active(it, u);
@@ -627,7 +658,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         int qr = 0;        // Q tiles of this tile slot rotated so far
         int rot_kw = -1;   // position (in this CTA's item sequence) of the last rotated item
         auto rotate_q = [&](int kw2) -> bool {
-            const FwdItem it2 = fwd_item<VL>(P, snake_item(kw2), vcur, kspan);
+            const FwdItem it2 = fwd_item<VL, KORD>(P, snake_item(kw2), vcur, kspan, kord_s);
             const TileInfo my2 = u == 0 ? it2.tu[0] : it2.tu[1];
             if (it2.ntiles == 0 || my2.ntiles == 0) return true;  // the tile is not loaded for this item
             if (!wait_warp(Q_FULL(u), qr & 1)) return false;
@@ -676,7 +707,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             return true;
         };
         for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-            const FwdItem it = fwd_item<VL>(P, w, vcur, kspan);
+            const FwdItem it = fwd_item<VL, KORD>(P, w, vcur, kspan, kord_s);
             const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
             const int bA = base[0], bB = base[1];
             base[0] += nA;
@@ -852,7 +883,9 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
                 : p.hd != HD ? (c ? fwd_tc2_kernel<BF16, HD, 12> : fwd_tc2_kernel<BF16, HD, 8>)
                 : p.cu_q   ? (c ? fwd_tc2_kernel<BF16, HD, 5> : fwd_tc2_kernel<BF16, HD, 1>)
                 : p.bias   ? fwd_tc2_kernel<BF16, HD, 2>
-                           : (c ? fwd_tc2_kernel<BF16, HD, 4> : fwd_tc2_kernel<BF16, HD, 0>);
+                : c        ? fwd_tc2_kernel<BF16, HD, 4>
+                : p.key_mask && p.B <= kMaskSpanMax ? fwd_tc2_kernel<BF16, HD, 32>
+                                                    : fwd_tc2_kernel<BF16, HD, 0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kLaunchBytes);
     if (e != cudaSuccess) return e;
     int dev = 0, nsm = 0;
