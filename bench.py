@@ -284,7 +284,8 @@ def workload_config(w):
 # Each case makes one workload's inputs on cuda:0 and returns the calls of one
 # repetition, in order.  Kernel launches per repetition (for a profiler's
 # --launch-skip): gqa_prefill 3 (fwd, dQ, dK/dV); swa_softcap, varlen_packed and
-# bias_prefill 3 (fwd, dQ, dK/dV); encoder_mask 1; decode_lq4 2 (split, combine).
+# bias_prefill 3 (fwd, dQ, dK/dV); encoder_mask 1; decode_lq4 2 (split, combine);
+# gqa_prefill_hd256 1; rope_prefill 3 (turn of k, cos/sin table, fwd).
 def _case_dense(A, synth, torch, dev, name, fwd_only=False, bias=False):
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w)
@@ -334,6 +335,18 @@ def _case_decode(A, synth, torch, dev):
                                   workspace=ws)]
 
 
+def _case_rope(A, synth, torch, dev):
+    w = synth.WORKLOADS["gqa_prefill"]
+    inp = synth.make_inputs(w)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Tq), dtype=torch.float32, device=dev)
+    ws = torch.empty(A.attn_fwd_rope_workspace_size("bfloat16", w.B, w.Tq, w.Tk, w.H, w.Hkv, w.hd), dtype=torch.uint8,
+                     device=dev)
+    return [lambda: A.attn_fwd_rope(q, k, v, o=o, lse=lse, workspace=ws, H=w.H, Hkv=w.Hkv, scale=w.scale,
+                                    causal=True)]
+
+
 PROFILE_CASES = {
     "gqa_prefill": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill"),
     "swa_softcap": lambda A, s, t, d: _case_dense(A, s, t, d, "swa_softcap"),
@@ -341,6 +354,8 @@ PROFILE_CASES = {
     "bias_prefill": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill", bias=True),
     "varlen_packed": lambda A, s, t, d: _case_varlen(A, s, t, d),
     "decode_lq4": lambda A, s, t, d: _case_decode(A, s, t, d),
+    "gqa_prefill_hd256": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill_hd256", fwd_only=True),
+    "rope_prefill": lambda A, s, t, d: _case_rope(A, s, t, d),
 }
 
 
