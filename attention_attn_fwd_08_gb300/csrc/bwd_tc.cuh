@@ -37,7 +37,10 @@
 namespace attn {
 namespace {
 
-constexpr int kThreads = 192;    // dK/dV: 4 compute warps, producer, MMA
+// dK/dV: compute warps (four, one key row per thread; eight with a softcap, two
+// per key row splitting each tile's query columns), then the producer and the MMA warp
+__host__ __device__ constexpr int dkdv_compute_warps(int mode) { return (mode & 4) ? 8 : 4; }
+__host__ __device__ constexpr int dkdv_threads(int mode) { return 32 * (dkdv_compute_warps(mode) + 2); }
 constexpr int kThreadsDQ = 384;
 // dQ registers: the eight compute warps take 184, the producers and MMA issuers 136
 // (256*184 + 128*136 = 64512 = 384 threads at launch * 168)
@@ -66,10 +69,11 @@ struct KVCfg {
     static constexpr int kStatOff = kGOff + kStages * kQBytes;  // [stage][2][BQ] floats: -LSE*log2e, -D
     static constexpr int kStatBytes = 2 * BQ * 4;
     static constexpr int kBarOff = kStatOff + kStages * kStatBytes;
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
-    // epilogue staging: two 32-row x 64-column slices (4 KB each) per compute warp
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1 + 1;
+    // epilogue staging: 32-row x 64-column slices of 4 KB, two per compute warp
+    // (one with eight compute warps)
     static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
-    static constexpr int kBytes = kStgOff + 4 * 8192;
+    static constexpr int kBytes = kStgOff + 8 * 4096;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
@@ -79,12 +83,14 @@ struct KVCfg {
 // instantiation carries only its own bookkeeping (the softcap's registers, live through
 // the tile loop, made the plain path spill when it was a run-time branch).
 template <bool BF16, int HD, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(dkdv_threads(MODE), 1)
     bwd_dkdv_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV) {
     using C = KVCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BKV = C::BKV;
+    constexpr int NCW = dkdv_compute_warps(MODE), HF = NCW / 4;  // HF warps per key row
+    constexpr int PRODUCER = NCW, MMA = NCW + 1;
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
     extern __shared__ uint8_t smem_raw[];
@@ -103,6 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto PT_FULL = [&](int b) { return 3 + 2 * NS + b; };
     const int ACC_DONE = 5 + 2 * NS;
     const int MMA_DONE = 6 + 2 * NS;
+    const int LD_DONE = 7 + 2 * NS;  // the compute warps have read S^T/dP^T of a tile (HF = 2)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 1-D grid over chunks of kv_chunk (batch, KV head) pairs, and inside a chunk key
@@ -127,11 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tile_i0 = [&](int n) { return (qt0 + n % max(nqt, 1)) * BQ; };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kNumBars; ++i) mbar_init(BAR(i), (i == PT_FULL(0) || i == PT_FULL(1)) ? 4 : 1);
+        for (int i = 0; i < C::kNumBars; ++i)
+            mbar_init(BAR(i), (i == PT_FULL(0) || i == PT_FULL(1) || i == LD_DONE) ? NCW : 1);
         abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == MMA) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = *tmem_slot;
     const uint32_t tDV = tbase + 256, tDK = tbase + 256 + HD;
 
-    if (warp == 4) {
+    if (warp == PRODUCER) {
         // producer and MMA issuer run as whole warps; one elected lane issues
         if (ntiles > 0) {
             if (elect_one()) {
@@ -187,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = max(0, issued - NS); n < issued; ++n)
                 mbar_wait(BAR(Q_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == MMA) {
         if (ntiles > 0) {
             constexpr uint32_t idS = idesc_f16(BF16, BKV, BQ, false, false);
             constexpr uint32_t idAcc = idesc_f16(BF16, BKV, HD, false, true);
@@ -247,23 +255,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
     } else {
-        // ------------------------------------------------ compute: one key row per thread
-        const int r = warp * 32 + lane;
+        // ------------ compute: warp w owns TMEM lane quarter w % 4 (one key row per
+        // thread); with HF = 2, warps w and w+4 split each tile's 64 query columns (hf)
+        const int wq = warp & 3, hf = warp >> 2;
+        const int r = wq * 32 + lane;
         const int j = j0 + r;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const bool key_live = j < sq.tk && (!P.key_mask || P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f);
         constexpr bool cap = (MODE & 4) != 0;
+        constexpr int kc = BQ / HF;  // query columns per thread
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         const uint64_t sl2_2 = f2_make(P.scale_log2, P.scale_log2), one2 = f2_make(1.f, 1.f);
         bool ok = true;
         for (int n = 0; n < ntiles; ++n) {
             const int bf = n & 1;
             const int h = tile_head(n), i0 = tile_i0(n);
-            // visible query columns of this key row in the tile
-            int clo = 0, chi = min(BQ, sq.tq - i0);
+            const int c0 = kc * hf;  // this thread's first query column of the tile
+            // visible query columns of this key row among the thread's: [clo, chi)
+            int clo = 0, chi = min(kc, sq.tq - i0 - c0);
             // query position p sees key j when p - wl <= j <= p + wr
-            if (P.wr >= 0) clo = max(clo, j - P.wr - P.q_offset - i0);
-            if (P.wl >= 0) chi = min(chi, j + P.wl - P.q_offset - i0 + 1);
+            if (P.wr >= 0) clo = max(clo, j - P.wr - P.q_offset - i0 - c0);
+            if (P.wl >= 0) chi = min(chi, j + P.wl - P.q_offset - i0 - c0 + 1);
             if (!key_live) chi = 0;
             // the stats arrive with Q/dO of this tile; S^T/dP^T come from the MMA
             const int s = n % NS;
@@ -272,57 +284,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            const float* st_l = stat + s * 2 * BQ;
+            const float* st_l = stat + s * 2 * BQ + c0;
             const float* st_d = st_l + BQ;
             tc_fence_after();
-            uint32_t sv[2][32], dp[2][32];
-            tmem_ld32(tbase + lane_off + bf * 64, sv[0]);
-            tmem_ld32(tbase + lane_off + bf * 64 + 32, sv[1]);
-            tmem_ld32(tbase + lane_off + 128 + bf * 64, dp[0]);
-            tmem_ld32(tbase + lane_off + 128 + bf * 64 + 32, dp[1]);
+            uint32_t sv[kc], dp[kc];
+            auto chunk = [](uint32_t* a, int c) -> uint32_t(&)[32] { return *reinterpret_cast<uint32_t(*)[32]>(a + 32 * c); };
+#pragma unroll
+            for (int c = 0; c < kc / 32; ++c) {
+                tmem_ld32(tbase + lane_off + bf * 64 + c0 + 32 * c, chunk(sv, c));
+                tmem_ld32(tbase + lane_off + 128 + bf * 64 + c0 + 32 * c, chunk(dp, c));
+            }
             tmem_ld_wait_only();
-            tmem_pin(sv[0]);
-            tmem_pin(sv[1]);
-            tmem_pin(dp[0]);
-            tmem_pin(dp[1]);
-            if (BIAS && key_live) {  // additive score bias of (query i0 + cc, key j); never with softcap here
+#pragma unroll
+            for (int c = 0; c < kc / 32; ++c) {
+                tmem_pin(chunk(sv, c));
+                tmem_pin(chunk(dp, c));
+            }
+            if constexpr (HF == 2) {
+                // P^T and dS^T go over the first 32 columns of the buffers, which hold the
+                // other warp's scores: both warps of a row must have read theirs first
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(BAR(LD_DONE));
+            }
+            if (BIAS && key_live) {  // additive score bias of (query i0 + c0 + cc, key j); never with softcap here
                 // rows past the last query read the last row (finite; those columns are masked
-                // below), so each half's 32 loads issue back to back without a branch
+                // below), so the 32 loads issue back to back without a branch
                 const float* col = P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh +
                                    (long long)j * P.bias_sk;
                 const float inv = 1.f / P.scale;
                 const int ilast = max(sq.tq - 1, 0);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < kc / 32; ++half) {
                     float bv[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        bv[e] = __ldg(col + (long long)min(i0 + 32 * half + e, ilast) * P.bias_sq);
+                        bv[e] = __ldg(col + (long long)min(i0 + c0 + 32 * half + e, ilast) * P.bias_sq);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        sv[half][e] = __float_as_uint(fmaf(bv[e], inv, __uint_as_float(sv[half][e])));
+                        sv[32 * half + e] = __float_as_uint(fmaf(bv[e], inv, __uint_as_float(sv[32 * half + e])));
                 }
             }
-            uint32_t pk[32], dk[32];
-            // With a softcap, the polynomial serves the tile unless a raw score of the
-            // row lies outside its range (checked before masking)
+            uint32_t pk[kc / 2], dk[kc / 2];
+            // With a softcap, the polynomial serves the warp's tile half unless a raw
+            // score of its rows lies outside its range (checked before masking)
             bool poly = false;
             if (cap) {
                 float amax = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < BQ; cc += 2)
-                    amax = max3f(amax, fabsf(__uint_as_float(sv[cc >> 5][cc & 31])),
-                                 fabsf(__uint_as_float(sv[cc >> 5][(cc & 31) + 1])));
+                for (int cc = 0; cc < kc; cc += 2)
+                    amax = max3f(amax, fabsf(__uint_as_float(sv[cc])), fabsf(__uint_as_float(sv[cc + 1])));
                 poly = __all_sync(0xffffffffu, amax <= cap_poly(P.scale, P.softcap).r_max);
             }
-            // In a tile where some pair is invisible, those scores become -inf first, so
-            // every tile runs one copy of the element loop (a rarely run second copy
-            // would be fetched into the instruction cache cold each time).
-            const bool full = key_live && clo <= 0 && chi >= BQ;
+            // Where some pair is invisible, those scores become -inf first, so every tile
+            // runs one copy of the element loop (a rarely run second copy would be fetched
+            // into the instruction cache cold each time).
+            const bool full = key_live && clo <= 0 && chi >= kc;
             if (!__all_sync(0xffffffffu, full)) {
 #pragma unroll
-                for (int cc = 0; cc < BQ; ++cc)
-                    sv[cc >> 5][cc & 31] = (cc >= clo && cc < chi) ? sv[cc >> 5][cc & 31] : 0xff800000u;
+                for (int cc = 0; cc < kc; ++cc) sv[cc] = (cc >= clo && cc < chi) ? sv[cc] : 0xff800000u;
                 poly = poly && cap_poly(P.scale, P.softcap).inf_ok;
             }
             // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate.
@@ -331,11 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto elems = [&](auto modec) {
                 constexpr int kMode = decltype(modec)::value;
 #pragma unroll
-                for (int c = 0; c < BQ; c += 2) {
+                for (int c = 0; c < kc; c += 2) {
                     const uint64_t nl = *reinterpret_cast<const uint64_t*>(st_l + c);
                     const uint64_t nd = *reinterpret_cast<const uint64_t*>(st_d + c);
-                    const float s0 = __uint_as_float(sv[c >> 5][c & 31]), s1 = __uint_as_float(sv[c >> 5][(c & 31) + 1]);
-                    const uint64_t dp2 = f2_make(__uint_as_float(dp[c >> 5][c & 31]), __uint_as_float(dp[c >> 5][(c & 31) + 1]));
+                    const float s0 = __uint_as_float(sv[c]), s1 = __uint_as_float(sv[c + 1]);
+                    const uint64_t dp2 = f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
                     float p0, p1, x0, x1;
                     uint64_t dcap = one2;
                     if constexpr (kMode == 2) {
@@ -373,23 +393,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!cap) elems(std::integral_constant<int, 0>());
             else if (poly) elems(std::integral_constant<int, 1>());
             else elems(std::integral_constant<int, 2>());
-            tmem_st32(tbase + lane_off + bf * 64, pk);
-            tmem_st32(tbase + lane_off + 128 + bf * 64, dk);
+            // 16-bit pairs over the first 32 columns of the buffers: this thread's kc
+            // query columns are operand columns kc/2 * hf .. + kc/2 - 1
+            if constexpr (HF == 2) {
+                if (!warp_wait(BAR(LD_DONE), n & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if constexpr (HF == 1) {
+                tmem_st32(tbase + lane_off + bf * 64, pk);
+                tmem_st32(tbase + lane_off + 128 + bf * 64, dk);
+            } else {
+                tmem_st16(tbase + lane_off + bf * 64 + 16 * hf, pk);
+                tmem_st16(tbase + lane_off + 128 + bf * 64 + 16 * hf, dk);
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(PT_FULL(bf)));
         }
-        // epilogue: dV, dK (x scale) for this key row; zero when no query sees it.  Each
-        // warp's 32 rows leave through two alternating 4 KB staging slices, 64 columns
-        // per tiled store (rows past Tk are not written).
+        // epilogue: dV, dK (x scale) for this key row; zero when no query sees it.  The
+        // (part, 64-column half) slices q = part * (HD/64) + half leave as tiled stores
+        // of 32 rows x 64 columns through 4 KB staging slices (rows past Tk are not
+        // written): with HF = 1 each warp stores all of its rows' slices through two
+        // alternating staging slices, with HF = 2 the two warps of a lane quarter split
+        // them by q % 2, one staging slice each.
         const bool have = ok && ntiles > 0 && warp_wait(BAR(ACC_DONE), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
         if (have) tc_fence_after();
         // A packed sequence's last keys may share a 32-row slice with the next
         // sequence's first: such a slice goes out row by row (this sequence's rows
         // only).  Dense tensors end where the maps end, which clips the tiled store.
-        const bool whole = !VL || j0 + warp * 32 + 32 <= sq.tk;
-        if (have || (ok && ntiles == 0)) {
+        const bool whole = !VL || j0 + wq * 32 + 32 <= sq.tk;
+        if ((have || (ok && ntiles == 0)) && HF == 1) {
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 const uint32_t tcol = part == 0 ? tDV : tDK;
@@ -434,23 +471,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (elect_one()) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
                     __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int jj = 0; jj < 8; ++jj) {
                         uint32_t w4[4];
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
-                            const int col = half * 64 + j * 8 + 2 * t;  // element column
+                            const int col = half * 64 + jj * 8 + 2 * t;  // element column
                             w4[t] = pack2<BF16>(__uint_as_float(acc[col >> 5][col & 31]) * mul,
                                                 __uint_as_float(acc[col >> 5][(col & 31) + 1]) * mul);
                         }
-                        st_shared_v4(slice + lane * 128 + ((j ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+                        st_shared_v4(slice + lane * 128 + ((jj ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (elect_one()) {
                         tile_store<PADH, HD>(part == 0 ? &tmDV : &tmDK, slice, kvh, half * 64,
-                                             sq.k0 + j0 + warp * 32, sq.zb);
+                                             sq.k0 + j0 + wq * 32, sq.zb);
                         bulk_commit_group();
                     }
+                }
+            }
+        }
+        if ((have || (ok && ntiles == 0)) && HF == 2) {
+            // each warp one slice: the (part, half) slices q with q % 2 == hf
+            const uint32_t slice = sbase + C::kStgOff + warp * 4096;
+#pragma unroll
+            for (int q = hf; q < 2 * (HD / 64); q += 2) {
+                const int part = q / (HD / 64), half = q % (HD / 64);
+                const uint32_t tcol = (part == 0 ? tDV : tDK) + half * 64;
+                const float mul = part == 0 ? 1.f : P.scale;
+                uint32_t acc[2][32];
+                if (have) {
+                    tmem_ld32(tcol + lane_off, acc[0]);
+                    tmem_ld32(tcol + lane_off + 32, acc[1]);
+                    tmem_ld_wait_only();
+                    tmem_pin(acc[0]);
+                    tmem_pin(acc[1]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) acc[c][e] = 0u;
+                }
+                if (!whole) {
+                    if (j < sq.tk) {
+                        uint4* row = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(part == 0 ? P.dv : P.dk) +
+                                                              ((long long)sq.k0 + j) * P.Hkv * HD + (long long)kvh * HD +
+                                                              half * 64);
+#pragma unroll
+                        for (int w4 = 0; w4 < 8; ++w4) {
+                            uint32_t q4[4];
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int col = w4 * 8 + 2 * t;
+                                q4[t] = pack2<BF16>(__uint_as_float(acc[col >> 5][col & 31]) * mul,
+                                                    __uint_as_float(acc[col >> 5][(col & 31) + 1]) * mul);
+                            }
+                            row[w4] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+                        }
+                    }
+                    continue;
+                }
+                // the slice's previous store has finished reading it
+                if (elect_one()) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int col = jj * 8 + 2 * t;  // element column within the half
+                        w4[t] = pack2<BF16>(__uint_as_float(acc[col >> 5][col & 31]) * mul,
+                                            __uint_as_float(acc[col >> 5][(col & 31) + 1]) * mul);
+                    }
+                    st_shared_v4(slice + lane * 128 + ((jj ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (elect_one()) {
+                    tile_store<PADH, HD>(part == 0 ? &tmDV : &tmDK, slice, kvh, half * 64, sq.k0 + j0 + wq * 32,
+                                         sq.zb);
+                    bulk_commit_group();
                 }
             }
         }
@@ -459,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == MMA) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
@@ -1053,7 +1153,8 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         const long long per = 2LL * p.G * p.Tq * p.hd * 2;
         // (packed sequences differ in length: their key blocks keep one global order)
         pc.kv_chunk = p.cu_q ? 0 : (int)std::max(1LL, std::min<long long>(p.Hkv * p.B, (32LL << 20) / std::max(per, 1LL)));
-        k<<<grid, kThreads, KVCfg<HD>::kLaunchBytes, s>>>(pc, m.q64, m.k, m.v, m.dout64, m.dk32, m.dv32);
+        const int threads = c ? dkdv_threads(4) : dkdv_threads(0);
+        k<<<grid, threads, KVCfg<HD>::kLaunchBytes, s>>>(pc, m.q64, m.k, m.v, m.dout64, m.dk32, m.dv32);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
