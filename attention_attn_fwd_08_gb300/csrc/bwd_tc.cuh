@@ -594,13 +594,10 @@ struct DqItem {
     Seq sq;
 };
 template <int BQ, int BK, bool VL>
-__device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
+__device__ __forceinline__ DqItem dq_item_at(const Params& P, int b, int h, int qb) {
     DqItem it;
-    const int nqb = (P.Tq + BQ - 1) / BQ;
-    const int hb = w % (P.H * P.B);
-    const int qb = nqb - 1 - w / (P.H * P.B);
-    it.h = hb % P.H;
-    it.b = hb / P.H;
+    it.h = h;
+    it.b = b;
     it.kvh = it.h / P.G;
     it.i0 = qb * BQ;
     it.sq = seq_of<VL>(P, it.b);
@@ -611,6 +608,52 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w) {
     it.kt0 = lo / BK;
     it.ntiles = hi > lo ? (hi + BK - 1) / BK - it.kt0 : 0;
     return it;
+}
+// Packed batches of at most kVlCompact sequences: only the query blocks that hold rows
+// of their own sequence are items.  Items run from the highest block index down; a
+// level holds H items for every sequence that reaches it, sequences in order, heads
+// innermost.  Lane b of a warp reads sequence b's block count, and a cursor walks the
+// levels once, so each sequence of calls must have non-decreasing item numbers; every
+// call is made by whole warps.  Otherwise items are numbered block-major over every
+// (batch, head), longest first, and the cursor is unused.
+struct DqCursor {
+    int level;      // the block index the cursor is at
+    int first;      // number of that level's first item
+    unsigned seqs;  // the sequences that reach that level
+};
+template <int BQ>
+__device__ __forceinline__ int dq_vl_blocks(const Params& P, int b) {
+    return b < P.B ? (seq_of<true>(P, b).tq + BQ - 1) / BQ : 0;
+}
+// the item count; sets the cursor at the first level
+template <int BQ, bool VL>
+__device__ __forceinline__ int dq_items(const Params& P, DqCursor& c) {
+    if (VL && P.B <= kVlCompact) {
+        const int nb = dq_vl_blocks<BQ>(P, threadIdx.x & 31);
+        c.level = (int)__reduce_max_sync(0xffffffffu, (unsigned)nb) - 1;
+        c.first = 0;
+        c.seqs = __ballot_sync(0xffffffffu, nb > 0 && nb > c.level);
+        return (int)__reduce_add_sync(0xffffffffu, (unsigned)nb) * P.H;
+    }
+    return (P.Tq + BQ - 1) / BQ * P.H * P.B;
+}
+template <int BQ, int BK, bool VL>
+__device__ __forceinline__ DqItem dq_item(const Params& P, int w, DqCursor& c) {
+    if (VL && P.B <= kVlCompact) {
+        while (w >= c.first + __popc(c.seqs) * P.H && c.level > 0) {
+            c.first += __popc(c.seqs) * P.H;
+            --c.level;
+            c.seqs = __ballot_sync(0xffffffffu, dq_vl_blocks<BQ>(P, threadIdx.x & 31) > c.level);
+        }
+        const int r = w - c.first, j = r / P.H;
+        unsigned m = c.seqs;
+        for (int t = 0; t < j && m; ++t) m &= m - 1;
+        // (w is below the item count, so the sequence exists)
+        return dq_item_at<BQ, BK, VL>(P, m ? __ffs(m) - 1 : 0, r - j * P.H, c.level);
+    }
+    const int nqb = (P.Tq + BQ - 1) / BQ;
+    const int hb = w % (P.H * P.B);
+    return dq_item_at<BQ, BK, VL>(P, hb / P.H, hb % P.H, nqb - 1 - w / (P.H * P.B));
 }
 
 // Persistent: one CTA per SM walks its items in snake order (snake_item).  The
@@ -652,7 +695,10 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     const int D_FULL = 10 + 2 * NS;  // D of an item's rows in shared memory (the Q/dO/O producer)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nitems = (P.Tq + BQ - 1) / BQ * P.H * P.B;
+    // every warp keeps its own cursors over the item sequence (one per monotone walk)
+    DqCursor cur;
+    const int nitems = dq_items<BQ, VL>(P, cur);
+    DqCursor cur2 = cur;  // the compute warps' look-ahead walk
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
@@ -706,7 +752,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         };
         int qn = 0;  // Q/dO/O loads so far
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
             if (it.ntiles == 0) {
 #pragma unroll
                 for (int m = 0; m < BQ / 32; ++m) stats(it, it.i0 + m * 32 + lane, 0.f);
@@ -766,7 +812,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         bool ok = true;
         int g = 0;  // K/V tiles loaded so far
         for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
             for (int n = 0; n < it.ntiles; ++n) {
                 const int s = g % NS, use = g / NS;
                 if (use > 0 && !warp_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) {
@@ -822,7 +868,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         bool ok = true;
         int gt = 0, act = 0;
         for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
             if (it.ntiles == 0) continue;
             ok = wait_all(QT_READY, act & 1);
             if (ok) ok = issue_one(gt);
@@ -910,7 +956,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             if (lane == 0) mbar_arrive(BAR(QT_READY));
             // issued here, consumed at the item's start: the latency hides behind
             // the current item's epilogue
-            l_copied = load_lse(dq_item<BQ, BK, VL>(P, w2));
+            l_copied = load_lse(dq_item<BQ, BK, VL>(P, w2, cur2));
             if (!warp_wait(BAR(D_FULL), qc & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) return false;
             d_copied = reinterpret_cast<const float*>(smem + C::kOOff)[r];
             ++qc;
@@ -920,7 +966,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             return true;
         };
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w);
+            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
             const int i = it.i0 + r;
             const int p = i + P.q_offset;
             const int tq = it.sq.tq, tk = it.sq.tk;
@@ -1031,7 +1077,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             // every S and dP of this item completed (their results were read above):
             // put the next active item's Q and dO into TMEM before this epilogue
             for (int k2 = k_ + 1, w2 = snake_item(k2); ntiles > 0 && w2 < nitems; w2 = snake_item(++k2)) {
-                if (dq_item<BQ, BK, VL>(P, w2).ntiles == 0) continue;
+                if (dq_item<BQ, BK, VL>(P, w2, cur2).ntiles == 0) continue;
                 ok = copy_q(w2);
                 break;
             }

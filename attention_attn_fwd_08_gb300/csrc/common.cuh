@@ -224,6 +224,9 @@ __device__ __forceinline__ int2 mask_span(const Params& P, int b, int tk) {
     return make_int2(first * seg, min(tk, (last + 1) * seg));
 }
 constexpr int kMaskSpanMax = 64;  // batches whose spans a kernel keeps in shared memory
+// packed batches of at most this many sequences get compact item numberings (one lane
+// per sequence)
+constexpr int kVlCompact = 32;
 
 // Range of keys [lo, hi) that any query with position in [p0, p1] can see,
 // before the key mask: the window [p - wl, p + wr] (-1 = unbounded side).

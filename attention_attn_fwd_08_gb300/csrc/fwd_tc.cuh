@@ -173,7 +173,6 @@ __device__ __forceinline__ int fwd_items(const Params& P) { return (P.Tq + 2 * B
 // sequence b's block count, and a cursor walks the levels once per CTA, as the
 // CTA's item numbers only grow.  Every call is made by whole warps.  More
 // sequences keep the plain numbering (a sequence's surplus items have no rows).
-constexpr int kVlCompact = 32;
 struct VlCursor {
     int level;      // the block index the cursor is at
     int first;      // number of that level's first item
