@@ -786,20 +786,32 @@ def components_round(c):
 
 def measure_e2e(A, w, inp, dev, stream, args, kw):
     """Same step through the public API from pinned host buffers: H2D of q,k,v,dO, fwd, bwd,
-    D2H of o,dq,dk,dv, every copy inside the timed region.  The copies that no later call
-    waits for run on a second stream under the kernels: dO's upload under the forward, O's
-    and dQ's downloads under the dK/dV pass (the backward is called as its two passes, dQ
-    then dK/dV, with one workspace).  Before timing, one overlapped step's downloads are
-    compared bit for bit with the serial order's (the kernels are deterministic); on a
-    mismatch or an error the serial order is timed instead, and `mode` says which ran."""
+    D2H of o,dq,dk,dv, every copy inside the timed region.
+
+    One step alone ("single_step_ms"): the copies no later call waits for run on a second
+    stream under the kernels (dO's upload under the forward, O's and dQ's downloads under
+    the dK/dV pass; the backward is called as its two passes, dQ then dK/dV).  The reported
+    throughput runs the steps back to back as a training loop would: two sets of device
+    tensors, uploads on one stream, kernels on a second, downloads on a third, so step
+    i+1's uploads run under step i's kernels and downloads (each step still copies its
+    own inputs up and its own results down inside the timed region).  Before timing, the
+    downloads of both orders are compared bit for bit with the serial order's (the
+    kernels are deterministic); on a mismatch or an error the serial order is timed
+    instead, and `mode` says which ran."""
     import torch
 
     h_in = [inp[n].pin_memory() for n in ("q", "k", "v", "do")]
-    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    d_sets = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(2)]
+    d_in = d_sets[0]
     h_out = [torch.empty_like(inp[n]).pin_memory() for n in ("q", "q", "k", "v")]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
-    ws = torch.empty(A.attn_bwd_workspace_size(w.B, w.Tq, w.H), dtype=torch.uint8, device=dev)
+    wss = [torch.empty(A.attn_bwd_workspace_size(w.B, w.Tq, w.H), dtype=torch.uint8, device=dev) for _ in range(2)]
+    ws = wss[0]
+    # per set: o, dq, dk, dv and the LSE, allocated once
+    o_sets = [[torch.empty_like(d_sets[b][0]), torch.empty_like(d_sets[b][0]), torch.empty_like(d_sets[b][1]),
+               torch.empty_like(d_sets[b][2]), torch.empty((w.B, w.H, w.Tq), dtype=torch.float32, device=dev)]
+              for b in range(2)]
 
     def serial_step():
         for h, d in zip(h_in, d_in):
@@ -834,9 +846,49 @@ def measure_e2e(A, w, inp, dev, stream, args, kw):
         h_out[3].copy_(dv, non_blocking=True)
         main.wait_stream(s2)  # the step ends when every download has landed
 
-    mode, step = "serial", serial_step
+    def pipelined_steps(n):
+        """n steps back to back: uploads, kernels and downloads on three streams, step i on
+        device set i % 2 (its inputs are overwritten only after step i-2's kernels, its
+        outputs only after step i-2's downloads)."""
+        main = torch.cuda.current_stream()
+        up, comp, down = side[1], side[2], side[3]
+        done_comp, done_down = [None, None], [None, None]
+        for st_ in (up, comp, down):
+            st_.wait_stream(main)
+        for i in range(n):
+            b = i % 2
+            q, k, v, do = d_sets[b]
+            o, dq, dk, dv, lse = o_sets[b]
+            if done_comp[b] is not None:
+                up.wait_event(done_comp[b])
+            with torch.cuda.stream(up):
+                for h, d in zip(h_in, d_sets[b]):
+                    d.copy_(h, non_blocking=True)
+            comp.wait_event(up.record_event())
+            if done_down[b] is not None:
+                comp.wait_event(done_down[b])
+            with torch.cuda.stream(comp):
+                A.attn_fwd(q, k, v, o=o, lse=lse, **kw)
+                A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=wss[b], phases=4, **kw)
+                mid = comp.record_event()  # O and dQ are final
+                A.attn_bwd(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=wss[b], phases=2, **kw)
+                done_comp[b] = comp.record_event()
+            down.wait_event(mid)
+            with torch.cuda.stream(down):
+                h_out[0].copy_(o, non_blocking=True)
+                h_out[1].copy_(dq, non_blocking=True)
+            down.wait_event(done_comp[b])
+            with torch.cuda.stream(down):
+                h_out[2].copy_(dk, non_blocking=True)
+                h_out[3].copy_(dv, non_blocking=True)
+            done_down[b] = down.record_event()
+        main.wait_stream(down)  # the last step ends when its downloads have landed
+
+    mode, single = "serial", serial_step
+    pipelined = False
     try:
-        side.append(torch.cuda.Stream(device=dev))
+        for _ in range(4):
+            side.append(torch.cuda.Stream(device=dev))
         serial_step()
         torch.cuda.synchronize()
         want = [t.clone() for t in h_out]
@@ -845,27 +897,46 @@ def measure_e2e(A, w, inp, dev, stream, args, kw):
         overlapped_step()
         torch.cuda.synchronize()
         if all(torch.equal(a, b) for a, b in zip(want, h_out)):
-            mode, step = "overlapped", overlapped_step
+            mode, single = "overlapped", overlapped_step
+            for t in h_out:
+                t.zero_()
+            pipelined_steps(3)  # the last of them ran on set 0
+            torch.cuda.synchronize()
+            if all(torch.equal(a, b) for a, b in zip(want, h_out)):
+                pipelined = True
     except Exception as e:  # keep the serial order; the bench line says so
         mode = "serial (overlapped order failed: %s)" % type(e).__name__
     torch.cuda.synchronize()
 
+    # one step alone
     for _ in range(args.warmup):
-        step()
+        single()
     torch.cuda.synchronize()
     times = []
     for _ in range(args.steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        step()
+        single()
         e1.record(stream)
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
-    ms = statistics.mean(times)
+    single_ms = statistics.mean(times)
+    ms = single_ms
+    if pipelined:
+        pipelined_steps(max(args.warmup, 2))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pipelined_steps(args.steps)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        mode = "steps back to back: each step's uploads, kernels and downloads on three streams, " \
+               "two device sets, the next step's uploads under this step's work"
     flops = 3.5 * FWD_FLOPS_PER_PAIR(w.hd) * visible_pairs(w)
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "mode": mode}
-
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "mode": mode, "single_step_ms": single_ms,
+            "single_step_mode": "overlapped" if single is overlapped_step else "serial"}
 
 if __name__ == "__main__":
     main()
