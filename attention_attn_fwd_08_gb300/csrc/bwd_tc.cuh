@@ -328,13 +328,14 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
             uint32_t pk[kc / 2], dk[kc / 2];
             // With a softcap, the polynomial serves the warp's tile half unless a raw
             // score of its rows lies outside its range (checked before masking)
-            bool poly = false;
+            bool poly = false, shorter = false;
             if (cap) {
                 float amax = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < kc; cc += 2)
                     amax = max3f(amax, fabsf(__uint_as_float(sv[cc])), fabsf(__uint_as_float(sv[cc + 1])));
                 poly = __all_sync(0xffffffffu, amax <= cap_poly(P.scale, P.softcap).r_max);
+                shorter = __all_sync(0xffffffffu, amax <= cap_short(P.scale, P.softcap).r_max);
             }
             // Where some pair is invisible, those scores become -inf first, so every tile
             // runs one copy of the element loop (a rarely run second copy would be fetched
@@ -344,9 +345,10 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
 #pragma unroll
                 for (int cc = 0; cc < kc; ++cc) sv[cc] = (cc >= clo && cc < chi) ? sv[cc] : 0xff800000u;
                 poly = poly && cap_poly(P.scale, P.softcap).inf_ok;
+                shorter = shorter && cap_short(P.scale, P.softcap).inf_ok;
             }
-            // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate.
-            // Pairs of columns go through the f32x2 unit together; the stats hold -LSE*log2e
+            // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate; 3: by
+            // the short polynomial.  Pairs of columns go through the f32x2 unit together; the stats hold -LSE*log2e
             // and -D, so x = st*log2e + nl and dS = P*(dP + nd)*(1 - tanh^2).
             auto elems = [&](auto modec) {
                 constexpr int kMode = decltype(modec)::value;
@@ -376,6 +378,13 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                             float d0, d1;
                             f2_split(f2_fma(f2_mul(g, g), cp.nc2, one2), d0, d1);
                             dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
+                        } else if constexpr (kMode == 3) {
+                            // the short polynomial (every raw score of the tile within its range);
+                            // a masked score gives g = -inf as above
+                            g = cap_g_short(cap_short(P.scale, P.softcap), g);
+                            float d0, d1;
+                            f2_split(f2_fma(f2_mul(g, g), cap_poly(P.scale, P.softcap).nc2, one2), d0, d1);
+                            dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
                         }
                         f2_split(f2_fma(g, sl2_2, nl), x0, x1);
                     }
@@ -391,6 +400,7 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                 }
             };
             if (!cap) elems(std::integral_constant<int, 0>());
+            else if (shorter) elems(std::integral_constant<int, 3>());
             else if (poly) elems(std::integral_constant<int, 1>());
             else elems(std::integral_constant<int, 2>());
             // 16-bit pairs over the first 32 columns of the buffers: this thread's kc
@@ -671,7 +681,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                   const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDQ) {
     using C = QCfg<HD>;
     constexpr int NS = C::kStages, BQ = C::BQ, BK = C::BK;
-    // MODE & 3 as for dK/dV; MODE & 8: a head size below HD (4-D maps)
+    // MODE & 3 as for dK/dV; MODE & 4: softcap; MODE & 8: a head size below HD (4-D maps)
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
     extern __shared__ uint8_t smem_raw[];
@@ -914,7 +924,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         const int wq = warp & 3, hf = warp >> 2;
         const int r = wq * 32 + lane;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-        const bool cap = P.softcap > 0.f;
+        constexpr bool cap = (MODE & 4) != 0;
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
         const uint64_t sl2_2 = f2_make(P.scale_log2, P.scale_log2), one2 = f2_make(1.f, 1.f);
         bool ok = true;
@@ -1009,13 +1019,14 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 uint32_t dsk[16];
                 // with a softcap, the polynomial serves the tile unless a raw score of the
                 // row lies outside its range (checked before masking)
-                bool poly = false;
+                bool poly = false, shorter = false;
                 if (cap) {
                     float amax = 0.f;
 #pragma unroll
                     for (int cc = 0; cc < 32; cc += 2)
                         amax = max3f(amax, fabsf(__uint_as_float(sv[cc])), fabsf(__uint_as_float(sv[cc + 1])));
                     poly = __all_sync(0xffffffffu, amax <= cap_poly(P.scale, P.softcap).r_max);
+                    shorter = __all_sync(0xffffffffu, amax <= cap_short(P.scale, P.softcap).r_max);
                 }
                 // invisible pairs become -inf scores first: one copy of the element loop
                 const bool full = row_ok && !P.key_mask && clo <= 0 && chi >= 32;
@@ -1024,9 +1035,10 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                     for (int cc = 0; cc < 32; ++cc)
                         sv[cc] = (cc >= clo && cc < chi && ((mbits >> cc) & 1u)) ? sv[cc] : 0xff800000u;
                     poly = poly && cap_poly(P.scale, P.softcap).inf_ok;
+                    shorter = shorter && cap_short(P.scale, P.softcap).inf_ok;
                 }
-                // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate.
-                // Pairs of columns go through the f32x2 unit together.
+                // Mode 0: no softcap; 1: softcap by the polynomial; 2: by tanh_accurate; 3: by
+                // the short polynomial.  Pairs of columns go through the f32x2 unit together.
                 auto elems = [&](auto modec) {
                     constexpr int kMode = decltype(modec)::value;
 #pragma unroll
@@ -1051,6 +1063,13 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                                 float d0, d1;
                                 f2_split(f2_fma(f2_mul(g, g), cp.nc2, one2), d0, d1);
                                 dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
+                            } else if constexpr (kMode == 3) {
+                                // the short polynomial (every raw score of the tile within its
+                                // range); a masked score gives g = -inf as above
+                                g = cap_g_short(cap_short(P.scale, P.softcap), g);
+                                float d0, d1;
+                                f2_split(f2_fma(f2_mul(g, g), cap_poly(P.scale, P.softcap).nc2, one2), d0, d1);
+                                dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
                             }
                             f2_split(f2_fma(g, sl2_2, nl2), x0, x1);
                         }
@@ -1063,6 +1082,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                     }
                 };
                 if (!cap) elems(std::integral_constant<int, 0>());
+                else if (shorter) elems(std::integral_constant<int, 3>());
                 else if (poly) elems(std::integral_constant<int, 1>());
                 else elems(std::integral_constant<int, 2>());
                 // packed into the first 16 of the 32 columns this warp read (the partner
@@ -1170,10 +1190,11 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
     }
     if (phases & 4) {
         // a head size below HD (dense batches without a bias only) runs the padded instantiations
-        auto k = p.hd != HD ? bwd_dq_kernel<BF16, HD, 8>
-                 : p.cu_q   ? bwd_dq_kernel<BF16, HD, 1>
+        const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
+        auto k = p.hd != HD ? (c ? bwd_dq_kernel<BF16, HD, 12> : bwd_dq_kernel<BF16, HD, 8>)
+                 : p.cu_q   ? (c ? bwd_dq_kernel<BF16, HD, 5> : bwd_dq_kernel<BF16, HD, 1>)
                  : p.bias   ? bwd_dq_kernel<BF16, HD, 2>
-                            : bwd_dq_kernel<BF16, HD, 0>;
+                            : (c ? bwd_dq_kernel<BF16, HD, 4> : bwd_dq_kernel<BF16, HD, 0>);
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
         int dev = 0, nsm = 0;

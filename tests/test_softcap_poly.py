@@ -1,4 +1,4 @@
-"""The softcap polynomials in csrc/common.cuh and csrc/fwd_tc.cuh against numpy's tanh.
+"""The softcap polynomials in csrc/common.cuh against numpy's tanh.
 
 tanh(y) = y * (1 + t * R(t)), t = y^2, serves |y| <= kTanhPolyY in the
 kernels; larger |y| fall back to the exp-based tanh.  The forward also has a
@@ -54,7 +54,7 @@ def test_poly_is_odd_and_leading_coefficient_positive():
 
 
 def _short_consts():
-    s = open(os.path.join(CSRC, "fwd_tc.cuh")).read()
+    s = open(SRC).read()
     y0 = float(re.search(r"kTanhShortY\s*=\s*([-0-9.eE+]+)f", s).group(1))
     r = [float(re.search(r"kTanhS%d\s*=\s*([-0-9.eE+]+)f" % i, s).group(1)) for i in range(2)]
     return y0, r
