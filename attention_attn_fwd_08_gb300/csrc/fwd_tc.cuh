@@ -613,13 +613,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
             else if (!accurate) p_pass(std::integral_constant<int, 1>());
             else p_pass(std::integral_constant<int, 2>());
         };
-        // Without a softcap at hd 128 the two tiles' softmaxes alternate A(k), B(k),
-        // A(k+1), ... within an item, so each runs while the tensor core works on the
-        // other tile's P.V and next S; left alone they fall into lockstep and the
-        // tensor core idles during both.  The longer softcap softmax (and the shorter
-        // MMAs of hd 64) do better with both warpgroups issuing at once (measured).
-        // base[u] counts tile u's softmaxes in earlier items.
-        const bool alternate = !cap && HD == 128;
+        // Without a softcap the two tiles' softmaxes alternate A(k), B(k), A(k+1), ...
+        // within an item, so each runs while the tensor core works on the other tile's
+        // P.V and next S; left alone they fall into lockstep and the tensor core idles
+        // during both.  The longer softcap softmax does better with both warpgroups
+        // issuing at once (measured).  base[u] counts tile u's softmaxes in earlier items.
+        const bool alternate = !cap;
         int base[2] = {0, 0};
         // Fused rotary embedding: turn this thread's row of tile u's Q in shared memory
         // once the tile of item w2 has landed, then release it to the MMA warp.  Pairs
