@@ -174,6 +174,34 @@ __device__ __forceinline__ FwdItem vl_item(const Params& P, VlCursor& c, int w) 
     return make_item<true>(P, valid ? __ffs(m) - 1 : 0, valid ? r - j * P.H : 0, c.level, valid, nullptr);
 }
 
+// The additive bias of row i over the key tile j0 .. j0+127 (0 past the keys), loaded
+// into registers before the tile's scores are needed, so that the loads' latency runs
+// under the waits for S and for the other tile's softmax.  Rows of 16-byte-aligned
+// contiguous bias load as float4.
+__device__ __forceinline__ void load_bias_row(const Params& P, int b, int h, int i, int j0, int tk,
+                                              float (&bv)[128]) {
+    const float* row = P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh + (long long)i * P.bias_sq;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int jc = j0 + 32 * c;
+        if (P.bias_sk == 1 && jc + 32 <= tk && ((reinterpret_cast<uintptr_t>(row + jc) & 15u) == 0)) {
+            const float4* r4 = reinterpret_cast<const float4*>(row + jc);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float4 v = __ldg(r4 + e);
+                bv[32 * c + 4 * e] = v.x;
+                bv[32 * c + 4 * e + 1] = v.y;
+                bv[32 * c + 4 * e + 2] = v.z;
+                bv[32 * c + 4 * e + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                bv[32 * c + e] = jc + e < tk ? __ldg(row + (long long)(jc + e) * P.bias_sk) : 0.f;
+        }
+    }
+}
+
 // KORD: dense key-masked batches with their spans in kspan and kord the batches by
 // kept span, longest first.  Without a window every query block of a batch sees
 // the same key tiles, so a batch's items run together, the longest spans first;
@@ -717,31 +745,50 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     if (P.wr >= 0) chi = min(chi, p + P.wr - j0 + 1);
                     if (P.wl >= 0) clo = max(clo, p - P.wl - j0);
                 }
+                // additive score bias (never with softcap here): loads issued before the waits
+                float bv[BIAS ? 128 : 1];
+                if constexpr (BIAS) {
+                    if (i < tq) load_bias_row(P, it.b, it.h, i, j0, tk, bv);
+                    else
+#pragma unroll
+                        for (int e = 0; e < 128; ++e) bv[e] = 0.f;
+                }
                 if (!wait_warp(S_FULL(u), sc & 1)) {
                     ok = false;
                     break;
                 }
                 ++sc;
                 tc_fence_after();
-                // the row's 128 scores, loaded while this tile waits for its turn
+                // the row's 128 scores, loaded while this tile waits for its turn (with a
+                // bias, a chunk at a time after the wait, each gaining its bias as it lands)
                 uint32_t sv[4][32];
+                if constexpr (!BIAS) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sv[c]);
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sv[c]);
+                }
                 if (alternate && (u == 0 ? (k >= 1 && k - 1 < nB) : (k < nA))) {
                     const int need = 4 * (u == 0 ? bB + k : bA + k + 1);  // warp arrivals
                     const bool rr = count_wait(&done_count[u ^ 1], need, P.status, ST_FWD_SOFTMAX, &abort_flag);
                     if (!__all_sync(0xffffffffu, rr)) {
-                        tmem_ld_wait_only();
+                        if constexpr (!BIAS) tmem_ld_wait_only();
                         ok = false;
                         break;
                     }
                 }
-                tmem_ld_wait_only();
+                if constexpr (BIAS) {
+                    const float inv = 1.f / P.scale;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
-                if (BIAS && i < tq) {  // additive score bias (never with softcap here)
+                    for (int c = 0; c < 4; ++c) {
+                        tmem_ld32(tS + lane_off + c * 32, sv[c]);
+                        tmem_ld_wait(sv[c]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) add_bias32(P, it.b, it.h, i, j0 + 32 * c, tk, sv[c]);
+                        for (int e = 0; e < 32; ++e)
+                            sv[c][e] = __float_as_uint(fmaf(bv[32 * c + e], inv, __uint_as_float(sv[c][e])));
+                    }
+                } else {
+                    tmem_ld_wait_only();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
                 }
                 if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits, sv);
                 else run_tile(std::integral_constant<bool, false>(), m_used, l, k, full, clo, chi, mbits, sv);
