@@ -277,6 +277,19 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
             if (P.wr >= 0) clo = max(clo, j - P.wr - P.q_offset - i0 - c0);
             if (P.wl >= 0) chi = min(chi, j + P.wl - P.q_offset - i0 - c0 + 1);
             if (!key_live) chi = 0;
+            // additive score bias of (query i0 + c0 + cc, key j) (never with softcap here): the
+            // first 32 columns' loads issue before the waits; rows past the last query read
+            // the last row (finite; those columns are masked below), so the loads issue
+            // back to back without a branch
+            const float* bcol = BIAS ? P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh +
+                                           (long long)(key_live ? j : 0) * P.bias_sk
+                                     : nullptr;
+            const int ilast = max(sq.tq - 1, 0);
+            float bv0[BIAS ? 32 : 1];
+            if constexpr (BIAS) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) bv0[e] = __ldg(bcol + (long long)min(i0 + c0 + e, ilast) * P.bias_sq);
+            }
             // the stats arrive with Q/dO of this tile; S^T/dP^T come from the MMA
             const int s = n % NS;
             if (!warp_wait(BAR(Q_FULL(s)), (n / NS) & 1, P.status, ST_BWD_COMPUTE, &abort_flag) ||
@@ -307,22 +320,19 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(LD_DONE));
             }
-            if (BIAS && key_live) {  // additive score bias of (query i0 + c0 + cc, key j); never with softcap here
-                // rows past the last query read the last row (finite; those columns are masked
-                // below), so the 32 loads issue back to back without a branch
-                const float* col = P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh +
-                                   (long long)j * P.bias_sk;
+            if constexpr (BIAS) {
                 const float inv = 1.f / P.scale;
-                const int ilast = max(sq.tq - 1, 0);
 #pragma unroll
                 for (int half = 0; half < kc / 32; ++half) {
                     float bv[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        bv[e] = __ldg(col + (long long)min(i0 + c0 + 32 * half + e, ilast) * P.bias_sq);
+                        bv[e] = half == 0 ? bv0[e]
+                                          : __ldg(bcol + (long long)min(i0 + c0 + 32 * half + e, ilast) * P.bias_sq);
+                    if (key_live)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        sv[32 * half + e] = __float_as_uint(fmaf(bv[e], inv, __uint_as_float(sv[32 * half + e])));
+                        for (int e = 0; e < 32; ++e)
+                            sv[32 * half + e] = __float_as_uint(fmaf(bv[e], inv, __uint_as_float(sv[32 * half + e])));
                 }
             }
             uint32_t pk[kc / 2], dk[kc / 2];
@@ -1004,6 +1014,27 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 if (P.wr >= 0) chi = min(chi, p + P.wr - jc + 1);
                 if (P.wl >= 0) clo = max(clo, p - P.wl - jc);
                 if (!row_ok) chi = 0;
+                // the additive bias of the row's 32 keys, loaded before the wait for S (0 past
+                // the keys; never with a softcap here)
+                float bv[BIAS ? 32 : 1];
+                if constexpr (BIAS) {
+                    const float* brow = P.bias + (long long)it.b * P.bias_sb + (long long)it.h * P.bias_sh +
+                                        (long long)(row_ok ? i : 0) * P.bias_sq;
+                    if (P.bias_sk == 1 && jc + 32 <= tk && ((reinterpret_cast<uintptr_t>(brow + jc) & 15u) == 0)) {
+                        const float4* r4 = reinterpret_cast<const float4*>(brow + jc);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 v4 = __ldg(r4 + e);
+                            bv[4 * e] = v4.x;
+                            bv[4 * e + 1] = v4.y;
+                            bv[4 * e + 2] = v4.z;
+                            bv[4 * e + 3] = v4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) bv[e] = jc + e < tk ? __ldg(brow + (long long)(jc + e) * P.bias_sk) : 0.f;
+                    }
+                }
                 if (!warp_wait(BAR(ST_FULL(bf)), (t >> 1) & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) {
                     ok = false;
                     break;
@@ -1015,7 +1046,13 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 tmem_ld_wait_only();
                 tmem_pin(sv);
                 tmem_pin(dp);
-                if (BIAS && row_ok) add_bias32(P, it.b, it.h, i, jc, tk, sv);  // (never with softcap here)
+                if constexpr (BIAS) {
+                    if (row_ok) {
+                        const float inv = 1.f / P.scale;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(fmaf(bv[e], inv, __uint_as_float(sv[e])));
+                    }
+                }
                 uint32_t dsk[16];
                 // with a softcap, the polynomial serves the tile unless a raw score of the
                 // row lies outside its range (checked before masking)

@@ -152,31 +152,6 @@ __device__ __forceinline__ Seq seq_any(const Params& P, int b) {
     return P.cu_q ? seq_of<true>(P, b) : seq_of<false>(P, b);
 }
 
-// ------------------------------------------------------------ score bias
-// Adds bias(b, h, i, j) / scale to 32 raw scores q.k of row i, keys j0 .. j0+31
-// (so that the scaled score gains the bias); keys from tk on get nothing (they
-// are invisible).  Contiguous 16-byte-aligned rows load as float4.
-__device__ __forceinline__ void add_bias32(const Params& P, int b, int h, int i, int j0, int tk, uint32_t (&s)[32]) {
-    const float* row = P.bias + (long long)b * P.bias_sb + (long long)h * P.bias_sh + (long long)i * P.bias_sq;
-    const float inv = 1.f / P.scale;
-    if (P.bias_sk == 1 && j0 + 32 <= tk && ((reinterpret_cast<uintptr_t>(row + j0) & 15u) == 0)) {
-        const float4* r4 = reinterpret_cast<const float4*>(row + j0);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 v = __ldg(r4 + e);
-            s[4 * e + 0] = __float_as_uint(fmaf(v.x, inv, __uint_as_float(s[4 * e + 0])));
-            s[4 * e + 1] = __float_as_uint(fmaf(v.y, inv, __uint_as_float(s[4 * e + 1])));
-            s[4 * e + 2] = __float_as_uint(fmaf(v.z, inv, __uint_as_float(s[4 * e + 2])));
-            s[4 * e + 3] = __float_as_uint(fmaf(v.w, inv, __uint_as_float(s[4 * e + 3])));
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-            if (j0 + e < tk)
-                s[e] = __float_as_uint(fmaf(__ldg(row + (long long)(j0 + e) * P.bias_sk), inv, __uint_as_float(s[e])));
-    }
-}
-
 // ------------------------------------------------------------ rotary turn
 // Rotate-half RoPE turn of the pair (a, b) = (x[i], x[i + hd/2]) by the angle whose
 // cosine and sine are c and s (the inverse turn passes -s).  Written out with fmaf
