@@ -118,8 +118,8 @@ attn_status check_common(attn_dtype dt, int B, int Tq, int Tk, int H, int Hkv, i
     if (mstride < 0) return ATTN_ERR_INVALID_ARG;
     if (key_mask && (reinterpret_cast<uintptr_t>(key_mask) & 3u)) return ATTN_ERR_INVALID_ARG;
     if ((long long)Tq + q_offset > INT32_MAX - 1) return ATTN_ERR_INVALID_ARG;
-    // head sizes: 64 and 128 on the tensor cores (16-bit); 32, 96 and 256 also on the
-    // CUDA-core kernels; the 16-bit decode split kernel takes 64, 128 and 256
+    // head sizes: 32, 64, 96, 128 and 256 (16-bit on the tensor cores, fp32 on the
+    // CUDA-core kernels); the 16-bit decode split kernel takes 64, 128 and 256
     if (hd != 32 && hd != 64 && hd != 96 && hd != 128 && hd != 256) return ATTN_ERR_UNSUPPORTED;
     if (decode_hd && dt != ATTN_F32 && hd != 64 && hd != 128 && hd != 256) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
@@ -144,13 +144,12 @@ Params base_params(int B, int Tq, int Tk, int H, int Hkv, int hd, float scale, i
 // fp16/bf16 at hd 64 / 128 run on the tensor cores, and so do hd 32 and 96 as 64 and
 // 128 with the columns past the head read as zeros (dense batches; packed sequences
 // and a score bias at those sizes take the CUDA-core kernels).  fp32 stays on the
-// CUDA-core kernels (no TF32, no 16-bit P), which is what fp32 accuracy needs, and so
-// does hd 256 (correct, not fast).
+// CUDA-core kernels (no TF32, no 16-bit P), which is what fp32 accuracy needs.
 bool padded_head(int hd) { return hd == 32 || hd == 96; }
 bool use_tcgen05(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 32 || hd == 64 || hd == 96 || hd == 128); }
 
-// The forward also runs 16-bit hd 256 on the tensor cores (one query tile per work
-// item, dense batches without a bias); its backward stays on the CUDA-core kernels.
+// 16-bit hd 256 also runs on the tensor cores in dense batches without a bias (the
+// forward one query tile per work item; the backward in separate dV, dK and dQ passes).
 bool use_tc_fwd(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) || (dt != ATTN_F32 && hd == 256); }
 
 // Tensor map of one activation for the tensor-core kernels: 3-D at hd 64 / 128, 4-D
@@ -217,7 +216,7 @@ const char* attn_status_string(attn_status s) {
 
 int attn_kernel_family(attn_dtype dt, int hd) { return use_tc_fwd(dt, hd) ? 1 : 0; }
 
-int attn_kernel_family_bwd(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) ? 1 : 0; }
+int attn_kernel_family_bwd(attn_dtype dt, int hd) { return use_tc_fwd(dt, hd) ? 1 : 0; }
 
 }  // extern "C"
 
@@ -308,14 +307,16 @@ attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     p.tq_pad = (Tq + 63) / 64 * 64;
     p.ndelta = static_cast<float*>(workspace);
     p.nlse2 = p.ndelta + (size_t)B * H * p.tq_pad;
-    if (!use_tcgen05(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd)))) {
+    if (!use_tc_fwd(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd) || hd == 256))) {
         // the fp32 dQ pass reads D from the workspace: pass 4 implies pass 1 there
         const int ph = (phases & 4) ? (phases | 1) : phases;
         const int nks = ((ph & 1) ? 1 : 0) + ((ph & 2) ? 1 : 0) + ((ph & 4) ? 1 : 0);
         return counted(launch_simt_bwd(p, (int)dt, ph, s), nks);
     }
-    // the tensor-core dQ pass forms D itself: pass 1 is then not run separately
-    const int nk = ((phases & 1) && !(phases & 4) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
+    // the tensor-core dQ pass forms D itself: pass 1 is then not run separately (at hd
+    // 256 the preprocess runs for passes 1 and 4, and dK and dV are two launches)
+    const int nk = hd == 256 ? ((phases & 5) ? 1 : 0) + ((phases & 2) ? 2 : 0) + ((phases & 4) ? 1 : 0)
+                             : ((phases & 1) && !(phases & 4) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
     BwdMaps maps;
     if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128) || !act_map(&maps.dout, dt, dout, hd, H, Tq, B, 128) ||
         !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, 128) || !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, 128) ||

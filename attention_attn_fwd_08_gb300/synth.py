@@ -13,7 +13,7 @@ Workloads (shapes of the attention settings the pages describe):
   encoder_mask    B=8  Tq=Tk=1024  H=Hkv=12  hd=64  bidirectional, per-sequence key mask, fp16 fwd
   decode_lq1/lq4  B=16 Lk=32768 Lq in {1,4} H=32 Hkv=8 hd=128 causal q_offset=Lk-Lq  bf16 decode
   varlen_packed   8 sequences of U{256..2048} rows packed back to back, H=32 Hkv=8 hd=128 causal bf16 fwd+bwd
-  gqa_prefill_hd256  B=4 Tq=Tk=2048 H=16 Hkv=4 hd=256 causal  bf16 forward
+  gqa_prefill_hd256  B=4 Tq=Tk=2048 H=16 Hkv=4 hd=256 causal  bf16 fwd+bwd
 """
 from __future__ import annotations
 
@@ -67,9 +67,9 @@ WORKLOADS = {
                            decode=True, seed=0x5EED0005),
     "decode_lq4": Workload("decode_lq4", "bf16", 16, 4, 32768, 32, 8, 128, True, q_offset=32764,
                            decode=True, seed=0x5EED0006),
-    # the GQA prefill's query width (H*hd = 4096) at head size 256, forward
+    # the GQA prefill's query width (H*hd = 4096) at head size 256
     "gqa_prefill_hd256": Workload("gqa_prefill_hd256", "bf16", 4, 2048, 2048, 16, 4, 256, True,
-                                  seed=0x5EED0008),
+                                  backward=True, seed=0x5EED0008),
     # Tq/Tk: the bound on a sequence's length (max_seqlen)
     "varlen_packed": Workload("varlen_packed", "bf16", 8, 2048, 2048, 32, 8, 128, True, backward=True,
                               seed=0x5EED0007),

@@ -285,7 +285,7 @@ def workload_config(w):
 # repetition, in order.  Kernel launches per repetition (for a profiler's
 # --launch-skip): gqa_prefill 3 (fwd, dQ, dK/dV); swa_softcap, varlen_packed and
 # bias_prefill 3 (fwd, dQ, dK/dV); encoder_mask 1; decode_lq4 2 (split, combine);
-# gqa_prefill_hd256 1; rope_prefill 3 (turn of k, cos/sin table, fwd).
+# gqa_prefill_hd256 5 (fwd, D, dV, dK, dQ); rope_prefill 3 (turn of k, cos/sin table, fwd).
 def _case_dense(A, synth, torch, dev, name, fwd_only=False, bias=False):
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w)
@@ -354,7 +354,7 @@ PROFILE_CASES = {
     "bias_prefill": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill", bias=True),
     "varlen_packed": lambda A, s, t, d: _case_varlen(A, s, t, d),
     "decode_lq4": lambda A, s, t, d: _case_decode(A, s, t, d),
-    "gqa_prefill_hd256": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill_hd256", fwd_only=True),
+    "gqa_prefill_hd256": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill_hd256"),
     "rope_prefill": lambda A, s, t, d: _case_rope(A, s, t, d),
 }
 
@@ -735,20 +735,26 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
         tf = fl * wb.hd * pairs / (t[n] * 1e-3) / 1e12
         out["bias_prefill_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
                                     "visible_pairs": pairs, "note": "GQA causal prefill with a [1,1,T,T] fp32 bias"}
-    # the GQA causal prefill's width at head size 256 (forward on the tensor cores)
+    # the GQA causal prefill's width at head size 256 (tensor cores; the backward as D,
+    # dV, dK and dQ passes, flops counted as 10*hd per visible pair like the other backwards)
     w2 = synth.WORKLOADS["gqa_prefill_hd256"]
     i2 = synth.make_inputs(w2)
-    q2, k2, v2 = (i2[n].to(dev) for n in ("q", "k", "v"))
-    o2 = torch.empty_like(q2)
+    q2, k2, v2, do2 = (i2[n].to(dev) for n in ("q", "k", "v", "do"))
+    o2, dq2, dk2, dv2 = torch.empty_like(q2), torch.empty_like(q2), torch.empty_like(k2), torch.empty_like(v2)
     l2 = torch.empty((w2.B, w2.H, w2.Tq), dtype=torch.float32, device=dev)
+    ws2 = torch.empty(A.attn_bwd_workspace_size(w2.B, w2.Tq, w2.H), dtype=torch.uint8, device=dev)
     kw2 = dict(H=w2.H, Hkv=w2.Hkv, scale=w2.scale, causal=True)
-    t = time_passes(torch, stream, [("fwd", lambda: A.attn_fwd(q2, k2, v2, o=o2, lse=l2, **kw2))], args, flush_buf)
+    t = time_passes(torch, stream, [
+        ("fwd", lambda: A.attn_fwd(q2, k2, v2, o=o2, lse=l2, **kw2)),
+        ("bwd", lambda: A.attn_bwd(q2, k2, v2, o2, do2, l2, dq=dq2, dk=dk2, dv=dv2, workspace=ws2, **kw2))],
+        args, flush_buf)
     pairs = visible_pairs(w2)
-    tf = 4 * w2.hd * pairs / (t["fwd"] * 1e-3) / 1e12
-    out["hd256_prefill_fwd"] = {"ms": t["fwd"], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
-                                "visible_pairs": pairs,
-                                "note": "B=4 T=2048 H=16 Hkv=4 hd=256 causal bf16 forward (tensor cores)"}
-    del q2, k2, v2, o2, l2
+    for n, fl in (("fwd", 4), ("bwd", 10)):
+        tf = fl * w2.hd * pairs / (t[n] * 1e-3) / 1e12
+        out["hd256_prefill_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                     "visible_pairs": pairs,
+                                     "note": "B=4 T=2048 H=16 Hkv=4 hd=256 causal bf16 (tensor cores)"}
+    del q2, k2, v2, do2, o2, dq2, dk2, dv2, l2, ws2
     # rotary embedding of the GQA prefill q and k (HBM-bound: each element read and written once)
     rq, rk = q.clone(), k.clone()
     t = time_passes(torch, stream, [("rope", lambda: (A.attn_rope(rq, H=wb.H, pos=0), A.attn_rope(rk, H=wb.Hkv, pos=0)))],

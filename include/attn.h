@@ -93,7 +93,8 @@ typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
  *               zeros; 256 with one 128-row query tile per work item; with an additive
  *               bias, or in packed sequences, 32, 96 and 256 take the CUDA-core
  *               kernels); fp32 runs on CUDA-core kernels (same results, no tensor-core
- *               speed).  attn_bwd at hd 256 runs on the CUDA-core kernels.
+ *               speed).  attn_bwd at hd 256 (dense, no bias) runs on the tensor cores
+ *               in separate dV, dK and dQ passes.
  *   scale     : > 0 and finite (1/sqrt(hd) in the usual case).
  *   causal    : 0/1.   window : >= 0, 0 = unbounded.   softcap : >= 0, 0 = off.
  *   q_offset  : >= 0, absolute position of query row 0.
@@ -400,8 +401,8 @@ ATTN_API attn_status attn_selftest_bounded_wait(unsigned int timeout_us, void* s
  * run on the tensor cores. */
 ATTN_API int attn_kernel_family(attn_dtype dt, int hd);
 
-/* The same for attn_bwd: 16-bit hd 32, 64, 96 and 128 run on the tensor cores, hd 256
- * on the CUDA-core kernels. */
+/* The same for attn_bwd (without a bias): 16-bit hd 32, 64, 96, 128 and 256 run on
+ * the tensor cores. */
 ATTN_API int attn_kernel_family_bwd(attn_dtype dt, int hd);
 
 /* Running total of kernels this library has enqueued in this process. */

@@ -190,11 +190,12 @@ def test_bias_prefill_fwd_bwd_full():
                           (gq, gk[:, r0:r1], gv[:, r0:r1]), w.dtype, what)
 
 
-def test_gqa_prefill_hd256_fwd_full():
-    """The hd 256 forward at its benchmark size: sampled blocks of two groups."""
+def test_gqa_prefill_hd256_fwd_bwd_full():
+    """hd 256 at its benchmark size: sampled blocks of two groups; the last 256 rows
+    are every viewer of keys [T-256, T), so dK/dV there are exact."""
     w = synth.WORKLOADS["gqa_prefill_hd256"]
     inp = synth.make_inputs(w)
     gpu = run_gpu(w, inp)
     T = w.Tq
     sample_block(w, inp, gpu, 0, 0, 0, 200, 0, 200)
-    sample_block(w, inp, gpu, 3, 3, T - 300, T, 0, T)
+    sample_block(w, inp, gpu, 3, 3, T - 256, T, 0, T, grad_keys=(T - 256, T))

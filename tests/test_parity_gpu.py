@@ -346,15 +346,15 @@ def test_guard_bands_untouched():
     assert (big[:pad] == 9.0).all() and (big[pad + n:] == 9.0).all()
 
 
-# In 16 bits hd 32 and 96 run on the tensor cores (padded), hd 256's forward too (one
-# query tile per work item) and its backward on the CUDA-core kernels; fp32 runs on
-# the CUDA-core kernels.
+# In 16 bits hd 32 and 96 run on the tensor cores (padded), hd 256 too (the forward one
+# query tile per work item, the backward in dV, dK and dQ passes); fp32 runs on the
+# CUDA-core kernels.
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 @pytest.mark.parametrize("hd", [32, 96, 256])
 def test_other_head_sizes_fwd_bwd(dt, hd):
     name = {"bf16": "bfloat16", "f32": "float32"}[dt]
     assert A.attn_kernel_family(name, hd) == (1 if dt != "f32" else 0)
-    assert A.attn_kernel_family_bwd(name, hd) == (1 if dt != "f32" and hd != 256 else 0)
+    assert A.attn_kernel_family_bwd(name, hd) == (1 if dt != "f32" else 0)
     run_fwd_case(dt, 2, 150, 150, 4, 2, hd, causal=True, window=60, softcap=20.0, backward=True, seed=950 + hd)
 
 
@@ -374,6 +374,20 @@ def test_fwd_hd256_tensor_core(dt, flags):
     """The hd 256 forward: several 64-key tiles and 128-row items, ragged tails, GQA."""
     Tq = 333
     run_fwd_case(dt, 2, Tq, Tq + flags.get("q_offset", 0), 4, 2, 256, seed=990, **flags)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("flags", HD256_FLAGS, ids=lambda f: "-".join("%s%s" % kv for kv in f.items()))
+def test_bwd_hd256_tensor_core(dt, flags):
+    """The hd 256 backward: two 64-row query tiles per GQA head and a ragged tail in
+    each 128-key block of the dV / dK passes, several 64-key tiles per 128-row dQ block."""
+    Tq = 333
+    run_fwd_case(dt, 2, Tq, Tq + flags.get("q_offset", 0), 4, 2, 256, backward=True, seed=1990, **flags)
+
+
+def test_bwd_hd256_many_blocks():
+    # more key blocks and query blocks (3 x 8 x 3, 3 x 32 x 3) than SMs, group of four heads
+    run_fwd_case("bf16", 3, 300, 300, 32, 8, 256, causal=True, backward=True, seed=1995)
 
 
 def test_fwd_hd256_many_items_per_cta():
