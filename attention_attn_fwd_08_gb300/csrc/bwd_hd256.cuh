@@ -22,7 +22,10 @@
 //     (TS, dS^T over the first 32 columns of S^T).  S^T and dP^T are single-buffered.
 //   CTA = 128 keys of one (b, kv head): warps 0-3 one key row per thread, 4 TMA
 //   producer (K once, then 64-row Q and dO tiles of every query head of the group into
-//   a two-stage ring), 5 TMEM owner and MMA issuer.
+//   two two-stage rings), 5 TMEM owner and MMA issuer.  The ring that the tile's first
+//   MMAs alone read (Q in the dV pass, dO in the dK pass) is released as soon as they
+//   complete, so its next load runs under the rest of the tile; the other ring carries
+//   the tile's -LSE*log2(e) and -D and is released by the accumulating MMA.
 // dQ pass: CTA = 128 query rows of one (b, h) over 64-key tiles.  TMEM S 0..63, dP
 //   64..127 (single-buffered), Q 128..255 (16-bit pairs, the A operand of S = Q K^T),
 //   dQ 256..511.  MMAs: S (TS), dP = dO V^T (SS), dQ += dS K (TS, dS over S).  dO stays
@@ -52,11 +55,12 @@ constexpr int kKBytes = BKV * HD * 2;      // 64 KB: the key block's K (V passes
 constexpr int kTBytes = BQ * HD * 2;       // 32 KB: one Q or dO tile
 constexpr int kKVStages = 2;
 constexpr int kKOff = 0;
-constexpr int kRingOff = kKBytes;          // stage s: Q, then dO
-constexpr int kStatOff = kRingOff + kKVStages * 2 * kTBytes;  // [stage][2][BQ] floats: -LSE*log2e, -D
+constexpr int kRingOff = kKBytes;          // the Q ring (stage s at + s * kTBytes), then the dO ring
+constexpr int kGRingOff = kRingOff + kKVStages * kTBytes;
+constexpr int kStatOff = kGRingOff + kKVStages * kTBytes;  // [stage][2][BQ] floats: -LSE*log2e, -D
 constexpr int kStatBytes = 2 * BQ * 4;
 constexpr int kKVBarOff = kStatOff + kKVStages * kStatBytes;
-constexpr int kKVNumBars = 16;
+constexpr int kKVNumBars = 18;
 constexpr int kKVLaunchBytes = kKVBarOff + kKVNumBars * 8 + 16 + 1024;
 static_assert(kKVLaunchBytes <= 227 * 1024, "shared memory");
 
@@ -113,19 +117,24 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int K_FULL = 0;
-    const int V_FULL = 1;     // (dK pass) V of the key block in ring stage 0
+    const int V_FULL = 1;     // (dK pass) V of the key block in the Q ring's space
     const int V_COPIED = 2;   // ... copied into TMEM (4 compute warps)
     const int ACC_DONE = 3;
     const int MMA_DONE = 4;
     auto Q_FULL = [&](int s) { return 5 + s; };
     auto Q_EMPTY = [&](int s) { return 7 + s; };
-    auto ST_FULL = [&](int bf) { return 9 + bf; };   // S^T (and dP^T) of a tile in TMEM
-    auto PT_FULL = [&](int bf) { return 11 + bf; };  // P^T (dS^T) of a tile in TMEM (4 compute warps)
+    auto G_FULL = [&](int s) { return 9 + s; };      // dO
+    auto G_EMPTY = [&](int s) { return 11 + s; };
+    auto ST_FULL = [&](int bf) { return 13 + bf; };  // S^T (and dP^T) of a tile in TMEM
+    auto PT_FULL = [&](int bf) { return 15 + bf; };  // P^T (dS^T) of a tile in TMEM (4 compute warps)
+    // the ring that carries the statistics and is released by the accumulating MMA
+    auto L_FULL = [&](int s) { return kDK ? Q_FULL(s) : G_FULL(s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // key blocks of a (b, kv head) in order (causally the first are seen by the most queries)
-    const int nkb = (P.Tk + BKV - 1) / BKV;
-    const int kb = (int)blockIdx.x % nkb, kg = (int)blockIdx.x / nkb;
+    // key blocks in order, every (b, kv head)'s block kb before any one's block kb + 1
+    // (causally the first are seen by the most queries: the heaviest CTAs start first)
+    const int ng = P.Hkv * P.B;
+    const int kb = (int)blockIdx.x / ng, kg = (int)blockIdx.x % ng;
     const int kvh = kg % P.Hkv, b = kg / P.Hkv;
     const int j0 = kb * BKV;
     int qlo, qhi;
@@ -168,7 +177,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
                     tma_load_3d(sbase + kKOff + bx * (BKV * 128), &tmK, BAR(K_FULL), kvh * HD + bx * 64, j0, b);
             bool ok = true;
             if constexpr (kDK) {
-                // V through ring stage 0 into TMEM, before the first Q/dO tile lands there
+                // V through the Q ring's space (both stages) into TMEM, before the first tiles
                 if (elect_one()) mbar_expect_tx(BAR(V_FULL), kKBytes);
 #pragma unroll
                 for (int bx = 0; bx < kBoxes; ++bx)
@@ -176,31 +185,50 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
                         tma_load_3d(sbase + kRingOff + bx * (BKV * 128), &tmV, BAR(V_FULL), kvh * HD + bx * 64, j0, b);
                 ok = warp_wait(BAR(V_COPIED), 0, P.status, ST_BWD_PRODUCER, &abort_flag);
             }
-            int issued = 0;
+            int nq = 0, ngo = 0;  // Q and dO tiles issued
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int s = n % NS, use = n / NS;
-                if (use > 0 && !warp_wait(BAR(Q_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag))
-                    break;
                 const int h = tile_head(n), i0 = tile_i0(n);
-                const uint32_t qa = sbase + kRingOff + s * 2 * kTBytes, ga = qa + kTBytes;
-                if (elect_one()) mbar_expect_tx(BAR(Q_FULL(s)), 2 * kTBytes + kStatBytes);
-#pragma unroll
-                for (int bx = 0; bx < kBoxes; ++bx) {
-                    if (elect_one()) tma_load_3d(qa + bx * (BQ * 128), &tmQ, BAR(Q_FULL(s)), h * HD + bx * 64, i0, b);
-                    if (elect_one()) tma_load_3d(ga + bx * (BQ * 128), &tmG, BAR(Q_FULL(s)), h * HD + bx * 64, i0, b);
+                // -LSE*log2(e) and -D of these 64 rows (padded rows: -inf and 0), with the
+                // ring released last
+                auto stats = [&](int bar) {
+                    const long long srow = ((long long)b * P.H + h) * P.tq_pad + i0;
+                    const uint32_t sdst = sbase + kStatOff + s * kStatBytes;
+                    if (elect_one()) bulk_load(sdst, P.nlse2 + srow, BQ * 4, BAR(bar));
+                    if (elect_one()) bulk_load(sdst + BQ * 4, P.ndelta + srow, BQ * 4, BAR(bar));
+                };
+                if (use > 0 && !warp_wait(BAR(Q_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) {
+                    ok = false;
+                    break;
                 }
-                // -LSE*log2(e) and -D of these 64 rows (padded rows: -inf and 0)
-                const long long srow = ((long long)b * P.H + h) * P.tq_pad + i0;
-                const uint32_t sdst = sbase + kStatOff + s * kStatBytes;
-                if (elect_one()) bulk_load(sdst, P.nlse2 + srow, BQ * 4, BAR(Q_FULL(s)));
-                if (elect_one()) bulk_load(sdst + BQ * 4, P.ndelta + srow, BQ * 4, BAR(Q_FULL(s)));
-                issued = n + 1;
+                if (elect_one()) mbar_expect_tx(BAR(Q_FULL(s)), kTBytes + (kDK ? kStatBytes : 0));
+#pragma unroll
+                for (int bx = 0; bx < kBoxes; ++bx)
+                    if (elect_one())
+                        tma_load_3d(sbase + kRingOff + s * kTBytes + bx * (BQ * 128), &tmQ, BAR(Q_FULL(s)),
+                                    h * HD + bx * 64, i0, b);
+                if (kDK) stats(Q_FULL(s));
+                nq = n + 1;
+                if (use > 0 && !warp_wait(BAR(G_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (elect_one()) mbar_expect_tx(BAR(G_FULL(s)), kTBytes + (kDK ? 0 : kStatBytes));
+#pragma unroll
+                for (int bx = 0; bx < kBoxes; ++bx)
+                    if (elect_one())
+                        tma_load_3d(sbase + kGRingOff + s * kTBytes + bx * (BQ * 128), &tmG, BAR(G_FULL(s)),
+                                    h * HD + bx * 64, i0, b);
+                if (!kDK) stats(G_FULL(s));
+                ngo = n + 1;
             }
             // every copy in flight lands before the CTA exits
             mbar_wait(BAR(K_FULL), 0, P.status, ST_TEARDOWN, nullptr);
             if (kDK) mbar_wait(BAR(V_FULL), 0, P.status, ST_TEARDOWN, nullptr);
-            for (int n = max(0, issued - NS); n < issued; ++n)
+            for (int n = max(0, nq - NS); n < nq; ++n)
                 mbar_wait(BAR(Q_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
+            for (int n = max(0, ngo - NS); n < ngo; ++n)
+                mbar_wait(BAR(G_FULL(n % NS)), (n / NS) & 1, P.status, ST_TEARDOWN, nullptr);
         }
     } else if (warp == 5) {
         // ---------------------------------------------- MMA issuer (whole warp)
@@ -217,8 +245,9 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
             auto issue_s = [&](int n) -> bool {
                 const int s = n % NS, bf = kDK ? 0 : (n & 1);
                 if (!wait_all(Q_FULL(s), (n / NS) & 1)) return false;
+                if (kDK && !wait_all(G_FULL(s), (n / NS) & 1)) return false;
                 tc_fence_after();
-                const uint32_t qa = sbase + kRingOff + s * 2 * kTBytes, ga = qa + kTBytes;
+                const uint32_t qa = sbase + kRingOff + s * kTBytes, ga = sbase + kGRingOff + s * kTBytes;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
@@ -236,27 +265,29 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
                     }
                 }
                 if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
+                // the tile's ring read only by these MMAs is free once they complete
+                if (elect_one()) mma_commit(BAR(kDK ? G_EMPTY(s) : Q_EMPTY(s)));
                 return true;
             };
             if (ok) ok = issue_s(0);
             if (!kDK && ok && ntiles > 1) ok = issue_s(1);
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int s = n % NS, bf = kDK ? 0 : (n & 1);
-                if (!wait_all(PT_FULL(bf), kDK ? (n & 1) : ((n >> 1) & 1))) {
+                if (!wait_all(PT_FULL(bf), kDK ? (n & 1) : ((n >> 1) & 1)) ||
+                    (!kDK && !wait_all(G_FULL(s), (n / NS) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 // dV += P^T dO, or dK += dS^T Q: the 16-bit operand over the first 32
                 // columns of the S^T buffer, B = the tile's dO (Q) as [query][hd]
-                const uint32_t qa = sbase + kRingOff + s * 2 * kTBytes;
-                const uint32_t bsrc = kDK ? qa : qa + kTBytes;
+                const uint32_t bsrc = kDK ? sbase + kRingOff + s * kTBytes : sbase + kGRingOff + s * kTBytes;
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
                     if (elect_one())
                         mma_ts(tAcc, tbase + bf * 64 + kk * 8, sdesc_sw128(bsrc + kk * 2048, BQ * 128, 1024), idAcc,
                                (n > 0 || kk > 0) ? 1u : 0u);
-                if (elect_one()) mma_commit(BAR(Q_EMPTY(s)));
+                if (elect_one()) mma_commit(BAR(kDK ? Q_EMPTY(s) : G_EMPTY(s)));
                 const int nx = kDK ? n + 1 : n + 2;
                 if (nx < ntiles) ok = issue_s(nx);
             }
@@ -296,7 +327,7 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(BAR(V_COPIED));  // ring stage 0 may be reloaded
+                if (lane == 0) mbar_arrive(BAR(V_COPIED));  // the Q ring's space may be reloaded
             }
         }
         for (int n = 0; ok && n < ntiles; ++n) {
@@ -308,8 +339,8 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
             if (P.wr >= 0) clo = max(clo, j - P.wr - P.q_offset - i0);
             if (P.wl >= 0) chi = min(chi, j + P.wl - P.q_offset - i0 + 1);
             if (!key_live) chi = 0;
-            // the stats arrive with Q/dO of this tile; S^T (dP^T) come from the MMA
-            if (!wait_warp(Q_FULL(s), (n / NS) & 1) ||
+            // the stats arrive with the tile's later-released ring; S^T (dP^T) come from the MMA
+            if (!wait_warp(L_FULL(s), (n / NS) & 1) ||
                 !wait_warp(ST_FULL(bf), kDK ? (n & 1) : ((n >> 1) & 1))) {
                 ok = false;
                 break;
@@ -422,9 +453,10 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
     auto KV_EMPTY = [&](int s) { return 7 + NS + s; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // query blocks longest first (causally the last see the most keys)
-    const int nqb = (P.Tq + BQD - 1) / BQD;
-    const int qb = nqb - 1 - (int)blockIdx.x % nqb, hb = (int)blockIdx.x / nqb;
+    // query blocks longest first (causally the last see the most keys), every head's
+    // block qb before any one's block qb - 1
+    const int nqb = (P.Tq + BQD - 1) / BQD, nh = P.H * P.B;
+    const int qb = nqb - 1 - (int)blockIdx.x / nh, hb = (int)blockIdx.x % nh;
     const int h = hb % P.H, b = hb / P.H, kvh = h / P.G;
     const int i0 = qb * BQD;
     const int prow0 = i0 + P.q_offset, prow1 = min(i0 + BQD, P.Tq) - 1 + P.q_offset;

@@ -427,9 +427,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_any_kernel(Params P) {
 
 template <typename T>
 cudaError_t preprocess_typed(const Params& p, cudaStream_t s) {
-    // lanes per row = hd * sizeof(T) / 16 for hd 64 or 128; a warp per row otherwise
+    // lanes per row = hd * sizeof(T) / 16 for hd 64 or 128 (and 16-bit hd 256: a warp of
+    // 16-byte loads per row); a warp per row with element loads otherwise
     const int lpr = p.hd * (int)sizeof(T) / 16;
-    if (p.hd == 64 || p.hd == 128) {
+    if (p.hd == 64 || p.hd == 128 || (p.hd == 256 && sizeof(T) == 2)) {
         if (lpr == 8) return preprocess_launch<T, 8>(p, s);
         if (lpr == 16) return preprocess_launch<T, 16>(p, s);
         return preprocess_launch<T, 32>(p, s);
