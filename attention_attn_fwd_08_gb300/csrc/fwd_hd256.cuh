@@ -363,11 +363,16 @@ __global__ void __launch_bounds__(h256::kThreads, 1)
                         // a masked score is -inf, and softcap*tanh(-inf) would be finite
                         return f2_make(r0 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r0 * cap_in), m0),
                                        r1 == -INFINITY ? -INFINITY : fmaf(cap_out, tanh_accurate(r1 * cap_in), m1));
+                    } else if constexpr (kMode == 1) {
+                        // x = r * (sl2 + u * S'(u)) + m with u = r^2 and S' the fit's S with
+                        // scale * log2(e) folded in
+                        const CapPoly cp = cap_poly(P.scale, P.softcap);
+                        const uint64_t u = f2_mul(rr, rr);
+                        uint64_t sp = f2_fma(u, f2_mul(cp.s3, sl2_2), f2_mul(cp.s2, sl2_2));
+                        sp = f2_fma(u, sp, f2_mul(cp.s1, sl2_2));
+                        sp = f2_fma(u, sp, f2_mul(cp.s0, sl2_2));
+                        return f2_fma(rr, f2_fma(u, sp, sl2_2), nms);
                     } else {
-                        if constexpr (kMode == 1) {
-                            uint64_t uu;
-                            rr = cap_g(cap_poly(P.scale, P.softcap), rr, uu);
-                        }
                         return f2_fma(rr, sl2_2, nms);
                     }
                 };
