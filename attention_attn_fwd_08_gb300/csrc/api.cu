@@ -235,9 +235,8 @@ attn_status fwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
         return fill_empty(dt, o, (long long)B * Tq * H * hd, lse, lse ? (long long)B * H * Tq : 0, s);
     if (!p.status) return ATTN_ERR_CUDA;
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
-    // a bias with a softcap has no tensor-core form (the cap is not linear in the raw
-    // score): those calls take the CUDA-core kernels
-    if (!use_tc_fwd(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd) || hd == 256)))
+    // a bias at the padded head sizes or at hd 256 takes the CUDA-core kernels
+    if (!use_tc_fwd(dt, hd) || (p.bias && (padded_head(hd) || hd == 256)))
         return counted(launch_simt_fwd(p, (int)dt, s), 1);
     FwdMaps maps;
     const int kv_rows = hd == 256 ? 64 : 128;  // keys per tile
@@ -307,7 +306,7 @@ attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     p.tq_pad = (Tq + 63) / 64 * 64;
     p.ndelta = static_cast<float*>(workspace);
     p.nlse2 = p.ndelta + (size_t)B * H * p.tq_pad;
-    if (!use_tc_fwd(dt, hd) || (p.bias && (p.softcap > 0.f || padded_head(hd) || hd == 256))) {
+    if (!use_tc_fwd(dt, hd) || (p.bias && (padded_head(hd) || hd == 256))) {
         // the fp32 dQ pass reads D from the workspace: pass 4 implies pass 1 there
         const int ph = (phases & 4) ? (phases | 1) : phases;
         const int nks = ((ph & 1) ? 1 : 0) + ((ph & 2) ? 1 : 0) + ((ph & 4) ? 1 : 0);

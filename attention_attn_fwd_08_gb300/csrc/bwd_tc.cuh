@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
             if (P.wr >= 0) clo = max(clo, j - P.wr - P.q_offset - i0 - c0);
             if (P.wl >= 0) chi = min(chi, j + P.wl - P.q_offset - i0 - c0 + 1);
             if (!key_live) chi = 0;
-            // additive score bias of (query i0 + c0 + cc, key j) (never with softcap here): the
+            // additive score bias of (query i0 + c0 + cc, key j): the
             // first 32 columns' loads issue before the waits; rows past the last query read
             // the last row (finite; those columns are masked below), so the loads issue
             // back to back without a branch
@@ -320,7 +320,9 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(BAR(LD_DONE));
             }
-            if constexpr (BIAS) {
+            // the bias joins the raw score here, or, with a softcap (which comes first), the
+            // capped score inside the element loop (then kc = 32: bv0 holds the thread's columns)
+            if constexpr (BIAS && !cap) {
                 const float inv = 1.f / P.scale;
 #pragma unroll
                 for (int half = 0; half < kc / 32; ++half) {
@@ -370,10 +372,13 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                     const uint64_t dp2 = f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
                     float p0, p1, x0, x1;
                     uint64_t dcap = one2;
+                    // with a softcap, the bias (log2 units) joins after the cap
+                    uint64_t nlb = nl;
+                    if constexpr (BIAS && cap) nlb = f2_add(nl, f2_make(bv0[c] * kLog2e, bv0[c + 1] * kLog2e));
                     if constexpr (kMode == 2) {
                         // softcap*tanh(-inf) would be finite: keep a masked score at -inf
                         float l0, l1;
-                        f2_split(nl, l0, l1);
+                        f2_split(nlb, l0, l1);
                         const float t0 = tanh_accurate(s0 * cap_in), t1 = tanh_accurate(s1 * cap_in);
                         x0 = s0 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t0, l0);
                         x1 = s1 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t1, l1);
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                             f2_split(f2_fma(f2_mul(g, g), cap_poly(P.scale, P.softcap).nc2, one2), d0, d1);
                             dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
                         }
-                        f2_split(f2_fma(g, sl2_2, nl), x0, x1);
+                        f2_split(f2_fma(g, sl2_2, nlb), x0, x1);
                     }
                     p0 = fast_exp2(x0);
                     p1 = fast_exp2(x1);
@@ -1015,7 +1020,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 if (P.wl >= 0) clo = max(clo, p - P.wl - jc);
                 if (!row_ok) chi = 0;
                 // the additive bias of the row's 32 keys, loaded before the wait for S (0 past
-                // the keys; never with a softcap here)
+                // the keys)
                 float bv[BIAS ? 32 : 1];
                 if constexpr (BIAS) {
                     const float* brow = P.bias + (long long)it.b * P.bias_sb + (long long)it.h * P.bias_sh +
@@ -1046,7 +1051,9 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 tmem_ld_wait_only();
                 tmem_pin(sv);
                 tmem_pin(dp);
-                if constexpr (BIAS) {
+                // the bias joins the raw score here, or, with a softcap (which comes first),
+                // the capped score inside the element loop
+                if constexpr (BIAS && !cap) {
                     if (row_ok) {
                         const float inv = 1.f / P.scale;
 #pragma unroll
@@ -1084,11 +1091,17 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                         const uint64_t dp2 = f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
                         float x0, x1;
                         uint64_t dcap = one2;
+                        // the bias (with a softcap) in log2 units, added after the cap
+                        float b0 = 0.f, b1 = 0.f;
+                        if constexpr (BIAS && cap) {
+                            b0 = bv[c] * kLog2e;
+                            b1 = bv[c + 1] * kLog2e;
+                        }
                         if constexpr (kMode == 2) {
                             // softcap*tanh(-inf) would be finite: keep a masked score at -inf
                             const float t0 = tanh_accurate(s0 * cap_in), t1 = tanh_accurate(s1 * cap_in);
-                            x0 = s0 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t0, -lse2);
-                            x1 = s1 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t1, -lse2);
+                            x0 = s0 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t0, b0 - lse2);
+                            x1 = s1 == -INFINITY ? -INFINITY : fmaf(P.softcap * kLog2e, t1, b1 - lse2);
                             dcap = f2_make(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
                         } else {
                             uint64_t g = f2_make(s0, s1);
@@ -1108,7 +1121,8 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                                 f2_split(f2_fma(f2_mul(g, g), cap_poly(P.scale, P.softcap).nc2, one2), d0, d1);
                                 dcap = f2_make(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
                             }
-                            f2_split(f2_fma(g, sl2_2, nl2), x0, x1);
+                            if constexpr (BIAS && cap) f2_split(f2_fma(g, sl2_2, f2_add(nl2, f2_make(b0, b1))), x0, x1);
+                            else f2_split(f2_fma(g, sl2_2, nl2), x0, x1);
                         }
                         const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
                         uint64_t ds = f2_mul(f2_make(p0, p1), f2_add(dp2, nd2));
@@ -1227,10 +1241,10 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
     }
     if (phases & 4) {
         // a head size below HD (dense batches without a bias only) runs the padded instantiations
-        const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
+        const bool c = p.softcap > 0.f;
         auto k = p.hd != HD ? (c ? bwd_dq_kernel<BF16, HD, 12> : bwd_dq_kernel<BF16, HD, 8>)
                  : p.cu_q   ? (c ? bwd_dq_kernel<BF16, HD, 5> : bwd_dq_kernel<BF16, HD, 1>)
-                 : p.bias   ? bwd_dq_kernel<BF16, HD, 2>
+                 : p.bias   ? (c ? bwd_dq_kernel<BF16, HD, 6> : bwd_dq_kernel<BF16, HD, 2>)
                             : (c ? bwd_dq_kernel<BF16, HD, 4> : bwd_dq_kernel<BF16, HD, 0>);
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;
@@ -1244,10 +1258,10 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
-        const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
+        const bool c = p.softcap > 0.f;
         auto k = p.hd != HD ? (c ? bwd_dkdv_kernel<BF16, HD, 12> : bwd_dkdv_kernel<BF16, HD, 8>)
                  : p.cu_q   ? (c ? bwd_dkdv_kernel<BF16, HD, 5> : bwd_dkdv_kernel<BF16, HD, 1>)
-                 : p.bias   ? bwd_dkdv_kernel<BF16, HD, 2>
+                 : p.bias   ? (c ? bwd_dkdv_kernel<BF16, HD, 6> : bwd_dkdv_kernel<BF16, HD, 2>)
                             : (c ? bwd_dkdv_kernel<BF16, HD, 4> : bwd_dkdv_kernel<BF16, HD, 0>);
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);
         if (e != cudaSuccess) return e;

@@ -753,7 +753,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     if (P.wr >= 0) chi = min(chi, p + P.wr - j0 + 1);
                     if (P.wl >= 0) clo = max(clo, p - P.wl - j0);
                 }
-                // additive score bias (never with softcap here): loads issued before the waits
+                // additive score bias: loads issued before the waits
                 float bv[BIAS ? 128 : 1];
                 if constexpr (BIAS) {
                     if (i < tq) load_bias_row(P, it.b, it.h, i, j0, tk, bv);
@@ -789,6 +789,33 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     for (int c = 0; c < 4; ++c) {
                         tmem_ld32(tS + lane_off + c * 32, sv[c]);
                         tmem_ld_wait(sv[c]);
+                        if constexpr (cap) {
+                            // the cap comes before the bias: the capped score in raw-score
+                            // units, g = tanh(s * scale / softcap) * softcap / scale, by the
+                            // fitted polynomial where every raw score of the warp's chunk lies
+                            // in its range, else by the exp-based tanh
+                            const CapPoly cp = cap_poly(P.scale, P.softcap);
+                            float am = 0.f;
+#pragma unroll
+                            for (int e = 0; e < 32; e += 2)
+                                am = max3f(am, fabsf(__uint_as_float(sv[c][e])), fabsf(__uint_as_float(sv[c][e + 1])));
+                            if (__all_sync(0xffffffffu, am <= cp.r_max)) {
+#pragma unroll
+                                for (int e = 0; e < 32; e += 2) {
+                                    uint64_t uu;
+                                    float g0, g1;
+                                    f2_split(cap_g(cp, f2_make(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), uu),
+                                             g0, g1);
+                                    sv[c][e] = __float_as_uint(g0);
+                                    sv[c][e + 1] = __float_as_uint(g1);
+                                }
+                            } else {
+                                const float cap_in = P.scale / P.softcap, cap_back = P.softcap / P.scale;
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    sv[c][e] = __float_as_uint(tanh_accurate(__uint_as_float(sv[c][e]) * cap_in) * cap_back);
+                            }
+                        }
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             sv[c][e] = __float_as_uint(fmaf(bv[32 * c + e], inv, __uint_as_float(sv[c][e])));
@@ -798,7 +825,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_pin(sv[c]);
                 }
-                if (cap) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits, sv);
+                // (with a bias the cap was applied above, before the bias)
+                if (cap && !BIAS) run_tile(std::integral_constant<bool, true>(), m_used, l, k, full, clo, chi, mbits, sv);
                 else run_tile(std::integral_constant<bool, false>(), m_used, l, k, full, clo, chi, mbits, sv);
                 tmem_st_wait();
                 tc_fence_before();
@@ -900,13 +928,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
 template <bool BF16, int HD>
 cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     using C = Fwd2Cfg<HD>;
-    const bool c = p.softcap > 0.f;  // (a bias with a softcap never reaches this kernel)
+    const bool c = p.softcap > 0.f;
     // a head size below HD (dense batches without a bias only) runs the padded instantiations
     // the rotary query turn (dense batches at hd 64 / 128) runs the MODE & 16 instantiations
     auto kern = p.rope_tab  ? (c ? fwd_tc2_kernel<BF16, HD, 20> : fwd_tc2_kernel<BF16, HD, 16>)
                 : p.hd != HD ? (c ? fwd_tc2_kernel<BF16, HD, 12> : fwd_tc2_kernel<BF16, HD, 8>)
                 : p.cu_q   ? (c ? fwd_tc2_kernel<BF16, HD, 5> : fwd_tc2_kernel<BF16, HD, 1>)
-                : p.bias   ? fwd_tc2_kernel<BF16, HD, 2>
+                : p.bias   ? (c ? fwd_tc2_kernel<BF16, HD, 6> : fwd_tc2_kernel<BF16, HD, 2>)
                 : c        ? fwd_tc2_kernel<BF16, HD, 4>
                 : p.key_mask && p.B <= kMaskSpanMax ? fwd_tc2_kernel<BF16, HD, 32>
                                                     : fwd_tc2_kernel<BF16, HD, 0>;

@@ -232,8 +232,9 @@ ATTN_API attn_status attn_decode_len(attn_dtype dt, const void* q, const void* k
  *                bias[b*bias_sb + h*bias_sh + i*bias_sq + j*bias_sk], strides in
  *                elements (0 broadcasts a dimension), 4-byte aligned; NULL for none.
  *                A -inf entry drops that pair.  The gradient treats it as a constant.
- *   Everything else as attn_fwd / attn_bwd (key mask included).  16-bit calls with
- *   both a bias and a softcap run on the CUDA-core kernels (same results, slower).
+ *   Everything else as attn_fwd / attn_bwd (key mask included).  With a bias,
+ *   16-bit calls at hd 64 and 128 run on the tensor cores (with or without a
+ *   softcap); at hd 32, 96 and 256 on the CUDA-core kernels (same results, slower).
  */
 ATTN_API attn_status attn_fwd_ex(attn_dtype dt, const void* q, const void* k, const void* v, void* o,
                         float* lse, int B, int Tq, int Tk, int H, int Hkv, int hd, float scale,

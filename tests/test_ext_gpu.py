@@ -1,7 +1,8 @@
 """Two-sided windows and the additive score bias on the GPU against the fp64
 oracle (fwd_ex / bwd_ex): every page's window rule, broadcast bias shapes,
--inf bias entries (a fully dropped row included), the CUDA-core route for a
-bias with a softcap, and the plain causal/window calls reproduced bit for bit.
+-inf bias entries (a fully dropped row included), a bias together with a softcap
+(the cap first, then the bias), and the plain causal/window calls reproduced bit
+for bit.
 Every call goes through the C ABI."""
 import math
 
@@ -86,8 +87,18 @@ def test_bias_with_minus_inf_entries(hd):
     run_ex("bf16", 2, 200, 200, 4, 2, hd, seed=831, wl=-1, wr=0, bias=b)
 
 
-def test_bias_with_softcap_takes_the_cuda_core_kernels():
-    run_ex("bf16", 1, 140, 140, 2, 1, 128, seed=840, wl=30, wr=30, softcap=5.0, bias=bias_of((1, 2, 140, 140), 841))
+@pytest.mark.parametrize("dt,hd,softcap", [("bf16", 128, 5.0), ("f16", 64, 30.0), ("bf16", 128, 50.0)])
+def test_bias_with_softcap(dt, hd, softcap):
+    """The tensor-core kernels with the cap applied before the bias: a small softcap
+    (scores beyond the fitted polynomial's range: the exp-based tanh), moderate ones
+    (the polynomial tiers), several tiles, a ragged tail and -inf bias entries."""
+    b = bias_of((2, 4, 300, 300), 841, holes=True)
+    run_ex(dt, 2, 300, 300, 4, 2, hd, seed=840, wl=30, wr=30, softcap=softcap, bias=b)
+    run_ex(dt, 1, 260, 260, 4, 2, hd, seed=842, wl=-1, wr=0, softcap=softcap, bias=bias_of((1, 4, 260, 260), 843))
+
+
+def test_bias_with_softcap_padded_head_takes_the_cuda_core_kernels():
+    run_ex("bf16", 1, 140, 140, 2, 1, 96, seed=844, wl=30, wr=30, softcap=5.0, bias=bias_of((1, 2, 140, 140), 845))
 
 
 def test_bias_fp32():
