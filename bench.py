@@ -735,6 +735,17 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
         tf = fl * wb.hd * pairs / (t[n] * 1e-3) / 1e12
         out["bias_prefill_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
                                     "visible_pairs": pairs, "note": "GQA causal prefill with a [1,1,T,T] fp32 bias"}
+    # the same with a softcap of 50 (the cap applied to the score, then the bias)
+    kwc = dict(kw, softcap=50.0)
+    t = time_passes(torch, stream, [
+        ("fwd", lambda: A.attn_fwd_ex(q, k, v, o=o, lse=lse, **kwc)),
+        ("bwd", lambda: A.attn_bwd_ex(q, k, v, o, do, lse, dq=dq, dk=dk, dv=dv, workspace=wsb, **kwc))], args,
+        flush_buf)
+    for n, fl in (("fwd", 4), ("bwd", 10)):
+        tf = fl * wb.hd * pairs / (t[n] * 1e-3) / 1e12
+        out["bias_softcap_prefill_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                            "visible_pairs": pairs,
+                                            "note": "GQA causal prefill with a [1,1,T,T] fp32 bias and softcap 50"}
     # the GQA causal prefill's width at head size 256 (tensor cores; the backward as D,
     # dV, dK and dQ passes, flops counted as 10*hd per visible pair like the other backwards)
     w2 = synth.WORKLOADS["gqa_prefill_hd256"]
