@@ -303,8 +303,8 @@ ATTN_API attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k
  * cudaMalloc and have no scratch buffer to pass in: for example a plugin that
  * is handed only its input and output buffers, a serving loop that forbids
  * device allocation after start-up so that a request can never fail for lack
- * of memory, or a C caller with no device allocator of its own.  The paper
- * has no counterpart to this call; it exists for those callers.
+ * of memory, or a C caller with no device allocator of its own.  None of the
+ * sources cited in this header defines such a call; it exists for those callers.
  *
  * Same arguments, kernels and results as attn_decode.  The split partials
  * live in one fixed array of 32 MiB that the library reserves in device
