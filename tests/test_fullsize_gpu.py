@@ -157,14 +157,16 @@ def test_varlen_packed_fwd_bwd_full():
                       (gq, gk[:, g0:], gv[:, g0:]), w.dtype, what)
 
 
-def test_bias_prefill_fwd_bwd_full():
-    """The bench's biased GQA prefill: causal (window_right 0) with a [1, 1, T, T] fp32 bias."""
+@pytest.mark.parametrize("softcap", [0.0, 50.0], ids=["bias", "bias-softcap50"])
+def test_bias_prefill_fwd_bwd_full(softcap):
+    """The bench's biased GQA prefill: causal (window_right 0) with a [1, 1, T, T] fp32 bias,
+    without and with a softcap (the cap applied to the score, then the bias)."""
     w = synth.WORKLOADS["gqa_prefill"]
     inp = synth.make_inputs(w)
     bias = synth.normal((1, 1, w.Tq, w.Tk), w.seed + 5, "f32")
     dev = "cuda"
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
-    kw = dict(H=w.H, Hkv=w.Hkv, scale=w.scale, window_left=-1, window_right=0)
+    kw = dict(H=w.H, Hkv=w.Hkv, scale=w.scale, window_left=-1, window_right=0, softcap=softcap)
     o, lse = A.attn_fwd_ex(q, k, v, bias=bias.to(dev), **kw)
     dq, dk, dv = A.attn_bwd_ex(q, k, v, o, do, lse, bias=bias.to(dev), **kw)
     torch.cuda.synchronize()
@@ -177,7 +179,8 @@ def test_bias_prefill_fwd_bwd_full():
         ks = f64(inp["k"][b:b + 1, :r1, kvh * hd:(kvh + 1) * hd])
         vs = f64(inp["v"][b:b + 1, :r1, kvh * hd:(kvh + 1) * hd])
         bs = f64(bias[:, :, r0:r1, :r1])
-        okw = dict(H=G, Hkv=1, scale=w.scale, window_left=-1, window_right=0, q_offset=r0, bias=bs)
+        okw = dict(H=G, Hkv=1, scale=w.scale, window_left=-1, window_right=0, q_offset=r0, bias=bs,
+                   softcap=softcap)
         o_ref, lse_ref = oracle.fwd_ex(qs, ks, vs, **okw)
         what = "bias b%d kvh%d rows[%d,%d)" % (b, kvh, r0, r1)
         compare_o_lse(o[b:b + 1, r0:r1, kvh * G * hd:(kvh + 1) * G * hd], lse[b:b + 1, kvh * G:(kvh + 1) * G, r0:r1],
