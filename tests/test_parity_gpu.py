@@ -385,6 +385,17 @@ def test_bwd_hd256_tensor_core(dt, flags):
     run_fwd_case(dt, 2, Tq, Tq + flags.get("q_offset", 0), 4, 2, 256, backward=True, seed=1990, **flags)
 
 
+@pytest.mark.parametrize("case", [
+    dict(B=1, Tq=5, Tk=70, H=2, Hkv=2, causal=False),                 # one query block, G = 1
+    dict(B=2, Tq=64, Tk=65, H=3, Hkv=1, causal=True, q_offset=1),     # a key past one tile, G = 3
+    dict(B=1, Tq=3, Tk=300, H=4, Hkv=2, causal=True, q_offset=297),   # decode-like rows
+], ids=["tiny-g1", "tile-edge-g3", "decode-like"])
+def test_bwd_hd256_edges(case):
+    c = dict(case)
+    B, Tq, Tk, H, Hkv = (c.pop(n) for n in ("B", "Tq", "Tk", "H", "Hkv"))
+    run_fwd_case("bf16", B, Tq, Tk, H, Hkv, 256, backward=True, seed=1997, **c)
+
+
 def test_bwd_hd256_many_blocks():
     # more key blocks and query blocks (3 x 8 x 3, 3 x 32 x 3) than SMs, group of four heads
     run_fwd_case("bf16", 3, 300, 300, 32, 8, 256, causal=True, backward=True, seed=1995)
