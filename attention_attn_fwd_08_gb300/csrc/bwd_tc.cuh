@@ -59,7 +59,7 @@ struct KVCfg {
     static constexpr int BKV = 128;  // keys per CTA
     static constexpr int BQ = 64;    // query rows per inner tile
     static constexpr int kBoxes = HD / 64;
-    static constexpr int kStages = HD == 128 ? 3 : 4;
+    static constexpr int kStages = 4;
     static constexpr int kKVBytes = BKV * HD * 2;
     static constexpr int kQBytes = BQ * HD * 2;  // one Q (or dO) tile
     static constexpr int kKOff = 0;
@@ -72,9 +72,10 @@ struct KVCfg {
     static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1 + 1;
     // epilogue staging: 32-row x 64-column slices of 4 KB, two per compute warp
     // (one with eight compute warps)
-    static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
-    static constexpr int kBytes = kStgOff + 8 * 4096;
+    static constexpr int kStgOff = kQOff;  // the Q ring, free once every tile's MMAs completed
+    static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+    static_assert(kStages * kQBytes >= 8 * 4096, "staging fits in the Q ring");
 };
 
 // MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
         // them by q % 2, one staging slice each.
         const bool have = ok && ntiles > 0 && warp_wait(BAR(ACC_DONE), 0, P.status, ST_BWD_COMPUTE, &abort_flag);
         if (have) tc_fence_after();
+        fence_proxy_async_smem();  // the staging slices reuse the Q ring the tensor core read
         // A packed sequence's last keys may share a 32-row slice with the next
         // sequence's first: such a slice goes out row by row (this sequence's rows
         // only).  Dense tensors end where the maps end, which clips the tiled store.
