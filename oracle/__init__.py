@@ -316,3 +316,73 @@ def rope(x, *, head_dim, pos=0, theta=10000.0):
             out[:, s, :, i] = a * c - b * sn
             out[:, s, :, i + half] = b * c + a * sn
     return out.reshape(B, T, C)
+
+
+def _packed_rows(seq_bounds, L, window):
+    """Visible keys of every row of a packed fused-QKV batch: row r attends keys j of
+    its own sequence, seq_bounds[r, 0] <= j < seq_bounds[r, 1], and with window > 0
+    only those with |r - j| <= window // 2 (brotensor ops/flash_attention.h,
+    flash_attention_packed_qkv_forward)."""
+    sb = np.asarray(seq_bounds, dtype=np.int64).reshape(L, 2)
+    rows = []
+    for r in range(L):
+        j = np.arange(max(int(sb[r, 0]), 0), min(int(sb[r, 1]), L))
+        if window > 0:
+            j = j[np.abs(r - j) <= window // 2]
+        rows.append(j)
+    return rows
+
+
+def _split_qkv(qkv, H):
+    qkv = _f64(qkv)
+    L, C = qkv.shape
+    hd = C // (3 * H)
+    if 3 * H * hd != C:
+        raise ValueError("qkv rows must hold 3 * H * head_dim values")
+    return (qkv[:, :H * hd].reshape(L, H, hd), qkv[:, H * hd:2 * H * hd].reshape(L, H, hd),
+            qkv[:, 2 * H * hd:].reshape(L, H, hd), L, hd)
+
+
+def packed_qkv_fwd(qkv, seq_bounds, *, H, scale, window=0):
+    """Packed bidirectional self-attention straight off a fused QKV projection
+    (brotensor ops/flash_attention.h, flash_attention_packed_qkv_forward): qkv is
+    [L, 3*H*hd], each row [q heads | k heads | v heads]; the visible keys of row r
+    are those of _packed_rows.  Written out row by row in numpy fp64 (independent of
+    attn_oracle.c).  Returns O [L, H*hd] and LSE [H, L] (-inf for a row that sees
+    no key, whose O is 0)."""
+    q, k, v, L, hd = _split_qkv(qkv, H)
+    o = np.zeros((L, H, hd))
+    lse = np.full((H, L), -np.inf)
+    for r, j in enumerate(_packed_rows(seq_bounds, L, window)):
+        if j.size == 0:
+            continue
+        s = scale * np.einsum("hd,jhd->hj", q[r], k[j])  # [H, keys]
+        mx = s.max(axis=1, keepdims=True)
+        p = np.exp(s - mx)
+        l = p.sum(axis=1, keepdims=True)
+        o[r] = np.einsum("hj,jhd->hd", p / l, v[j])
+        lse[:, r] = (mx + np.log(l))[:, 0]
+    return o.reshape(L, H * hd), lse
+
+
+def packed_qkv_bwd(qkv, do, seq_bounds, *, H, scale, window=0):
+    """Backward of packed_qkv_fwd (brotensor flash_attention_packed_qkv_backward):
+    dQKV [L, 3*H*hd], each row [dQ heads | dK heads | dV heads].  Per row r and head:
+    P = softmax(scale * q_r . k_j) over its visible keys, dP_j = dO_r . v_j,
+    dS = P (dP - sum(P dP)), dq_r = scale * sum_j dS_j k_j, dk_j += scale * dS_j q_r,
+    dv_j += P_j dO_r; row by row in numpy fp64."""
+    q, k, v, L, hd = _split_qkv(qkv, H)
+    do = _f64(do).reshape(L, H, hd)
+    dq, dk, dv = np.zeros((L, H, hd)), np.zeros((L, H, hd)), np.zeros((L, H, hd))
+    for r, j in enumerate(_packed_rows(seq_bounds, L, window)):
+        if j.size == 0:
+            continue
+        s = scale * np.einsum("hd,jhd->hj", q[r], k[j])
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        dp = np.einsum("hd,jhd->hj", do[r], v[j])
+        ds = p * (dp - (p * dp).sum(axis=1, keepdims=True))
+        dq[r] = scale * np.einsum("hj,jhd->hd", ds, k[j])
+        dk[j] += scale * np.einsum("hj,hd->jhd", ds, q[r])
+        dv[j] += np.einsum("hj,hd->jhd", p, do[r])
+    return np.concatenate([dq.reshape(L, -1), dk.reshape(L, -1), dv.reshape(L, -1)], axis=1)
