@@ -21,7 +21,7 @@ import os
 import threading
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_decode_len", "attn_varlen_fwd", "attn_varlen_bwd", "attn_fwd_ex", "attn_bwd_ex", "attn_rope", "attn_bwd_workspace_size", "attn_decode_workspace_size", "attn_decode_plan",
-           "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_kernel_family_bwd", "attn_fwd_rope", "attn_bwd_rope", "attn_fwd_rope_workspace_size", "attn_bwd_rope_workspace_size", "attn_launch_count", "AttnError", "lib",
+           "attn_get_device_status", "attn_selftest_bounded_wait", "attn_kernel_family", "attn_kernel_family_bwd", "attn_fwd_rope", "attn_bwd_rope", "attn_fwd_rope_workspace_size", "attn_bwd_rope_workspace_size", "attn_launch_count", "attn_packed_qkv_fwd", "attn_packed_qkv_bwd", "attn_packed_qkv_workspace_size", "AttnError", "lib",
            "library_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +83,12 @@ def lib():
         L.attn_varlen_fwd.restype = i
         L.attn_varlen_bwd.argtypes = [i] + [vp] * 10 + [sz, vp, vp] + [i] * 8 + [f, i, i, f, vp]
         L.attn_varlen_bwd.restype = i
+        L.attn_packed_qkv_workspace_size.argtypes = [i, i, i, i, i]
+        L.attn_packed_qkv_workspace_size.restype = sz
+        L.attn_packed_qkv_fwd.argtypes = [i, vp, vp, vp, vp, vp, sz, i, i, i, f, i, vp]
+        L.attn_packed_qkv_fwd.restype = i
+        L.attn_packed_qkv_bwd.argtypes = [i, vp, vp, vp, vp, vp, sz, i, i, i, f, i, vp]
+        L.attn_packed_qkv_bwd.restype = i
         L.attn_status_string.argtypes = [i]
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
@@ -548,3 +554,67 @@ def attn_kernel_family(dtype: str, hd: int) -> int:
 def attn_kernel_family_bwd(dtype: str, hd: int) -> int:
     """1 when attn_bwd runs (dtype, hd) on the tensor cores, 0 on the CUDA-core kernels."""
     return int(lib().attn_kernel_family_bwd(_DT[dtype], int(hd)))
+
+
+# ------------------------------------------------------------ packed fused-QKV rows
+def _packed_dims(qkv, seq_bounds, H):
+    torch = _torch()
+    if qkv.dim() != 2 or qkv.shape[1] % (3 * H):
+        raise ValueError("qkv must be [L, 3*H*hd]")
+    L = int(qkv.shape[0])
+    if seq_bounds.dtype != torch.int32 or tuple(seq_bounds.shape) != (L, 2) or not seq_bounds.is_contiguous():
+        raise ValueError("seq_bounds must be a contiguous int32 tensor of shape [L, 2]")
+    return L, int(qkv.shape[1]) // (3 * H)
+
+
+def attn_packed_qkv_workspace_size(dtype: str, L: int, H: int, hd: int, backward: bool = False) -> int:
+    """Workspace bytes attn_packed_qkv_fwd (or, with backward, attn_packed_qkv_bwd) needs."""
+    return int(lib().attn_packed_qkv_workspace_size(_DT[dtype], int(L), int(H), int(hd), int(bool(backward))))
+
+
+def attn_packed_qkv_fwd(qkv, seq_bounds, *, H, scale=None, window=0, o=None, lse=None, want_lse=True, workspace=None,
+                        stream=None):
+    """Packed bidirectional self-attention off a fused QKV projection: qkv [L, 3*H*hd] rows
+    [q heads | k heads | v heads]; row r attends the keys of its own sequence, rows
+    seq_bounds[r, 0] .. seq_bounds[r, 1]-1 (int32 [L, 2] on the device), within
+    |r - j| <= window // 2 when window > 0.  Returns (o [L, H*hd], lse [H, L])."""
+    torch = _torch()
+    _contig(qkv, seq_bounds, o, lse)
+    L, hd = _packed_dims(qkv, seq_bounds, H)
+    if o is not None and (o.device != qkv.device or o.dtype != qkv.dtype or tuple(o.shape) != (L, H * hd)):
+        raise ValueError("o must be a %s tensor of shape %s on %s" % (qkv.dtype, (L, H * hd), qkv.device))
+    _placed(qkv, f32=[("lse", lse, (H, L))], device=[("seq_bounds", seq_bounds), ("workspace", workspace)])
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    o = torch.empty((L, H * hd), dtype=qkv.dtype, device=qkv.device) if o is None else o
+    if lse is None and want_lse:
+        lse = torch.empty((H, L), dtype=torch.float32, device=qkv.device)
+    nbytes = lib().attn_packed_qkv_workspace_size(_dt(qkv), L, H, hd, 0)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=qkv.device)
+    st = lib().attn_packed_qkv_fwd(_dt(qkv), _ptr(qkv), _ptr(seq_bounds), _ptr(o), _ptr(lse), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), L, H, hd, float(scale), int(window),
+                                   _stream(stream))
+    _check(st, "attn_packed_qkv_fwd")
+    return o, lse
+
+
+def attn_packed_qkv_bwd(qkv, do, seq_bounds, *, H, scale=None, window=0, dqkv=None, workspace=None, stream=None):
+    """Backward of attn_packed_qkv_fwd from do [L, H*hd]: returns dqkv [L, 3*H*hd] (rows
+    [dq | dk | dv]), overwritten; O and LSE are formed again from qkv."""
+    torch = _torch()
+    _contig(qkv, do, seq_bounds, dqkv)
+    L, hd = _packed_dims(qkv, seq_bounds, H)
+    for name, t, shape in (("do", do, (L, H * hd)), ("dqkv", dqkv, (L, 3 * H * hd))):
+        if t is not None and (t.device != qkv.device or t.dtype != qkv.dtype or tuple(t.shape) != shape):
+            raise ValueError("%s must be a %s tensor of shape %s on %s" % (name, qkv.dtype, shape, qkv.device))
+    _placed(qkv, device=[("seq_bounds", seq_bounds), ("workspace", workspace)])
+    scale = 1.0 / math.sqrt(hd) if scale is None else scale
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    nbytes = lib().attn_packed_qkv_workspace_size(_dt(qkv), L, H, hd, 1)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=qkv.device)
+    st = lib().attn_packed_qkv_bwd(_dt(qkv), _ptr(qkv), _ptr(do), _ptr(seq_bounds), _ptr(dqkv), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), L, H, hd, float(scale), int(window),
+                                   _stream(stream))
+    _check(st, "attn_packed_qkv_bwd")
+    return dqkv

@@ -235,8 +235,9 @@ attn_status fwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
         return fill_empty(dt, o, (long long)B * Tq * H * hd, lse, lse ? (long long)B * H * Tq : 0, s);
     if (!p.status) return ATTN_ERR_CUDA;
     p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
-    // a bias at the padded head sizes or at hd 256 takes the CUDA-core kernels
-    if (!use_tc_fwd(dt, hd) || (p.bias && (padded_head(hd) || hd == 256)))
+    // a bias or packed fused-QKV rows at the padded head sizes or at hd 256 take the
+    // CUDA-core kernels
+    if (!use_tc_fwd(dt, hd) || ((p.bias || p.row_bounds) && (padded_head(hd) || hd == 256)))
         return counted(launch_simt_fwd(p, (int)dt, s), 1);
     FwdMaps maps;
     const int kv_rows = hd == 256 ? 64 : 128;  // keys per tile
@@ -306,7 +307,7 @@ attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     p.tq_pad = (Tq + 63) / 64 * 64;
     p.ndelta = static_cast<float*>(workspace);
     p.nlse2 = p.ndelta + (size_t)B * H * p.tq_pad;
-    if (!use_tc_fwd(dt, hd) || (p.bias && (padded_head(hd) || hd == 256))) {
+    if (!use_tc_fwd(dt, hd) || ((p.bias || p.row_bounds) && (padded_head(hd) || hd == 256))) {
         // the fp32 dQ pass reads D from the workspace: pass 4 implies pass 1 there
         const int ph = (phases & 4) ? (phases | 1) : phases;
         const int nks = ((ph & 1) ? 1 : 0) + ((ph & 2) ? 1 : 0) + ((ph & 4) ? 1 : 0);
@@ -787,6 +788,104 @@ attn_status attn_selftest_bounded_wait(unsigned int timeout_us, void* stream) {
     unsigned int* ptr = status_ptr();
     if (!ptr) return ATTN_ERR_CUDA;
     return counted(launch_selftest_wait(ptr, timeout_us, static_cast<cudaStream_t>(stream)), 1);
+}
+
+}  // extern "C"
+
+// --------------------------------------------------- packed fused-QKV rows
+namespace {
+
+// The q, k and v columns of a packed [L][3*H*hd] row block copied into three
+// contiguous [L][H*hd] tensors (one strided copy each).
+attn_status split_qkv(attn_dtype dt, const void* qkv, void* q, void* k, void* v, int L, int H, int hd,
+                      cudaStream_t s) {
+    const size_t w = (size_t)H * hd * elem_size(dt);
+    const uint8_t* src = static_cast<const uint8_t*>(qkv);
+    void* dst[3] = {q, k, v};
+    for (int t = 0; t < 3; ++t)
+        if (cudaMemcpy2DAsync(dst[t], w, src + t * w, 3 * w, w, (size_t)L, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status check_packed(attn_dtype dt, const void* qkv, const int* seq_bounds, int L, int H, int hd, float scale,
+                         int window) {
+    if (L < 0 || window < 0) return ATTN_ERR_INVALID_ARG;
+    attn_status st = check_common(dt, 1, L, L, H, H, hd, scale, 0, 0, 0.f, 0, nullptr, 0);
+    if (st != ATTN_OK) return st;
+    if (L > 0 && (!qkv || !seq_bounds || !aligned16(qkv) || (reinterpret_cast<uintptr_t>(seq_bounds) & 7u)))
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+// One batch of L rows, keys and queries alike, no causal rule; brotensor's
+// bidirectional window |r - j| <= window/2 is the two-sided window (window/2, window/2).
+Params packed_params(const int* seq_bounds, int L, int H, int hd, float scale, int window) {
+    Params p = base_params(1, L, L, H, H, hd, scale, 0, 0, 0.f, 0, nullptr, 0);
+    p.wl = p.wr = window > 0 ? window / 2 : -1;
+    p.row_bounds = reinterpret_cast<const int2*>(seq_bounds);
+    return p;
+}
+
+size_t tensor_bytes(attn_dtype dt, int L, int H, int hd) { return align256((size_t)L * H * hd * elem_size(dt)); }
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_packed_qkv_workspace_size(attn_dtype dt, int L, int H, int hd, int backward) {
+    if (L < 0 || H <= 0 || hd <= 0) return 0;
+    const size_t t = tensor_bytes(dt, L, H, hd);
+    if (!backward) return 3 * t;  // q, k, v
+    // q, k, v, O, LSE, dq, dk, dv and the backward's own workspace
+    return 7 * t + align256((size_t)H * L * sizeof(float)) + align256(attn_bwd_workspace_size(1, L, H));
+}
+
+attn_status attn_packed_qkv_fwd(attn_dtype dt, const void* qkv, const int* seq_bounds, void* o, float* lse,
+                                void* workspace, size_t workspace_bytes, int L, int H, int hd, float scale,
+                                int window, void* stream) {
+    attn_status st = check_packed(dt, qkv, seq_bounds, L, H, hd, scale, window);
+    if (st != ATTN_OK) return st;
+    if (L == 0) return ATTN_OK;
+    if (!o || !workspace || !aligned16(workspace) || workspace_bytes < attn_packed_qkv_workspace_size(dt, L, H, hd, 0))
+        return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t t = tensor_bytes(dt, L, H, hd);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if ((st = split_qkv(dt, qkv, ws, ws + t, ws + 2 * t, L, H, hd, s)) != ATTN_OK) return st;
+    return fwd_launch(dt, ws, ws + t, ws + 2 * t, o, lse, packed_params(seq_bounds, L, H, hd, scale, window), stream);
+}
+
+attn_status attn_packed_qkv_bwd(attn_dtype dt, const void* qkv, const void* dout, const int* seq_bounds, void* dqkv,
+                                void* workspace, size_t workspace_bytes, int L, int H, int hd, float scale,
+                                int window, void* stream) {
+    attn_status st = check_packed(dt, qkv, seq_bounds, L, H, hd, scale, window);
+    if (st != ATTN_OK) return st;
+    if (L == 0) return ATTN_OK;
+    if (!dout || !dqkv || !aligned16(dout) || !aligned16(dqkv) || !workspace || !aligned16(workspace) ||
+        workspace_bytes < attn_packed_qkv_workspace_size(dt, L, H, hd, 1))
+        return ATTN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t t = tensor_bytes(dt, L, H, hd), lse_bytes = align256((size_t)H * L * sizeof(float));
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint8_t *q = ws, *k = ws + t, *v = ws + 2 * t, *o = ws + 3 * t;
+    float* lse = reinterpret_cast<float*>(ws + 4 * t);
+    uint8_t *dq = ws + 4 * t + lse_bytes, *dk = dq + t, *dv = dq + 2 * t, *wb = dq + 3 * t;
+    const Params p = packed_params(seq_bounds, L, H, hd, scale, window);
+    // the backward consumes no forward results: O and LSE are formed again here
+    if ((st = split_qkv(dt, qkv, q, k, v, L, H, hd, s)) != ATTN_OK) return st;
+    if ((st = fwd_launch(dt, q, k, v, o, lse, p, stream)) != ATTN_OK) return st;
+    if ((st = bwd_launch(dt, q, k, v, o, dout, lse, dq, dk, dv, wb, attn_bwd_workspace_size(1, L, H), p, stream, 7)) !=
+        ATTN_OK)
+        return st;
+    // dq, dk, dv into their columns of the packed gradient rows
+    const size_t w = (size_t)H * hd * elem_size(dt);
+    const void* src[3] = {dq, dk, dv};
+    for (int c = 0; c < 3; ++c)
+        if (cudaMemcpy2DAsync(static_cast<uint8_t*>(dqkv) + c * w, 3 * w, src[c], w, w, (size_t)L,
+                              cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    return ATTN_OK;
 }
 
 }  // extern "C"

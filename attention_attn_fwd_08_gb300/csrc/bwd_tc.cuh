@@ -80,7 +80,8 @@ struct KVCfg {
 
 // MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
 // an additive score bias; MODE & 4: softcap; MODE & 8: a head size below HD through
-// 4-D maps (the columns past the head load as zeros and are never stored).  Each
+// 4-D maps (the columns past the head load as zeros and are never stored); MODE 64:
+// packed fused-QKV rows of one batch, each row limited to its own sequence.  Each
 // instantiation carries only its own bookkeeping (the softcap's registers, live through
 // the tile loop, made the plain path spill when it was a run-time branch).
 template <bool BF16, int HD, int MODE>
@@ -93,6 +94,8 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
     constexpr int NCW = dkdv_compute_warps(MODE), HF = NCW / 4;  // HF warps per key row
     constexpr int PRODUCER = NCW, MMA = NCW + 1;
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
+    constexpr bool RB = (MODE & 64) != 0;  // packed fused-QKV rows: per-row sequence bounds
+    static_assert(!RB || MODE == 64, "the row bounds are built for dense batches without other modes");
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,6 +131,10 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
     if (j0 >= sq.tk) return;  // (packed) past this sequence's keys: nothing to write
     int qlo, qhi;
     query_range(P.wl, P.wr, sq.tq, P.q_offset, j0, min(j0 + BKV, sq.tk), &qlo, &qhi);
+    if constexpr (RB) {  // packed fused-QKV rows: a key is seen only from its own sequence
+        qlo = max(qlo, row_keys(P, j0, sq.tq).x);
+        qhi = max(qlo, min(qhi, row_keys(P, min(j0 + BKV, sq.tk) - 1, sq.tq).y));
+    }
     const int qt0 = qlo / BQ;
     const int nqt = qhi > qlo ? (qhi + BQ - 1) / BQ - qt0 : 0;
     const int ntiles = nqt * P.G;  // (head, query tile) pairs, head-major
@@ -263,6 +270,8 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
         const int j = j0 + r;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const bool key_live = j < sq.tk && (!P.key_mask || P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f);
+        int2 rk_key = make_int2(0, sq.tq);  // packed fused-QKV rows: this key's sequence
+        if constexpr (RB) rk_key = row_keys(P, max(min(j, sq.tk - 1), 0), sq.tq);
         constexpr bool cap = (MODE & 4) != 0;
         constexpr int kc = BQ / HF;  // query columns per thread
         const float cap_in = P.scale / fmaxf(P.softcap, 1e-30f);
@@ -277,6 +286,10 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
             // query position p sees key j when p - wl <= j <= p + wr
             if (P.wr >= 0) clo = max(clo, j - P.wr - P.q_offset - i0 - c0);
             if (P.wl >= 0) chi = min(chi, j + P.wl - P.q_offset - i0 - c0 + 1);
+            if constexpr (RB) {  // packed fused-QKV rows: the queries of this key's sequence
+                clo = max(clo, rk_key.x - i0 - c0);
+                chi = min(chi, rk_key.y - i0 - c0);
+            }
             if (!key_live) chi = 0;
             // additive score bias of (query i0 + c0 + cc, key j): the
             // first 32 columns' loads issue before the waits; rows past the last query read
@@ -620,7 +633,7 @@ struct DqItem {
     int b, h, kvh, i0, kt0, ntiles;
     Seq sq;
 };
-template <int BQ, int BK, bool VL>
+template <int BQ, int BK, bool VL, bool RB = false>
 __device__ __forceinline__ DqItem dq_item_at(const Params& P, int b, int h, int qb) {
     DqItem it;
     it.h = h;
@@ -629,9 +642,14 @@ __device__ __forceinline__ DqItem dq_item_at(const Params& P, int b, int h, int 
     it.i0 = qb * BQ;
     it.sq = seq_of<VL>(P, it.b);
     int lo = 0, hi = 0;
-    if (it.i0 < it.sq.tq)  // (packed) items past a sequence's rows have no tiles
-        key_range(P.wl, P.wr, it.sq.tk, it.i0 + P.q_offset, min(it.i0 + BQ, it.sq.tq) - 1 + P.q_offset, &lo,
-                  &hi);
+    if (it.i0 < it.sq.tq) {  // (packed) items past a sequence's rows have no tiles
+        const int ilast = min(it.i0 + BQ, it.sq.tq) - 1;
+        key_range(P.wl, P.wr, it.sq.tk, it.i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+        if constexpr (RB) {  // packed fused-QKV rows: between the first row's sequence start and the last's end
+            lo = max(lo, row_keys(P, it.i0, it.sq.tk).x);
+            hi = max(lo, min(hi, row_keys(P, ilast, it.sq.tk).y));
+        }
+    }
     it.kt0 = lo / BK;
     it.ntiles = hi > lo ? (hi + BK - 1) / BK - it.kt0 : 0;
     return it;
@@ -664,7 +682,7 @@ __device__ __forceinline__ int dq_items(const Params& P, DqCursor& c) {
     }
     return (P.Tq + BQ - 1) / BQ * P.H * P.B;
 }
-template <int BQ, int BK, bool VL>
+template <int BQ, int BK, bool VL, bool RB = false>
 __device__ __forceinline__ DqItem dq_item(const Params& P, int w, DqCursor& c) {
     if (VL && P.B <= kVlCompact) {
         while (w >= c.first + __popc(c.seqs) * P.H && c.level > 0) {
@@ -676,11 +694,11 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w, DqCursor& c) {
         unsigned m = c.seqs;
         for (int t = 0; t < j && m; ++t) m &= m - 1;
         // (w is below the item count, so the sequence exists)
-        return dq_item_at<BQ, BK, VL>(P, m ? __ffs(m) - 1 : 0, r - j * P.H, c.level);
+        return dq_item_at<BQ, BK, VL, RB>(P, m ? __ffs(m) - 1 : 0, r - j * P.H, c.level);
     }
     const int nqb = (P.Tq + BQ - 1) / BQ;
     const int hb = w % (P.H * P.B);
-    return dq_item_at<BQ, BK, VL>(P, hb / P.H, hb % P.H, nqb - 1 - w / (P.H * P.B));
+    return dq_item_at<BQ, BK, VL, RB>(P, hb / P.H, hb % P.H, nqb - 1 - w / (P.H * P.B));
 }
 
 // Persistent: one CTA per SM walks its items in snake order (snake_item).  The
@@ -700,6 +718,8 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     constexpr int NS = C::kStages, BQ = C::BQ, BK = C::BK;
     // MODE & 3 as for dK/dV; MODE & 4: softcap; MODE & 8: a head size below HD (4-D maps)
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
+    constexpr bool RB = (MODE & 64) != 0;  // packed fused-QKV rows: per-row sequence bounds
+    static_assert(!RB || MODE == 64, "the row bounds are built for dense batches without other modes");
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -779,7 +799,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         };
         int qn = 0;  // Q/dO/O loads so far
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
+            const DqItem it = dq_item<BQ, BK, VL, RB>(P, w, cur);
             if (it.ntiles == 0) {
 #pragma unroll
                 for (int m = 0; m < BQ / 32; ++m) stats(it, it.i0 + m * 32 + lane, 0.f);
@@ -839,7 +859,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         bool ok = true;
         int g = 0;  // K/V tiles loaded so far
         for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
+            const DqItem it = dq_item<BQ, BK, VL, RB>(P, w, cur);
             for (int n = 0; n < it.ntiles; ++n) {
                 const int s = g % NS, use = g / NS;
                 if (use > 0 && !warp_wait(BAR(KV_EMPTY(s)), (use - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) {
@@ -895,7 +915,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
         bool ok = true;
         int gt = 0, act = 0;
         for (int k_ = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
+            const DqItem it = dq_item<BQ, BK, VL, RB>(P, w, cur);
             if (it.ntiles == 0) continue;
             ok = wait_all(QT_READY, act & 1);
             if (ok) ok = issue_one(gt);
@@ -983,7 +1003,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             if (lane == 0) mbar_arrive(BAR(QT_READY));
             // issued here, consumed at the item's start: the latency hides behind
             // the current item's epilogue
-            l_copied = load_lse(dq_item<BQ, BK, VL>(P, w2, cur2));
+            l_copied = load_lse(dq_item<BQ, BK, VL, RB>(P, w2, cur2));
             if (!warp_wait(BAR(D_FULL), qc & 1, P.status, ST_BWD_COMPUTE, &abort_flag)) return false;
             d_copied = reinterpret_cast<const float*>(smem + C::kOOff)[r];
             ++qc;
@@ -993,12 +1013,14 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             return true;
         };
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
-            const DqItem it = dq_item<BQ, BK, VL>(P, w, cur);
+            const DqItem it = dq_item<BQ, BK, VL, RB>(P, w, cur);
             const int i = it.i0 + r;
             const int p = i + P.q_offset;
             const int tq = it.sq.tq, tk = it.sq.tk;
             const bool row_ok = i < tq;
             const int ntiles = it.ntiles;
+            int2 rk_own = make_int2(0, tk);  // packed fused-QKV rows: this row's sequence
+            if constexpr (RB) rk_own = row_keys(P, max(min(i, tq - 1), 0), tk);
             float lse2 = INFINITY, Dd = 0.f;
             if (ntiles > 0 && copied != w) ok = copy_q(w);
             if (row_ok && ntiles > 0) {
@@ -1020,6 +1042,10 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 int clo = 0, chi = min(32, tk - jc);
                 if (P.wr >= 0) chi = min(chi, p + P.wr - jc + 1);
                 if (P.wl >= 0) clo = max(clo, p - P.wl - jc);
+                if constexpr (RB) {  // packed fused-QKV rows: this row's sequence
+                    clo = max(clo, rk_own.x - jc);
+                    chi = min(chi, rk_own.y - jc);
+                }
                 if (!row_ok) chi = 0;
                 // the additive bias of the row's 32 keys, loaded before the wait for S (0 past
                 // the keys)
@@ -1150,7 +1176,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             // every S and dP of this item completed (their results were read above):
             // put the next active item's Q and dO into TMEM before this epilogue
             for (int k2 = k_ + 1, w2 = snake_item(k2); ntiles > 0 && w2 < nitems; w2 = snake_item(++k2)) {
-                if (dq_item<BQ, BK, VL>(P, w2, cur2).ntiles == 0) continue;
+                if (dq_item<BQ, BK, VL, RB>(P, w2, cur2).ntiles == 0) continue;
                 ok = copy_q(w2);
                 break;
             }
@@ -1246,6 +1272,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         const bool c = p.softcap > 0.f;
         auto k = p.hd != HD ? (c ? bwd_dq_kernel<BF16, HD, 12> : bwd_dq_kernel<BF16, HD, 8>)
                  : p.cu_q   ? (c ? bwd_dq_kernel<BF16, HD, 5> : bwd_dq_kernel<BF16, HD, 1>)
+                 : p.row_bounds ? bwd_dq_kernel<BF16, HD, 64>
                  : p.bias   ? (c ? bwd_dq_kernel<BF16, HD, 6> : bwd_dq_kernel<BF16, HD, 2>)
                             : (c ? bwd_dq_kernel<BF16, HD, 4> : bwd_dq_kernel<BF16, HD, 0>);
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
@@ -1263,6 +1290,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         const bool c = p.softcap > 0.f;
         auto k = p.hd != HD ? (c ? bwd_dkdv_kernel<BF16, HD, 12> : bwd_dkdv_kernel<BF16, HD, 8>)
                  : p.cu_q   ? (c ? bwd_dkdv_kernel<BF16, HD, 5> : bwd_dkdv_kernel<BF16, HD, 1>)
+                 : p.row_bounds ? bwd_dkdv_kernel<BF16, HD, 64>
                  : p.bias   ? (c ? bwd_dkdv_kernel<BF16, HD, 6> : bwd_dkdv_kernel<BF16, HD, 2>)
                             : (c ? bwd_dkdv_kernel<BF16, HD, 4> : bwd_dkdv_kernel<BF16, HD, 0>);
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, KVCfg<HD>::kLaunchBytes);

@@ -57,6 +57,11 @@ struct Params {
     // index c at rope_tab[2 * (c * rope_npos + s)], [+1]; rope_npos positions
     const float* rope_tab;
     int rope_npos;
+    // Packed fused-QKV rows (one batch, Tq = Tk, q_offset 0), or NULL: row r sees only
+    // keys j in [row_bounds[r].x, row_bounds[r].y), its own sequence (a range holding r;
+    // the sequences lie back to back, so the bounds never decrease down the rows).  The
+    // window then applies inside the sequence.
+    const int2* row_bounds;
     unsigned int* status;
 };
 
@@ -163,9 +168,20 @@ __device__ __forceinline__ void rope_turn(float a, float b, float c, float s, fl
 }
 
 // ------------------------------------------------------------ visibility
+// Keys [x, y) that packed fused-QKV row r may see by its sequence bounds, clamped to
+// [0, n) so that no access leaves the rows.
+__device__ __forceinline__ int2 row_keys(const Params& P, int r, int n) {
+    const int2 rb = __ldg(P.row_bounds + r);
+    return make_int2(max(rb.x, 0), min(rb.y, n));
+}
+
 // Key j (of tk) visible to the query at absolute position p (see include/attn.h).
 __device__ __forceinline__ bool visible(const Params& P, int b, int p, int j, int tk) {
     if (j < 0 || j >= tk) return false;
+    if (P.row_bounds) {  // packed fused-QKV rows: position p is row p of the one batch
+        const int2 rk = row_keys(P, p, tk);
+        if (j < rk.x || j >= rk.y) return false;
+    }
     if (P.wr >= 0 && j > p + P.wr) return false;
     if (P.wl >= 0 && j < p - P.wl) return false;
     if (P.key_mask && !(P.key_mask[(long long)b * P.mask_bstride + j] > 0.5f)) return false;

@@ -107,7 +107,7 @@ struct FwdItem {
 // The item of query block cq (rows 256*cq ..) of head h in sequence b; an item
 // that is not valid has no rows.
 // kspan: the key-mask spans of the batches (shared memory), or NULL for none
-template <bool VL>
+template <bool VL, bool RB = false>
 __device__ __forceinline__ FwdItem make_item(const Params& P, int b, int h, int cq, bool valid, const int2* kspan) {
     FwdItem it;
     it.h = h;
@@ -118,8 +118,18 @@ __device__ __forceinline__ FwdItem make_item(const Params& P, int b, int h, int 
     if (!valid) it.sq.tq = 0;
     it.hasB = it.i0 + BM < it.sq.tq;
     const int2 span = kspan ? kspan[b] : make_int2(0, it.sq.tk);
-    it.tu[0] = it.i0 < it.sq.tq ? tile_range(P, it.i0, it.sq.tq, it.sq.tk, span) : TileInfo{0, 0};
-    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM, it.sq.tq, it.sq.tk, span) : TileInfo{0, 0};
+    // packed fused-QKV rows: a tile's keys lie between its first row's sequence start
+    // and its last row's sequence end
+    auto span_of = [&](int i0) -> int2 {
+        if constexpr (!RB) {
+            return span;
+        } else {
+            const int ilast = min(i0 + BM, it.sq.tq) - 1;
+            return make_int2(max(span.x, row_keys(P, i0, it.sq.tk).x), min(span.y, row_keys(P, ilast, it.sq.tk).y));
+        }
+    };
+    it.tu[0] = it.i0 < it.sq.tq ? tile_range(P, it.i0, it.sq.tq, it.sq.tk, span_of(it.i0)) : TileInfo{0, 0};
+    it.tu[1] = it.hasB ? tile_range(P, it.i0 + BM, it.sq.tq, it.sq.tk, span_of(it.i0 + BM)) : TileInfo{0, 0};
     int t0 = it.tu[0].t0, t1 = it.tu[0].t0 + it.tu[0].ntiles;
     if (it.tu[1].ntiles > 0) {
         if (it.tu[0].ntiles == 0) {
@@ -206,7 +216,7 @@ __device__ __forceinline__ void load_bias_row(const Params& P, int b, int h, int
 // kept span, longest first.  Without a window every query block of a batch sees
 // the same key tiles, so a batch's items run together, the longest spans first;
 // otherwise each level of query blocks takes its batches in that order.
-template <bool VL, bool KORD = false>
+template <bool VL, bool KORD = false, bool RB = false>
 __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c, const int2* kspan,
                                             const unsigned char* kord = nullptr) {
     if constexpr (VL) {
@@ -216,13 +226,13 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c,
     if constexpr (KORD) {
         if (P.wl < 0 && P.wr < 0) {
             const int per = P.H * ncq, rem = w % per;
-            return make_item<VL>(P, kord[w / per], rem % P.H, rem / P.H, true, kspan);
+            return make_item<VL, RB>(P, kord[w / per], rem % P.H, rem / P.H, true, kspan);
         }
         const int hb = w % (P.H * P.B);
-        return make_item<VL>(P, kord[hb / P.H], hb % P.H, ncq - 1 - w / (P.H * P.B), true, kspan);
+        return make_item<VL, RB>(P, kord[hb / P.H], hb % P.H, ncq - 1 - w / (P.H * P.B), true, kspan);
     }
     const int hb = w % (P.H * P.B);
-    return make_item<VL>(P, hb / P.H, hb % P.H, ncq - 1 - w / (P.H * P.B), true, kspan);
+    return make_item<VL, RB>(P, hb / P.H, hb % P.H, ncq - 1 - w / (P.H * P.B), true, kspan);
 }
 
 // MODE & 3 -- 0: dense; 1: packed variable-length sequences (cu_seqlens); 2: dense with
@@ -234,12 +244,16 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c,
 // x[c + hd/2]) by the angles of P.rope_tab once the tile lands, and the MMA warp
 // waits for that (Q_ROT) instead of the load.  Each instantiation carries only its
 // own bookkeeping.  MODE & 32: dense key-masked batches (at most kMaskSpanMax of
-// them), the items numbered by the batches' kept key spans, longest first.
+// them), the items numbered by the batches' kept key spans, longest first.  MODE 64:
+// packed fused-QKV rows of one batch, each query row limited to its own sequence's
+// keys (P.row_bounds) inside the window.
 template <bool BF16, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads2, 1)
     fwd_tc2_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO) {
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0, ROPE = (MODE & 16) != 0;
+    constexpr bool RB = (MODE & 64) != 0;  // packed fused-QKV rows: per-row sequence bounds
+    static_assert(!RB || MODE == 64, "the row bounds are built for dense batches without other modes");
     constexpr bool KORD = (MODE & 32) != 0;
     static_assert(!(KORD && (MODE & 31) != 0), "the span order is built for plain dense key-masked batches");
     static_assert(!(PADH && VL), "padded head sizes are built for dense batches only");
@@ -346,7 +360,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int gk = 0, gv = 0;   // K and V tiles loaded so far (ring positions)
             int qn[2] = {0, 0};   // Q tiles loaded so far, per tile slot
             for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-                const FwdItem it = fwd_item<VL, KORD>(P, w, vcur, kspan, kord_s);
+                const FwdItem it = fwd_item<VL, KORD, RB>(P, w, vcur, kspan, kord_s);
                 if (it.ntiles == 0) continue;
                 for (int u = 0; ok && u < 2; ++u) {
                     if (!active(it, u)) continue;
@@ -416,7 +430,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             int pc = 0;   // P_FULL(u) phases consumed
             int act = 0;  // items in which this tile was active so far
             for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-                const FwdItem it = fwd_item<VL, KORD>(P, w, vcur, kspan, kord_s);
+                const FwdItem it = fwd_item<VL, KORD, RB>(P, w, vcur, kspan, kord_s);
                 if (it.ntiles == 0) continue;
                 const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
                 const bool on = active(it, u);
@@ -663,7 +677,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         int qr = 0;        // Q tiles of this tile slot rotated so far
         int rot_kw = -1;   // position (in this CTA's item sequence) of the last rotated item
         auto rotate_q = [&](int kw2) -> bool {
-            const FwdItem it2 = fwd_item<VL, KORD>(P, snake_item(kw2), vcur, kspan, kord_s);
+            const FwdItem it2 = fwd_item<VL, KORD, RB>(P, snake_item(kw2), vcur, kspan, kord_s);
             const TileInfo my2 = u == 0 ? it2.tu[0] : it2.tu[1];
             if (it2.ntiles == 0 || my2.ntiles == 0) return true;  // the tile is not loaded for this item
             if (!wait_warp(Q_FULL(u), qr & 1)) return false;
@@ -712,7 +726,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             return true;
         };
         for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
-            const FwdItem it = fwd_item<VL, KORD>(P, w, vcur, kspan, kord_s);
+            const FwdItem it = fwd_item<VL, KORD, RB>(P, w, vcur, kspan, kord_s);
             const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
             const int bA = base[0], bB = base[1];
             base[0] += nA;
@@ -724,6 +738,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const int p = i + P.q_offset;
             const int prow0 = ib + P.q_offset, prow1 = min(ib + BM, tq) - 1 + P.q_offset;
             const TileInfo my = u == 0 ? it.tu[0] : it.tu[1];
+            // packed fused-QKV rows: this row's sequence, and the keys every row of the tile sees
+            int2 rk_own = make_int2(0, tk), rk_all = make_int2(0, tk);
+            if constexpr (RB) {
+                rk_own = row_keys(P, max(min(i, tq - 1), 0), tk);
+                rk_all = make_int2(row_keys(P, min(ib + BM, tq) - 1, tk).x, row_keys(P, ib, tk).y);
+            }
             if constexpr (ROPE) {
                 // this item's Q, unless the previous item's end already turned it
                 if (my.ntiles > 0 && rot_kw != kw && !rotate_q(kw)) {
@@ -745,13 +765,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 }
                 // a tile whose keys the mask keeps whole needs no mask pass
                 const bool full = tile_full(P.wl, P.wr, tk, prow0, prow1, j0, j0 + BN) &&
-                                  (mbits[0] & mbits[1] & mbits[2] & mbits[3]) == 0xffffffffu;
+                                  (mbits[0] & mbits[1] & mbits[2] & mbits[3]) == 0xffffffffu &&
+                                  (!RB || (j0 >= rk_all.x && j0 + BN <= rk_all.y));
                 // this row's visible columns of the tile: [clo, chi), and the key-mask bits
                 int clo = 0, chi = BN;
                 if (!full) {
                     chi = min(chi, tk - j0);
                     if (P.wr >= 0) chi = min(chi, p + P.wr - j0 + 1);
                     if (P.wl >= 0) clo = max(clo, p - P.wl - j0);
+                    if constexpr (RB) {
+                        clo = max(clo, rk_own.x - j0);
+                        chi = min(chi, rk_own.y - j0);
+                    }
                 }
                 // additive score bias: loads issued before the waits
                 float bv[BIAS ? 128 : 1];
@@ -931,7 +956,9 @@ cudaError_t fwd2_typed(const Params& p, const FwdMaps& m, cudaStream_t s) {
     const bool c = p.softcap > 0.f;
     // a head size below HD (dense batches without a bias only) runs the padded instantiations
     // the rotary query turn (dense batches at hd 64 / 128) runs the MODE & 16 instantiations
+    // packed fused-QKV rows (one dense batch at hd 64 / 128, no other mode) run MODE 64
     auto kern = p.rope_tab  ? (c ? fwd_tc2_kernel<BF16, HD, 20> : fwd_tc2_kernel<BF16, HD, 16>)
+                : p.row_bounds ? fwd_tc2_kernel<BF16, HD, 64>
                 : p.hd != HD ? (c ? fwd_tc2_kernel<BF16, HD, 12> : fwd_tc2_kernel<BF16, HD, 8>)
                 : p.cu_q   ? (c ? fwd_tc2_kernel<BF16, HD, 5> : fwd_tc2_kernel<BF16, HD, 1>)
                 : p.bias   ? (c ? fwd_tc2_kernel<BF16, HD, 6> : fwd_tc2_kernel<BF16, HD, 2>)

@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(kRows * 32) simt_fwd_kernel(Params P) {
     const int ilast = min(i0 + kRows, sq.tq) - 1;
     int lo, hi;
     key_range(P.wl, P.wr, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+    if (P.row_bounds) {  // packed fused-QKV rows: the block's first and last rows bound its keys
+        lo = max(lo, row_keys(P, i0, sq.tk).x);
+        hi = max(lo, min(hi, row_keys(P, ilast, sq.tk).y));
+    }
 
     for (int d = lane; d < HD; d += 32)
         Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, sq, i, h)[d]) : 0.f;
@@ -209,6 +213,10 @@ __global__ void __launch_bounds__(kRows * 32) simt_dq_kernel(Params P) {
     const int ilast = min(i0 + kRows, sq.tq) - 1;
     int lo, hi;
     key_range(P.wl, P.wr, sq.tk, i0 + P.q_offset, ilast + P.q_offset, &lo, &hi);
+    if (P.row_bounds) {  // packed fused-QKV rows: the block's first and last rows bound its keys
+        lo = max(lo, row_keys(P, i0, sq.tk).x);
+        hi = max(lo, min(hi, row_keys(P, ilast, sq.tk).y));
+    }
     for (int d = lane; d < HD; d += 32) {
         Qs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.q, sq, i, h)[d]) : 0.f;
         Gs[warp * HD + d] = row_ok ? Elem<T>::to_f(qrow<T>(P, P.dout, sq, i, h)[d]) : 0.f;
@@ -296,6 +304,10 @@ __global__ void __launch_bounds__(kRows * 32) simt_dkdv_kernel(Params P) {
     const int jlast = min(j0 + kRows, sq.tk);
     int qlo, qhi;
     query_range(P.wl, P.wr, sq.tq, P.q_offset, j0, jlast, &qlo, &qhi);
+    if (P.row_bounds) {  // packed fused-QKV rows: a key is seen only from its own sequence
+        qlo = max(qlo, row_keys(P, j0, sq.tq).x);
+        qhi = max(qlo, min(qhi, row_keys(P, jlast - 1, sq.tq).y));
+    }
     for (int d = lane; d < HD; d += 32) {
         Ks[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.k, sq, j, kvh)[d]) : 0.f;
         Vs[warp * HD + d] = key_ok ? Elem<T>::to_f(kvrow<T>(P, P.v, sq, j, kvh)[d]) : 0.f;

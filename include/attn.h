@@ -299,6 +299,39 @@ ATTN_API attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k
                         void* stream);
 
 /*
+ * Packed bidirectional self-attention straight off a fused QKV projection.
+ * Source: brotensor ops/flash_attention.h, flash_attention_packed_qkv_forward /
+ * flash_attention_packed_qkv_backward (many sequences of any lengths packed back to
+ * back in one row block, rows attending only inside their own sequence, an optional
+ * bidirectional window; the backward recomputes the softmax from q, k and v).
+ *   qkv        : [L][3*H*hd], each row [q heads | k heads | v heads], 16-byte aligned.
+ *   seq_bounds : [L][2] int32 on the device, 8-byte aligned: row r's sequence is rows
+ *                [seq_bounds[r][0], seq_bounds[r][1]), a range holding r; sequences
+ *                lie back to back, so the bounds never decrease down the rows (the
+ *                kernels rely on it to pick each tile's keys; bounds past [0, L) are
+ *                clipped).  Membership is data: the launch shape depends on L only.
+ *   window     : >= 0; > 0: row r sees keys j of its sequence with |r - j| <= window/2
+ *                (integer division); 0: every key of its sequence.  Non-causal.
+ *   scale      : > 0 (1/sqrt(hd) in the usual case).  H: heads (no grouping).
+ *   attn_packed_qkv_fwd : o [L][H*hd] (overwritten); lse [H][L] fp32, or NULL.
+ *   attn_packed_qkv_bwd : dqkv [L][3*H*hd] (overwritten), each row [dq | dk | dv], from
+ *                dout [L][H*hd]; O and LSE are formed again from qkv.
+ *   workspace  : at least attn_packed_qkv_workspace_size(dt, L, H, hd, backward) bytes,
+ *                16-byte aligned; contents on entry are ignored.  The calls copy q, k
+ *                and v into it (strided copies on the stream) and run the forward /
+ *                backward kernels on those: 16-bit hd 64 / 128 on the tensor cores,
+ *                other types and head sizes on the CUDA-core kernels.
+ *   Errors as attn_fwd; L = 0 is a no-op.
+ */
+ATTN_API size_t attn_packed_qkv_workspace_size(attn_dtype dt, int L, int H, int hd, int backward);
+ATTN_API attn_status attn_packed_qkv_fwd(attn_dtype dt, const void* qkv, const int* seq_bounds, void* o,
+                        float* lse, void* workspace, size_t workspace_bytes, int L, int H, int hd,
+                        float scale, int window, void* stream);
+ATTN_API attn_status attn_packed_qkv_bwd(attn_dtype dt, const void* qkv, const void* dout,
+                        const int* seq_bounds, void* dqkv, void* workspace, size_t workspace_bytes,
+                        int L, int H, int hd, float scale, int window, void* stream);
+
+/*
  * attn_decode without a workspace argument, for callers that cannot call
  * cudaMalloc and have no scratch buffer to pass in: for example a plugin that
  * is handed only its input and output buffers, a serving loop that forbids
