@@ -68,14 +68,16 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D map over a [batches][rows][inner] 16-bit tensor, box {64, box_rows, 1},
-// 128-byte swizzle (inner box = 64 elements = 128 bytes).
+// 128-byte swizzle (inner box = 64 elements = 128 bytes).  Rows lie row_stride
+// elements apart (inner when 0): a map over some columns of wider rows.
 bool make_map(CUtensorMap* m, int dt, const void* base, long long inner, long long rows, long long batches,
-              int box_rows) {
+              int box_rows, long long row_stride = 0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const CUtensorMapDataType t = dt == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const long long rs = row_stride > 0 ? row_stride : inner;
     cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)batches};
-    cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * rows * 2};
+    cuuint64_t strides[2] = {(cuuint64_t)rs * 2, (cuuint64_t)rs * rows * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(m, t, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -153,11 +155,12 @@ bool use_tcgen05(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 32 || 
 bool use_tc_fwd(attn_dtype dt, int hd) { return use_tcgen05(dt, hd) || (dt != ATTN_F32 && hd == 256); }
 
 // Tensor map of one activation for the tensor-core kernels: 3-D at hd 64 / 128, 4-D
-// (zero-filled past the head) at hd 32 / 96.
+// (zero-filled past the head) at hd 32 / 96.  A row stride (elements; 0 = heads*hd)
+// maps the activation's columns inside wider rows (3-D maps only).
 bool act_map(CUtensorMap* m, attn_dtype dt, const void* base, int hd, long long heads, long long rows,
-             long long batches, int box_rows) {
-    if (padded_head(hd)) return make_map4(m, (int)dt, base, hd, heads, rows, batches, box_rows);
-    return make_map(m, (int)dt, base, heads * hd, rows, batches, box_rows);
+             long long batches, int box_rows, long long row_stride = 0) {
+    if (padded_head(hd)) return row_stride == 0 && make_map4(m, (int)dt, base, hd, heads, rows, batches, box_rows);
+    return make_map(m, (int)dt, base, heads * hd, rows, batches, box_rows, row_stride);
 }
 
 // Decode split plan: a deterministic function of the shape.  Aim for about
@@ -222,9 +225,11 @@ int attn_kernel_family_bwd(attn_dtype dt, int hd) { return use_tc_fwd(dt, hd) ? 
 
 namespace {
 
-// The forward once the arguments are checked and the window set in p.
+// The forward once the arguments are checked and the window set in p.  With
+// in_stride > 0 the rows of q, k and v lie in_stride elements apart (the tensor-core
+// kernels only: the caller routes such calls there).
 attn_status fwd_launch(attn_dtype dt, const void* q, const void* k, const void* v, void* o, float* lse, Params p,
-                       void* stream) {
+                       void* stream, long long in_stride = 0) {
     const int B = p.B, Tq = p.Tq, Tk = p.Tk, H = p.H, Hkv = p.Hkv, hd = p.hd;
     if (B == 0 || Tq == 0) return ATTN_OK;
     if (!q || !o || (Tk > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
@@ -241,8 +246,9 @@ attn_status fwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
         return counted(launch_simt_fwd(p, (int)dt, s), 1);
     FwdMaps maps;
     const int kv_rows = hd == 256 ? 64 : 128;  // keys per tile
-    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128) || !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, kv_rows) ||
-        !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, kv_rows) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 32))
+    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128, in_stride) ||
+        !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, kv_rows, in_stride) ||
+        !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, kv_rows, in_stride) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 32))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_fwd(p, (int)dt, maps, s), 1);
 }
@@ -273,10 +279,12 @@ size_t attn_bwd_workspace_size(int B, int Tq, int H) {
 
 namespace {
 
-// The backward once the arguments are checked and the window set in p.
+// The backward once the arguments are checked and the window set in p.  With
+// in_stride / grad_stride > 0 the rows of q, k, v / of dq, dk, dv lie that many
+// elements apart (the tensor-core kernels only: the caller routes such calls there).
 attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* v, const void* o, const void* dout,
                        const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                       Params p, void* stream, int phases) {
+                       Params p, void* stream, int phases, long long in_stride = 0, long long grad_stride = 0) {
     const int B = p.B, Tq = p.Tq, Tk = p.Tk, H = p.H, Hkv = p.Hkv, hd = p.hd;
     if (phases <= 0 || phases > 7) return ATTN_ERR_INVALID_ARG;
     if (B == 0) return ATTN_OK;
@@ -318,14 +326,15 @@ attn_status bwd_launch(attn_dtype dt, const void* q, const void* k, const void* 
     const int nk = hd == 256 ? ((phases & 5) ? 1 : 0) + ((phases & 2) ? 2 : 0) + ((phases & 4) ? 1 : 0)
                              : ((phases & 1) && !(phases & 4) ? 1 : 0) + ((phases & 2) ? 1 : 0) + ((phases & 4) ? 1 : 0);
     BwdMaps maps;
-    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128) || !act_map(&maps.dout, dt, dout, hd, H, Tq, B, 128) ||
-        !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, 128) || !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, 128) ||
-        !act_map(&maps.q64, dt, q, hd, H, Tq, B, 64) || !act_map(&maps.dout64, dt, dout, hd, H, Tq, B, 64) ||
-        !act_map(&maps.k64, dt, k, hd, Hkv, Tk, B, 64) || !act_map(&maps.v64, dt, v, hd, Hkv, Tk, B, 64) ||
+    const long long is = in_stride, gs = grad_stride;
+    if (!act_map(&maps.q, dt, q, hd, H, Tq, B, 128, is) || !act_map(&maps.dout, dt, dout, hd, H, Tq, B, 128) ||
+        !act_map(&maps.k, dt, k, hd, Hkv, Tk, B, 128, is) || !act_map(&maps.v, dt, v, hd, Hkv, Tk, B, 128, is) ||
+        !act_map(&maps.q64, dt, q, hd, H, Tq, B, 64, is) || !act_map(&maps.dout64, dt, dout, hd, H, Tq, B, 64) ||
+        !act_map(&maps.k64, dt, k, hd, Hkv, Tk, B, 64, is) || !act_map(&maps.v64, dt, v, hd, Hkv, Tk, B, 64, is) ||
         ((phases & 4) &&
-         (!act_map(&maps.dq32, dt, dq, hd, H, Tq, B, 32) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 128))) ||
+         (!act_map(&maps.dq32, dt, dq, hd, H, Tq, B, 32, gs) || !act_map(&maps.o, dt, o, hd, H, Tq, B, 128))) ||
         ((phases & 2) &&
-         (!act_map(&maps.dk32, dt, dk, hd, Hkv, Tk, B, 32) || !act_map(&maps.dv32, dt, dv, hd, Hkv, Tk, B, 32))))
+         (!act_map(&maps.dk32, dt, dk, hd, Hkv, Tk, B, 32, gs) || !act_map(&maps.dv32, dt, dv, hd, Hkv, Tk, B, 32, gs))))
         return ATTN_ERR_CUDA;
     return counted(launch_tc_bwd(p, (int)dt, maps, phases, s), nk);
 }
@@ -829,6 +838,11 @@ Params packed_params(const int* seq_bounds, int L, int H, int hd, float scale, i
 
 size_t tensor_bytes(attn_dtype dt, int L, int H, int hd) { return align256((size_t)L * H * hd * elem_size(dt)); }
 
+// 16-bit rows at hd 64 / 128 go to the tensor-core kernels, whose tensor maps read q,
+// k and v in place from the packed rows (and write dq, dk, dv into them); the
+// CUDA-core kernels take contiguous copies.
+bool packed_in_place(attn_dtype dt, int hd) { return dt != ATTN_F32 && (hd == 64 || hd == 128); }
+
 }  // namespace
 
 extern "C" {
@@ -850,10 +864,16 @@ attn_status attn_packed_qkv_fwd(attn_dtype dt, const void* qkv, const int* seq_b
     if (!o || !workspace || !aligned16(workspace) || workspace_bytes < attn_packed_qkv_workspace_size(dt, L, H, hd, 0))
         return ATTN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Params p = packed_params(seq_bounds, L, H, hd, scale, window);
+    if (packed_in_place(dt, hd)) {
+        const size_t w = (size_t)H * hd * elem_size(dt);
+        const uint8_t* r = static_cast<const uint8_t*>(qkv);
+        return fwd_launch(dt, r, r + w, r + 2 * w, o, lse, p, stream, 3LL * H * hd);
+    }
     const size_t t = tensor_bytes(dt, L, H, hd);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if ((st = split_qkv(dt, qkv, ws, ws + t, ws + 2 * t, L, H, hd, s)) != ATTN_OK) return st;
-    return fwd_launch(dt, ws, ws + t, ws + 2 * t, o, lse, packed_params(seq_bounds, L, H, hd, scale, window), stream);
+    return fwd_launch(dt, ws, ws + t, ws + 2 * t, o, lse, p, stream);
 }
 
 attn_status attn_packed_qkv_bwd(attn_dtype dt, const void* qkv, const void* dout, const int* seq_bounds, void* dqkv,
@@ -872,14 +892,22 @@ attn_status attn_packed_qkv_bwd(attn_dtype dt, const void* qkv, const void* dout
     float* lse = reinterpret_cast<float*>(ws + 4 * t);
     uint8_t *dq = ws + 4 * t + lse_bytes, *dk = dq + t, *dv = dq + 2 * t, *wb = dq + 3 * t;
     const Params p = packed_params(seq_bounds, L, H, hd, scale, window);
+    const size_t w = (size_t)H * hd * elem_size(dt);
     // the backward consumes no forward results: O and LSE are formed again here
+    if (packed_in_place(dt, hd)) {
+        const uint8_t* r = static_cast<const uint8_t*>(qkv);
+        uint8_t* g = static_cast<uint8_t*>(dqkv);
+        const long long rs = 3LL * H * hd;
+        if ((st = fwd_launch(dt, r, r + w, r + 2 * w, o, lse, p, stream, rs)) != ATTN_OK) return st;
+        return bwd_launch(dt, r, r + w, r + 2 * w, o, dout, lse, g, g + w, g + 2 * w, wb, attn_bwd_workspace_size(1, L, H),
+                          p, stream, 7, rs, rs);
+    }
     if ((st = split_qkv(dt, qkv, q, k, v, L, H, hd, s)) != ATTN_OK) return st;
     if ((st = fwd_launch(dt, q, k, v, o, lse, p, stream)) != ATTN_OK) return st;
     if ((st = bwd_launch(dt, q, k, v, o, dout, lse, dq, dk, dv, wb, attn_bwd_workspace_size(1, L, H), p, stream, 7)) !=
         ATTN_OK)
         return st;
     // dq, dk, dv into their columns of the packed gradient rows
-    const size_t w = (size_t)H * hd * elem_size(dt);
     const void* src[3] = {dq, dk, dv};
     for (int c = 0; c < 3; ++c)
         if (cudaMemcpy2DAsync(static_cast<uint8_t*>(dqkv) + c * w, 3 * w, src[c], w, w, (size_t)L,

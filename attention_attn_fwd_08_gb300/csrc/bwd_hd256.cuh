@@ -252,21 +252,19 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
                     const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                    if (elect_one())
-                        mma_ss(tbase + bf * 64, sdesc_sw128(sbase + kKOff + aoff, 16, 1024),
+                    mma_ss_e(tbase + bf * 64, sdesc_sw128(sbase + kKOff + aoff, 16, 1024),
                                sdesc_sw128(qa + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                 }
                 if constexpr (kDK) {
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                        if (elect_one())
-                            mma_ts(tbase + 64, tV + kk * 8, sdesc_sw128(ga + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                        mma_ts_e(tbase + 64, tV + kk * 8, sdesc_sw128(ga + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                     }
                 }
-                if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
+                mma_commit_e(BAR(ST_FULL(bf)));
                 // the tile's ring read only by these MMAs is free once they complete
-                if (elect_one()) mma_commit(BAR(kDK ? G_EMPTY(s) : Q_EMPTY(s)));
+                mma_commit_e(BAR(kDK ? G_EMPTY(s) : Q_EMPTY(s)));
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -284,15 +282,14 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
                 const uint32_t bsrc = kDK ? sbase + kRingOff + s * kTBytes : sbase + kGRingOff + s * kTBytes;
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    if (elect_one())
-                        mma_ts(tAcc, tbase + bf * 64 + kk * 8, sdesc_sw128(bsrc + kk * 2048, BQ * 128, 1024), idAcc,
+                    mma_ts_e(tAcc, tbase + bf * 64 + kk * 8, sdesc_sw128(bsrc + kk * 2048, BQ * 128, 1024), idAcc,
                                (n > 0 || kk > 0) ? 1u : 0u);
-                if (elect_one()) mma_commit(BAR(kDK ? Q_EMPTY(s) : G_EMPTY(s)));
+                mma_commit_e(BAR(kDK ? Q_EMPTY(s) : G_EMPTY(s)));
                 const int nx = kDK ? n + 1 : n + 2;
                 if (nx < ntiles) ok = issue_s(nx);
             }
-            if (ok && elect_one()) mma_commit(BAR(ACC_DONE));
-            if (elect_one()) mma_commit(BAR(MMA_DONE));
+            if (ok) mma_commit_e(BAR(ACC_DONE));
+            mma_commit_e(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
     } else {
@@ -539,17 +536,16 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t boff = (kk >> 2) * (BKD * 128) + (kk & 3) * 32;
-                    if (elect_one()) mma_ts(tS, tQ + kk * 8, sdesc_sw128(ka + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    mma_ts_e(tS, tQ + kk * 8, sdesc_sw128(ka + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * (BQD * 128) + (kk & 3) * 32;
                     const uint32_t boff = (kk >> 2) * (BKD * 128) + (kk & 3) * 32;
-                    if (elect_one())
-                        mma_ss(tDP, sdesc_sw128(sbase + kDoOff + aoff, 16, 1024), sdesc_sw128(va + boff, 16, 1024), idS,
+                    mma_ss_e(tDP, sdesc_sw128(sbase + kDoOff + aoff, 16, 1024), sdesc_sw128(va + boff, 16, 1024), idS,
                                kk > 0 ? 1u : 0u);
                 }
-                if (elect_one()) mma_commit(BAR(SD_FULL));
+                mma_commit_e(BAR(SD_FULL));
                 return true;
             };
             if (ok) ok = issue_sd(0);
@@ -564,14 +560,13 @@ __global__ void __launch_bounds__(b256::kThreads, 1)
                 const uint32_t ka = sbase + kDqRingOff + s * 2 * kKTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < BKD / 16; ++kk)
-                    if (elect_one())
-                        mma_ts(tDQ, tS + kk * 8, sdesc_sw128(ka + kk * 2048, BKD * 128, 1024), idAcc,
+                    mma_ts_e(tDQ, tS + kk * 8, sdesc_sw128(ka + kk * 2048, BKD * 128, 1024), idAcc,
                                (n > 0 || kk > 0) ? 1u : 0u);
-                if (elect_one()) mma_commit(BAR(KV_EMPTY(s)));
+                mma_commit_e(BAR(KV_EMPTY(s)));
                 if (n + 1 < nkt) ok = issue_sd(n + 1);
             }
-            if (ok && elect_one()) mma_commit(BAR(ACC_DONE));
-            if (elect_one()) mma_commit(BAR(MMA_DONE));
+            if (ok) mma_commit_e(BAR(ACC_DONE));
+            mma_commit_e(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
     } else {

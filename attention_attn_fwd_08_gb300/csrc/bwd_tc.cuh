@@ -218,19 +218,17 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
                     const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                    if (elect_one())
-                        mma_ss(tbase + bf * 64, sdesc_sw128(sbase + C::kKOff + aoff, 16, 1024),
+                    mma_ss_e(tbase + bf * 64, sdesc_sw128(sbase + C::kKOff + aoff, 16, 1024),
                                sdesc_sw128(qa + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * (BKV * 128) + (kk & 3) * 32;
                     const uint32_t boff = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                    if (elect_one())
-                        mma_ss(tbase + 128 + bf * 64, sdesc_sw128(sbase + C::kVOff + aoff, 16, 1024),
+                    mma_ss_e(tbase + 128 + bf * 64, sdesc_sw128(sbase + C::kVOff + aoff, 16, 1024),
                                sdesc_sw128(ga + boff, 16, 1024), idS, kk > 0 ? 1u : 0u);
                 }
-                if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
+                mma_commit_e(BAR(ST_FULL(bf)));
                 return true;
             };
             if (ok) ok = issue_sd(0);
@@ -245,21 +243,19 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
                 const uint32_t qa = sbase + C::kQOff + s * C::kQBytes, ga = sbase + C::kGOff + s * C::kQBytes;
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk) {
-                    if (elect_one())
-                        mma_ts(tDV, tbase + bf * 64 + kk * 8, sdesc_sw128(ga + kk * 2048, BQ * 128, 1024), idAcc,
+                    mma_ts_e(tDV, tbase + bf * 64 + kk * 8, sdesc_sw128(ga + kk * 2048, BQ * 128, 1024), idAcc,
                                (n > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk) {
-                    if (elect_one())
-                        mma_ts(tDK, tbase + 128 + bf * 64 + kk * 8, sdesc_sw128(qa + kk * 2048, BQ * 128, 1024),
+                    mma_ts_e(tDK, tbase + 128 + bf * 64 + kk * 8, sdesc_sw128(qa + kk * 2048, BQ * 128, 1024),
                                idAcc, (n > 0 || kk > 0) ? 1u : 0u);
                 }
-                if (elect_one()) mma_commit(BAR(Q_EMPTY(s)));
+                mma_commit_e(BAR(Q_EMPTY(s)));
                 if (n + 2 < ntiles) ok = issue_sd(n + 2);
             }
-            if (ok && elect_one()) mma_commit(BAR(ACC_DONE));
-            if (elect_one()) mma_commit(BAR(MMA_DONE));
+            if (ok) mma_commit_e(BAR(ACC_DONE));
+            mma_commit_e(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }
     } else {
@@ -907,9 +903,9 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint32_t boff = ((kk >> 2) * (BK * 128) + (kk & 3) * 32) >> 4;
-                if (elect_one()) mma_ts(d, a + kk * 8, bdesc + boff, idS, kk > 0 ? 1u : 0u);
+                mma_ts_e(d, a + kk * 8, bdesc + boff, idS, kk > 0 ? 1u : 0u);
             }
-            if (elect_one()) mma_commit(BAR(ST_FULL(bf)));
+            mma_commit_e(BAR(ST_FULL(bf)));
             return true;
         };
         bool ok = true;
@@ -938,20 +934,19 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                     const uint64_t kdesc = sdesc_sw128(sbase + C::kKOff + s * C::kKBytes, BK * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        if (elect_one())
-                            mma_ts(tDQ, tbase + bf * 64 + pcol(kk), kdesc + ((kk * 2048) >> 4), idAcc,
+                        mma_ts_e(tDQ, tbase + bf * 64 + pcol(kk), kdesc + ((kk * 2048) >> 4), idAcc,
                                    (n > 0 || kk > 0) ? 1u : 0u);
                 } else {
                     tc_fence_after();
                 }
-                if (elect_one()) mma_commit(BAR(KV_EMPTY(s)));
+                mma_commit_e(BAR(KV_EMPTY(s)));
                 if (n + 2 < it.ntiles) ok = issue_one(t + 2);
             }
-            if (ok && !issues_dp && elect_one()) mma_commit(BAR(DQ_DONE));
+            if (ok && !issues_dp) mma_commit_e(BAR(DQ_DONE));
             gt += it.ntiles;
             ++act;
         }
-        if (elect_one()) mma_commit(BAR(MMA_DONE));
+        mma_commit_e(BAR(MMA_DONE));
         mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
     }
     } else {

@@ -202,11 +202,11 @@ __global__ void __launch_bounds__(h256::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint32_t boff = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
-                if (elect_one()) mma_ts(tbase + (t & 1) * 64, tQ + kk * 8, kdesc + boff, idS, kk > 0 ? 1u : 0u);
+                mma_ts_e(tbase + (t & 1) * 64, tQ + kk * 8, kdesc + boff, idS, kk > 0 ? 1u : 0u);
             }
-            if (elect_one()) mma_commit(BAR(S_FULL(t & 1)));
-            if (elect_one()) mma_commit(BAR(K_EMPTY(s)));
-            if (last && elect_one()) mma_commit(BAR(QT_EMPTY));
+            mma_commit_e(BAR(S_FULL(t & 1)));
+            mma_commit_e(BAR(K_EMPTY(s)));
+            if (last) mma_commit_e(BAR(QT_EMPTY));
             return true;
         };
         for (int kw = 0, w = snake_item(0); ok && w < nitems; w = snake_item(++kw)) {
@@ -227,18 +227,17 @@ __global__ void __launch_bounds__(h256::kThreads, 1)
                 const uint64_t vdesc = sdesc_sw128(sbase + kVOff + s * kKVBytes, BN * 128, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    if (elect_one())
-                        mma_ts(tO, tbase + (t & 1) * 64 + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
+                    mma_ts_e(tO, tbase + (t & 1) * 64 + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
                                (n > 0 || kk > 0) ? 1u : 0u);
-                if (elect_one()) mma_commit(BAR(V_EMPTY(s)));
-                if (elect_one()) mma_commit(BAR(PV_DONE));
-                if (n == it.ntiles - 1 && elect_one()) mma_commit(BAR(O_DONE));
+                mma_commit_e(BAR(V_EMPTY(s)));
+                mma_commit_e(BAR(PV_DONE));
+                if (n == it.ntiles - 1) mma_commit_e(BAR(O_DONE));
                 if (n + 2 < it.ntiles) ok = issue_s(t + 2, n + 2 == it.ntiles - 1);
             }
             gt += it.ntiles;
             ++act;
         }
-        if (elect_one()) mma_commit(BAR(MMA_DONE));
+        mma_commit_e(BAR(MMA_DONE));
         mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
     } else if (warp < 4) {
         // ------------------------------------ softmax + epilogue, one thread per row

@@ -445,10 +445,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         const uint32_t off_q = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
                         const uint32_t off_k = ((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4;
-                        if (elect_one()) mma_ss(tS, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
+                        mma_ss_e(tS, qdesc + off_q, kdesc + off_k, idS, kk > 0 ? 1u : 0u);
                     }
-                    if (elect_one()) mma_commit(BAR(S_FULL(u)));
-                    if (last_of_u(n) && elect_one()) mma_commit(BAR(Q_EMPTY(u)));
+                    mma_commit_e(BAR(S_FULL(u)));
+                    if (last_of_u(n)) mma_commit_e(BAR(Q_EMPTY(u)));
                 };
                 // O_u (+)= P_u V(n); the item's last one signals the epilogue
                 auto issue_pv = [&](int n, int k) {
@@ -456,10 +456,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     const uint64_t vdesc = sdesc_sw128(sbase + C::kVOff + vs * C::kKVBytes, BN * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        if (elect_one())
-                            mma_ts(tO, tS + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
+                        mma_ts_e(tO, tS + kk * 8, vdesc + ((kk * 16 * 128) >> 4), idPV,
                                    (k > 0 || kk > 0) ? 1u : 0u);
-                    if (k == my.ntiles - 1 && elect_one()) mma_commit(BAR(O_DONE(u)));
+                    if (k == my.ntiles - 1) mma_commit_e(BAR(O_DONE(u)));
                 };
                 // Each step first waits for V(n) and K(n+1) (normally long resident), so
                 // that once P(n) arrives PV(n) and S(n+1) issue back to back.  The stage
@@ -476,7 +475,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
                 }
                 tc_fence_after();
                 if (has(0)) issue_s(0);
-                if (elect_one()) mma_commit(BAR(K_EMPTY(g % NS)));
+                mma_commit_e(BAR(K_EMPTY(g % NS)));
                 for (int n = 0; ok && n < it.ntiles; ++n) {
                     const int gn = g + n;
                     ok = wait_all(V_FULL(gn % NS), (gn / NS) & 1);
@@ -492,13 +491,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                     tc_fence_after();
                     if (has(n)) issue_pv(n, k);
                     if (n + 1 < it.ntiles && has(n + 1)) issue_s(n + 1);
-                    if (elect_one()) mma_commit(BAR(V_EMPTY(gn % NS)));
-                    if (n + 1 < it.ntiles && elect_one()) mma_commit(BAR(K_EMPTY((gn + 1) % NS)));
+                    mma_commit_e(BAR(V_EMPTY(gn % NS)));
+                    if (n + 1 < it.ntiles) mma_commit_e(BAR(K_EMPTY((gn + 1) % NS)));
                 }
                 g += it.ntiles;
                 if (on) ++act;
             }
-            if (elect_one()) mma_commit(BAR(MMA_DONE));
+            mma_commit_e(BAR(MMA_DONE));
             mbar_wait(BAR(MMA_DONE), 0, P.status, ST_TEARDOWN, nullptr);
         }  // warp 11 only fills the producer warpgroup
     } else {
@@ -729,6 +728,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
             const FwdItem it = fwd_item<VL, KORD, RB>(P, w, vcur, kspan, kord_s);
             const int nA = it.tu[0].ntiles, nB = it.tu[1].ntiles;
             const int bA = base[0], bB = base[1];
+            // The turns pair the tiles' k-th key tiles.  A tile whose first key tile lies
+            // more than one behind the other's could wait for a turn whose S needs a K/V
+            // ring stage that only its own later P.V releases (packed fused-QKV rows,
+            // where a tile that ends a long sequence starts many key tiles before the
+            // next one): such items run both softmaxes at once.
+            const bool alt = alternate && abs(it.tu[0].t0 - it.tu[1].t0) <= 1;
             base[0] += nA;
             base[1] += nB;
             const int ib = it.i0 + u * BM;  // first row of this tile
@@ -799,7 +804,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, sv[c]);
                 }
-                if (alternate && (u == 0 ? (k >= 1 && k - 1 < nB) : (k < nA))) {
+                if (alt && (u == 0 ? (k >= 1 && k - 1 < nB) : (k < nA))) {
                     const int need = 4 * (u == 0 ? bB + k : bA + k + 1);  // warp arrivals
                     const bool rr = count_wait(&done_count[u ^ 1], need, P.status, ST_FWD_SOFTMAX, &abort_flag);
                     if (!__all_sync(0xffffffffu, rr)) {

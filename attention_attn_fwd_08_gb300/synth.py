@@ -14,6 +14,8 @@ Workloads (shapes of the attention settings the pages describe):
   decode_lq1/lq4  B=16 Lk=32768 Lq in {1,4} H=32 Hkv=8 hd=128 causal q_offset=Lk-Lq  bf16 decode
   varlen_packed   8 sequences of U{256..2048} rows packed back to back, H=32 Hkv=8 hd=128 causal bf16 fwd+bwd
   gqa_prefill_hd256  B=4 Tq=Tk=2048 H=16 Hkv=4 hd=256 causal  bf16 fwd+bwd
+  packed_qkv      16 sequences of U{128..1024} rows packed back to back as fused QKV rows,
+                  H=12 hd=64, bidirectional within each sequence, bf16 fwd+bwd
 """
 from __future__ import annotations
 
@@ -73,6 +75,9 @@ WORKLOADS = {
     # Tq/Tk: the bound on a sequence's length (max_seqlen)
     "varlen_packed": Workload("varlen_packed", "bf16", 8, 2048, 2048, 32, 8, 128, True, backward=True,
                               seed=0x5EED0007),
+    # encoder batching off a fused QKV projection: B sequences, Tq the longest length
+    "packed_qkv": Workload("packed_qkv", "bf16", 16, 1024, 1024, 12, 12, 64, False, backward=True,
+                           seed=0x5EED0009),
 }
 
 
@@ -127,4 +132,22 @@ def make_packed_inputs(w: Workload) -> dict:
         "do": normal((total, w.H * w.hd), w.seed + 3, w.dtype),
         "lengths": lens,
         "cu": cu,
+    }
+
+
+def make_packed_qkv_inputs(w: Workload) -> dict:
+    """Fused QKV rows [L, 3*H*hd] and dO [L, H*hd] (CPU) for w: w.B sequences with
+    lengths drawn uniformly from [w.Tq // 8, w.Tq] packed back to back, each row's
+    sequence bounds ``seq_bounds`` (int32 [L, 2]: first row, one past the last row)
+    and the lengths."""
+    lens = mask_lengths(w.B, w.Tq // 8, w.Tq, w.seed + 4)
+    L = int(lens.sum())
+    ends = torch.cumsum(lens, 0)
+    starts = ends - lens
+    seq_bounds = torch.stack([torch.repeat_interleave(starts, lens), torch.repeat_interleave(ends, lens)], 1)
+    return {
+        "qkv": normal((L, 3 * w.H * w.hd), w.seed + 0, w.dtype),
+        "do": normal((L, w.H * w.hd), w.seed + 3, w.dtype),
+        "seq_bounds": seq_bounds.to(torch.int32).contiguous(),
+        "lengths": lens,
     }

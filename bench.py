@@ -285,7 +285,9 @@ def workload_config(w):
 # repetition, in order.  Kernel launches per repetition (for a profiler's
 # --launch-skip): gqa_prefill 3 (fwd, dQ, dK/dV); swa_softcap, varlen_packed and
 # bias_prefill 3 (fwd, dQ, dK/dV); encoder_mask 1; decode_lq4 2 (split, combine);
-# gqa_prefill_hd256 5 (fwd, D, dV, dK, dQ); rope_prefill 3 (turn of k, cos/sin table, fwd).
+# gqa_prefill_hd256 5 (fwd, D, dV, dK, dQ); rope_prefill 3 (turn of k, cos/sin table, fwd);
+# packed_qkv: 3 copies and the forward, then 3 copies, the forward, dQ, dK/dV and 3 copies
+# (kernel launches: fwd, fwd, dQ, dK/dV).
 def _case_dense(A, synth, torch, dev, name, fwd_only=False, bias=False):
     w = synth.WORKLOADS[name]
     inp = synth.make_inputs(w)
@@ -324,6 +326,20 @@ def _case_varlen(A, synth, torch, dev):
                                       **kw)]
 
 
+def _case_packed_qkv(A, synth, torch, dev):
+    w = synth.WORKLOADS["packed_qkv"]
+    pi = synth.make_packed_qkv_inputs(w)
+    qkv, do, sb = pi["qkv"].to(dev), pi["do"].to(dev), pi["seq_bounds"].to(dev)
+    L = qkv.shape[0]
+    o = torch.empty((L, w.H * w.hd), dtype=qkv.dtype, device=dev)
+    lse = torch.empty((w.H, L), dtype=torch.float32, device=dev)
+    dqkv = torch.empty_like(qkv)
+    ws = torch.empty(A.attn_packed_qkv_workspace_size("bfloat16", L, w.H, w.hd, backward=True), dtype=torch.uint8,
+                     device=dev)
+    return [lambda: A.attn_packed_qkv_fwd(qkv, sb, H=w.H, o=o, lse=lse, workspace=ws),
+            lambda: A.attn_packed_qkv_bwd(qkv, do, sb, H=w.H, dqkv=dqkv, workspace=ws)]
+
+
 def _case_decode(A, synth, torch, dev):
     w = synth.WORKLOADS["decode_lq4"]
     di = synth.make_inputs(w)
@@ -356,6 +372,7 @@ PROFILE_CASES = {
     "decode_lq4": lambda A, s, t, d: _case_decode(A, s, t, d),
     "gqa_prefill_hd256": lambda A, s, t, d: _case_dense(A, s, t, d, "gqa_prefill_hd256"),
     "rope_prefill": lambda A, s, t, d: _case_rope(A, s, t, d),
+    "packed_qkv": lambda A, s, t, d: _case_packed_qkv(A, s, t, d),
 }
 
 
@@ -766,6 +783,32 @@ def masked_workloads(A, synth, torch, dev, stream, args, flush_buf, peaks):
                                      "visible_pairs": pairs,
                                      "note": "B=4 T=2048 H=16 Hkv=4 hd=256 causal bf16 (tensor cores)"}
     del q2, k2, v2, do2, o2, dq2, dk2, dv2, l2, ws2
+    # packed bidirectional encoder batch straight off fused QKV rows (per-row sequence
+    # bounds); the call includes splitting q, k, v out of the rows (and, backward,
+    # forming O and LSE again and interleaving dQ, dK, dV into the dQKV rows)
+    wp = synth.WORKLOADS["packed_qkv"]
+    pi = synth.make_packed_qkv_inputs(wp)
+    qkv, dop = pi["qkv"].to(dev), pi["do"].to(dev)
+    sb = pi["seq_bounds"].to(dev)
+    Lp = qkv.shape[0]
+    op = torch.empty((Lp, wp.H * wp.hd), dtype=qkv.dtype, device=dev)
+    lp = torch.empty((wp.H, Lp), dtype=torch.float32, device=dev)
+    dqkv = torch.empty_like(qkv)
+    wsp = torch.empty(A.attn_packed_qkv_workspace_size("bfloat16", Lp, wp.H, wp.hd, backward=True),
+                      dtype=torch.uint8, device=dev)
+    t = time_passes(torch, stream, [
+        ("fwd", lambda: A.attn_packed_qkv_fwd(qkv, sb, H=wp.H, o=op, lse=lp, workspace=wsp)),
+        ("bwd", lambda: A.attn_packed_qkv_bwd(qkv, dop, sb, H=wp.H, dqkv=dqkv, workspace=wsp))], args, flush_buf)
+    pairs = sum(int(n) * int(n) for n in pi["lengths"]) * wp.H
+    for n, fl in (("fwd", 4), ("bwd", 14)):
+        tf = fl * wp.hd * pairs / (t[n] * 1e-3) / 1e12
+        out["packed_qkv_" + n] = {"ms": t[n], "TFLOP/s": tf, "frac_of_bf16_peak": tf / peaks["bf16"],
+                                  "visible_pairs": pairs, "rows": Lp,
+                                  "note": "16 bidirectional sequences of U{128..1024} rows as fused QKV rows, H=12 "
+                                          "hd=64 bf16; " + ("forward" if n == "fwd" else
+                                                            "backward with its recompute of O and LSE, counted as "
+                                                            "14*hd per pair (forward 4 + backward 10)")}
+    del qkv, dop, sb, op, lp, dqkv, wsp
     # rotary embedding of the GQA prefill q and k (HBM-bound: each element read and written once)
     rq, rk = q.clone(), k.clone()
     t = time_passes(torch, stream, [("rope", lambda: (A.attn_rope(rq, H=wb.H, pos=0), A.attn_rope(rk, H=wb.Hkv, pos=0)))],

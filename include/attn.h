@@ -317,10 +317,13 @@ ATTN_API attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k
  *   attn_packed_qkv_bwd : dqkv [L][3*H*hd] (overwritten), each row [dq | dk | dv], from
  *                dout [L][H*hd]; O and LSE are formed again from qkv.
  *   workspace  : at least attn_packed_qkv_workspace_size(dt, L, H, hd, backward) bytes,
- *                16-byte aligned; contents on entry are ignored.  The calls copy q, k
- *                and v into it (strided copies on the stream) and run the forward /
- *                backward kernels on those: 16-bit hd 64 / 128 on the tensor cores,
- *                other types and head sizes on the CUDA-core kernels.
+ *                16-byte aligned; contents on entry are ignored.  16-bit rows at hd
+ *                64 / 128 run on the tensor cores, whose tensor maps read q, k and v
+ *                in place from the rows (and the backward writes dq, dk, dv straight
+ *                into the dqkv rows); the workspace then holds only the backward's O,
+ *                LSE and D.  Other types and head sizes run on the CUDA-core kernels
+ *                over contiguous copies of q, k and v made in the workspace (strided
+ *                copies on the stream), the backward's gradients copied into dqkv.
  *   Errors as attn_fwd; L = 0 is a no-op.
  */
 ATTN_API size_t attn_packed_qkv_workspace_size(attn_dtype dt, int L, int H, int hd, int backward);

@@ -70,6 +70,15 @@ def test_packed_qkv_tensor_cores(dt, hd, window):
     run_packed(dt, [300, 1, 129, 64, 2, 250], 2, hd, window, seed=2100 + hd + window)
 
 
+@pytest.mark.parametrize("dt,hd", [("bf16", 64), ("f16", 128)])
+def test_packed_qkv_tiles_far_apart(dt, hd):
+    """A 256-row block whose first 128-row tile ends a long sequence and whose second lies
+    in the next one: the two tiles' first key tiles are up to eight apart (their softmaxes
+    must not take turns then), here with a window too."""
+    for window in (0, 300):
+        run_packed(dt, [600, 1000, 130, 900, 270], 2, hd, window, seed=2150 + hd + window)
+
+
 @pytest.mark.parametrize("lengths", [[777], [1] * 40, [17, 300, 5, 500]], ids=["one-sequence", "one-row-each", "mixed"])
 def test_packed_qkv_packings(lengths):
     run_packed("bf16", lengths, 4, 128, 0, seed=2200 + len(lengths))
@@ -112,3 +121,35 @@ def test_packed_qkv_rejects_bad_arguments():
         A.attn_packed_qkv_fwd(qkv, sb[:4], H=2)
     with pytest.raises(A.AttnError):
         A.attn_packed_qkv_fwd(qkv, sb, H=2, window=-1)
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_packed_qkv_full_size(window):
+    """The benchmark's packing (16 sequences of U{128..1024} rows, H=12 hd=64 bf16),
+    forward and backward in one call each as timed; sequences are independent, so the
+    shortest, a middle and the longest one are checked against the oracle run on that
+    sequence's rows alone."""
+    w = synth.WORKLOADS["packed_qkv"]
+    pi = synth.make_packed_qkv_inputs(w)
+    qkv, do, sb = pi["qkv"], pi["do"], pi["seq_bounds"]
+    o, lse = A.attn_packed_qkv_fwd(qkv.cuda(), sb.cuda(), H=w.H, window=window)
+    dqkv = A.attn_packed_qkv_bwd(qkv.cuda(), do.cuda(), sb.cuda(), H=w.H, window=window)
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    assert st == A.OK, "device status word %#x" % word
+    o, lse, dqkv = o.cpu(), lse.cpu(), dqkv.cpu()
+    lens = pi["lengths"].tolist()
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    order = np.argsort(lens, kind="stable")
+    nw = w.H * w.hd
+    for s in sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])}):
+        a, n = int(starts[s]), int(lens[s])
+        rows = slice(a, a + n)
+        sub = bounds_of([n]).numpy()
+        what = "packed_qkv window %d, sequence %d (%d rows)" % (window, s, n)
+        o_ref, lse_ref = oracle.packed_qkv_fwd(f64(qkv[rows]), sub, H=w.H, scale=w.scale, window=window)
+        compare_o_lse(o[rows][None], lse[:, rows][None], o_ref[None], lse_ref[None], "bf16", what)
+        g_ref = oracle.packed_qkv_bwd(f64(qkv[rows]), f64(do[rows]), sub, H=w.H, scale=w.scale, window=window)
+        g = dqkv[rows]
+        compare_grads((g[:, :nw], g[:, nw:2 * nw], g[:, 2 * nw:]),
+                      (g_ref[:, :nw], g_ref[:, nw:2 * nw], g_ref[:, 2 * nw:]), "bf16", what)
