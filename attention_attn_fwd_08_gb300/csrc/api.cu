@@ -838,6 +838,57 @@ Params packed_params(const int* seq_bounds, int L, int H, int hd, float scale, i
 
 size_t tensor_bytes(attn_dtype dt, int L, int H, int hd) { return align256((size_t)L * H * hd * elem_size(dt)); }
 
+// Heaviest-first orders of the row blocks of a packed batch, for the work-item
+// numbering of the tensor-core kernels: blocks of 256 rows (the forward's items) into
+// ord256, of 128 rows (the dQ items and the dK/dV key blocks) into ord128.  A block's
+// weight is the span of keys its rows see, from its first row's sequence start (less
+// the window) to its last row's sequence end (plus the window); with the bounds
+// monotone down the rows, that span holds all of the block's visible pairs.  Ties keep
+// block order.  One CTA, for at most kOrderMax blocks of 128 rows.
+constexpr int kOrderMax = 2048;
+__global__ void packed_order_kernel(const int2* sb, int L, int wl, int wr, int* ord256, int* ord128) {
+    __shared__ int cost[kOrderMax];
+    for (int pass = 0; pass < 2; ++pass) {
+        const int rows = pass == 0 ? 256 : 128;
+        const int n = (L + rows - 1) / rows;
+        int* ord = pass == 0 ? ord256 : ord128;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int r0 = i * rows, r1 = min(r0 + rows, L) - 1;
+            int lo = min(max(__ldg(&sb[r0].x), 0), L), hi = min(max(__ldg(&sb[r1].y), 0), L);
+            if (wl >= 0) lo = max(lo, r0 - wl);
+            if (wr >= 0) hi = min(hi, r1 + wr + 1);
+            cost[i] = max(hi - lo, 0);
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int c = cost[i];
+            int rank = 0;
+            for (int j = 0; j < n; ++j) {
+                const int cj = cost[j];
+                rank += (cj > c || (cj == c && j < i)) ? 1 : 0;
+            }
+            ord[rank] = i;
+        }
+        __syncthreads();
+    }
+}
+
+// The two orders in the workspace at ws (ints: ord256 then ord128), or false when the
+// batch has too many blocks (the kernels then keep their plain order).
+bool packed_order(const int* seq_bounds, int L, const Params& p, void* ws, int** ord256, int** ord128,
+                  cudaStream_t s, attn_status* st) {
+    const int n256 = (L + 255) / 256, n128 = (L + 127) / 128;
+    *ord256 = *ord128 = nullptr;
+    *st = ATTN_OK;
+    if (n128 > kOrderMax) return false;
+    int* o = static_cast<int*>(ws);
+    packed_order_kernel<<<1, 1024, 0, s>>>(reinterpret_cast<const int2*>(seq_bounds), L, p.wl, p.wr, o, o + n256);
+    if ((*st = counted(cudaGetLastError(), 1)) != ATTN_OK) return false;
+    *ord256 = o;
+    *ord128 = o + n256;
+    return true;
+}
+
 // 16-bit rows at hd 64 / 128 go to the tensor-core kernels, whose tensor maps read q,
 // k and v in place from the packed rows (and write dq, dk, dv into them); the
 // CUDA-core kernels take contiguous copies.
@@ -864,10 +915,14 @@ attn_status attn_packed_qkv_fwd(attn_dtype dt, const void* qkv, const int* seq_b
     if (!o || !workspace || !aligned16(workspace) || workspace_bytes < attn_packed_qkv_workspace_size(dt, L, H, hd, 0))
         return ATTN_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const Params p = packed_params(seq_bounds, L, H, hd, scale, window);
+    Params p = packed_params(seq_bounds, L, H, hd, scale, window);
     if (packed_in_place(dt, hd)) {
         const size_t w = (size_t)H * hd * elem_size(dt);
         const uint8_t* r = static_cast<const uint8_t*>(qkv);
+        int *ord256, *ord128;
+        packed_order(seq_bounds, L, p, workspace, &ord256, &ord128, s, &st);
+        if (st != ATTN_OK) return st;
+        p.item_order = ord256;
         return fwd_launch(dt, r, r + w, r + 2 * w, o, lse, p, stream, 3LL * H * hd);
     }
     const size_t t = tensor_bytes(dt, L, H, hd);
@@ -898,9 +953,16 @@ attn_status attn_packed_qkv_bwd(attn_dtype dt, const void* qkv, const void* dout
         const uint8_t* r = static_cast<const uint8_t*>(qkv);
         uint8_t* g = static_cast<uint8_t*>(dqkv);
         const long long rs = 3LL * H * hd;
-        if ((st = fwd_launch(dt, r, r + w, r + 2 * w, o, lse, p, stream, rs)) != ATTN_OK) return st;
+        // the block orders go where the CUDA-core path keeps its copy of q
+        int *ord256, *ord128;
+        packed_order(seq_bounds, L, p, q, &ord256, &ord128, s, &st);
+        if (st != ATTN_OK) return st;
+        Params pf = p, pb = p;
+        pf.item_order = ord256;
+        pb.item_order = ord128;
+        if ((st = fwd_launch(dt, r, r + w, r + 2 * w, o, lse, pf, stream, rs)) != ATTN_OK) return st;
         return bwd_launch(dt, r, r + w, r + 2 * w, o, dout, lse, g, g + w, g + 2 * w, wb, attn_bwd_workspace_size(1, L, H),
-                          p, stream, 7, rs, rs);
+                          pb, stream, 7, rs, rs);
     }
     if ((st = split_qkv(dt, qkv, q, k, v, L, H, hd, s)) != ATTN_OK) return st;
     if ((st = fwd_launch(dt, q, k, v, o, lse, p, stream)) != ATTN_OK) return st;

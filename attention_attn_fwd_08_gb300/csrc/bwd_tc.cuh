@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
     const int within = (int)blockIdx.x - cidx * nkb * CH;
     const int kg = cidx * CH + within % ch;
     const int kvh = kg % P.Hkv, b = kg / P.Hkv;
-    const int j0 = (within / ch) * BKV;
+    // (packed fused-QKV rows: key blocks heaviest first, when an order is given)
+    const int j0 = (RB && P.item_order ? __ldg(P.item_order + within / ch) : within / ch) * BKV;
     const Seq sq = seq_of<VL>(P, b);
     if (j0 >= sq.tk) return;  // (packed) past this sequence's keys: nothing to write
     int qlo, qhi;
@@ -691,6 +692,9 @@ __device__ __forceinline__ DqItem dq_item(const Params& P, int w, DqCursor& c) {
         for (int t = 0; t < j && m; ++t) m &= m - 1;
         // (w is below the item count, so the sequence exists)
         return dq_item_at<BQ, BK, VL, RB>(P, m ? __ffs(m) - 1 : 0, r - j * P.H, c.level);
+    }
+    if constexpr (RB) {  // packed fused-QKV rows (one batch): blocks heaviest first
+        if (P.item_order) return dq_item_at<BQ, BK, VL, RB>(P, 0, w % P.H, __ldg(P.item_order + w / P.H));
     }
     const int nqb = (P.Tq + BQ - 1) / BQ;
     const int hb = w % (P.H * P.B);

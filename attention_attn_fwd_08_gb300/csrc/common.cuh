@@ -62,6 +62,11 @@ struct Params {
     // the sequences lie back to back, so the bounds never decrease down the rows).  The
     // window then applies inside the sequence.
     const int2* row_bounds;
+    // With row_bounds, the order in which the work items' row blocks run (heaviest
+    // first: a permutation of the blocks of 256 rows in the forward, of 128 rows in the
+    // backward), or NULL for the plain order.  It decides only which CTA takes which
+    // block when; every block is computed the same way.
+    const int* item_order;
     unsigned int* status;
 };
 

@@ -223,6 +223,9 @@ __device__ __forceinline__ FwdItem fwd_item(const Params& P, int w, VlCursor& c,
         if (P.B <= kVlCompact) return vl_item(P, c, w);
     }
     const int ncq = (P.Tq + 2 * BM - 1) / (2 * BM);
+    if constexpr (RB) {  // packed fused-QKV rows (one batch): blocks heaviest first
+        if (P.item_order) return make_item<VL, RB>(P, 0, w % P.H, __ldg(P.item_order + w / P.H), true, kspan);
+    }
     if constexpr (KORD) {
         if (P.wl < 0 && P.wr < 0) {
             const int per = P.H * ncq, rem = w % per;
@@ -662,12 +665,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
             else if (!accurate) p_pass(std::integral_constant<int, 1>());
             else p_pass(std::integral_constant<int, 2>());
         };
-        // Without a softcap the two tiles' softmaxes alternate A(k), B(k), A(k+1), ...
-        // within an item, so each runs while the tensor core works on the other tile's
-        // P.V and next S; left alone they fall into lockstep and the tensor core idles
-        // during both.  The longer softcap softmax does better with both warpgroups
-        // issuing at once (measured).  base[u] counts tile u's softmaxes in earlier items.
-        const bool alternate = !cap;
+        // The two tiles' softmaxes alternate A(k), B(k), A(k+1), ... within an item, so
+        // each runs while the tensor core works on the other tile's P.V and next S; left
+        // alone they fall into lockstep and the tensor core idles during both.  (With a
+        // softcap, both at once measured faster while each MMA issue took a branch
+        // around it; with the predicated issue the turns win there too, except with a
+        // bias as well, whose longer softmax still runs better with both at once.)
+        // base[u] counts tile u's softmaxes in earlier items.
+        constexpr bool kTurns = !(BIAS && cap);
         int base[2] = {0, 0};
         // Fused rotary embedding: turn this thread's row of tile u's Q in shared memory
         // once the tile of item w2 has landed, then release it to the MMA warp.  Pairs
@@ -733,7 +738,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             // ring stage that only its own later P.V releases (packed fused-QKV rows,
             // where a tile that ends a long sequence starts many key tiles before the
             // next one): such items run both softmaxes at once.
-            const bool alt = alternate && abs(it.tu[0].t0 - it.tu[1].t0) <= 1;
+            const bool alt = kTurns && abs(it.tu[0].t0 - it.tu[1].t0) <= 1;
             base[0] += nA;
             base[1] += nB;
             const int ib = it.i0 + u * BM;  // first row of this tile

@@ -320,8 +320,10 @@ ATTN_API attn_status attn_varlen_bwd(attn_dtype dt, const void* q, const void* k
  *                16-byte aligned; contents on entry are ignored.  16-bit rows at hd
  *                64 / 128 run on the tensor cores, whose tensor maps read q, k and v
  *                in place from the rows (and the backward writes dq, dk, dv straight
- *                into the dqkv rows); the workspace then holds only the backward's O,
- *                LSE and D.  Other types and head sizes run on the CUDA-core kernels
+ *                into the dqkv rows); the workspace then holds only the order in which
+ *                the row blocks run (heaviest first, formed on the stream by a small
+ *                kernel from seq_bounds) and the backward's O, LSE and D.  Other types
+ *                and head sizes run on the CUDA-core kernels
  *                over contiguous copies of q, k and v made in the workspace (strided
  *                copies on the stream), the backward's gradients copied into dqkv.
  *   Errors as attn_fwd; L = 0 is a no-op.
