@@ -846,31 +846,45 @@ size_t tensor_bytes(attn_dtype dt, int L, int H, int hd) { return align256((size
 // monotone down the rows, that span holds all of the block's visible pairs.  Ties keep
 // block order.  One CTA, for at most kOrderMax blocks of 128 rows.
 constexpr int kOrderMax = 2048;
-__global__ void packed_order_kernel(const int2* sb, int L, int wl, int wr, int* ord256, int* ord128) {
-    __shared__ int cost[kOrderMax];
-    for (int pass = 0; pass < 2; ++pass) {
-        const int rows = pass == 0 ? 256 : 128;
-        const int n = (L + rows - 1) / rows;
-        int* ord = pass == 0 ? ord256 : ord128;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const int r0 = i * rows, r1 = min(r0 + rows, L) - 1;
-            int lo = min(max(__ldg(&sb[r0].x), 0), L), hi = min(max(__ldg(&sb[r1].y), 0), L);
-            if (wl >= 0) lo = max(lo, r0 - wl);
-            if (wr >= 0) hi = min(hi, r1 + wr + 1);
-            cost[i] = max(hi - lo, 0);
+__device__ __forceinline__ void rank_blocks(const int* cost, int n, int* ord) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int c = cost[i];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) {
+            const int cj = cost[j];
+            rank += (cj > c || (cj == c && j < i)) ? 1 : 0;
         }
-        __syncthreads();
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-            const int c = cost[i];
-            int rank = 0;
-            for (int j = 0; j < n; ++j) {
-                const int cj = cost[j];
-                rank += (cj > c || (cj == c && j < i)) ? 1 : 0;
-            }
-            ord[rank] = i;
-        }
-        __syncthreads();
+        ord[rank] = i;
     }
+}
+__global__ void packed_order_kernel(const int2* sb, int L, int wl, int wr, int* ord256, int* ord128) {
+    // sequence start of each 128-row block's first row, sequence end of its last row
+    __shared__ int lo_s[kOrderMax], hi_s[kOrderMax];
+    __shared__ int cost[kOrderMax + kOrderMax / 2];  // 128-row blocks, then 256-row blocks
+    const int n128 = (L + 127) / 128, n256 = (L + 255) / 256;
+    for (int i = threadIdx.x; i < n128; i += blockDim.x) {
+        lo_s[i] = min(max(__ldg(&sb[i * 128].x), 0), L);
+        hi_s[i] = min(max(__ldg(&sb[min(i * 128 + 128, L) - 1].y), 0), L);
+    }
+    __syncthreads();
+    // the span of keys rows r0 .. r1 see: 128-row blocks b0 .. b1
+    auto span = [&](int b0, int b1, int r0, int r1) {
+        int lo = lo_s[b0], hi = hi_s[b1];
+        if (wl >= 0) lo = max(lo, r0 - wl);
+        if (wr >= 0) hi = min(hi, r1 + wr + 1);
+        return max(hi - lo, 0);
+    };
+    for (int i = threadIdx.x; i < n128 + n256; i += blockDim.x) {
+        if (i < n128) {
+            cost[i] = span(i, i, i * 128, min(i * 128 + 128, L) - 1);
+        } else {
+            const int k = i - n128;
+            cost[i] = span(2 * k, min(2 * k + 1, n128 - 1), k * 256, min(k * 256 + 256, L) - 1);
+        }
+    }
+    __syncthreads();
+    rank_blocks(cost, n128, ord128);
+    rank_blocks(cost + n128, n256, ord256);
 }
 
 // The two orders in the workspace at ws (ints: ord256 then ord128), or false when the
