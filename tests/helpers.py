@@ -25,7 +25,8 @@ def f64(t):
 
 def make_mask(kind, B, Tk, seed):
     """None | 'shared' (one random 1/0 row) | 'batch' (prefix lengths) | 'holes' (random per batch,
-    first keys masked so early causal rows see nothing)."""
+    first keys masked so early causal rows see nothing) | 'band' (one unbroken run of kept keys
+    per batch, starting past key 0 and ending before the last key)."""
     if kind is None:
         return None
     g = torch.Generator().manual_seed(seed)
@@ -36,6 +37,11 @@ def make_mask(kind, B, Tk, seed):
     if kind == "batch":
         lens = synth.mask_lengths(B, max(1, Tk // 2), Tk, seed)
         return synth.prefix_mask(lens, Tk)
+    if kind == "band":
+        m = torch.zeros(B, Tk)
+        for b in range(B):
+            m[b, min(1 + 17 * b, Tk - 1):max(Tk - 3 - 5 * b, min(2 + 17 * b, Tk))] = 1.0
+        return m
     if kind == "holes":
         m = (torch.rand(B, Tk, generator=g) > 0.4).float()
         m[:, : min(3, Tk)] = 0.0

@@ -153,3 +153,34 @@ def test_packed_qkv_full_size(window):
         g = dqkv[rows]
         compare_grads((g[:, :nw], g[:, nw:2 * nw], g[:, 2 * nw:]),
                       (g_ref[:, :nw], g_ref[:, nw:2 * nw], g_ref[:, 2 * nw:]), "bf16", what)
+
+
+def test_packed_qkv_past_the_block_order():
+    """More than 2048 blocks of 128 rows (262 145 rows): the kernels keep their plain item
+    order (no heaviest-first pass) and large row indices; three sequences are checked
+    against the oracle, forward and backward."""
+    H, hd, n = 1, 64, 256
+    lengths = [1024] * n
+    lengths[-1] += 1
+    sb = bounds_of(lengths)
+    L = sb.shape[0]
+    assert (L + 127) // 128 > 2048
+    qkv = synth.normal((L, 3 * H * hd), 2500, "bf16")
+    do = synth.normal((L, H * hd), 2501, "bf16")
+    o, lse = A.attn_packed_qkv_fwd(qkv.cuda(), sb.cuda(), H=H)
+    dqkv = A.attn_packed_qkv_bwd(qkv.cuda(), do.cuda(), sb.cuda(), H=H)
+    torch.cuda.synchronize()
+    st, word = A.attn_get_device_status()
+    assert st == A.OK, "device status word %#x" % word
+    o, lse, dqkv = o.cpu(), lse.cpu(), dqkv.cpu()
+    for s in (0, n // 2, n - 1):
+        a = 1024 * s
+        rows = slice(a, a + lengths[s])
+        sub = bounds_of([lengths[s]]).numpy()
+        what = "packed_qkv L%d, sequence %d" % (L, s)
+        o_ref, lse_ref = oracle.packed_qkv_fwd(f64(qkv[rows]), sub, H=H, scale=1 / math.sqrt(hd))
+        compare_o_lse(o[rows][None], lse[:, rows][None], o_ref[None], lse_ref[None], "bf16", what)
+        g_ref = oracle.packed_qkv_bwd(f64(qkv[rows]), f64(do[rows]), sub, H=H, scale=1 / math.sqrt(hd))
+        g = dqkv[rows]
+        compare_grads((g[:, :hd], g[:, hd:2 * hd], g[:, 2 * hd:]), (g_ref[:, :hd], g_ref[:, hd:2 * hd], g_ref[:, 2 * hd:]),
+                      "bf16", what)

@@ -21,6 +21,7 @@ FWD_FLAGS = [
     dict(causal=False, softcap=5.0, mask="batch"),
     dict(causal=False, window=64, mask="shared"),
     dict(causal=True, mask="holes"),          # early rows fully masked
+    dict(causal=False, mask="band"),          # key tiles inside an unbroken kept run read no mask
     dict(causal=True, q_offset=77, window=150),
 ]
 
@@ -51,6 +52,7 @@ MULTI_ITEM_FLAGS = [
     dict(causal=True),
     dict(causal=True, window=200, softcap=30.0),
     dict(causal=False, mask="holes"),
+    dict(causal=False, mask="band"),
     dict(causal=True, q_offset=100, window=300),
 ]
 
