@@ -603,26 +603,36 @@ __global__ void __launch_bounds__(dkdv_threads(MODE), 1)
 }
 
 // ===================================================================== dQ
-template <int HD>
+template <int HD, bool OSTG = false>
 struct QCfg {
     static constexpr int BQ = 128;  // query rows per item
     static constexpr int BK = 64;   // keys per inner tile
     static constexpr int kBoxes = HD / 64;
-    static constexpr int kStages = HD == 128 ? 3 : 4;
+    // OSTG: the next item's O tile (for D = rowsum(dO*O)), and then D, land in the
+    // epilogue staging between epilogues, which leaves room for a fourth K/V stage at
+    // hd 128; otherwise O has a tile of its own.
+    static constexpr int kStages = OSTG || HD != 128 ? 4 : 3;
     static constexpr int kQBytes = BQ * HD * 2;
     static constexpr int kKBytes = BK * HD * 2;  // one K (or V) tile
     static constexpr int kQOff = 0;
-    static constexpr int kGOff = kQBytes;      // dO
-    static constexpr int kOOff = 2 * kQBytes;  // O (for D = rowsum(dO*O))
-    static constexpr int kKOff = 3 * kQBytes;
+    static constexpr int kGOff = kQBytes;  // dO
+    static constexpr int kKOff = (OSTG ? 2 : 3) * kQBytes;
     static constexpr int kVOff = kKOff + kStages * kKBytes;
     static constexpr int kBarOff = kVOff + kStages * kKBytes;
     static constexpr int kNumBars = 11 + 2 * kStages;
     // epilogue staging: one 32-row x 64-column slice (4 KB) per compute warp (8)
     static constexpr int kStgOff = (kBarOff + kNumBars * 8 + 16 + 1023) / 1024 * 1024;
+    static constexpr int kOOff = OSTG ? kStgOff : 2 * kQBytes;  // O, then D of its rows
     static constexpr int kBytes = kStgOff + 8 * 4096;
     static constexpr int kLaunchBytes = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+    static_assert(!OSTG || kQBytes <= 8 * 4096, "the O tile fits in the staging slices");
 };
+// shared memory a dQ launch asks for (either layout)
+template <int HD>
+constexpr int dq_launch_bytes() {
+    return QCfg<HD, false>::kLaunchBytes > QCfg<HD, true>::kLaunchBytes ? QCfg<HD, false>::kLaunchBytes
+                                                                          : QCfg<HD, true>::kLaunchBytes;
+}
 
 // One dQ work item: 128 query rows of one (batch, head) and the key tiles they
 // see.  Items are numbered longest first (every head's last query block first).
@@ -714,7 +724,11 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     bwd_dq_kernel(const Params P, const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                   const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmDQ) {
-    using C = QCfg<HD>;
+    // at hd 128 without a softcap O shares the epilogue staging and the K/V ring gets a
+    // fourth stage (GQA prefill dQ 0.2007 -> 0.1884 ms); the softcap instantiations,
+    // bound by their element work, measured slower that way (0.2314 -> 0.2335 ms)
+    constexpr bool OSTG = HD == 128 && (MODE & 4) == 0;
+    using C = QCfg<HD, OSTG>;
     constexpr int NS = C::kStages, BQ = C::BQ, BK = C::BK;
     // MODE & 3 as for dK/dV; MODE & 4: softcap; MODE & 8: a head size below HD (4-D maps)
     constexpr bool VL = (MODE & 3) == 1, BIAS = (MODE & 3) == 2, PADH = (MODE & 8) != 0;
@@ -727,6 +741,9 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     __shared__ int abort_flag;
+    // compute-warp epilogues whose staging slices have been read out (8 per item):
+    // an O tile may land in the staging only after every epilogue before it
+    __shared__ int stg_done;
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     const int QG_FULL = 0;   // Q, dO and O of an item in shared memory
@@ -757,6 +774,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             mbar_init(BAR(i), count);
         }
         abort_flag = 0;
+        stg_done = 0;
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -797,7 +815,8 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
             P.ndelta[srow] = i2 < it.sq.tq ? -dval : 0.f;
             P.nlse2[srow] = nl2;
         };
-        int qn = 0;  // Q/dO/O loads so far
+        int qn = 0;         // Q/dO/O loads so far
+        int prev_act = -1;  // position of the last item loaded
         for (int k_ = 0, w = snake_item(0); w < nitems; w = snake_item(++k_)) {
             const DqItem it = dq_item<BQ, BK, VL, RB>(P, w, cur);
             if (it.ntiles == 0) {
@@ -806,6 +825,16 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                 continue;
             }
             if (qn > 0 && !warp_wait(BAR(QG_EMPTY), (qn - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) break;
+            if constexpr (OSTG) {
+                // O goes into the epilogue staging: the epilogues of every item before
+                // the previous loaded one (for the first, before this one) must be out
+                // of it.  The compute warps copy this item's Q/dO and read its D before
+                // the previous item's epilogue, so no later epilogue can touch the
+                // staging before D is read.
+                const int need = 8 * (prev_act >= 0 ? prev_act : k_);
+                if (!__all_sync(0xffffffffu, count_wait(&stg_done, need, P.status, ST_BWD_PRODUCER, &abort_flag)))
+                    break;
+            }
             if (elect_one()) mbar_expect_tx(BAR(QG_FULL), 3 * C::kQBytes);
 #pragma unroll
             for (int bx = 0; bx < C::kBoxes; ++bx) {
@@ -820,6 +849,7 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                                         it.sq.q0 + it.i0, it.sq.zb);
             }
             ++qn;
+            prev_act = k_;
             if (!warp_wait(BAR(QG_FULL), (qn - 1) & 1, P.status, ST_BWD_PRODUCER, &abort_flag)) break;
             float dv[BQ / 32];
 #pragma unroll
@@ -1243,6 +1273,12 @@ __global__ void __launch_bounds__(kThreadsDQ, 1)
                     bulk_commit_group();
                 }
             }
+            if constexpr (OSTG) {
+                // the staging may take the next O tile once this warp's store has read its slice
+                if (elect_one()) bulk_wait_read_all();
+                __syncwarp();
+                if (lane == 0) atomicAdd(&stg_done, 1);
+            }
             gt += ntiles;
         }
         if (elect_one()) bulk_wait_all();
@@ -1274,7 +1310,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
                  : p.row_bounds ? bwd_dq_kernel<BF16, HD, 64>
                  : p.bias   ? (c ? bwd_dq_kernel<BF16, HD, 6> : bwd_dq_kernel<BF16, HD, 2>)
                             : (c ? bwd_dq_kernel<BF16, HD, 4> : bwd_dq_kernel<BF16, HD, 0>);
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, QCfg<HD>::kLaunchBytes);
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_launch_bytes<HD>());
         if (e != cudaSuccess) return e;
         int dev = 0, nsm = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1282,7 +1318,7 @@ cudaError_t bwd_typed(const Params& p, const BwdMaps& m, int phases, cudaStream_
         // persistent: one CTA per SM (one fits); each walks its items in snake order
         const long long items = (long long)((p.Tq + 127) / 128) * p.H * p.B;
         const unsigned grid = (unsigned)(items < nsm ? items : nsm);
-        k<<<grid, kThreadsDQ, QCfg<HD>::kLaunchBytes, s>>>(p, m.q, m.k64, m.v64, m.dout, m.o, m.dq32);
+        k<<<grid, kThreadsDQ, dq_launch_bytes<HD>(), s>>>(p, m.q, m.k64, m.v64, m.dout, m.o, m.dq32);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (phases & 2) {
